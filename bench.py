@@ -1,0 +1,480 @@
+#!/usr/bin/env python
+"""Benchmark of the QLoRA NF4 linear hot path on one B300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--quick] [--full]
+
+Headline (one JSON line on stdout, rank 0): fused forward + backward of the
+Llama-7B attention projection -- W 4096x4096 NF4 + double quant, 2048 tokens,
+LoRA r=16, alpha=32 -- in TFLOP/s (4MNK + 6Mr(N+K) algorithmic flops per
+step), inputs resident in HBM, L2 flushed between steps, CUDA events on the
+launching stream, max over ranks.  Also on the line:
+
+* ``roofline``: the dominant kernel of the step, timed live with events
+  around each of its launches, against the measured bf16 peak;
+* ``e2e``: the same step through the public API with the inputs copied from
+  pinned host memory and the LoRA gradients read back every step;
+* ``cpu_baseline``: the float64 CPU oracle on a bounded sample of the workload;
+* ``secondary``: the 32-layer Llama-7B decode sweep (weight GB/s at 1, 4, 16
+  tokens), dequantise and quantise GB/s, and with --full the MLP block and the
+  65B-shaped quantise stream + up-projection step.
+
+``--impl reference`` times the CPU oracle (the reference for this build) on a
+bounded sample of the same workload and prints the same line with
+``"impl": "reference"``.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "QLoRA NF4 linear fwd+bwd TFLOP/s; NF4 GEMV weight GB/s; % of roofline"
+N_, K_, M_, R_, ALPHA_ = 4096, 4096, 2048, 16, 32.0
+WORKLOAD = "Llama-7B attention projection: W 4096x4096 NF4+DQ, 2048 tokens (4 x 512), LoRA r=16 alpha=32, fwd+bwd"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+def step_flops(m, n, k, r):
+    return 4.0 * m * n * k + 6.0 * m * r * (n + k)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for ln in f:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if "Active" in r[5 + i] and "Not" not in r[5 + i]})
+        loaded = [v for v in sm if mx and v > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ distributed
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle leg
+def oracle_sample(rows: int, seed_rows: int = 0):
+    """Build the oracle inputs for a bounded sample of the headline workload (host only)."""
+    import numpy as np
+
+    import synthetic
+    from oracle import nf4
+    case = synthetic.linear_case(N_, K_, M_, R_, ALPHA_, device="cpu", base_seed=0)
+    idx = np.random.default_rng(seed_rows).choice(M_, rows, replace=False)
+    f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    rec = nf4.quantize(case.w.float().numpy(), N_, K_)
+    return {"rec": rec, "x": f(case.x)[idx], "a": f(case.a), "b": f(case.b), "dy": f(case.dy)[idx]}
+
+
+def oracle_step(s):
+    """One oracle fwd+bwd on the sampled rows: dequantise W, forward, backward."""
+    from oracle import linear, nf4
+    rec = s["rec"]
+    wd = nf4.dequantize(rec["codes"], rec["q"], rec["step"], rec["mu"], N_, K_)
+    _, t = linear.lora_forward(s["x"], wd, s["a"], s["b"], ALPHA_, R_)
+    linear.lora_backward(s["dy"], s["x"], wd, s["a"], s["b"], ALPHA_, R_, t)
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(budget_s: float = 12.0, rows: int = 256):
+    s = oracle_sample(rows)
+    flops = step_flops(rows, N_, K_, R_)
+    oracle_step(s)  # warm
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        oracle_step(s)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": "float64 oracle fwd+bwd (dequantise the 4096x4096 NF4 record + LoRA linear forward and "
+                      "backward) on %d of the 2048 token rows, %d repetitions, %.2f s each" % (rows, n, dt)}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    rows = args.ref_rows
+    s = oracle_sample(rows)
+    flops = step_flops(rows, N_, K_, R_)
+    for _ in range(args.warmup):
+        oracle_step(s)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(s)
+    dt = (time.perf_counter() - t0) / args.steps
+    val = flops / dt / 1e12
+    cores = blas_threads()
+    line = {"metric": METRIC, "value": val, "unit": "TFLOP/s", "impl": "reference", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n": N_, "k": K_, "m": M_, "r": R_, "alpha": ALPHA_,
+                       "sample_rows": rows},
+            "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "float64 oracle fwd+bwd on %d of the 2048 token rows per step" % rows},
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU legs
+def time_events(torch, fn, steps, flush=None):
+    """Per-step device time (ms) with events around fn only (flush outside)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in evs:
+        if flush is not None:
+            flush()
+        s.record()
+        fn()
+        e.record()
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def decode_sweep(q, torch, layers: int = 32, tokens=(1, 4, 16), passes: int = 10):
+    """Weight GB/s of the Llama-7B decode stack: one pass = Y = X deq(W)^T + s (X A^T) B^T on all
+    7 x `layers` matrices, captured in one CUDA graph per token count."""
+    import synthetic
+    shapes = synthetic.LLAMA7B_LAYER
+    recs, loras = [], []
+    for layer in range(layers):
+        for mi, (n, k) in enumerate(shapes):
+            w = synthetic.weight(n, k, device="cuda", seed=synthetic.stack_seed(layer, mi))
+            recs.append(q.quantize(w))
+            del w
+            loras.append(synthetic.lora_pair(n, k, 16, device="cuda", seed=50_000 + 2 * (7 * layer + mi)))
+    q.check_status()
+    weight_bytes = sum(r.nbytes() for r in recs)
+    lora_bytes = sum(a.numel() * 2 + b.numel() * 2 for a, b in loras)
+    out = {"matrices": len(recs), "weight_bytes_per_pass": weight_bytes, "lora_bytes_per_pass": lora_bytes}
+    for t in tokens:
+        xs = [synthetic.activations(t, r.k, device="cuda", seed=90_000 + i) for i, r in enumerate(recs)]
+        ys = [torch.empty((t, r.n), dtype=torch.bfloat16, device="cuda") for r in recs]
+        ts = [torch.empty((t, 16), dtype=torch.float32, device="cuda") for r in recs]
+        wsb = max(q.fwd_workspace_bytes(t, r.n, r.k, 16) for r in recs)
+        ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
+
+        def one_pass():
+            for i, r in enumerate(recs):
+                q.linear_fwd(xs[i], r, loras[i][0], loras[i][1], 32.0, y=ys[i], t_save=ts[i], workspace=ws)
+
+        one_pass()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            one_pass()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        ms = time_events(torch, g.replay, passes)
+        q.check_status()
+        io_bytes = sum(x.numel() * 2 for x in xs) + sum(y.numel() * 2 for y in ys)
+        med = statistics.median(ms)
+        out["t%d" % t] = {"ms_per_pass": med, "weight_gbs": (weight_bytes + lora_bytes) / med / 1e6,
+                          "all_bytes_gbs": (weight_bytes + lora_bytes + io_bytes) / med / 1e6}
+        del g, xs, ys, ts, ws
+    del recs, loras
+    torch.cuda.empty_cache()
+    return out
+
+
+def dequant_quant_rates(q, torch, rec, w, flush):
+    n, k = rec.n, rec.k
+    out_b = torch.empty((n, k), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        q.dequantize(rec, out=out_b)
+    ms = statistics.median(time_events(torch, lambda: q.dequantize(rec, out=out_b), 10, flush))
+    deq_bytes = rec.nbytes() + n * k * 2
+    wsq = torch.empty(q.quantize_workspace_bytes(n, k), dtype=torch.uint8, device="cuda")
+    rec2 = q.NF4Weight.empty(n, k)
+    for _ in range(3):
+        q.quantize(w, out=rec2, workspace=wsq)
+    msq = statistics.median(time_events(torch, lambda: q.quantize(w, out=rec2, workspace=wsq), 10, flush))
+    q.check_status()
+    quant_bytes = n * k * 2 + rec.nbytes()
+    return {"dequant": {"shape": [n, k], "ms": ms, "gbs": deq_bytes / ms / 1e6, "bytes": deq_bytes},
+            "quantize": {"shape": [n, k], "ms": msq, "gbs": quant_bytes / msq / 1e6, "bytes": quant_bytes,
+                         "kernels": 3}}
+
+
+def traffic_for(kernel: str):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it matches the current source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    import hashlib
+    src = hashlib.sha1(open(os.path.join(ROOT, "bit_quantized_fine_nf4_b300", "csrc", "qgemm.cu"), "rb").read())
+    cur = src.hexdigest()[:12]
+    for ln in open(p):
+        parts = ln.split()
+        if len(parts) >= 3 and parts[0] == kernel and parts[2] == cur:
+            return float(parts[1])
+    return None
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import bit_quantized_fine_nf4_b300 as q
+    import synthetic
+
+    q.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    peaks, peak_src = load_peaks()
+    # -------------------------------------------------------------- workload (resident in HBM)
+    case = synthetic.linear_case(N_, K_, M_, R_, ALPHA_, device="cuda", base_seed=0)
+    rec = q.quantize(case.w)
+    q.check_status()
+    x, a, b, dy = case.x, case.a, case.b, case.dy
+    y = torch.empty((M_, N_), dtype=torch.bfloat16, device=dev)
+    t_save = torch.empty((M_, R_), dtype=torch.float32, device=dev)
+    dx = torch.empty((M_, K_), dtype=torch.bfloat16, device=dev)
+    da = torch.empty((R_, K_), dtype=torch.float32, device=dev)
+    db = torch.empty((N_, R_), dtype=torch.float32, device=dev)
+    ws_f = torch.empty(max(q.fwd_workspace_bytes(M_, N_, K_, R_), 256), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(max(q.bwd_workspace_bytes(M_, N_, K_, R_), 256), dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 126 MB L2
+
+    def flush():
+        flush_buf.zero_()
+
+    def allreduce_grads():
+        if world > 1:
+            import torch.distributed as dist
+            dist.all_reduce(da)
+            dist.all_reduce(db)
+
+    def step():
+        q.linear_fwd(x, rec, a, b, ALPHA_, y=y, t_save=t_save, workspace=ws_f)
+        q.linear_bwd(dy, x, rec, a, b, ALPHA_, t_save, dx=dx, da=da, db=db, workspace=ws_b)
+        allreduce_grads()
+
+    flops = step_flops(M_, N_, K_, R_)
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    q.check_status()
+
+    # -------------------------------------------------------------- headline timed region
+    clocks = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    l0 = q.launch_count()
+    ms = time_events(torch, step, args.steps, flush)
+    launches = q.launch_count() - l0
+    barrier(world)
+    clk = clocks.stop()
+    q.check_status()
+    ms_step = allreduce_max(sum(ms) / len(ms), world)
+    value = flops * world / (ms_step / 1e3) / 1e12
+
+    # -------------------------------------------------------------- roofline of the dominant kernel
+    q.profile_reset()
+    q.profile_enable(True)
+    time_events(torch, step, args.steps, flush)
+    q.profile_enable(False)
+    prof = q.profile_read()
+    q.check_status()
+    kflops = {
+        "fwd_gemm": 2.0 * M_ * N_ * K_ + 2.0 * M_ * R_ * N_,
+        "bwd_dx_gemm": 2.0 * M_ * N_ * K_ + 2.0 * M_ * R_ * K_,
+    }
+    dominant = max(prof.items(), key=lambda kv: kv[1][0])[0] if prof else None
+    roof = None
+    if dominant in kflops:
+        tot_ms, calls = prof[dominant]
+        avg = tot_ms / calls
+        ach = kflops[dominant] / (avg / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": dominant, "achieved": ach, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"], "traffic": traffic_for(dominant),
+                "peak_source": peak_src + " bf16 burst (kernel timed inside a sub-millisecond step)",
+                "avg_launch_ms": avg, "flops_per_launch": kflops[dominant]}
+    shares = {k: {"ms_per_step": v[0] / args.steps, "share": v[0] / sum(t for t, _ in prof.values())}
+              for k, v in prof.items()} if prof else {}
+    for k, kf in kflops.items():
+        if k in prof:
+            tot, c = prof[k]
+            shares[k]["tflops"] = kf / (tot / c / 1e3) / 1e12
+
+    # -------------------------------------------------------------- end to end (host buffers)
+    x_h = x.cpu().pin_memory()
+    dy_h = dy.cpu().pin_memory()
+    da_h = torch.empty(da.shape, dtype=da.dtype).pin_memory()
+    db_h = torch.empty(db.shape, dtype=db.dtype).pin_memory()
+
+    def e2e_step():
+        x.copy_(x_h, non_blocking=True)
+        dy.copy_(dy_h, non_blocking=True)
+        step()
+        da_h.copy_(da, non_blocking=True)
+        db_h.copy_(db, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = time_events(torch, e2e_step, args.steps, flush)
+    e2e_step_ms = allreduce_max(sum(e2e_ms) / len(e2e_ms), world)
+    e2e = {"value": flops * world / (e2e_step_ms / 1e3) / 1e12, "unit": "TFLOP/s",
+           "h2d_bytes_per_step": x.numel() * 2 + dy.numel() * 2, "d2h_bytes_per_step": da.numel() * 4 + db.numel() * 4,
+           "ms_per_step": e2e_step_ms}
+
+    # -------------------------------------------------------------- secondary figures
+    secondary = {"kernel_shares": shares}
+    if not args.quick:
+        secondary.update(dequant_quant_rates(q, torch, rec, case.w, flush))
+        del y, dx
+        torch.cuda.empty_cache()
+        sweep = decode_sweep(q, torch, layers=args.decode_layers)
+        for t in (1, 4, 16):
+            if "t%d" % t in sweep:
+                sweep["t%d" % t]["frac_of_hbm"] = sweep["t%d" % t]["weight_gbs"] / peaks["hbm_gbs"]
+        secondary["decode_sweep"] = sweep
+        secondary["dequant"]["frac_of_hbm"] = secondary["dequant"]["gbs"] / peaks["hbm_gbs"]
+        secondary["quantize"]["frac_of_hbm"] = secondary["quantize"]["gbs"] / peaks["hbm_gbs"]
+
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "n": N_, "k": K_, "m": M_, "r": R_, "alpha": ALPHA_,
+                       "weights": "nf4 + double-quant (block 64, dq group 256)",
+                       "l2": "flushed between steps (256 MB write outside the timed events)",
+                       "parallelism": "dp%d (replica per GPU, all-reduce of dA/dB)" % world},
+            "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
+            "frac_of_bf16_peak": value / world / peaks["bf16_tflops"], "secondary": secondary}
+    if rank == 0 and world == 1 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline only (no decode sweep / dequant rates)")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--ref-rows", type=int, default=128)
+    ap.add_argument("--decode-layers", type=int, default=32)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup(args)
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,486 @@
+// C entry points of libqlora_nf4.so (declared and documented in include/qlora_nf4.h):
+// argument checks, workspace carving, the latched device status word.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kernels.h"
+#include "qlora_nf4.h"
+
+// Latched device status bits of this module (one word per device).
+static __device__ unsigned g_qlora_status;
+
+namespace {
+
+thread_local char t_last_error[512] = "";
+std::atomic<unsigned long long> g_wait_ns{2000000000ull};
+
+struct DevInfo {
+  bool ready = false;
+  int supported = 0;
+  int num_sms = 0;
+  unsigned* status = nullptr;
+};
+std::mutex g_mu;
+DevInfo g_dev[128];
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_last_error, sizeof(t_last_error), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int device(DevInfo** out) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (d < 0 || d >= 128) return fail(QLORA_ERR_UNSUPPORTED, "device index %d", d);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& di = g_dev[d];
+  if (!di.ready) {
+    int major = 0, minor = 0, sms = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, d);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, d);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+    di.supported = (major == 10 && minor == 3);
+    di.num_sms = sms;
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_qlora_status);
+    if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
+    di.status = static_cast<unsigned*>(p);
+    di.ready = true;
+  }
+  if (!di.supported) return fail(QLORA_ERR_UNSUPPORTED, "the kernels are built for sm_103a only");
+  *out = &di;
+  return QLORA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+int cuda_ret(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return QLORA_OK;
+  if (e == cudaErrorInvalidValue && qlora::tensor_map_error()[0])
+    return fail(QLORA_ERR_CUDA, "%s: %s", what, qlora::tensor_map_error());
+  return fail(QLORA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int check_weight(const qlora_nf4_weight* w) {
+  if (!w) return fail(QLORA_ERR_INVALID_ARGUMENT, "weight record is NULL");
+  if (!w->codes || !w->absmax_q || !w->absmax_step || !w->absmax_mean)
+    return fail(QLORA_ERR_INVALID_ARGUMENT, "weight record has a NULL pointer");
+  if (!aligned16(w->codes) || !aligned16(w->absmax_q))
+    return fail(QLORA_ERR_INVALID_ARGUMENT, "weight codes / absmax_q must be 16-byte aligned");
+  if (w->n <= 0 || w->k <= 0) return fail(QLORA_ERR_INVALID_ARGUMENT, "weight shape [%lld, %lld]", (long long)w->n, (long long)w->k);
+  if (w->k % 64) return fail(QLORA_ERR_UNSUPPORTED, "k = %lld is not a multiple of 64", (long long)w->k);
+  if (w->n % 8) return fail(QLORA_ERR_UNSUPPORTED, "n = %lld is not a multiple of 8", (long long)w->n);
+  if (w->n >= (1ll << 31) || w->k >= (1ll << 31)) return fail(QLORA_ERR_UNSUPPORTED, "weight dimension >= 2^31");
+  return QLORA_OK;
+}
+
+int check_rank(int r) {
+  if (r < 8 || r > 128 || (r % 8)) return fail(QLORA_ERR_UNSUPPORTED, "rank r = %d (need 8 <= r <= 128, r %% 8 == 0)", r);
+  return QLORA_OK;
+}
+
+int check_ptr(const void* p, const char* name) {
+  if (!p) return fail(QLORA_ERR_INVALID_ARGUMENT, "%s is NULL", name);
+  if (!aligned16(p)) return fail(QLORA_ERR_INVALID_ARGUMENT, "%s is not 16-byte aligned", name);
+  return QLORA_OK;
+}
+
+struct FwdWs {
+  size_t st, ld, gemm, total;
+};
+FwdWs fwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
+  FwdWs w;
+  if (m <= 0) {
+    w.st = w.ld = w.gemm = w.total = 0;
+    return w;
+  }
+  w.st = align256(static_cast<size_t>(m) * r * 2);
+  w.ld = align256(qlora::lora_down_workspace_bytes(static_cast<int>(m), static_cast<int>(k), r, sms));
+  w.gemm = align256(qlora::fwd_gemm_workspace_bytes(static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), sms));
+  w.total = w.st + w.ld + w.gemm;
+  return w;
+}
+
+struct BwdWs {
+  size_t bt, su, st, ld, total;
+};
+BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
+  (void)k;
+  BwdWs w;
+  if (m <= 0) {
+    w.bt = w.su = w.st = w.ld = w.total = 0;
+    return w;
+  }
+  w.bt = align256(static_cast<size_t>(n) * r * 2);
+  w.su = align256(static_cast<size_t>(m) * r * 2);
+  w.st = w.su;
+  w.ld = align256(qlora::lora_down_workspace_bytes(static_cast<int>(m), static_cast<int>(n), r, sms));
+  w.total = w.bt + w.su + w.st + w.ld;
+  return w;
+}
+
+// ---------------------------------------------------------------- tracing
+// Every launcher call made by the entry points is counted (kernels launched),
+// and, while profiling is on, bracketed by two CUDA events on its stream.
+enum ProfName : int {
+  P_QUANTIZE = 0, P_DEQUANTIZE, P_LORA_DOWN, P_FWD_GEMM, P_TRANSPOSE, P_SCALE, P_BWD_GEMM, P_LORA_GRADS,
+  P_SILU_FWD, P_SILU_BWD, P_SELFTEST, P_COUNT
+};
+const char* const kProfNames[P_COUNT] = {"nf4_quantize(3 kernels)", "nf4_dequantize", "lora_down", "fwd_gemm",
+                                         "transpose_b", "scale_t", "bwd_dx_gemm", "lora_grads", "silu_mul_fwd",
+                                         "silu_mul_bwd", "wait_selftest"};
+std::atomic<unsigned long long> g_launches{0};
+std::atomic<bool> g_prof_on{false};
+struct ProfRec {
+  int name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_free;
+double g_prof_ms[P_COUNT] = {0};
+long long g_prof_calls[P_COUNT] = {0};
+
+cudaEvent_t prof_event() {
+  if (!g_prof_free.empty()) {
+    cudaEvent_t e = g_prof_free.back();
+    g_prof_free.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+struct Span {
+  int name;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  Span(int n, cudaStream_t st, int kernels) : name(n), s(st) {
+    g_launches.fetch_add(static_cast<unsigned long long>(kernels));
+    if (!g_prof_on.load()) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    a = prof_event();
+    if (a) cudaEventRecord(a, s);
+  }
+  ~Span() {
+    if (!a) return;
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    cudaEvent_t b = prof_event();
+    if (!b) return;
+    cudaEventRecord(b, s);
+    g_prof_recs.push_back(ProfRec{name, a, b});
+  }
+};
+
+qlora::Nf4Dev to_dev(const qlora_nf4_weight* w) {
+  qlora::Nf4Dev d;
+  d.codes = w->codes;
+  d.absq = w->absmax_q;
+  d.step = w->absmax_step;
+  d.mean = w->absmax_mean;
+  d.n = w->n;
+  d.k = w->k;
+  return d;
+}
+
+}  // namespace
+
+extern "C" {
+
+int qlora_nf4_quantize_workspace_bytes(int64_t n, int64_t k, size_t* bytes) {
+  if (!bytes) return fail(QLORA_ERR_INVALID_ARGUMENT, "bytes is NULL");
+  if (n <= 0 || k <= 0 || k % 64) return fail(QLORA_ERR_INVALID_ARGUMENT, "shape [%lld, %lld]", (long long)n, (long long)k);
+  *bytes = align256(static_cast<size_t>(n) * k / 64 * 4) + 256 * 8 + 256;
+  return QLORA_OK;
+}
+
+int qlora_nf4_quantize(const void* w, int w_dtype, int64_t n, int64_t k, const qlora_nf4_weight* out,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if ((rc = check_weight(out))) return rc;
+  if (out->n != n || out->k != k) return fail(QLORA_ERR_INVALID_ARGUMENT, "record shape differs from the weight shape");
+  if ((rc = check_ptr(w, "w"))) return rc;
+  if (w_dtype != QLORA_DTYPE_F32 && w_dtype != QLORA_DTYPE_BF16) return fail(QLORA_ERR_INVALID_ARGUMENT, "w_dtype %d", w_dtype);
+  size_t need = 0;
+  qlora_nf4_quantize_workspace_bytes(n, k, &need);
+  if ((rc = check_ptr(workspace, "workspace"))) return rc;
+  if (workspace_bytes < need) return fail(QLORA_ERR_INVALID_ARGUMENT, "workspace %zu < %zu bytes", workspace_bytes, need);
+  float* absmax = static_cast<float*>(workspace);
+  void* bins = static_cast<char*>(workspace) + align256(static_cast<size_t>(n) * k / 64 * 4);
+  Span sp(P_QUANTIZE, static_cast<cudaStream_t>(stream), 3);
+  return cuda_ret(qlora::launch_nf4_quantize(w, w_dtype == QLORA_DTYPE_F32 ? 0 : 1, n * k, out->codes, absmax,
+                                             out->absmax_q, out->absmax_step, out->absmax_mean, bins, di->status,
+                                             di->num_sms, static_cast<cudaStream_t>(stream)),
+                  "quantize");
+}
+
+int qlora_nf4_dequantize(const qlora_nf4_weight* w, uint16_t* out, void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if ((rc = check_weight(w))) return rc;
+  if ((rc = check_ptr(out, "out"))) return rc;
+  Span sp(P_DEQUANTIZE, static_cast<cudaStream_t>(stream), 1);
+  return cuda_ret(qlora::launch_nf4_dequantize(w->codes, w->absmax_q, w->absmax_step, w->absmax_mean, out,
+                                               w->n * w->k, di->num_sms, static_cast<cudaStream_t>(stream)),
+                  "dequantize");
+}
+
+int qlora_linear_fwd_workspace_bytes(int64_t m, int64_t n, int64_t k, int r, size_t* bytes) {
+  if (!bytes) return fail(QLORA_ERR_INVALID_ARGUMENT, "bytes is NULL");
+  if (m < 0 || n <= 0 || k <= 0 || m >= (1ll << 31)) return fail(QLORA_ERR_INVALID_ARGUMENT, "shape");
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  *bytes = fwd_ws(m, n, k, r, di->num_sms).total;
+  return QLORA_OK;
+}
+
+int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, const uint16_t* lora_a,
+                     const uint16_t* lora_b, int r, float alpha, uint16_t* y, float* t_save, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if ((rc = check_weight(w))) return rc;
+  if ((rc = check_rank(r))) return rc;
+  if (m < 0 || m >= (1ll << 31)) return fail(QLORA_ERR_INVALID_ARGUMENT, "m = %lld", (long long)m);
+  if (m == 0) return QLORA_OK;
+  if ((rc = check_ptr(x, "x")) || (rc = check_ptr(lora_a, "lora_a")) || (rc = check_ptr(lora_b, "lora_b")) ||
+      (rc = check_ptr(y, "y")) || (rc = check_ptr(t_save, "t_save")))
+    return rc;
+  const FwdWs ws = fwd_ws(m, w->n, w->k, r, di->num_sms);
+  if ((rc = check_ptr(workspace, "workspace"))) return rc;
+  if (workspace_bytes < ws.total) return fail(QLORA_ERR_INVALID_ARGUMENT, "workspace %zu < %zu bytes", workspace_bytes, ws.total);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(workspace);
+  __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(base);
+  const float scale = alpha / static_cast<float>(r);
+  const int M = static_cast<int>(m), N = static_cast<int>(w->n), K = static_cast<int>(w->k);
+  cudaError_t e;
+  {
+    Span sp(P_LORA_DOWN, s, 1);
+    e = qlora::launch_lora_down(reinterpret_cast<const __nv_bfloat16*>(x),
+                                          reinterpret_cast<const __nv_bfloat16*>(lora_a), M, K, r, scale, t_save, st,
+                                          base + ws.st, di->num_sms, s);
+  }
+  if (e != cudaSuccess) return cuda_ret(e, "lora_down");
+  {
+    Span sp(P_FWD_GEMM, s, 1);
+    e = qlora::launch_fwd_gemm(reinterpret_cast<const __nv_bfloat16*>(x), M, to_dev(w), st,
+                             reinterpret_cast<const __nv_bfloat16*>(lora_b), r, reinterpret_cast<__nv_bfloat16*>(y),
+                             base + ws.st + ws.ld, di->status, g_wait_ns.load(), di->num_sms, s);
+  }
+  (void)N;
+  return cuda_ret(e, "fwd_gemm");
+}
+
+int qlora_linear_bwd_workspace_bytes(int64_t m, int64_t n, int64_t k, int r, size_t* bytes) {
+  if (!bytes) return fail(QLORA_ERR_INVALID_ARGUMENT, "bytes is NULL");
+  if (m < 0 || n <= 0 || k <= 0 || m >= (1ll << 31)) return fail(QLORA_ERR_INVALID_ARGUMENT, "shape");
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  *bytes = bwd_ws(m, n, k, r, di->num_sms).total;
+  return QLORA_OK;
+}
+
+int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlora_nf4_weight* w,
+                     const uint16_t* lora_a, const uint16_t* lora_b, int r, float alpha, const float* t_save,
+                     uint16_t* dx, float* da, float* db, int flags, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if ((rc = check_weight(w))) return rc;
+  if ((rc = check_rank(r))) return rc;
+  if (m < 0 || m >= (1ll << 31)) return fail(QLORA_ERR_INVALID_ARGUMENT, "m = %lld", (long long)m);
+  if (flags & ~(QLORA_ACCUM_DX | QLORA_ACCUM_DA | QLORA_ACCUM_DB)) return fail(QLORA_ERR_INVALID_ARGUMENT, "flags 0x%x", flags);
+  if ((rc = check_ptr(da, "da")) || (rc = check_ptr(db, "db"))) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (m == 0) {
+    // no tokens: the gradients are zero (or unchanged when accumulating)
+    cudaError_t e = cudaSuccess;
+    if (!(flags & QLORA_ACCUM_DA)) e = cudaMemsetAsync(da, 0, static_cast<size_t>(r) * w->k * 4, s);
+    if (e == cudaSuccess && !(flags & QLORA_ACCUM_DB)) e = cudaMemsetAsync(db, 0, static_cast<size_t>(w->n) * r * 4, s);
+    return cuda_ret(e, "bwd m == 0");
+  }
+  if ((rc = check_ptr(dy, "dy")) || (rc = check_ptr(x, "x")) || (rc = check_ptr(lora_a, "lora_a")) ||
+      (rc = check_ptr(lora_b, "lora_b")) || (rc = check_ptr(t_save, "t_save")) || (rc = check_ptr(dx, "dx")))
+    return rc;
+  const BwdWs ws = bwd_ws(m, w->n, w->k, r, di->num_sms);
+  if ((rc = check_ptr(workspace, "workspace"))) return rc;
+  if (workspace_bytes < ws.total) return fail(QLORA_ERR_INVALID_ARGUMENT, "workspace %zu < %zu bytes", workspace_bytes, ws.total);
+  char* base = static_cast<char*>(workspace);
+  __nv_bfloat16* bt = reinterpret_cast<__nv_bfloat16*>(base);
+  __nv_bfloat16* su = reinterpret_cast<__nv_bfloat16*>(base + ws.bt);
+  __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(base + ws.bt + ws.su);
+  void* ldws = base + ws.bt + ws.su + ws.st;
+  const float scale = alpha / static_cast<float>(r);
+  const int M = static_cast<int>(m), N = static_cast<int>(w->n), K = static_cast<int>(w->k);
+  const uint64_t wait = g_wait_ns.load();
+  const __nv_bfloat16* dyb = reinterpret_cast<const __nv_bfloat16*>(dy);
+  const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
+  cudaError_t e;
+  {
+    Span sp(P_TRANSPOSE, s, 1);
+    e = qlora::launch_transpose_bf16(reinterpret_cast<const __nv_bfloat16*>(lora_b), bt, N, r, s);
+  }
+  if (e != cudaSuccess) return cuda_ret(e, "transpose B");
+  {
+    Span sp(P_LORA_DOWN, s, 1);
+    e = qlora::launch_lora_down(dyb, bt, M, N, r, scale, nullptr, su, ldws, di->num_sms, s);
+  }
+  if (e != cudaSuccess) return cuda_ret(e, "lora_down (U)");
+  {
+    Span sp(P_SCALE, s, 1);
+    e = qlora::launch_scale_to_bf16(t_save, st, static_cast<int64_t>(M) * r, scale, di->num_sms, s);
+  }
+  if (e != cudaSuccess) return cuda_ret(e, "scale T");
+  {
+    Span sp(P_BWD_GEMM, s, 1);
+    e = qlora::launch_bwd_dx_gemm(dyb, M, to_dev(w), su, reinterpret_cast<const __nv_bfloat16*>(lora_a), r,
+                                  reinterpret_cast<__nv_bfloat16*>(dx), (flags & QLORA_ACCUM_DX) ? 1 : 0, di->status,
+                                  wait, s);
+  }
+  if (e != cudaSuccess) return cuda_ret(e, "bwd dx gemm");
+  {
+    Span sp(P_LORA_GRADS, s, 1);
+    e = qlora::launch_lora_grads(xb, dyb, su, st, M, N, K, r, da, db, (flags & QLORA_ACCUM_DA) ? 1 : 0,
+                                 (flags & QLORA_ACCUM_DB) ? 1 : 0, di->status, wait, s);
+  }
+  return cuda_ret(e, "lora grads");
+}
+
+int qlora_silu_mul_fwd(const uint16_t* g, const uint16_t* u, uint16_t* h, int64_t count, void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if (count < 0 || (count & 1)) return fail(QLORA_ERR_INVALID_ARGUMENT, "count %lld must be even and >= 0", (long long)count);
+  if (count == 0) return QLORA_OK;
+  if ((rc = check_ptr(g, "g")) || (rc = check_ptr(u, "u")) || (rc = check_ptr(h, "h"))) return rc;
+  Span sp(P_SILU_FWD, static_cast<cudaStream_t>(stream), 1);
+  return cuda_ret(qlora::launch_silu_mul_fwd(g, u, h, count, di->num_sms, static_cast<cudaStream_t>(stream)), "silu fwd");
+}
+
+int qlora_silu_mul_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u, uint16_t* dg, uint16_t* du,
+                       int64_t count, void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if (count < 0 || (count & 1)) return fail(QLORA_ERR_INVALID_ARGUMENT, "count %lld must be even and >= 0", (long long)count);
+  if (count == 0) return QLORA_OK;
+  if ((rc = check_ptr(dh, "dh")) || (rc = check_ptr(g, "g")) || (rc = check_ptr(u, "u")) || (rc = check_ptr(dg, "dg")) ||
+      (rc = check_ptr(du, "du")))
+    return rc;
+  Span sp(P_SILU_BWD, static_cast<cudaStream_t>(stream), 1);
+  return cuda_ret(qlora::launch_silu_mul_bwd(dh, g, u, dg, du, count, di->num_sms, static_cast<cudaStream_t>(stream)),
+                  "silu bwd");
+}
+
+int qlora_get_status(void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "stream synchronize: %s", cudaGetErrorString(e));
+  unsigned st = 0;
+  e = cudaMemcpy(&st, di->status, sizeof(st), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  if (st) {
+    const unsigned zero = 0;
+    e = cudaMemcpy(di->status, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+  }
+  if (st & qlora::ST_TIMEOUT) return fail(QLORA_ERR_TIMEOUT, "a bounded wait expired on the device");
+  if (st & qlora::ST_NONFINITE) return fail(QLORA_ERR_NONFINITE, "non-finite weight seen by the quantiser");
+  if (st) return fail(QLORA_ERR_CUDA, "device status 0x%x", st);
+  return QLORA_OK;
+}
+
+const char* qlora_strerror(int code) {
+  switch (code) {
+    case QLORA_OK: return "ok";
+    case QLORA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case QLORA_ERR_UNSUPPORTED: return "unsupported device or shape";
+    case QLORA_ERR_CUDA: return "CUDA error";
+    case QLORA_ERR_TIMEOUT: return "bounded device wait expired";
+    case QLORA_ERR_NONFINITE: return "non-finite weight";
+    default: return "unknown error code";
+  }
+}
+
+const char* qlora_last_error(void) { return t_last_error; }
+
+int qlora_set_wait_limit_ns(uint64_t ns) {
+  if (ns == 0) return fail(QLORA_ERR_INVALID_ARGUMENT, "wait limit must be > 0");
+  g_wait_ns.store(ns);
+  return QLORA_OK;
+}
+
+int qlora_selftest_wait_timeout(uint64_t wait_ns, void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if (wait_ns == 0 || wait_ns > 10000000000ull) return fail(QLORA_ERR_INVALID_ARGUMENT, "wait_ns out of range");
+  Span sp(P_SELFTEST, static_cast<cudaStream_t>(stream), 1);
+  return cuda_ret(qlora::launch_wait_selftest(di->status, wait_ns, static_cast<cudaStream_t>(stream)), "selftest");
+}
+
+unsigned long long qlora_launch_count(void) { return g_launches.load(); }
+
+int qlora_profile_enable(int on) {
+  g_prof_on.store(on != 0);
+  return QLORA_OK;
+}
+
+int qlora_profile_collect(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (const ProfRec& r : g_prof_recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+      g_prof_ms[r.name] += ms;
+      g_prof_calls[r.name] += 1;
+    }
+    g_prof_free.push_back(r.a);
+    g_prof_free.push_back(r.b);
+  }
+  g_prof_recs.clear();
+  return P_COUNT;
+}
+
+const char* qlora_profile_name(int i) { return (i >= 0 && i < P_COUNT) ? kProfNames[i] : ""; }
+
+double qlora_profile_total_ms(int i) { return (i >= 0 && i < P_COUNT) ? g_prof_ms[i] : 0.0; }
+
+long long qlora_profile_calls(int i) { return (i >= 0 && i < P_COUNT) ? g_prof_calls[i] : 0; }
+
+int qlora_profile_reset(void) {
+  qlora_profile_collect();
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (int i = 0; i < P_COUNT; ++i) {
+    g_prof_ms[i] = 0.0;
+    g_prof_calls[i] = 0;
+  }
+  return QLORA_OK;
+}
+
+int qlora_device_sm_count(void) {
+  DevInfo* di = nullptr;
+  if (device(&di)) return 0;
+  return di->num_sms;
+}
+
+}  // extern "C"

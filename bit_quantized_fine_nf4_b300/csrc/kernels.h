@@ -1,0 +1,69 @@
+// Host-side launchers of the device kernels (internal to the library; the
+// public entry points are in include/qlora_nf4.h).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace qlora {
+
+// Bits of the latched device status word.
+enum : unsigned {
+  ST_TIMEOUT = 1u,    // a bounded wait expired
+  ST_NONFINITE = 2u,  // NaN / Inf weight seen by the quantiser
+};
+
+// nf4_quant.cu
+cudaError_t launch_nf4_quantize(const void* w, int w_dtype, int64_t n_elems, uint8_t* codes, float* absmax,
+                                int8_t* absq, float* step, float* mean, void* ws_bins, unsigned* status,
+                                int num_sms, cudaStream_t s);
+cudaError_t launch_nf4_dequantize(const uint8_t* codes, const int8_t* absq, const float* step, const float* mean,
+                                  uint16_t* out, int64_t n_elems, int num_sms, cudaStream_t s);
+
+// lora_small.cu
+int lora_down_splits(int M, int K, int num_sms);
+size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms);
+cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int M, int K, int r, float scale,
+                             float* out_f32, __nv_bfloat16* out_bf16, void* ws, int num_sms, cudaStream_t s);
+cudaError_t launch_transpose_bf16(const __nv_bfloat16* src, __nv_bfloat16* dst, int rows, int cols, cudaStream_t s);
+cudaError_t launch_scale_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, float scale, int num_sms,
+                                 cudaStream_t s);
+cudaError_t launch_silu_mul_fwd(const uint16_t* g, const uint16_t* u, uint16_t* h, int64_t n, int num_sms,
+                                cudaStream_t s);
+cudaError_t launch_silu_mul_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u, uint16_t* dg, uint16_t* du,
+                                int64_t n, int num_sms, cudaStream_t s);
+
+// qgemm.cu
+struct Nf4Dev {
+  const uint8_t* codes;
+  const int8_t* absq;
+  const float* step;
+  const float* mean;
+  int64_t n, k;
+};
+
+// Forward / decode: Y[M, N] = X[M, K] deq(W)^T + sT[M, r] B[N, r]^T   (sT = bf16(s * X A^T))
+size_t fwd_gemm_workspace_bytes(int M, int N, int K, int num_sms);
+cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, const __nv_bfloat16* st,
+                            const __nv_bfloat16* lora_b, int r, __nv_bfloat16* y, void* ws, unsigned* status,
+                            uint64_t wait_ns, int num_sms, cudaStream_t s);
+
+// Backward dX[M, K] (+)= dY[M, N] deq(W) + sU[M, r] A[r, K]   (sU = bf16(s * dY B))
+cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
+                               const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
+                               unsigned* status, uint64_t wait_ns, cudaStream_t s);
+
+// LoRA gradients: dA[r, K] (+)= sU^T X   and   dB[N, r] (+)= dY^T sT
+cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __nv_bfloat16* su,
+                              const __nv_bfloat16* st, int M, int N, int K, int r, float* da, float* db,
+                              int accum_da, int accum_db, unsigned* status, uint64_t wait_ns, cudaStream_t s);
+
+// Bounded-wait self test: one CTA waits on an mbarrier nothing arrives on.
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t wait_ns, cudaStream_t s);
+
+const char* tensor_map_error();
+
+}  // namespace qlora

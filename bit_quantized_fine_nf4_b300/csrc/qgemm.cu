@@ -1,0 +1,816 @@
+// tcgen05 GEMMs of the QLoRA NF4 linear.
+//
+// Glossary "QLoRA", "How QLoRA works": every frozen layer dequantises its NF4
+// weight to bfloat16 before the matmul and adds the LoRA output; gradients
+// flow through the dequantised weight into the two LoRA matrices only.  Day 25
+// notes, sections 2.1 / 6.2: output W0 x + s B A x with s = alpha / r.
+//
+// Here the dequantised weight never reaches HBM: producer warps decode NF4
+// codes straight into tensor-core operands.
+//
+// k_qgemm_wa  (forward and small-token decode)
+//   D^T[n, m] = sum_k deq(W)[n, k] X[m, k]  +  sum_j B[n, j] sT[m, j]
+//   A operand = 128 rows of deq(W) (then of LoRA B), written by the producers
+//               into TMEM with tcgen05.st (one thread = one row = one TMEM lane,
+//               one 64-wide k block = one absmax block = 32 TMEM columns);
+//   B operand = NTOK token rows of X (then of sT = bf16(s X A^T)), TMA, 128B swizzle.
+//   The LoRA up-projection is one (or two, r > 64) extra k blocks of the same
+//   accumulator.  Optional split-K with a fixed-order reduction (decode shapes).
+// k_qgemm_wb  (backward dX)
+//   D[m, k] = sum_n dY[m, n] deq(W)[n, k]  +  sum_j sU[m, j] A[j, k]
+//   A operand = 128 token rows of dY (then sU = bf16(s dY B)), TMA;
+//   B operand = deq(W)[n-block of 64, 256 output columns], MN-major 128B swizzle,
+//               written by the producers with st.shared (then LoRA A rows, TMA).
+// k_lora_grad (LoRA gradients, both MN-major operands, HBM-bound)
+//   dA^T[k, j] = sum_m X[m, k] sU[m, j],   dB[n, j] = sum_m dY[m, n] sT[m, j].
+#include <cudaTypedefs.h>
+
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace qlora {
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ void abort_cta(unsigned* status, int* abort_flag) {
+  latch_status(status, ST_TIMEOUT);
+  *reinterpret_cast<volatile int*>(abort_flag) = 1;
+}
+
+// ====================================================================== forward / decode
+struct WaParams {
+  const uint8_t* codes;
+  const int8_t* absq;
+  const float* step;
+  const float* mean;
+  const __nv_bfloat16* lora_b;  // [N, r]
+  __nv_bfloat16* y;             // [M, N]
+  float* partial;               // [splits][tiles][128][NTOK] (split-K only)
+  unsigned* counters;           // [tiles]
+  unsigned* status;
+  int M, N, K, r;
+  int kb_per_split, splits, lora_blocks;
+  unsigned long long wait_ns;
+};
+
+constexpr int kWaThreads = 320;  // warp 0: TMA + TMEM alloc, warp 1: MMA, warps 2..9: producers / epilogue
+
+template <int NTOK, int STAGES>
+struct WaCfg {
+  static constexpr uint32_t kBBytes = NTOK * 128;
+  static constexpr uint32_t kDCol = STAGES * 32;
+  static constexpr uint32_t kTmemCols =
+      (kDCol + NTOK) <= 32 ? 32 : (kDCol + NTOK) <= 64 ? 64 : (kDCol + NTOK) <= 128 ? 128 : (kDCol + NTOK) <= 256 ? 256 : 512;
+  static constexpr size_t kSmem = 1024 + STAGES * kBBytes + (2 * STAGES + 1) * 8 + 16;
+  static_assert(kDCol + NTOK <= 512, "TMEM budget");
+  static_assert(NTOK % 16 == 0 && NTOK >= 16 && NTOK <= 256, "MMA N for M = 128");
+};
+
+template <int NTOK, int STAGES>
+__global__ void __launch_bounds__(kWaThreads, 1)
+    k_qgemm_wa(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_st, const WaParams p) {
+  using Cfg = WaCfg<NTOK, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sb = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * Cfg::kBBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  int* last_flag = abort_flag + 1;
+  volatile int* vabort = abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * 128, tok0 = blockIdx.y * NTOK, split = blockIdx.z;
+  const int tile = blockIdx.x + gridDim.x * blockIdx.y;
+  const int kb_total = p.K / 64;
+  const int kb_begin = split * p.kb_per_split;
+  const int kb_end = min(kb_total, kb_begin + p.kb_per_split);
+  const int n_main = kb_end - kb_begin;
+  const int n_iter = n_main + (split == p.splits - 1 ? p.lora_blocks : 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1 + 128);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_st);
+      for (int i = 0; i < n_iter; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
+        mbar_arrive_expect_tx(&full[s], Cfg::kBBytes);
+        if (i < n_main)
+          tma_load_2d(sb + s * Cfg::kBBytes, &tm_x, &full[s], (kb_begin + i) * 64, tok0);
+        else
+          tma_load_2d(sb + s * Cfg::kBBytes, &tm_st, &full[s], (i - n_main) * 64, tok0);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, NTOK, 0, 0);
+      const uint32_t d_tmem = tbase + Cfg::kDCol;
+      for (int i = 0; i < n_iter; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (!mbar_wait(&full[s], ph, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
+        tc_fence_after();
+        const uint32_t b_addr = smem_u32(sb + s * Cfg::kBBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t bdesc = sdesc_sw128(b_addr + kk * 32, 16, 1024);
+          mma_bf16_ts(d_tmem, tbase + s * 32 + kk * 8, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(acc_full);
+    }
+  } else {
+    // ---------------------------------------------------------------- producers
+    const int team = (warp - 2) >> 2;
+    const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31 are the only ones this warp may touch
+    const int row = n0 + quarter * 32 + lane;
+    const bool row_ok = row < p.N;
+    const float mu = *p.mean;
+    const int kb_row = p.K / 64;
+    const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    bool alive = true;
+    for (int i = team; i < n_iter && alive; i += 2) {
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      uint32_t words[32];
+      if (i < n_main) {
+        const int kb = kb_begin + i;
+        if (row_ok) {
+          const uint8_t* cp = p.codes + static_cast<int64_t>(row) * (p.K / 2) + kb * 32;
+          const uint4 c0 = ldg_nc_v4(cp), c1 = ldg_nc_v4(cp + 16);
+          const int64_t ai = static_cast<int64_t>(row) * kb_row + kb;
+          const float a2 = restore_absmax(p.absq[ai], p.step[ai >> 8], mu);
+          nf4_decode_block(c0, c1, a2, words);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) words[c] = 0;
+        }
+      } else {
+        const int jb = (i - n_main) * 64;
+        const uint32_t* brow = reinterpret_cast<const uint32_t*>(p.lora_b + static_cast<int64_t>(row) * p.r);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int j = jb + 2 * c;
+          words[c] = (row_ok && j < p.r) ? brow[j >> 1] : 0u;
+        }
+      }
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort));
+      if (!ok) { if (lane == 0) abort_cta(p.status, abort_flag); alive = false; break; }
+      tc_fence_after();
+      __syncwarp();
+      tmem_st_32x32b_x32(tbase + lane_field + s * 32, words);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&full[s]);
+    }
+    // ---------------------------------------------------------------- epilogue
+    bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, p.wait_ns, vabort));
+    ok = ok && !*vabort;
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    const int col_lo = (NTOK <= 32) ? 0 : team * (NTOK / 2);
+    const int ncols = (NTOK <= 32) ? (team == 0 ? NTOK : 0) : NTOK / 2;
+    const uint32_t dcol = tbase + lane_field + Cfg::kDCol;
+    if (ok) {
+      if (p.splits == 1) {
+        for (int c = col_lo; c < col_lo + ncols; c += 16) {
+          uint32_t v[16];
+          __syncwarp();
+          tmem_ld_32x32b_x16(dcol + c, v);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int tok = tok0 + c + j;
+              if (tok < p.M) p.y[static_cast<int64_t>(tok) * p.N + row] = __float2bfloat16_rn(__uint_as_float(v[j]));
+            }
+          }
+        }
+      } else {
+        float* part = p.partial + (static_cast<int64_t>(split) * gridDim.x * gridDim.y + tile) * 128 * NTOK +
+                      (quarter * 32 + lane) * NTOK;
+        for (int c = col_lo; c < col_lo + ncols; c += 16) {
+          uint32_t v[16];
+          __syncwarp();
+          tmem_ld_32x32b_x16(dcol + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 16; j += 4)
+            *reinterpret_cast<uint4*>(part + c + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+      }
+    }
+    if (p.splits > 1) {
+      __threadfence();
+      named_bar_sync(1, 256);
+      if (threadIdx.x == 64) *last_flag = (atomicAdd(p.counters + tile, 1u) == static_cast<unsigned>(p.splits - 1));
+      named_bar_sync(1, 256);
+      if (*reinterpret_cast<volatile int*>(last_flag)) {
+        __threadfence();
+        if (row_ok) {
+          for (int c = col_lo; c < col_lo + ncols; ++c) {
+            const int tok = tok0 + c;
+            if (tok >= p.M) break;
+            float acc = 0.f;
+            for (int sp = 0; sp < p.splits; ++sp)
+              acc += __ldcg(p.partial + (static_cast<int64_t>(sp) * gridDim.x * gridDim.y + tile) * 128 * NTOK +
+                            (quarter * 32 + lane) * NTOK + c);
+            p.y[static_cast<int64_t>(tok) * p.N + row] = __float2bfloat16_rn(acc);
+          }
+        }
+        if (threadIdx.x == 64) p.counters[tile] = 0;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, Cfg::kTmemCols);
+  }
+}
+
+// ====================================================================== backward dX
+struct WbParams {
+  const uint8_t* codes;
+  const int8_t* absq;
+  const float* step;
+  const float* mean;
+  __nv_bfloat16* dx;  // [M, K]
+  unsigned* status;
+  int M, N, K, r;
+  int lora_blocks, accumulate;
+  unsigned long long wait_ns;
+};
+
+constexpr int kWbThreads = 320;
+constexpr uint32_t kWbABytes = 128 * 128;      // 128 tokens x 64 n, bf16
+constexpr uint32_t kWbBBytes = 4 * 64 * 128;   // 4 slabs of [64 n rows x 64 k]
+constexpr uint32_t kWbStage = kWbABytes + kWbBBytes;
+
+template <int STAGES>
+struct WbCfg {
+  static constexpr size_t kSmem = 1024 + STAGES * kWbStage + (2 * STAGES + 1) * 8 + 16;
+};
+
+template <int STAGES>
+__global__ void __launch_bounds__(kWbThreads, 1)
+    k_qgemm_wb(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_su,
+               const __grid_constant__ CUtensorMap tm_la, const WbParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * kWbStage);
+  uint64_t* empty = full + STAGES;
+  uint64_t* acc_full = empty + STAGES;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  volatile int* vabort = abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k0 = blockIdx.x * 256, tok0 = blockIdx.y * 128;
+  const int n_main = (p.N + 63) / 64;
+  const int n_iter = n_main + p.lora_blocks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1 + 128);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(tmem_holder, 256);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_dy);
+      tma_prefetch_desc(&tm_su);
+      tma_prefetch_desc(&tm_la);
+      for (int i = 0; i < n_iter; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
+        uint8_t* sa = smem + s * kWbStage;
+        if (i < n_main) {
+          mbar_arrive_expect_tx(&full[s], kWbABytes);
+          tma_load_2d(sa, &tm_dy, &full[s], i * 64, tok0);
+        } else {
+          const int e = i - n_main;
+          mbar_arrive_expect_tx(&full[s], kWbStage);
+          tma_load_2d(sa, &tm_su, &full[s], e * 64, tok0);
+#pragma unroll
+          for (int sl = 0; sl < 4; ++sl) tma_load_2d(sa + kWbABytes + sl * 8192, &tm_la, &full[s], k0 + sl * 64, e * 64);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, 256, 0, 1);
+      for (int i = 0; i < n_iter; ++i) {
+        const int s = i % STAGES;
+        const uint32_t ph = (i / STAGES) & 1;
+        if (!mbar_wait(&full[s], ph, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(smem + s * kWbStage);
+        const uint32_t b_addr = a_addr + kWbABytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t adesc = sdesc_sw128(a_addr + kk * 32, 16, 1024);
+          const uint64_t bdesc = sdesc_sw128(b_addr + kk * 2048, 8192, 1024);
+          mma_bf16_ss(tbase, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(acc_full);
+    }
+  } else {
+    // ---------------------------------------------------------------- producers
+    const int team = (warp - 2) >> 2;
+    const int t = ((warp - 2) & 3) * 32 + lane;  // 0..127 within the team
+    const float mu = *p.mean;
+    const int kb_row = p.K / 64;
+    bool alive = true;
+    for (int i = team; i < n_iter && alive; i += 2) {
+      const int s = i % STAGES;
+      const uint32_t ph = (i / STAGES) & 1;
+      const bool is_main = i < n_main;
+      uint4 c[2][2];
+      float a2[2];
+      bool uok[2];
+      if (is_main) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int u = t + h * 128;
+          const int rrow = u & 63, slab = u >> 6;
+          const int n = i * 64 + rrow;
+          const int kblk = (k0 >> 6) + slab;
+          uok[h] = (n < p.N) && (kblk < kb_row);
+          if (uok[h]) {
+            const uint8_t* cp = p.codes + static_cast<int64_t>(n) * (p.K / 2) + kblk * 32;
+            c[h][0] = ldg_nc_v4(cp);
+            c[h][1] = ldg_nc_v4(cp + 16);
+            const int64_t ai = static_cast<int64_t>(n) * kb_row + kblk;
+            a2[h] = restore_absmax(p.absq[ai], p.step[ai >> 8], mu);
+          }
+        }
+      }
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort));
+      if (!ok) { if (lane == 0) abort_cta(p.status, abort_flag); alive = false; break; }
+      if (is_main) {
+        const uint32_t sbase = smem_u32(smem + s * kWbStage + kWbABytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int u = t + h * 128;
+          const uint32_t rrow = u & 63, slab = u >> 6;
+          uint32_t words[32];
+          if (uok[h]) {
+            nf4_decode_block(c[h][0], c[h][1], a2[h], words);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) words[q] = 0;
+          }
+          const uint32_t slab_base = sbase + slab * 8192;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            sts_v4(slab_base + sw128_offset(rrow, ch), words[4 * ch], words[4 * ch + 1], words[4 * ch + 2],
+                   words[4 * ch + 3]);
+        }
+        fence_proxy_async_smem();
+      }
+      mbar_arrive(&full[s]);
+    }
+    // ---------------------------------------------------------------- epilogue
+    bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, p.wait_ns, vabort));
+    ok = ok && !*vabort;
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    const int quarter = warp & 3;
+    const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    const int tok = tok0 + quarter * 32 + lane;
+    if (ok) {
+      for (int cc = 0; cc < 128; cc += 32) {
+        const int col = team * 128 + cc;
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(tbase + lane_field + col, v);
+        tmem_ld_wait();
+        const int kc = k0 + col;
+        if (tok < p.M && kc < p.K) {
+          uint4* dst = reinterpret_cast<uint4*>(p.dx + static_cast<int64_t>(tok) * p.K + kc);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) f[j] = __uint_as_float(v[8 * q + j]);
+            if (p.accumulate) {
+              const uint4 old = dst[q];
+              const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                f[2 * j] += __uint_as_float(ow[j] << 16);
+                f[2 * j + 1] += __uint_as_float(ow[j] & 0xffff0000u);
+              }
+            }
+            dst[q] = make_uint4(pack_bf16x2_rn(f[0], f[1]), pack_bf16x2_rn(f[2], f[3]), pack_bf16x2_rn(f[4], f[5]),
+                                pack_bf16x2_rn(f[6], f[7]));
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 256);
+  }
+}
+
+// ====================================================================== LoRA gradients
+struct LgParams {
+  float* da;  // [r, K]
+  float* db;  // [N, r]
+  unsigned* status;
+  int M, N, K, r;
+  int tiles_a;
+  int accum_da, accum_db;
+  unsigned long long wait_ns;
+};
+
+constexpr int kLgThreads = 192;  // warp 0 TMA + TMEM, warp 1 MMA, warps 2..5 epilogue
+constexpr int kLgStages = 4;
+
+template <int RP>  // MMA N: 64 or 128
+struct LgCfg {
+  static constexpr uint32_t kABytes = 2 * 8192;           // [64 m x 128 c] as two 64-wide slabs
+  static constexpr uint32_t kBBytes = (RP / 64) * 8192;   // [64 m x RP j]
+  static constexpr uint32_t kStage = kABytes + kBBytes;
+  static constexpr size_t kSmem = 1024 + kLgStages * kStage + (2 * kLgStages + 1) * 8 + 16;
+};
+
+template <int RP>
+__global__ void __launch_bounds__(kLgThreads, 1)
+    k_lora_grad(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
+                const __grid_constant__ CUtensorMap tm_su, const __grid_constant__ CUtensorMap tm_st,
+                const LgParams p) {
+  using Cfg = LgCfg<RP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kLgStages * Cfg::kStage);
+  uint64_t* empty = full + kLgStages;
+  uint64_t* acc_full = empty + kLgStages;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  volatile int* vabort = abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool is_b = blockIdx.x >= p.tiles_a;
+  const int c0 = (is_b ? blockIdx.x - p.tiles_a : blockIdx.x) * 128;
+  const int C = is_b ? p.N : p.K;
+  const CUtensorMap* tq = is_b ? &tm_dy : &tm_x;
+  const CUtensorMap* tp = is_b ? &tm_st : &tm_su;
+  const int n_iter = (p.M + 63) / 64;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kLgStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  constexpr uint32_t kCols = RP < 32 ? 32 : RP;
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(tmem_holder, kCols);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(tq);
+      tma_prefetch_desc(tp);
+      for (int i = 0; i < n_iter; ++i) {
+        const int s = i % kLgStages;
+        const uint32_t ph = (i / kLgStages) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
+        uint8_t* sa = smem + s * Cfg::kStage;
+        mbar_arrive_expect_tx(&full[s], Cfg::kStage);
+        tma_load_2d(sa, tq, &full[s], c0, i * 64);
+        tma_load_2d(sa + 8192, tq, &full[s], c0 + 64, i * 64);
+#pragma unroll
+        for (int sl = 0; sl < RP / 64; ++sl) tma_load_2d(sa + Cfg::kABytes + sl * 8192, tp, &full[s], sl * 64, i * 64);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, RP, 1, 1);
+      for (int i = 0; i < n_iter; ++i) {
+        const int s = i % kLgStages;
+        const uint32_t ph = (i / kLgStages) & 1;
+        if (!mbar_wait(&full[s], ph, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(smem + s * Cfg::kStage);
+        const uint32_t b_addr = a_addr + Cfg::kABytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint64_t adesc = sdesc_sw128(a_addr + kk * 2048, 8192, 1024);
+          const uint64_t bdesc = sdesc_sw128(b_addr + kk * 2048, 8192, 1024);
+          mma_bf16_ss(tbase, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+      }
+      mma_commit(acc_full);
+    }
+  } else {
+    bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, p.wait_ns, vabort));
+    ok = ok && !*vabort;
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    const int quarter = warp & 3;
+    const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    const int c = c0 + quarter * 32 + lane;
+    if (ok) {
+      for (int j0 = 0; j0 < RP; j0 += 16) {
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld_32x32b_x16(tbase + lane_field + j0, v);
+        tmem_ld_wait();
+        if (c < C) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) {
+            const int j = j0 + jj;
+            if (j >= p.r) break;
+            const float val = __uint_as_float(v[jj]);
+            if (!is_b) {
+              float* d = p.da + static_cast<int64_t>(j) * p.K + c;
+              *d = p.accum_da ? (*d + val) : val;
+            } else {
+              float* d = p.db + static_cast<int64_t>(c) * p.r + j;
+              *d = p.accum_db ? (*d + val) : val;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, kCols);
+  }
+}
+
+// ====================================================================== bounded-wait self test
+__global__ void k_wait_selftest(unsigned* status, unsigned long long wait_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, wait_ns, nullptr)) latch_status(status, ST_TIMEOUT);
+}
+
+// ====================================================================== host side
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+static char g_tm_err[256] = "";
+
+const char* tensor_map_error() { return g_tm_err; }
+
+static bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    const cudaError_t e =
+        cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e == cudaSuccess && q == cudaDriverEntryPointSuccess && fn)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    else
+      snprintf(g_tm_err, sizeof(g_tm_err), "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(e));
+  });
+  return g_encode != nullptr;
+}
+
+// bf16 matrix [outer, inner] with row pitch `pitch` bytes; box [box_outer, box_inner]; 128-byte swizzle.
+static bool make_tm(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
+                    uint32_t box_inner, uint32_t box_outer) {
+  if (!get_encode()) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {pitch};
+  const cuuint32_t box[2] = {box_inner, box_outer};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    snprintf(g_tm_err, sizeof(g_tm_err), "cuTensorMapEncodeTiled failed (%d) for [%llu x %llu] pitch %llu", (int)r,
+             (unsigned long long)outer, (unsigned long long)inner, (unsigned long long)pitch);
+    return false;
+  }
+  return true;
+}
+
+struct FwdPlan {
+  int ntok, row_tiles, tok_tiles, splits, kb_per_split;
+};
+
+static FwdPlan plan_fwd(int M, int N, int K, int num_sms) {
+  FwdPlan pl;
+  if (M < 1) M = 1;
+  if (num_sms < 1) num_sms = 1;
+  pl.ntok = M <= 16 ? 16 : (M <= 64 ? 64 : 256);
+  pl.row_tiles = (N + 127) / 128;
+  pl.tok_tiles = (M + pl.ntok - 1) / pl.ntok;
+  const int tiles = pl.row_tiles * pl.tok_tiles;
+  const int kb_total = K / 64;
+  int splits = 1;
+  if (tiles < num_sms) {
+    const int want = pl.ntok == 256 ? num_sms : 2 * num_sms;  // small tiles: two CTAs per SM fit
+    splits = (want + tiles - 1) / tiles;
+    if (splits > kb_total) splits = kb_total;
+    if (pl.ntok == 256 && splits > 4) splits = 4;
+  }
+  pl.kb_per_split = (kb_total + splits - 1) / splits;
+  pl.splits = (kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
+  return pl;
+}
+
+size_t fwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
+  const FwdPlan pl = plan_fwd(M, N, K, num_sms);
+  if (pl.splits == 1) return 0;
+  const size_t tiles = static_cast<size_t>(pl.row_tiles) * pl.tok_tiles;
+  return pl.splits * tiles * 128 * pl.ntok * sizeof(float) + tiles * 4 + 256;
+}
+
+template <int NTOK, int STAGES>
+static cudaError_t run_wa(const CUtensorMap& tx, const CUtensorMap& tst, const WaParams& prm, dim3 grid,
+                          cudaStream_t s) {
+  using Cfg = WaCfg<NTOK, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(k_qgemm_wa<NTOK, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(Cfg::kSmem));
+  if (e != cudaSuccess) return e;
+  k_qgemm_wa<NTOK, STAGES><<<grid, kWaThreads, Cfg::kSmem, s>>>(tx, tst, prm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, const __nv_bfloat16* st,
+                            const __nv_bfloat16* lora_b, int r, __nv_bfloat16* y, void* ws, unsigned* status,
+                            uint64_t wait_ns, int num_sms, cudaStream_t s) {
+  const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
+  const FwdPlan pl = plan_fwd(M, N, K, num_sms);
+  CUtensorMap tx, tst;
+  if (!make_tm(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, pl.ntok)) return cudaErrorInvalidValue;
+  if (!make_tm(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, pl.ntok)) return cudaErrorInvalidValue;
+  WaParams prm;
+  prm.codes = w.codes;
+  prm.absq = w.absq;
+  prm.step = w.step;
+  prm.mean = w.mean;
+  prm.lora_b = lora_b;
+  prm.y = y;
+  prm.partial = nullptr;
+  prm.counters = nullptr;
+  prm.status = status;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.r = r;
+  prm.kb_per_split = pl.kb_per_split;
+  prm.splits = pl.splits;
+  prm.lora_blocks = (r + 63) / 64;
+  prm.wait_ns = wait_ns;
+  if (pl.splits > 1) {
+    const size_t tiles = static_cast<size_t>(pl.row_tiles) * pl.tok_tiles;
+    prm.partial = static_cast<float*>(ws);
+    prm.counters = reinterpret_cast<unsigned*>(prm.partial + pl.splits * tiles * 128 * pl.ntok);
+    const cudaError_t e = cudaMemsetAsync(prm.counters, 0, tiles * 4, s);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid(pl.row_tiles, pl.tok_tiles, pl.splits);
+  if (pl.ntok == 16) return run_wa<16, 4>(tx, tst, prm, grid, s);
+  if (pl.ntok == 64) return run_wa<64, 4>(tx, tst, prm, grid, s);
+  return run_wa<256, 4>(tx, tst, prm, grid, s);
+}
+
+cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
+                               const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
+                               unsigned* status, uint64_t wait_ns, cudaStream_t s) {
+  const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
+  CUtensorMap tdy, tsu, tla;
+  if (!make_tm(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tm(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tm(&tla, lora_a, K, r, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
+  WbParams prm;
+  prm.codes = w.codes;
+  prm.absq = w.absq;
+  prm.step = w.step;
+  prm.mean = w.mean;
+  prm.dx = dx;
+  prm.status = status;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.r = r;
+  prm.lora_blocks = (r + 63) / 64;
+  prm.accumulate = accumulate;
+  prm.wait_ns = wait_ns;
+  constexpr int kStages = 4;
+  const size_t smem = WbCfg<kStages>::kSmem;
+  cudaError_t e =
+      cudaFuncSetAttribute(k_qgemm_wb<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  const dim3 grid((K + 255) / 256, (M + 127) / 128);
+  k_qgemm_wb<kStages><<<grid, kWbThreads, smem, s>>>(tdy, tsu, tla, prm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __nv_bfloat16* su,
+                              const __nv_bfloat16* st, int M, int N, int K, int r, float* da, float* db,
+                              int accum_da, int accum_db, unsigned* status, uint64_t wait_ns, cudaStream_t s) {
+  CUtensorMap tx, tdy, tsu, tst;
+  if (!make_tm(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_tm(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_tm(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_tm(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
+  LgParams prm;
+  prm.da = da;
+  prm.db = db;
+  prm.status = status;
+  prm.M = M;
+  prm.N = N;
+  prm.K = K;
+  prm.r = r;
+  prm.tiles_a = (K + 127) / 128;
+  prm.accum_da = accum_da;
+  prm.accum_db = accum_db;
+  prm.wait_ns = wait_ns;
+  const dim3 grid(prm.tiles_a + (N + 127) / 128);
+  if (r <= 64) {
+    const size_t smem = LgCfg<64>::kSmem;
+    cudaError_t e =
+        cudaFuncSetAttribute(k_lora_grad<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k_lora_grad<64><<<grid, kLgThreads, smem, s>>>(tx, tdy, tsu, tst, prm);
+  } else {
+    const size_t smem = LgCfg<128>::kSmem;
+    cudaError_t e =
+        cudaFuncSetAttribute(k_lora_grad<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    k_lora_grad<128><<<grid, kLgThreads, smem, s>>>(tx, tdy, tsu, tst, prm);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(unsigned* status, uint64_t wait_ns, cudaStream_t s) {
+  k_wait_selftest<<<1, 32, 0, s>>>(status, wait_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace qlora

@@ -1,0 +1,217 @@
+/*
+ * qlora_nf4.h -- C ABI of libqlora_nf4.so: the QLoRA NF4 linear layer on one
+ * B300 GPU (sm_103a).
+ *
+ * What it computes (sources cited by page title and section):
+ *   - Ultralytics glossary "QLoRA", section "How QLoRA works": each weight is a
+ *     4-bit code indexing one of 16 NF4 levels (normal quantiles with an exact
+ *     zero, normalised to [-1, 1]); 64 weights share one absmax scale; the
+ *     scales are quantised again to 8 bits in groups of 256 ("double
+ *     quantisation"); the frozen layer dequantises to bfloat16 before the
+ *     matmul, adds the LoRA output, and backpropagation updates only the two
+ *     LoRA matrices.
+ *   - Day 25 notes "Fine-tuning and LoRA/QLoRA", section 2.1: W = W0 + B A with
+ *     B in R^{d x r}, A in R^{r x k}; section 6.2: scale s = alpha / r.
+ *   - fedte.cc "QLoRA fine-tuning on 4 GB", section 1: 0.5 byte per parameter
+ *     for the codes, one fp32 scale per 64 parameters before double quantisation.
+ *
+ * Conventions for every entry point:
+ *   - All tensors are DEVICE pointers on the current CUDA device, row-major,
+ *     16-byte aligned, allocated and owned by the caller.  The library never
+ *     allocates or frees device memory.  Workspace sizes are queried with the
+ *     *_workspace_bytes calls; workspaces need 256-byte alignment and may be
+ *     reused between calls that are ordered on the same stream.
+ *   - bfloat16 tensors are passed as uint16_t* (raw bf16 bits).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Calls are asynchronous on that stream and never synchronise the host,
+ *     except qlora_get_status.
+ *   - Argument errors are returned synchronously, before anything is launched.
+ *     Errors found on the device (a bounded wait that expired, a non-finite
+ *     weight) are latched in a per-device status word and returned by
+ *     qlora_get_status.
+ *   - Shapes: W is [n, k] (out x in, as a PyTorch Linear); k % 64 == 0,
+ *     n % 8 == 0; tokens m >= 0 (m == 0 is a no-op); LoRA rank r with
+ *     r % 8 == 0 and 8 <= r <= 128; all of m, n, k < 2^31.
+ */
+#ifndef QLORA_NF4_H_
+#define QLORA_NF4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ----------------------------------------------------------------- return codes */
+#define QLORA_OK 0
+#define QLORA_ERR_INVALID_ARGUMENT 1 /* null / misaligned pointer, bad shape or dtype */
+#define QLORA_ERR_UNSUPPORTED 2      /* not an sm_103 device, or a shape outside the limits above */
+#define QLORA_ERR_CUDA 3             /* a CUDA launch or runtime call failed (see qlora_last_error) */
+#define QLORA_ERR_TIMEOUT 4          /* a kernel's bounded wait expired (device status) */
+#define QLORA_ERR_NONFINITE 5        /* NaN / Inf weight seen by the quantiser (device status) */
+
+/* ----------------------------------------------------------------- dtypes and flags */
+#define QLORA_DTYPE_F32 0
+#define QLORA_DTYPE_BF16 1
+
+#define QLORA_ACCUM_DX 1 /* qlora_linear_bwd: dx += result instead of dx = result */
+#define QLORA_ACCUM_DA 2 /* qlora_linear_bwd: da += result (gradient accumulation) */
+#define QLORA_ACCUM_DB 4 /* qlora_linear_bwd: db += result */
+
+/*
+ * The quantised weight record (device pointers, caller-owned).
+ *   codes        uint8 [n*k/2]  two 4-bit codes per byte; element 2i of the
+ *                               row-major weight in the HIGH nibble of byte i.
+ *   absmax_q     int8  [n*k/64] double-quantised block scale of each block of
+ *                               64 consecutive row-major elements.
+ *   absmax_step  f32   [ceil(n*k/64 / 256)] one step per group of 256 scales.
+ *   absmax_mean  f32   [1]      per-tensor mean of the raw block scales.
+ * Restored scale of block b: a' = (float)absmax_q[b] * absmax_step[b/256] + absmax_mean
+ * (two float32 roundings); restored weight: bf16_rn(L[code] * a').
+ */
+typedef struct qlora_nf4_weight {
+  uint8_t* codes;
+  int8_t* absmax_q;
+  float* absmax_step;
+  float* absmax_mean;
+  int64_t n;
+  int64_t k;
+} qlora_nf4_weight;
+
+/* ----------------------------------------------------------------- quantisation */
+
+/* Bytes of workspace qlora_nf4_quantize needs for an [n, k] weight. */
+int qlora_nf4_quantize_workspace_bytes(int64_t n, int64_t k, size_t* bytes);
+
+/*
+ * NF4-quantise a row-major weight w [n, k] (float32 or bfloat16, w_dtype) into
+ * `out` (whose n and k must equal the arguments).  Glossary "QLoRA", "How QLoRA
+ * works": absmax of every 64 consecutive elements; code = index of the level
+ * nearest to w / absmax (float32 division; ties to the lower index; an
+ * all-zero block gives the zero level); then double quantisation of the
+ * absmax array: mu = float32(RN64(exact sum of scales) / count), per group of
+ * 256 scales step = max|a - mu| / 127 and q = clamp(rint((a - mu)/step), -127, 127)
+ * (q = 0 where step == 0).  A non-finite weight latches QLORA_ERR_NONFINITE
+ * (outputs then undefined).  Bit-exact against the definition.
+ */
+int qlora_nf4_quantize(const void* w, int w_dtype, int64_t n, int64_t k, const qlora_nf4_weight* out,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Dequantise the whole record to bfloat16 out [n, k] (glossary "QLoRA", "How
+ * QLoRA works": restored weight = level * restored scale, in bfloat16).
+ * Bit-exact against the definition in the record comment above.
+ */
+int qlora_nf4_dequantize(const qlora_nf4_weight* w, uint16_t* out, void* stream);
+
+/* ----------------------------------------------------------------- the QLoRA linear */
+
+/* Bytes of workspace qlora_linear_fwd needs for m tokens of an [n, k] weight with rank r. */
+int qlora_linear_fwd_workspace_bytes(int64_t m, int64_t n, int64_t k, int r, size_t* bytes);
+
+/*
+ * Forward: Y = X deq(W)^T + s (X A^T) B^T with s = alpha / r (Day 25 notes,
+ * sections 2.1 and 6.2; glossary "QLoRA", "How QLoRA works").
+ *   x      bf16 [m, k]      input tokens
+ *   lora_a bf16 [r, k]      LoRA A
+ *   lora_b bf16 [n, r]      LoRA B
+ *   y      bf16 [m, n]      output (overwritten)
+ *   t_save f32  [m, r]      X A^T, written for the backward pass
+ * The NF4 codes are decoded straight into tensor-core operands; no bf16 copy
+ * of W is written to memory.  Accumulation is float32; s (X A^T) enters the
+ * product rounded to bfloat16.
+ */
+int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, const uint16_t* lora_a,
+                     const uint16_t* lora_b, int r, float alpha, uint16_t* y, float* t_save, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace qlora_linear_bwd needs. */
+int qlora_linear_bwd_workspace_bytes(int64_t m, int64_t n, int64_t k, int r, size_t* bytes);
+
+/*
+ * Backward of qlora_linear_fwd for upstream gradient dy bf16 [m, n]
+ * (glossary "QLoRA", "How QLoRA works": gradients go through the dequantised
+ * weight, only the LoRA matrices are updated -- there is no dW output):
+ *   U  = dY B
+ *   dx bf16 [m, k] = dY deq(W) + s U A
+ *   da f32  [r, k] = s U^T X
+ *   db f32  [n, r] = s dY^T T        (T = t_save from the forward)
+ * flags: QLORA_ACCUM_DX / QLORA_ACCUM_DA / QLORA_ACCUM_DB add into the outputs.
+ * s U and s T enter the tensor-core products rounded to bfloat16.
+ */
+int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlora_nf4_weight* w,
+                     const uint16_t* lora_a, const uint16_t* lora_b, int r, float alpha, const float* t_save,
+                     uint16_t* dx, float* da, float* db, int flags, void* workspace, size_t workspace_bytes,
+                     void* stream);
+
+/* ----------------------------------------------------------------- MLP glue */
+
+/*
+ * h = silu(g) * u elementwise on `count` bf16 values (count even, float32 math).
+ * Not on the pages: the plain definition of the gate between the gate/up and
+ * down projections of a Llama MLP block.
+ */
+int qlora_silu_mul_fwd(const uint16_t* g, const uint16_t* u, uint16_t* h, int64_t count, void* stream);
+
+/* dg = dh * u * sigma(g) * (1 + g (1 - sigma(g))),  du = dh * silu(g). */
+int qlora_silu_mul_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u, uint16_t* dg, uint16_t* du,
+                       int64_t count, void* stream);
+
+/* ----------------------------------------------------------------- status and diagnostics */
+
+/*
+ * Synchronise `stream`, return and clear the latched device status of the
+ * current device: QLORA_OK, QLORA_ERR_TIMEOUT, QLORA_ERR_NONFINITE, or
+ * QLORA_ERR_CUDA if the synchronisation itself failed.
+ */
+int qlora_get_status(void* stream);
+
+/* Static description of a return code. */
+const char* qlora_strerror(int code);
+
+/* Details of the last error returned on this host thread ("" if none). */
+const char* qlora_last_error(void);
+
+/*
+ * Time limit of every bounded wait inside the kernels, in nanoseconds
+ * (default 2e9).  A kernel whose wait expires latches QLORA_ERR_TIMEOUT,
+ * releases its tensor memory and returns; the context stays usable.
+ */
+int qlora_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Launch one CTA that waits on an mbarrier no one arrives on, with limit
+ * `wait_ns`.  The following qlora_get_status must return QLORA_ERR_TIMEOUT.
+ * Exercises the timeout path without faulting or hanging the GPU.
+ */
+int qlora_selftest_wait_timeout(uint64_t wait_ns, void* stream);
+
+/* Number of multiprocessors the kernels size their grids for (0 if no device). */
+int qlora_device_sm_count(void);
+
+/* ----------------------------------------------------------------- tracing */
+
+/* Total number of kernels the entry points above have launched in this process. */
+unsigned long long qlora_launch_count(void);
+
+/*
+ * While on, every kernel launch made by an entry point is bracketed by two
+ * CUDA events on its stream (a few microseconds of host work per launch).
+ * qlora_profile_collect() waits for the recorded events and adds their
+ * elapsed times into per-launcher totals, read with qlora_profile_name /
+ * _total_ms / _calls for i in [0, qlora_profile_collect()).  Names are the
+ * launchers: "fwd_gemm", "bwd_dx_gemm", "lora_down", "lora_grads", ...
+ */
+int qlora_profile_enable(int on);
+int qlora_profile_collect(void);
+const char* qlora_profile_name(int i);
+double qlora_profile_total_ms(int i);
+long long qlora_profile_calls(int i);
+int qlora_profile_reset(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QLORA_NF4_H_ */

@@ -1,0 +1,143 @@
+"""GPU parity: QLoRA linear forward / backward / decode against the float64 oracle.
+
+The CUDA path (through the C ABI) and the oracle see the same seeded bf16
+inputs; the oracle quantises W itself.  The bar is the relative Frobenius
+error GEMM_TOL for bf16-in / fp32-accumulate outputs and gradients.  Cases
+span several tiles with ragged tails, the small-token decode path (split-K),
+ranks 8 / 16 / 64 / 128, the isolated LoRA path (W = 0) and B = 0.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from oracle import linear, nf4
+from tests._helpers import GEMM_TOL, rel_fro, to_np32, to_np64
+
+pytestmark = pytest.mark.gpu
+
+
+def _deq_oracle(w_cpu):
+    n, k = w_cpu.shape
+    rec = nf4.quantize(to_np32(w_cpu), n, k)
+    return nf4.dequantize(rec["codes"], rec["q"], rec["step"], rec["mu"], n, k)
+
+
+def _run(lib, case, flags=0):
+    w = case.w.cuda()
+    rec = lib.quantize(w)
+    x, a, b, dy = (t.cuda() for t in (case.x, case.a, case.b, case.dy))
+    y, t = lib.linear_fwd(x, rec, a, b, case.alpha)
+    dx, da, db = lib.linear_bwd(dy, x, rec, a, b, case.alpha, t, flags=flags)
+    lib.check_status()
+    return rec, y, t, dx, da, db
+
+
+def _check_all(lib, case, rows=None):
+    rec, y, t, dx, da, db = _run(lib, case)
+    wd = _deq_oracle(case.w)
+    x, a, b, dy = (to_np64(v) for v in (case.x, case.a, case.b, case.dy))
+    r = case.r
+    t_ref = x @ a.T
+    assert rel_fro(to_np64(t), t_ref) < 1e-5
+    dxr, dar, dbr, _ = linear.lora_backward(dy, x, wd, a, b, case.alpha, r, t_ref)
+    assert rel_fro(to_np64(da), dar) < GEMM_TOL
+    assert rel_fro(to_np64(db), dbr) < GEMM_TOL
+    if rows is None:
+        yr, _ = linear.lora_forward(x, wd, a, b, case.alpha, r)
+        assert rel_fro(to_np64(y), yr) < GEMM_TOL
+        assert rel_fro(to_np64(dx), dxr) < GEMM_TOL
+    else:
+        yr, _ = linear.lora_forward_rows(x[rows], wd, a, b, case.alpha, r)
+        assert rel_fro(to_np64(y)[rows], yr) < GEMM_TOL
+        dxr_rows = linear.lora_backward_dx_rows(dy[rows], wd, a, b, case.alpha, r)
+        assert rel_fro(to_np64(dx)[rows], dxr_rows) < GEMM_TOL
+    return y, dx, da, db
+
+
+def test_tiny_case(lib):
+    _check_all(lib, synthetic.tiny_case())
+
+
+@pytest.mark.parametrize("m,n,k,r", [(300, 640, 512, 16), (129, 264, 320, 8), (260, 384, 1024, 64),
+                                     (130, 256, 256, 128), (17, 512, 512, 16), (64, 136, 448, 24)])
+def test_ragged_tiles(lib, m, n, k, r):
+    case = synthetic.linear_case(n, k, m, r, 2.0 * r, base_seed=m + n + k + r)
+    _check_all(lib, case)
+
+
+@pytest.mark.parametrize("m", [1, 4, 16])
+def test_decode_tokens(lib, m):
+    case = synthetic.linear_case(4096, 4096, m, 16, 32.0, base_seed=100 + m)
+    _check_all(lib, case)
+
+
+def test_decode_down_proj_shape(lib):
+    case = synthetic.linear_case(4096, 11008, 4, 16, 32.0, base_seed=7)
+    _check_all(lib, case)
+
+
+def test_attention_projection_sampled_rows(lib):
+    """The 4096^2, 2048-token, r=16 workload: full dA/dB, sampled rows of Y and dX."""
+    case = synthetic.linear_case(4096, 4096, 2048, 16, 32.0, device="cuda", base_seed=0)
+    case = synthetic.LinearCase(*(t.cpu() for t in (case.w, case.x, case.a, case.b, case.dy)), case.alpha, case.r)
+    rows = np.random.default_rng(0).choice(2048, 48, replace=False)
+    rows = np.concatenate([rows, [0, 127, 128, 2047]])
+    _check_all(lib, case, rows=rows)
+
+
+def test_lora_path_alone_with_zero_weight(lib):
+    """W = 0 dequantises to 0, so Y and dX are the LoRA terms alone (large B)."""
+    case = synthetic.linear_case(384, 512, 200, 16, 32.0, base_seed=11)
+    case.w.zero_()
+    case.b.copy_((torch.randn(case.b.shape, generator=torch.Generator().manual_seed(5))).to(torch.bfloat16))
+    y, dx, _, _ = _check_all(lib, case)
+    assert float(y.float().abs().max()) > 0 and float(dx.float().abs().max()) > 0
+
+
+def test_b_zero_is_plain_dequantised_linear(lib):
+    case = synthetic.linear_case(256, 512, 96, 16, 32.0, base_seed=12)
+    case.b.zero_()
+    rec, y, t, dx, da, db = _run(lib, case)
+    wd = lib.dequantize(rec).float()
+    ref = case.x.cuda().float() @ wd.T
+    assert rel_fro(to_np64(y), to_np64(ref)) < GEMM_TOL
+    assert float(da.abs().max()) == 0.0
+
+
+def test_accumulate_flags(lib):
+    case = synthetic.linear_case(256, 256, 64, 16, 32.0, base_seed=13)
+    rec, y, t, dx, da, db = _run(lib, case)
+    x, a, b, dy = (v.cuda() for v in (case.x, case.a, case.b, case.dy))
+    dx2, da2, db2 = dx.clone(), da.clone(), db.clone()
+    lib.linear_bwd(dy, x, rec, a, b, case.alpha, t, dx=dx2, da=da2, db=db2,
+                   flags=lib.ACCUM_DX | lib.ACCUM_DA | lib.ACCUM_DB)
+    lib.check_status()
+    assert rel_fro(to_np64(da2), 2 * to_np64(da)) < 1e-6
+    assert rel_fro(to_np64(db2), 2 * to_np64(db)) < 1e-6
+    assert rel_fro(to_np64(dx2), 2 * to_np64(dx)) < 1e-2
+
+
+def test_zero_tokens(lib):
+    case = synthetic.linear_case(256, 256, 8, 16, 32.0, base_seed=14)
+    rec = lib.quantize(case.w.cuda())
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    a, b = case.a.cuda(), case.b.cuda()
+    y, t = lib.linear_fwd(x, rec, a, b, 32.0)
+    da = torch.full((16, 256), 3.0, device="cuda")
+    db = torch.full((256, 16), 3.0, device="cuda")
+    lib.linear_bwd(torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"), x, rec, a, b, 32.0, t,
+                   dx=torch.empty((0, 256), dtype=torch.bfloat16, device="cuda"), da=da, db=db)
+    lib.check_status()
+    assert y.shape == (0, 256) and float(da.abs().max()) == 0.0 and float(db.abs().max()) == 0.0
+
+
+def test_bad_rank_rejected(lib):
+    case = synthetic.linear_case(256, 256, 8, 16, 32.0, base_seed=15)
+    rec = lib.quantize(case.w.cuda())
+    a = torch.zeros((12, 256), dtype=torch.bfloat16, device="cuda")
+    b = torch.zeros((256, 12), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lib.QloraError) as e:
+        lib.linear_fwd(case.x.cuda(), rec, a, b, 24.0)
+    assert e.value.code == lib.QLORA_ERR_UNSUPPORTED

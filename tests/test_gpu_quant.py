@@ -1,0 +1,122 @@
+"""GPU parity: NF4 quantise / double quant / dequantise, bit-exact against the oracle.
+
+Calls the CUDA path through the C ABI (ctypes binding) on seeded synthetic
+weights and compares every output byte with ``oracle.nf4``.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import synthetic
+from oracle import nf4
+from tests._helpers import to_np32
+
+pytestmark = pytest.mark.gpu
+
+
+def _oracle_record(w_cpu: torch.Tensor):
+    n, k = w_cpu.shape
+    return nf4.quantize(to_np32(w_cpu), n, k)
+
+
+def _assert_record_equal(lib, rec, ref, n, k):
+    assert np.array_equal(rec.codes.cpu().numpy(), ref["codes"]), "4-bit codes differ"
+    assert np.array_equal(rec.absmax_q.cpu().numpy(), ref["q"]), "int8 absmax codes differ"
+    assert np.array_equal(rec.absmax_step.cpu().numpy().view(np.uint32), ref["step"].view(np.uint32)), "steps differ"
+    assert rec.absmax_mean.cpu().numpy().view(np.uint32)[0] == np.float32(ref["mu"]).view(np.uint32), "mean differs"
+    wd = lib.dequantize(rec)
+    lib.check_status()
+    ref_bits = nf4.dequantize_bf16_bits(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
+    got_bits = wd.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got_bits, ref_bits), "dequantised bf16 differs"
+
+
+def test_tiny_case_fp32(lib):
+    case = synthetic.tiny_case()
+    w = case.w.cuda()
+    rec = lib.quantize(w)
+    lib.check_status()
+    _assert_record_equal(lib, rec, _oracle_record(case.w), 256, 256)
+
+
+@pytest.mark.parametrize("n,k", [(8, 64), (24, 192), (136, 640), (512, 4160)])
+def test_ragged_shapes_bf16(lib, n, k):
+    w = synthetic.weight(n, k, device="cuda", seed=n * 7 + k)
+    rec = lib.quantize(w)
+    lib.check_status()
+    _assert_record_equal(lib, rec, _oracle_record(w.cpu()), n, k)
+
+
+def test_attention_projection_4096(lib):
+    w = synthetic.weight(4096, 4096, device="cuda", seed=0)
+    rec = lib.quantize(w)
+    lib.check_status()
+    _assert_record_equal(lib, rec, _oracle_record(w.cpu()), 4096, 4096)
+
+
+def test_encode_boundaries_and_special_blocks(lib):
+    """Blocks of absmax 1 (so x = w exactly) filled with every fp32 value near each
+    decision boundary, exact levels, exact ties, zeros and an all-zero block."""
+    lv = nf4.nf4_levels_f32()
+    vals = []
+    for j in range(15):
+        mid = np.float32((np.float64(lv[j]) + np.float64(lv[j + 1])) / 2)
+        v = mid
+        for _ in range(6):
+            v = np.nextafter(v, np.float32(-2))
+        for _ in range(13):
+            vals.append(v)
+            v = np.nextafter(v, np.float32(2))
+    vals += list(lv) + [lv[6] / 2, lv[8] / 2, np.float32(0), np.float32(-0.0)]
+    vals = np.array(vals, dtype=np.float32)
+    per = 63
+    nb = (vals.size + per - 1) // per
+    w = np.zeros((nb + 1, 64), dtype=np.float32)
+    for b in range(nb):
+        chunk = vals[b * per:(b + 1) * per]
+        w[b, :chunk.size] = chunk
+        w[b, 63] = 1.0
+    # last block stays all zero
+    n = 8 * ((w.size // 64 + 7) // 8)
+    full = np.zeros((n * 64,), dtype=np.float32)
+    full[: w.size] = w.reshape(-1)
+    full = full.reshape(n, 64)
+    rec = lib.quantize(torch.from_numpy(full).cuda())
+    lib.check_status()
+    _assert_record_equal(lib, rec, nf4.quantize(full, n, 64), n, 64)
+
+
+def test_nonfinite_is_reported(lib):
+    w = synthetic.weight(16, 128, device="cuda", seed=3)
+    w[5, 17] = float("nan")
+    lib.quantize(w)
+    assert lib.get_status() == lib.QLORA_ERR_NONFINITE
+    assert lib.get_status() == lib.QLORA_OK  # cleared
+    w2 = synthetic.weight(16, 128, device="cuda", seed=4)
+    rec = lib.quantize(w2)
+    lib.check_status()
+    _assert_record_equal(lib, rec, _oracle_record(w2.cpu()), 16, 128)
+
+
+def test_invalid_arguments_are_rejected(lib):
+    w = synthetic.weight(16, 96, device="cuda", seed=5)  # k not a multiple of 64
+    with pytest.raises(lib.QloraError) as e:
+        lib.quantize(w)
+    assert e.value.code in (lib.QLORA_ERR_INVALID_ARGUMENT, lib.QLORA_ERR_UNSUPPORTED)
+    w = synthetic.weight(16, 128, device="cuda", seed=5)
+    rec = lib.NF4Weight.empty(16, 128)
+    bad = torch.empty(16 * 128 + 8, dtype=torch.bfloat16, device="cuda")[1:].view(-1)[: 16 * 128].view(16, 128)
+    with pytest.raises(lib.QloraError) as e:
+        lib.quantize(bad, rec)
+    assert e.value.code == lib.QLORA_ERR_INVALID_ARGUMENT
+    lib.check_status()
+
+
+def test_bounded_wait_timeout_keeps_context(lib):
+    lib.selftest_wait_timeout(20_000_000)  # 20 ms on a barrier nothing arrives on
+    assert lib.get_status() == lib.QLORA_ERR_TIMEOUT
+    w = synthetic.weight(8, 64, device="cuda", seed=6)
+    rec = lib.quantize(w)
+    lib.check_status()
+    _assert_record_equal(lib, rec, _oracle_record(w.cpu()), 8, 64)
