@@ -34,6 +34,7 @@ from ._binding import (  # noqa: F401
     profile_read,
     profile_reset,
     quantize,
+    quantize_noalloc,
     quantize_workspace_bytes,
     selftest_wait_timeout,
     set_wait_limit_ns,

@@ -34,6 +34,7 @@ ACCUM_DB = 4
 EXPORTS = (
     "qlora_nf4_quantize_workspace_bytes",
     "qlora_nf4_quantize",
+    "qlora_nf4_quantize_noalloc",
     "qlora_nf4_dequantize",
     "qlora_linear_fwd_workspace_bytes",
     "qlora_linear_fwd",
@@ -96,6 +97,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     sig = {
         "qlora_nf4_quantize_workspace_bytes": (c_int, [_I64, _I64, _PSZ]),
         "qlora_nf4_quantize": (c_int, [_P, c_int, _I64, _I64, _PW, _P, _SZ, _P]),
+        "qlora_nf4_quantize_noalloc": (c_int, [_P, c_int, _I64, _I64, _PW, _P]),
         "qlora_nf4_dequantize": (c_int, [_PW, _P, _P]),
         "qlora_linear_fwd_workspace_bytes": (c_int, [_I64, _I64, _I64, c_int, _PSZ]),
         "qlora_linear_fwd": (c_int, [_P, _I64, _PW, _P, _P, c_int, c_float, _P, _P, _P, _SZ, _P]),
@@ -204,6 +206,21 @@ def quantize(w: torch.Tensor, out: NF4Weight | None = None, workspace=None, stre
     ws, wsb = _ws(quantize_workspace_bytes(n, k), w.device, workspace)
     rec = out.c_struct()
     _check(lib.qlora_nf4_quantize(_ptr(w), dtype, n, k, ctypes.byref(rec), _ptr(ws), wsb, _stream(stream)))
+    return out
+
+
+def quantize_noalloc(w: torch.Tensor, out: NF4Weight | None = None, stream=None) -> NF4Weight:
+    """qlora_nf4_quantize_noalloc: same result as quantize(), scratch from the library's fixed
+    device array instead of a workspace (n*k <= 2^26; calls must not overlap on the GPU)."""
+    lib = load()
+    n, k = w.shape
+    if out is None:
+        out = NF4Weight.empty(n, k, w.device)
+    dtype = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}.get(w.dtype)
+    if dtype is None:
+        raise ValueError("weight must be float32 or bfloat16")
+    rec = out.c_struct()
+    _check(lib.qlora_nf4_quantize_noalloc(_ptr(w), dtype, n, k, ctypes.byref(rec), _stream(stream)))
     return out
 
 

@@ -226,6 +226,31 @@ int qlora_nf4_quantize(const void* w, int w_dtype, int64_t n, int64_t k, const q
                   "quantize");
 }
 
+int qlora_nf4_quantize_noalloc(const void* w, int w_dtype, int64_t n, int64_t k, const qlora_nf4_weight* out,
+                               void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if ((rc = check_weight(out))) return rc;
+  if (out->n != n || out->k != k) return fail(QLORA_ERR_INVALID_ARGUMENT, "record shape differs from the weight shape");
+  if ((rc = check_ptr(w, "w"))) return rc;
+  if (w_dtype != QLORA_DTYPE_F32 && w_dtype != QLORA_DTYPE_BF16) return fail(QLORA_ERR_INVALID_ARGUMENT, "w_dtype %d", w_dtype);
+  if (n * k > qlora::noalloc_max_weights())
+    return fail(QLORA_ERR_UNSUPPORTED,
+                "n*k = %lld weights exceeds the fixed scratch of the no-allocation quantiser (%lld weights); "
+                "use qlora_nf4_quantize with a caller workspace",
+                (long long)(n * k), (long long)qlora::noalloc_max_weights());
+  float* absmax = nullptr;
+  void* bins = nullptr;
+  cudaError_t e = qlora::noalloc_scratch(&absmax, &bins);
+  if (e != cudaSuccess) return cuda_ret(e, "no-allocation scratch address");
+  Span sp(P_QUANTIZE, static_cast<cudaStream_t>(stream), 3);
+  return cuda_ret(qlora::launch_nf4_quantize(w, w_dtype == QLORA_DTYPE_F32 ? 0 : 1, n * k, out->codes, absmax,
+                                             out->absmax_q, out->absmax_step, out->absmax_mean, bins, di->status,
+                                             di->num_sms, static_cast<cudaStream_t>(stream)),
+                  "quantize (no allocation)");
+}
+
 int qlora_nf4_dequantize(const qlora_nf4_weight* w, uint16_t* out, void* stream) {
   DevInfo* di = nullptr;
   int rc = device(&di);

@@ -15,6 +15,8 @@
 // Bit-exactness: every float32 operation that decides a code or a dequantised
 // value is an explicitly rounded intrinsic (__fdiv_rn / __fsub_rn / __fmul_rn /
 // __fadd_rn / rintf / bf16 round-to-nearest), so no FMA contraction changes it.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -279,6 +281,43 @@ __global__ void __launch_bounds__(256) k_nf4_dequantize(const uint8_t* __restric
     }
     __syncwarp();
   }
+}
+
+// ------------------------------------------------------------------ fixed scratch (no-allocation entry point)
+// Scratch of qlora_nf4_quantize_noalloc: the float32 absmax of up to
+// kNoAllocMaxBlocks blocks of 64 weights, then the 256 exact-sum bins and the
+// CTA counter of the mean.  It is module-scope device memory: every device
+// that loads the library holds one copy until the process exits.  All calls
+// on a device share it; the bins and the counter are cleared by every call,
+// the absmax region is fully rewritten, so nothing carries over -- but two
+// calls whose kernels overlap on the GPU race on it.
+constexpr int64_t kNoAllocMaxBlocks = int64_t(1) << 20;  // n*k <= 2^26 weights
+constexpr size_t kNoAllocBinsOffset = static_cast<size_t>(kNoAllocMaxBlocks) * 4;
+constexpr size_t kNoAllocBytes = kNoAllocBinsOffset + 256 * 8 + 256;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+int64_t noalloc_max_weights() { return kNoAllocMaxBlocks * 64; }
+
+// Device address of the scratch on the current device.  The first call on a
+// device looks it up with cudaGetSymbolAddress (the host-side name of a
+// __device__ array is not a device address) and caches it per device.
+cudaError_t noalloc_scratch(float** absmax, void** bins) {
+  static std::mutex mu;
+  static void* addr[128] = {};
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  if (d < 0 || d >= 128) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[d]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[d] = p;
+  }
+  *absmax = static_cast<float*>(addr[d]);
+  *bins = static_cast<char*>(addr[d]) + kNoAllocBinsOffset;
+  return cudaSuccess;
 }
 
 // ------------------------------------------------------------------ launchers

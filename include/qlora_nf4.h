@@ -99,6 +99,30 @@ int qlora_nf4_quantize(const void* w, int w_dtype, int64_t n, int64_t k, const q
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * qlora_nf4_quantize without a workspace argument, for callers that cannot
+ * allocate device memory on the call path: plugins hosted by a framework that
+ * owns all device memory through its own pool and forbids cudaMalloc/cudaFree
+ * outside it, services with a memory budget fixed at start-up, and
+ * latency-critical code where a cudaMalloc or cudaFree (which can synchronise
+ * the device) is not acceptable.  The pages have no counterpart of this call;
+ * it computes exactly what qlora_nf4_quantize computes (same kernels, same
+ * bits), with the scratch taken from a fixed module-scope device array.
+ *   - Limit: n * k <= 2^26 weights (1,048,576 absmax blocks; 4 MiB + 2.3 KiB of
+ *     scratch, held by every device that loads the library until exit).
+ *     Larger weights return QLORA_ERR_UNSUPPORTED before anything is launched.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the scratch address for that device
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make the
+ *     first call on each device before any stream capture.
+ *   - All calls on a device share the scratch.  Each call clears the parts
+ *     that must start at zero and overwrites the rest, but calls whose kernels
+ *     overlap on the GPU (different streams without ordering) race on it:
+ *     order them on one stream.
+ */
+int qlora_nf4_quantize_noalloc(const void* w, int w_dtype, int64_t n, int64_t k, const qlora_nf4_weight* out,
+                               void* stream);
+
+/*
  * Dequantise the whole record to bfloat16 out [n, k] (glossary "QLoRA", "How
  * QLoRA works": restored weight = level * restored scale, in bfloat16).
  * Bit-exact against the definition in the record comment above.
