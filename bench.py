@@ -298,6 +298,111 @@ def dequant_quant_rates(q, torch, rec, w, flush):
                          "kernels": 3}}
 
 
+def mlp_block(q, torch, steps, flush, hidden=4096, inter=11008, m=2048, r=16, alpha=32.0):
+    """Llama-7B MLP block fwd+bwd: gate/up [inter, hidden], down [hidden, inter], SiLU*up between."""
+    import synthetic
+    dev = "cuda"
+    recs = [q.quantize(synthetic.weight(n, k, device=dev, seed=s)) for (n, k, s) in
+            ((inter, hidden, 11), (inter, hidden, 12), (hidden, inter, 13))]
+    loras = [synthetic.lora_pair(inter, hidden, r, device=dev, seed=21), synthetic.lora_pair(inter, hidden, r, device=dev, seed=23),
+             synthetic.lora_pair(hidden, inter, r, device=dev, seed=25)]
+    x = synthetic.activations(m, hidden, device=dev, seed=31)
+    dy = synthetic.activations(m, hidden, device=dev, seed=32)
+    bf = lambda *sh: torch.empty(sh, dtype=torch.bfloat16, device=dev)  # noqa: E731
+    g, u, h, yv, dh, dg, du, dx = bf(m, inter), bf(m, inter), bf(m, inter), bf(m, hidden), bf(m, inter), bf(m, inter), \
+        bf(m, inter), bf(m, hidden)
+    ts = [torch.empty((m, r), dtype=torch.float32, device=dev) for _ in range(3)]
+    das = [torch.empty((r, rec.k), dtype=torch.float32, device=dev) for rec in recs]
+    dbs = [torch.empty((rec.n, r), dtype=torch.float32, device=dev) for rec in recs]
+    wsf = torch.empty(max(q.fwd_workspace_bytes(m, rec.n, rec.k, r) for rec in recs) + 256, dtype=torch.uint8, device=dev)
+    wsb = torch.empty(max(q.bwd_workspace_bytes(m, rec.n, rec.k, r) for rec in recs) + 256, dtype=torch.uint8, device=dev)
+
+    def fwd_bwd():
+        q.linear_fwd(x, recs[0], *loras[0], alpha, y=g, t_save=ts[0], workspace=wsf)
+        q.linear_fwd(x, recs[1], *loras[1], alpha, y=u, t_save=ts[1], workspace=wsf)
+        q.silu_mul_fwd(g, u, h)
+        q.linear_fwd(h, recs[2], *loras[2], alpha, y=yv, t_save=ts[2], workspace=wsf)
+        q.linear_bwd(dy, h, recs[2], *loras[2], alpha, ts[2], dx=dh, da=das[2], db=dbs[2], workspace=wsb)
+        q.silu_mul_bwd(dh, g, u, dg, du)
+        q.linear_bwd(dg, x, recs[0], *loras[0], alpha, ts[0], dx=dx, da=das[0], db=dbs[0], workspace=wsb)
+        q.linear_bwd(du, x, recs[1], *loras[1], alpha, ts[1], dx=dx, da=das[1], db=dbs[1], workspace=wsb,
+                     flags=q.ACCUM_DX)
+
+    fwd_bwd()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fwd_bwd()
+    for _ in range(3):
+        flush()
+        graph.replay()
+    ms = statistics.median(time_events(torch, graph.replay, steps, flush))
+    q.check_status()
+    flops = step_flops(m, inter, hidden, r) * 3
+    return {"workload": "Llama-7B MLP block: gate/up 11008x4096, down 4096x11008, 2048 tokens, r=16, SiLU*up",
+            "ms_per_step": ms, "tflops": flops / (ms / 1e3) / 1e12, "flops_per_step": flops}
+
+
+def llama65b(q, torch, steps, flush, layers=80, m=4096, r=64, alpha=16.0):
+    """Stream-quantise 80 Llama-65B-shaped layers (bf16 N(0, 0.02^2) made one matrix at a time), then
+    fwd+bwd of one 22016x8192 up-projection at 4096 tokens, r=64."""
+    import synthetic
+    recs = []
+    qms = 0.0
+    params = 0
+    gen_ms = 0.0
+    for layer in range(layers):
+        for mi, (n, k) in enumerate(synthetic.LLAMA65B_LAYER):
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record()
+            w = synthetic.weight(n, k, device="cuda", seed=synthetic.stack_seed(layer, mi))
+            e1.record()
+            recs.append(q.quantize(w))
+            e2.record()
+            e2.synchronize()
+            gen_ms += e0.elapsed_time(e1)
+            qms += e1.elapsed_time(e2)
+            params += n * k
+            del w
+    q.check_status()
+    resident = sum(rc.nbytes() for rc in recs)
+    qbytes = 2 * params + resident
+    up = recs[4]  # layer 0 up-projection, 22016 x 8192
+    a, b = synthetic.lora_pair(up.n, up.k, r, device="cuda", seed=77)
+    x = synthetic.activations(m, up.k, device="cuda", seed=78)
+    dy = synthetic.activations(m, up.n, device="cuda", seed=79)
+    y = torch.empty((m, up.n), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((m, up.k), dtype=torch.bfloat16, device="cuda")
+    t = torch.empty((m, r), dtype=torch.float32, device="cuda")
+    da = torch.empty((r, up.k), dtype=torch.float32, device="cuda")
+    db = torch.empty((up.n, r), dtype=torch.float32, device="cuda")
+    wsf = torch.empty(q.fwd_workspace_bytes(m, up.n, up.k, r) + 256, dtype=torch.uint8, device="cuda")
+    wsb = torch.empty(q.bwd_workspace_bytes(m, up.n, up.k, r) + 256, dtype=torch.uint8, device="cuda")
+
+    def fwd_bwd():
+        q.linear_fwd(x, up, a, b, alpha, y=y, t_save=t, workspace=wsf)
+        q.linear_bwd(dy, x, up, a, b, alpha, t, dx=dx, da=da, db=db, workspace=wsb)
+
+    fwd_bwd()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fwd_bwd()
+    for _ in range(3):
+        flush()
+        graph.replay()
+    ms = statistics.median(time_events(torch, graph.replay, steps, flush))
+    q.check_status()
+    flops = step_flops(m, up.n, up.k, r)
+    out = {"layers": layers, "matrices": len(recs), "params": params, "resident_gb": resident / 1e9,
+           "quantize_ms": qms, "quantize_gbs": qbytes / qms / 1e6, "weight_generation_ms_not_counted": gen_ms,
+           "upproj_fwd_bwd": {"n": up.n, "k": up.k, "m": m, "r": r, "alpha": alpha, "ms_per_step": ms,
+                              "tflops": flops / (ms / 1e3) / 1e12, "flops_per_step": flops}}
+    del recs, up, x, dy, y, dx
+    torch.cuda.empty_cache()
+    return out
+
+
 def traffic_for(kernel: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it matches the current source."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -341,16 +446,37 @@ def run_ours(args, world, rank, local):
 
     def allreduce_grads():
         if world > 1:
-            import torch.distributed as dist
-            dist.all_reduce(da)
-            dist.all_reduce(db)
+            from bit_quantized_fine_nf4_b300.dp import allreduce_lora_grads
+            allreduce_lora_grads(da, db)
 
-    def step():
+    def fwd_bwd():
         q.linear_fwd(x, rec, a, b, ALPHA_, y=y, t_save=t_save, workspace=ws_f)
         q.linear_bwd(dy, x, rec, a, b, ALPHA_, t_save, dx=dx, da=da, db=db, workspace=ws_b)
+
+    def eager_step():
+        fwd_bwd()
         allreduce_grads()
 
     flops = step_flops(M_, N_, K_, R_)
+    for _ in range(args.warmup):
+        flush()
+        eager_step()
+    torch.cuda.synchronize()
+    q.check_status()
+
+    # One fwd+bwd captured in a CUDA graph: the same library calls, replayed
+    # without per-call host work.  The dA/dB all-reduce (N > 1) stays eager.
+    l0 = q.launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fwd_bwd()
+    kernels_per_step = q.launch_count() - l0
+
+    def graph_step():
+        graph.replay()
+        allreduce_grads()
+
+    step = graph_step if not args.eager else eager_step
     for _ in range(args.warmup):
         flush()
         step()
@@ -364,17 +490,27 @@ def run_ours(args, world, rank, local):
     clocks.start()
     l0 = q.launch_count()
     ms = time_events(torch, step, args.steps, flush)
-    launches = q.launch_count() - l0
+    launches = (q.launch_count() - l0) if args.eager else kernels_per_step * args.steps
     barrier(world)
     clk = clocks.stop()
     q.check_status()
     ms_step = allreduce_max(sum(ms) / len(ms), world)
     value = flops * world / (ms_step / 1e3) / 1e12
 
+    # eager calls (host launch work in the loop), for reference
+    eager_ms = time_events(torch, eager_step, args.steps, flush)
+    eager_ms_step = allreduce_max(sum(eager_ms) / len(eager_ms), world)
+
     # -------------------------------------------------------------- roofline of the dominant kernel
+    # eager launches, each bracketed by events; a GPU sleep before each step lets
+    # the host queue the whole step first so no submission latency lands inside.
+    def padded_flush():
+        flush()
+        torch.cuda._sleep(2_000_000)
+
     q.profile_reset()
     q.profile_enable(True)
-    time_events(torch, step, args.steps, flush)
+    time_events(torch, eager_step, args.steps, padded_flush)
     q.profile_enable(False)
     prof = q.profile_read()
     q.check_status()
@@ -422,7 +558,10 @@ def run_ours(args, world, rank, local):
            "ms_per_step": e2e_step_ms}
 
     # -------------------------------------------------------------- secondary figures
-    secondary = {"kernel_shares": shares}
+    secondary = {"kernel_shares": shares,
+                 "eager_calls": {"ms_per_step": eager_ms_step,
+                                 "tflops": flops * world / (eager_ms_step / 1e3) / 1e12},
+                 "kernels_per_step": kernels_per_step}
     if not args.quick:
         secondary.update(dequant_quant_rates(q, torch, rec, case.w, flush))
         del y, dx
@@ -434,12 +573,20 @@ def run_ours(args, world, rank, local):
         secondary["decode_sweep"] = sweep
         secondary["dequant"]["frac_of_hbm"] = secondary["dequant"]["gbs"] / peaks["hbm_gbs"]
         secondary["quantize"]["frac_of_hbm"] = secondary["quantize"]["gbs"] / peaks["hbm_gbs"]
+    if args.full:
+        secondary["mlp_block"] = mlp_block(q, torch, args.steps, flush)
+        secondary["mlp_block"]["frac_of_bf16_peak"] = secondary["mlp_block"]["tflops"] / peaks["bf16_tflops"]
+        secondary["llama65b"] = llama65b(q, torch, max(3, args.steps // 4), flush)
+        secondary["llama65b"]["upproj_fwd_bwd"]["frac_of_bf16_peak"] = (
+            secondary["llama65b"]["upproj_fwd_bwd"]["tflops"] / peaks["bf16_tflops"])
 
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD, "n": N_, "k": K_, "m": M_, "r": R_, "alpha": ALPHA_,
                        "weights": "nf4 + double-quant (block 64, dq group 256)",
+                       "launch": "eager library calls" if args.eager else
+                                 "library calls captured once in a CUDA graph, replayed per step",
                        "l2": "flushed between steps (256 MB write outside the timed events)",
                        "parallelism": "dp%d (replica per GPU, all-reduce of dA/dB)" % world},
             "roofline": roof, "e2e": e2e, "gpu_launches": launches, "clocks": clk,
@@ -457,6 +604,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no decode sweep / dequant rates)")
+    ap.add_argument("--eager", action="store_true", help="time eager library calls instead of the graph replay")
+    ap.add_argument("--full", action="store_true", help="also the MLP block and the 65B-shaped stream + up-proj")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=128)

@@ -111,20 +111,19 @@ FwdWs fwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 }
 
 struct BwdWs {
-  size_t bt, su, st, ld, total;
+  size_t su, st, ld, lg, total;
 };
 BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
-  (void)k;
   BwdWs w;
   if (m <= 0) {
-    w.bt = w.su = w.st = w.ld = w.total = 0;
+    w.su = w.st = w.ld = w.lg = w.total = 0;
     return w;
   }
-  w.bt = align256(static_cast<size_t>(n) * r * 2);
   w.su = align256(static_cast<size_t>(m) * r * 2);
   w.st = w.su;
   w.ld = align256(qlora::lora_down_workspace_bytes(static_cast<int>(m), static_cast<int>(n), r, sms));
-  w.total = w.bt + w.su + w.st + w.ld;
+  w.lg = align256(qlora::lora_grads_workspace_bytes(static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), r, sms));
+  w.total = w.su + w.st + w.ld + w.lg;
   return w;
 }
 
@@ -132,12 +131,12 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 // Every launcher call made by the entry points is counted (kernels launched),
 // and, while profiling is on, bracketed by two CUDA events on its stream.
 enum ProfName : int {
-  P_QUANTIZE = 0, P_DEQUANTIZE, P_LORA_DOWN, P_FWD_GEMM, P_TRANSPOSE, P_SCALE, P_BWD_GEMM, P_LORA_GRADS,
-  P_SILU_FWD, P_SILU_BWD, P_SELFTEST, P_COUNT
+  P_QUANTIZE = 0, P_DEQUANTIZE, P_LORA_DOWN, P_FWD_GEMM, P_BWD_GEMM, P_LORA_GRADS, P_SILU_FWD, P_SILU_BWD,
+  P_SELFTEST, P_COUNT
 };
 const char* const kProfNames[P_COUNT] = {"nf4_quantize(3 kernels)", "nf4_dequantize", "lora_down", "fwd_gemm",
-                                         "transpose_b", "scale_t", "bwd_dx_gemm", "lora_grads", "silu_mul_fwd",
-                                         "silu_mul_bwd", "wait_selftest"};
+                                         "bwd_dx_gemm", "lora_grads", "silu_mul_fwd", "silu_mul_bwd",
+                                         "wait_selftest"};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<bool> g_prof_on{false};
 struct ProfRec {
@@ -298,8 +297,8 @@ int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, co
   {
     Span sp(P_LORA_DOWN, s, 1);
     e = qlora::launch_lora_down(reinterpret_cast<const __nv_bfloat16*>(x),
-                                          reinterpret_cast<const __nv_bfloat16*>(lora_a), M, K, r, scale, t_save, st,
-                                          base + ws.st, di->num_sms, s);
+                                reinterpret_cast<const __nv_bfloat16*>(lora_a), 1, M, K, r, scale, t_save, st,
+                                base + ws.st, di->num_sms, s);
   }
   if (e != cudaSuccess) return cuda_ret(e, "lora_down");
   {
@@ -349,10 +348,10 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
   if ((rc = check_ptr(workspace, "workspace"))) return rc;
   if (workspace_bytes < ws.total) return fail(QLORA_ERR_INVALID_ARGUMENT, "workspace %zu < %zu bytes", workspace_bytes, ws.total);
   char* base = static_cast<char*>(workspace);
-  __nv_bfloat16* bt = reinterpret_cast<__nv_bfloat16*>(base);
-  __nv_bfloat16* su = reinterpret_cast<__nv_bfloat16*>(base + ws.bt);
-  __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(base + ws.bt + ws.su);
-  void* ldws = base + ws.bt + ws.su + ws.st;
+  __nv_bfloat16* su = reinterpret_cast<__nv_bfloat16*>(base);
+  __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(base + ws.su);
+  void* ldws = base + ws.su + ws.st;
+  void* lgws = base + ws.su + ws.st + ws.ld;
   const float scale = alpha / static_cast<float>(r);
   const int M = static_cast<int>(m), N = static_cast<int>(w->n), K = static_cast<int>(w->k);
   const uint64_t wait = g_wait_ns.load();
@@ -360,20 +359,12 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
   cudaError_t e;
   {
-    Span sp(P_TRANSPOSE, s, 1);
-    e = qlora::launch_transpose_bf16(reinterpret_cast<const __nv_bfloat16*>(lora_b), bt, N, r, s);
-  }
-  if (e != cudaSuccess) return cuda_ret(e, "transpose B");
-  {
+    // U = dY B (B read as stored) and, in the same launch, sT = bf16(s * t_save)
     Span sp(P_LORA_DOWN, s, 1);
-    e = qlora::launch_lora_down(dyb, bt, M, N, r, scale, nullptr, su, ldws, di->num_sms, s);
+    e = qlora::launch_lora_down(dyb, reinterpret_cast<const __nv_bfloat16*>(lora_b), 0, M, N, r, scale, nullptr, su,
+                                ldws, di->num_sms, s, t_save, st, static_cast<int64_t>(M) * r, scale);
   }
   if (e != cudaSuccess) return cuda_ret(e, "lora_down (U)");
-  {
-    Span sp(P_SCALE, s, 1);
-    e = qlora::launch_scale_to_bf16(t_save, st, static_cast<int64_t>(M) * r, scale, di->num_sms, s);
-  }
-  if (e != cudaSuccess) return cuda_ret(e, "scale T");
   {
     Span sp(P_BWD_GEMM, s, 1);
     e = qlora::launch_bwd_dx_gemm(dyb, M, to_dev(w), su, reinterpret_cast<const __nv_bfloat16*>(lora_a), r,
@@ -384,7 +375,7 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
   {
     Span sp(P_LORA_GRADS, s, 1);
     e = qlora::launch_lora_grads(xb, dyb, su, st, M, N, K, r, da, db, (flags & QLORA_ACCUM_DA) ? 1 : 0,
-                                 (flags & QLORA_ACCUM_DB) ? 1 : 0, di->status, wait, s);
+                                 (flags & QLORA_ACCUM_DB) ? 1 : 0, lgws, di->status, wait, di->num_sms, s);
   }
   return cuda_ret(e, "lora grads");
 }

@@ -13,6 +13,10 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 #include "kernels.h"
 
 namespace qlora {
@@ -303,6 +307,34 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
 __device__ __forceinline__ void sts_v4(uint32_t saddr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
+}
+
+// Host: raise a kernel's dynamic shared-memory limit once per (kernel, device)
+// (the attribute call is host work; repeating it on every launch costs
+// microseconds).  Keyed by the kernel's address: template instances of one
+// kernel share a function type but not an address.
+inline bool smem_limit_done(const void* kernel, int device, bool mark) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lk(mu);
+  const auto key = std::make_pair(kernel, device);
+  if (mark) {
+    done.insert(key);
+    return true;
+  }
+  return done.count(key) != 0;
+}
+
+template <typename Kernel>
+inline cudaError_t set_smem_limit_once(Kernel* kernel, size_t bytes) {
+  int d = 0;
+  cudaError_t e = cudaGetDevice(&d);
+  if (e != cudaSuccess) return e;
+  const void* key = reinterpret_cast<const void*>(kernel);
+  if (smem_limit_done(key, d, false)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess) smem_limit_done(key, d, true);
+  return e;
 }
 
 }  // namespace qlora

@@ -29,11 +29,12 @@ cudaError_t launch_nf4_dequantize(const uint8_t* codes, const int8_t* absq, cons
 // lora_small.cu
 int lora_down_splits(int M, int K, int num_sms);
 size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms);
-cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int M, int K, int r, float scale,
-                             float* out_f32, __nv_bfloat16* out_bf16, void* ws, int num_sms, cudaStream_t s);
-cudaError_t launch_transpose_bf16(const __nv_bfloat16* src, __nv_bfloat16* dst, int rows, int cols, cudaStream_t s);
-cudaError_t launch_scale_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, float scale, int num_sms,
-                                 cudaStream_t s);
+// out = in . mt^T with mt either [r, K] (mt_kmajor) or [K, r]; optional side job
+// cvt_dst[i] = bf16(cvt_scale * cvt_src[i]) for i < cvt_n in the same launch.
+cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int mt_kmajor, int M, int K, int r,
+                             float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int num_sms,
+                             cudaStream_t s, const float* cvt_src = nullptr, __nv_bfloat16* cvt_dst = nullptr,
+                             int64_t cvt_n = 0, float cvt_scale = 1.0f);
 cudaError_t launch_silu_mul_fwd(const uint16_t* g, const uint16_t* u, uint16_t* h, int64_t n, int num_sms,
                                 cudaStream_t s);
 cudaError_t launch_silu_mul_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u, uint16_t* dg, uint16_t* du,
@@ -60,9 +61,11 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
                                unsigned* status, uint64_t wait_ns, cudaStream_t s);
 
 // LoRA gradients: dA[r, K] (+)= sU^T X   and   dB[N, r] (+)= dY^T sT
+size_t lora_grads_workspace_bytes(int M, int N, int K, int r, int num_sms);
 cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __nv_bfloat16* su,
                               const __nv_bfloat16* st, int M, int N, int K, int r, float* da, float* db,
-                              int accum_da, int accum_db, unsigned* status, uint64_t wait_ns, cudaStream_t s);
+                              int accum_da, int accum_db, void* ws, unsigned* status, uint64_t wait_ns, int num_sms,
+                              cudaStream_t s);
 
 // Bounded-wait self test: one CTA waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t wait_ns, cudaStream_t s);

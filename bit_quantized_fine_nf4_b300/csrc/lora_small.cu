@@ -4,9 +4,9 @@
 // frozen linear is B (A x) with A in R^{r x k}, B in R^{d x r}; section 6.2:
 // it is scaled by s = alpha / r.
 //
-// k_lora_down:   out[m, j] = sum_k in[m, k] * mt[j, k]   (in [M, K], mt [r, K], bf16, K % 8 == 0)
-//   forward:  T = X A^T   (mt = A)
-//   backward: U = dY B    (mt = B^T, made by k_transpose_bf16)
+// k_lora_down:   out[m, j] = sum_k in[m, k] * mt(j, k)   (in [M, K] bf16, K % 8 == 0)
+//   forward:  T = X A^T   (mt = A, [r, K])
+//   backward: U = dY B    (mt = B as stored, [N, r])
 // The contraction is HBM-bound (one read of `in`, r <= 128 outputs per row),
 // so it runs on the warp-level mma.sync path with 16-byte loads; the K range
 // is split over the 8 warps of a CTA and over CTAs, and the partial sums are
@@ -29,19 +29,42 @@ __device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, ui
 }
 
 // CTA = 8 warps, 16 rows of `in`.  Warp w handles 32-wide k chunks c with
-// c % (8 * splits) == 8 * blockIdx.y + w.  Within a chunk, thread (g, q) =
-// (lane / 4, lane % 4) loads 8 consecutive k (16 bytes) of rows g and g + 8,
-// and the k order inside the two m16n8k16 steps is permuted consistently for
-// both operands so each fragment register is one aligned 32-bit word.
-template <int NT>  // number of 8-wide output column tiles (r_pad = 8 * NT)
+// c % (8 * splits) == 8 * blockIdx.y + w, two chunks per loop trip so their
+// loads are in flight together.  Within a chunk, thread (g, q) = (lane / 4,
+// lane % 4) loads 8 consecutive k (16 bytes) of rows g and g + 8, and the k
+// order inside the two m16n8k16 steps is permuted consistently for both
+// operands so each fragment register holds 2 consecutive k.
+// MT_KMAJOR: mt is [r, K] (row j contiguous in k); otherwise mt is [K, r]
+// (the LoRA B matrix as stored) and each fragment gathers 8 strided values.
+// Side job (optional): every thread first converts a slice of cvt_src (f32)
+// to bf16(cvt_scale * v) in cvt_dst -- an independent elementwise pass that
+// rides along in the same launch.
+template <int NT, bool MT_KMAJOR>
+__device__ __forceinline__ uint4 load_mt_frag(const __nv_bfloat16* __restrict__ mt, int j, int kb, int K, int r) {
+  if (MT_KMAJOR) return ldg_nc_v4(mt + static_cast<int64_t>(j) * K + kb);
+  const unsigned short* p = reinterpret_cast<const unsigned short*>(mt) + static_cast<int64_t>(kb) * r + j;
+  uint32_t v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __ldg(p + static_cast<int64_t>(i) * r);
+  return make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
+}
+
+template <int NT, bool MT_KMAJOR>
 __global__ void __launch_bounds__(256) k_lora_down(const __nv_bfloat16* __restrict__ in,
                                                    const __nv_bfloat16* __restrict__ mt, int M, int K, int r,
                                                    int splits, float* __restrict__ partial,
                                                    unsigned* __restrict__ counters, float scale,
-                                                   float* __restrict__ out_f32, __nv_bfloat16* __restrict__ out_bf16) {
+                                                   float* __restrict__ out_f32, __nv_bfloat16* __restrict__ out_bf16,
+                                                   const float* __restrict__ cvt_src, __nv_bfloat16* __restrict__ cvt_dst,
+                                                   int64_t cvt_n, float cvt_scale) {
   constexpr int RP = NT * 8;
   extern __shared__ float s_red[];  // [8 warps][16 rows][RP]
   __shared__ int s_last;
+  if (cvt_n > 0) {
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * gridDim.y * blockDim.x;
+    const int64_t tid = (static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t i = tid; i < cvt_n; i += nthreads) cvt_dst[i] = __float2bfloat16_rn(__fmul_rn(cvt_src[i], cvt_scale));
+  }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
   const int m0 = blockIdx.x * 16;
@@ -54,17 +77,29 @@ __global__ void __launch_bounds__(256) k_lora_down(const __nv_bfloat16* __restri
   const int n_chunks = (K + 31) / 32;
   const int stride = 8 * splits;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  for (int c = 8 * blockIdx.y + warp; c < n_chunks; c += stride) {
-    const int kb = c * 32 + q * 8;
-    const bool kin = kb < K;
-    const uint4 xa = (kin && rowa < M) ? ldg_nc_v4(in + static_cast<int64_t>(rowa) * K + kb) : zero;
-    const uint4 xb = (kin && rowb < M) ? ldg_nc_v4(in + static_cast<int64_t>(rowb) * K + kb) : zero;
+  const __nv_bfloat16* ina = in + static_cast<int64_t>(rowa) * K;
+  const __nv_bfloat16* inb = in + static_cast<int64_t>(rowb) * K;
+  for (int c = 8 * blockIdx.y + warp; c < n_chunks; c += 2 * stride) {
+    uint4 xa[2], xb[2], bv[2][NT];
 #pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      const int j = t * 8 + g;
-      const uint4 bv = (kin && j < r) ? ldg_nc_v4(mt + static_cast<int64_t>(j) * K + kb) : zero;
-      mma_m16n8k16_bf16(acc[t], xa.x, xb.x, xa.y, xb.y, bv.x, bv.y);
-      mma_m16n8k16_bf16(acc[t], xa.z, xb.z, xa.w, xb.w, bv.z, bv.w);
+    for (int u = 0; u < 2; ++u) {
+      const int kb = (c + u * stride) * 32 + q * 8;
+      const bool kin = kb < K;
+      xa[u] = (kin && rowa < M) ? ldg_nc_v4(ina + kb) : zero;
+      xb[u] = (kin && rowb < M) ? ldg_nc_v4(inb + kb) : zero;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int j = t * 8 + g;
+        bv[u][t] = (kin && j < r) ? load_mt_frag<NT, MT_KMAJOR>(mt, j, kb, K, r) : zero;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        mma_m16n8k16_bf16(acc[t], xa[u].x, xb[u].x, xa[u].y, xb[u].y, bv[u][t].x, bv[u][t].y);
+        mma_m16n8k16_bf16(acc[t], xa[u].z, xb[u].z, xa[u].w, xb[u].w, bv[u][t].z, bv[u][t].w);
+      }
     }
   }
   // intra-CTA reduction over the 8 warps in warp order
@@ -117,30 +152,6 @@ __global__ void __launch_bounds__(256) k_lora_down(const __nv_bfloat16* __restri
   if (threadIdx.x == 0) counters[blockIdx.x] = 0;
 }
 
-// dst[c, r] = src[r, c]   (bf16, rows x cols source)
-__global__ void k_transpose_bf16(const __nv_bfloat16* __restrict__ src, __nv_bfloat16* __restrict__ dst, int rows,
-                                 int cols) {
-  __shared__ __nv_bfloat16 tile[32][33];
-  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int rr = r0 + i, cc = c0 + threadIdx.x;
-    if (rr < rows && cc < cols) tile[i][threadIdx.x] = src[static_cast<int64_t>(rr) * cols + cc];
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += blockDim.y) {
-    const int cc = c0 + i, rr = r0 + threadIdx.x;
-    if (rr < rows && cc < cols) dst[static_cast<int64_t>(cc) * rows + rr] = tile[threadIdx.x][i];
-  }
-}
-
-// dst = bf16_rn(scale * src)
-__global__ void k_scale_to_bf16(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t n,
-                                float scale) {
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
-    dst[i] = __float2bfloat16_rn(__fmul_rn(src[i], scale));
-}
-
 // ------------------------------------------------------------------ SiLU * up
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -182,9 +193,10 @@ __global__ void __launch_bounds__(256) k_silu_mul_bwd(const uint32_t* __restrict
 
 // ------------------------------------------------------------------ launchers
 int lora_down_splits(int M, int K, int num_sms) {
+  // aim for two CTAs per SM while each warp keeps at least one two-chunk trip
   const int tiles = M > 0 ? (M + 15) / 16 : 1;
   int splits = 1;
-  while (tiles * splits < num_sms && splits * 2 * 8 * 32 <= K) splits *= 2;
+  while (tiles * splits < 2 * num_sms && splits * 2 * 8 * 64 <= K) splits *= 2;
   return splits;
 }
 
@@ -196,8 +208,10 @@ size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms) {
   return static_cast<size_t>(splits) * tiles * 16 * rp * sizeof(float) + static_cast<size_t>(tiles) * 4 + 256;
 }
 
-cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int M, int K, int r, float scale,
-                             float* out_f32, __nv_bfloat16* out_bf16, void* ws, int num_sms, cudaStream_t s) {
+cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int mt_kmajor, int M, int K, int r,
+                             float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int num_sms,
+                             cudaStream_t s, const float* cvt_src, __nv_bfloat16* cvt_dst, int64_t cvt_n,
+                             float cvt_scale) {
   const int tiles = (M + 15) / 16;
   const int splits = lora_down_splits(M, K, num_sms);
   const int rp = r <= 16 ? 16 : (r <= 32 ? 32 : (r <= 64 ? 64 : 128));
@@ -211,31 +225,25 @@ cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, i
   }
   const dim3 grid(tiles, splits);
   const size_t smem = static_cast<size_t>(8) * 16 * rp * sizeof(float);
-#define QLORA_LD(NT)                                                                                          \
+#define QLORA_LD(NT, KM)                                                                                      \
   do {                                                                                                        \
-    cudaFuncSetAttribute(k_lora_down<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)); \
-    k_lora_down<NT><<<grid, 256, smem, s>>>(in, mt, M, K, r, splits, partial, counters, scale, out_f32, out_bf16); \
+    set_smem_limit_once(k_lora_down<NT, KM>, smem);                                                           \
+    k_lora_down<NT, KM><<<grid, 256, smem, s>>>(in, mt, M, K, r, splits, partial, counters, scale, out_f32,   \
+                                                out_bf16, cvt_src, cvt_dst, cvt_n, cvt_scale);                \
   } while (0)
-  if (rp == 16) QLORA_LD(2);
-  else if (rp == 32) QLORA_LD(4);
-  else if (rp == 64) QLORA_LD(8);
-  else QLORA_LD(16);
+#define QLORA_LD2(NT) \
+  do {                \
+    if (mt_kmajor)    \
+      QLORA_LD(NT, true); \
+    else              \
+      QLORA_LD(NT, false); \
+  } while (0)
+  if (rp == 16) QLORA_LD2(2);
+  else if (rp == 32) QLORA_LD2(4);
+  else if (rp == 64) QLORA_LD2(8);
+  else QLORA_LD2(16);
+#undef QLORA_LD2
 #undef QLORA_LD
-  return cudaGetLastError();
-}
-
-cudaError_t launch_transpose_bf16(const __nv_bfloat16* src, __nv_bfloat16* dst, int rows, int cols, cudaStream_t s) {
-  const dim3 grid((cols + 31) / 32, (rows + 31) / 32), block(32, 8);
-  k_transpose_bf16<<<grid, block, 0, s>>>(src, dst, rows, cols);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_scale_to_bf16(const float* src, __nv_bfloat16* dst, int64_t n, float scale, int num_sms,
-                                 cudaStream_t s) {
-  int64_t g = (n + 255) / 256;
-  if (g > num_sms * 8) g = num_sms * 8;
-  if (g < 1) g = 1;
-  k_scale_to_bf16<<<static_cast<unsigned>(g), 256, 0, s>>>(src, dst, n, scale);
   return cudaGetLastError();
 }
 

@@ -469,9 +469,12 @@ __global__ void __launch_bounds__(kWbThreads, 1)
 struct LgParams {
   float* da;  // [r, K]
   float* db;  // [N, r]
+  float* partial;      // [splits][tiles][128][r] (splits > 1)
+  unsigned* counters;  // [tiles]
   unsigned* status;
   int M, N, K, r;
-  int tiles_a;
+  int tiles_a, tiles;
+  int splits, iters_per_split;
   int accum_da, accum_db;
   unsigned long long wait_ns;
 };
@@ -508,7 +511,10 @@ __global__ void __launch_bounds__(kLgThreads, 1)
   const int C = is_b ? p.N : p.K;
   const CUtensorMap* tq = is_b ? &tm_dy : &tm_x;
   const CUtensorMap* tp = is_b ? &tm_st : &tm_su;
-  const int n_iter = (p.M + 63) / 64;
+  const int split = blockIdx.y;
+  const int it0 = split * p.iters_per_split;
+  const int n_iter = min((p.M + 63) / 64, it0 + p.iters_per_split) - it0;  // >= 1 by construction
+  int* last_flag = abort_flag + 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kLgStages; ++s) {
@@ -538,11 +544,12 @@ __global__ void __launch_bounds__(kLgThreads, 1)
         const uint32_t ph = (i / kLgStages) & 1;
         if (!mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
         uint8_t* sa = smem + s * Cfg::kStage;
+        const int mrow = (it0 + i) * 64;
         mbar_arrive_expect_tx(&full[s], Cfg::kStage);
-        tma_load_2d(sa, tq, &full[s], c0, i * 64);
-        tma_load_2d(sa + 8192, tq, &full[s], c0 + 64, i * 64);
+        tma_load_2d(sa, tq, &full[s], c0, mrow);
+        tma_load_2d(sa + 8192, tq, &full[s], c0 + 64, mrow);
 #pragma unroll
-        for (int sl = 0; sl < RP / 64; ++sl) tma_load_2d(sa + Cfg::kABytes + sl * 8192, tp, &full[s], sl * 64, i * 64);
+        for (int sl = 0; sl < RP / 64; ++sl) tma_load_2d(sa + Cfg::kABytes + sl * 8192, tp, &full[s], sl * 64, mrow);
       }
     }
   } else if (warp == 1) {
@@ -573,27 +580,50 @@ __global__ void __launch_bounds__(kLgThreads, 1)
     const int quarter = warp & 3;
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
     const int c = c0 + quarter * 32 + lane;
+    const int tile = blockIdx.x;
+    float* mine = p.partial + (static_cast<int64_t>(split) * p.tiles + tile) * 128 * p.r + (quarter * 32 + lane) * p.r;
+    auto store = [&](int j, float val) {
+      if (!is_b) {
+        float* d = p.da + static_cast<int64_t>(j) * p.K + c;
+        *d = p.accum_da ? (*d + val) : val;
+      } else {
+        float* d = p.db + static_cast<int64_t>(c) * p.r + j;
+        *d = p.accum_db ? (*d + val) : val;
+      }
+    };
     if (ok) {
-      for (int j0 = 0; j0 < RP; j0 += 16) {
+      for (int j0 = 0; j0 < RP && j0 < p.r; j0 += 16) {
         uint32_t v[16];
         __syncwarp();
         tmem_ld_32x32b_x16(tbase + lane_field + j0, v);
         tmem_ld_wait();
-        if (c < C) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj) {
-            const int j = j0 + jj;
-            if (j >= p.r) break;
-            const float val = __uint_as_float(v[jj]);
-            if (!is_b) {
-              float* d = p.da + static_cast<int64_t>(j) * p.K + c;
-              *d = p.accum_da ? (*d + val) : val;
-            } else {
-              float* d = p.db + static_cast<int64_t>(c) * p.r + j;
-              *d = p.accum_db ? (*d + val) : val;
-            }
+        for (int jj = 0; jj < 16; ++jj) {
+          const int j = j0 + jj;
+          if (j >= p.r) break;
+          if (p.splits > 1) mine[j] = __uint_as_float(v[jj]);
+          else if (c < C) store(j, __uint_as_float(v[jj]));
+        }
+      }
+    }
+    if (p.splits > 1) {
+      // the last CTA of this column tile adds the splits in split order
+      __threadfence();
+      named_bar_sync(1, 128);
+      if (threadIdx.x == 64) *last_flag = (atomicAdd(p.counters + tile, 1u) == static_cast<unsigned>(p.splits - 1));
+      named_bar_sync(1, 128);
+      if (*reinterpret_cast<volatile int*>(last_flag)) {
+        __threadfence();
+        if (c < C) {
+          for (int j = 0; j < p.r; ++j) {
+            float acc = 0.f;
+            for (int sp = 0; sp < p.splits; ++sp)
+              acc += __ldcg(p.partial + (static_cast<int64_t>(sp) * p.tiles + tile) * 128 * p.r +
+                            (quarter * 32 + lane) * p.r + j);
+            store(j, acc);
           }
         }
+        if (threadIdx.x == 64) p.counters[tile] = 0;
       }
     }
   }
@@ -693,8 +723,7 @@ template <int NTOK, int STAGES>
 static cudaError_t run_wa(const CUtensorMap& tx, const CUtensorMap& tst, const WaParams& prm, dim3 grid,
                           cudaStream_t s) {
   using Cfg = WaCfg<NTOK, STAGES>;
-  cudaError_t e = cudaFuncSetAttribute(k_qgemm_wa<NTOK, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(Cfg::kSmem));
+  cudaError_t e = set_smem_limit_once(k_qgemm_wa<NTOK, STAGES>, Cfg::kSmem);
   if (e != cudaSuccess) return e;
   k_qgemm_wa<NTOK, STAGES><<<grid, kWaThreads, Cfg::kSmem, s>>>(tx, tst, prm);
   return cudaGetLastError();
@@ -763,45 +792,76 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
   prm.wait_ns = wait_ns;
   constexpr int kStages = 4;
   const size_t smem = WbCfg<kStages>::kSmem;
-  cudaError_t e =
-      cudaFuncSetAttribute(k_qgemm_wb<kStages>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  cudaError_t e = set_smem_limit_once(k_qgemm_wb<kStages>, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((K + 255) / 256, (M + 127) / 128);
   k_qgemm_wb<kStages><<<grid, kWbThreads, smem, s>>>(tdy, tsu, tla, prm);
   return cudaGetLastError();
 }
 
+struct LgPlan {
+  int tiles_a, tiles, splits, iters;
+};
+static LgPlan plan_lg(int M, int N, int K, int num_sms) {
+  LgPlan pl;
+  pl.tiles_a = (K + 127) / 128;
+  pl.tiles = pl.tiles_a + (N + 127) / 128;
+  const int n_iter = (M + 63) / 64;
+  int splits = 1;
+  while (pl.tiles * splits < 2 * num_sms && splits * 2 * 4 <= n_iter) splits *= 2;  // >= 4 m-blocks per split
+  pl.iters = (n_iter + splits - 1) / splits;
+  pl.splits = (n_iter + pl.iters - 1) / pl.iters;
+  return pl;
+}
+
+size_t lora_grads_workspace_bytes(int M, int N, int K, int r, int num_sms) {
+  const LgPlan pl = plan_lg(M, N, K, num_sms);
+  if (pl.splits == 1) return 0;
+  return static_cast<size_t>(pl.splits) * pl.tiles * 128 * r * 4 + static_cast<size_t>(pl.tiles) * 4 + 256;
+}
+
 cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __nv_bfloat16* su,
                               const __nv_bfloat16* st, int M, int N, int K, int r, float* da, float* db,
-                              int accum_da, int accum_db, unsigned* status, uint64_t wait_ns, cudaStream_t s) {
+                              int accum_da, int accum_db, void* ws, unsigned* status, uint64_t wait_ns, int num_sms,
+                              cudaStream_t s) {
   CUtensorMap tx, tdy, tsu, tst;
   if (!make_tm(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
   if (!make_tm(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 64)) return cudaErrorInvalidValue;
   if (!make_tm(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
   if (!make_tm(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
+  const LgPlan pl = plan_lg(M, N, K, num_sms);
   LgParams prm;
   prm.da = da;
   prm.db = db;
+  prm.partial = nullptr;
+  prm.counters = nullptr;
   prm.status = status;
   prm.M = M;
   prm.N = N;
   prm.K = K;
   prm.r = r;
-  prm.tiles_a = (K + 127) / 128;
+  prm.tiles_a = pl.tiles_a;
+  prm.tiles = pl.tiles;
+  prm.splits = pl.splits;
+  prm.iters_per_split = pl.iters;
   prm.accum_da = accum_da;
   prm.accum_db = accum_db;
   prm.wait_ns = wait_ns;
-  const dim3 grid(prm.tiles_a + (N + 127) / 128);
+  if (pl.splits > 1) {
+    prm.partial = static_cast<float*>(ws);
+    prm.counters = reinterpret_cast<unsigned*>(prm.partial + static_cast<size_t>(pl.splits) * pl.tiles * 128 * r);
+    const cudaError_t e = cudaMemsetAsync(prm.counters, 0, static_cast<size_t>(pl.tiles) * 4, s);
+    if (e != cudaSuccess) return e;
+  }
+  const dim3 grid(pl.tiles, pl.splits);
   if (r <= 64) {
     const size_t smem = LgCfg<64>::kSmem;
-    cudaError_t e =
-        cudaFuncSetAttribute(k_lora_grad<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = set_smem_limit_once(k_lora_grad<64>, smem);
     if (e != cudaSuccess) return e;
     k_lora_grad<64><<<grid, kLgThreads, smem, s>>>(tx, tdy, tsu, tst, prm);
   } else {
     const size_t smem = LgCfg<128>::kSmem;
-    cudaError_t e =
-        cudaFuncSetAttribute(k_lora_grad<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    cudaError_t e = set_smem_limit_once(k_lora_grad<128>, smem);
     if (e != cudaSuccess) return e;
     k_lora_grad<128><<<grid, kLgThreads, smem, s>>>(tx, tdy, tsu, tst, prm);
   }

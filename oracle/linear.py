@@ -64,6 +64,16 @@ def lora_backward(dy, x, wdeq, a, b, alpha: float, r: int, t=None):
     return dx, da, db, u
 
 
+def lora_grads(dy, x, a, b, alpha: float, r: int, t=None):
+    """``(dA, dB)`` of :func:`lora_backward` without dX (the same two formulas)."""
+    dy, x, a, b = _f64(dy), _f64(x), _f64(a), _f64(b)
+    s = lora_scale(alpha, r)
+    if t is None:
+        t = x @ a.T
+    u = dy @ b
+    return s * (u.T @ x), s * (dy.T @ _f64(t))
+
+
 def lora_forward_rows(x_rows, wdeq, a, b, alpha: float, r: int):
     """:func:`lora_forward` on a subset of token rows (rows are independent)."""
     return lora_forward(x_rows, wdeq, a, b, alpha, r)

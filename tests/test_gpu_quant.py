@@ -120,3 +120,31 @@ def test_bounded_wait_timeout_keeps_context(lib):
     rec = lib.quantize(w)
     lib.check_status()
     _assert_record_equal(lib, rec, _oracle_record(w.cpu()), 8, 64)
+
+
+def test_65b_upproj_weight_sampled_rows(lib):
+    """22016 x 8192 (Llama-65B up-projection): the double quantisation of all
+    2.8 M block scales bit-exact, codes and dequantised rows on 64 sampled rows."""
+    n, k = 22016, 8192
+    w = synthetic.weight(n, k, device="cuda", seed=4242)
+    rec = lib.quantize(w)
+    lib.check_status()
+    wc = to_np32(w.cpu())
+    a = nf4.blockwise_absmax(wc)
+    q, step, mu = nf4.double_quant(a)
+    assert np.array_equal(rec.absmax_q.cpu().numpy(), q)
+    assert np.array_equal(rec.absmax_step.cpu().numpy().view(np.uint32), step.view(np.uint32))
+    assert rec.absmax_mean.cpu().numpy().view(np.uint32)[0] == np.float32(mu).view(np.uint32)
+    rows = np.sort(np.random.default_rng(1).choice(n, 64, replace=False))
+    codes_gpu = rec.codes.cpu().numpy().reshape(n, k // 2)
+    bpr = k // 64
+    for r0 in rows:
+        ref = nf4.pack_codes(nf4.nf4_encode(wc[r0], a[r0 * bpr:(r0 + 1) * bpr]))
+        assert np.array_equal(codes_gpu[r0], ref)
+    wd = lib.dequantize(rec)[torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy().view(np.uint16)
+    lv = nf4.nf4_levels_f32()
+    a2 = nf4.dequant_absmax(q, step, mu).reshape(n, bpr)
+    for i, r0 in enumerate(rows):
+        c = nf4.unpack_codes(codes_gpu[r0]).reshape(bpr, 64)
+        ref = nf4.f32_to_bf16_bits((lv[c] * a2[r0][:, None]).astype(np.float32)).reshape(-1)
+        assert np.array_equal(wd[i], ref)

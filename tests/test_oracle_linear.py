@@ -119,3 +119,10 @@ def test_silu_mul_matches_autograd():
     assert linear.silu_mul_forward(0.0, 5.0) == 0.0
     dg0, _ = linear.silu_mul_backward(1.0, 0.0, 1.0)
     assert dg0 == pytest.approx(0.5)
+
+
+def test_lora_grads_helper_agrees_with_backward():
+    x, w, a, b, dy = _case(seed=7)
+    _, da, db, _ = linear.lora_backward(dy, x, w, a, b, 16.0, 8)
+    da2, db2 = linear.lora_grads(dy, x, a, b, 16.0, 8)
+    assert np.array_equal(da, da2) and np.array_equal(db, db2)
