@@ -233,8 +233,14 @@ def time_events(torch, fn, steps, flush=None):
 
 
 def decode_sweep(q, torch, layers: int = 32, tokens=(1, 4, 16), passes: int = 10):
-    """Weight GB/s of the Llama-7B decode stack: one pass = Y = X deq(W)^T + s (X A^T) B^T on all
-    7 x `layers` matrices, captured in one CUDA graph per token count."""
+    """Weight GB/s of the Llama-7B decode stack at 1, 4 and 16 tokens.
+
+    One pass = Y = X deq(W)^T + s (X A^T) B^T for all 7 x `layers` matrices, r=16, alpha=32.
+    * ``grouped``: the whole stack as one qlora_linear_fwd_grouped call (independent inputs per matrix);
+    * ``per_layer``: the dependency order of a decoder layer -- q,k,v | o | gate,up | down -- as four
+      grouped calls per layer (128 calls per pass), captured in one CUDA graph;
+    * ``per_matrix``: one qlora_linear_fwd call per matrix (224 calls), captured in one CUDA graph.
+    """
     import synthetic
     shapes = synthetic.LLAMA7B_LAYER
     recs, loras = [], []
@@ -248,9 +254,40 @@ def decode_sweep(q, torch, layers: int = 32, tokens=(1, 4, 16), passes: int = 10
     weight_bytes = sum(r.nbytes() for r in recs)
     lora_bytes = sum(a.numel() * 2 + b.numel() * 2 for a, b in loras)
     out = {"matrices": len(recs), "weight_bytes_per_pass": weight_bytes, "lora_bytes_per_pass": lora_bytes}
+    stages = [(0, 3), (3, 4), (4, 6), (6, 7)]  # q,k,v | o | gate,up | down
     for t in tokens:
         xs = [synthetic.activations(t, r.k, device="cuda", seed=90_000 + i) for i, r in enumerate(recs)]
         ys = [torch.empty((t, r.n), dtype=torch.bfloat16, device="cuda") for r in recs]
+        probs = [(xs[i], recs[i], loras[i][0], loras[i][1], 32.0, ys[i], None) for i in range(len(recs))]
+        io_bytes = sum(x.numel() * 2 for x in xs) + sum(y.numel() * 2 for y in ys)
+        res = {}
+        # grouped: one call for the whole stack
+        g_all = q.GroupedForward(probs)
+        g_all.run()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g_all.run()
+        ms = statistics.median(time_events(torch, g_all.run, passes))
+        res["grouped"] = {"ms_per_pass": ms, "weight_gbs": (weight_bytes + lora_bytes) / ms / 1e6, "launches": 2}
+        # per layer: 4 dependent groups per layer
+        groups = [q.GroupedForward(probs[7 * L + a:7 * L + b]) for L in range(layers) for (a, b) in stages]
+
+        def per_layer():
+            for g in groups:
+                g.run()
+
+        per_layer()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            per_layer()
+        for _ in range(3):
+            graph.replay()
+        ms = statistics.median(time_events(torch, graph.replay, passes))
+        res["per_layer"] = {"ms_per_pass": ms, "weight_gbs": (weight_bytes + lora_bytes) / ms / 1e6,
+                            "launches": 2 * len(groups)}
+        del graph
+        # per matrix: one single-problem call each
         ts = [torch.empty((t, 16), dtype=torch.float32, device="cuda") for r in recs]
         wsb = max(q.fwd_workspace_bytes(t, r.n, r.k, 16) for r in recs)
         ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device="cuda")
@@ -261,19 +298,17 @@ def decode_sweep(q, torch, layers: int = 32, tokens=(1, 4, 16), passes: int = 10
 
         one_pass()
         torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
             one_pass()
         for _ in range(3):
-            g.replay()
-        torch.cuda.synchronize()
-        ms = time_events(torch, g.replay, passes)
+            graph.replay()
+        ms = statistics.median(time_events(torch, graph.replay, passes))
+        res["per_matrix"] = {"ms_per_pass": ms, "weight_gbs": (weight_bytes + lora_bytes) / ms / 1e6}
         q.check_status()
-        io_bytes = sum(x.numel() * 2 for x in xs) + sum(y.numel() * 2 for y in ys)
-        med = statistics.median(ms)
-        out["t%d" % t] = {"ms_per_pass": med, "weight_gbs": (weight_bytes + lora_bytes) / med / 1e6,
-                          "all_bytes_gbs": (weight_bytes + lora_bytes + io_bytes) / med / 1e6}
-        del g, xs, ys, ts, ws
+        res["io_bytes_per_pass"] = io_bytes
+        out["t%d" % t] = res
+        del graph, xs, ys, ts, ws, g_all, groups
     del recs, loras
     torch.cuda.empty_cache()
     return out
@@ -568,8 +603,10 @@ def run_ours(args, world, rank, local):
         torch.cuda.empty_cache()
         sweep = decode_sweep(q, torch, layers=args.decode_layers)
         for t in (1, 4, 16):
-            if "t%d" % t in sweep:
-                sweep["t%d" % t]["frac_of_hbm"] = sweep["t%d" % t]["weight_gbs"] / peaks["hbm_gbs"]
+            for mode in ("grouped", "per_layer", "per_matrix"):
+                d = sweep.get("t%d" % t, {}).get(mode)
+                if d:
+                    d["frac_of_hbm"] = d["weight_gbs"] / peaks["hbm_gbs"]
         secondary["decode_sweep"] = sweep
         secondary["dequant"]["frac_of_hbm"] = secondary["dequant"]["gbs"] / peaks["hbm_gbs"]
         secondary["quantize"]["frac_of_hbm"] = secondary["quantize"]["gbs"] / peaks["hbm_gbs"]

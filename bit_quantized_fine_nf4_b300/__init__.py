@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     ACCUM_DB,
     ACCUM_DX,
     EXPORTS,
+    GroupedForward,
     LIB_PATH,
     NF4Weight,
     QloraError,
@@ -29,6 +30,7 @@ from ._binding import (  # noqa: F401
     launch_count,
     linear_bwd,
     linear_fwd,
+    linear_fwd_grouped,
     load,
     profile_enable,
     profile_read,

@@ -40,6 +40,8 @@ EXPORTS = (
     "qlora_linear_fwd",
     "qlora_linear_bwd_workspace_bytes",
     "qlora_linear_bwd",
+    "qlora_linear_fwd_grouped_workspace_bytes",
+    "qlora_linear_fwd_grouped",
     "qlora_silu_mul_fwd",
     "qlora_silu_mul_bwd",
     "qlora_get_status",
@@ -75,12 +77,27 @@ class _Weight(ctypes.Structure):
     ]
 
 
+class _Problem(ctypes.Structure):
+    _fields_ = [
+        ("x", ctypes.c_void_p),
+        ("m", ctypes.c_int64),
+        ("w", ctypes.POINTER(_Weight)),
+        ("lora_a", ctypes.c_void_p),
+        ("lora_b", ctypes.c_void_p),
+        ("r", ctypes.c_int),
+        ("alpha", ctypes.c_float),
+        ("y", ctypes.c_void_p),
+        ("t_save", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _SZ = ctypes.c_size_t
 _PSZ = ctypes.POINTER(ctypes.c_size_t)
 _PW = ctypes.POINTER(_Weight)
+_PP = ctypes.POINTER(_Problem)
 
 
 def load(path: str | None = None) -> ctypes.CDLL:
@@ -104,6 +121,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "qlora_linear_bwd_workspace_bytes": (c_int, [_I64, _I64, _I64, c_int, _PSZ]),
         "qlora_linear_bwd": (c_int, [_P, _P, _I64, _PW, _P, _P, c_int, c_float, _P, _P, _P, _P, c_int, _P, _SZ,
                                      _P]),
+        "qlora_linear_fwd_grouped_workspace_bytes": (c_int, [_PP, c_int, _PSZ]),
+        "qlora_linear_fwd_grouped": (c_int, [_PP, c_int, _P, _SZ, _P]),
         "qlora_silu_mul_fwd": (c_int, [_P, _P, _P, _I64, _P]),
         "qlora_silu_mul_bwd": (c_int, [_P, _P, _P, _P, _P, _I64, _P]),
         "qlora_get_status": (c_int, [_P]),
@@ -283,6 +302,43 @@ def linear_bwd(dy: torch.Tensor, x: torch.Tensor, rec: NF4Weight, lora_a: torch.
                                 _ptr(t_save), _ptr(dx), _ptr(da), _ptr(db), int(flags), _ptr(ws), wsb,
                                 _stream(stream)))
     return dx, da, db
+
+
+class GroupedForward:
+    """A prepared list of small-token problems for qlora_linear_fwd_grouped.
+
+    ``problems``: sequence of (x [m, k] bf16, NF4Weight, A [r, k], B [n, r], alpha, y [m, n] bf16 or None,
+    t_save [m, r] f32 or None).  The ctypes array and the workspace are built once; ``run()`` is one call.
+    """
+
+    def __init__(self, problems, workspace=None):
+        lib = load()
+        self._keep = []
+        n = len(problems)
+        self.arr = (_Problem * max(n, 1))()
+        self.ys = []
+        for i, (x, rec, a, b, alpha, y, t_save) in enumerate(problems):
+            if y is None:
+                y = torch.empty((x.shape[0], rec.n), dtype=torch.bfloat16, device=x.device)
+            w = rec.c_struct()
+            self._keep.append(w)
+            self.arr[i] = _Problem(_ptr(x), x.shape[0], ctypes.pointer(w), _ptr(a), _ptr(b), a.shape[0],
+                                   float(alpha), _ptr(y), _ptr(t_save) if t_save is not None else None)
+            self.ys.append(y)
+        self.count = n
+        b_ = ctypes.c_size_t(0)
+        _check(lib.qlora_linear_fwd_grouped_workspace_bytes(self.arr, n, ctypes.byref(b_)))
+        dev = problems[0][0].device if n else "cuda"
+        self.ws, self.wsb = _ws(b_.value, dev, workspace)
+
+    def run(self, stream=None):
+        _check(load().qlora_linear_fwd_grouped(self.arr, self.count, _ptr(self.ws), self.wsb, _stream(stream)))
+        return self.ys
+
+
+def linear_fwd_grouped(problems, workspace=None, stream=None):
+    """One qlora_linear_fwd_grouped call; returns the list of y tensors."""
+    return GroupedForward(problems, workspace).run(stream)
 
 
 def silu_mul_fwd(g: torch.Tensor, u: torch.Tensor, h: torch.Tensor | None = None, stream=None) -> torch.Tensor:

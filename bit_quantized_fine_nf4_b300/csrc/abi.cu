@@ -132,11 +132,11 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 // and, while profiling is on, bracketed by two CUDA events on its stream.
 enum ProfName : int {
   P_QUANTIZE = 0, P_DEQUANTIZE, P_LORA_DOWN, P_FWD_GEMM, P_BWD_GEMM, P_LORA_GRADS, P_SILU_FWD, P_SILU_BWD,
-  P_SELFTEST, P_COUNT
+  P_SELFTEST, P_FWD_GROUPED, P_COUNT
 };
 const char* const kProfNames[P_COUNT] = {"nf4_quantize(3 kernels)", "nf4_dequantize", "lora_down", "fwd_gemm",
                                          "bwd_dx_gemm", "lora_grads", "silu_mul_fwd", "silu_mul_bwd",
-                                         "wait_selftest"};
+                                         "wait_selftest", "fwd_grouped(2 kernels)"};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<bool> g_prof_on{false};
 struct ProfRec {
@@ -378,6 +378,60 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
                                  (flags & QLORA_ACCUM_DB) ? 1 : 0, lgws, di->status, wait, di->num_sms, s);
   }
   return cuda_ret(e, "lora grads");
+}
+
+int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problems, int count, size_t* bytes) {
+  if (!bytes) return fail(QLORA_ERR_INVALID_ARGUMENT, "bytes is NULL");
+  if (count < 0 || (count > 0 && !problems)) return fail(QLORA_ERR_INVALID_ARGUMENT, "problems");
+  size_t tot = 0;
+  for (int i = 0; i < count; ++i) tot += (static_cast<size_t>(problems[i].m) * problems[i].r * 2 + 255) & ~size_t(255);
+  *bytes = tot;
+  return QLORA_OK;
+}
+
+int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if (count < 0 || (count > 0 && !problems)) return fail(QLORA_ERR_INVALID_ARGUMENT, "problems");
+  if (count == 0) return QLORA_OK;
+  std::vector<qlora::GroupedProblem> gp(static_cast<size_t>(count));
+  size_t need = 0;
+  for (int i = 0; i < count; ++i) {
+    const qlora_linear_problem& q = problems[i];
+    if ((rc = check_weight(q.w))) return fail(rc, "problem %d: %s", i, t_last_error);
+    if (q.m < 1 || q.m > 16) return fail(QLORA_ERR_UNSUPPORTED, "problem %d: m = %lld (the grouped path takes 1..16 tokens)", i, (long long)q.m);
+    if (q.r < 8 || q.r > 64 || (q.r % 8)) return fail(QLORA_ERR_UNSUPPORTED, "problem %d: r = %d (grouped path: 8 <= r <= 64, r %% 8 == 0)", i, q.r);
+    if ((rc = check_ptr(q.x, "x")) || (rc = check_ptr(q.lora_a, "lora_a")) || (rc = check_ptr(q.lora_b, "lora_b")) ||
+        (rc = check_ptr(q.y, "y")))
+      return fail(rc, "problem %d: %s", i, t_last_error);
+    if (q.t_save && !aligned16(q.t_save)) return fail(QLORA_ERR_INVALID_ARGUMENT, "problem %d: t_save not 16-byte aligned", i);
+    qlora::GroupedProblem& g = gp[static_cast<size_t>(i)];
+    g.x = reinterpret_cast<const __nv_bfloat16*>(q.x);
+    g.w = to_dev(q.w);
+    g.lora_a = reinterpret_cast<const __nv_bfloat16*>(q.lora_a);
+    g.lora_b = reinterpret_cast<const __nv_bfloat16*>(q.lora_b);
+    g.m = static_cast<int>(q.m);
+    g.r = q.r;
+    g.alpha = q.alpha;
+    g.y = reinterpret_cast<__nv_bfloat16*>(q.y);
+    g.t_save = q.t_save;
+    need += (static_cast<size_t>(q.m) * q.r * 2 + 255) & ~size_t(255);
+  }
+  if ((rc = check_ptr(workspace, "workspace"))) return rc;
+  if (workspace_bytes < need) return fail(QLORA_ERR_INVALID_ARGUMENT, "workspace %zu < %zu bytes", workspace_bytes, need);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int chunk = qlora::fwd_grouped_max_problems();
+  char* ws = static_cast<char*>(workspace);
+  for (int i0 = 0; i0 < count; i0 += chunk) {
+    const int n = count - i0 < chunk ? count - i0 : chunk;
+    Span sp(P_FWD_GROUPED, s, 2);
+    cudaError_t e = qlora::launch_fwd_grouped(gp.data() + i0, n, ws, di->status, g_wait_ns.load(), di->num_sms, s);
+    if (e != cudaSuccess) return cuda_ret(e, "fwd grouped");
+    ws += qlora::fwd_grouped_workspace_bytes(gp.data() + i0, n);
+  }
+  return QLORA_OK;
 }
 
 int qlora_silu_mul_fwd(const uint16_t* g, const uint16_t* u, uint16_t* h, int64_t count, void* stream) {

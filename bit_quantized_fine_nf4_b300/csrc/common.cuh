@@ -78,6 +78,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// A bounded wait expired: latch the status and make the CTA's other roles stop waiting.
+__device__ __forceinline__ void abort_cta(unsigned* status, int* abort_flag) {
+  latch_status(status, ST_TIMEOUT);
+  *reinterpret_cast<volatile int*>(abort_flag) = 1;
+}
+
 // ------------------------------------------------------------------ proxies / fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

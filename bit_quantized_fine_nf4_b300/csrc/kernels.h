@@ -67,6 +67,22 @@ cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, c
                               int accum_da, int accum_db, void* ws, unsigned* status, uint64_t wait_ns, int num_sms,
                               cudaStream_t s);
 
+// Grouped small-token forward (qgemv_grouped.cu): one problem of the list.
+struct GroupedProblem {
+  const __nv_bfloat16* x;       // [m, k], m <= 16
+  Nf4Dev w;                     // [n, k]
+  const __nv_bfloat16* lora_a;  // [r, k]
+  const __nv_bfloat16* lora_b;  // [n, r]
+  int m, r;                     // r <= 64
+  float alpha;
+  __nv_bfloat16* y;             // [m, n]
+  float* t_save;                // [m, r] or null
+};
+int fwd_grouped_max_problems();
+size_t fwd_grouped_workspace_bytes(const GroupedProblem* probs, int count);
+cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws, unsigned* status, uint64_t wait_ns,
+                               int num_sms, cudaStream_t s);
+
 // Bounded-wait self test: one CTA waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t wait_ns, cudaStream_t s);
 

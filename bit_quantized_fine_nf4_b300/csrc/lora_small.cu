@@ -29,8 +29,8 @@ __device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, ui
 }
 
 // CTA = 8 warps, 16 rows of `in`.  Warp w handles 32-wide k chunks c with
-// c % (8 * splits) == 8 * blockIdx.y + w, two chunks per loop trip so their
-// loads are in flight together.  Within a chunk, thread (g, q) = (lane / 4,
+// c % (8 * splits) == 8 * blockIdx.y + w, 4 (or 2 for r > 16) chunks per loop
+// trip so their loads are in flight together.  Within a chunk, thread (g, q) = (lane / 4,
 // lane % 4) loads 8 consecutive k (16 bytes) of rows g and g + 8, and the k
 // order inside the two m16n8k16 steps is permuted consistently for both
 // operands so each fragment register holds 2 consecutive k.
@@ -79,10 +79,11 @@ __global__ void __launch_bounds__(256) k_lora_down(const __nv_bfloat16* __restri
   const uint4 zero = make_uint4(0, 0, 0, 0);
   const __nv_bfloat16* ina = in + static_cast<int64_t>(rowa) * K;
   const __nv_bfloat16* inb = in + static_cast<int64_t>(rowb) * K;
-  for (int c = 8 * blockIdx.y + warp; c < n_chunks; c += 2 * stride) {
-    uint4 xa[2], xb[2], bv[2][NT];
+  constexpr int UNROLL = NT <= 2 ? 4 : 2;  // chunks whose loads are in flight together
+  for (int c = 8 * blockIdx.y + warp; c < n_chunks; c += UNROLL * stride) {
+    uint4 xa[UNROLL], xb[UNROLL], bv[UNROLL][NT];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
       const int kb = (c + u * stride) * 32 + q * 8;
       const bool kin = kb < K;
       xa[u] = (kin && rowa < M) ? ldg_nc_v4(ina + kb) : zero;
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(256) k_lora_down(const __nv_bfloat16* __restri
       }
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (int u = 0; u < UNROLL; ++u) {
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         mma_m16n8k16_bf16(acc[t], xa[u].x, xb[u].x, xa[u].y, xb[u].y, bv[u][t].x, bv[u][t].y);
@@ -193,11 +194,14 @@ __global__ void __launch_bounds__(256) k_silu_mul_bwd(const uint32_t* __restrict
 
 // ------------------------------------------------------------------ launchers
 int lora_down_splits(int M, int K, int num_sms) {
-  // aim for two CTAs per SM while each warp keeps at least one two-chunk trip
+  // Enough CTAs that every warp makes a single trip (4 chunks of 32 k in flight)
+  // when the grid stays below ~8 CTAs per SM; otherwise as many as fit.
+  (void)num_sms;
   const int tiles = M > 0 ? (M + 15) / 16 : 1;
-  int splits = 1;
-  while (tiles * splits < 2 * num_sms && splits * 2 * 8 * 64 <= K) splits *= 2;
-  return splits;
+  const int n_chunks = (K + 31) / 32;
+  int splits = (n_chunks + 31) / 32;
+  while (splits > 1 && tiles * splits > 8 * 148) splits = (splits + 1) / 2;
+  return splits < 1 ? 1 : splits;
 }
 
 size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms) {

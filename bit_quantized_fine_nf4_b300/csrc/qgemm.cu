@@ -33,14 +33,6 @@
 
 namespace qlora {
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-__device__ __forceinline__ void abort_cta(unsigned* status, int* abort_flag) {
-  latch_status(status, ST_TIMEOUT);
-  *reinterpret_cast<volatile int*>(abort_flag) = 1;
-}
 
 // ====================================================================== forward / decode
 struct WaParams {
@@ -807,8 +799,10 @@ static LgPlan plan_lg(int M, int N, int K, int num_sms) {
   pl.tiles_a = (K + 127) / 128;
   pl.tiles = pl.tiles_a + (N + 127) / 128;
   const int n_iter = (M + 63) / 64;
+  // grow the split while the doubled grid still fits in one wave (two CTAs per SM)
+  // and every split keeps >= 8 m-blocks, so each CTA's 4-stage ring stays full
   int splits = 1;
-  while (pl.tiles * splits < 2 * num_sms && splits * 2 * 4 <= n_iter) splits *= 2;  // >= 4 m-blocks per split
+  while (pl.tiles * splits * 2 <= 2 * num_sms && splits * 2 * 8 <= n_iter) splits *= 2;
   pl.iters = (n_iter + splits - 1) / splits;
   pl.splits = (n_iter + pl.iters - 1) / pl.iters;
   return pl;

@@ -1,0 +1,556 @@
+// Grouped small-token forward (decode): Y_p = X_p deq(W_p)^T + s_p (X_p A_p^T) B_p^T
+// for a list of independent problems p (1..16 tokens each), in two launches.
+//
+// Glossary "QLoRA", "How QLoRA works": the frozen layer dequantises NF4 to
+// bf16 before the matmul and adds the LoRA output; Day 25 notes section 4.4:
+// inference runs the 4-bit base with the adapter attached.  With few tokens the
+// step is a stream over the weight codes, so what matters is keeping HBM busy:
+// one launch walks the 128-row tiles of every matrix in the list.
+//
+// k_lora_down_grouped  one CTA per problem: st_p = bf16(s_p X_p A_p^T) (and
+//                      X_p A_p^T in f32 if asked), 16 warps splitting k.
+// k_qgemv_grouped      work item = (problem, 128-row tile), dealt round-robin
+//                      to the CTAs.  Per 64-wide k block ("stage"):
+//   - a stage is two 64-wide k blocks; producer warps 1-4 decode the even
+//     block, warps 5-8 the odd one, one weight row per thread, into TMEM
+//     (tcgen05 A operand, M = 128).  Each thread prefetches its row's codes,
+//     block-scale byte, group step and mean, plus one 16-byte slice of the
+//     16-token activation tile (later of the sT tile), with cp.async into a
+//     private shared-memory ring kPrefetch stages ahead, with a meta word that
+//     tells the consuming pass what the stage is; after the stage frees, the
+//     slice goes into the 128-byte swizzled K-major B operand;
+//   - one thread issues tcgen05.mma (N = 16) into a double-buffered TMEM
+//     accumulator; the LoRA up-projection is the item's last stage(s);
+//   - the producers drain item j's accumulator after producing item j+1.
+// Deterministic: every output element is written once, no atomics.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace qlora {
+
+constexpr int kGvMaxProbs = 300;
+
+struct GvProb {
+  const uint8_t* codes;
+  const int8_t* absq;
+  const float* step;
+  const float* mean;
+  const __nv_bfloat16* x;       // [m, k]
+  const __nv_bfloat16* lora_b;  // [n, r]
+  const __nv_bfloat16* st;      // [m, r]  bf16(s x A^T)
+  __nv_bfloat16* y;             // [m, n]
+  int n, k, m, r;
+  int item0;  // first work item of this problem
+  int pad;
+};
+
+struct GvParams {
+  int count, total_items;
+  unsigned long long wait_ns;
+  unsigned* status;
+  GvProb prob[kGvMaxProbs];
+};
+
+struct GlProb {
+  const __nv_bfloat16* x;   // [m, k]
+  const __nv_bfloat16* a;   // [r, k]
+  __nv_bfloat16* st;        // [m, r]
+  float* t_save;            // [m, r] or null
+  int m, k, r;
+  float scale;
+};
+
+struct GlParams {
+  int count;
+  GlProb prob[kGvMaxProbs];
+};
+
+__device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ====================================================================== grouped LoRA down
+// Same k-permuted m16n8k16 fragments as k_lora_down; one CTA per problem, 16
+// warps over k, fixed-order reduction of the warps' partial sums.
+template <int NT>
+__global__ void __launch_bounds__(512) k_lora_down_grouped(const __grid_constant__ GlParams p) {
+  constexpr int RP = NT * 8;
+  extern __shared__ float s_red_flat[];  // [16 warps][16 rows][RP]
+  auto s_red = reinterpret_cast<float(*)[16 * RP]>(s_red_flat);
+  const GlProb& pr = p.prob[blockIdx.x];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane >> 2, q = lane & 3;
+  float acc[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  const int n_chunks = pr.k / 32;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  constexpr int U = NT <= 2 ? 4 : 2;
+  for (int c = warp; c < n_chunks; c += 16 * U) {
+    uint4 xa[U], xb[U], bv[U][NT];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int cc = c + 16 * u;
+      const int kb = cc * 32 + q * 8;
+      const bool kin = cc < n_chunks;
+      xa[u] = (kin && g < pr.m) ? ldg_nc_v4(pr.x + static_cast<int64_t>(g) * pr.k + kb) : zero;
+      xb[u] = (kin && g + 8 < pr.m) ? ldg_nc_v4(pr.x + static_cast<int64_t>(g + 8) * pr.k + kb) : zero;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int j = t * 8 + g;
+        bv[u][t] = (kin && j < pr.r) ? ldg_nc_v4(pr.a + static_cast<int64_t>(j) * pr.k + kb) : zero;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        mma_m16n8k16(acc[t], xa[u].x, xb[u].x, xa[u].y, xb[u].y, bv[u][t].x, bv[u][t].y);
+        mma_m16n8k16(acc[t], xa[u].z, xb[u].z, xa[u].w, xb[u].w, bv[u][t].z, bv[u][t].w);
+      }
+  }
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int col = t * 8 + 2 * q;
+    s_red[warp][g * RP + col] = acc[t][0];
+    s_red[warp][g * RP + col + 1] = acc[t][1];
+    s_red[warp][(g + 8) * RP + col] = acc[t][2];
+    s_red[warp][(g + 8) * RP + col + 1] = acc[t][3];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < 16 * RP; idx += 512) {
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < 16; ++w) v += s_red[w][idx];
+    const int row = idx / RP, j = idx % RP;
+    if (row >= pr.m || j >= pr.r) continue;
+    if (pr.t_save) pr.t_save[row * pr.r + j] = v;
+    pr.st[row * pr.r + j] = __float2bfloat16_rn(__fmul_rn(v, pr.scale));
+  }
+}
+
+// ====================================================================== grouped decode GEMV
+constexpr int kGvThreads = 288;  // warp 0 MMA + TMEM, warps 1..8 producers
+constexpr int kGvStages = 3;     // TMEM / smem ring depth (a stage = two 64-wide k blocks)
+constexpr int kGvPrefetch = 4;   // producer cp.async distance, in stages
+constexpr int kGvTok = 16;       // MMA N
+constexpr uint32_t kGvBBytes = 2 * kGvTok * 128;  // two 64-wide slabs of 16 token rows
+constexpr uint32_t kGvDCol = kGvStages * 64;
+constexpr uint32_t kGvTmemCols = 256;
+constexpr uint32_t kGvSlot = 64;
+constexpr size_t kGvSmem = 1024 + kGvStages * kGvBBytes + 256 * kGvPrefetch * kGvSlot + (2 * kGvStages + 4) * 8 + 16;
+static_assert(kGvDCol + 2 * kGvTok <= kGvTmemCols, "TMEM budget");
+
+// Slot layout (one per producer thread per prefetched stage):
+//   [0,32) codes of the thread's row and k block   [32,48) activation slice
+//   [48,52) word holding the block-scale byte       [52,56) group step
+//   [56,60) per-tensor mean                         [60,64) meta (written by the thread)
+enum : uint32_t {
+  kMetaValid = 1u,      // the stage exists
+  kMetaLora = 2u,       // LoRA stage (A = B rows, B operand = sT)
+  kMetaRowOk = 4u,      // row < n and the k block (or j block) is inside the matrix
+  kMetaLast = 32u,      // last stage of its work item
+};
+// meta bits 3-4: byte of the scale word; bits 16-31: problem index
+
+__device__ __forceinline__ int gv_find_prob(const GvParams& p, int item) {
+  int lo = 0, hi = p.count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.prob[mid].item0 <= item) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Walks the stages of this CTA's work items (item = blockIdx.x + j * gridDim.x)
+// with the current problem's fields cached in registers.
+struct GvWalk {
+  int j, l, nst, nmain, kb;  // item counter, stage in item, stages, main stages, k blocks
+  int p, rt;
+  bool done;
+  const uint8_t* codes;
+  const int8_t* absq;
+  const float* step;
+  const float* mean;
+  const __nv_bfloat16* x;
+  const __nv_bfloat16* st;
+  int n, k, m, r;
+};
+
+__device__ __forceinline__ void gv_set_item(const GvParams& p, GvWalk& w) {
+  const int item = blockIdx.x + w.j * gridDim.x;
+  w.done = item >= p.total_items;
+  if (w.done) return;
+  w.p = gv_find_prob(p, item);
+  const GvProb& pr = p.prob[w.p];
+  w.rt = item - pr.item0;
+  w.codes = pr.codes;
+  w.absq = pr.absq;
+  w.step = pr.step;
+  w.mean = pr.mean;
+  w.x = pr.x;
+  w.st = pr.st;
+  w.n = pr.n;
+  w.k = pr.k;
+  w.m = pr.m;
+  w.r = pr.r;
+  w.kb = pr.k / 64;
+  w.nmain = (w.kb + 1) / 2;
+  w.nst = w.nmain + 1;  // one LoRA stage: r <= 128 = two 64-wide j blocks
+  w.l = 0;
+}
+
+__device__ __forceinline__ void gv_begin(const GvParams& p, GvWalk& w) {
+  w.j = 0;
+  gv_set_item(p, w);
+}
+
+__device__ __forceinline__ void gv_next(const GvParams& p, GvWalk& w) {
+  if (++w.l >= w.nst) {
+    ++w.j;
+    gv_set_item(p, w);
+  }
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gptr) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t saddr, const void* gptr) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(saddr), "l"(gptr) : "memory");
+}
+__device__ __forceinline__ void cp_async16_zfill(uint32_t saddr, const void* gptr, bool valid) {
+  const int src = valid ? 16 : 0;  // 0 source bytes: the 16 destination bytes are zero-filled
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(gptr), "r"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t saddr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(saddr));
+  return v;
+}
+__device__ __forceinline__ void sts_u32(uint32_t saddr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
+}
+
+// Prefetch this thread's share of stage `w` into the slot at `sa`: half h takes
+// k block 2l+h of row `row`, and activation slice (token tt/8, chunk tt%8) of
+// slab h.  Always commits one cp.async group.
+__device__ __forceinline__ void gv_prefetch(const GvWalk& w, int half, int rlocal, int tt, uint32_t sa) {
+  uint32_t meta = 0;
+  if (!w.done) {
+    meta = kMetaValid | (static_cast<uint32_t>(w.p) << 16) | (w.l == w.nst - 1 ? kMetaLast : 0u);
+    const int tok = tt >> 3, ch = tt & 7;
+    const int row = w.rt * 128 + rlocal;
+    if (w.l < w.nmain) {
+      const int blk = 2 * w.l + half;
+      const bool kin = blk < w.kb;
+      if (kin && row < w.n) {
+        const uint8_t* cp = w.codes + static_cast<int64_t>(row) * (w.k / 2) + blk * 32;
+        cp_async16(sa, cp);
+        cp_async16(sa + 16, cp + 16);
+        const int64_t ai = static_cast<int64_t>(row) * w.kb + blk;
+        cp_async4(sa + 48, w.absq + (ai & ~int64_t(3)));
+        cp_async4(sa + 52, w.step + (ai >> 8));
+        cp_async4(sa + 56, w.mean);
+        meta |= kMetaRowOk | (static_cast<uint32_t>(ai & 3) << 3);
+      }
+      const bool v = kin && tok < w.m;
+      cp_async16_zfill(sa + 32, w.x + (v ? static_cast<int64_t>(tok) * w.k + blk * 64 + ch * 8 : 0), v);
+    } else {
+      meta |= kMetaLora;
+      const int jb = half * 64;
+      if (row < w.n && jb < w.r) meta |= kMetaRowOk;
+      const int col = jb + ch * 8;
+      const bool v = tok < w.m && col < w.r;
+      cp_async16_zfill(sa + 32, w.st + (v ? static_cast<int64_t>(tok) * w.r + col : 0), v);
+    }
+  }
+  sts_u32(sa + 60, meta);
+  cp_async_commit();
+}
+
+__global__ void __launch_bounds__(kGvThreads, 2) k_qgemv_grouped(const __grid_constant__ GvParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sb = smem;                             // [kGvStages][2 slabs][16 rows][128 B]
+  uint8_t* slots = smem + kGvStages * kGvBBytes;  // [kGvPrefetch][256 threads][kGvSlot]
+  uint64_t* full = reinterpret_cast<uint64_t*>(slots + 256 * kGvPrefetch * kGvSlot);
+  uint64_t* empty = full + kGvStages;
+  uint64_t* acc_full = empty + kGvStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  volatile int* vabort = abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGvStages; ++s) {
+      mbar_init(&full[s], 256);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 256);
+    }
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(tmem_holder, kGvTmemCols);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, kGvTok, 0, 0);
+      int j = 0, g = 0;
+      while (blockIdx.x + j * gridDim.x < p.total_items) {
+        const int pi = gv_find_prob(p, blockIdx.x + j * gridDim.x);
+        const int nst = (p.prob[pi].k / 64 + 1) / 2 + 1;
+        const int buf = j & 1;
+        if (!mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.wait_ns, vabort)) {
+          abort_cta(p.status, abort_flag);
+          break;
+        }
+        bool ok = true;
+        for (int l = 0; l < nst; ++l, ++g) {
+          const int s = g % kGvStages;
+          if (!mbar_wait(&full[s], (g / kGvStages) & 1, p.wait_ns, vabort)) {
+            abort_cta(p.status, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t b_addr = smem_u32(sb + s * kGvBBytes);
+          const uint32_t d_tmem = tbase + kGvDCol + buf * kGvTok;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t bdesc = sdesc_sw128(b_addr + (kk >> 2) * (kGvTok * 128) + (kk & 3) * 32, 16, 1024);
+            mma_bf16_ts(d_tmem, tbase + s * 64 + kk * 8, bdesc, idesc, (l > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[buf]);
+        ++j;
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ producers (+ deferred epilogue)
+    const int half = (warp - 1) >> 2;              // k block 2l + half of each stage
+    const int quarter = warp & 3;                  // TMEM lanes this warp may touch
+    const int rlocal = quarter * 32 + lane;        // row within the 128-row tile
+    const int t = threadIdx.x - 32;                // slot index 0..255
+    const int tt = ((warp - 1) & 3) * 32 + lane;   // activation slice 0..127 of slab `half`
+    const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t slot0 = smem_u32(slots) + t * kGvSlot;
+    auto slot_addr = [&](int u) { return slot0 + static_cast<uint32_t>(u % kGvPrefetch) * 256 * kGvSlot; };
+
+    GvWalk pre;
+    gv_begin(p, pre);
+    for (int u = 0; u < kGvPrefetch; ++u) {
+      gv_prefetch(pre, half, rlocal, tt, slot_addr(u));
+      if (!pre.done) gv_next(p, pre);
+    }
+
+    auto drain = [&](int jd) {
+      const int buf = jd & 1;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (jd >> 1) & 1, p.wait_ns, vabort));
+      ok = __all_sync(0xffffffffu, ok && !*vabort);
+      if (ok) {
+        tc_fence_after();
+        const int item = blockIdx.x + jd * gridDim.x;
+        const int pi = gv_find_prob(p, item);
+        const GvProb& pr = p.prob[pi];
+        const int row = (item - pr.item0) * 128 + rlocal;
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld_32x32b_x16(tbase + lane_field + kGvDCol + buf * kGvTok, v);
+        tmem_ld_wait();
+        if (row < pr.n) {
+          __nv_bfloat16* yrow = pr.y + row;
+          const int m = pr.m, n = pr.n;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float val = __uint_as_float(half ? v[8 + i] : v[i]);
+            const int tok = half * 8 + i;
+            if (tok < m) yrow[static_cast<int64_t>(tok) * n] = __float2bfloat16_rn(val);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+      return ok;
+    };
+
+    int u = 0, j = 0;
+    bool alive = true;
+    while (alive) {
+      cp_async_wait<kGvPrefetch - 1>();
+      const uint32_t sa = slot_addr(u);
+      const uint32_t meta = lds_u32(sa + 60);
+      if (!(meta & kMetaValid)) break;
+      const int s = u % kGvStages;
+      const uint32_t ph = (u / kGvStages) & 1;
+      const uint4 act = lds_v4(sa + 32);
+      uint32_t words[32];
+      if (!(meta & kMetaRowOk)) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) words[c] = 0;
+      } else if (!(meta & kMetaLora)) {
+        const uint4 c0 = lds_v4(sa), c1 = lds_v4(sa + 16);
+        const uint32_t qw = lds_u32(sa + 48);
+        const int8_t qv = static_cast<int8_t>((qw >> (8 * ((meta >> 3) & 3))) & 0xffu);
+        const float a2 = restore_absmax(qv, __uint_as_float(lds_u32(sa + 52)), __uint_as_float(lds_u32(sa + 56)));
+        nf4_decode_block(c0, c1, a2, words);
+      } else {
+        const GvProb& pr = p.prob[meta >> 16];
+        const int row = (blockIdx.x + j * gridDim.x - pr.item0) * 128 + rlocal;
+        const uint32_t* brow = reinterpret_cast<const uint32_t*>(pr.lora_b + static_cast<int64_t>(row) * pr.r);
+        const int jb = half * 64;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) words[c] = (jb + 2 * c < pr.r) ? __ldg(brow + ((jb >> 1) + c)) : 0u;
+      }
+      // refill the slot with the stage kGvPrefetch ahead (its contents are in registers now)
+      __syncwarp();
+      gv_prefetch(pre, half, rlocal, tt, sa);
+      if (!pre.done) gv_next(p, pre);
+
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort));
+      if (!ok) {
+        if (lane == 0) abort_cta(p.status, abort_flag);
+        alive = false;
+        break;
+      }
+      tc_fence_after();
+      sts_v4(smem_u32(sb + s * kGvBBytes) + half * (kGvTok * 128) + sw128_offset(tt >> 3, tt & 7), act.x, act.y,
+             act.z, act.w);
+      fence_proxy_async_smem();
+      __syncwarp();
+      tmem_st_32x32b_x32(tbase + lane_field + s * 64 + half * 32, words);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&full[s]);
+      ++u;
+      if (meta & kMetaLast) {
+        // item j is fully produced: drain item j - 1 (its MMAs are done or nearly)
+        if (j >= 1 && !drain(j - 1)) alive = false;
+        ++j;
+      }
+    }
+    if (alive && j >= 1) drain(j - 1);
+    cp_async_wait<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, kGvTmemCols);
+  }
+}
+
+// ====================================================================== host
+static_assert(sizeof(GvParams) <= 32000, "kernel parameter budget");
+static_assert(sizeof(GlParams) <= 32000, "kernel parameter budget");
+
+int fwd_grouped_max_problems() { return kGvMaxProbs; }
+
+cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws, unsigned* status, uint64_t wait_ns,
+                               int num_sms, cudaStream_t s) {
+  static GvParams gv;  // host staging of the by-value parameter block (not thread safe by design: one caller)
+  static GlParams gl;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lk(mu);
+  memset(&gv, 0, sizeof(gv));
+  memset(&gl, 0, sizeof(gl));
+  char* base = static_cast<char*>(ws);
+  size_t off = 0;
+  int items = 0, rmax = 8;
+  for (int i = 0; i < count; ++i) {
+    const GroupedProblem& q = probs[i];
+    __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(base + off);
+    off += (static_cast<size_t>(q.m) * q.r * 2 + 255) & ~size_t(255);
+    GvProb& g = gv.prob[i];
+    g.codes = q.w.codes;
+    g.absq = q.w.absq;
+    g.step = q.w.step;
+    g.mean = q.w.mean;
+    g.x = q.x;
+    g.lora_b = q.lora_b;
+    g.st = st;
+    g.y = q.y;
+    g.n = static_cast<int>(q.w.n);
+    g.k = static_cast<int>(q.w.k);
+    g.m = q.m;
+    g.r = q.r;
+    g.item0 = items;
+    items += (g.n + 127) / 128;
+    GlProb& l = gl.prob[i];
+    l.x = q.x;
+    l.a = q.lora_a;
+    l.st = st;
+    l.t_save = q.t_save;
+    l.m = q.m;
+    l.k = g.k;
+    l.r = q.r;
+    l.scale = q.alpha / static_cast<float>(q.r);
+    if (q.r > rmax) rmax = q.r;
+  }
+  gv.count = count;
+  gv.total_items = items;
+  gv.wait_ns = wait_ns;
+  gv.status = status;
+  gl.count = count;
+  cudaError_t e;
+  if (rmax <= 16) {
+    e = set_smem_limit_once(k_lora_down_grouped<2>, 16 * 16 * 16 * 4);
+    if (e == cudaSuccess) k_lora_down_grouped<2><<<count, 512, 16 * 16 * 16 * 4, s>>>(gl);
+  } else if (rmax <= 32) {
+    e = set_smem_limit_once(k_lora_down_grouped<4>, 16 * 16 * 32 * 4);
+    if (e == cudaSuccess) k_lora_down_grouped<4><<<count, 512, 16 * 16 * 32 * 4, s>>>(gl);
+  } else {
+    e = set_smem_limit_once(k_lora_down_grouped<8>, 16 * 16 * 64 * 4);
+    if (e == cudaSuccess) k_lora_down_grouped<8><<<count, 512, 16 * 16 * 64 * 4, s>>>(gl);
+  }
+  if (e != cudaSuccess) return e;
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  e = set_smem_limit_once(k_qgemv_grouped, kGvSmem);
+  if (e != cudaSuccess) return e;
+  int grid = 2 * num_sms;
+  if (grid > items) grid = items;
+  k_qgemv_grouped<<<grid, kGvThreads, kGvSmem, s>>>(gv);
+  return cudaGetLastError();
+}
+
+size_t fwd_grouped_workspace_bytes(const GroupedProblem* probs, int count) {
+  size_t off = 0;
+  for (int i = 0; i < count; ++i) off += (static_cast<size_t>(probs[i].m) * probs[i].r * 2 + 255) & ~size_t(255);
+  return off;
+}
+
+}  // namespace qlora

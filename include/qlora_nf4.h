@@ -169,6 +169,36 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
                      uint16_t* dx, float* da, float* db, int flags, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/*
+ * One small-token forward problem of a grouped call (host struct; the
+ * pointers in it are device pointers, `w` points to a host record struct).
+ */
+typedef struct qlora_linear_problem {
+  const uint16_t* x;           /* bf16 [m, k], 1 <= m <= 16 */
+  int64_t m;
+  const qlora_nf4_weight* w;   /* [n, k] */
+  const uint16_t* lora_a;      /* bf16 [r, k] */
+  const uint16_t* lora_b;      /* bf16 [n, r] */
+  int r;                       /* 8 <= r <= 64, r % 8 == 0 */
+  float alpha;
+  uint16_t* y;                 /* bf16 [m, n] (overwritten) */
+  float* t_save;               /* f32 [m, r] = X A^T, or NULL */
+} qlora_linear_problem;
+
+/* Bytes of workspace qlora_linear_fwd_grouped needs for this list. */
+int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problems, int count, size_t* bytes);
+
+/*
+ * qlora_linear_fwd for a list of independent small-token problems (decode:
+ * each matrix of a layer stack applied to 1..16 tokens), in two kernel
+ * launches per 300 problems: all X A^T products, then one pass that streams
+ * every weight of the list.  Same arithmetic as qlora_linear_fwd (bf16
+ * operands, fp32 accumulation, s X A^T rounded to bf16); every y is written
+ * once, deterministically.  `problems` is a host array of `count` entries.
+ */
+int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
 /* ----------------------------------------------------------------- MLP glue */
 
 /*
