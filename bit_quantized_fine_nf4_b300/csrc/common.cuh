@@ -88,6 +88,15 @@ __device__ __forceinline__ void abort_cta(unsigned* status, int* abort_flag) {
   *reinterpret_cast<volatile int*>(abort_flag) = 1;
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Let the next kernel in the stream start launching now (it still has to wait
+// with griddep_wait before it reads anything this grid writes).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one depends on have completed and their writes are visible.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ proxies / fences
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(256) k_lora_down(const __nv_bfloat16* __restri
   constexpr int RP = NT * 8;
   extern __shared__ float s_red[];  // [8 warps][16 rows][RP]
   __shared__ int s_last;
+  // the GEMM that consumes this kernel's output only needs it for its last k block
+  griddep_launch_dependents();
   if (cvt_n > 0) {
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * gridDim.y * blockDim.x;
     const int64_t tid = (static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
@@ -79,7 +81,8 @@ __global__ void __launch_bounds__(256) k_lora_down(const __nv_bfloat16* __restri
   const uint4 zero = make_uint4(0, 0, 0, 0);
   const __nv_bfloat16* ina = in + static_cast<int64_t>(rowa) * K;
   const __nv_bfloat16* inb = in + static_cast<int64_t>(rowb) * K;
-  constexpr int UNROLL = NT <= 2 ? 4 : 2;  // chunks whose loads are in flight together
+  // chunks whose loads are in flight together (the strided B gathers cost registers)
+  constexpr int UNROLL = (NT <= 2 && MT_KMAJOR) ? 4 : 2;
   for (int c = 8 * blockIdx.y + warp; c < n_chunks; c += UNROLL * stride) {
     uint4 xa[UNROLL], xb[UNROLL], bv[UNROLL][NT];
 #pragma unroll

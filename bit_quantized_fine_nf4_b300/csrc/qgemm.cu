@@ -18,7 +18,8 @@
 //   accumulator.  Optional split-K with a fixed-order reduction (decode shapes).
 // k_qgemm_wb  (backward dX)
 //   D[m, k] = sum_n dY[m, n] deq(W)[n, k]  +  sum_j sU[m, j] A[j, k]
-//   A operand = 128 token rows of dY (then sU = bf16(s dY B)), TMA;
+//   A operand = 2 x 128 token rows of dY (then sU = bf16(s dY B)), TMA, two
+//               accumulators sharing each dequantised B block;
 //   B operand = deq(W)[n-block of 64, 256 output columns], MN-major 128B swizzle,
 //               written by the producers with st.shared (then LoRA A rows, TMA).
 // k_lora_grad (LoRA gradients, both MN-major operands, HBM-bound)
@@ -27,6 +28,7 @@
 
 #include <cstdio>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -50,7 +52,8 @@ struct WaParams {
   unsigned long long wait_ns;
 };
 
-constexpr int kWaThreads = 320;  // warp 0: TMA + TMEM alloc, warp 1: MMA, warps 2..9: producers / epilogue
+constexpr int kWaTeams = 4;      // producer teams (4 warps each) taking k blocks round-robin
+constexpr int kWaThreads = 64 + kWaTeams * 128;  // warp 0: TMA + TMEM alloc, warp 1: MMA, then the producer teams
 
 template <int NTOK, int STAGES>
 struct WaCfg {
@@ -114,6 +117,7 @@ __global__ void __launch_bounds__(kWaThreads, 1)
         const int s = i % STAGES;
         const uint32_t ph = (i / STAGES) & 1;
         if (!mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
+        if (i == n_main) griddep_wait();  // sT is written by the preceding LoRA down kernel
         mbar_arrive_expect_tx(&full[s], Cfg::kBBytes);
         if (i < n_main)
           tma_load_2d(sb + s * Cfg::kBBytes, &tm_x, &full[s], (kb_begin + i) * 64, tok0);
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(kWaThreads, 1)
     const int kb_row = p.K / 64;
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
     bool alive = true;
-    for (int i = team; i < n_iter && alive; i += 2) {
+    for (int i = team; i < n_iter && alive; i += kWaTeams) {
       const int s = i % STAGES;
       const uint32_t ph = (i / STAGES) & 1;
       uint32_t words[32];
@@ -189,8 +193,10 @@ __global__ void __launch_bounds__(kWaThreads, 1)
     ok = ok && !*vabort;
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    const int col_lo = (NTOK <= 32) ? 0 : team * (NTOK / 2);
-    const int ncols = (NTOK <= 32) ? (team == 0 ? NTOK : 0) : NTOK / 2;
+    // column share of this team: NTOK / kWaTeams columns (all of them for team 0 when NTOK is small)
+    constexpr int kShare = (NTOK / kWaTeams) >= 16 ? NTOK / kWaTeams : NTOK;
+    const int col_lo = (kShare == NTOK) ? 0 : team * kShare;
+    const int ncols = (kShare == NTOK) ? (team == 0 ? NTOK : 0) : kShare;
     const uint32_t dcol = tbase + lane_field + Cfg::kDCol;
     if (ok) {
       if (p.splits == 1) {
@@ -223,9 +229,9 @@ __global__ void __launch_bounds__(kWaThreads, 1)
     }
     if (p.splits > 1) {
       __threadfence();
-      named_bar_sync(1, 256);
+      named_bar_sync(1, kWaTeams * 128);
       if (threadIdx.x == 64) *last_flag = (atomicAdd(p.counters + tile, 1u) == static_cast<unsigned>(p.splits - 1));
-      named_bar_sync(1, 256);
+      named_bar_sync(1, kWaTeams * 128);
       if (*reinterpret_cast<volatile int*>(last_flag)) {
         __threadfence();
         if (row_ok) {
@@ -265,8 +271,9 @@ struct WbParams {
   unsigned long long wait_ns;
 };
 
-constexpr int kWbThreads = 320;
-constexpr uint32_t kWbABytes = 128 * 128;      // 128 tokens x 64 n, bf16
+constexpr int kWbTeamThreads = 256;  // one team decodes a whole [64 n x 256 k] block: one 64-weight unit per thread
+constexpr int kWbThreads = 64 + 2 * kWbTeamThreads;  // warp 0 TMA + TMEM, warp 1 MMA, two producer teams
+constexpr uint32_t kWbABytes = 256 * 128;      // 256 tokens x 64 n, bf16 (two M = 128 halves)
 constexpr uint32_t kWbBBytes = 4 * 64 * 128;   // 4 slabs of [64 n rows x 64 k]
 constexpr uint32_t kWbStage = kWbABytes + kWbBBytes;
 
@@ -275,6 +282,9 @@ struct WbCfg {
   static constexpr size_t kSmem = 1024 + STAGES * kWbStage + (2 * STAGES + 1) * 8 + 16;
 };
 
+// Tile: 256 tokens x 256 output columns.  Each dequantised W block [64 n x 256 k]
+// feeds two M = 128 MMAs (tokens 0..127 and 128..255) into two TMEM
+// accumulators (columns 0..255 and 256..511), so the decode is shared by 256 tokens.
 template <int STAGES>
 __global__ void __launch_bounds__(kWbThreads, 1)
     k_qgemm_wb(const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_su,
@@ -289,13 +299,13 @@ __global__ void __launch_bounds__(kWbThreads, 1)
   volatile int* vabort = abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int k0 = blockIdx.x * 256, tok0 = blockIdx.y * 128;
+  const int k0 = blockIdx.x * 256, tok0 = blockIdx.y * 256;
   const int n_main = (p.N + 63) / 64;
   const int n_iter = n_main + p.lora_blocks;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1 + 128);
+      mbar_init(&full[s], 1 + kWbTeamThreads);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
@@ -304,7 +314,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
   }
   if (warp == 0) {
     __syncwarp();
-    tmem_alloc(tmem_holder, 256);
+    tmem_alloc(tmem_holder, 512);
   }
   tc_fence_before();
   __syncthreads();
@@ -326,6 +336,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
           tma_load_2d(sa, &tm_dy, &full[s], i * 64, tok0);
         } else {
           const int e = i - n_main;
+          if (e == 0) griddep_wait();  // sU is written by the preceding LoRA down kernel
           mbar_arrive_expect_tx(&full[s], kWbStage);
           tma_load_2d(sa, &tm_su, &full[s], e * 64, tok0);
 #pragma unroll
@@ -345,9 +356,10 @@ __global__ void __launch_bounds__(kWbThreads, 1)
         const uint32_t b_addr = a_addr + kWbABytes;
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t adesc = sdesc_sw128(a_addr + kk * 32, 16, 1024);
           const uint64_t bdesc = sdesc_sw128(b_addr + kk * 2048, 8192, 1024);
-          mma_bf16_ss(tbase, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          mma_bf16_ss(tbase, sdesc_sw128(a_addr + kk * 32, 16, 1024), bdesc, idesc, acc);
+          mma_bf16_ss(tbase + 256, sdesc_sw128(a_addr + 128 * 128 + kk * 32, 16, 1024), bdesc, idesc, acc);
         }
         mma_commit(&empty[s]);
       }
@@ -355,74 +367,63 @@ __global__ void __launch_bounds__(kWbThreads, 1)
     }
   } else {
     // ---------------------------------------------------------------- producers
-    const int team = (warp - 2) >> 2;
-    const int t = ((warp - 2) & 3) * 32 + lane;  // 0..127 within the team
+    const int team = (warp - 2) >> 3;                    // 0 or 1: k blocks of this parity
+    const int t = ((warp - 2) & 7) * 32 + lane;          // 0..255: unit within the block
+    const uint32_t rrow = t & 63, slab = t >> 6;         // weight row n - 64 i, 64-wide k slab
     const float mu = *p.mean;
     const int kb_row = p.K / 64;
+    const int kblk = (k0 >> 6) + slab;
     bool alive = true;
     for (int i = team; i < n_iter && alive; i += 2) {
       const int s = i % STAGES;
       const uint32_t ph = (i / STAGES) & 1;
       const bool is_main = i < n_main;
-      uint4 c[2][2];
-      float a2[2];
-      bool uok[2];
-      if (is_main) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int u = t + h * 128;
-          const int rrow = u & 63, slab = u >> 6;
-          const int n = i * 64 + rrow;
-          const int kblk = (k0 >> 6) + slab;
-          uok[h] = (n < p.N) && (kblk < kb_row);
-          if (uok[h]) {
-            const uint8_t* cp = p.codes + static_cast<int64_t>(n) * (p.K / 2) + kblk * 32;
-            c[h][0] = ldg_nc_v4(cp);
-            c[h][1] = ldg_nc_v4(cp + 16);
-            const int64_t ai = static_cast<int64_t>(n) * kb_row + kblk;
-            a2[h] = restore_absmax(p.absq[ai], p.step[ai >> 8], mu);
-          }
-        }
+      uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
+      float a2 = 0.f;
+      const int n = i * 64 + rrow;
+      const bool uok = is_main && (n < p.N) && (kblk < kb_row);
+      if (uok) {
+        const uint8_t* cp = p.codes + static_cast<int64_t>(n) * (p.K / 2) + kblk * 32;
+        c0 = ldg_nc_v4(cp);
+        c1 = ldg_nc_v4(cp + 16);
+        const int64_t ai = static_cast<int64_t>(n) * kb_row + kblk;
+        a2 = restore_absmax(p.absq[ai], p.step[ai >> 8], mu);
       }
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort));
       if (!ok) { if (lane == 0) abort_cta(p.status, abort_flag); alive = false; break; }
       if (is_main) {
-        const uint32_t sbase = smem_u32(smem + s * kWbStage + kWbABytes);
+        uint32_t words[32];
+        if (uok) {
+          nf4_decode_block(c0, c1, a2, words);
+        } else {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int u = t + h * 128;
-          const uint32_t rrow = u & 63, slab = u >> 6;
-          uint32_t words[32];
-          if (uok[h]) {
-            nf4_decode_block(c[h][0], c[h][1], a2[h], words);
-          } else {
-#pragma unroll
-            for (int q = 0; q < 32; ++q) words[q] = 0;
-          }
-          const uint32_t slab_base = sbase + slab * 8192;
-#pragma unroll
-          for (int ch = 0; ch < 8; ++ch)
-            sts_v4(slab_base + sw128_offset(rrow, ch), words[4 * ch], words[4 * ch + 1], words[4 * ch + 2],
-                   words[4 * ch + 3]);
+          for (int q = 0; q < 32; ++q) words[q] = 0;
         }
+        const uint32_t slab_base = smem_u32(smem + s * kWbStage + kWbABytes) + slab * 8192;
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          sts_v4(slab_base + sw128_offset(rrow, ch), words[4 * ch], words[4 * ch + 1], words[4 * ch + 2],
+                 words[4 * ch + 3]);
         fence_proxy_async_smem();
       }
       mbar_arrive(&full[s]);
     }
     // ---------------------------------------------------------------- epilogue
+    // the four warps of each TMEM lane quarter share its 2 accumulators x 8 column chunks
     bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, p.wait_ns, vabort));
     ok = ok && !*vabort;
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     const int quarter = warp & 3;
+    const int wq = (warp - 2) >> 2;  // 0..3 among the warps of this quarter
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-    const int tok = tok0 + quarter * 32 + lane;
     if (ok) {
-      for (int cc = 0; cc < 128; cc += 32) {
-        const int col = team * 128 + cc;
+      for (int chunk = wq; chunk < 16; chunk += 4) {
+        const int acc = chunk >> 3, col = (chunk & 7) * 32;
+        const int tok = tok0 + acc * 128 + quarter * 32 + lane;
         uint32_t v[32];
         __syncwarp();
-        tmem_ld_32x32b_x32(tbase + lane_field + col, v);
+        tmem_ld_32x32b_x32(tbase + lane_field + acc * 256 + col, v);
         tmem_ld_wait();
         const int kc = k0 + col;
         if (tok < p.M && kc < p.K) {
@@ -453,7 +454,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tbase, 256);
+    tmem_dealloc(tbase, 512);
   }
 }
 
@@ -472,14 +473,14 @@ struct LgParams {
 };
 
 constexpr int kLgThreads = 192;  // warp 0 TMA + TMEM, warp 1 MMA, warps 2..5 epilogue
-constexpr int kLgStages = 4;
 
 template <int RP>  // MMA N: 64 or 128
 struct LgCfg {
   static constexpr uint32_t kABytes = 2 * 8192;           // [64 m x 128 c] as two 64-wide slabs
   static constexpr uint32_t kBBytes = (RP / 64) * 8192;   // [64 m x RP j]
   static constexpr uint32_t kStage = kABytes + kBBytes;
-  static constexpr size_t kSmem = 1024 + kLgStages * kStage + (2 * kLgStages + 1) * 8 + 16;
+  static constexpr int kStages = RP == 64 ? 8 : 6;        // deep ring: one CTA streams every token
+  static constexpr size_t kSmem = 1024 + kStages * kStage + (2 * kStages + 1) * 8 + 16;
 };
 
 template <int RP>
@@ -488,6 +489,7 @@ __global__ void __launch_bounds__(kLgThreads, 1)
                 const __grid_constant__ CUtensorMap tm_su, const __grid_constant__ CUtensorMap tm_st,
                 const LgParams p) {
   using Cfg = LgCfg<RP>;
+  constexpr int kLgStages = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kLgStages * Cfg::kStage);
@@ -589,12 +591,17 @@ __global__ void __launch_bounds__(kLgThreads, 1)
         __syncwarp();
         tmem_ld_32x32b_x16(tbase + lane_field + j0, v);
         tmem_ld_wait();
+        if (p.splits > 1) {
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const int j = j0 + jj;
-          if (j >= p.r) break;
-          if (p.splits > 1) mine[j] = __uint_as_float(v[jj]);
-          else if (c < C) store(j, __uint_as_float(v[jj]));
+          for (int jj = 0; jj < 16; jj += 4)
+            if (j0 + jj < p.r)
+              *reinterpret_cast<float4*>(mine + j0 + jj) =
+                  make_float4(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1]), __uint_as_float(v[jj + 2]),
+                              __uint_as_float(v[jj + 3]));
+        } else if (c < C) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            if (j0 + jj < p.r) store(j0 + jj, __uint_as_float(v[jj]));
         }
       }
     }
@@ -607,12 +614,29 @@ __global__ void __launch_bounds__(kLgThreads, 1)
       if (*reinterpret_cast<volatile int*>(last_flag)) {
         __threadfence();
         if (c < C) {
-          for (int j = 0; j < p.r; ++j) {
-            float acc = 0.f;
-            for (int sp = 0; sp < p.splits; ++sp)
-              acc += __ldcg(p.partial + (static_cast<int64_t>(sp) * p.tiles + tile) * 128 * p.r +
-                            (quarter * 32 + lane) * p.r + j);
-            store(j, acc);
+          // 16 columns at a time: issue every partial load first (one L2 round trip), then add in split order
+          for (int j0 = 0; j0 < p.r; j0 += 16) {
+            float acc[16];
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.f;
+            for (int sp = 0; sp < p.splits; ++sp) {
+              const float4* src = reinterpret_cast<const float4*>(
+                  p.partial + (static_cast<int64_t>(sp) * p.tiles + tile) * 128 * p.r + (quarter * 32 + lane) * p.r + j0);
+              float4 v4[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                v4[q] = (j0 + 4 * q < p.r) ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);  // stay inside the row
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                acc[4 * q] += v4[q].x;
+                acc[4 * q + 1] += v4[q].y;
+                acc[4 * q + 2] += v4[q].z;
+                acc[4 * q + 3] += v4[q].w;
+              }
+            }
+#pragma unroll
+            for (int jj = 0; jj < 16; ++jj)
+              if (j0 + jj < p.r) store(j0 + jj, acc[jj]);
           }
         }
         if (threadIdx.x == 64) p.counters[tile] = 0;
@@ -711,13 +735,33 @@ size_t fwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
   return pl.splits * tiles * 128 * pl.ntok * sizeof(float) + tiles * 4 + 256;
 }
 
+// Launch with programmatic stream serialization: the kernel may start while the
+// preceding kernel of the stream (the LoRA down-projection) still runs; it
+// waits for it (griddep_wait) only before loading that kernel's output.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int NTOK, int STAGES>
 static cudaError_t run_wa(const CUtensorMap& tx, const CUtensorMap& tst, const WaParams& prm, dim3 grid,
                           cudaStream_t s) {
   using Cfg = WaCfg<NTOK, STAGES>;
   cudaError_t e = set_smem_limit_once(k_qgemm_wa<NTOK, STAGES>, Cfg::kSmem);
   if (e != cudaSuccess) return e;
-  k_qgemm_wa<NTOK, STAGES><<<grid, kWaThreads, Cfg::kSmem, s>>>(tx, tst, prm);
+  e = launch_pdl(k_qgemm_wa<NTOK, STAGES>, grid, dim3(kWaThreads), Cfg::kSmem, s, tx, tst, prm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -765,8 +809,8 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
                                unsigned* status, uint64_t wait_ns, cudaStream_t s) {
   const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
   CUtensorMap tdy, tsu, tla;
-  if (!make_tm(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 128)) return cudaErrorInvalidValue;
-  if (!make_tm(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tm(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 256)) return cudaErrorInvalidValue;
+  if (!make_tm(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 256)) return cudaErrorInvalidValue;
   if (!make_tm(&tla, lora_a, K, r, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
   WbParams prm;
   prm.codes = w.codes;
@@ -782,12 +826,13 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
   prm.lora_blocks = (r + 63) / 64;
   prm.accumulate = accumulate;
   prm.wait_ns = wait_ns;
-  constexpr int kStages = 4;
+  constexpr int kStages = 3;
   const size_t smem = WbCfg<kStages>::kSmem;
   cudaError_t e = set_smem_limit_once(k_qgemm_wb<kStages>, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((K + 255) / 256, (M + 127) / 128);
-  k_qgemm_wb<kStages><<<grid, kWbThreads, smem, s>>>(tdy, tsu, tla, prm);
+  const dim3 grid((K + 255) / 256, (M + 255) / 256);
+  e = launch_pdl(k_qgemm_wb<kStages>, grid, dim3(kWbThreads), smem, s, tdy, tsu, tla, prm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -799,10 +844,10 @@ static LgPlan plan_lg(int M, int N, int K, int num_sms) {
   pl.tiles_a = (K + 127) / 128;
   pl.tiles = pl.tiles_a + (N + 127) / 128;
   const int n_iter = (M + 63) / 64;
-  // grow the split while the doubled grid still fits in one wave (two CTAs per SM)
-  // and every split keeps >= 8 m-blocks, so each CTA's 4-stage ring stays full
+  // split over tokens only while the doubled grid still fits one wave (one CTA
+  // per SM with the deep ring) and every split keeps >= 16 m-blocks
   int splits = 1;
-  while (pl.tiles * splits * 2 <= 2 * num_sms && splits * 2 * 8 <= n_iter) splits *= 2;
+  while (pl.tiles * splits * 2 <= num_sms && splits * 2 * 16 <= n_iter) splits *= 2;
   pl.iters = (n_iter + splits - 1) / splits;
   pl.splits = (n_iter + pl.iters - 1) / pl.iters;
   return pl;
