@@ -295,10 +295,13 @@ int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, co
   const int M = static_cast<int>(m), N = static_cast<int>(w->n), K = static_cast<int>(w->k);
   cudaError_t e;
   {
+    // T = X A^T on the SMs the GEMM's last wave leaves idle; the GEMM starts
+    // beside it and waits for T only before its LoRA k block
     Span sp(P_LORA_DOWN, s, 1);
+    const int cap = qlora::idle_sms_beside(qlora::fwd_gemm_ctas(M, N, K, di->num_sms), di->num_sms);
     e = qlora::launch_lora_down(reinterpret_cast<const __nv_bfloat16*>(x),
                                 reinterpret_cast<const __nv_bfloat16*>(lora_a), 1, M, K, r, scale, t_save, st,
-                                base + ws.st, di->num_sms, s);
+                                base + ws.st, cap, s);
   }
   if (e != cudaSuccess) return cuda_ret(e, "lora_down");
   {
@@ -307,7 +310,6 @@ int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, co
                              reinterpret_cast<const __nv_bfloat16*>(lora_b), r, reinterpret_cast<__nv_bfloat16*>(y),
                              base + ws.st + ws.ld, di->status, g_wait_ns.load(), di->num_sms, s);
   }
-  (void)N;
   return cuda_ret(e, "fwd_gemm");
 }
 
@@ -358,6 +360,10 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
   const __nv_bfloat16* dyb = reinterpret_cast<const __nv_bfloat16*>(dy);
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
   cudaError_t e;
+  // Order: U (all SMs) -> dA, dB (on the SMs the dX GEMM's last wave leaves
+  // idle) -> dX GEMM.  The last two start early (programmatic dependent launch)
+  // and wait for their predecessor only before they read its output, so the
+  // gradient kernel runs beside the GEMM instead of after it.
   {
     // U = dY B (B read as stored) and, in the same launch, sT = bf16(s * t_save)
     Span sp(P_LORA_DOWN, s, 1);
@@ -366,18 +372,19 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
   }
   if (e != cudaSuccess) return cuda_ret(e, "lora_down (U)");
   {
+    Span sp(P_LORA_GRADS, s, 1);
+    const int cap = qlora::idle_sms_beside(qlora::bwd_gemm_ctas(M, N, K), di->num_sms);
+    e = qlora::launch_lora_grads(xb, dyb, su, st, M, N, K, r, da, db, (flags & QLORA_ACCUM_DA) ? 1 : 0,
+                                 (flags & QLORA_ACCUM_DB) ? 1 : 0, lgws, di->status, wait, cap, s);
+  }
+  if (e != cudaSuccess) return cuda_ret(e, "lora grads");
+  {
     Span sp(P_BWD_GEMM, s, 1);
     e = qlora::launch_bwd_dx_gemm(dyb, M, to_dev(w), su, reinterpret_cast<const __nv_bfloat16*>(lora_a), r,
                                   reinterpret_cast<__nv_bfloat16*>(dx), (flags & QLORA_ACCUM_DX) ? 1 : 0, di->status,
                                   wait, s);
   }
-  if (e != cudaSuccess) return cuda_ret(e, "bwd dx gemm");
-  {
-    Span sp(P_LORA_GRADS, s, 1);
-    e = qlora::launch_lora_grads(xb, dyb, su, st, M, N, K, r, da, db, (flags & QLORA_ACCUM_DA) ? 1 : 0,
-                                 (flags & QLORA_ACCUM_DB) ? 1 : 0, lgws, di->status, wait, di->num_sms, s);
-  }
-  return cuda_ret(e, "lora grads");
+  return cuda_ret(e, "bwd dx gemm");
 }
 
 int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problems, int count, size_t* bytes) {

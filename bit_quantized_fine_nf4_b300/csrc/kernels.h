@@ -27,12 +27,12 @@ cudaError_t launch_nf4_dequantize(const uint8_t* codes, const int8_t* absq, cons
                                   uint16_t* out, int64_t n_elems, int num_sms, cudaStream_t s);
 
 // lora_small.cu
-int lora_down_splits(int M, int K, int num_sms);
 size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms);
-// out = in . mt^T with mt either [r, K] (mt_kmajor) or [K, r]; optional side job
-// cvt_dst[i] = bf16(cvt_scale * cvt_src[i]) for i < cvt_n in the same launch.
+// out = in . mt^T with mt either [r, K] (mt_kmajor) or [K, r], by at most
+// max_ctas persistent CTAs; optional side job cvt_dst[i] = bf16(cvt_scale *
+// cvt_src[i]) for i < cvt_n in the same launch.
 cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int mt_kmajor, int M, int K, int r,
-                             float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int num_sms,
+                             float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int max_ctas,
                              cudaStream_t s, const float* cvt_src = nullptr, __nv_bfloat16* cvt_dst = nullptr,
                              int64_t cvt_n = 0, float cvt_scale = 1.0f);
 cudaError_t launch_silu_mul_fwd(const uint16_t* g, const uint16_t* u, uint16_t* h, int64_t n, int num_sms,
@@ -64,8 +64,12 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
 size_t lora_grads_workspace_bytes(int M, int N, int K, int r, int num_sms);
 cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __nv_bfloat16* su,
                               const __nv_bfloat16* st, int M, int N, int K, int r, float* da, float* db,
-                              int accum_da, int accum_db, void* ws, unsigned* status, uint64_t wait_ns, int num_sms,
+                              int accum_da, int accum_db, void* ws, unsigned* status, uint64_t wait_ns, int max_ctas,
                               cudaStream_t s);
+// Grid sizes of the GEMMs and the SMs they leave idle (budget for side kernels).
+int fwd_gemm_ctas(int M, int N, int K, int num_sms);
+int bwd_gemm_ctas(int M, int N, int K);
+int idle_sms_beside(int gemm_ctas, int num_sms);
 
 // Grouped small-token forward (qgemv_grouped.cu): one problem of the list.
 struct GroupedProblem {

@@ -8,9 +8,10 @@
 //   forward:  T = X A^T   (mt = A, [r, K])
 //   backward: U = dY B    (mt = B as stored, [N, r])
 // The contraction is HBM-bound (one read of `in`, r <= 128 outputs per row),
-// so it runs on the warp-level mma.sync path with 16-byte loads; the K range
-// is split over the 8 warps of a CTA and over CTAs, and the partial sums are
-// added in a fixed order (deterministic).
+// so it runs on the warp-level mma.sync path with 16-byte loads.  The grid is
+// persistent and capped by the caller (it runs on the SMs a GEMM leaves idle);
+// the K range of a 16-row tile is split over the warps of one CTA and the
+// partial sums are added in warp order (deterministic, no cross-CTA step).
 //
 // The SiLU * up glue between the MLP linears is not on the pages; it is the
 // plain definition h = silu(g) * u, evaluated in float32.
@@ -28,17 +29,17 @@ __device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, ui
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// CTA = 8 warps, 16 rows of `in`.  Warp w handles 32-wide k chunks c with
-// c % (8 * splits) == 8 * blockIdx.y + w, 4 (or 2 for r > 16) chunks per loop
-// trip so their loads are in flight together.  Within a chunk, thread (g, q) = (lane / 4,
-// lane % 4) loads 8 consecutive k (16 bytes) of rows g and g + 8, and the k
-// order inside the two m16n8k16 steps is permuted consistently for both
-// operands so each fragment register holds 2 consecutive k.
+// Persistent CTAs of W warps walk 16-row tiles of `in` (tile = blockIdx.x,
+// += gridDim.x); the W warps of a CTA split k (32-wide chunks, chunk c taken by
+// warp c % W, 4 or 2 chunks per loop trip so their loads are in flight
+// together) and add their partial sums in warp order.  Within a chunk, thread
+// (g, q) = (lane / 4, lane % 4) loads 8 consecutive k (16 bytes) of rows g and
+// g + 8, and the k order inside the two m16n8k16 steps is permuted the same way
+// for both operands so each fragment register holds 2 consecutive k.
 // MT_KMAJOR: mt is [r, K] (row j contiguous in k); otherwise mt is [K, r]
 // (the LoRA B matrix as stored) and each fragment gathers 8 strided values.
-// Side job (optional): every thread first converts a slice of cvt_src (f32)
-// to bf16(cvt_scale * v) in cvt_dst -- an independent elementwise pass that
-// rides along in the same launch.
+// Side job (optional): cvt_dst[i] = bf16(cvt_scale * cvt_src[i]), spread over
+// all threads of the grid -- an independent elementwise pass in the same launch.
 template <int NT, bool MT_KMAJOR>
 __device__ __forceinline__ uint4 load_mt_frag(const __nv_bfloat16* __restrict__ mt, int j, int kb, int K, int r) {
   if (MT_KMAJOR) return ldg_nc_v4(mt + static_cast<int64_t>(j) * K + kb);
@@ -49,111 +50,82 @@ __device__ __forceinline__ uint4 load_mt_frag(const __nv_bfloat16* __restrict__ 
   return make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
 }
 
-template <int NT, bool MT_KMAJOR>
-__global__ void __launch_bounds__(256) k_lora_down(const __nv_bfloat16* __restrict__ in,
-                                                   const __nv_bfloat16* __restrict__ mt, int M, int K, int r,
-                                                   int splits, float* __restrict__ partial,
-                                                   unsigned* __restrict__ counters, float scale,
-                                                   float* __restrict__ out_f32, __nv_bfloat16* __restrict__ out_bf16,
-                                                   const float* __restrict__ cvt_src, __nv_bfloat16* __restrict__ cvt_dst,
-                                                   int64_t cvt_n, float cvt_scale) {
+template <int NT, bool MT_KMAJOR, int W>
+__global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __restrict__ in,
+                                                      const __nv_bfloat16* __restrict__ mt, int M, int K, int r,
+                                                      float scale, float* __restrict__ out_f32,
+                                                      __nv_bfloat16* __restrict__ out_bf16,
+                                                      const float* __restrict__ cvt_src,
+                                                      __nv_bfloat16* __restrict__ cvt_dst, int64_t cvt_n,
+                                                      float cvt_scale) {
   constexpr int RP = NT * 8;
-  extern __shared__ float s_red[];  // [8 warps][16 rows][RP]
-  __shared__ int s_last;
+  extern __shared__ float s_red[];  // [W warps][16 rows][RP]
   // the GEMM that consumes this kernel's output only needs it for its last k block
   griddep_launch_dependents();
   if (cvt_n > 0) {
-    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * gridDim.y * blockDim.x;
-    const int64_t tid = (static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
-    for (int64_t i = tid; i < cvt_n; i += nthreads) cvt_dst[i] = __float2bfloat16_rn(__fmul_rn(cvt_src[i], cvt_scale));
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < cvt_n; i += nthreads)
+      cvt_dst[i] = __float2bfloat16_rn(__fmul_rn(cvt_src[i], cvt_scale));
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
-  const int m0 = blockIdx.x * 16;
-  const int rowa = m0 + g, rowb = m0 + g + 8;
-  float acc[NT][4];
-#pragma unroll
-  for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-
-  // K % 8 == 0: each thread's 8-element slice is either fully inside K or fully past it
-  const int n_chunks = (K + 31) / 32;
-  const int stride = 8 * splits;
+  const int n_chunks = (K + 31) / 32;  // K % 8 == 0: a thread's 8-wide slice is fully inside K or past it
+  const int tiles = (M + 15) / 16;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  const __nv_bfloat16* ina = in + static_cast<int64_t>(rowa) * K;
-  const __nv_bfloat16* inb = in + static_cast<int64_t>(rowb) * K;
-  // chunks whose loads are in flight together (the strided B gathers cost registers)
   constexpr int UNROLL = (NT <= 2 && MT_KMAJOR) ? 4 : 2;
-  for (int c = 8 * blockIdx.y + warp; c < n_chunks; c += UNROLL * stride) {
-    uint4 xa[UNROLL], xb[UNROLL], bv[UNROLL][NT];
+  for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int m0 = tile * 16;
+    const int rowa = m0 + g, rowb = m0 + g + 8;
+    const __nv_bfloat16* ina = in + static_cast<int64_t>(rowa) * K;
+    const __nv_bfloat16* inb = in + static_cast<int64_t>(rowb) * K;
+    float acc[NT][4];
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-      const int kb = (c + u * stride) * 32 + q * 8;
-      const bool kin = kb < K;
-      xa[u] = (kin && rowa < M) ? ldg_nc_v4(ina + kb) : zero;
-      xb[u] = (kin && rowb < M) ? ldg_nc_v4(inb + kb) : zero;
+    for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    for (int c = warp; c < n_chunks; c += UNROLL * W) {
+      uint4 xa[UNROLL], xb[UNROLL], bv[UNROLL][NT];
 #pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int j = t * 8 + g;
-        bv[u][t] = (kin && j < r) ? load_mt_frag<NT, MT_KMAJOR>(mt, j, kb, K, r) : zero;
+      for (int u = 0; u < UNROLL; ++u) {
+        const int kb = (c + u * W) * 32 + q * 8;
+        const bool kin = kb < K;
+        xa[u] = (kin && rowa < M) ? ldg_nc_v4(ina + kb) : zero;
+        xb[u] = (kin && rowb < M) ? ldg_nc_v4(inb + kb) : zero;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int j = t * 8 + g;
+          bv[u][t] = (kin && j < r) ? load_mt_frag<NT, MT_KMAJOR>(mt, j, kb, K, r) : zero;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          mma_m16n8k16_bf16(acc[t], xa[u].x, xb[u].x, xa[u].y, xb[u].y, bv[u][t].x, bv[u][t].y);
+          mma_m16n8k16_bf16(acc[t], xa[u].z, xb[u].z, xa[u].w, xb[u].w, bv[u][t].z, bv[u][t].w);
+        }
       }
     }
+    // reduction over the W warps in warp order
 #pragma unroll
-    for (int u = 0; u < UNROLL; ++u) {
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        mma_m16n8k16_bf16(acc[t], xa[u].x, xb[u].x, xa[u].y, xb[u].y, bv[u][t].x, bv[u][t].y);
-        mma_m16n8k16_bf16(acc[t], xa[u].z, xb[u].z, xa[u].w, xb[u].w, bv[u][t].z, bv[u][t].w);
-      }
+    for (int t = 0; t < NT; ++t) {
+      const int col = t * 8 + 2 * q;
+      float* base = s_red + warp * 16 * RP;
+      base[g * RP + col] = acc[t][0];
+      base[g * RP + col + 1] = acc[t][1];
+      base[(g + 8) * RP + col] = acc[t][2];
+      base[(g + 8) * RP + col + 1] = acc[t][3];
     }
-  }
-  // intra-CTA reduction over the 8 warps in warp order
-#pragma unroll
-  for (int t = 0; t < NT; ++t) {
-    const int col = t * 8 + 2 * q;
-    float* base = s_red + warp * 16 * RP;
-    base[g * RP + col] = acc[t][0];
-    base[g * RP + col + 1] = acc[t][1];
-    base[(g + 8) * RP + col] = acc[t][2];
-    base[(g + 8) * RP + col + 1] = acc[t][3];
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < 16 * RP; idx += 256) {
-    float v = 0.f;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) v += s_red[w * 16 * RP + idx];
-    s_red[idx] = v;  // warp 0's slot now holds the CTA sum (each idx read before written by this thread only)
-  }
-  if (splits == 1) {
     __syncthreads();
-    for (int idx = threadIdx.x; idx < 16 * RP; idx += 256) {
+    for (int idx = threadIdx.x; idx < 16 * RP; idx += W * 32) {
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < W; ++w) v += s_red[w * 16 * RP + idx];
       const int row = m0 + idx / RP, j = idx % RP;
       if (row >= M || j >= r) continue;
-      const float v = s_red[idx];
       if (out_f32) out_f32[static_cast<int64_t>(row) * r + j] = v;
       if (out_bf16) out_bf16[static_cast<int64_t>(row) * r + j] = __float2bfloat16_rn(__fmul_rn(v, scale));
     }
-    return;
+    __syncthreads();  // s_red is reused by the next tile
   }
-  // split-K over CTAs: publish, last CTA of this row tile adds the splits in order
-  float* mine = partial + (static_cast<int64_t>(blockIdx.y) * gridDim.x + blockIdx.x) * 16 * RP;
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < 16 * RP; idx += 256) mine[idx] = s_red[idx];
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(counters + blockIdx.x, 1u) == static_cast<unsigned>(splits - 1));
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int idx = threadIdx.x; idx < 16 * RP; idx += 256) {
-    float v = 0.f;
-    for (int sp = 0; sp < splits; ++sp)
-      v += __ldcg(partial + (static_cast<int64_t>(sp) * gridDim.x + blockIdx.x) * 16 * RP + idx);
-    const int row = m0 + idx / RP, j = idx % RP;
-    if (row >= M || j >= r) continue;
-    if (out_f32) out_f32[static_cast<int64_t>(row) * r + j] = v;
-    if (out_bf16) out_bf16[static_cast<int64_t>(row) * r + j] = __float2bfloat16_rn(__fmul_rn(v, scale));
-  }
-  if (threadIdx.x == 0) counters[blockIdx.x] = 0;
 }
 
 // ------------------------------------------------------------------ SiLU * up
@@ -196,59 +168,38 @@ __global__ void __launch_bounds__(256) k_silu_mul_bwd(const uint32_t* __restrict
 }
 
 // ------------------------------------------------------------------ launchers
-int lora_down_splits(int M, int K, int num_sms) {
-  // Enough CTAs that every warp makes a single trip (4 chunks of 32 k in flight)
-  // when the grid stays below ~8 CTAs per SM; otherwise as many as fit.
-  (void)num_sms;
-  const int tiles = M > 0 ? (M + 15) / 16 : 1;
-  const int n_chunks = (K + 31) / 32;
-  int splits = (n_chunks + 31) / 32;
-  while (splits > 1 && tiles * splits > 8 * 148) splits = (splits + 1) / 2;
-  return splits < 1 ? 1 : splits;
-}
-
 size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms) {
-  const int splits = lora_down_splits(M, K, num_sms);
-  if (splits == 1) return 0;
-  const int tiles = (M + 15) / 16;
-  const int rp = r <= 16 ? 16 : (r <= 32 ? 32 : (r <= 64 ? 64 : 128));
-  return static_cast<size_t>(splits) * tiles * 16 * rp * sizeof(float) + static_cast<size_t>(tiles) * 4 + 256;
+  (void)M, (void)K, (void)r, (void)num_sms;
+  return 0;  // no cross-CTA reduction
 }
 
 cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int mt_kmajor, int M, int K, int r,
-                             float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int num_sms,
+                             float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int max_ctas,
                              cudaStream_t s, const float* cvt_src, __nv_bfloat16* cvt_dst, int64_t cvt_n,
                              float cvt_scale) {
+  (void)ws;
   const int tiles = (M + 15) / 16;
-  const int splits = lora_down_splits(M, K, num_sms);
   const int rp = r <= 16 ? 16 : (r <= 32 ? 32 : (r <= 64 ? 64 : 128));
-  float* partial = nullptr;
-  unsigned* counters = nullptr;
-  if (splits > 1) {
-    partial = static_cast<float*>(ws);
-    counters = reinterpret_cast<unsigned*>(partial + static_cast<size_t>(splits) * tiles * 16 * rp);
-    cudaError_t e = cudaMemsetAsync(counters, 0, static_cast<size_t>(tiles) * 4, s);
-    if (e != cudaSuccess) return e;
-  }
-  const dim3 grid(tiles, splits);
-  const size_t smem = static_cast<size_t>(8) * 16 * rp * sizeof(float);
-#define QLORA_LD(NT, KM)                                                                                      \
+  int grid = tiles < max_ctas ? tiles : max_ctas;
+  if (grid < 1) grid = 1;
+#define QLORA_LD(NT, KM, W)                                                                                   \
   do {                                                                                                        \
-    set_smem_limit_once(k_lora_down<NT, KM>, smem);                                                           \
-    k_lora_down<NT, KM><<<grid, 256, smem, s>>>(in, mt, M, K, r, splits, partial, counters, scale, out_f32,   \
-                                                out_bf16, cvt_src, cvt_dst, cvt_n, cvt_scale);                \
+    const size_t smem = static_cast<size_t>(W) * 16 * rp * sizeof(float);                                     \
+    set_smem_limit_once(k_lora_down<NT, KM, W>, smem);                                                        \
+    k_lora_down<NT, KM, W><<<grid, W * 32, smem, s>>>(in, mt, M, K, r, scale, out_f32, out_bf16, cvt_src,     \
+                                                      cvt_dst, cvt_n, cvt_scale);                             \
   } while (0)
-#define QLORA_LD2(NT) \
-  do {                \
-    if (mt_kmajor)    \
-      QLORA_LD(NT, true); \
-    else              \
-      QLORA_LD(NT, false); \
+#define QLORA_LD2(NT, W)     \
+  do {                       \
+    if (mt_kmajor)           \
+      QLORA_LD(NT, true, W); \
+    else                     \
+      QLORA_LD(NT, false, W); \
   } while (0)
-  if (rp == 16) QLORA_LD2(2);
-  else if (rp == 32) QLORA_LD2(4);
-  else if (rp == 64) QLORA_LD2(8);
-  else QLORA_LD2(16);
+  if (rp == 16) QLORA_LD2(2, 16);
+  else if (rp == 32) QLORA_LD2(4, 16);
+  else if (rp == 64) QLORA_LD2(8, 8);
+  else QLORA_LD2(16, 8);
 #undef QLORA_LD2
 #undef QLORA_LD
   return cudaGetLastError();

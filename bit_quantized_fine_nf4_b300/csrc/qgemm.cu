@@ -462,12 +462,9 @@ __global__ void __launch_bounds__(kWbThreads, 1)
 struct LgParams {
   float* da;  // [r, K]
   float* db;  // [N, r]
-  float* partial;      // [splits][tiles][128][r] (splits > 1)
-  unsigned* counters;  // [tiles]
   unsigned* status;
   int M, N, K, r;
-  int tiles_a, tiles;
-  int splits, iters_per_split;
+  int tiles_a, tiles;  // 128-column tiles of dA^T (first tiles_a) and of dB
   int accum_da, accum_db;
   unsigned long long wait_ns;
 };
@@ -479,10 +476,13 @@ struct LgCfg {
   static constexpr uint32_t kABytes = 2 * 8192;           // [64 m x 128 c] as two 64-wide slabs
   static constexpr uint32_t kBBytes = (RP / 64) * 8192;   // [64 m x RP j]
   static constexpr uint32_t kStage = kABytes + kBBytes;
-  static constexpr int kStages = RP == 64 ? 8 : 6;        // deep ring: one CTA streams every token
-  static constexpr size_t kSmem = 1024 + kStages * kStage + (2 * kStages + 1) * 8 + 16;
+  static constexpr int kStages = RP == 64 ? 8 : 6;        // deep ring: few CTAs stream every token
+  static constexpr uint32_t kTmemCols = 2 * RP;           // double-buffered accumulator
+  static constexpr size_t kSmem = 1024 + kStages * kStage + (2 * kStages + 4) * 8 + 16;
 };
 
+// Persistent: CTA b takes column tiles b, b + gridDim.x, ...; for each, all
+// tokens stream through the TMA ring (no cross-CTA reduction: deterministic).
 template <int RP>
 __global__ void __launch_bounds__(kLgThreads, 1)
     k_lora_grad(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_dy,
@@ -494,35 +494,31 @@ __global__ void __launch_bounds__(kLgThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kLgStages * Cfg::kStage);
   uint64_t* empty = full + kLgStages;
-  uint64_t* acc_full = empty + kLgStages;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* acc_full = empty + kLgStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;      // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
   volatile int* vabort = abort_flag;
 
+  griddep_launch_dependents();  // the dX GEMM that follows needs nothing from this kernel until its end
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const bool is_b = blockIdx.x >= p.tiles_a;
-  const int c0 = (is_b ? blockIdx.x - p.tiles_a : blockIdx.x) * 128;
-  const int C = is_b ? p.N : p.K;
-  const CUtensorMap* tq = is_b ? &tm_dy : &tm_x;
-  const CUtensorMap* tp = is_b ? &tm_st : &tm_su;
-  const int split = blockIdx.y;
-  const int it0 = split * p.iters_per_split;
-  const int n_iter = min((p.M + 63) / 64, it0 + p.iters_per_split) - it0;  // >= 1 by construction
-  int* last_flag = abort_flag + 1;
+  const int n_iter = (p.M + 63) / 64;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kLgStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  constexpr uint32_t kCols = RP < 32 ? 32 : RP;
   if (warp == 0) {
     __syncwarp();
-    tmem_alloc(tmem_holder, kCols);
+    tmem_alloc(tmem_holder, Cfg::kTmemCols);
   }
   tc_fence_before();
   __syncthreads();
@@ -531,116 +527,101 @@ __global__ void __launch_bounds__(kLgThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      tma_prefetch_desc(tq);
-      tma_prefetch_desc(tp);
-      for (int i = 0; i < n_iter; ++i) {
-        const int s = i % kLgStages;
-        const uint32_t ph = (i / kLgStages) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
-        uint8_t* sa = smem + s * Cfg::kStage;
-        const int mrow = (it0 + i) * 64;
-        mbar_arrive_expect_tx(&full[s], Cfg::kStage);
-        tma_load_2d(sa, tq, &full[s], c0, mrow);
-        tma_load_2d(sa + 8192, tq, &full[s], c0 + 64, mrow);
+      griddep_wait();  // sU and sT come from the preceding kernel
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_dy);
+      int g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x) {
+        const bool is_b = tile >= p.tiles_a;
+        const int c0 = (is_b ? tile - p.tiles_a : tile) * 128;
+        const CUtensorMap* tq = is_b ? &tm_dy : &tm_x;
+        const CUtensorMap* tp = is_b ? &tm_st : &tm_su;
+        for (int i = 0; i < n_iter; ++i, ++g) {
+          const int s = g % kLgStages;
+          const uint32_t ph = (g / kLgStages) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); ok = false; break; }
+          uint8_t* sa = smem + s * Cfg::kStage;
+          mbar_arrive_expect_tx(&full[s], Cfg::kStage);
+          tma_load_2d(sa, tq, &full[s], c0, i * 64);
+          tma_load_2d(sa + 8192, tq, &full[s], c0 + 64, i * 64);
 #pragma unroll
-        for (int sl = 0; sl < RP / 64; ++sl) tma_load_2d(sa + Cfg::kABytes + sl * 8192, tp, &full[s], sl * 64, mrow);
+          for (int sl = 0; sl < RP / 64; ++sl) tma_load_2d(sa + Cfg::kABytes + sl * 8192, tp, &full[s], sl * 64, i * 64);
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, RP, 1, 1);
-      for (int i = 0; i < n_iter; ++i) {
-        const int s = i % kLgStages;
-        const uint32_t ph = (i / kLgStages) & 1;
-        if (!mbar_wait(&full[s], ph, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
+      int g = 0, j = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < p.tiles && ok; tile += gridDim.x, ++j) {
+        const int buf = j & 1;
+        if (!mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(smem + s * Cfg::kStage);
-        const uint32_t b_addr = a_addr + Cfg::kABytes;
+        for (int i = 0; i < n_iter; ++i, ++g) {
+          const int s = g % kLgStages;
+          const uint32_t ph = (g / kLgStages) & 1;
+          if (!mbar_wait(&full[s], ph, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * Cfg::kStage);
+          const uint32_t b_addr = a_addr + Cfg::kABytes;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          const uint64_t adesc = sdesc_sw128(a_addr + kk * 2048, 8192, 1024);
-          const uint64_t bdesc = sdesc_sw128(b_addr + kk * 2048, 8192, 1024);
-          mma_bf16_ss(tbase, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t adesc = sdesc_sw128(a_addr + kk * 2048, 8192, 1024);
+            const uint64_t bdesc = sdesc_sw128(b_addr + kk * 2048, 8192, 1024);
+            mma_bf16_ss(tbase + buf * RP, adesc, bdesc, idesc, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[s]);
         }
-        mma_commit(&empty[s]);
+        if (ok) mma_commit(&acc_full[buf]);
       }
-      mma_commit(acc_full);
     }
   } else {
-    bool ok = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, p.wait_ns, vabort));
-    ok = ok && !*vabort;
-    ok = __all_sync(0xffffffffu, ok);
-    tc_fence_after();
     const int quarter = warp & 3;
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-    const int c = c0 + quarter * 32 + lane;
-    const int tile = blockIdx.x;
-    float* mine = p.partial + (static_cast<int64_t>(split) * p.tiles + tile) * 128 * p.r + (quarter * 32 + lane) * p.r;
-    auto store = [&](int j, float val) {
-      if (!is_b) {
-        float* d = p.da + static_cast<int64_t>(j) * p.K + c;
-        *d = p.accum_da ? (*d + val) : val;
-      } else {
-        float* d = p.db + static_cast<int64_t>(c) * p.r + j;
-        *d = p.accum_db ? (*d + val) : val;
-      }
-    };
-    if (ok) {
+    int j = 0;
+    for (int tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++j) {
+      const int buf = j & 1;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (j >> 1) & 1, p.wait_ns, vabort));
+      ok = __all_sync(0xffffffffu, ok && !*vabort);
+      if (!ok) break;
+      tc_fence_after();
+      const bool is_b = tile >= p.tiles_a;
+      const int c = (is_b ? tile - p.tiles_a : tile) * 128 + quarter * 32 + lane;
+      const int C = is_b ? p.N : p.K;
       for (int j0 = 0; j0 < RP && j0 < p.r; j0 += 16) {
         uint32_t v[16];
         __syncwarp();
-        tmem_ld_32x32b_x16(tbase + lane_field + j0, v);
+        tmem_ld_32x32b_x16(tbase + lane_field + buf * RP + j0, v);
         tmem_ld_wait();
-        if (p.splits > 1) {
-#pragma unroll
-          for (int jj = 0; jj < 16; jj += 4)
-            if (j0 + jj < p.r)
-              *reinterpret_cast<float4*>(mine + j0 + jj) =
-                  make_float4(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1]), __uint_as_float(v[jj + 2]),
-                              __uint_as_float(v[jj + 3]));
-        } else if (c < C) {
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            if (j0 + jj < p.r) store(j0 + jj, __uint_as_float(v[jj]));
-        }
-      }
-    }
-    if (p.splits > 1) {
-      // the last CTA of this column tile adds the splits in split order
-      __threadfence();
-      named_bar_sync(1, 128);
-      if (threadIdx.x == 64) *last_flag = (atomicAdd(p.counters + tile, 1u) == static_cast<unsigned>(p.splits - 1));
-      named_bar_sync(1, 128);
-      if (*reinterpret_cast<volatile int*>(last_flag)) {
-        __threadfence();
         if (c < C) {
-          // 16 columns at a time: issue every partial load first (one L2 round trip), then add in split order
-          for (int j0 = 0; j0 < p.r; j0 += 16) {
-            float acc[16];
+          if (!is_b) {
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) acc[jj] = 0.f;
-            for (int sp = 0; sp < p.splits; ++sp) {
-              const float4* src = reinterpret_cast<const float4*>(
-                  p.partial + (static_cast<int64_t>(sp) * p.tiles + tile) * 128 * p.r + (quarter * 32 + lane) * p.r + j0);
-              float4 v4[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                v4[q] = (j0 + 4 * q < p.r) ? __ldcg(src + q) : make_float4(0.f, 0.f, 0.f, 0.f);  // stay inside the row
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                acc[4 * q] += v4[q].x;
-                acc[4 * q + 1] += v4[q].y;
-                acc[4 * q + 2] += v4[q].z;
-                acc[4 * q + 3] += v4[q].w;
-              }
+            for (int jj = 0; jj < 16; ++jj) {
+              if (j0 + jj >= p.r) break;
+              float* d = p.da + static_cast<int64_t>(j0 + jj) * p.K + c;
+              const float val = __uint_as_float(v[jj]);
+              *d = p.accum_da ? (*d + val) : val;
             }
+          } else {
+            float* d = p.db + static_cast<int64_t>(c) * p.r + j0;  // 16 consecutive floats (r % 8 == 0)
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-              if (j0 + jj < p.r) store(j0 + jj, acc[jj]);
+            for (int jj = 0; jj < 16; jj += 4) {
+              if (j0 + jj >= p.r) break;
+              float4 val = make_float4(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1]),
+                                       __uint_as_float(v[jj + 2]), __uint_as_float(v[jj + 3]));
+              if (p.accum_db) {
+                const float4 o = *reinterpret_cast<const float4*>(d + jj);
+                val.x += o.x; val.y += o.y; val.z += o.z; val.w += o.w;
+              }
+              *reinterpret_cast<float4*>(d + jj) = val;
+            }
           }
         }
-        if (threadIdx.x == 64) p.counters[tile] = 0;
       }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
     }
   }
   tc_fence_before();
@@ -648,7 +629,7 @@ __global__ void __launch_bounds__(kLgThreads, 1)
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tbase, kCols);
+    tmem_dealloc(tbase, Cfg::kTmemCols);
   }
 }
 
@@ -836,75 +817,64 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
   return cudaGetLastError();
 }
 
-struct LgPlan {
-  int tiles_a, tiles, splits, iters;
-};
-static LgPlan plan_lg(int M, int N, int K, int num_sms) {
-  LgPlan pl;
-  pl.tiles_a = (K + 127) / 128;
-  pl.tiles = pl.tiles_a + (N + 127) / 128;
-  const int n_iter = (M + 63) / 64;
-  // split over tokens only while the doubled grid still fits one wave (one CTA
-  // per SM with the deep ring) and every split keeps >= 16 m-blocks
-  int splits = 1;
-  while (pl.tiles * splits * 2 <= num_sms && splits * 2 * 16 <= n_iter) splits *= 2;
-  pl.iters = (n_iter + splits - 1) / splits;
-  pl.splits = (n_iter + pl.iters - 1) / pl.iters;
-  return pl;
-}
-
 size_t lora_grads_workspace_bytes(int M, int N, int K, int r, int num_sms) {
-  const LgPlan pl = plan_lg(M, N, K, num_sms);
-  if (pl.splits == 1) return 0;
-  return static_cast<size_t>(pl.splits) * pl.tiles * 128 * r * 4 + static_cast<size_t>(pl.tiles) * 4 + 256;
+  (void)M, (void)N, (void)K, (void)r, (void)num_sms;
+  return 0;  // no cross-CTA reduction
 }
 
 cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __nv_bfloat16* su,
                               const __nv_bfloat16* st, int M, int N, int K, int r, float* da, float* db,
-                              int accum_da, int accum_db, void* ws, unsigned* status, uint64_t wait_ns, int num_sms,
+                              int accum_da, int accum_db, void* ws, unsigned* status, uint64_t wait_ns, int max_ctas,
                               cudaStream_t s) {
+  (void)ws;
   CUtensorMap tx, tdy, tsu, tst;
   if (!make_tm(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
   if (!make_tm(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 64)) return cudaErrorInvalidValue;
   if (!make_tm(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
   if (!make_tm(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
-  const LgPlan pl = plan_lg(M, N, K, num_sms);
   LgParams prm;
   prm.da = da;
   prm.db = db;
-  prm.partial = nullptr;
-  prm.counters = nullptr;
   prm.status = status;
   prm.M = M;
   prm.N = N;
   prm.K = K;
   prm.r = r;
-  prm.tiles_a = pl.tiles_a;
-  prm.tiles = pl.tiles;
-  prm.splits = pl.splits;
-  prm.iters_per_split = pl.iters;
+  prm.tiles_a = (K + 127) / 128;
+  prm.tiles = prm.tiles_a + (N + 127) / 128;
   prm.accum_da = accum_da;
   prm.accum_db = accum_db;
   prm.wait_ns = wait_ns;
-  if (pl.splits > 1) {
-    prm.partial = static_cast<float*>(ws);
-    prm.counters = reinterpret_cast<unsigned*>(prm.partial + static_cast<size_t>(pl.splits) * pl.tiles * 128 * r);
-    const cudaError_t e = cudaMemsetAsync(prm.counters, 0, static_cast<size_t>(pl.tiles) * 4, s);
-    if (e != cudaSuccess) return e;
-  }
-  const dim3 grid(pl.tiles, pl.splits);
+  int grid = prm.tiles < max_ctas ? prm.tiles : max_ctas;
+  if (grid < 1) grid = 1;
+  cudaError_t e;
   if (r <= 64) {
-    const size_t smem = LgCfg<64>::kSmem;
-    cudaError_t e = set_smem_limit_once(k_lora_grad<64>, smem);
-    if (e != cudaSuccess) return e;
-    k_lora_grad<64><<<grid, kLgThreads, smem, s>>>(tx, tdy, tsu, tst, prm);
+    e = set_smem_limit_once(k_lora_grad<64>, LgCfg<64>::kSmem);
+    if (e == cudaSuccess) e = launch_pdl(k_lora_grad<64>, dim3(grid), dim3(kLgThreads), LgCfg<64>::kSmem, s, tx, tdy, tsu, tst, prm);
   } else {
-    const size_t smem = LgCfg<128>::kSmem;
-    cudaError_t e = set_smem_limit_once(k_lora_grad<128>, smem);
-    if (e != cudaSuccess) return e;
-    k_lora_grad<128><<<grid, kLgThreads, smem, s>>>(tx, tdy, tsu, tst, prm);
+    e = set_smem_limit_once(k_lora_grad<128>, LgCfg<128>::kSmem);
+    if (e == cudaSuccess) e = launch_pdl(k_lora_grad<128>, dim3(grid), dim3(kLgThreads), LgCfg<128>::kSmem, s, tx, tdy, tsu, tst, prm);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// SMs a GEMM grid leaves idle in its last wave: the budget for the side kernels
+// that run beside it (all of them when the grid fills its waves exactly).
+int idle_sms_beside(int gemm_ctas, int num_sms) {
+  const int rem = gemm_ctas % num_sms;
+  const int idle = rem == 0 ? 0 : num_sms - rem;
+  return idle >= 8 ? idle : num_sms;
+}
+
+int fwd_gemm_ctas(int M, int N, int K, int num_sms) {
+  const FwdPlan pl = plan_fwd(M, N, K, num_sms);
+  return pl.row_tiles * pl.tok_tiles * pl.splits;
+}
+
+int bwd_gemm_ctas(int M, int N, int K) {
+  (void)N;
+  return ((K + 255) / 256) * ((M + 255) / 256);
 }
 
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t wait_ns, cudaStream_t s) {
