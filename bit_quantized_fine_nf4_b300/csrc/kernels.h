@@ -66,6 +66,19 @@ cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, c
                               const __nv_bfloat16* st, int M, int N, int K, int r, float* da, float* db,
                               int accum_da, int accum_db, void* ws, unsigned* status, uint64_t wait_ns, int max_ctas,
                               cudaStream_t s);
+// CTA-pair versions of both GEMMs (qgemm_pair.cu), used for M > 256 tokens.
+bool use_pair_gemm(int M);
+int fwd_pair_ctas(int M, int N);
+int bwd_pair_ctas(int M, int K);
+cudaError_t launch_fwd_gemm_pair(const __nv_bfloat16* x, int M, const Nf4Dev& w, const __nv_bfloat16* st,
+                                 const __nv_bfloat16* lora_b, int r, __nv_bfloat16* y, unsigned* status,
+                                 uint64_t wait_ns, cudaStream_t s);
+cudaError_t launch_bwd_gemm_pair(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
+                                 const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
+                                 unsigned* status, uint64_t wait_ns, cudaStream_t s);
+// 2-D bf16 tensor map, 128-byte swizzle, zero fill outside [outer x inner] (qgemm.cu).
+bool make_tensor_map_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
+                             uint32_t box_inner, uint32_t box_outer);
 // Grid sizes of the GEMMs and the SMs they leave idle (budget for side kernels).
 int fwd_gemm_ctas(int M, int N, int K, int num_sms);
 int bwd_gemm_ctas(int M, int N, int K);

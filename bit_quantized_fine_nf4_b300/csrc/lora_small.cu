@@ -181,13 +181,27 @@ cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, i
   const int tiles = (M + 15) / 16;
   const int rp = r <= 16 ? 16 : (r <= 32 ? 32 : (r <= 64 ? 64 : 128));
   int grid = tiles < max_ctas ? tiles : max_ctas;
+  if (grid >= 2) grid &= ~1;  // clusters of two: the CTAs sit on whole TPCs, which the pair GEMMs need
   if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = grid >= 2 ? 1 : 0;
+  cudaError_t e = cudaSuccess;
 #define QLORA_LD(NT, KM, W)                                                                                   \
   do {                                                                                                        \
     const size_t smem = static_cast<size_t>(W) * 16 * rp * sizeof(float);                                     \
     set_smem_limit_once(k_lora_down<NT, KM, W>, smem);                                                        \
-    k_lora_down<NT, KM, W><<<grid, W * 32, smem, s>>>(in, mt, M, K, r, scale, out_f32, out_bf16, cvt_src,     \
-                                                      cvt_dst, cvt_n, cvt_scale);                             \
+    cfg.blockDim = dim3(W * 32);                                                                              \
+    cfg.dynamicSmemBytes = smem;                                                                              \
+    e = cudaLaunchKernelEx(&cfg, k_lora_down<NT, KM, W>, in, mt, M, K, r, scale, out_f32, out_bf16, cvt_src,  \
+                           cvt_dst, cvt_n, cvt_scale);                                                        \
   } while (0)
 #define QLORA_LD2(NT, W)     \
   do {                       \
@@ -202,6 +216,7 @@ cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, i
   else QLORA_LD2(16, 8);
 #undef QLORA_LD2
 #undef QLORA_LD
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -153,18 +153,32 @@ __global__ void __launch_bounds__(kWaThreads, 1)
     const float mu = *p.mean;
     const int kb_row = p.K / 64;
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    // the codes and absmax of a k block are loaded one trip ahead of its decode
+    const uint8_t* row_codes = p.codes + static_cast<int64_t>(row) * (p.K / 2);
+    const int64_t row_abs = static_cast<int64_t>(row) * kb_row;
+    uint4 nc0 = make_uint4(0, 0, 0, 0), nc1 = nc0;
+    int8_t nq = 0;
+    float nstep = 0.f;
+    auto fetch = [&](int i) {
+      if (i < n_main && row_ok) {
+        const int kb = kb_begin + i;
+        nc0 = ldg_nc_v4(row_codes + kb * 32);
+        nc1 = ldg_nc_v4(row_codes + kb * 32 + 16);
+        nq = p.absq[row_abs + kb];
+        nstep = p.step[(row_abs + kb) >> 8];
+      }
+    };
+    fetch(team);
     bool alive = true;
     for (int i = team; i < n_iter && alive; i += kWaTeams) {
       const int s = i % STAGES;
       const uint32_t ph = (i / STAGES) & 1;
       uint32_t words[32];
       if (i < n_main) {
-        const int kb = kb_begin + i;
+        const uint4 c0 = nc0, c1 = nc1;
+        const float a2 = restore_absmax(nq, nstep, mu);
+        fetch(i + kWaTeams);
         if (row_ok) {
-          const uint8_t* cp = p.codes + static_cast<int64_t>(row) * (p.K / 2) + kb * 32;
-          const uint4 c0 = ldg_nc_v4(cp), c1 = ldg_nc_v4(cp + 16);
-          const int64_t ai = static_cast<int64_t>(row) * kb_row + kb;
-          const float a2 = restore_absmax(p.absq[ai], p.step[ai >> 8], mu);
           nf4_decode_block(c0, c1, a2, words);
         } else {
 #pragma unroll
@@ -373,22 +387,32 @@ __global__ void __launch_bounds__(kWbThreads, 1)
     const float mu = *p.mean;
     const int kb_row = p.K / 64;
     const int kblk = (k0 >> 6) + slab;
+    // the codes and absmax of a unit are loaded one trip ahead of its decode
+    uint4 nc0 = make_uint4(0, 0, 0, 0), nc1 = nc0;
+    int8_t nq = 0;
+    float nstep = 0.f;
+    auto fetch = [&](int i) {
+      const int n = i * 64 + rrow;
+      if (i < n_main && n < p.N && kblk < kb_row) {
+        const uint8_t* cp = p.codes + static_cast<int64_t>(n) * (p.K / 2) + kblk * 32;
+        nc0 = ldg_nc_v4(cp);
+        nc1 = ldg_nc_v4(cp + 16);
+        const int64_t ai = static_cast<int64_t>(n) * kb_row + kblk;
+        nq = p.absq[ai];
+        nstep = p.step[ai >> 8];
+      }
+    };
+    fetch(team);
     bool alive = true;
     for (int i = team; i < n_iter && alive; i += 2) {
       const int s = i % STAGES;
       const uint32_t ph = (i / STAGES) & 1;
       const bool is_main = i < n_main;
-      uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
-      float a2 = 0.f;
       const int n = i * 64 + rrow;
       const bool uok = is_main && (n < p.N) && (kblk < kb_row);
-      if (uok) {
-        const uint8_t* cp = p.codes + static_cast<int64_t>(n) * (p.K / 2) + kblk * 32;
-        c0 = ldg_nc_v4(cp);
-        c1 = ldg_nc_v4(cp + 16);
-        const int64_t ai = static_cast<int64_t>(n) * kb_row + kblk;
-        a2 = restore_absmax(p.absq[ai], p.step[ai >> 8], mu);
-      }
+      const uint4 c0 = nc0, c1 = nc1;
+      const float a2 = restore_absmax(nq, nstep, mu);
+      fetch(i + 2);
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort));
       if (!ok) { if (lane == 0) abort_cta(p.status, abort_flag); alive = false; break; }
       if (is_main) {
@@ -666,7 +690,7 @@ static bool get_encode() {
 }
 
 // bf16 matrix [outer, inner] with row pitch `pitch` bytes; box [box_outer, box_inner]; 128-byte swizzle.
-static bool make_tm(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
+bool make_tensor_map_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
                     uint32_t box_inner, uint32_t box_outer) {
   if (!get_encode()) return false;
   const cuuint64_t dims[2] = {inner, outer};
@@ -710,6 +734,7 @@ static FwdPlan plan_fwd(int M, int N, int K, int num_sms) {
 }
 
 size_t fwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
+  if (use_pair_gemm(M)) return 0;
   const FwdPlan pl = plan_fwd(M, N, K, num_sms);
   if (pl.splits == 1) return 0;
   const size_t tiles = static_cast<size_t>(pl.row_tiles) * pl.tok_tiles;
@@ -719,19 +744,24 @@ size_t fwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
 // Launch with programmatic stream serialization: the kernel may start while the
 // preceding kernel of the stream (the LoRA down-projection) still runs; it
 // waits for it (griddep_wait) only before loading that kernel's output.
+// `cluster` > 1: clusters of that many CTAs along x.
 template <typename... KArgs, typename... Args>
 static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              Args&&... args) {
+                              int cluster, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -741,7 +771,7 @@ static cudaError_t run_wa(const CUtensorMap& tx, const CUtensorMap& tst, const W
   using Cfg = WaCfg<NTOK, STAGES>;
   cudaError_t e = set_smem_limit_once(k_qgemm_wa<NTOK, STAGES>, Cfg::kSmem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(k_qgemm_wa<NTOK, STAGES>, grid, dim3(kWaThreads), Cfg::kSmem, s, tx, tst, prm);
+  e = launch_pdl(k_qgemm_wa<NTOK, STAGES>, grid, dim3(kWaThreads), Cfg::kSmem, s, 1, tx, tst, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -749,11 +779,12 @@ static cudaError_t run_wa(const CUtensorMap& tx, const CUtensorMap& tst, const W
 cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, const __nv_bfloat16* st,
                             const __nv_bfloat16* lora_b, int r, __nv_bfloat16* y, void* ws, unsigned* status,
                             uint64_t wait_ns, int num_sms, cudaStream_t s) {
+  if (use_pair_gemm(M)) return launch_fwd_gemm_pair(x, M, w, st, lora_b, r, y, status, wait_ns, s);
   const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
   const FwdPlan pl = plan_fwd(M, N, K, num_sms);
   CUtensorMap tx, tst;
-  if (!make_tm(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, pl.ntok)) return cudaErrorInvalidValue;
-  if (!make_tm(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, pl.ntok)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, pl.ntok)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, pl.ntok)) return cudaErrorInvalidValue;
   WaParams prm;
   prm.codes = w.codes;
   prm.absq = w.absq;
@@ -788,11 +819,12 @@ cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, cons
 cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
                                const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
                                unsigned* status, uint64_t wait_ns, cudaStream_t s) {
+  if (use_pair_gemm(M)) return launch_bwd_gemm_pair(dy, M, w, su, lora_a, r, dx, accumulate, status, wait_ns, s);
   const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
   CUtensorMap tdy, tsu, tla;
-  if (!make_tm(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 256)) return cudaErrorInvalidValue;
-  if (!make_tm(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 256)) return cudaErrorInvalidValue;
-  if (!make_tm(&tla, lora_a, K, r, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 256)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 256)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tla, lora_a, K, r, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
   WbParams prm;
   prm.codes = w.codes;
   prm.absq = w.absq;
@@ -812,7 +844,7 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
   cudaError_t e = set_smem_limit_once(k_qgemm_wb<kStages>, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid((K + 255) / 256, (M + 255) / 256);
-  e = launch_pdl(k_qgemm_wb<kStages>, grid, dim3(kWbThreads), smem, s, tdy, tsu, tla, prm);
+  e = launch_pdl(k_qgemm_wb<kStages>, grid, dim3(kWbThreads), smem, s, 1, tdy, tsu, tla, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -828,10 +860,10 @@ cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, c
                               cudaStream_t s) {
   (void)ws;
   CUtensorMap tx, tdy, tsu, tst;
-  if (!make_tm(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
-  if (!make_tm(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 64)) return cudaErrorInvalidValue;
-  if (!make_tm(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
-  if (!make_tm(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
   LgParams prm;
   prm.da = da;
   prm.db = db;
@@ -846,14 +878,16 @@ cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, c
   prm.accum_db = accum_db;
   prm.wait_ns = wait_ns;
   int grid = prm.tiles < max_ctas ? prm.tiles : max_ctas;
+  if (grid >= 2) grid &= ~1;  // clusters of two: the CTAs sit on whole TPCs, which the pair GEMMs need
   if (grid < 1) grid = 1;
+  const int cluster = grid >= 2 ? 2 : 1;
   cudaError_t e;
   if (r <= 64) {
     e = set_smem_limit_once(k_lora_grad<64>, LgCfg<64>::kSmem);
-    if (e == cudaSuccess) e = launch_pdl(k_lora_grad<64>, dim3(grid), dim3(kLgThreads), LgCfg<64>::kSmem, s, tx, tdy, tsu, tst, prm);
+    if (e == cudaSuccess) e = launch_pdl(k_lora_grad<64>, dim3(grid), dim3(kLgThreads), LgCfg<64>::kSmem, s, cluster, tx, tdy, tsu, tst, prm);
   } else {
     e = set_smem_limit_once(k_lora_grad<128>, LgCfg<128>::kSmem);
-    if (e == cudaSuccess) e = launch_pdl(k_lora_grad<128>, dim3(grid), dim3(kLgThreads), LgCfg<128>::kSmem, s, tx, tdy, tsu, tst, prm);
+    if (e == cudaSuccess) e = launch_pdl(k_lora_grad<128>, dim3(grid), dim3(kLgThreads), LgCfg<128>::kSmem, s, cluster, tx, tdy, tsu, tst, prm);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -868,12 +902,14 @@ int idle_sms_beside(int gemm_ctas, int num_sms) {
 }
 
 int fwd_gemm_ctas(int M, int N, int K, int num_sms) {
+  if (use_pair_gemm(M)) return fwd_pair_ctas(M, N);
   const FwdPlan pl = plan_fwd(M, N, K, num_sms);
   return pl.row_tiles * pl.tok_tiles * pl.splits;
 }
 
 int bwd_gemm_ctas(int M, int N, int K) {
   (void)N;
+  if (use_pair_gemm(M)) return bwd_pair_ctas(M, K);
   return ((K + 255) / 256) * ((M + 255) / 256);
 }
 

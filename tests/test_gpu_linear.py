@@ -159,3 +159,32 @@ def test_mlp_gate_shape_sampled_rows(lib):
 def test_65b_upproj_sampled_rows(lib):
     """22016 x 8192 (Llama-65B up-projection), 4096 tokens, r=64, alpha=16."""
     _sampled_big(lib, 22016, 8192, 4096, 64, 16.0, seed=65, nrows=12)
+
+
+# More than 256 tokens take the CTA-pair GEMMs (512-token tiles, 256-row / 256-column pair tiles).
+@pytest.mark.parametrize("m,n,k,r", [(600, 320, 448, 16), (777, 1024, 768, 128), (1030, 136, 64, 8),
+                                     (257, 512, 1280, 32), (1536, 768, 512, 64)])
+def test_pair_tiles_ragged(lib, m, n, k, r):
+    case = synthetic.linear_case(n, k, m, r, 2.0 * r, base_seed=3 * m + n + k + r)
+    _check_all(lib, case)
+
+
+def test_pair_accumulate_flags(lib):
+    case = synthetic.linear_case(384, 320, 520, 16, 32.0, base_seed=21)
+    rec, y, t, dx, da, db = _run(lib, case)
+    x, a, b, dy = (v.cuda() for v in (case.x, case.a, case.b, case.dy))
+    dx2, da2, db2 = dx.clone(), da.clone(), db.clone()
+    lib.linear_bwd(dy, x, rec, a, b, case.alpha, t, dx=dx2, da=da2, db=db2,
+                   flags=lib.ACCUM_DX | lib.ACCUM_DA | lib.ACCUM_DB)
+    lib.check_status()
+    assert rel_fro(to_np64(da2), 2 * to_np64(da)) < 1e-6
+    assert rel_fro(to_np64(db2), 2 * to_np64(db)) < 1e-6
+    assert rel_fro(to_np64(dx2), 2 * to_np64(dx)) < 1e-2
+
+
+def test_pair_lora_path_alone_with_zero_weight(lib):
+    case = synthetic.linear_case(512, 256, 600, 16, 32.0, base_seed=22)
+    case.w.zero_()
+    case.b.copy_((torch.randn(case.b.shape, generator=torch.Generator().manual_seed(6))).to(torch.bfloat16))
+    y, dx, _, _ = _check_all(lib, case)
+    assert float(y.float().abs().max()) > 0 and float(dx.float().abs().max()) > 0
