@@ -23,6 +23,11 @@ struct DevInfo {
   int supported = 0;
   int num_sms = 0;
   unsigned* status = nullptr;
+  // the backward's LoRA gradient kernel runs on this stream, beside the dX
+  // GEMM of the caller's stream (fork after U, join before the call returns)
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex side_mu;
 };
 std::mutex g_mu;
 DevInfo g_dev[128];
@@ -53,6 +58,12 @@ int device(DevInfo** out) {
     e = cudaGetSymbolAddress(&p, g_qlora_status);
     if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "status word: %s", cudaGetErrorString(e));
     di.status = static_cast<unsigned*>(p);
+    if (di.supported) {
+      e = cudaStreamCreateWithFlags(&di.side, cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&di.fork, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&di.join, cudaEventDisableTiming);
+      if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
+    }
     di.ready = true;
   }
   if (!di.supported) return fail(QLORA_ERR_UNSUPPORTED, "the kernels are built for sm_103a only");
@@ -110,6 +121,9 @@ FwdWs fwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
   return w;
 }
 
+// The forward's LoRA down-projection runs as the tiled TMA kernel beside the CTA-pair GEMM.
+bool use_side(int64_t m, int r) { return qlora::use_pair_gemm(static_cast<int>(m)) && qlora::lora_side_supported(r); }
+
 struct BwdWs {
   size_t su, st, ld, lg, total;
 };
@@ -132,11 +146,11 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 // and, while profiling is on, bracketed by two CUDA events on its stream.
 enum ProfName : int {
   P_QUANTIZE = 0, P_DEQUANTIZE, P_LORA_DOWN, P_FWD_GEMM, P_BWD_GEMM, P_LORA_GRADS, P_SILU_FWD, P_SILU_BWD,
-  P_SELFTEST, P_FWD_GROUPED, P_COUNT
+  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_COUNT
 };
 const char* const kProfNames[P_COUNT] = {"nf4_quantize(3 kernels)", "nf4_dequantize", "lora_down", "fwd_gemm",
                                          "bwd_dx_gemm", "lora_grads", "silu_mul_fwd", "silu_mul_bwd",
-                                         "wait_selftest", "fwd_grouped(2 kernels)"};
+                                         "wait_selftest", "fwd_grouped(2 kernels)", "lora_side_fwd"};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<bool> g_prof_on{false};
 struct ProfRec {
@@ -297,11 +311,18 @@ int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, co
   {
     // T = X A^T on the SMs the GEMM's last wave leaves idle; the GEMM starts
     // beside it and waits for T only before its LoRA k block
-    Span sp(P_LORA_DOWN, s, 1);
     const int cap = qlora::idle_sms_beside(qlora::fwd_gemm_ctas(M, N, K, di->num_sms), di->num_sms);
-    e = qlora::launch_lora_down(reinterpret_cast<const __nv_bfloat16*>(x),
-                                reinterpret_cast<const __nv_bfloat16*>(lora_a), 1, M, K, r, scale, t_save, st,
-                                base + ws.st, cap, s);
+    if (use_side(M, r)) {
+      Span sp(P_LORA_SIDE_FWD, s, 1);
+      e = qlora::launch_lora_side_fwd(reinterpret_cast<const __nv_bfloat16*>(x),
+                                      reinterpret_cast<const __nv_bfloat16*>(lora_a), M, K, r, scale, t_save, st, cap,
+                                      di->status, g_wait_ns.load(), s);
+    } else {
+      Span sp(P_LORA_DOWN, s, 1);
+      e = qlora::launch_lora_down(reinterpret_cast<const __nv_bfloat16*>(x),
+                                  reinterpret_cast<const __nv_bfloat16*>(lora_a), 1, M, K, r, scale, t_save, st,
+                                  base + ws.st, cap, s);
+    }
   }
   if (e != cudaSuccess) return cuda_ret(e, "lora_down");
   {
@@ -360,10 +381,11 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
   const __nv_bfloat16* dyb = reinterpret_cast<const __nv_bfloat16*>(dy);
   const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(x);
   cudaError_t e;
-  // Order: U (all SMs) -> dA, dB (on the SMs the dX GEMM's last wave leaves
-  // idle) -> dX GEMM.  The last two start early (programmatic dependent launch)
-  // and wait for their predecessor only before they read its output, so the
-  // gradient kernel runs beside the GEMM instead of after it.
+  // U (all SMs) on the caller's stream, then the dX GEMM there (started early by
+  // programmatic dependent launch, it waits for U only before its LoRA k block)
+  // and, forked onto the side stream after U, the dA / dB kernel on the SMs the
+  // GEMM leaves idle; the caller's stream waits for the side stream before the
+  // call returns.
   {
     // U = dY B (B read as stored) and, in the same launch, sT = bf16(s * t_save)
     Span sp(P_LORA_DOWN, s, 1);
@@ -371,19 +393,26 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
                                 ldws, di->num_sms, s, t_save, st, static_cast<int64_t>(M) * r, scale);
   }
   if (e != cudaSuccess) return cuda_ret(e, "lora_down (U)");
+  std::lock_guard<std::mutex> lk(di->side_mu);
+  e = cudaEventRecord(di->fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(di->side, di->fork, 0);
+  if (e != cudaSuccess) return cuda_ret(e, "fork to the side stream");
   {
-    Span sp(P_LORA_GRADS, s, 1);
+    Span sp(P_LORA_GRADS, di->side, 1);
     const int cap = qlora::idle_sms_beside(qlora::bwd_gemm_ctas(M, N, K), di->num_sms);
     e = qlora::launch_lora_grads(xb, dyb, su, st, M, N, K, r, da, db, (flags & QLORA_ACCUM_DA) ? 1 : 0,
-                                 (flags & QLORA_ACCUM_DB) ? 1 : 0, lgws, di->status, wait, cap, s);
+                                 (flags & QLORA_ACCUM_DB) ? 1 : 0, lgws, di->status, wait, cap, di->side);
   }
-  if (e != cudaSuccess) return cuda_ret(e, "lora grads");
-  {
+  cudaError_t ej = cudaEventRecord(di->join, di->side);
+  if (e == cudaSuccess) {
     Span sp(P_BWD_GEMM, s, 1);
     e = qlora::launch_bwd_dx_gemm(dyb, M, to_dev(w), su, reinterpret_cast<const __nv_bfloat16*>(lora_a), r,
                                   reinterpret_cast<__nv_bfloat16*>(dx), (flags & QLORA_ACCUM_DX) ? 1 : 0, di->status,
                                   wait, s);
   }
+  // always join, so a stream capture never ends with the side stream forked
+  const cudaError_t ew = ej == cudaSuccess ? cudaStreamWaitEvent(s, di->join, 0) : ej;
+  if (e == cudaSuccess) e = ew;
   return cuda_ret(e, "bwd dx gemm");
 }
 

@@ -79,6 +79,12 @@ cudaError_t launch_bwd_gemm_pair(const __nv_bfloat16* dy, int M, const Nf4Dev& w
 // 2-D bf16 tensor map, 128-byte swizzle, zero fill outside [outer x inner] (qgemm.cu).
 bool make_tensor_map_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
                              uint32_t box_inner, uint32_t box_outer);
+// Forward LoRA down-projection beside the pair GEMM (lora_side.cu), 8 <= r <= 64:
+// T = X A^T -> t_save, sT = bf16(s T), by at most max_ctas CTAs.
+bool lora_side_supported(int r);
+cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lora_a, int M, int K, int r, float scale,
+                                 float* t_save, __nv_bfloat16* st, int max_ctas, unsigned* status, uint64_t wait_ns,
+                                 cudaStream_t s);
 // Grid sizes of the GEMMs and the SMs they leave idle (budget for side kernels).
 int fwd_gemm_ctas(int M, int N, int K, int num_sms);
 int bwd_gemm_ctas(int M, int N, int K);

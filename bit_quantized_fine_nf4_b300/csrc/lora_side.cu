@@ -1,0 +1,205 @@
+// LoRA down-projection T = X A^T of the forward, beside the CTA-pair GEMM, on
+// few SMs (Day 25 notes "Fine-tuning and LoRA/QLoRA", section 2.1: the branch
+// B (A x); section 6.2: scaled by s = alpha / r):  t_save = T (fp32), sT = bf16(s T).
+//
+// Each CTA walks 128-token tiles: TMA streams X [128 tok x 64 k] and A_lora
+// [RP x 64 k] (K-major, 128B swizzle; RP = r rounded up to 16, rows past r are
+// zero) through a deep ring (an SM's read rate grows with the bytes in flight),
+// one thread issues M = 128 x N = RP MMAs into a double-buffered TMEM
+// accumulator, and four warps write t_save and sT.  The GEMM that consumes sT
+// starts beside this kernel and waits for it only before its LoRA k block.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace qlora {
+
+struct SideParams {
+  float* t_out;          // t_save [M, r]
+  __nv_bfloat16* s_out;  // sT [M, r]
+  unsigned* status;
+  int M, K, r, rp;
+  int stages, stage_bytes;
+  float scale;
+  unsigned long long wait_ns;
+};
+
+constexpr int kSideThreads = 192;  // warp 0 TMA + TMEM, warp 1 MMA, warps 2..5 epilogue
+constexpr int kSideMaxStages = 8;
+constexpr int kSideBox = 128 * 128;  // [128 rows x 64] bf16
+
+__global__ void __launch_bounds__(kSideThreads, 1)
+    k_lora_side(const __grid_constant__ CUtensorMap tm_a,  // X [M, K]        box 64 x 128
+                const __grid_constant__ CUtensorMap tm_b,  // A_lora [r, K]   box 64 x RP
+                const SideParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int S = p.stages, SB = p.stage_bytes, RP = p.rp;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * SB);
+  uint64_t* empty = full + kSideMaxStages;
+  uint64_t* acc_full = empty + kSideMaxStages;  // [2]
+  uint64_t* acc_empty = acc_full + 2;           // [2]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_empty + 2);
+  int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  volatile int* vabort = abort_flag;
+
+  griddep_launch_dependents();  // the GEMM that follows needs sT only for its last k block
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles = (p.M + 127) / 128;
+  const int n1 = p.K / 64;
+  const uint32_t alloc = 2 * RP <= 32 ? 32 : 2 * RP <= 64 ? 64 : 128;
+  const uint32_t idesc = idesc_bf16_f32(128, RP, 0, 0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSideMaxStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], 128);
+    }
+    *abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == 0) {
+    __syncwarp();
+    tmem_alloc(tmem_holder, alloc);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+      int g = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+        for (int i = 0; i < n1; ++i, ++g) {
+          const int s = g % S;
+          if (!mbar_wait(&empty[s], ((g / S) & 1) ^ 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); ok = false; break; }
+          uint8_t* st = smem + s * SB;
+          mbar_arrive_expect_tx(&full[s], kSideBox + RP * 128);
+          tma_load_2d(st, &tm_a, &full[s], i * 64, tile * 128);
+          tma_load_2d(st + kSideBox, &tm_b, &full[s], i * 64, 0);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int g = 0, j = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x, ++j) {
+        const int buf = j & 1;
+        if (!mbar_wait(&acc_empty[buf], ((j >> 1) & 1) ^ 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); break; }
+        tc_fence_after();
+        const uint32_t d = tbase + buf * RP;
+        for (int i = 0; i < n1; ++i, ++g) {
+          const int s = g % S;
+          if (!mbar_wait(&full[s], (g / S) & 1, p.wait_ns, vabort)) { abort_cta(p.status, abort_flag); ok = false; break; }
+          tc_fence_after();
+          const uint32_t a = smem_u32(smem + s * SB);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16_ss(d, sdesc_sw128(a + kk * 32, 16, 1024), sdesc_sw128(a + kSideBox + kk * 32, 16, 1024), idesc,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(&acc_full[buf]);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (128 threads)
+    const int quarter = warp & 3;          // this warp's TMEM lane quarter
+    const int lrow = quarter * 32 + lane;  // TMEM lane = token row of the tile
+    const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    int j = 0;
+    for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++j) {
+      const int buf = j & 1;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&acc_full[buf], (j >> 1) & 1, p.wait_ns, vabort));
+      if (!ok) break;
+      tc_fence_after();
+      const int tok = tile * 128 + lrow;
+      for (int c = 0; c < RP; c += 16) {
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld_32x32b_x16(tbase + lane_field + buf * RP + c, v);
+        tmem_ld_wait();
+        if (tok < p.M) {
+#pragma unroll
+          for (int q = 0; q < 16; q += 4) {
+            if (c + q < p.r) {  // r % 8 == 0: four consecutive columns are all inside r or all past it
+              const float4 f = make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]), __uint_as_float(v[q + 2]),
+                                           __uint_as_float(v[q + 3]));
+              const int64_t o = static_cast<int64_t>(tok) * p.r + c + q;
+              *reinterpret_cast<float4*>(p.t_out + o) = f;
+              *reinterpret_cast<uint2*>(p.s_out + o) =
+                  make_uint2(pack_bf16x2_rn(__fmul_rn(f.x, p.scale), __fmul_rn(f.y, p.scale)),
+                             pack_bf16x2_rn(__fmul_rn(f.z, p.scale), __fmul_rn(f.w, p.scale)));
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, alloc);
+  }
+}
+
+// ------------------------------------------------------------------ host
+bool lora_side_supported(int r) { return r >= 8 && r <= 64 && r % 8 == 0; }
+
+cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lora_a, int M, int K, int r, float scale,
+                                 float* t_save, __nv_bfloat16* st, int max_ctas, unsigned* status, uint64_t wait_ns,
+                                 cudaStream_t s) {
+  const int rp = (r + 15) / 16 * 16;
+  CUtensorMap ta, tb;
+  if (!make_tensor_map_bf16_2d(&ta, x, K, M, static_cast<uint64_t>(K) * 2, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tb, lora_a, K, r, static_cast<uint64_t>(K) * 2, 64, rp)) return cudaErrorInvalidValue;
+  SideParams prm = {};
+  prm.t_out = t_save;
+  prm.s_out = st;
+  prm.status = status;
+  prm.M = M;
+  prm.K = K;
+  prm.r = r;
+  prm.rp = rp;
+  prm.stage_bytes = kSideBox + rp * 128;
+  prm.stages = (200 * 1024) / prm.stage_bytes;
+  if (prm.stages > kSideMaxStages) prm.stages = kSideMaxStages;
+  prm.scale = scale;
+  prm.wait_ns = wait_ns;
+  const size_t smem = 1024 + static_cast<size_t>(prm.stages) * prm.stage_bytes + (2 * kSideMaxStages + 4) * 8 + 16;
+  const int tiles = (M + 127) / 128;
+  int grid = tiles < max_ctas ? tiles : max_ctas;
+  if (grid >= 2) grid &= ~1;  // clusters of two: whole TPCs stay free for the pair GEMM
+  if (grid < 1) grid = 1;
+  cudaError_t e = set_smem_limit_once(k_lora_side, 232448);  // once per kernel: the largest size any rank needs
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kSideThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = grid >= 2 ? 1 : 0;
+  e = cudaLaunchKernelEx(&cfg, k_lora_side, ta, tb, prm);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace qlora

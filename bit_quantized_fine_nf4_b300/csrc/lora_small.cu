@@ -37,7 +37,11 @@ __device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, ui
 // g + 8, and the k order inside the two m16n8k16 steps is permuted the same way
 // for both operands so each fragment register holds 2 consecutive k.
 // MT_KMAJOR: mt is [r, K] (row j contiguous in k); otherwise mt is [K, r]
-// (the LoRA B matrix as stored) and each fragment gathers 8 strided values.
+// (the LoRA B matrix as stored).  STAGED: the CTA first copies mt into shared
+// memory as [RP rows j][K] (transposing [K, r]), rows padded by 16 bytes so the
+// 16-byte fragment loads of 8 rows x 4 threads hit distinct bank groups; every
+// tile then reads its fragments from there.  Unstaged, fragments come from
+// global memory (and gather 8 strided values when mt is [K, r]).
 // Side job (optional): cvt_dst[i] = bf16(cvt_scale * cvt_src[i]), spread over
 // all threads of the grid -- an independent elementwise pass in the same launch.
 template <int NT, bool MT_KMAJOR>
@@ -50,7 +54,7 @@ __device__ __forceinline__ uint4 load_mt_frag(const __nv_bfloat16* __restrict__ 
   return make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
 }
 
-template <int NT, bool MT_KMAJOR, int W>
+template <int NT, bool MT_KMAJOR, int W, bool STAGED>
 __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __restrict__ in,
                                                       const __nv_bfloat16* __restrict__ mt, int M, int K, int r,
                                                       float scale, float* __restrict__ out_f32,
@@ -59,9 +63,37 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
                                                       __nv_bfloat16* __restrict__ cvt_dst, int64_t cvt_n,
                                                       float cvt_scale) {
   constexpr int RP = NT * 8;
-  extern __shared__ float s_red[];  // [W warps][16 rows][RP]
+  extern __shared__ float s_red[];  // [W warps][16 rows][RP], then (STAGED) mt as [RP][K + 8] bf16
+  unsigned short* s_mt = reinterpret_cast<unsigned short*>(s_red + W * 16 * RP);
+  const int mt_pitch = K + 8;
   // the GEMM that consumes this kernel's output only needs it for its last k block
   griddep_launch_dependents();
+  if (STAGED) {
+    if (MT_KMAJOR) {
+      // rows j < r: 16-byte copies; rows r .. RP - 1: zero
+      const int per_row = K / 8;
+      for (int i = threadIdx.x; i < RP * per_row; i += W * 32) {
+        const int j = i / per_row, c = (i - j * per_row) * 8;
+        const uint4 v = j < r ? ldg_nc_v4(mt + static_cast<int64_t>(j) * K + c) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(s_mt + j * mt_pitch + c) = v;
+      }
+    } else {
+      // mt[k][j] -> s_mt[j][k]; one thread per (k, 8 j)
+      const int jg = RP / 8;
+      for (int i = threadIdx.x; i < K * jg; i += W * 32) {
+        const int k = i / jg, j0 = (i - k * jg) * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (j0 < r) v = *reinterpret_cast<const uint4*>(mt + static_cast<int64_t>(k) * r + j0);  // r % 8 == 0
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          s_mt[(j0 + 2 * e) * mt_pitch + k] = static_cast<unsigned short>(w[e] & 0xffffu);
+          s_mt[(j0 + 2 * e + 1) * mt_pitch + k] = static_cast<unsigned short>(w[e] >> 16);
+        }
+      }
+    }
+    __syncthreads();
+  }
   if (cvt_n > 0) {
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < cvt_n; i += nthreads)
@@ -72,7 +104,7 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
   const int n_chunks = (K + 31) / 32;  // K % 8 == 0: a thread's 8-wide slice is fully inside K or past it
   const int tiles = (M + 15) / 16;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  constexpr int UNROLL = (NT <= 2 && MT_KMAJOR) ? 4 : 2;
+  constexpr int UNROLL = (NT <= 2 && (MT_KMAJOR || STAGED)) ? 4 : 2;
   for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int m0 = tile * 16;
     const int rowa = m0 + g, rowb = m0 + g + 8;
@@ -92,7 +124,10 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
           const int j = t * 8 + g;
-          bv[u][t] = (kin && j < r) ? load_mt_frag<NT, MT_KMAJOR>(mt, j, kb, K, r) : zero;
+          if (STAGED)
+            bv[u][t] = kin ? *reinterpret_cast<const uint4*>(s_mt + j * mt_pitch + kb) : zero;
+          else
+            bv[u][t] = (kin && j < r) ? load_mt_frag<NT, MT_KMAJOR>(mt, j, kb, K, r) : zero;
         }
       }
 #pragma unroll
@@ -194,14 +229,26 @@ cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, i
   cfg.attrs = attr;
   cfg.numAttrs = grid >= 2 ? 1 : 0;
   cudaError_t e = cudaSuccess;
-#define QLORA_LD(NT, KM, W)                                                                                   \
-  do {                                                                                                        \
-    const size_t smem = static_cast<size_t>(W) * 16 * rp * sizeof(float);                                     \
-    set_smem_limit_once(k_lora_down<NT, KM, W>, smem);                                                        \
-    cfg.blockDim = dim3(W * 32);                                                                              \
-    cfg.dynamicSmemBytes = smem;                                                                              \
-    e = cudaLaunchKernelEx(&cfg, k_lora_down<NT, KM, W>, in, mt, M, K, r, scale, out_f32, out_bf16, cvt_src,  \
-                           cvt_dst, cvt_n, cvt_scale);                                                        \
+  // mt staged in shared memory when it fits beside the reduction buffer
+  const size_t stage_bytes = static_cast<size_t>(rp) * (static_cast<size_t>(K) + 8) * 2;
+  // (pays off only when each CTA walks several tiles)
+  const bool staged = tiles >= 4 * grid && stage_bytes + 16 * 16 * static_cast<size_t>(rp) * sizeof(float) <= 200 * 1024;
+#define QLORA_LD_ST(NT, KM, W, ST)                                                                               \
+  do {                                                                                                           \
+    const size_t smem = static_cast<size_t>(W) * 16 * rp * sizeof(float) + (ST ? stage_bytes : 0);               \
+    e = set_smem_limit_once(k_lora_down<NT, KM, W, ST>, ST ? 227 * 1024 : smem);                                 \
+    if (e != cudaSuccess) break;                                                                                 \
+    cfg.blockDim = dim3(W * 32);                                                                                 \
+    cfg.dynamicSmemBytes = smem;                                                                                 \
+    e = cudaLaunchKernelEx(&cfg, k_lora_down<NT, KM, W, ST>, in, mt, M, K, r, scale, out_f32, out_bf16, cvt_src, \
+                           cvt_dst, cvt_n, cvt_scale);                                                           \
+  } while (0)
+#define QLORA_LD(NT, KM, W)           \
+  do {                                \
+    if (staged)                       \
+      QLORA_LD_ST(NT, KM, W, true);   \
+    else                              \
+      QLORA_LD_ST(NT, KM, W, false);  \
   } while (0)
 #define QLORA_LD2(NT, W)     \
   do {                       \
@@ -216,6 +263,7 @@ cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, i
   else QLORA_LD2(16, 8);
 #undef QLORA_LD2
 #undef QLORA_LD
+#undef QLORA_LD_ST
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
