@@ -444,7 +444,7 @@ def traffic_for(kernel: str):
     if not os.path.exists(p):
         return None
     import hashlib
-    src = hashlib.sha1(open(os.path.join(ROOT, "bit_quantized_fine_nf4_b300", "csrc", "qgemm.cu"), "rb").read())
+    src = hashlib.sha1(open(os.path.join(ROOT, "bit_quantized_fine_nf4_b300", "csrc", "qgemm_pair.cu"), "rb").read())
     cur = src.hexdigest()[:12]
     for ln in open(p):
         parts = ln.split()
