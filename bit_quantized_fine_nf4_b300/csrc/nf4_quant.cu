@@ -140,10 +140,10 @@ __global__ void __launch_bounds__(256) k_nf4_quantize(const T* __restrict__ w, i
 // B[e] = sum of m over values with exponent field e (64-bit, exact for up to
 // 2^40 values).  The last CTA turns the bins into a 320-bit integer and
 // rounds it once to float64 (round to nearest, ties to even).
-__device__ double exact_bins_to_double(const unsigned long long* bins) {
+__device__ double exact_bins_to_double(const unsigned long long* bins) {  // bins: shared memory
   uint64_t limb[6] = {0, 0, 0, 0, 0, 0};  // little-endian 384-bit accumulator of sum * 2^149
   for (int e = 0; e < 255; ++e) {
-    const uint64_t v = __ldcg(bins + e);
+    const uint64_t v = bins[e];
     if (!v) continue;
     const int sh = (e < 1 ? 1 : e) - 1;  // 0..253
     const int li = sh >> 6, bo = sh & 63;
@@ -190,13 +190,27 @@ __global__ void __launch_bounds__(256) k_absmax_mean(const float* __restrict__ a
   __shared__ int s_last;
   for (int i = threadIdx.x; i < 256; i += blockDim.x) s_bins[i] = 0;
   __syncthreads();
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_a;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const uint32_t u = __float_as_uint(absmax[i]) & 0x7fffffffu;
-    const uint32_t e = u >> 23;
-    if (e >= 255) { latch_status(status, ST_NONFINITE); continue; }
-    const uint64_t m = (e == 0) ? (u & 0x7fffffu) : ((u & 0x7fffffu) | 0x800000u);
-    if (m) atomicAdd(&s_bins[e], static_cast<unsigned long long>(m));
+  // whole warps walk the array; lanes holding the same exponent add their
+  // mantissas in the warp (< 32 * 2^24, exact in 32 bits) and one of them adds
+  // the group's sum to the shared bin
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x; base < n_a; base += stride) {
+    const int64_t i = base + threadIdx.x;
+    uint32_t e = 256, m = 0;  // 256: no value in this lane
+    if (i < n_a) {
+      const uint32_t u = __float_as_uint(absmax[i]) & 0x7fffffffu;
+      e = u >> 23;
+      if (e >= 255) {
+        latch_status(status, ST_NONFINITE);
+        e = 256;
+      } else {
+        m = (e == 0) ? (u & 0x7fffffu) : ((u & 0x7fffffu) | 0x800000u);
+      }
+    }
+    const unsigned grp = __match_any_sync(0xffffffffu, e);
+    const unsigned sum = __reduce_add_sync(grp, m);
+    if (e < 255 && sum && (threadIdx.x & 31) == __ffs(grp) - 1)
+      atomicAdd(&s_bins[e], static_cast<unsigned long long>(sum));
   }
   __syncthreads();
   for (int i = threadIdx.x; i < 256; i += blockDim.x)
@@ -205,10 +219,15 @@ __global__ void __launch_bounds__(256) k_absmax_mean(const float* __restrict__ a
   __syncthreads();
   if (threadIdx.x == 0) s_last = (atomicAdd(counter, 1u) == gridDim.x - 1);
   __syncthreads();
-  if (s_last && threadIdx.x == 0) {
+  if (s_last) {
+    // the last CTA reads all bins at once, then one thread converts them exactly
     __threadfence();
-    const double s = exact_bins_to_double(bins);
-    *mean_out = __double2float_rn(__ddiv_rn(s, static_cast<double>(n_a)));
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) s_bins[i] = __ldcg(bins + i);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const double s = exact_bins_to_double(s_bins);
+      *mean_out = __double2float_rn(__ddiv_rn(s, static_cast<double>(n_a)));
+    }
   }
 }
 
