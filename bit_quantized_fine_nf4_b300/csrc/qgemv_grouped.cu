@@ -477,6 +477,218 @@ __global__ void __launch_bounds__(kGvThreads, 2) k_qgemv_grouped(const __grid_co
 static_assert(sizeof(GvParams) <= 32000, "kernel parameter budget");
 static_assert(sizeof(GlParams) <= 32000, "kernel parameter budget");
 
+// ====================================================================== CUDA-core decode (1..4 tokens)
+// With at most 4 tokens the tensor path is bound by the decode (four ALU ops
+// per weight); here the level lookup is one shared-memory load per two weights
+// from a byte-indexed table of (L[hi], L[lo]) bf16 pairs with one column per
+// lane (256 x 32 words: each lane reads its own bank, no conflicts), the block
+// scale a' multiplies a 32-weight partial sum, and every activation load serves
+// two rows.  The levels enter as bf16(L) times the float32 scale (the tensor
+// path rounds bf16(L a')); both are within a bf16 rounding of the exact
+// product.  A step is two 64-blocks; thread (g, c) of a warp owns rows g and
+// g + 8 of the warp's 16 and the 32 contiguous weights c (0..3) of the step
+// (block 2 step + c / 2); the 4 lanes of a row are added with shuffles at the
+// end.  Codes come through a per-thread cp.async ring (16 bytes per row per
+// step) kCcDepth steps ahead; block-scale bytes are read 4 blocks at a time;
+// activations are staged as float32 in windows of kCcWin columns, 4 floats of
+// padding after every 32 so the 4 chunks a warp reads sit in different banks.
+constexpr int kCcThreads = 256;
+constexpr int kCcDepth = 6;
+constexpr int kCcWin = 2048;
+constexpr int kCcXStride = kCcWin / 32 * 36;  // floats per staged token row
+template <int MT>
+constexpr size_t cc_smem() {
+  return 256 * 32 * 4 + static_cast<size_t>(kCcDepth) * kCcThreads * 32 + static_cast<size_t>(MT) * kCcXStride * 4;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kCcThreads, 2) k_gemv_cc(const __grid_constant__ GvParams p) {
+  extern __shared__ __align__(16) uint32_t sm_cc[];
+  uint32_t* tab = sm_cc;                                         // [256 bytes][32 lanes]
+  uint8_t* ring = reinterpret_cast<uint8_t*>(sm_cc + 256 * 32);  // [kCcDepth][2 rows][256 threads][16 B]
+  float* xs = reinterpret_cast<float*>(ring + kCcDepth * kCcThreads * 32);  // [MT][kCcXStride]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  for (int i = tid; i < 256 * 32; i += kCcThreads) {
+    const int b = i >> 5;  // byte: element 2i in the high nibble, 2i + 1 in the low nibble
+    const __nv_bfloat16 lo = __float2bfloat16_rn(nf4_level(b >> 4)), hi = __float2bfloat16_rn(nf4_level(b & 15));
+    tab[i] = static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(&lo)) |
+             (static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(&hi)) << 16);
+  }
+  const uint32_t ring_me = smem_u32(ring) + tid * 16;
+  const uint32_t tab_me = smem_u32(tab) + lane * 4;
+  for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
+    int lo_i = 0, hi_i = p.count - 1;  // problem of this item: last one with item0 <= item
+    while (lo_i < hi_i) {
+      const int mid = (lo_i + hi_i + 1) >> 1;
+      if (p.prob[mid].item0 <= item) lo_i = mid; else hi_i = mid - 1;
+    }
+    const uint8_t* codes = p.prob[lo_i].codes;
+    const int8_t* absq = p.prob[lo_i].absq;
+    const float* stepv = p.prob[lo_i].step;
+    const __nv_bfloat16* xg = p.prob[lo_i].x;
+    const int n = p.prob[lo_i].n, k = p.prob[lo_i].k, m = p.prob[lo_i].m;
+    const int row0 = (item - p.prob[lo_i].item0) * 128 + warp * 16 + g, row1 = row0 + 8;
+    const bool ok0 = row0 < n, ok1 = row1 < n;
+    const int kb_row = k / 64, nsteps = (kb_row + 1) / 2;
+    const float mu = *p.prob[lo_i].mean;
+    const uint8_t* cp0 = codes + static_cast<int64_t>(ok0 ? row0 : 0) * (k / 2) + c * 16;
+    const uint8_t* cp1 = codes + static_cast<int64_t>(ok1 ? row1 : 0) * (k / 2) + c * 16;
+    const int64_t ab0 = static_cast<int64_t>(ok0 ? row0 : 0) * kb_row, ab1 = static_cast<int64_t>(ok1 ? row1 : 0) * kb_row;
+    auto issue = [&](int st) {  // step st's 32 weights of both rows into the ring
+      const int kb = 2 * st + (c >> 1);
+      if (kb < kb_row) {
+        const uint32_t slot = ring_me + (st % kCcDepth) * (kCcThreads * 32);
+        if (ok0) cp_async16(slot, cp0 + st * 64);
+        if (ok1) cp_async16(slot + kCcThreads * 16, cp1 + st * 64);
+      }
+      cp_async_commit();
+    };
+    float acc0[MT], acc1[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) acc0[t] = acc1[t] = 0.f;
+    uint32_t q4_0 = 0, q4_1 = 0;  // block-scale bytes of blocks 4 qb .. 4 qb + 3 (little-endian)
+    int qb = -1;
+    int g0 = -1, g1 = -1;         // double-quant groups of the cached steps
+    float st0 = 0.f, st1 = 0.f;
+    __syncthreads();  // the table is built; the previous item is done with xs
+#pragma unroll 1
+    for (int d = 0; d < kCcDepth - 1; ++d) issue(d);
+    for (int w0 = 0; w0 < k; w0 += kCcWin) {
+      const int wlen = min(kCcWin, k - w0);
+      // activations of this window as float32 (rows t >= m are zero)
+      for (int i = tid; i < MT * (wlen / 8); i += kCcThreads) {
+        const int t = i / (wlen / 8), k8 = (i - t * (wlen / 8)) * 8;
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (t < m) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xg + static_cast<int64_t>(t) * k + w0 + k8);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            f[2 * e] = __uint_as_float(w[e] << 16);
+            f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+          }
+        }
+        float4* dst = reinterpret_cast<float4*>(xs + t * kCcXStride + k8 + (k8 >> 5) * 4);
+        dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+        dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+      }
+      __syncthreads();
+      const int s0 = w0 / 128, s1 = (w0 + wlen + 127) / 128;
+      for (int st = s0; st < s1; ++st) {
+        issue(st + kCcDepth - 1);
+        const int kb = 2 * st + (c >> 1);
+        const bool kin = kb < kb_row;
+        if (kin && (kb >> 2) != qb) {  // 4 scale bytes at a time (kb_row % 4 == 0 keeps them aligned)
+          qb = kb >> 2;
+          const int kb4 = kb & ~3;
+          if ((kb_row & 3) == 0) {
+            if (ok0) q4_0 = *reinterpret_cast<const uint32_t*>(absq + ab0 + kb4);
+            if (ok1) q4_1 = *reinterpret_cast<const uint32_t*>(absq + ab1 + kb4);
+          } else {
+            q4_0 = q4_1 = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              if (kb4 + e < kb_row) {
+                if (ok0) q4_0 |= static_cast<uint32_t>(static_cast<uint8_t>(absq[ab0 + kb4 + e])) << (8 * e);
+                if (ok1) q4_1 |= static_cast<uint32_t>(static_cast<uint8_t>(absq[ab1 + kb4 + e])) << (8 * e);
+              }
+            }
+          }
+        }
+        const int gr0 = static_cast<int>((ab0 + kb) >> 8), gr1 = static_cast<int>((ab1 + kb) >> 8);
+        if (kin && gr0 != g0) { g0 = gr0; st0 = ok0 ? stepv[gr0] : 0.f; }
+        if (kin && gr1 != g1) { g1 = gr1; st1 = ok1 ? stepv[gr1] : 0.f; }
+        const int sh = 8 * (kb & 3);
+        const float a0 = (ok0 && kin) ? restore_absmax(static_cast<int8_t>((q4_0 >> sh) & 0xffu), st0, mu) : 0.f;
+        const float a1 = (ok1 && kin) ? restore_absmax(static_cast<int8_t>((q4_1 >> sh) & 0xffu), st1, mu) : 0.f;
+        cp_async_wait<kCcDepth - 1>();
+        const uint32_t slot = ring_me + (st % kCcDepth) * (kCcThreads * 32);
+        const uint4 cw0 = lds_v4(slot), cw1 = lds_v4(slot + kCcThreads * 16);
+        const uint32_t wr0[4] = {cw0.x, cw0.y, cw0.z, cw0.w}, wr1[4] = {cw1.x, cw1.y, cw1.z, cw1.w};
+        float sa0[MT], sa1[MT];
+#pragma unroll
+        for (int t = 0; t < MT; ++t) sa0[t] = sa1[t] = 0.f;
+        const float* xk = xs + ((st * 128 - w0) / 32 + c) * 36;  // the thread's 32 columns, padded layout
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {  // 8 weights = one 32-bit code word per row
+          float xv[MT][8];
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            const float4 u = *reinterpret_cast<const float4*>(xk + t * kCcXStride + h * 8);
+            const float4 v = *reinterpret_cast<const float4*>(xk + t * kCcXStride + h * 8 + 4);
+            xv[t][0] = u.x; xv[t][1] = u.y; xv[t][2] = u.z; xv[t][3] = u.w;
+            xv[t][4] = v.x; xv[t][5] = v.y; xv[t][6] = v.z; xv[t][7] = v.w;
+          }
+          const uint32_t c0w = (ok0 && kin) ? wr0[h] : 0u, c1w = (ok1 && kin) ? wr1[h] : 0u;
+#pragma unroll
+          for (int bi = 0; bi < 4; ++bi) {
+            uint32_t e0, e1;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(e0) : "r"(tab_me + ((c0w >> (8 * bi)) & 0xffu) * 128));
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(e1) : "r"(tab_me + ((c1w >> (8 * bi)) & 0xffu) * 128));
+            const float l00 = __uint_as_float(e0 << 16), l01 = __uint_as_float(e0 & 0xffff0000u);
+            const float l10 = __uint_as_float(e1 << 16), l11 = __uint_as_float(e1 & 0xffff0000u);
+#pragma unroll
+            for (int t = 0; t < MT; ++t) {
+              sa0[t] = fmaf(xv[t][2 * bi], l00, fmaf(xv[t][2 * bi + 1], l01, sa0[t]));
+              sa1[t] = fmaf(xv[t][2 * bi], l10, fmaf(xv[t][2 * bi + 1], l11, sa1[t]));
+            }
+          }
+        }
+        if (kin) {  // past the last block the activations read are stale: nothing is added
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            acc0[t] = fmaf(a0, sa0[t], acc0[t]);
+            acc1[t] = fmaf(a1, sa1[t], acc1[t]);
+          }
+        }
+      }
+      __syncthreads();  // xs is rewritten by the next window
+    }
+    cp_async_wait<0>();
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      acc0[t] += __shfl_xor_sync(0xffffffffu, acc0[t], 1);
+      acc0[t] += __shfl_xor_sync(0xffffffffu, acc0[t], 2);
+      acc1[t] += __shfl_xor_sync(0xffffffffu, acc1[t], 1);
+      acc1[t] += __shfl_xor_sync(0xffffffffu, acc1[t], 2);
+    }
+    // LoRA up-projection: + sum_j st[t][j] B[row][j]; the 4 lanes of a row split j
+    const __nv_bfloat16* lb = p.prob[lo_i].lora_b;
+    const __nv_bfloat16* stv = p.prob[lo_i].st;
+    const int r = p.prob[lo_i].r, jq = r / 4;  // r % 8 == 0
+    float l0[MT], l1[MT];
+#pragma unroll
+    for (int t = 0; t < MT; ++t) l0[t] = l1[t] = 0.f;
+    for (int j = c * jq; j < (c + 1) * jq; ++j) {
+      const float b0 = ok0 ? __bfloat162float(lb[static_cast<int64_t>(row0) * r + j]) : 0.f;
+      const float b1 = ok1 ? __bfloat162float(lb[static_cast<int64_t>(row1) * r + j]) : 0.f;
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const float sv = t < m ? __bfloat162float(stv[static_cast<int64_t>(t) * r + j]) : 0.f;
+        l0[t] = fmaf(sv, b0, l0[t]);
+        l1[t] = fmaf(sv, b1, l1[t]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < MT; ++t) {
+      l0[t] += __shfl_xor_sync(0xffffffffu, l0[t], 1);
+      l0[t] += __shfl_xor_sync(0xffffffffu, l0[t], 2);
+      l1[t] += __shfl_xor_sync(0xffffffffu, l1[t], 1);
+      l1[t] += __shfl_xor_sync(0xffffffffu, l1[t], 2);
+    }
+    if (c == 0) {
+      __nv_bfloat16* y = p.prob[lo_i].y;
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        if (t >= m) break;
+        if (ok0) y[static_cast<int64_t>(t) * n + row0] = __float2bfloat16_rn(acc0[t] + l0[t]);
+        if (ok1) y[static_cast<int64_t>(t) * n + row1] = __float2bfloat16_rn(acc1[t] + l1[t]);
+      }
+    }
+  }
+}
+
 int fwd_grouped_max_problems() { return kGvMaxProbs; }
 
 cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws, unsigned* status, uint64_t wait_ns,
@@ -489,7 +701,7 @@ cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws,
   memset(&gl, 0, sizeof(gl));
   char* base = static_cast<char*>(ws);
   size_t off = 0;
-  int items = 0, rmax = 8;
+  int items = 0, rmax = 8, mmax = 1;
   for (int i = 0; i < count; ++i) {
     const GroupedProblem& q = probs[i];
     __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(base + off);
@@ -519,6 +731,7 @@ cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws,
     l.r = q.r;
     l.scale = q.alpha / static_cast<float>(q.r);
     if (q.r > rmax) rmax = q.r;
+    if (q.m > mmax) mmax = q.m;
   }
   gv.count = count;
   gv.total_items = items;
@@ -539,10 +752,24 @@ cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws,
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  e = set_smem_limit_once(k_qgemv_grouped, kGvSmem);
-  if (e != cudaSuccess) return e;
   int grid = 2 * num_sms;
   if (grid > items) grid = items;
+  if (mmax <= 2) {
+    // CUDA-core decode for 1 or 2 token columns (with more, the FMAs per weight
+    // catch up with the tensor path's decode cost)
+#define QLORA_CC(MT)                                                              \
+  do {                                                                            \
+    e = set_smem_limit_once(k_gemv_cc<MT>, cc_smem<MT>());                        \
+    if (e == cudaSuccess) k_gemv_cc<MT><<<grid, kCcThreads, cc_smem<MT>(), s>>>(gv); \
+  } while (0)
+    if (mmax == 1) QLORA_CC(1);
+    else QLORA_CC(2);
+#undef QLORA_CC
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
+  e = set_smem_limit_once(k_qgemv_grouped, kGvSmem);
+  if (e != cudaSuccess) return e;
   k_qgemv_grouped<<<grid, kGvThreads, kGvSmem, s>>>(gv);
   return cudaGetLastError();
 }

@@ -58,3 +58,26 @@ def test_grouped_rejects_large_token_counts(lib):
         lib.linear_fwd_grouped([(c.x, rec, c.a, c.b, c.alpha, None, None)])
     assert e.value.code == lib.QLORA_ERR_UNSUPPORTED
     lib.check_status()
+
+
+SMALL_SHAPES = [  # at most 1 / 2 tokens: the CUDA-core decode path; at most 4: the tensor path
+    (4096, 4096, 1, 16), (4096, 11008, 4, 16), (11008, 4096, 2, 16), (136, 640, 3, 8),
+    (264, 320, 4, 64), (128, 64, 1, 8), (512, 4160, 2, 24), (1032, 2112, 1, 32),
+]
+
+
+@pytest.mark.parametrize("mmax", [1, 2, 4])
+def test_grouped_small_token_path(lib, mmax):
+    shapes = [(n, k, min(m, mmax), r) for (n, k, m, r) in SMALL_SHAPES]
+    cases = [synthetic.linear_case(n, k, m, r, 2.0 * r, device="cuda", base_seed=700 + 10 * i + mmax)
+             for i, (n, k, m, r) in enumerate(shapes)]
+    recs = [lib.quantize(c.w) for c in cases]
+    probs = [(c.x, rec, c.a, c.b, c.alpha, None, None) for c, rec in zip(cases, recs)]
+    ys = lib.linear_fwd_grouped(probs)
+    lib.check_status()
+    for i, (c, rec) in enumerate(zip(cases, recs)):
+        n, k = c.w.shape
+        ref = nf4.quantize(to_np32(c.w.cpu()), n, k)
+        wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
+        yr, _ = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
+        assert rel_fro(to_np64(ys[i]), yr) < GEMM_TOL, shapes[i]
