@@ -1,5 +1,6 @@
 // Grouped small-token forward (decode): Y_p = X_p deq(W_p)^T + s_p (X_p A_p^T) B_p^T
-// for a list of independent problems p (1..16 tokens each), in two launches.
+// for a list of independent problems p (1..16 tokens each), in two launches
+// (k_gemv_cc on the CUDA cores when no problem has more than 2 tokens).
 //
 // Glossary "QLoRA", "How QLoRA works": the frozen layer dequantises NF4 to
 // bf16 before the matmul and adds the LoRA output; Day 25 notes section 4.4:
@@ -13,7 +14,10 @@
 //                      to the CTAs.  Per 64-wide k block ("stage"):
 //   - a stage is two 64-wide k blocks; producer warps 1-4 decode the even
 //     block, warps 5-8 the odd one, one weight row per thread, into TMEM
-//     (tcgen05 A operand, M = 128).  Each thread prefetches its row's codes,
+//     (tcgen05 A operand, M = 128): a weight pair is a bf16 (L[hi], L[lo])
+//     pair from a byte-indexed shared-memory table (one column per lane, no
+//     bank conflicts) times bf16(a') in one packed multiply (within a bf16
+//     rounding of bf16(L a'); the fwd/bwd GEMMs keep the exact bf16(L a')).  Each thread prefetches its row's codes,
 //     block-scale byte, group step and mean, plus one 16-byte slice of the
 //     16-token activation tile (later of the sT tile), with cp.async into a
 //     private shared-memory ring kPrefetch stages ahead, with a meta word that
@@ -147,13 +151,19 @@ constexpr uint32_t kGvBBytes = 2 * kGvTok * 128;  // two 64-wide slabs of 16 tok
 constexpr uint32_t kGvDCol = kGvStages * 64;
 constexpr uint32_t kGvTmemCols = 256;
 constexpr uint32_t kGvSlot = 64;
-constexpr size_t kGvSmem = 1024 + kGvStages * kGvBBytes + 256 * kGvPrefetch * kGvSlot + (2 * kGvStages + 4) * 8 + 16;
+constexpr size_t kGvTab = 256 * 32 * 4;  // level-pair table, one column per lane
+constexpr size_t kGvSmem =
+    1024 + kGvStages * kGvBBytes + 256 * kGvPrefetch * kGvSlot + kGvTab + (2 * kGvStages + 4) * 8 + 16;
 static_assert(kGvDCol + 2 * kGvTok <= kGvTmemCols, "TMEM budget");
 
-// Slot layout (one per producer thread per prefetched stage):
-//   [0,32) codes of the thread's row and k block   [32,48) activation slice
-//   [48,52) word holding the block-scale byte       [52,56) group step
-//   [56,60) per-tensor mean                         [60,64) meta (written by the thread)
+// Slots of a prefetched stage, one per producer thread, stored field by field
+// (structure of arrays: consecutive threads at consecutive 16- or 4-byte
+// addresses, so the slot reads and the cp.async writes are free of bank
+// conflicts): codes of the thread's row and k block (two 16-byte halves),
+// activation slice, word holding the block-scale byte, group step, per-tensor
+// mean, meta (written by the thread).
+constexpr uint32_t kGvFCode0 = 0, kGvFCode1 = 16 * 256, kGvFAct = 32 * 256, kGvFScale = 48 * 256,
+                   kGvFStep = 52 * 256, kGvFMean = 56 * 256, kGvFMeta = 60 * 256;
 enum : uint32_t {
   kMetaValid = 1u,      // the stage exists
   kMetaLora = 2u,       // LoRA stage (A = B rows, B operand = sT)
@@ -250,10 +260,10 @@ __device__ __forceinline__ void sts_u32(uint32_t saddr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(saddr), "r"(v) : "memory");
 }
 
-// Prefetch this thread's share of stage `w` into the slot at `sa`: half h takes
-// k block 2l+h of row `row`, and activation slice (token tt/8, chunk tt%8) of
-// slab h.  Always commits one cp.async group.
-__device__ __forceinline__ void gv_prefetch(const GvWalk& w, int half, int rlocal, int tt, uint32_t sa) {
+// Prefetch this thread's share of stage `w` into its slot of the prefetch stage
+// at `sa` (thread t): half h takes k block 2l+h of row `row`, and activation
+// slice (token tt/8, chunk tt%8) of slab h.  Always commits one cp.async group.
+__device__ __forceinline__ void gv_prefetch(const GvWalk& w, int half, int rlocal, int tt, uint32_t sa, int t) {
   uint32_t meta = 0;
   if (!w.done) {
     meta = kMetaValid | (static_cast<uint32_t>(w.p) << 16) | (w.l == w.nst - 1 ? kMetaLast : 0u);
@@ -264,26 +274,26 @@ __device__ __forceinline__ void gv_prefetch(const GvWalk& w, int half, int rloca
       const bool kin = blk < w.kb;
       if (kin && row < w.n) {
         const uint8_t* cp = w.codes + static_cast<int64_t>(row) * (w.k / 2) + blk * 32;
-        cp_async16(sa, cp);
-        cp_async16(sa + 16, cp + 16);
+        cp_async16(sa + kGvFCode0 + t * 16, cp);
+        cp_async16(sa + kGvFCode1 + t * 16, cp + 16);
         const int64_t ai = static_cast<int64_t>(row) * w.kb + blk;
-        cp_async4(sa + 48, w.absq + (ai & ~int64_t(3)));
-        cp_async4(sa + 52, w.step + (ai >> 8));
-        cp_async4(sa + 56, w.mean);
+        cp_async4(sa + kGvFScale + t * 4, w.absq + (ai & ~int64_t(3)));
+        cp_async4(sa + kGvFStep + t * 4, w.step + (ai >> 8));
+        cp_async4(sa + kGvFMean + t * 4, w.mean);
         meta |= kMetaRowOk | (static_cast<uint32_t>(ai & 3) << 3);
       }
       const bool v = kin && tok < w.m;
-      cp_async16_zfill(sa + 32, w.x + (v ? static_cast<int64_t>(tok) * w.k + blk * 64 + ch * 8 : 0), v);
+      cp_async16_zfill(sa + kGvFAct + t * 16, w.x + (v ? static_cast<int64_t>(tok) * w.k + blk * 64 + ch * 8 : 0), v);
     } else {
       meta |= kMetaLora;
       const int jb = half * 64;
       if (row < w.n && jb < w.r) meta |= kMetaRowOk;
       const int col = jb + ch * 8;
       const bool v = tok < w.m && col < w.r;
-      cp_async16_zfill(sa + 32, w.st + (v ? static_cast<int64_t>(tok) * w.r + col : 0), v);
+      cp_async16_zfill(sa + kGvFAct + t * 16, w.st + (v ? static_cast<int64_t>(tok) * w.r + col : 0), v);
     }
   }
-  sts_u32(sa + 60, meta);
+  sts_u32(sa + kGvFMeta + t * 4, meta);
   cp_async_commit();
 }
 
@@ -292,7 +302,8 @@ __global__ void __launch_bounds__(kGvThreads, 2) k_qgemv_grouped(const __grid_co
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sb = smem;                             // [kGvStages][2 slabs][16 rows][128 B]
   uint8_t* slots = smem + kGvStages * kGvBBytes;  // [kGvPrefetch][256 threads][kGvSlot]
-  uint64_t* full = reinterpret_cast<uint64_t*>(slots + 256 * kGvPrefetch * kGvSlot);
+  uint32_t* tab = reinterpret_cast<uint32_t*>(slots + 256 * kGvPrefetch * kGvSlot);  // [256 bytes][32 lanes]
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(tab) + kGvTab);
   uint64_t* empty = full + kGvStages;
   uint64_t* acc_full = empty + kGvStages;  // [2]
   uint64_t* acc_empty = acc_full + 2;      // [2]
@@ -316,6 +327,13 @@ __global__ void __launch_bounds__(kGvThreads, 2) k_qgemv_grouped(const __grid_co
   if (warp == 0) {
     __syncwarp();
     tmem_alloc(tmem_holder, kGvTmemCols);
+  }
+  // level pairs (L[hi nibble], L[lo nibble]) as bf16, same in every column
+  for (int i = threadIdx.x; i < 256 * 32; i += kGvThreads) {
+    const int b = i >> 5;
+    const __nv_bfloat16 lo = __float2bfloat16_rn(nf4_level(b >> 4)), hi = __float2bfloat16_rn(nf4_level(b & 15));
+    tab[i] = static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(&lo)) |
+             (static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(&hi)) << 16);
   }
   tc_fence_before();
   __syncthreads();
@@ -366,13 +384,13 @@ __global__ void __launch_bounds__(kGvThreads, 2) k_qgemv_grouped(const __grid_co
     const int t = threadIdx.x - 32;                // slot index 0..255
     const int tt = ((warp - 1) & 3) * 32 + lane;   // activation slice 0..127 of slab `half`
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t slot0 = smem_u32(slots) + t * kGvSlot;
+    const uint32_t slot0 = smem_u32(slots);
     auto slot_addr = [&](int u) { return slot0 + static_cast<uint32_t>(u % kGvPrefetch) * 256 * kGvSlot; };
 
     GvWalk pre;
     gv_begin(p, pre);
     for (int u = 0; u < kGvPrefetch; ++u) {
-      gv_prefetch(pre, half, rlocal, tt, slot_addr(u));
+      gv_prefetch(pre, half, rlocal, tt, slot_addr(u), t);
       if (!pre.done) gv_next(p, pre);
     }
 
@@ -411,21 +429,31 @@ __global__ void __launch_bounds__(kGvThreads, 2) k_qgemv_grouped(const __grid_co
     while (alive) {
       cp_async_wait<kGvPrefetch - 1>();
       const uint32_t sa = slot_addr(u);
-      const uint32_t meta = lds_u32(sa + 60);
+      const uint32_t meta = lds_u32(sa + kGvFMeta + t * 4);
       if (!(meta & kMetaValid)) break;
       const int s = u % kGvStages;
       const uint32_t ph = (u / kGvStages) & 1;
-      const uint4 act = lds_v4(sa + 32);
+      const uint4 act = lds_v4(sa + kGvFAct + t * 16);
       uint32_t words[32];
       if (!(meta & kMetaRowOk)) {
 #pragma unroll
         for (int c = 0; c < 32; ++c) words[c] = 0;
       } else if (!(meta & kMetaLora)) {
-        const uint4 c0 = lds_v4(sa), c1 = lds_v4(sa + 16);
-        const uint32_t qw = lds_u32(sa + 48);
+        const uint4 c0 = lds_v4(sa + kGvFCode0 + t * 16), c1 = lds_v4(sa + kGvFCode1 + t * 16);
+        const uint32_t qw = lds_u32(sa + kGvFScale + t * 4);
         const int8_t qv = static_cast<int8_t>((qw >> (8 * ((meta >> 3) & 3))) & 0xffu);
-        const float a2 = restore_absmax(qv, __uint_as_float(lds_u32(sa + 52)), __uint_as_float(lds_u32(sa + 56)));
-        nf4_decode_block(c0, c1, a2, words);
+        const float a2 = restore_absmax(qv, __uint_as_float(lds_u32(sa + kGvFStep + t * 4)),
+                                        __uint_as_float(lds_u32(sa + kGvFMean + t * 4)));
+        // weight pair = bf16(L) pair (one conflict-free table load) times bf16(a') in one packed multiply
+        const __nv_bfloat162 a2b = __float2bfloat162_rn(a2);
+        const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const uint32_t tab_me = smem_u32(tab) + lane * 4;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t e = lds_u32(tab_me + ((cw[i >> 2] >> (8 * (i & 3))) & 0xffu) * 128);
+          const __nv_bfloat162 v = __hmul2(*reinterpret_cast<const __nv_bfloat162*>(&e), a2b);
+          words[i] = *reinterpret_cast<const uint32_t*>(&v);
+        }
       } else {
         const GvProb& pr = p.prob[meta >> 16];
         const int row = (blockIdx.x + j * gridDim.x - pr.item0) * 128 + rlocal;
@@ -436,7 +464,7 @@ __global__ void __launch_bounds__(kGvThreads, 2) k_qgemv_grouped(const __grid_co
       }
       // refill the slot with the stage kGvPrefetch ahead (its contents are in registers now)
       __syncwarp();
-      gv_prefetch(pre, half, rlocal, tt, sa);
+      gv_prefetch(pre, half, rlocal, tt, sa, t);
       if (!pre.done) gv_next(p, pre);
 
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort));
