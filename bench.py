@@ -314,8 +314,13 @@ def decode_sweep(q, torch, layers: int = 32, tokens=(1, 4, 16), passes: int = 10
     return out
 
 
-def dequant_quant_rates(q, torch, rec, w, flush):
-    n, k = rec.n, rec.k
+def dequant_quant_rates(q, torch, flush, n=22016, k=8192):
+    """Quantise / dequantise rates on one 22016x8192 matrix (the Llama-65B up-projection shape:
+    360 MB of bf16 per call, so the per-launch overhead of a few microseconds does not dominate)."""
+    import synthetic
+    w = synthetic.weight(n, k, device="cuda", seed=2201)
+    rec = q.quantize(w)
+    q.check_status()
     out_b = torch.empty((n, k), dtype=torch.bfloat16, device="cuda")
     for _ in range(3):
         q.dequantize(rec, out=out_b)
@@ -328,6 +333,8 @@ def dequant_quant_rates(q, torch, rec, w, flush):
     msq = statistics.median(time_events(torch, lambda: q.quantize(w, out=rec2, workspace=wsq), 10, flush))
     q.check_status()
     quant_bytes = n * k * 2 + rec.nbytes()
+    del w, rec, rec2, out_b, wsq
+    torch.cuda.empty_cache()
     return {"dequant": {"shape": [n, k], "ms": ms, "gbs": deq_bytes / ms / 1e6, "bytes": deq_bytes},
             "quantize": {"shape": [n, k], "ms": msq, "gbs": quant_bytes / msq / 1e6, "bytes": quant_bytes,
                          "kernels": 3}}
@@ -601,7 +608,7 @@ def run_ours(args, world, rank, local):
                                  "tflops": flops * world / (eager_ms_step / 1e3) / 1e12},
                  "kernels_per_step": kernels_per_step}
     if not args.quick:
-        secondary.update(dequant_quant_rates(q, torch, rec, case.w, flush))
+        secondary.update(dequant_quant_rates(q, torch, flush))
         del y, dx
         torch.cuda.empty_cache()
         sweep = decode_sweep(q, torch, layers=args.decode_layers)

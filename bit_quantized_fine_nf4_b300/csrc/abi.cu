@@ -235,7 +235,7 @@ int qlora_nf4_quantize(const void* w, int w_dtype, int64_t n, int64_t k, const q
   Span sp(P_QUANTIZE, static_cast<cudaStream_t>(stream), 3);
   return cuda_ret(qlora::launch_nf4_quantize(w, w_dtype == QLORA_DTYPE_F32 ? 0 : 1, n * k, out->codes, absmax,
                                              out->absmax_q, out->absmax_step, out->absmax_mean, bins, di->status,
-                                             di->num_sms, static_cast<cudaStream_t>(stream)),
+                                             g_wait_ns.load(), di->num_sms, static_cast<cudaStream_t>(stream)),
                   "quantize");
 }
 
@@ -260,7 +260,7 @@ int qlora_nf4_quantize_noalloc(const void* w, int w_dtype, int64_t n, int64_t k,
   Span sp(P_QUANTIZE, static_cast<cudaStream_t>(stream), 3);
   return cuda_ret(qlora::launch_nf4_quantize(w, w_dtype == QLORA_DTYPE_F32 ? 0 : 1, n * k, out->codes, absmax,
                                              out->absmax_q, out->absmax_step, out->absmax_mean, bins, di->status,
-                                             di->num_sms, static_cast<cudaStream_t>(stream)),
+                                             g_wait_ns.load(), di->num_sms, static_cast<cudaStream_t>(stream)),
                   "quantize (no allocation)");
 }
 

@@ -19,7 +19,7 @@ enum : unsigned {
 // nf4_quant.cu
 cudaError_t launch_nf4_quantize(const void* w, int w_dtype, int64_t n_elems, uint8_t* codes, float* absmax,
                                 int8_t* absq, float* step, float* mean, void* ws_bins, unsigned* status,
-                                int num_sms, cudaStream_t s);
+                                uint64_t wait_ns, int num_sms, cudaStream_t s);
 // Fixed scratch of the no-allocation quantise entry point (nf4_quant.cu).
 int64_t noalloc_max_weights();
 cudaError_t noalloc_scratch(float** absmax, void** bins);

@@ -87,6 +87,51 @@ def test_encode_boundaries_and_special_blocks(lib):
     _assert_record_equal(lib, rec, nf4.quantize(full, n, 64), n, 64)
 
 
+def _bf16_threshold_blocks():
+    """bf16 blocks of 64: for absmax values a spread over the whole bf16 exponent
+    range (subnormal to 2^126), the eight bf16 values on each side of a * m_j for
+    every decision boundary m_j (the midpoint of two neighbouring NF4 levels),
+    both signs, with a itself in the block's last slot."""
+    lv = nf4.nf4_levels_f32().astype(np.float64)
+    mids = (lv[:-1] + lv[1:]) / 2
+    abits = sorted(set(list(range(0x0001, 0x7f80, 0x00c7)) +
+                       [0x0080, 0x00ff, 0x0100, 0x0101, 0x3f80, 0x3f81, 0x3fff, 0x7dff, 0x7e00, 0x7e01, 0x7f7f]))
+    blocks = []
+    for ab in abits:
+        a = nf4.bf16_bits_to_f32(np.array([ab], dtype=np.uint16))[0]
+        vals = []
+        for m in mids:
+            tb = int(nf4.f32_to_bf16_bits(np.array([abs(a * m)], dtype=np.float32))[0])
+            for mag in range(max(tb - 8, 0), tb + 9):
+                if mag <= ab:
+                    vals.append(mag | (0x8000 if m < 0 else 0))
+        vals = np.array(vals, dtype=np.uint16)
+        for c0 in range(0, vals.size, 63):
+            blk = np.zeros(64, dtype=np.uint16)
+            chunk = vals[c0:c0 + 63]
+            blk[:chunk.size] = chunk
+            blk[63] = ab
+            blocks.append(blk)
+    while len(blocks) % 8:  # rows of the [n, 64] weight: n a multiple of 8
+        blocks.append(np.zeros(64, dtype=np.uint16))
+    bits = np.stack(blocks)
+    return nf4.bf16_bits_to_f32(bits.reshape(-1)).reshape(bits.shape)
+
+
+def test_bf16_codes_near_every_boundary_all_exponents(lib):
+    """The bf16 path takes the quotient from the rounded reciprocal with one
+    correction and the code from a bucket table; its codes must equal the
+    oracle's (IEEE quotient, nearest level, lower index on ties) for weights
+    packed around every decision boundary at every block-scale exponent."""
+    w = _bf16_threshold_blocks()
+    n = w.shape[0]
+    rec = lib.quantize(torch.from_numpy(w).to(torch.bfloat16).cuda())
+    lib.check_status()
+    a = nf4.blockwise_absmax(w)
+    ref = nf4.pack_codes(nf4.nf4_encode(w.reshape(-1), a))
+    assert np.array_equal(rec.codes.cpu().numpy(), ref), "4-bit codes differ"
+
+
 def test_nonfinite_is_reported(lib):
     w = synthetic.weight(16, 128, device="cuda", seed=3)
     w[5, 17] = float("nan")
