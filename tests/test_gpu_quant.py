@@ -132,6 +132,37 @@ def test_bf16_codes_near_every_boundary_all_exponents(lib):
     assert np.array_equal(rec.codes.cpu().numpy(), ref), "4-bit codes differ"
 
 
+def test_bf16_every_weight_value_for_sampled_scales(lib):
+    """For 200 block scales a (bf16) spread over the whole exponent range --
+    subnormal, both edges of the range where the bf16 path decides without a
+    quotient (2^-90 and 2^120), and ordinary values -- blocks holding every bf16
+    weight w with |w| <= a, both signs: all codes equal the oracle's."""
+    rng = np.random.default_rng(2024)
+    edges = [0x0001, 0x007f, 0x0080, 0x0100, 0x127f, 0x1280, 0x1281, 0x3c00, 0x3f80, 0x3fff,
+             0x7b7f, 0x7b80, 0x7b81, 0x7f7f]
+    abits = sorted(set(edges + list(rng.integers(1, 0x7f80, size=186))))
+    blocks = []
+    for ab in abits:
+        mags = np.arange(0, ab + 1, dtype=np.uint32)
+        vals = np.concatenate([mags, mags[1:] | 0x8000]).astype(np.uint16)
+        nb = (vals.size + 62) // 63
+        blk = np.zeros((nb, 64), dtype=np.uint16)
+        flat = blk[:, :63].reshape(-1)
+        flat[:vals.size] = vals
+        blk[:, :63] = flat.reshape(nb, 63)
+        blk[:, 63] = ab
+        blocks.append(blk)
+    bits = np.concatenate(blocks)
+    pad = (-bits.shape[0]) % 8
+    if pad:
+        bits = np.concatenate([bits, np.zeros((pad, 64), dtype=np.uint16)])
+    w = nf4.bf16_bits_to_f32(bits.reshape(-1)).reshape(bits.shape)
+    rec = lib.quantize(torch.from_numpy(w).to(torch.bfloat16).cuda())
+    lib.check_status()
+    ref = nf4.pack_codes(nf4.nf4_encode(w.reshape(-1), nf4.blockwise_absmax(w)))
+    assert np.array_equal(rec.codes.cpu().numpy(), ref), "4-bit codes differ"
+
+
 def test_nonfinite_is_reported(lib):
     w = synthetic.weight(16, 128, device="cuda", seed=3)
     w[5, 17] = float("nan")
