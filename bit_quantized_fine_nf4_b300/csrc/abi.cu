@@ -416,33 +416,22 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
   return cuda_ret(e, "bwd dx gemm");
 }
 
-int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problems, int count, size_t* bytes) {
-  if (!bytes) return fail(QLORA_ERR_INVALID_ARGUMENT, "bytes is NULL");
-  if (count < 0 || (count > 0 && !problems)) return fail(QLORA_ERR_INVALID_ARGUMENT, "problems");
-  size_t tot = 0;
-  for (int i = 0; i < count; ++i) tot += (static_cast<size_t>(problems[i].m) * problems[i].r * 2 + 255) & ~size_t(255);
-  *bytes = tot;
-  return QLORA_OK;
-}
-
-int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, void* workspace, size_t workspace_bytes,
-                             void* stream) {
-  DevInfo* di = nullptr;
-  int rc = device(&di);
-  if (rc) return rc;
-  if (count < 0 || (count > 0 && !problems)) return fail(QLORA_ERR_INVALID_ARGUMENT, "problems");
-  if (count == 0) return QLORA_OK;
-  std::vector<qlora::GroupedProblem> gp(static_cast<size_t>(count));
-  size_t need = 0;
+// The grouped problems as the launcher sees them (shapes only are needed for the workspace plan).
+static int grouped_problems(const qlora_linear_problem* problems, int count, std::vector<qlora::GroupedProblem>& gp,
+                            bool check_pointers) {
+  gp.assign(static_cast<size_t>(count), qlora::GroupedProblem{});
+  int rc = 0;
   for (int i = 0; i < count; ++i) {
     const qlora_linear_problem& q = problems[i];
     if ((rc = check_weight(q.w))) return fail(rc, "problem %d: %s", i, t_last_error);
     if (q.m < 1 || q.m > 16) return fail(QLORA_ERR_UNSUPPORTED, "problem %d: m = %lld (the grouped path takes 1..16 tokens)", i, (long long)q.m);
     if (q.r < 8 || q.r > 64 || (q.r % 8)) return fail(QLORA_ERR_UNSUPPORTED, "problem %d: r = %d (grouped path: 8 <= r <= 64, r %% 8 == 0)", i, q.r);
-    if ((rc = check_ptr(q.x, "x")) || (rc = check_ptr(q.lora_a, "lora_a")) || (rc = check_ptr(q.lora_b, "lora_b")) ||
-        (rc = check_ptr(q.y, "y")))
-      return fail(rc, "problem %d: %s", i, t_last_error);
-    if (q.t_save && !aligned16(q.t_save)) return fail(QLORA_ERR_INVALID_ARGUMENT, "problem %d: t_save not 16-byte aligned", i);
+    if (check_pointers) {
+      if ((rc = check_ptr(q.x, "x")) || (rc = check_ptr(q.lora_a, "lora_a")) || (rc = check_ptr(q.lora_b, "lora_b")) ||
+          (rc = check_ptr(q.y, "y")))
+        return fail(rc, "problem %d: %s", i, t_last_error);
+      if (q.t_save && !aligned16(q.t_save)) return fail(QLORA_ERR_INVALID_ARGUMENT, "problem %d: t_save not 16-byte aligned", i);
+    }
     qlora::GroupedProblem& g = gp[static_cast<size_t>(i)];
     g.x = reinterpret_cast<const __nv_bfloat16*>(q.x);
     g.w = to_dev(q.w);
@@ -453,8 +442,44 @@ int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, vo
     g.alpha = q.alpha;
     g.y = reinterpret_cast<__nv_bfloat16*>(q.y);
     g.t_save = q.t_save;
-    need += (static_cast<size_t>(q.m) * q.r * 2 + 255) & ~size_t(255);
   }
+  return QLORA_OK;
+}
+
+// Workspace of the launches: problems go out in chunks of at most
+// fwd_grouped_max_problems(), each chunk with its own plan.
+static size_t grouped_workspace(const std::vector<qlora::GroupedProblem>& gp, int num_sms) {
+  const int count = static_cast<int>(gp.size()), chunk = qlora::fwd_grouped_max_problems();
+  size_t tot = 0;
+  for (int i0 = 0; i0 < count; i0 += chunk)
+    tot += qlora::fwd_grouped_workspace_bytes(gp.data() + i0, count - i0 < chunk ? count - i0 : chunk, num_sms);
+  return tot;
+}
+
+int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problems, int count, size_t* bytes) {
+  if (!bytes) return fail(QLORA_ERR_INVALID_ARGUMENT, "bytes is NULL");
+  if (count < 0 || (count > 0 && !problems)) return fail(QLORA_ERR_INVALID_ARGUMENT, "problems");
+  *bytes = 0;
+  if (count == 0) return QLORA_OK;
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  std::vector<qlora::GroupedProblem> gp;
+  if ((rc = grouped_problems(problems, count, gp, false))) return rc;
+  *bytes = grouped_workspace(gp, di->num_sms);
+  return QLORA_OK;
+}
+
+int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if (count < 0 || (count > 0 && !problems)) return fail(QLORA_ERR_INVALID_ARGUMENT, "problems");
+  if (count == 0) return QLORA_OK;
+  std::vector<qlora::GroupedProblem> gp;
+  if ((rc = grouped_problems(problems, count, gp, true))) return rc;
+  const size_t need = grouped_workspace(gp, di->num_sms);
   if ((rc = check_ptr(workspace, "workspace"))) return rc;
   if (workspace_bytes < need) return fail(QLORA_ERR_INVALID_ARGUMENT, "workspace %zu < %zu bytes", workspace_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -465,7 +490,7 @@ int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, vo
     Span sp(P_FWD_GROUPED, s, 2);
     cudaError_t e = qlora::launch_fwd_grouped(gp.data() + i0, n, ws, di->status, g_wait_ns.load(), di->num_sms, s);
     if (e != cudaSuccess) return cuda_ret(e, "fwd grouped");
-    ws += qlora::fwd_grouped_workspace_bytes(gp.data() + i0, n);
+    ws += qlora::fwd_grouped_workspace_bytes(gp.data() + i0, n, di->num_sms);
   }
   return QLORA_OK;
 }

@@ -102,7 +102,7 @@ struct GroupedProblem {
   float* t_save;                // [m, r] or null
 };
 int fwd_grouped_max_problems();
-size_t fwd_grouped_workspace_bytes(const GroupedProblem* probs, int count);
+size_t fwd_grouped_workspace_bytes(const GroupedProblem* probs, int count, int num_sms);
 cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws, unsigned* status, uint64_t wait_ns,
                                int num_sms, cudaStream_t s);
 

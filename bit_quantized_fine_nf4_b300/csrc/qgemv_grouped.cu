@@ -30,6 +30,7 @@
 #include <cstdio>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -47,6 +48,8 @@ struct GvProb {
   const __nv_bfloat16* lora_b;  // [n, r]
   const __nv_bfloat16* st;      // [m, r]  bf16(s x A^T)
   __nv_bfloat16* y;             // [m, n]
+  float* part;                  // [splits][m][n] float32 partial sums (CUDA-core path with splits > 1)
+  unsigned* cnt;                // [row tiles] arrival counters of the splits (zeroed by the LoRA-down launch)
   int n, k, m, r;
   int item0;  // first work item of this problem
   int pad;
@@ -54,6 +57,8 @@ struct GvProb {
 
 struct GvParams {
   int count, total_items;
+  int splits;  // CUDA-core path: k splits per row tile
+  int group;   // CUDA-core path: consecutive row tiles per work item
   unsigned long long wait_ns;
   unsigned* status;
   GvProb prob[kGvMaxProbs];
@@ -70,6 +75,8 @@ struct GlProb {
 
 struct GlParams {
   int count;
+  int n_cnt;      // split counters to zero before the GEMV launch
+  unsigned* cnt;
   GlProb prob[kGvMaxProbs];
 };
 
@@ -88,6 +95,12 @@ __device__ __forceinline__ void mma_m16n8k16(float (&d)[4], uint32_t a0, uint32_
 template <int NT>
 __global__ void __launch_bounds__(512) k_lora_down_grouped(const __grid_constant__ GlParams p) {
   constexpr int RP = NT * 8;
+  // X may come from the kernel before, and that kernel may be the previous
+  // call's GEMV still reading this workspace: wait for it, then let the GEMV
+  // of this call start (it waits for this kernel before it needs sT)
+  griddep_wait();
+  griddep_launch_dependents();
+  for (int i = blockIdx.x * 512 + threadIdx.x; i < p.n_cnt; i += gridDim.x * 512) p.cnt[i] = 0u;
   extern __shared__ float s_red_flat[];  // [16 warps][16 rows][RP]
   auto s_red = reinterpret_cast<float(*)[16 * RP]>(s_red_flat);
   const GlProb& pr = p.prob[blockIdx.x];
@@ -505,36 +518,296 @@ __global__ void __launch_bounds__(kGvThreads, 2) k_qgemv_grouped(const __grid_co
 static_assert(sizeof(GvParams) <= 32000, "kernel parameter budget");
 static_assert(sizeof(GlParams) <= 32000, "kernel parameter budget");
 
-// ====================================================================== CUDA-core decode (1..4 tokens)
-// With at most 4 tokens the tensor path is bound by the decode (four ALU ops
-// per weight); here the level lookup is one shared-memory load per two weights
-// from a byte-indexed table of (L[hi], L[lo]) bf16 pairs with one column per
-// lane (256 x 32 words: each lane reads its own bank, no conflicts), the block
-// scale a' multiplies a 32-weight partial sum, and every activation load serves
-// two rows.  The levels enter as bf16(L) times the float32 scale (the tensor
-// path rounds bf16(L a')); both are within a bf16 rounding of the exact
-// product.  A step is two 64-blocks; thread (g, c) of a warp owns rows g and
-// g + 8 of the warp's 16 and the 32 contiguous weights c (0..3) of the step
-// (block 2 step + c / 2); the 4 lanes of a row are added with shuffles at the
-// end.  Codes come through a per-thread cp.async ring (16 bytes per row per
-// step) kCcDepth steps ahead; block-scale bytes are read 4 blocks at a time;
-// activations are staged as float32 in windows of kCcWin columns, 4 floats of
-// padding after every 32 so the 4 chunks a warp reads sit in different banks.
+// ====================================================================== CUDA-core decode (1 or 2 tokens)
+// With one or two tokens the tensor path is bound by its decode; here a weight
+// pair costs a byte extract, one shared-memory load and two mixed-precision
+// FMAs per token (fma.rn.f32.bf16: the bf16 x bf16 product is exact in
+// float32, one rounding into the float32 sum).  The table holds, for every
+// code byte, the bf16 pair (L[hi], L[lo]) with one column per lane (each lane
+// reads its own bank); activations are staged as bf16, so the two halves of a
+// staged word meet the two halves of a table word.  The block scale a'
+// multiplies a 32-weight partial sum, so the level enters as bf16(L) times the
+// float32 scale (the tensor path rounds bf16(L a'): both are within a bf16
+// rounding of the exact product).
+//
+// Layout: a row tile is 16 rows, warp w owning rows 2 w and 2 w + 1; a k range
+// is walked in segments of 1024 weights, lane l taking weights 32 l .. 32 l +
+// 31 of each segment (half of a 64-block: one scale per lane and row), so
+// every code load is 512 contiguous bytes of a row.  A work item is (problem,
+// run of `group` consecutive tiles, k split): the item's activations (at most
+// kCcMaxK columns, the splits see to that) are staged once, 16 bytes of
+// padding after every 32 columns so the lanes' chunks fall in different
+// banks, and each warp walks the item's (tile, segment) pairs as one stream
+// with the codes of the next kCcAhead pairs in registers.  The lanes' partial
+// sums of a row meet in a warp reduction at the end of each tile.  When the
+// tiles of a launch fill fewer than all CTA slots, each tile's k range is
+// split: every split writes its float32 partial sums, and the last split to
+// arrive (a per-tile counter) adds them in split order, adds the LoRA term and
+// writes Y -- the result does not depend on the arrival order.
 constexpr int kCcThreads = 256;
-constexpr int kCcDepth = 6;
-constexpr int kCcWin = 2048;
-constexpr int kCcXStride = kCcWin / 32 * 36;  // floats per staged token row
+constexpr int kCcRowsPerWarp = 2;
+constexpr int kCcRows = kCcRowsPerWarp * (kCcThreads / 32);  // rows per tile
+constexpr int kCcCtasPerSm = 2;
+constexpr int kCcSeg = 1024;    // weights per row per segment (32 lanes x 32)
+constexpr int kCcAhead = 2;     // (tile, segment) pairs of codes in flight per warp beyond the current one
+constexpr int kCcMaxK = 12288;  // staged activation columns of one item
+constexpr int kCcXStride = kCcMaxK / 32 * 40;  // bf16 per staged token row (32 columns + 8 padding)
+constexpr int kCcMaxSplits = 8;
 template <int MT>
 constexpr size_t cc_smem() {
-  return 256 * 32 * 4 + static_cast<size_t>(kCcDepth) * kCcThreads * 32 + static_cast<size_t>(MT) * kCcXStride * 4;
+  return 256 * 32 * 4 + static_cast<size_t>(MT) * kCcXStride * 2 + 16;
+}
+
+// acc += bf16(lo of x) * bf16(lo of l) + bf16(hi of x) * bf16(hi of l), each step rounded once in float32
+__device__ __forceinline__ void cc_fma_pair(float& acc_lo, float& acc_hi, uint32_t x, uint32_t l) {
+  asm("{\n\t.reg .b16 xl, xh, ll, lh;\n\t"
+      "mov.b32 {xl, xh}, %2;\n\t"
+      "mov.b32 {ll, lh}, %3;\n\t"
+      "fma.rn.f32.bf16 %0, xl, ll, %0;\n\t"
+      "fma.rn.f32.bf16 %1, xh, lh, %1;\n\t}"
+      : "+f"(acc_lo), "+f"(acc_hi)
+      : "r"(x), "r"(l));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kCcThreads, 2) k_gemv_cc(const __grid_constant__ GvParams p) {
+__global__ void __launch_bounds__(kCcThreads, kCcCtasPerSm) k_gemv_cc(const __grid_constant__ GvParams p) {
+  constexpr int R = kCcRowsPerWarp;
+  constexpr int NS = kCcAhead + 1;  // register slots
   extern __shared__ __align__(16) uint32_t sm_cc[];
-  uint32_t* tab = sm_cc;                                         // [256 bytes][32 lanes]
-  uint8_t* ring = reinterpret_cast<uint8_t*>(sm_cc + 256 * 32);  // [kCcDepth][2 rows][256 threads][16 B]
-  float* xs = reinterpret_cast<float*>(ring + kCcDepth * kCcThreads * 32);  // [MT][kCcXStride]
+  uint32_t* tab = sm_cc;                                                  // [256 bytes][32 lanes]
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(sm_cc + 256 * 32);  // [MT][kCcXStride]
+  int* s_last = reinterpret_cast<int*>(xs + MT * kCcXStride);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int i = tid; i < 256 * 32; i += kCcThreads) {
+    const int b = i >> 5;  // byte: element 2i in the high nibble, 2i + 1 in the low nibble
+    const __nv_bfloat16 lo = __float2bfloat16_rn(nf4_level(b >> 4)), hi = __float2bfloat16_rn(nf4_level(b & 15));
+    tab[i] = static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(&lo)) |
+             (static_cast<uint32_t>(*reinterpret_cast<const unsigned short*>(&hi)) << 16);
+  }
+  const uint32_t tab_me = smem_u32(tab) + lane * 4;
+  const uint32_t xs_me = smem_u32(xs) + lane * 80;  // the lane's 32 columns of a segment
+  const int S = p.splits, G = p.group;
+  griddep_launch_dependents();  // the next launch waits for this grid before it touches anything of it
+  for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
+    int lo_i = 0, hi_i = p.count - 1;  // problem of this item: last one with item0 <= item
+    while (lo_i < hi_i) {
+      const int mid = (lo_i + hi_i + 1) >> 1;
+      if (p.prob[mid].item0 <= item) lo_i = mid; else hi_i = mid - 1;
+    }
+    const GvProb& pr = p.prob[lo_i];
+    const int local = item - pr.item0, run = local / S, split = local - run * S;
+    const int n = pr.n, k = pr.k, m = pr.m, r = pr.r;
+    const int kb_row = k / 64;
+    const int ntiles = (n + kCcRows - 1) / kCcRows;
+    const int tile0 = run * G, tile_end = min(ntiles, tile0 + G);
+    const int nseg = (k + kCcSeg - 1) / kCcSeg;
+    const int per = (nseg + S - 1) / S;
+    const int sg_begin = split * per, sg_end = min(nseg, sg_begin + per);
+    const int nsg = sg_end > sg_begin ? sg_end - sg_begin : 0;
+    const int npairs = (tile_end - tile0) * nsg;
+    const float mu = *pr.mean;
+    const int k_begin = sg_begin * kCcSeg, k_end = min(sg_end * kCcSeg, k);
+    // codes and scale bytes of pair f = (tile tile0 + f / nsg, segment sg_begin + f % nsg), zero past the end
+    // (the block's int8 scale and its group's step travel with the codes)
+    auto load_pair = [&](int f, uint4 (&cw)[R], uint32_t (&qv)[R], float (&sv)[R]) {
+      const bool in = f < npairs;
+      const int tl = in ? tile0 + f / nsg : 0;
+      const int kw = (in ? sg_begin + f % nsg : 0) * kCcSeg + lane * 32;
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        const int rw = tl * kCcRows + warp * R + q;
+        const bool v = in && kw < k && rw < n;
+        const int64_t blk = static_cast<int64_t>(rw) * kb_row + kw / 64;
+        cw[q] = v ? ldg_nc_v4(pr.codes + static_cast<int64_t>(rw) * (k / 2) + kw / 2) : make_uint4(0, 0, 0, 0);
+        qv[q] = v ? static_cast<uint32_t>(static_cast<uint8_t>(__ldg(pr.absq + blk))) : 0u;
+        sv[q] = v ? __ldg(pr.step + (blk >> 8)) : 0.f;
+      }
+    };
+    uint4 cw[NS][R];
+    uint32_t qv[NS][R];
+    float sq[NS][R];
+#pragma unroll
+    for (int d = 0; d < kCcAhead; ++d) load_pair(d, cw[d], qv[d], sq[d]);
+    __syncthreads();  // the table is built; the previous item is done with xs
+    // activations of the item's k range as bf16, 16-byte chunks (rows t >= m are zero)
+    {
+      const int len = k_end - k_begin;
+      for (int i = tid; i < MT * (len / 8); i += kCcThreads) {
+        const int t = i / (len / 8), k8 = (i - t * (len / 8)) * 8;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (t < m) v = __ldcg(reinterpret_cast<const uint4*>(pr.x + static_cast<int64_t>(t) * k + k_begin + k8));
+        *reinterpret_cast<uint4*>(xs + t * kCcXStride + k8 + (k8 >> 5) * 8) = v;
+      }
+    }
+    __syncthreads();
+    float acc[R][MT];
+    float bv[R][2];  // LoRA B entries of the tile's rows: lane j holds B[row][j] and B[row][j + 32]
+    float sv[MT][2];  // sT of the item's problem, lanes over j (read once, after the wait below)
+    bool have_st = false;
+    int f = 0;
+    for (int tl = tile0; tl < tile_end; ++tl) {
+      int row[R];
+      bool ok[R];
+#pragma unroll
+      for (int q = 0; q < R; ++q) {
+        row[q] = tl * kCcRows + warp * R + q;
+        ok[q] = row[q] < n;
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[q][t] = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = lane + 32 * h;
+          bv[q][h] = (ok[q] && j < r) ? __bfloat162float(pr.lora_b[static_cast<int64_t>(row[q]) * r + j]) : 0.f;
+        }
+      }
+      auto pair = [&](auto slot_c, int sg) {
+        constexpr int cur = decltype(slot_c)::value;
+        constexpr int nxt = (cur + kCcAhead) % NS;
+        load_pair(f + kCcAhead, cw[nxt], qv[nxt], sq[nxt]);
+        const int kw = sg * kCcSeg + lane * 32;
+        const bool kin = kw < k;
+        float a[R];  // block scales a' = q * step + mu of the lane's block in each row
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+          a[q] = (kin && ok[q]) ? restore_absmax(static_cast<int8_t>(qv[cur][q]), sq[cur][q], mu) : 0.f;
+        float se[R][MT], so[R][MT];  // even / odd weight partial sums
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+#pragma unroll
+          for (int t = 0; t < MT; ++t) se[q][t] = so[q][t] = 0.f;
+        const uint32_t xk = xs_me + ((sg * kCcSeg - k_begin) / 32) * 80;
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {  // 8 weights = one 32-bit code word per row
+          uint4 xv[MT];
+#pragma unroll
+          for (int t = 0; t < MT; ++t) xv[t] = lds_v4(xk + t * (kCcXStride * 2) + h * 16);
+#pragma unroll
+          for (int q = 0; q < R; ++q) {
+            const uint32_t cwd = h == 0 ? cw[cur][q].x : h == 1 ? cw[cur][q].y : h == 2 ? cw[cur][q].z : cw[cur][q].w;
+#pragma unroll
+            for (int bi = 0; bi < 4; ++bi) {
+              uint32_t e;
+              asm("ld.shared.u32 %0, [%1];" : "=r"(e) : "r"(tab_me + (prmt(cwd, 0u, 0x4440u | bi) << 7)));
+#pragma unroll
+              for (int t = 0; t < MT; ++t) {
+                const uint32_t xw = bi == 0 ? xv[t].x : bi == 1 ? xv[t].y : bi == 2 ? xv[t].z : xv[t].w;
+                cc_fma_pair(se[q][t], so[q][t], xw, e);
+              }
+            }
+          }
+        }
+        if (kin) {  // past the last block the activations read are stale: nothing is added
+#pragma unroll
+          for (int q = 0; q < R; ++q)
+#pragma unroll
+            for (int t = 0; t < MT; ++t) acc[q][t] = fmaf(a[q], se[q][t] + so[q][t], acc[q][t]);
+        }
+      };
+      for (int sg = sg_begin; sg < sg_end; ++sg, ++f) {
+        switch (f % NS) {  // the register slot of pair f (static inside each case)
+          case 0: pair(std::integral_constant<int, 0>{}, sg); break;
+          case 1: pair(std::integral_constant<int, 1>{}, sg); break;
+          default: pair(std::integral_constant<int, 2>{}, sg); break;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < R; ++q)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) acc[q][t] = warp_sum(acc[q][t]);
+      // sT and the zeroed split counters come from the LoRA-down launch before
+      // this one; X did not (that launch waited for X's producer before it let
+      // this grid start), so only this part waits for it
+      griddep_wait();
+      if (S > 1) {
+        // this split's partial sums, then the last split of the tile finishes the rows
+        if (lane == 0) {
+#pragma unroll
+          for (int t = 0; t < MT; ++t) {
+            if (t >= m) break;
+            float* pp = pr.part + (static_cast<int64_t>(split) * m + t) * n;
+#pragma unroll
+            for (int q = 0; q < R; ++q)
+              if (ok[q]) pp[row[q]] = acc[q][t];
+          }
+        }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) *s_last = atomicAdd(pr.cnt + tl, 1u) == static_cast<unsigned>(S - 1);
+        __syncthreads();
+        const bool last = *s_last != 0;
+        __syncthreads();  // every thread has read the flag before it is written for the next tile
+        if (!last) continue;
+        __threadfence();
+        // lane q * MT + t adds the splits of row q, token t in split order
+        float tot = 0.f;
+        const int q_l = lane / MT, t_l = lane % MT;
+        if (lane < R * MT && t_l < m) {
+          int rr = n;
+#pragma unroll
+          for (int q = 0; q < R; ++q)
+            if (q == q_l) rr = row[q];
+          if (rr < n)
+            for (int sp = 0; sp < S; ++sp) tot += __ldcg(pr.part + (static_cast<int64_t>(sp) * m + t_l) * n + rr);
+        }
+#pragma unroll
+        for (int q = 0; q < R; ++q)
+#pragma unroll
+          for (int t = 0; t < MT; ++t) acc[q][t] = __shfl_sync(0xffffffffu, tot, q * MT + t);
+      }
+      // LoRA up-projection: + sum_j sT[t][j] B[row][j], lanes over j
+      if (!have_st) {
+        have_st = true;
+#pragma unroll
+        for (int t = 0; t < MT; ++t)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = lane + 32 * h;
+            sv[t][h] = (t < m && j < r) ? __bfloat162float(__ldcg(pr.st + static_cast<int64_t>(t) * r + j)) : 0.f;
+          }
+      }
+#pragma unroll
+      for (int q = 0; q < R; ++q)
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          const float l = warp_sum(fmaf(sv[t][0], bv[q][0], sv[t][1] * bv[q][1]));
+          if (lane == 0 && t < m && ok[q])
+            pr.y[static_cast<int64_t>(t) * n + row[q]] = __float2bfloat16_rn(acc[q][t] + l);
+        }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------- long lists
+// When a list has at least one 128-row tile per CTA slot, per-item latency
+// matters less than the steady stream, and this layout streams best: a work
+// item is (problem, 128-row tile) over the whole k range; thread (g, c) of
+// warp w owns rows 16 w + g and 16 w + g + 8 and the 32 contiguous weights c
+// (0..3) of every 128-weight step; codes come through a per-thread cp.async
+// ring (16 bytes per row per step) kCwDepth steps ahead, activations are
+// staged as bf16 in windows of kCwWin columns (16 bytes of padding after every
+// 32), the 4 lanes of a row are added with shuffles.  Same table, same
+// mixed-precision FMAs and the same float32 block scale as k_gemv_cc.
+constexpr int kCwRows = 128;
+constexpr int kCwDepth = 8;
+constexpr int kCwWin = 2048;
+constexpr int kCwXStride = kCwWin / 32 * 40;  // bf16 per staged token row
+template <int MT>
+constexpr size_t cw_smem() {
+  return 256 * 32 * 4 + static_cast<size_t>(kCwDepth) * kCcThreads * 32 + static_cast<size_t>(MT) * kCwXStride * 2;
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kCcThreads, kCcCtasPerSm) k_gemv_cc_wide(const __grid_constant__ GvParams p) {
+  extern __shared__ __align__(16) uint32_t sm_cw[];
+  uint32_t* tab = sm_cw;                                                      // [256 bytes][32 lanes]
+  uint8_t* ring = reinterpret_cast<uint8_t*>(sm_cw + 256 * 32);               // [kCwDepth][2 rows][256 threads][16 B]
+  __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(ring + kCwDepth * kCcThreads * 32);  // [MT][kCwXStride]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
   for (int i = tid; i < 256 * 32; i += kCcThreads) {
@@ -545,33 +818,43 @@ __global__ void __launch_bounds__(kCcThreads, 2) k_gemv_cc(const __grid_constant
   }
   const uint32_t ring_me = smem_u32(ring) + tid * 16;
   const uint32_t tab_me = smem_u32(tab) + lane * 4;
+  const uint32_t xs_me = smem_u32(xs) + c * 80;  // the thread's 32 columns of a 128-column step
+  griddep_launch_dependents();  // the next launch waits for this grid before it touches anything of it
   for (int item = blockIdx.x; item < p.total_items; item += gridDim.x) {
     int lo_i = 0, hi_i = p.count - 1;  // problem of this item: last one with item0 <= item
     while (lo_i < hi_i) {
       const int mid = (lo_i + hi_i + 1) >> 1;
       if (p.prob[mid].item0 <= item) lo_i = mid; else hi_i = mid - 1;
     }
-    const uint8_t* codes = p.prob[lo_i].codes;
-    const int8_t* absq = p.prob[lo_i].absq;
-    const float* stepv = p.prob[lo_i].step;
-    const __nv_bfloat16* xg = p.prob[lo_i].x;
-    const int n = p.prob[lo_i].n, k = p.prob[lo_i].k, m = p.prob[lo_i].m;
-    const int row0 = (item - p.prob[lo_i].item0) * 128 + warp * 16 + g, row1 = row0 + 8;
+    const GvProb& pr = p.prob[lo_i];
+    const int n = pr.n, k = pr.k, m = pr.m, r = pr.r;
+    const int row0 = (item - pr.item0) * kCwRows + warp * 16 + g, row1 = row0 + 8;
     const bool ok0 = row0 < n, ok1 = row1 < n;
     const int kb_row = k / 64, nsteps = (kb_row + 1) / 2;
-    const float mu = *p.prob[lo_i].mean;
-    const uint8_t* cp0 = codes + static_cast<int64_t>(ok0 ? row0 : 0) * (k / 2) + c * 16;
-    const uint8_t* cp1 = codes + static_cast<int64_t>(ok1 ? row1 : 0) * (k / 2) + c * 16;
+    const float mu = *pr.mean;
+    const uint8_t* cp0 = pr.codes + static_cast<int64_t>(ok0 ? row0 : 0) * (k / 2) + c * 16;
+    const uint8_t* cp1 = pr.codes + static_cast<int64_t>(ok1 ? row1 : 0) * (k / 2) + c * 16;
     const int64_t ab0 = static_cast<int64_t>(ok0 ? row0 : 0) * kb_row, ab1 = static_cast<int64_t>(ok1 ? row1 : 0) * kb_row;
     auto issue = [&](int st) {  // step st's 32 weights of both rows into the ring
       const int kb = 2 * st + (c >> 1);
-      if (kb < kb_row) {
-        const uint32_t slot = ring_me + (st % kCcDepth) * (kCcThreads * 32);
+      if (st < nsteps && kb < kb_row) {
+        const uint32_t slot = ring_me + (st % kCwDepth) * (kCcThreads * 32);
         if (ok0) cp_async16(slot, cp0 + st * 64);
         if (ok1) cp_async16(slot + kCcThreads * 16, cp1 + st * 64);
       }
       cp_async_commit();
     };
+#pragma unroll 1
+    for (int d = 0; d < kCwDepth - 1; ++d) issue(d);
+    // the LoRA B entries of the two rows this thread adds at the end (r / 4 of each row, r <= 64)
+    const int jq = r / 4;  // r % 8 == 0: even, so 4-byte loads are aligned
+    uint32_t bw0[8], bw1[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const bool in = 2 * u < jq;
+      bw0[u] = (ok0 && in) ? *reinterpret_cast<const uint32_t*>(pr.lora_b + static_cast<int64_t>(row0) * r + c * jq + 2 * u) : 0u;
+      bw1[u] = (ok1 && in) ? *reinterpret_cast<const uint32_t*>(pr.lora_b + static_cast<int64_t>(row1) * r + c * jq + 2 * u) : 0u;
+    }
     float acc0[MT], acc1[MT];
 #pragma unroll
     for (int t = 0; t < MT; ++t) acc0[t] = acc1[t] = 0.f;
@@ -580,94 +863,75 @@ __global__ void __launch_bounds__(kCcThreads, 2) k_gemv_cc(const __grid_constant
     int g0 = -1, g1 = -1;         // double-quant groups of the cached steps
     float st0 = 0.f, st1 = 0.f;
     __syncthreads();  // the table is built; the previous item is done with xs
-#pragma unroll 1
-    for (int d = 0; d < kCcDepth - 1; ++d) issue(d);
-    for (int w0 = 0; w0 < k; w0 += kCcWin) {
-      const int wlen = min(kCcWin, k - w0);
-      // activations of this window as float32 (rows t >= m are zero)
+    for (int w0 = 0; w0 < k; w0 += kCwWin) {
+      const int wlen = min(kCwWin, k - w0);
       for (int i = tid; i < MT * (wlen / 8); i += kCcThreads) {
         const int t = i / (wlen / 8), k8 = (i - t * (wlen / 8)) * 8;
-        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (t < m) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xg + static_cast<int64_t>(t) * k + w0 + k8);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            f[2 * e] = __uint_as_float(w[e] << 16);
-            f[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-          }
-        }
-        float4* dst = reinterpret_cast<float4*>(xs + t * kCcXStride + k8 + (k8 >> 5) * 4);
-        dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-        dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (t < m) v = __ldcg(reinterpret_cast<const uint4*>(pr.x + static_cast<int64_t>(t) * k + w0 + k8));
+        *reinterpret_cast<uint4*>(xs + t * kCwXStride + k8 + (k8 >> 5) * 8) = v;
       }
       __syncthreads();
       const int s0 = w0 / 128, s1 = (w0 + wlen + 127) / 128;
       for (int st = s0; st < s1; ++st) {
-        issue(st + kCcDepth - 1);
+        issue(st + kCwDepth - 1);
         const int kb = 2 * st + (c >> 1);
         const bool kin = kb < kb_row;
         if (kin && (kb >> 2) != qb) {  // 4 scale bytes at a time (kb_row % 4 == 0 keeps them aligned)
           qb = kb >> 2;
           const int kb4 = kb & ~3;
           if ((kb_row & 3) == 0) {
-            if (ok0) q4_0 = *reinterpret_cast<const uint32_t*>(absq + ab0 + kb4);
-            if (ok1) q4_1 = *reinterpret_cast<const uint32_t*>(absq + ab1 + kb4);
+            if (ok0) q4_0 = *reinterpret_cast<const uint32_t*>(pr.absq + ab0 + kb4);
+            if (ok1) q4_1 = *reinterpret_cast<const uint32_t*>(pr.absq + ab1 + kb4);
           } else {
             q4_0 = q4_1 = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               if (kb4 + e < kb_row) {
-                if (ok0) q4_0 |= static_cast<uint32_t>(static_cast<uint8_t>(absq[ab0 + kb4 + e])) << (8 * e);
-                if (ok1) q4_1 |= static_cast<uint32_t>(static_cast<uint8_t>(absq[ab1 + kb4 + e])) << (8 * e);
+                if (ok0) q4_0 |= static_cast<uint32_t>(static_cast<uint8_t>(pr.absq[ab0 + kb4 + e])) << (8 * e);
+                if (ok1) q4_1 |= static_cast<uint32_t>(static_cast<uint8_t>(pr.absq[ab1 + kb4 + e])) << (8 * e);
               }
             }
           }
         }
         const int gr0 = static_cast<int>((ab0 + kb) >> 8), gr1 = static_cast<int>((ab1 + kb) >> 8);
-        if (kin && gr0 != g0) { g0 = gr0; st0 = ok0 ? stepv[gr0] : 0.f; }
-        if (kin && gr1 != g1) { g1 = gr1; st1 = ok1 ? stepv[gr1] : 0.f; }
+        if (kin && gr0 != g0) { g0 = gr0; st0 = ok0 ? pr.step[gr0] : 0.f; }
+        if (kin && gr1 != g1) { g1 = gr1; st1 = ok1 ? pr.step[gr1] : 0.f; }
         const int sh = 8 * (kb & 3);
         const float a0 = (ok0 && kin) ? restore_absmax(static_cast<int8_t>((q4_0 >> sh) & 0xffu), st0, mu) : 0.f;
         const float a1 = (ok1 && kin) ? restore_absmax(static_cast<int8_t>((q4_1 >> sh) & 0xffu), st1, mu) : 0.f;
-        cp_async_wait<kCcDepth - 1>();
-        const uint32_t slot = ring_me + (st % kCcDepth) * (kCcThreads * 32);
+        cp_async_wait<kCwDepth - 1>();
+        const uint32_t slot = ring_me + (st % kCwDepth) * (kCcThreads * 32);
         const uint4 cw0 = lds_v4(slot), cw1 = lds_v4(slot + kCcThreads * 16);
         const uint32_t wr0[4] = {cw0.x, cw0.y, cw0.z, cw0.w}, wr1[4] = {cw1.x, cw1.y, cw1.z, cw1.w};
-        float sa0[MT], sa1[MT];
+        float s0e[MT], s0o[MT], s1e[MT], s1o[MT];  // even / odd weight partial sums of the two rows
 #pragma unroll
-        for (int t = 0; t < MT; ++t) sa0[t] = sa1[t] = 0.f;
-        const float* xk = xs + ((st * 128 - w0) / 32 + c) * 36;  // the thread's 32 columns, padded layout
+        for (int t = 0; t < MT; ++t) s0e[t] = s0o[t] = s1e[t] = s1o[t] = 0.f;
+        const uint32_t xk = xs_me + ((st * 128 - w0) / 128) * 320;  // 4 chunks of 80 bytes per step
 #pragma unroll
         for (int h = 0; h < 4; ++h) {  // 8 weights = one 32-bit code word per row
-          float xv[MT][8];
+          uint4 xv[MT];
 #pragma unroll
-          for (int t = 0; t < MT; ++t) {
-            const float4 u = *reinterpret_cast<const float4*>(xk + t * kCcXStride + h * 8);
-            const float4 v = *reinterpret_cast<const float4*>(xk + t * kCcXStride + h * 8 + 4);
-            xv[t][0] = u.x; xv[t][1] = u.y; xv[t][2] = u.z; xv[t][3] = u.w;
-            xv[t][4] = v.x; xv[t][5] = v.y; xv[t][6] = v.z; xv[t][7] = v.w;
-          }
+          for (int t = 0; t < MT; ++t) xv[t] = lds_v4(xk + t * (kCwXStride * 2) + h * 16);
           const uint32_t c0w = (ok0 && kin) ? wr0[h] : 0u, c1w = (ok1 && kin) ? wr1[h] : 0u;
 #pragma unroll
           for (int bi = 0; bi < 4; ++bi) {
             uint32_t e0, e1;
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(e0) : "r"(tab_me + ((c0w >> (8 * bi)) & 0xffu) * 128));
-            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(e1) : "r"(tab_me + ((c1w >> (8 * bi)) & 0xffu) * 128));
-            const float l00 = __uint_as_float(e0 << 16), l01 = __uint_as_float(e0 & 0xffff0000u);
-            const float l10 = __uint_as_float(e1 << 16), l11 = __uint_as_float(e1 & 0xffff0000u);
+            asm("ld.shared.u32 %0, [%1];" : "=r"(e0) : "r"(tab_me + (prmt(c0w, 0u, 0x4440u | bi) << 7)));
+            asm("ld.shared.u32 %0, [%1];" : "=r"(e1) : "r"(tab_me + (prmt(c1w, 0u, 0x4440u | bi) << 7)));
 #pragma unroll
             for (int t = 0; t < MT; ++t) {
-              sa0[t] = fmaf(xv[t][2 * bi], l00, fmaf(xv[t][2 * bi + 1], l01, sa0[t]));
-              sa1[t] = fmaf(xv[t][2 * bi], l10, fmaf(xv[t][2 * bi + 1], l11, sa1[t]));
+              const uint32_t xw = bi == 0 ? xv[t].x : bi == 1 ? xv[t].y : bi == 2 ? xv[t].z : xv[t].w;
+              cc_fma_pair(s0e[t], s0o[t], xw, e0);
+              cc_fma_pair(s1e[t], s1o[t], xw, e1);
             }
           }
         }
         if (kin) {  // past the last block the activations read are stale: nothing is added
 #pragma unroll
           for (int t = 0; t < MT; ++t) {
-            acc0[t] = fmaf(a0, sa0[t], acc0[t]);
-            acc1[t] = fmaf(a1, sa1[t], acc1[t]);
+            acc0[t] = fmaf(a0, s0e[t] + s0o[t], acc0[t]);
+            acc1[t] = fmaf(a1, s1e[t] + s1o[t], acc1[t]);
           }
         }
       }
@@ -681,21 +945,23 @@ __global__ void __launch_bounds__(kCcThreads, 2) k_gemv_cc(const __grid_constant
       acc1[t] += __shfl_xor_sync(0xffffffffu, acc1[t], 1);
       acc1[t] += __shfl_xor_sync(0xffffffffu, acc1[t], 2);
     }
+    griddep_wait();  // sT comes from the LoRA-down launch before this one
     // LoRA up-projection: + sum_j st[t][j] B[row][j]; the 4 lanes of a row split j
-    const __nv_bfloat16* lb = p.prob[lo_i].lora_b;
-    const __nv_bfloat16* stv = p.prob[lo_i].st;
-    const int r = p.prob[lo_i].r, jq = r / 4;  // r % 8 == 0
     float l0[MT], l1[MT];
 #pragma unroll
     for (int t = 0; t < MT; ++t) l0[t] = l1[t] = 0.f;
-    for (int j = c * jq; j < (c + 1) * jq; ++j) {
-      const float b0 = ok0 ? __bfloat162float(lb[static_cast<int64_t>(row0) * r + j]) : 0.f;
-      const float b1 = ok1 ? __bfloat162float(lb[static_cast<int64_t>(row1) * r + j]) : 0.f;
 #pragma unroll
-      for (int t = 0; t < MT; ++t) {
-        const float sv = t < m ? __bfloat162float(stv[static_cast<int64_t>(t) * r + j]) : 0.f;
-        l0[t] = fmaf(sv, b0, l0[t]);
-        l1[t] = fmaf(sv, b1, l1[t]);
+    for (int jj = 0; jj < 16; ++jj) {
+      if (jj < jq) {
+        const int j = c * jq + jj;
+        const float b0 = __uint_as_float((jj & 1) ? (bw0[jj >> 1] & 0xffff0000u) : (bw0[jj >> 1] << 16));
+        const float b1 = __uint_as_float((jj & 1) ? (bw1[jj >> 1] & 0xffff0000u) : (bw1[jj >> 1] << 16));
+#pragma unroll
+        for (int t = 0; t < MT; ++t) {
+          const float sv = t < m ? __bfloat162float(__ldcg(pr.st + static_cast<int64_t>(t) * r + j)) : 0.f;
+          l0[t] = fmaf(sv, b0, l0[t]);
+          l1[t] = fmaf(sv, b1, l1[t]);
+        }
       }
     }
 #pragma unroll
@@ -706,18 +972,106 @@ __global__ void __launch_bounds__(kCcThreads, 2) k_gemv_cc(const __grid_constant
       l1[t] += __shfl_xor_sync(0xffffffffu, l1[t], 2);
     }
     if (c == 0) {
-      __nv_bfloat16* y = p.prob[lo_i].y;
 #pragma unroll
       for (int t = 0; t < MT; ++t) {
         if (t >= m) break;
-        if (ok0) y[static_cast<int64_t>(t) * n + row0] = __float2bfloat16_rn(acc0[t] + l0[t]);
-        if (ok1) y[static_cast<int64_t>(t) * n + row1] = __float2bfloat16_rn(acc1[t] + l1[t]);
+        if (ok0) pr.y[static_cast<int64_t>(t) * n + row0] = __float2bfloat16_rn(acc0[t] + l0[t]);
+        if (ok1) pr.y[static_cast<int64_t>(t) * n + row1] = __float2bfloat16_rn(acc1[t] + l1[t]);
       }
     }
   }
 }
 
 int fwd_grouped_max_problems() { return kGvMaxProbs; }
+
+// Work plan of one launch: which GEMV, the k splits of the CUDA-core path,
+// and the workspace regions (bf16 sT per problem, float32 partials, tile
+// counters), each 256-byte aligned.
+struct GroupedPlan {
+  bool cuda_core;
+  bool wide;  // CUDA-core path, long list: k_gemv_cc_wide
+  int mmax, rmax, splits, group, items;
+  size_t st_bytes, part_bytes, cnt_bytes;
+};
+
+static size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Launch with programmatic stream serialisation: the kernel may start while the
+// one before it in the stream finishes; it waits (griddepcontrol.wait) before
+// it reads anything that kernel writes.
+template <typename P>
+static cudaError_t launch_dependent(void (*kernel)(P), int grid, int block, size_t smem, cudaStream_t s, const P& prm) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, prm);
+}
+
+static GroupedPlan plan_grouped(const GroupedProblem* probs, int count, int num_sms) {
+  GroupedPlan pl = {};
+  pl.mmax = 1;
+  pl.rmax = 8;
+  int tiles = 0, nsteps_min = 1 << 30;
+  for (int i = 0; i < count; ++i) {
+    if (probs[i].m > pl.mmax) pl.mmax = probs[i].m;
+    if (probs[i].r > pl.rmax) pl.rmax = probs[i].r;
+    tiles += static_cast<int>((probs[i].w.n + kCcRows - 1) / kCcRows);
+    const int nseg = static_cast<int>((probs[i].w.k + kCcSeg - 1) / kCcSeg);
+    if (nseg < nsteps_min) nsteps_min = nseg;
+    pl.st_bytes += align256(static_cast<size_t>(probs[i].m) * probs[i].r * 2);
+  }
+  pl.cuda_core = pl.mmax <= 2;
+  pl.splits = 1;
+  pl.group = 1;
+  int tiles_wide = 0;
+  for (int i = 0; i < count; ++i) tiles_wide += static_cast<int>((probs[i].w.n + kCwRows - 1) / kCwRows);
+  pl.wide = pl.cuda_core && tiles_wide >= kCcCtasPerSm * num_sms;
+  if (pl.wide) {
+    pl.items = tiles_wide;
+  } else if (pl.cuda_core) {
+    // every split's k range fits the staged activations; more splits when the
+    // tiles leave CTA slots idle (at least 2 segments per split)
+    const int slots = kCcCtasPerSm * num_sms;
+    int kmax = 64;
+    for (int i = 0; i < count; ++i)
+      if (probs[i].w.k > kmax) kmax = static_cast<int>(probs[i].w.k);
+    const int s_min = (kmax + kCcMaxK - 1) / kCcMaxK;
+    int s = 1;
+    if (tiles > 0 && tiles < slots) s = slots / tiles;
+    if (s > kCcMaxSplits) s = kCcMaxSplits;
+    if (s > nsteps_min / 2) s = nsteps_min / 2;
+    pl.splits = s > s_min ? s : s_min;
+    // runs of consecutive tiles per item: about 4 items per CTA slot
+    const long long work = static_cast<long long>(tiles) * pl.splits;
+    if (work > 4LL * slots) pl.group = static_cast<int>(work / (4LL * slots));
+    pl.items = 0;
+    for (int i = 0; i < count; ++i) {
+      const int t = static_cast<int>((probs[i].w.n + kCcRows - 1) / kCcRows);
+      pl.items += (t + pl.group - 1) / pl.group * pl.splits;
+    }
+    if (pl.splits > 1) {
+      for (int i = 0; i < count; ++i)
+        pl.part_bytes += align256(static_cast<size_t>(pl.splits) * probs[i].m * probs[i].w.n * 4);
+      pl.cnt_bytes = align256(static_cast<size_t>(tiles) * 4);
+    }
+  } else {
+    pl.items = 0;
+    for (int i = 0; i < count; ++i) pl.items += static_cast<int>((probs[i].w.n + 127) / 128);
+  }
+  return pl;
+}
+
+size_t fwd_grouped_workspace_bytes(const GroupedProblem* probs, int count, int num_sms) {
+  const GroupedPlan pl = plan_grouped(probs, count, num_sms);
+  return pl.st_bytes + pl.part_bytes + pl.cnt_bytes;
+}
 
 cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws, unsigned* status, uint64_t wait_ns,
                                int num_sms, cudaStream_t s) {
@@ -727,13 +1081,14 @@ cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws,
   std::lock_guard<std::mutex> lk(mu);
   memset(&gv, 0, sizeof(gv));
   memset(&gl, 0, sizeof(gl));
+  const GroupedPlan pl = plan_grouped(probs, count, num_sms);
   char* base = static_cast<char*>(ws);
-  size_t off = 0;
-  int items = 0, rmax = 8, mmax = 1;
+  size_t off = 0, off_part = pl.st_bytes, off_cnt = pl.st_bytes + pl.part_bytes;
+  int items = 0, tiles = 0;
   for (int i = 0; i < count; ++i) {
     const GroupedProblem& q = probs[i];
     __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(base + off);
-    off += (static_cast<size_t>(q.m) * q.r * 2 + 255) & ~size_t(255);
+    off += align256(static_cast<size_t>(q.m) * q.r * 2);
     GvProb& g = gv.prob[i];
     g.codes = q.w.codes;
     g.absq = q.w.absq;
@@ -748,7 +1103,20 @@ cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws,
     g.m = q.m;
     g.r = q.r;
     g.item0 = items;
-    items += (g.n + 127) / 128;
+    if (pl.wide) {
+      items += (g.n + kCwRows - 1) / kCwRows;
+    } else if (pl.cuda_core) {
+      const int t = (g.n + kCcRows - 1) / kCcRows;
+      items += (t + pl.group - 1) / pl.group * pl.splits;
+      if (pl.splits > 1) {
+        g.part = reinterpret_cast<float*>(base + off_part);
+        off_part += align256(static_cast<size_t>(pl.splits) * q.m * g.n * 4);
+        g.cnt = reinterpret_cast<unsigned*>(base + off_cnt) + tiles;
+      }
+      tiles += t;
+    } else {
+      items += (g.n + 127) / 128;
+    }
     GlProb& l = gl.prob[i];
     l.x = q.x;
     l.a = q.lora_a;
@@ -758,54 +1126,58 @@ cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws,
     l.k = g.k;
     l.r = q.r;
     l.scale = q.alpha / static_cast<float>(q.r);
-    if (q.r > rmax) rmax = q.r;
-    if (q.m > mmax) mmax = q.m;
   }
   gv.count = count;
   gv.total_items = items;
+  gv.splits = pl.splits;
+  gv.group = pl.group;
   gv.wait_ns = wait_ns;
   gv.status = status;
   gl.count = count;
+  if (pl.cuda_core && pl.splits > 1) {  // the LoRA-down launch zeroes the split counters
+    gl.n_cnt = tiles;
+    gl.cnt = reinterpret_cast<unsigned*>(base + off_cnt);
+  }
   cudaError_t e;
-  if (rmax <= 16) {
+  if (pl.rmax <= 16) {
     e = set_smem_limit_once(k_lora_down_grouped<2>, 16 * 16 * 16 * 4);
-    if (e == cudaSuccess) k_lora_down_grouped<2><<<count, 512, 16 * 16 * 16 * 4, s>>>(gl);
-  } else if (rmax <= 32) {
+    if (e == cudaSuccess) e = launch_dependent(k_lora_down_grouped<2>, count, 512, 16 * 16 * 16 * 4, s, gl);
+  } else if (pl.rmax <= 32) {
     e = set_smem_limit_once(k_lora_down_grouped<4>, 16 * 16 * 32 * 4);
-    if (e == cudaSuccess) k_lora_down_grouped<4><<<count, 512, 16 * 16 * 32 * 4, s>>>(gl);
+    if (e == cudaSuccess) e = launch_dependent(k_lora_down_grouped<4>, count, 512, 16 * 16 * 32 * 4, s, gl);
   } else {
     e = set_smem_limit_once(k_lora_down_grouped<8>, 16 * 16 * 64 * 4);
-    if (e == cudaSuccess) k_lora_down_grouped<8><<<count, 512, 16 * 16 * 64 * 4, s>>>(gl);
+    if (e == cudaSuccess) e = launch_dependent(k_lora_down_grouped<8>, count, 512, 16 * 16 * 64 * 4, s, gl);
   }
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  int grid = 2 * num_sms;
-  if (grid > items) grid = items;
-  if (mmax <= 2) {
+  if (pl.cuda_core) {
     // CUDA-core decode for 1 or 2 token columns (with more, the FMAs per weight
     // catch up with the tensor path's decode cost)
-#define QLORA_CC(MT)                                                              \
-  do {                                                                            \
-    e = set_smem_limit_once(k_gemv_cc<MT>, cc_smem<MT>());                        \
-    if (e == cudaSuccess) k_gemv_cc<MT><<<grid, kCcThreads, cc_smem<MT>(), s>>>(gv); \
+    const int grid = items < kCcCtasPerSm * num_sms ? items : kCcCtasPerSm * num_sms;
+#define QLORA_CC(MT)                                                                                       \
+  do {                                                                                                     \
+    if (pl.wide) {                                                                                         \
+      e = set_smem_limit_once(k_gemv_cc_wide<MT>, cw_smem<MT>());                                          \
+      if (e == cudaSuccess) e = launch_dependent(k_gemv_cc_wide<MT>, grid, kCcThreads, cw_smem<MT>(), s, gv); \
+    } else {                                                                                               \
+      e = set_smem_limit_once(k_gemv_cc<MT>, cc_smem<MT>());                                               \
+      if (e == cudaSuccess) e = launch_dependent(k_gemv_cc<MT>, grid, kCcThreads, cc_smem<MT>(), s, gv);   \
+    }                                                                                                      \
   } while (0)
-    if (mmax == 1) QLORA_CC(1);
+    if (pl.mmax == 1) QLORA_CC(1);
     else QLORA_CC(2);
 #undef QLORA_CC
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
   }
+  int grid = 2 * num_sms;
+  if (grid > items) grid = items;
   e = set_smem_limit_once(k_qgemv_grouped, kGvSmem);
   if (e != cudaSuccess) return e;
   k_qgemv_grouped<<<grid, kGvThreads, kGvSmem, s>>>(gv);
   return cudaGetLastError();
-}
-
-size_t fwd_grouped_workspace_bytes(const GroupedProblem* probs, int count) {
-  size_t off = 0;
-  for (int i = 0; i < count; ++i) off += (static_cast<size_t>(probs[i].m) * probs[i].r * 2 + 255) & ~size_t(255);
-  return off;
 }
 
 }  // namespace qlora

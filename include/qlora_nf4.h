@@ -185,7 +185,11 @@ typedef struct qlora_linear_problem {
   float* t_save;               /* f32 [m, r] = X A^T, or NULL */
 } qlora_linear_problem;
 
-/* Bytes of workspace qlora_linear_fwd_grouped needs for this list. */
+/*
+ * Bytes of workspace qlora_linear_fwd_grouped needs for this list on the
+ * current device (the split of the weight stream over the SMs depends on the
+ * device's SM count).
+ */
 int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problems, int count, size_t* bytes);
 
 /*
@@ -193,8 +197,12 @@ int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problem
  * each matrix of a layer stack applied to 1..16 tokens), in two kernel
  * launches per 300 problems: all X A^T products, then one pass that streams
  * every weight of the list.  Same arithmetic as qlora_linear_fwd (bf16
- * operands, fp32 accumulation, s X A^T rounded to bf16); every y is written
- * once, deterministically.  `problems` is a host array of `count` entries.
+ * operands, fp32 accumulation, s X A^T rounded to bf16), except that with at
+ * most 2 tokens the levels multiply in float32 (L times the float32 block
+ * scale, where the tensor-core path rounds bf16(L a')).  Short lists split the
+ * k range of each 256-row tile over several SMs; the splits' float32 partial
+ * sums are added in a fixed order, so every y is deterministic.  `problems` is
+ * a host array of `count` entries.
  */
 int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, void* workspace, size_t workspace_bytes,
                              void* stream);

@@ -81,3 +81,54 @@ def test_grouped_small_token_path(lib, mmax):
         wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
         yr, _ = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
         assert rel_fro(to_np64(ys[i]), yr) < GEMM_TOL, shapes[i]
+
+
+SPLIT_LISTS = [  # short lists at 1-2 tokens: each 256-row tile's k range is split over several SMs
+    [(4096, 4096, 1, 16)],                        # 16 tiles -> 8 splits
+    [(4096, 11008, 1, 16)],                       # the down projection: 8 splits of 86 steps
+    [(296, 1088, 2, 8), (264, 2112, 1, 16)],      # ragged rows, 17 blocks a row (odd), 2 splits
+    [(1032, 4160, 2, 24)],                        # 33 steps over 8 splits: the last split is empty
+]
+
+
+@pytest.mark.parametrize("which", range(len(SPLIT_LISTS)))
+def test_grouped_split_k_matches_oracle_and_is_deterministic(lib, which):
+    shapes = SPLIT_LISTS[which]
+    cases = [synthetic.linear_case(n, k, m, r, 2.0 * r, device="cuda", base_seed=900 + 10 * i + which)
+             for i, (n, k, m, r) in enumerate(shapes)]
+    recs = [lib.quantize(c.w) for c in cases]
+    probs = [(c.x, rec, c.a, c.b, c.alpha, None, None) for c, rec in zip(cases, recs)]
+    g = lib.GroupedForward(probs)
+    ys = [y.clone() for y in g.run()]
+    ys2 = g.run()
+    lib.check_status()
+    for i, (c, rec) in enumerate(zip(cases, recs)):
+        assert torch.equal(ys[i], ys2[i]), shapes[i]
+        n, k = c.w.shape
+        ref = nf4.quantize(to_np32(c.w.cpu()), n, k)
+        wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
+        yr, _ = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
+        assert rel_fro(to_np64(ys[i]), yr) < GEMM_TOL, shapes[i]
+
+
+def test_grouped_long_list_one_and_two_tokens(lib):
+    """A list long enough to give every CTA slot a 128-row tile of its own (48
+    problems, 312 tiles for a 148-SM B300): the layout streamed for long lists,
+    ragged rows, 1 and 2 tokens, against the oracle; a second call gives the same bits."""
+    base = [(768, 256, 1, 8), (776, 320, 2, 16), (1024, 1088, 1, 16), (520, 512, 2, 24)]
+    shapes = [base[i % 4] for i in range(48)]
+    cases = [synthetic.linear_case(n, k, m, r, 2.0 * r, device="cuda", base_seed=1300 + 7 * i)
+             for i, (n, k, m, r) in enumerate(shapes)]
+    recs = [lib.quantize(c.w) for c in cases]
+    probs = [(c.x, rec, c.a, c.b, c.alpha, None, None) for c, rec in zip(cases, recs)]
+    g = lib.GroupedForward(probs)
+    ys = [y.clone() for y in g.run()]
+    ys2 = g.run()
+    lib.check_status()
+    for i, (c, rec) in enumerate(zip(cases, recs)):
+        assert torch.equal(ys[i], ys2[i]), shapes[i]
+        n, k = c.w.shape
+        ref = nf4.quantize(to_np32(c.w.cpu()), n, k)
+        wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
+        yr, _ = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
+        assert rel_fro(to_np64(ys[i]), yr) < GEMM_TOL, shapes[i]
