@@ -21,6 +21,11 @@ launching stream, max over ranks.  Also on the line:
 ``--impl reference`` times the CPU oracle (the reference for this build) on a
 bounded sample of the same workload and prints the same line with
 ``"impl": "reference"``.
+
+``--only quant [--shape NxK]`` / ``--only decode [--decode-layers L]`` run just
+that secondary measurement (quantise + dequantise of one bf16 weight; the 1-token
+decode sweep) and print its figures -- a small, repeatable workload for
+profilers, not a bench line.
 """
 
 from __future__ import annotations
@@ -657,7 +662,20 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--decode-layers", type=int, default=32)
+    ap.add_argument("--only", choices=("quant", "decode"), default=None,
+                    help="run one secondary measurement alone (a workload for profilers)")
+    ap.add_argument("--shape", default="22016x8192", help="weight shape for --only quant")
     args = ap.parse_args(argv)
+    if args.only:
+        import torch
+        import bit_quantized_fine_nf4_b300 as q
+        q.load()
+        if args.only == "quant":
+            n, k = (int(v) for v in args.shape.lower().split("x"))
+            print(json.dumps(dequant_quant_rates(q, torch, None, n=n, k=k)), flush=True)
+        else:
+            print(json.dumps(decode_sweep(q, torch, layers=args.decode_layers, tokens=(1,))), flush=True)
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -97,7 +97,8 @@ def test_grouped_split_k_matches_oracle_and_is_deterministic(lib, which):
     cases = [synthetic.linear_case(n, k, m, r, 2.0 * r, device="cuda", base_seed=900 + 10 * i + which)
              for i, (n, k, m, r) in enumerate(shapes)]
     recs = [lib.quantize(c.w) for c in cases]
-    probs = [(c.x, rec, c.a, c.b, c.alpha, None, None) for c, rec in zip(cases, recs)]
+    ts = [torch.full((c.m, c.r), float("nan"), dtype=torch.float32, device="cuda") for c in cases]
+    probs = [(c.x, rec, c.a, c.b, c.alpha, None, t) for c, rec, t in zip(cases, recs, ts)]
     g = lib.GroupedForward(probs)
     ys = [y.clone() for y in g.run()]
     ys2 = g.run()
@@ -107,8 +108,9 @@ def test_grouped_split_k_matches_oracle_and_is_deterministic(lib, which):
         n, k = c.w.shape
         ref = nf4.quantize(to_np32(c.w.cpu()), n, k)
         wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
-        yr, _ = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
+        yr, tr = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
         assert rel_fro(to_np64(ys[i]), yr) < GEMM_TOL, shapes[i]
+        assert rel_fro(to_np64(ts[i]), tr) < 1e-5, shapes[i]
 
 
 def test_grouped_long_list_one_and_two_tokens(lib):
