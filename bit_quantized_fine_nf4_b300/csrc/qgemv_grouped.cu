@@ -535,7 +535,7 @@ static_assert(sizeof(GlParams) <= 32000, "kernel parameter budget");
 // 31 of each segment (half of a 64-block: one scale per lane and row), so
 // every code load is 512 contiguous bytes of a row.  A work item is (problem,
 // run of `group` consecutive tiles, k split): the item's activations (at most
-// kCcMaxK columns, the splits see to that) are staged once, 16 bytes of
+// cc_max_k columns, the splits see to that) are staged once, 16 bytes of
 // padding after every 32 columns so the lanes' chunks fall in different
 // banks, and each warp walks the item's (tile, segment) pairs as one stream
 // with the codes of the next kCcAhead pairs in registers.  The lanes' partial
@@ -550,12 +550,13 @@ constexpr int kCcRows = kCcRowsPerWarp * (kCcThreads / 32);  // rows per tile
 constexpr int kCcCtasPerSm = 2;
 constexpr int kCcSeg = 1024;    // weights per row per segment (32 lanes x 32)
 constexpr int kCcAhead = 2;     // (tile, segment) pairs of codes in flight per warp beyond the current one
-constexpr int kCcMaxK = 12288;  // staged activation columns of one item
-constexpr int kCcXStride = kCcMaxK / 32 * 40;  // bf16 per staged token row (32 columns + 8 padding)
+// staged activation columns of one item (two CTAs per SM at every token count)
+__host__ __device__ constexpr int cc_max_k(int mt) { return mt <= 2 ? 12288 : 6144; }
+__host__ __device__ constexpr int cc_xstride(int mt) { return cc_max_k(mt) / 32 * 40; }  // bf16 per staged token row (32 columns + 8 padding)
 constexpr int kCcMaxSplits = 8;
 template <int MT>
 constexpr size_t cc_smem() {
-  return 256 * 32 * 4 + static_cast<size_t>(MT) * kCcXStride * 2 + 16;
+  return 256 * 32 * 4 + static_cast<size_t>(MT) * cc_xstride(MT) * 2 + 16;
 }
 
 // acc += bf16(lo of x) * bf16(lo of l) + bf16(hi of x) * bf16(hi of l), each step rounded once in float32
@@ -579,6 +580,7 @@ template <int MT>
 __global__ void __launch_bounds__(kCcThreads, kCcCtasPerSm) k_gemv_cc(const __grid_constant__ GvParams p) {
   constexpr int R = kCcRowsPerWarp;
   constexpr int NS = kCcAhead + 1;  // register slots
+  constexpr int kCcXStride = cc_xstride(MT);
   extern __shared__ __align__(16) uint32_t sm_cc[];
   uint32_t* tab = sm_cc;                                                  // [256 bytes][32 lanes]
   __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(sm_cc + 256 * 32);  // [MT][kCcXStride]
@@ -1033,6 +1035,9 @@ static GroupedPlan plan_grouped(const GroupedProblem* probs, int count, int num_
   int tiles_wide = 0;
   for (int i = 0; i < count; ++i) tiles_wide += static_cast<int>((probs[i].w.n + kCwRows - 1) / kCwRows);
   pl.wide = pl.cuda_core && tiles_wide >= kCcCtasPerSm * num_sms;
+  // short lists of 3 or 4 tokens take the split CUDA-core layout as well (the
+  // tensor path's 128-row tiles would leave most SMs idle)
+  if (!pl.cuda_core && pl.mmax <= 4 && tiles_wide < kCcCtasPerSm * num_sms) pl.cuda_core = true;
   if (pl.wide) {
     pl.items = tiles_wide;
   } else if (pl.cuda_core) {
@@ -1042,7 +1047,7 @@ static GroupedPlan plan_grouped(const GroupedProblem* probs, int count, int num_
     int kmax = 64;
     for (int i = 0; i < count; ++i)
       if (probs[i].w.k > kmax) kmax = static_cast<int>(probs[i].w.k);
-    const int s_min = (kmax + kCcMaxK - 1) / kCcMaxK;
+    const int s_min = (kmax + cc_max_k(pl.mmax) - 1) / cc_max_k(pl.mmax);
     int s = 1;
     if (tiles > 0 && tiles < slots) s = slots / tiles;
     if (s > kCcMaxSplits) s = kCcMaxSplits;
@@ -1166,8 +1171,14 @@ cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws,
       if (e == cudaSuccess) e = launch_dependent(k_gemv_cc<MT>, grid, kCcThreads, cc_smem<MT>(), s, gv);   \
     }                                                                                                      \
   } while (0)
-    if (pl.mmax == 1) QLORA_CC(1);
-    else QLORA_CC(2);
+    if (pl.mmax == 1) {
+      QLORA_CC(1);
+    } else if (pl.mmax == 2) {
+      QLORA_CC(2);
+    } else {  // 3 or 4 tokens, short list (never the long-list layout)
+      e = set_smem_limit_once(k_gemv_cc<4>, cc_smem<4>());
+      if (e == cudaSuccess) e = launch_dependent(k_gemv_cc<4>, grid, kCcThreads, cc_smem<4>(), s, gv);
+    }
 #undef QLORA_CC
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
