@@ -1,15 +1,23 @@
 // Grouped small-token forward (decode): Y_p = X_p deq(W_p)^T + s_p (X_p A_p^T) B_p^T
-// for a list of independent problems p (1..16 tokens each), in two launches
-// (k_gemv_cc on the CUDA cores when no problem has more than 2 tokens).
+// for a list of independent problems p (1..16 tokens each), in two launches:
+// k_lora_down_grouped, then one GEMV over every weight of the list --
+//   k_gemv_cc_wide   CUDA cores, at most 2 tokens, lists with at least one
+//                    128-row tile per CTA slot (a whole layer stack);
+//   k_gemv_cc        CUDA cores, at most 4 tokens, shorter lists (one decoder
+//                    layer's q,k,v or gate,up): 16-row tiles, k split over
+//                    the SMs when the tiles do not fill them;
+//   k_qgemv_grouped  tensor cores, everything else (up to 16 tokens).
 //
 // Glossary "QLoRA", "How QLoRA works": the frozen layer dequantises NF4 to
 // bf16 before the matmul and adds the LoRA output; Day 25 notes section 4.4:
 // inference runs the 4-bit base with the adapter attached.  With few tokens the
-// step is a stream over the weight codes, so what matters is keeping HBM busy:
-// one launch walks the 128-row tiles of every matrix in the list.
+// step is a stream over the weight codes, so what matters is keeping HBM busy.
 //
 // k_lora_down_grouped  one CTA per problem: st_p = bf16(s_p X_p A_p^T) (and
-//                      X_p A_p^T in f32 if asked), 16 warps splitting k.
+//                      X_p A_p^T in f32 if asked), 16 warps splitting k; it
+//                      lets the GEMV launch right after it has waited for its
+//                      own predecessor, and the CUDA-core GEMVs wait for it
+//                      only before their LoRA term.
 // k_qgemv_grouped      work item = (problem, 128-row tile), dealt round-robin
 //                      to the CTAs.  Per 64-wide k block ("stage"):
 //   - a stage is two 64-wide k blocks; producer warps 1-4 decode the even
@@ -17,16 +25,18 @@
 //     (tcgen05 A operand, M = 128): a weight pair is a bf16 (L[hi], L[lo])
 //     pair from a byte-indexed shared-memory table (one column per lane, no
 //     bank conflicts) times bf16(a') in one packed multiply (within a bf16
-//     rounding of bf16(L a'); the fwd/bwd GEMMs keep the exact bf16(L a')).  Each thread prefetches its row's codes,
-//     block-scale byte, group step and mean, plus one 16-byte slice of the
-//     16-token activation tile (later of the sT tile), with cp.async into a
-//     private shared-memory ring kPrefetch stages ahead, with a meta word that
-//     tells the consuming pass what the stage is; after the stage frees, the
-//     slice goes into the 128-byte swizzled K-major B operand;
+//     rounding of bf16(L a'); the fwd/bwd GEMMs keep the exact bf16(L a')).
+//     Each thread prefetches its row's codes, block-scale byte, group step and
+//     mean, plus one 16-byte slice of the 16-token activation tile (later of
+//     the sT tile), with cp.async into a private shared-memory ring kPrefetch
+//     stages ahead, with a meta word that tells the consuming pass what the
+//     stage is; after the stage frees, the slice goes into the 128-byte
+//     swizzled K-major B operand;
 //   - one thread issues tcgen05.mma (N = 16) into a double-buffered TMEM
 //     accumulator; the LoRA up-projection is the item's last stage(s);
 //   - the producers drain item j's accumulator after producing item j+1.
-// Deterministic: every output element is written once, no atomics.
+// Deterministic: every output element is written once (the split CUDA-core
+// path adds its float32 partial sums in a fixed order).
 #include <cstdio>
 #include <cstring>
 #include <mutex>
