@@ -15,8 +15,14 @@ launching stream, max over ranks.  Also on the line:
   pinned host memory and the LoRA gradients read back every step;
 * ``cpu_baseline``: the float64 CPU oracle on a bounded sample of the workload;
 * ``secondary``: the 32-layer Llama-7B decode sweep (weight GB/s at 1, 4, 16
-  tokens), dequantise and quantise GB/s, and with --full the MLP block and the
-  65B-shaped quantise stream + up-projection step.
+  tokens; ``decode_per_layer`` is the decoder's dependency order, four calls a
+  layer), dequantise and quantise GB/s, the Llama-7B MLP block fwd+bwd
+  (``mlp_block``) and the 65B-shaped quantise stream + up-projection step
+  (``llama65b``), each with its fraction of the measured roofline.
+
+``--gpus N`` without a torchrun environment re-launches this script under
+``torch.distributed.run`` with N ranks on 127.0.0.1 (one replica per GPU); under
+torchrun, ``WORLD_SIZE`` must equal N.
 
 ``--impl reference`` times the CPU oracle (the reference for this build) on a
 bounded sample of the same workload and prints the same line with
@@ -625,10 +631,22 @@ def run_ours(args, world, rank, local):
         secondary["decode_sweep"] = sweep
         secondary["dequant"]["frac_of_hbm"] = secondary["dequant"]["gbs"] / peaks["hbm_gbs"]
         secondary["quantize"]["frac_of_hbm"] = secondary["quantize"]["gbs"] / peaks["hbm_gbs"]
-    if args.full:
+    if not args.quick:
+        secondary["decode_per_layer"] = {
+            "t%d" % t: {"weight_gbs": sweep["t%d" % t]["per_layer"]["weight_gbs"],
+                        "frac_of_hbm": sweep["t%d" % t]["per_layer"]["frac_of_hbm"],
+                        "ms_per_pass": sweep["t%d" % t]["per_layer"]["ms_per_pass"]}
+            for t in (1, 4, 16) if "t%d" % t in sweep}
+        cs = ClockSampler(local)
+        cs.start()
         secondary["mlp_block"] = mlp_block(q, torch, args.steps, flush)
+        secondary["mlp_block"]["clocks"] = cs.stop()
         secondary["mlp_block"]["frac_of_bf16_peak"] = secondary["mlp_block"]["tflops"] / peaks["bf16_tflops"]
+        cs = ClockSampler(local)
+        cs.start()
         secondary["llama65b"] = llama65b(q, torch, max(3, args.steps // 4), flush)
+        secondary["llama65b"]["clocks"] = cs.stop()
+        secondary["llama65b"]["quantize_frac_of_hbm"] = secondary["llama65b"]["quantize_gbs"] / peaks["hbm_gbs"]
         secondary["llama65b"]["upproj_fwd_bwd"]["frac_of_bf16_peak"] = (
             secondary["llama65b"]["upproj_fwd_bwd"]["tflops"] / peaks["bf16_tflops"])
 
@@ -649,6 +667,19 @@ def run_ours(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+def relaunch_under_torchrun(n: int, argv) -> int:
+    """Run this script as n ranks (one per GPU) under torch.distributed.run on 127.0.0.1."""
+    import socket
+    sk = socket.socket()
+    sk.bind(("127.0.0.1", 0))
+    port = sk.getsockname()[1]
+    sk.close()
+    args = list(sys.argv[1:] if argv is None else argv)
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", str(n),
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__), *args]
+    return subprocess.call(cmd)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -657,7 +688,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only (no decode sweep / dequant rates)")
     ap.add_argument("--eager", action="store_true", help="time eager library calls instead of the graph replay")
-    ap.add_argument("--full", action="store_true", help="also the MLP block and the 65B-shaped stream + up-proj")
+    ap.add_argument("--full", action="store_true", help="(kept for old command lines: the MLP block and the 65B "
+                                                        "leg are part of the default run)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=128)
@@ -683,6 +715,12 @@ def main(argv=None):
         rank = int(os.environ.get("RANK", "0"))
         run_reference(args, world, rank)
         return
+    env_world = os.environ.get("WORLD_SIZE")
+    if env_world is None and args.gpus > 1:
+        sys.exit(relaunch_under_torchrun(args.gpus, argv))
+    if env_world is not None and int(env_world) != args.gpus:
+        sys.stderr.write("bench.py: --gpus %d but WORLD_SIZE=%s\n" % (args.gpus, env_world))
+        sys.exit(2)
     world, rank, local = dist_setup(args)
     run_ours(args, world, rank, local)
     if world > 1:

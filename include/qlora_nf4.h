@@ -108,12 +108,21 @@ int qlora_nf4_quantize(const void* w, int w_dtype, int64_t n, int64_t k, const q
  * it computes exactly what qlora_nf4_quantize computes (same kernels, same
  * bits), with the scratch taken from a fixed module-scope device array.
  *   - Limit: n * k <= 2^26 weights (1,048,576 absmax blocks; 4 MiB + 2.3 KiB of
- *     scratch, held by every device that loads the library until exit).
- *     Larger weights return QLORA_ERR_UNSUPPORTED before anything is launched.
- *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on a device looks up the scratch address for that device
- *     (cudaGetSymbolAddress, with that device current) and caches it; make the
- *     first call on each device before any stream capture.
+ *     scratch, held on every device that has loaded the library's kernels,
+ *     until exit).  Larger weights return QLORA_ERR_UNSUPPORTED before
+ *     anything is launched.
+ *   - Allocates nothing on the call path: no cudaMalloc, cudaFree or
+ *     allocating library call.
+ *   - When the scratch is reserved: under CUDA's default lazy module loading
+ *     the library's device code, and with it the scratch, is loaded on a
+ *     device by the first call that needs it -- the first call of this entry
+ *     point on that device (which looks up the scratch address with
+ *     cudaGetSymbolAddress, with that device current, and caches it) or of any
+ *     other entry point that launches a kernel.  A caller whose memory budget
+ *     is fixed at start-up should therefore make one call on each device at
+ *     start-up (also before any stream capture), or run with
+ *     CUDA_MODULE_LOADING=EAGER so the scratch is reserved when the CUDA
+ *     context is created.
  *   - All calls on a device share the scratch.  Each call clears the parts
  *     that must start at zero and overwrites the rest, but calls whose kernels
  *     overlap on the GPU (different streams without ordering) race on it:

@@ -16,7 +16,7 @@ Sources (page title, section):
   "double quantisation"): 64 parameters share one fp32 scale; 0.5 byte per
   parameter for the codes.
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 
 * table built in float64 and rounded once to float32 (the page builds it in
   torch float32; both give the page's worked-example MSE to 4 digits);
@@ -73,26 +73,38 @@ def bf16_bits_to_f32(b) -> np.ndarray:
 # --------------------------------------------------------------------------
 # NF4 level table
 # --------------------------------------------------------------------------
-def _linspace64(a: float, b: float, n: int) -> np.ndarray:
-    """``n`` evenly spaced points from ``a`` to ``b`` inclusive, in float64."""
-    return np.array([a + i * (b - a) / (n - 1) for i in range(n)], dtype=np.float64)
+# Largest probability at which the levels take a normal quantile (glossary
+# "QLoRA", "How QLoRA works"); the two halves of the table use evenly spaced
+# probabilities from here down toward one half.
+P_TOP = 0.9677083
+
+
+def _side_quantiles(count: int) -> list:
+    """Standard-normal quantiles at ``count`` probabilities, the first P_TOP,
+    then equal steps of (1/2 - P_TOP) / count toward 1/2 (1/2 itself is not
+    taken, so no quantile here is zero).  Largest quantile first.  ``ndtri``
+    (the inverse normal CDF) is the library step."""
+    probs = [P_TOP + i * (0.5 - P_TOP) / count for i in range(count)]
+    return [float(ndtri(pr)) for pr in probs]
 
 
 def nf4_levels_f64() -> np.ndarray:
-    """The 16 NF4 levels in float64.
+    """The 16 NF4 levels in float64, ascending.
 
-    Ultralytics glossary "QLoRA", "How QLoRA works" (the snippet that builds
-    the levels as bitsandbytes does): 8 positive levels are the standard-normal
-    quantiles at 9 evenly spaced probabilities from 0.9677083 down to 0.5 with
-    the last (0.5) dropped; 7 negative levels are the negated quantiles at 8
-    evenly spaced probabilities over the same range, last dropped; one exact
-    zero; sort ascending; divide by the largest so the ends are -1 and +1.
-    ``ndtri`` (the inverse normal CDF) is the library step.
+    Glossary "QLoRA", "How QLoRA works": the levels sit at quantiles of the
+    standard normal with one exact zero, 7 below it and 8 above it, and the
+    table is scaled so its ends are -1 and +1.  The 8 positive levels take the
+    quantiles of :func:`_side_quantiles` with 8 steps; the 7 negative levels
+    take the negated quantiles with 7 steps (so the two sides are not mirror
+    images); every level is divided by the largest quantile, which both sides
+    share (the one at P_TOP).
     """
-    positive = ndtri(_linspace64(0.9677083, 0.5, 9)[:-1])
-    negative = -ndtri(_linspace64(0.9677083, 0.5, 8)[:-1])
-    levels = np.sort(np.concatenate([negative, [0.0], positive]))
-    return levels / levels.max()
+    upper = _side_quantiles(8)
+    lower = _side_quantiles(7)
+    top = upper[0]
+    negative = [-q / top for q in lower]                # -1 first, rising toward 0
+    positive = [q / top for q in reversed(upper)]       # smallest first, +1 last
+    return np.array(negative + [0.0] + positive, dtype=np.float64)
 
 
 def nf4_levels_f32() -> np.ndarray:
@@ -178,6 +190,15 @@ def unpack_codes(packed: np.ndarray) -> np.ndarray:
     out[0::2] = p >> 4
     out[1::2] = p & 0x0F
     return out
+
+
+def restore_with_levels(codes: np.ndarray, absmax: np.ndarray, levels: np.ndarray) -> np.ndarray:
+    """Reconstruction ``levels[code] * absmax`` in float32 with the raw block scale
+    (glossary "QLoRA", "How QLoRA works": the restored weight is the level times
+    the block's scale).  ``codes`` holds one code per element (not packed)."""
+    c = np.asarray(codes, dtype=np.uint8).reshape(-1, BLOCK)
+    a = np.asarray(absmax, dtype=F32).reshape(-1, 1)
+    return (np.asarray(levels, dtype=F32)[c] * a).astype(F32).reshape(-1)
 
 
 # --------------------------------------------------------------------------

@@ -5,7 +5,7 @@ arithmetic (no quantisation, no level table, no matmul).  Both the oracle side
 and the CUDA side are fed from here.
 
 Shapes and distributions follow the five workload descriptions of the QLoRA
-linear (Llama-7B / 65B shaped, see DESIGN.md "Input recipe"):
+linear (Llama-7B / 65B shaped):
 
 * weights ~ N(0, 0.02^2), drawn in float32, rounded to bfloat16 unless the
   workload keeps float32 (the tiny case);

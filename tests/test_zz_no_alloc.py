@@ -38,6 +38,23 @@ def test_noalloc_quantize_matches_workspace_quantize_twice(lib):
         _same_record(got, ref)
 
 
+def test_noalloc_largest_accepted_weight(lib):
+    """n*k == 2^26 exactly (8192 x 8192, the limit): bit-exact against the workspace quantiser,
+    twice in a row; one row more (8200 x 8192) is refused before anything runs."""
+    w = synthetic.weight(8192, 8192, device="cuda", seed=3)
+    ref = lib.quantize(w)
+    for _ in range(2):
+        got = lib.quantize_noalloc(w)
+        lib.check_status()
+        _same_record(got, ref)
+    import torch
+    big = torch.zeros((8200, 8192), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(lib.QloraError) as e:
+        lib.quantize_noalloc(big)
+    assert e.value.code == lib.QLORA_ERR_UNSUPPORTED
+    lib.check_status()
+
+
 def test_noalloc_quantize_float32_input(lib):
     case = synthetic.tiny_case()
     w = case.w.cuda()
