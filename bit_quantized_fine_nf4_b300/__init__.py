@@ -32,6 +32,8 @@ from ._binding import (  # noqa: F401
     linear_fwd,
     linear_fwd_grouped,
     load,
+    lowrank_update,
+    merge,
     profile_enable,
     profile_read,
     profile_reset,

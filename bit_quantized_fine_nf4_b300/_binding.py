@@ -36,6 +36,8 @@ EXPORTS = (
     "qlora_nf4_quantize",
     "qlora_nf4_quantize_noalloc",
     "qlora_nf4_dequantize",
+    "qlora_nf4_merge",
+    "qlora_lowrank_update",
     "qlora_linear_fwd_workspace_bytes",
     "qlora_linear_fwd",
     "qlora_linear_bwd_workspace_bytes",
@@ -116,6 +118,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "qlora_nf4_quantize": (c_int, [_P, c_int, _I64, _I64, _PW, _P, _SZ, _P]),
         "qlora_nf4_quantize_noalloc": (c_int, [_P, c_int, _I64, _I64, _PW, _P]),
         "qlora_nf4_dequantize": (c_int, [_PW, _P, _P]),
+        "qlora_nf4_merge": (c_int, [_PW, _P, _P, c_int, c_float, _P, _P]),
+        "qlora_lowrank_update": (c_int, [_P, c_int, _I64, _I64, _PW, _P, _P, c_int, c_float, _P, _P]),
         "qlora_linear_fwd_workspace_bytes": (c_int, [_I64, _I64, _I64, c_int, _PSZ]),
         "qlora_linear_fwd": (c_int, [_P, _I64, _PW, _P, _P, c_int, c_float, _P, _P, _P, _SZ, _P]),
         "qlora_linear_bwd_workspace_bytes": (c_int, [_I64, _I64, _I64, c_int, _PSZ]),
@@ -249,6 +253,36 @@ def dequantize(rec: NF4Weight, out: torch.Tensor | None = None, stream=None) -> 
         out = torch.empty((rec.n, rec.k), dtype=torch.bfloat16, device=rec.codes.device)
     c = rec.c_struct()
     _check(lib.qlora_nf4_dequantize(ctypes.byref(c), _ptr(out), _stream(stream)))
+    return out
+
+
+def merge(rec: NF4Weight, lora_a: torch.Tensor, lora_b: torch.Tensor, alpha: float, out: torch.Tensor | None = None,
+          stream=None) -> torch.Tensor:
+    """bf16 [n, k] = bf16(deq(W) + (alpha/r) B A): the merged weight for export (qlora_nf4_merge)."""
+    lib = load()
+    if out is None:
+        out = torch.empty((rec.n, rec.k), dtype=torch.bfloat16, device=rec.codes.device)
+    c = rec.c_struct()
+    _check(lib.qlora_nf4_merge(ctypes.byref(c), _ptr(lora_a), _ptr(lora_b), lora_a.shape[0], float(alpha), _ptr(out),
+                               _stream(stream)))
+    return out
+
+
+def lowrank_update(w: torch.Tensor, sub: NF4Weight | None = None, lora_a: torch.Tensor | None = None,
+                   lora_b: torch.Tensor | None = None, coef: float = 0.0, out: torch.Tensor | None = None,
+                   stream=None) -> torch.Tensor:
+    """float32 [n, k] = (W - deq(sub)) + coef B A (qlora_lowrank_update); sub and the LoRA pair are optional."""
+    lib = load()
+    n, k = w.shape
+    dtype = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16}.get(w.dtype)
+    if dtype is None:
+        raise ValueError("weight must be float32 or bfloat16")
+    if out is None:
+        out = torch.empty((n, k), dtype=torch.float32, device=w.device)
+    r = 0 if lora_a is None else lora_a.shape[0]
+    cs = ctypes.byref(sub.c_struct()) if sub is not None else None
+    _check(lib.qlora_lowrank_update(_ptr(w), dtype, n, k, cs, _ptr(lora_a), _ptr(lora_b), r, float(coef), _ptr(out),
+                                    _stream(stream)))
     return out
 
 

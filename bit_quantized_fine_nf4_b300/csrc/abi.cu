@@ -95,9 +95,12 @@ int check_weight(const qlora_nf4_weight* w) {
 }
 
 int check_rank(int r) {
-  if (r < 8 || r > 128 || (r % 8)) return fail(QLORA_ERR_UNSUPPORTED, "rank r = %d (need 8 <= r <= 128, r %% 8 == 0)", r);
+  if (r < 1 || r > 128) return fail(QLORA_ERR_UNSUPPORTED, "rank r = %d (need 1 <= r <= 128)", r);
   return QLORA_OK;
 }
+
+// Bytes of one internal bf16 LoRA operand (sT or sU): m rows of lora_ld(r) columns.
+size_t lora_operand_bytes(int64_t m, int r) { return align256(static_cast<size_t>(m) * qlora::lora_ld(r) * 2); }
 
 int check_ptr(const void* p, const char* name) {
   if (!p) return fail(QLORA_ERR_INVALID_ARGUMENT, "%s is NULL", name);
@@ -114,7 +117,7 @@ FwdWs fwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
     w.st = w.ld = w.gemm = w.total = 0;
     return w;
   }
-  w.st = align256(static_cast<size_t>(m) * r * 2);
+  w.st = lora_operand_bytes(m, r);
   w.ld = align256(qlora::lora_down_workspace_bytes(static_cast<int>(m), static_cast<int>(k), r, sms));
   w.gemm = align256(qlora::fwd_gemm_workspace_bytes(static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), sms));
   w.total = w.st + w.ld + w.gemm;
@@ -133,7 +136,7 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
     w.su = w.st = w.ld = w.lg = w.total = 0;
     return w;
   }
-  w.su = align256(static_cast<size_t>(m) * r * 2);
+  w.su = lora_operand_bytes(m, r);
   w.st = w.su;
   w.ld = align256(qlora::lora_down_workspace_bytes(static_cast<int>(m), static_cast<int>(n), r, sms));
   w.lg = align256(qlora::lora_grads_workspace_bytes(static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), r, sms));
@@ -146,11 +149,12 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 // and, while profiling is on, bracketed by two CUDA events on its stream.
 enum ProfName : int {
   P_QUANTIZE = 0, P_DEQUANTIZE, P_LORA_DOWN, P_FWD_GEMM, P_BWD_GEMM, P_LORA_GRADS, P_SILU_FWD, P_SILU_BWD,
-  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_COUNT
+  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_MERGE, P_LOWRANK, P_COUNT
 };
 const char* const kProfNames[P_COUNT] = {"nf4_quantize(3 kernels)", "nf4_dequantize", "lora_down", "fwd_gemm",
                                          "bwd_dx_gemm", "lora_grads", "silu_mul_fwd", "silu_mul_bwd",
-                                         "wait_selftest", "fwd_grouped(2 kernels)", "lora_side_fwd"};
+                                         "wait_selftest", "fwd_grouped(2 kernels)", "lora_side_fwd", "nf4_merge",
+                                         "lowrank_update"};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<bool> g_prof_on{false};
 struct ProfRec {
@@ -276,6 +280,48 @@ int qlora_nf4_dequantize(const qlora_nf4_weight* w, uint16_t* out, void* stream)
                   "dequantize");
 }
 
+int qlora_nf4_merge(const qlora_nf4_weight* w, const uint16_t* lora_a, const uint16_t* lora_b, int r, float alpha,
+                    uint16_t* out, void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if ((rc = check_weight(w))) return rc;
+  if ((rc = check_rank(r))) return rc;
+  if ((rc = check_ptr(lora_a, "lora_a")) || (rc = check_ptr(lora_b, "lora_b")) || (rc = check_ptr(out, "out"))) return rc;
+  Span sp(P_MERGE, static_cast<cudaStream_t>(stream), 1);
+  return cuda_ret(qlora::launch_nf4_merge(to_dev(w), reinterpret_cast<const __nv_bfloat16*>(lora_a),
+                                          reinterpret_cast<const __nv_bfloat16*>(lora_b), r,
+                                          alpha / static_cast<float>(r), reinterpret_cast<__nv_bfloat16*>(out),
+                                          static_cast<cudaStream_t>(stream)),
+                  "merge");
+}
+
+int qlora_lowrank_update(const void* w, int w_dtype, int64_t n, int64_t k, const qlora_nf4_weight* sub,
+                         const uint16_t* lora_a, const uint16_t* lora_b, int r, float coef, float* out, void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if ((rc = check_ptr(w, "w")) || (rc = check_ptr(out, "out"))) return rc;
+  if (w_dtype != QLORA_DTYPE_F32 && w_dtype != QLORA_DTYPE_BF16) return fail(QLORA_ERR_INVALID_ARGUMENT, "w_dtype %d", w_dtype);
+  if (n <= 0 || k <= 0) return fail(QLORA_ERR_INVALID_ARGUMENT, "shape [%lld, %lld]", (long long)n, (long long)k);
+  if (k % 64) return fail(QLORA_ERR_UNSUPPORTED, "k = %lld is not a multiple of 64", (long long)k);
+  if (n >= (1ll << 31) || k >= (1ll << 31)) return fail(QLORA_ERR_UNSUPPORTED, "dimension >= 2^31");
+  if (sub) {
+    if ((rc = check_weight(sub))) return rc;
+    if (sub->n != n || sub->k != k) return fail(QLORA_ERR_INVALID_ARGUMENT, "record shape differs from the weight shape");
+  }
+  if (r < 0 || r > 128) return fail(QLORA_ERR_UNSUPPORTED, "rank r = %d (need 0 <= r <= 128)", r);
+  if (r > 0 && ((rc = check_ptr(lora_a, "lora_a")) || (rc = check_ptr(lora_b, "lora_b")))) return rc;
+  qlora::Nf4Dev d;
+  if (sub) d = to_dev(sub);
+  Span sp(P_LOWRANK, static_cast<cudaStream_t>(stream), 1);
+  return cuda_ret(qlora::launch_lowrank_update(w, w_dtype == QLORA_DTYPE_BF16 ? 1 : 0, sub ? &d : nullptr,
+                                               reinterpret_cast<const __nv_bfloat16*>(lora_a),
+                                               reinterpret_cast<const __nv_bfloat16*>(lora_b), r, coef, out, n, k,
+                                               static_cast<cudaStream_t>(stream)),
+                  "lowrank update");
+}
+
 int qlora_linear_fwd_workspace_bytes(int64_t m, int64_t n, int64_t k, int r, size_t* bytes) {
   if (!bytes) return fail(QLORA_ERR_INVALID_ARGUMENT, "bytes is NULL");
   if (m < 0 || n <= 0 || k <= 0 || m >= (1ll << 31)) return fail(QLORA_ERR_INVALID_ARGUMENT, "shape");
@@ -390,7 +436,7 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
     // U = dY B (B read as stored) and, in the same launch, sT = bf16(s * t_save)
     Span sp(P_LORA_DOWN, s, 1);
     e = qlora::launch_lora_down(dyb, reinterpret_cast<const __nv_bfloat16*>(lora_b), 0, M, N, r, scale, nullptr, su,
-                                ldws, di->num_sms, s, t_save, st, static_cast<int64_t>(M) * r, scale);
+                                ldws, di->num_sms, s, t_save, st, static_cast<int64_t>(M), scale);
   }
   if (e != cudaSuccess) return cuda_ret(e, "lora_down (U)");
   std::lock_guard<std::mutex> lk(di->side_mu);

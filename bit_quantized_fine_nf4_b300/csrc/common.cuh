@@ -392,6 +392,31 @@ __device__ __forceinline__ void sts_v4(uint32_t saddr, uint32_t a, uint32_t b, u
                : "memory");
 }
 
+// 64 LoRA B entries B[row, jb .. jb+63] as 32 bf16x2 words (zero past r or
+// past the last row).  B is [n_rows, r] row-major: with r even its rows start
+// on 4-byte boundaries and are read in 32-bit words; with r odd, element by element.
+__device__ __forceinline__ void load_lora_b_row(const __nv_bfloat16* lora_b, int row, int n_rows, int r, int jb,
+                                                uint32_t (&words)[32]) {
+  const bool row_ok = row < n_rows;
+  if ((r & 1) == 0) {
+    const uint32_t* brow = reinterpret_cast<const uint32_t*>(lora_b + static_cast<int64_t>(row) * r);
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int j = jb + 2 * c;
+      words[c] = (row_ok && j < r) ? brow[j >> 1] : 0u;
+    }
+  } else {
+    const unsigned short* b16 = reinterpret_cast<const unsigned short*>(lora_b) + static_cast<int64_t>(row) * r;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) {
+      const int j = jb + 2 * c;
+      const uint32_t lo = (row_ok && j < r) ? b16[j] : 0u;
+      const uint32_t hi = (row_ok && j + 1 < r) ? b16[j + 1] : 0u;
+      words[c] = lo | (hi << 16);
+    }
+  }
+}
+
 // Host: raise a kernel's dynamic shared-memory limit once per (kernel, device)
 // (the attribute call is host work; repeating it on every launch costs
 // microseconds).  Keyed by the kernel's address: template instances of one

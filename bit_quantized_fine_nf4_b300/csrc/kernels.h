@@ -28,13 +28,18 @@ cudaError_t launch_nf4_dequantize(const uint8_t* codes, const int8_t* absq, cons
 
 // lora_small.cu
 size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms);
+// Row stride of the internal bf16 LoRA operands sT / sU ([rows, r] padded with
+// zero columns): r rounded up to a multiple of 8, so every row starts on a
+// 16-byte boundary as TMA requires.
+__host__ __device__ inline int lora_ld(int r) { return (r + 7) & ~7; }
 // out = in . mt^T with mt either [r, K] (mt_kmajor) or [K, r], by at most
-// max_ctas persistent CTAs; optional side job cvt_dst[i] = bf16(cvt_scale *
-// cvt_src[i]) for i < cvt_n in the same launch.
+// max_ctas persistent CTAs: out_f32 [M, r], out_bf16 = bf16(scale out) [M, lora_ld(r)];
+// optional side job cvt_dst = bf16(cvt_scale * cvt_src) for the cvt_rows x r
+// matrix cvt_src into cvt_dst [cvt_rows, lora_ld(r)], in the same launch.
 cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int mt_kmajor, int M, int K, int r,
                              float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int max_ctas,
                              cudaStream_t s, const float* cvt_src = nullptr, __nv_bfloat16* cvt_dst = nullptr,
-                             int64_t cvt_n = 0, float cvt_scale = 1.0f);
+                             int64_t cvt_rows = 0, float cvt_scale = 1.0f);
 cudaError_t launch_silu_mul_fwd(const uint16_t* g, const uint16_t* u, uint16_t* h, int64_t n, int num_sms,
                                 cudaStream_t s);
 cudaError_t launch_silu_mul_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u, uint16_t* dg, uint16_t* du,
@@ -76,10 +81,18 @@ cudaError_t launch_fwd_gemm_pair(const __nv_bfloat16* x, int M, const Nf4Dev& w,
 cudaError_t launch_bwd_gemm_pair(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
                                  const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
                                  unsigned* status, uint64_t wait_ns, cudaStream_t s);
+// Low-rank combinations (nf4_merge.cu).
+// out[n, k] = bf16(deq(W) + scale * B A), the B A sum a float32 FMA chain in j order.
+cudaError_t launch_nf4_merge(const Nf4Dev& w, const __nv_bfloat16* lora_a, const __nv_bfloat16* lora_b, int r,
+                             float scale, __nv_bfloat16* out, cudaStream_t s);
+// out[n, k] = (W - deq(sub)) + coef * B A in float32 (sub may be null; r may be 0).
+cudaError_t launch_lowrank_update(const void* dense, int dense_bf16, const Nf4Dev* sub, const __nv_bfloat16* lora_a,
+                                  const __nv_bfloat16* lora_b, int r, float coef, float* out, int64_t n, int64_t k,
+                                  cudaStream_t s);
 // 2-D bf16 tensor map, 128-byte swizzle, zero fill outside [outer x inner] (qgemm.cu).
 bool make_tensor_map_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
                              uint32_t box_inner, uint32_t box_outer);
-// Forward LoRA down-projection beside the pair GEMM (lora_side.cu), 8 <= r <= 64:
+// Forward LoRA down-projection beside the pair GEMM (lora_side.cu), 1 <= r <= 64:
 // T = X A^T -> t_save, sT = bf16(s T), by at most max_ctas CTAs.
 bool lora_side_supported(int r);
 cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lora_a, int M, int K, int r, float scale,

@@ -6,7 +6,7 @@
 // [RP x 64 k] (K-major, 128B swizzle; RP = r rounded up to 16, rows past r are
 // zero) through a deep ring (an SM's read rate grows with the bytes in flight),
 // one thread issues M = 128 x N = RP MMAs into a double-buffered TMEM
-// accumulator, and four warps write t_save and sT.  The GEMM that consumes sT
+// accumulator, and four warps write t_save [M, r] and sT [M, lora_ld(r)].  The GEMM that consumes sT
 // starts beside this kernel and waits for it only before its LoRA k block.
 #include "common.cuh"
 #include "kernels.h"
@@ -15,7 +15,7 @@ namespace qlora {
 
 struct SideParams {
   float* t_out;          // t_save [M, r]
-  __nv_bfloat16* s_out;  // sT [M, r]
+  __nv_bfloat16* s_out;  // sT [M, lora_ld(r)]
   unsigned* status;
   int M, K, r, rp;
   int stages, stage_bytes;
@@ -122,6 +122,7 @@ __global__ void __launch_bounds__(kSideThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int tok = tile * 128 + lrow;
+      const int rk = lora_ld(p.r);  // sT row stride; columns r .. rk-1 are zero (A rows past r load as zero)
       for (int c = 0; c < RP; c += 16) {
         uint32_t v[16];
         __syncwarp();
@@ -130,14 +131,19 @@ __global__ void __launch_bounds__(kSideThreads, 1)
         if (tok < p.M) {
 #pragma unroll
           for (int q = 0; q < 16; q += 4) {
-            if (c + q < p.r) {  // r % 8 == 0: four consecutive columns are all inside r or all past it
-              const float4 f = make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]), __uint_as_float(v[q + 2]),
-                                           __uint_as_float(v[q + 3]));
-              const int64_t o = static_cast<int64_t>(tok) * p.r + c + q;
-              *reinterpret_cast<float4*>(p.t_out + o) = f;
-              *reinterpret_cast<uint2*>(p.s_out + o) =
-                  make_uint2(pack_bf16x2_rn(__fmul_rn(f.x, p.scale), __fmul_rn(f.y, p.scale)),
-                             pack_bf16x2_rn(__fmul_rn(f.z, p.scale), __fmul_rn(f.w, p.scale)));
+            const float f[4] = {__uint_as_float(v[q]), __uint_as_float(v[q + 1]), __uint_as_float(v[q + 2]),
+                                __uint_as_float(v[q + 3])};
+            if (c + q < rk)  // rk % 8 == 0: four consecutive columns are all inside rk or all past it
+              *reinterpret_cast<uint2*>(p.s_out + static_cast<int64_t>(tok) * rk + c + q) =
+                  make_uint2(pack_bf16x2_rn(__fmul_rn(f[0], p.scale), __fmul_rn(f[1], p.scale)),
+                             pack_bf16x2_rn(__fmul_rn(f[2], p.scale), __fmul_rn(f[3], p.scale)));
+            float* to = p.t_out + static_cast<int64_t>(tok) * p.r + c + q;
+            if ((p.r & 3) == 0) {  // rows of t_save start on 16-byte boundaries
+              if (c + q < p.r) *reinterpret_cast<float4*>(to) = make_float4(f[0], f[1], f[2], f[3]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (c + q + e < p.r) to[e] = f[e];
             }
           }
         }
@@ -156,7 +162,7 @@ __global__ void __launch_bounds__(kSideThreads, 1)
 }
 
 // ------------------------------------------------------------------ host
-bool lora_side_supported(int r) { return r >= 8 && r <= 64 && r % 8 == 0; }
+bool lora_side_supported(int r) { return r >= 1 && r <= 64; }
 
 cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lora_a, int M, int K, int r, float scale,
                                  float* t_save, __nv_bfloat16* st, int max_ctas, unsigned* status, uint64_t wait_ns,

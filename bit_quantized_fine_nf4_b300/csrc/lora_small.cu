@@ -42,8 +42,14 @@ __device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, ui
 // 16-byte fragment loads of 8 rows x 4 threads hit distinct bank groups; every
 // tile then reads its fragments from there.  Unstaged, fragments come from
 // global memory (and gather 8 strided values when mt is [K, r]).
-// Side job (optional): cvt_dst[i] = bf16(cvt_scale * cvt_src[i]), spread over
-// all threads of the grid -- an independent elementwise pass in the same launch.
+// Outputs: out_f32 [M, r] (row stride r) and out_bf16 = bf16(scale * out)
+// [M, rk] with rk = r rounded up to a multiple of 8 (the row stride of the
+// internal bf16 LoRA operands, which the tensor-core kernels load by TMA); its
+// columns r .. rk-1 are zero.
+// Side job (optional): cvt_dst[i, j] = bf16(cvt_scale * cvt_src[i, j]) for the
+// cvt_rows x r matrix cvt_src (row stride r) into cvt_dst (row stride rk, zero
+// in columns r .. rk-1), spread over all threads of the grid -- an independent
+// elementwise pass in the same launch.
 template <int NT, bool MT_KMAJOR>
 __device__ __forceinline__ uint4 load_mt_frag(const __nv_bfloat16* __restrict__ mt, int j, int kb, int K, int r) {
   if (MT_KMAJOR) return ldg_nc_v4(mt + static_cast<int64_t>(j) * K + kb);
@@ -60,7 +66,7 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
                                                       float scale, float* __restrict__ out_f32,
                                                       __nv_bfloat16* __restrict__ out_bf16,
                                                       const float* __restrict__ cvt_src,
-                                                      __nv_bfloat16* __restrict__ cvt_dst, int64_t cvt_n,
+                                                      __nv_bfloat16* __restrict__ cvt_dst, int64_t cvt_rows,
                                                       float cvt_scale) {
   constexpr int RP = NT * 8;
   extern __shared__ float s_red[];  // [W warps][16 rows][RP], then (STAGED) mt as [RP][K + 8] bf16
@@ -82,22 +88,33 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
       const int jg = RP / 8;
       for (int i = threadIdx.x; i < K * jg; i += W * 32) {
         const int k = i / jg, j0 = (i - k * jg) * 8;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (j0 < r) v = *reinterpret_cast<const uint4*>(mt + static_cast<int64_t>(k) * r + j0);  // r % 8 == 0
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const unsigned short* src = reinterpret_cast<const unsigned short*>(mt) + static_cast<int64_t>(k) * r;
+        if ((r & 7) == 0) {  // rows of mt start on 16-byte boundaries
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (j0 < r) v = *reinterpret_cast<const uint4*>(src + j0);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          s_mt[(j0 + 2 * e) * mt_pitch + k] = static_cast<unsigned short>(w[e] & 0xffffu);
-          s_mt[(j0 + 2 * e + 1) * mt_pitch + k] = static_cast<unsigned short>(w[e] >> 16);
+          for (int e = 0; e < 4; ++e) {
+            s_mt[(j0 + 2 * e) * mt_pitch + k] = static_cast<unsigned short>(w[e] & 0xffffu);
+            s_mt[(j0 + 2 * e + 1) * mt_pitch + k] = static_cast<unsigned short>(w[e] >> 16);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s_mt[(j0 + e) * mt_pitch + k] = j0 + e < r ? src[j0 + e] : 0;
         }
       }
     }
     __syncthreads();
   }
-  if (cvt_n > 0) {
+  const int rk = (r + 7) & ~7;
+  if (cvt_rows > 0) {
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < cvt_n; i += nthreads)
-      cvt_dst[i] = __float2bfloat16_rn(__fmul_rn(cvt_src[i], cvt_scale));
+    const int64_t n_out = cvt_rows * rk;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_out; i += nthreads) {
+      const int64_t row = i / rk;
+      const int j = static_cast<int>(i - row * rk);
+      cvt_dst[i] = j < r ? __float2bfloat16_rn(__fmul_rn(cvt_src[row * r + j], cvt_scale)) : __float2bfloat16_rn(0.f);
+    }
   }
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, q = lane & 3;
@@ -155,9 +172,10 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
 #pragma unroll
       for (int w = 0; w < W; ++w) v += s_red[w * 16 * RP + idx];
       const int row = m0 + idx / RP, j = idx % RP;
-      if (row >= M || j >= r) continue;
-      if (out_f32) out_f32[static_cast<int64_t>(row) * r + j] = v;
-      if (out_bf16) out_bf16[static_cast<int64_t>(row) * r + j] = __float2bfloat16_rn(__fmul_rn(v, scale));
+      if (row >= M) continue;
+      // columns j >= r of the product are exactly zero (mt rows past r load as zero)
+      if (out_f32 && j < r) out_f32[static_cast<int64_t>(row) * r + j] = v;
+      if (out_bf16 && j < rk) out_bf16[static_cast<int64_t>(row) * rk + j] = __float2bfloat16_rn(__fmul_rn(v, scale));
     }
     __syncthreads();  // s_red is reused by the next tile
   }
@@ -210,7 +228,7 @@ size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms) {
 
 cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int mt_kmajor, int M, int K, int r,
                              float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int max_ctas,
-                             cudaStream_t s, const float* cvt_src, __nv_bfloat16* cvt_dst, int64_t cvt_n,
+                             cudaStream_t s, const float* cvt_src, __nv_bfloat16* cvt_dst, int64_t cvt_rows,
                              float cvt_scale) {
   (void)ws;
   const int tiles = (M + 15) / 16;
@@ -241,7 +259,7 @@ cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, i
     cfg.blockDim = dim3(W * 32);                                                                                 \
     cfg.dynamicSmemBytes = smem;                                                                                 \
     e = cudaLaunchKernelEx(&cfg, k_lora_down<NT, KM, W, ST>, in, mt, M, K, r, scale, out_f32, out_bf16, cvt_src, \
-                           cvt_dst, cvt_n, cvt_scale);                                                           \
+                           cvt_dst, cvt_rows, cvt_scale);                                                        \
   } while (0)
 #define QLORA_LD(NT, KM, W)           \
   do {                                \

@@ -1,0 +1,231 @@
+// Low-rank combinations of a frozen weight with its LoRA branch:
+//
+//   merge / export   out_bf16[n, k] = bf16( deq(W)[n, k] + s * sum_j B[n, j] A[j, k] )
+//   dense update     out_f32[n, k]  = W[n, k] (- deq(Q)[n, k]) + c * sum_j B[n, j] A[j, k]
+//
+// Day 25 notes "Fine-tuning and LoRA/QLoRA", section 2.6: after training the
+// product B A is added to W0 and the layer is a plain linear again.  P1 tutorial
+// "QLoRA: fine-tuning 7B on a 24 GB card", section 3.8, and the glossary "QLoRA",
+// section "Trade-offs": a 4-bit base cannot be merged as is -- dequantise it to
+// 16 bits first, merge, and quantise again for serving.  The dense update
+// (W - s B A, W - deq(Q)) is the arithmetic of the LoftQ initialisation of the
+// same tutorial, section 3.10.
+//
+// The arithmetic is fixed so the result is reproducible bit for bit:
+//   deq(W)[n, k] = bf16_rn(L[code] * a') exactly as the dequantiser computes it;
+//   acc = sum over j = 0, 1, ..., r-1 of B[n, j] * A[j, k] in float32, one fused
+//         multiply-add per term (B and A are bf16, so every product is exact and
+//         each step rounds once, like a separate add);
+//   merge:  bf16_rn(deq + s * acc)   (s * acc rounded, then the add rounded);
+//   update: (W - deq(Q)) + c * acc   (each operation rounded once in float32).
+//
+// Layout: a CTA of 8 warps takes a tile of 32 rows x 256 columns; warp w owns
+// rows 4w .. 4w+3, lane l the 8 columns 8l .. 8l+7 of each.  A[:, tile columns]
+// is staged once in shared memory as float32 [r][256], B[tile rows, :] as
+// float32 [r][32] (transposed), so each term costs two 16-byte loads of A, one
+// broadcast load of B and 16 packed float32x2 FMAs for 32 outputs.  The
+// weight is HBM traffic (0.516 B per weight read, 2 or 4 B written); the FMA
+// chain is r multiply-adds per weight on the CUDA cores.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace qlora {
+
+constexpr int kMgRows = 32;
+constexpr int kMgCols = 256;
+constexpr int kMgThreads = 256;
+
+enum MgBase : int { MG_NF4 = 0, MG_F32 = 1, MG_BF16 = 2 };
+
+struct MgParams {
+  // NF4 record (the merge base, or the record subtracted by the dense update)
+  const uint8_t* codes;
+  const int8_t* absq;
+  const float* step;
+  const float* mean;
+  const void* dense;            // dense W [n, k] (float32 or bfloat16), dense update only
+  const __nv_bfloat16* lora_a;  // [r, k]
+  const __nv_bfloat16* lora_b;  // [n, r]
+  void* out;                    // bf16 (merge) or float32 (update) [n, k]
+  int n, k, r;
+  float coef;
+};
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
+
+// The 8 dequantised weights of row n, columns k .. k+7 (k % 8 == 0), as float32
+// holding bf16 values.
+__device__ __forceinline__ void deq8(const MgParams& p, const float* s_lv, float mu, int n, int k, float (&w)[8]) {
+  const int64_t e0 = static_cast<int64_t>(n) * p.k + k;
+  const uint32_t word = *reinterpret_cast<const uint32_t*>(p.codes + e0 / 2);
+  const int64_t b = e0 / 64;
+  const float a2 = restore_absmax(p.absq[b], p.step[b >> 8], mu);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    // element 2i sits in the high nibble of byte i
+    const uint32_t c = (word >> (8 * (e >> 1) + ((e & 1) ? 0 : 4))) & 15u;
+    w[e] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(s_lv[c], a2)));
+  }
+}
+
+template <int BASE, bool SUB_NF4, bool OUT_BF16>
+__global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p) {
+  extern __shared__ float s_mg[];
+  float* s_a = s_mg;                        // [r][256]
+  float* s_bt = s_a + p.r * kMgCols;        // [r][32]
+  float* s_lv = s_bt + p.r * kMgRows;       // [16]
+  const int n0 = blockIdx.y * kMgRows, k0 = blockIdx.x * kMgCols;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kcols = min(kMgCols, p.k - k0);  // a multiple of 64
+  // stage A[:, k0 .. k0 + kcols) and B[n0 .. n0 + 32, :]^T as float32
+  for (int i = threadIdx.x; i < p.r * (kMgCols / 8); i += kMgThreads) {
+    const int j = i / (kMgCols / 8), c8 = (i % (kMgCols / 8)) * 8;
+    float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
+    if (c8 < kcols) {
+      const uint4 v = ldg_nc_v4(p.lora_a + static_cast<int64_t>(j) * p.k + k0 + c8);
+      lo = make_float4(bf16_bits_to_f32(v.x & 0xffffu), bf16_bits_to_f32(v.x >> 16), bf16_bits_to_f32(v.y & 0xffffu),
+                       bf16_bits_to_f32(v.y >> 16));
+      hi = make_float4(bf16_bits_to_f32(v.z & 0xffffu), bf16_bits_to_f32(v.z >> 16), bf16_bits_to_f32(v.w & 0xffffu),
+                       bf16_bits_to_f32(v.w >> 16));
+    }
+    *reinterpret_cast<float4*>(s_a + j * kMgCols + c8) = lo;
+    *reinterpret_cast<float4*>(s_a + j * kMgCols + c8 + 4) = hi;
+  }
+  const unsigned short* b16 = reinterpret_cast<const unsigned short*>(p.lora_b);
+  for (int i = threadIdx.x; i < p.r * kMgRows; i += kMgThreads) {
+    const int row = i % kMgRows, j = i / kMgRows;  // consecutive threads write consecutive banks
+    const int n = n0 + row;
+    s_bt[j * kMgRows + row] = n < p.n ? bf16_bits_to_f32(b16[static_cast<int64_t>(n) * p.r + j]) : 0.f;
+  }
+  if (threadIdx.x < 16) {
+    constexpr uint32_t hex[16] = QLORA_NF4_LEVELS_HEX;
+    s_lv[threadIdx.x] = __uint_as_float(hex[threadIdx.x]);
+  }
+  __syncthreads();
+
+  const int kc = k0 + lane * 8;
+  if (lane * 8 >= kcols) return;
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+  const float* a_col = s_a + lane * 8;
+  const float* b_row = s_bt + warp * 4;
+  for (int j = 0; j < p.r; ++j) {
+    const float4 a0 = *reinterpret_cast<const float4*>(a_col + j * kMgCols);
+    const float4 a1 = *reinterpret_cast<const float4*>(a_col + j * kMgCols + 4);
+    const float4 bb = *reinterpret_cast<const float4*>(b_row + j * kMgRows);
+    const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+    const float2 ap[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
+                          make_float2(a1.z, a1.w)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 b2 = make_float2(bv[i], bv[i]);
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        float2 c = make_float2(acc[i][2 * h], acc[i][2 * h + 1]);
+        c = __ffma2_rn(b2, ap[h], c);
+        acc[i][2 * h] = c.x;
+        acc[i][2 * h + 1] = c.y;
+      }
+    }
+  }
+
+  const float mu = (BASE == MG_NF4 || SUB_NF4) ? *p.mean : 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = n0 + warp * 4 + i;
+    if (n >= p.n) break;
+    float base[8];
+    if (BASE == MG_NF4) {
+      deq8(p, s_lv, mu, n, kc, base);
+    } else {
+      const int64_t o = static_cast<int64_t>(n) * p.k + kc;
+      if (BASE == MG_F32) {
+        const float4 v0 = *reinterpret_cast<const float4*>(static_cast<const float*>(p.dense) + o);
+        const float4 v1 = *reinterpret_cast<const float4*>(static_cast<const float*>(p.dense) + o + 4);
+        base[0] = v0.x; base[1] = v0.y; base[2] = v0.z; base[3] = v0.w;
+        base[4] = v1.x; base[5] = v1.y; base[6] = v1.z; base[7] = v1.w;
+      } else {
+        const uint4 v = ldg_nc_v4(static_cast<const __nv_bfloat16*>(p.dense) + o);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          base[2 * h] = bf16_bits_to_f32(wv[h] & 0xffffu);
+          base[2 * h + 1] = bf16_bits_to_f32(wv[h] >> 16);
+        }
+      }
+      if (SUB_NF4) {
+        float q[8];
+        deq8(p, s_lv, mu, n, kc, q);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) base[e] = __fsub_rn(base[e], q[e]);
+      }
+    }
+    float o8[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o8[e] = p.r > 0 ? __fadd_rn(base[e], __fmul_rn(p.coef, acc[i][e])) : base[e];
+    const int64_t o = static_cast<int64_t>(n) * p.k + kc;
+    if (OUT_BF16) {
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o) =
+          make_uint4(pack_bf16x2_rn(o8[0], o8[1]), pack_bf16x2_rn(o8[2], o8[3]), pack_bf16x2_rn(o8[4], o8[5]),
+                     pack_bf16x2_rn(o8[6], o8[7]));
+    } else {
+      float* dst = static_cast<float*>(p.out) + o;
+      *reinterpret_cast<float4*>(dst) = make_float4(o8[0], o8[1], o8[2], o8[3]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(o8[4], o8[5], o8[6], o8[7]);
+    }
+  }
+}
+
+template <int BASE, bool SUB_NF4, bool OUT_BF16>
+static cudaError_t run_combine(const MgParams& p, cudaStream_t s) {
+  const size_t smem = (static_cast<size_t>(p.r) * (kMgCols + kMgRows) + 16) * sizeof(float);
+  cudaError_t e = set_smem_limit_once(k_lowrank_combine<BASE, SUB_NF4, OUT_BF16>, (128 * (kMgCols + kMgRows) + 16) * 4);
+  if (e != cudaSuccess) return e;
+  const dim3 grid((p.k + kMgCols - 1) / kMgCols, (p.n + kMgRows - 1) / kMgRows);
+  k_lowrank_combine<BASE, SUB_NF4, OUT_BF16><<<grid, kMgThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_nf4_merge(const Nf4Dev& w, const __nv_bfloat16* lora_a, const __nv_bfloat16* lora_b, int r,
+                             float scale, __nv_bfloat16* out, cudaStream_t s) {
+  MgParams p = {};
+  p.codes = w.codes;
+  p.absq = w.absq;
+  p.step = w.step;
+  p.mean = w.mean;
+  p.lora_a = lora_a;
+  p.lora_b = lora_b;
+  p.out = out;
+  p.n = static_cast<int>(w.n);
+  p.k = static_cast<int>(w.k);
+  p.r = r;
+  p.coef = scale;
+  return run_combine<MG_NF4, false, true>(p, s);
+}
+
+cudaError_t launch_lowrank_update(const void* dense, int dense_bf16, const Nf4Dev* sub, const __nv_bfloat16* lora_a,
+                                  const __nv_bfloat16* lora_b, int r, float coef, float* out, int64_t n, int64_t k,
+                                  cudaStream_t s) {
+  MgParams p = {};
+  if (sub) {
+    p.codes = sub->codes;
+    p.absq = sub->absq;
+    p.step = sub->step;
+    p.mean = sub->mean;
+  }
+  p.dense = dense;
+  p.lora_a = lora_a;
+  p.lora_b = lora_b;
+  p.out = out;
+  p.n = static_cast<int>(n);
+  p.k = static_cast<int>(k);
+  p.r = r;
+  p.coef = coef;
+  if (dense_bf16) return sub ? run_combine<MG_BF16, true, false>(p, s) : run_combine<MG_BF16, false, false>(p, s);
+  return sub ? run_combine<MG_F32, true, false>(p, s) : run_combine<MG_F32, false, false>(p, s);
+}
+
+}  // namespace qlora

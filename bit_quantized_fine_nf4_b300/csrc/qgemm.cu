@@ -185,13 +185,7 @@ __global__ void __launch_bounds__(kWaThreads, 1)
           for (int c = 0; c < 32; ++c) words[c] = 0;
         }
       } else {
-        const int jb = (i - n_main) * 64;
-        const uint32_t* brow = reinterpret_cast<const uint32_t*>(p.lora_b + static_cast<int64_t>(row) * p.r);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int j = jb + 2 * c;
-          words[c] = (row_ok && j < p.r) ? brow[j >> 1] : 0u;
-        }
+        load_lora_b_row(p.lora_b, row, p.N, p.r, (i - n_main) * 64, words);
       }
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&empty[s], ph ^ 1, p.wait_ns, vabort));
       if (!ok) { if (lane == 0) abort_cta(p.status, abort_flag); alive = false; break; }
@@ -629,17 +623,26 @@ __global__ void __launch_bounds__(kLgThreads, 1)
               *d = p.accum_da ? (*d + val) : val;
             }
           } else {
-            float* d = p.db + static_cast<int64_t>(c) * p.r + j0;  // 16 consecutive floats (r % 8 == 0)
+            float* d = p.db + static_cast<int64_t>(c) * p.r + j0;
+            if ((p.r & 3) == 0) {  // rows of dB start on 16-byte boundaries: 4 floats at a time
 #pragma unroll
-            for (int jj = 0; jj < 16; jj += 4) {
-              if (j0 + jj >= p.r) break;
-              float4 val = make_float4(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1]),
-                                       __uint_as_float(v[jj + 2]), __uint_as_float(v[jj + 3]));
-              if (p.accum_db) {
-                const float4 o = *reinterpret_cast<const float4*>(d + jj);
-                val.x += o.x; val.y += o.y; val.z += o.z; val.w += o.w;
+              for (int jj = 0; jj < 16; jj += 4) {
+                if (j0 + jj >= p.r) break;
+                float4 val = make_float4(__uint_as_float(v[jj]), __uint_as_float(v[jj + 1]),
+                                         __uint_as_float(v[jj + 2]), __uint_as_float(v[jj + 3]));
+                if (p.accum_db) {
+                  const float4 o = *reinterpret_cast<const float4*>(d + jj);
+                  val.x += o.x; val.y += o.y; val.z += o.z; val.w += o.w;
+                }
+                *reinterpret_cast<float4*>(d + jj) = val;
               }
-              *reinterpret_cast<float4*>(d + jj) = val;
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 16; ++jj) {
+                if (j0 + jj >= p.r) break;
+                const float val = __uint_as_float(v[jj]);
+                d[jj] = p.accum_db ? d[jj] + val : val;
+              }
             }
           }
         }
@@ -784,7 +787,8 @@ cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, cons
   const FwdPlan pl = plan_fwd(M, N, K, num_sms);
   CUtensorMap tx, tst;
   if (!make_tensor_map_bf16_2d(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, pl.ntok)) return cudaErrorInvalidValue;
-  if (!make_tensor_map_bf16_2d(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, pl.ntok)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tst, st, lora_ld(r), M, static_cast<uint64_t>(lora_ld(r)) * 2, 64, pl.ntok))
+    return cudaErrorInvalidValue;
   WaParams prm;
   prm.codes = w.codes;
   prm.absq = w.absq;
@@ -823,7 +827,8 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
   const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
   CUtensorMap tdy, tsu, tla;
   if (!make_tensor_map_bf16_2d(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 256)) return cudaErrorInvalidValue;
-  if (!make_tensor_map_bf16_2d(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 256)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tsu, su, lora_ld(r), M, static_cast<uint64_t>(lora_ld(r)) * 2, 64, 256))
+    return cudaErrorInvalidValue;
   if (!make_tensor_map_bf16_2d(&tla, lora_a, K, r, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
   WbParams prm;
   prm.codes = w.codes;
@@ -862,8 +867,9 @@ cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, c
   CUtensorMap tx, tdy, tsu, tst;
   if (!make_tensor_map_bf16_2d(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
   if (!make_tensor_map_bf16_2d(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 64)) return cudaErrorInvalidValue;
-  if (!make_tensor_map_bf16_2d(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
-  if (!make_tensor_map_bf16_2d(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
+  const uint64_t rk = static_cast<uint64_t>(lora_ld(r));
+  if (!make_tensor_map_bf16_2d(&tsu, su, rk, M, rk * 2, 64, 64)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tst, st, rk, M, rk * 2, 64, 64)) return cudaErrorInvalidValue;
   LgParams prm;
   prm.da = da;
   prm.db = db;

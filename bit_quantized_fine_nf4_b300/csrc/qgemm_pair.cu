@@ -254,13 +254,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
         }
       } else if (!BWD) {
         // LoRA B: K-major row n_fix, 64 j
-        const int jb = (i - n_main) * 64;
-        const uint32_t* brow = reinterpret_cast<const uint32_t*>(p.lora_b + static_cast<int64_t>(n_fix) * p.r);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int j = jb + 2 * c;
-          words[c] = (n_fix < p.N && j < p.r) ? brow[j >> 1] : 0u;
-        }
+        load_lora_b_row(p.lora_b, n_fix, p.N, p.r, (i - n_main) * 64, words);
       } else {
         // LoRA A: MN-major row j = jb + rrow, 64 output columns from col0
         const int j = (i - n_main) * 64 + static_cast<int>(rrow);
@@ -416,8 +410,9 @@ cudaError_t launch_fwd_gemm_pair(const __nv_bfloat16* x, int M, const Nf4Dev& w,
                                  uint64_t wait_ns, cudaStream_t s) {
   const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
   CUtensorMap tx, tst;
+  const int rk = lora_ld(r);
   if (!make_tensor_map_bf16_2d(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, 128)) return cudaErrorInvalidValue;
-  if (!make_tensor_map_bf16_2d(&tst, st, r, M, static_cast<uint64_t>(r) * 2, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tst, st, rk, M, static_cast<uint64_t>(rk) * 2, 64, 128)) return cudaErrorInvalidValue;
   PairParams prm = pair_params(w, lora_b, nullptr, y, status, M, r, 0, wait_ns);
   prm.out_cols = N;
   CUtensorMap ty = tst;
@@ -431,8 +426,9 @@ cudaError_t launch_bwd_gemm_pair(const __nv_bfloat16* dy, int M, const Nf4Dev& w
                                  unsigned* status, uint64_t wait_ns, cudaStream_t s) {
   const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
   CUtensorMap tdy, tsu;
+  const int rk = lora_ld(r);
   if (!make_tensor_map_bf16_2d(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 128)) return cudaErrorInvalidValue;
-  if (!make_tensor_map_bf16_2d(&tsu, su, r, M, static_cast<uint64_t>(r) * 2, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tsu, su, rk, M, static_cast<uint64_t>(rk) * 2, 64, 128)) return cudaErrorInvalidValue;
   PairParams prm = pair_params(w, nullptr, lora_a, dx, status, M, r, accumulate, wait_ns);
   prm.out_cols = K;
   CUtensorMap tdx = tsu;

@@ -29,9 +29,14 @@
  *     Errors found on the device (a bounded wait that expired, a non-finite
  *     weight) are latched in a per-device status word and returned by
  *     qlora_get_status.
- *   - Shapes: W is [n, k] (out x in, as a PyTorch Linear); k % 64 == 0,
- *     n % 8 == 0; tokens m >= 0 (m == 0 is a no-op); LoRA rank r with
- *     r % 8 == 0 and 8 <= r <= 128; all of m, n, k < 2^31.
+ *   - Shapes: W is [n, k] (out x in, as a PyTorch Linear); k % 64 == 0
+ *     (a block of 64 never crosses a row); tokens m >= 0 (m == 0 is a no-op);
+ *     LoRA rank 1 <= r <= 128 (Day 25 notes, section 6.2: r is a free
+ *     hyper-parameter, 4 to 64 typical); all of m, n, k < 2^31.
+ *     n % 8 == 0 as well: the activations Y and dY have n columns and are read
+ *     and written by the Tensor Memory Accelerator, whose row pitch must be a
+ *     multiple of 16 bytes (n bf16 values).  Every Llama projection satisfies
+ *     both (n, k in {4096, 8192, 11008, 22016}).
  */
 #ifndef QLORA_NF4_H_
 #define QLORA_NF4_H_
@@ -137,6 +142,40 @@ int qlora_nf4_quantize_noalloc(const void* w, int w_dtype, int64_t n, int64_t k,
  * Bit-exact against the definition in the record comment above.
  */
 int qlora_nf4_dequantize(const qlora_nf4_weight* w, uint16_t* out, void* stream);
+
+/* ----------------------------------------------------------------- merge / export */
+
+/*
+ * Merge the trained LoRA branch into the dequantised base:
+ *   out bf16 [n, k] = bf16_rn( deq(W) + s * (B A) ),   s = alpha / r
+ * (Day 25 notes "Fine-tuning and LoRA/QLoRA", section 2.6: W_merged = W0 + B A;
+ * P1 tutorial "QLoRA: fine-tuning 7B on a 24 GB card", section 3.8, and glossary
+ * "QLoRA", "Trade-offs": a 4-bit base is dequantised to 16 bits before the
+ * merge, and re-quantised for serving -- pass `out` to qlora_nf4_quantize).
+ *   lora_a bf16 [r, k], lora_b bf16 [n, r], 1 <= r <= 128.
+ * Arithmetic (bit-exact against this definition): deq(W) as qlora_nf4_dequantize
+ * gives it; (B A)[n, k] accumulated in float32 over j = 0 .. r-1 in that order,
+ * one fused multiply-add per term (the bf16 products are exact); s * (B A)
+ * rounded to float32, added to deq(W) in float32, rounded to bf16.
+ */
+int qlora_nf4_merge(const qlora_nf4_weight* w, const uint16_t* lora_a, const uint16_t* lora_b, int r, float alpha,
+                    uint16_t* out, void* stream);
+
+/*
+ * Dense low-rank update in float32, the arithmetic step of the LoftQ
+ * initialisation (P1 tutorial, section 3.10: alternate quantising the weight
+ * minus the LoRA branch and fitting the branch to what quantisation lost):
+ *   out f32 [n, k] = (W - deq(sub)) + coef * (B A)
+ *   w      float32 or bfloat16 [n, k] (w_dtype), k % 64 == 0
+ *   sub    NF4 record [n, k] subtracted from W, or NULL (nothing subtracted)
+ *   lora_a bf16 [r, k], lora_b bf16 [n, r], 0 <= r <= 128 (r == 0: no B A
+ *          term; the pointers may then be NULL)
+ * Each float32 operation rounds once; B A is the same float32 FMA chain as in
+ * qlora_nf4_merge.  With coef = -alpha / r it gives the weight LoftQ quantises;
+ * with sub set and r == 0, the residual it factorises.
+ */
+int qlora_lowrank_update(const void* w, int w_dtype, int64_t n, int64_t k, const qlora_nf4_weight* sub,
+                         const uint16_t* lora_a, const uint16_t* lora_b, int r, float coef, float* out, void* stream);
 
 /* ----------------------------------------------------------------- the QLoRA linear */
 

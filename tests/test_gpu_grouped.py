@@ -12,7 +12,7 @@ import torch
 
 import synthetic
 from oracle import linear, nf4
-from tests._helpers import GEMM_TOL, rel_fro, to_np32, to_np64
+from tests._helpers import GEMM_TOL, t_save_tol, rel_fro, to_np32, to_np64
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +46,7 @@ def test_grouped_matches_oracle_and_single_calls(lib):
         wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
         yr, tr = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
         assert rel_fro(to_np64(ys[i]), yr) < GEMM_TOL, SHAPES[i]
-        assert rel_fro(to_np64(probs[i][6]), tr) < 1e-5, SHAPES[i]
+        assert rel_fro(to_np64(probs[i][6]), tr) < t_save_tol(c.k), SHAPES[i]
         y1, _ = lib.linear_fwd(c.x, rec, c.a, c.b, c.alpha)
         assert rel_fro(to_np64(ys[i]), to_np64(y1)) < 1e-2, SHAPES[i]
 
@@ -110,7 +110,7 @@ def test_grouped_split_k_matches_oracle_and_is_deterministic(lib, which):
         wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
         yr, tr = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
         assert rel_fro(to_np64(ys[i]), yr) < GEMM_TOL, shapes[i]
-        assert rel_fro(to_np64(ts[i]), tr) < 1e-5, shapes[i]
+        assert rel_fro(to_np64(ts[i]), tr) < t_save_tol(c.k), shapes[i]
 
 
 def test_grouped_long_list_one_and_two_tokens(lib):
