@@ -30,6 +30,8 @@ ACCUM_DX = 1
 ACCUM_DA = 2
 ACCUM_DB = 4
 
+ADAMW_PREFETCH = 1
+
 # every symbol include/qlora_nf4.h declares
 EXPORTS = (
     "qlora_nf4_quantize_workspace_bytes",
@@ -44,6 +46,7 @@ EXPORTS = (
     "qlora_linear_bwd",
     "qlora_linear_fwd_grouped_workspace_bytes",
     "qlora_linear_fwd_grouped",
+    "qlora_adamw_step",
     "qlora_silu_mul_fwd",
     "qlora_silu_mul_bwd",
     "qlora_get_status",
@@ -93,6 +96,17 @@ class _Problem(ctypes.Structure):
     ]
 
 
+class _AdamwTensor(ctypes.Structure):
+    _fields_ = [
+        ("master", ctypes.c_void_p),
+        ("param", ctypes.c_void_p),
+        ("grad", ctypes.c_void_p),
+        ("exp_avg", ctypes.c_void_p),
+        ("exp_avg_sq", ctypes.c_void_p),
+        ("numel", ctypes.c_int64),
+    ]
+
+
 _lib = None
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -127,6 +141,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                      _P]),
         "qlora_linear_fwd_grouped_workspace_bytes": (c_int, [_PP, c_int, _PSZ]),
         "qlora_linear_fwd_grouped": (c_int, [_PP, c_int, _P, _SZ, _P]),
+        "qlora_adamw_step": (c_int, [ctypes.POINTER(_AdamwTensor), c_int, c_float, c_float, c_float, c_float,
+                                     c_float, _I64, c_int, _P]),
         "qlora_silu_mul_fwd": (c_int, [_P, _P, _P, _I64, _P]),
         "qlora_silu_mul_bwd": (c_int, [_P, _P, _P, _P, _P, _I64, _P]),
         "qlora_get_status": (c_int, [_P]),
@@ -373,6 +389,81 @@ class GroupedForward:
 def linear_fwd_grouped(problems, workspace=None, stream=None):
     """One qlora_linear_fwd_grouped call; returns the list of y tensors."""
     return GroupedForward(problems, workspace).run(stream)
+
+
+def _addr(x) -> int | None:
+    """Device address of a tensor, or an integer address as given (e.g. managed memory)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "ptr"):
+        return int(x.ptr)
+    return _ptr(x)
+
+
+def adamw_step(tensors, lr: float, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+               weight_decay: float = 0.0, step: int = 1, prefetch: bool = False, stream=None) -> None:
+    """One AdamW step (qlora_adamw_step) on a list of dicts with keys ``master``, ``param``
+    (bf16 copy or None), ``grad``, ``exp_avg``, ``exp_avg_sq`` and, when the entries are raw
+    addresses or ManagedBuffer objects, ``numel``.  All tensors of the list go in one launch."""
+    arr = (_AdamwTensor * max(len(tensors), 1))()
+    for i, t in enumerate(tensors):
+        numel = t.get("numel")
+        if numel is None:
+            numel = t["grad"].numel()
+        arr[i] = _AdamwTensor(_addr(t["master"]), _addr(t.get("param")), _addr(t["grad"]), _addr(t["exp_avg"]),
+                              _addr(t["exp_avg_sq"]), int(numel))
+    _check(load().qlora_adamw_step(arr, len(tensors), float(lr), float(beta1), float(beta2), float(eps),
+                                   float(weight_decay), int(step), ADAMW_PREFETCH if prefetch else 0,
+                                   _stream(stream)))
+
+
+class ManagedBuffer:
+    """Memory from cudaMallocManaged: one address valid on the GPU and the host, paged
+    between them by the driver (where the paged optimizer keeps its state).  Allocated by
+    the caller through the CUDA runtime, never by the library."""
+
+    _rt = None
+
+    @classmethod
+    def _runtime(cls):
+        if cls._rt is None:
+            here = os.path.dirname(torch.__file__)
+            cands = [os.path.join(here, "..", "nvidia", "cu13", "lib", "libcudart.so.13"), "libcudart.so.13",
+                     "/usr/local/cuda/lib64/libcudart.so"]
+            err = None
+            for c in cands:
+                try:
+                    cls._rt = ctypes.CDLL(c)
+                    break
+                except OSError as e:
+                    err = e
+            if cls._rt is None:
+                raise RuntimeError("CUDA runtime library not found: %s" % err)
+            cls._rt.cudaMallocManaged.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_size_t, ctypes.c_uint]
+            cls._rt.cudaFree.argtypes = [ctypes.c_void_p]
+            cls._rt.cudaDeviceSynchronize.argtypes = []
+        return cls._rt
+
+    def __init__(self, nbytes: int):
+        rt = self._runtime()
+        p = ctypes.c_void_p()
+        rc = rt.cudaMallocManaged(ctypes.byref(p), ctypes.c_size_t(max(int(nbytes), 16)), 1)  # cudaMemAttachGlobal
+        if rc != 0:
+            raise RuntimeError("cudaMallocManaged failed (%d)" % rc)
+        self.ptr = p.value
+        self.nbytes = int(nbytes)
+
+    def host_view(self, ctype, count: int):
+        """A numpy view of the buffer on the host (synchronise the device before reading)."""
+        import numpy as np
+        return np.ctypeslib.as_array((ctype * count).from_address(self.ptr))
+
+    def free(self) -> None:
+        if self.ptr:
+            self._runtime().cudaFree(ctypes.c_void_p(self.ptr))
+            self.ptr = 0
 
 
 def silu_mul_fwd(g: torch.Tensor, u: torch.Tensor, h: torch.Tensor | None = None, stream=None) -> torch.Tensor:

@@ -149,12 +149,12 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 // and, while profiling is on, bracketed by two CUDA events on its stream.
 enum ProfName : int {
   P_QUANTIZE = 0, P_DEQUANTIZE, P_LORA_DOWN, P_FWD_GEMM, P_BWD_GEMM, P_LORA_GRADS, P_SILU_FWD, P_SILU_BWD,
-  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_MERGE, P_LOWRANK, P_COUNT
+  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_MERGE, P_LOWRANK, P_ADAMW, P_COUNT
 };
 const char* const kProfNames[P_COUNT] = {"nf4_quantize(3 kernels)", "nf4_dequantize", "lora_down", "fwd_gemm",
                                          "bwd_dx_gemm", "lora_grads", "silu_mul_fwd", "silu_mul_bwd",
                                          "wait_selftest", "fwd_grouped(2 kernels)", "lora_side_fwd", "nf4_merge",
-                                         "lowrank_update"};
+                                         "lowrank_update", "adamw"};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<bool> g_prof_on{false};
 struct ProfRec {
@@ -320,6 +320,60 @@ int qlora_lowrank_update(const void* w, int w_dtype, int64_t n, int64_t k, const
                                                reinterpret_cast<const __nv_bfloat16*>(lora_b), r, coef, out, n, k,
                                                static_cast<cudaStream_t>(stream)),
                   "lowrank update");
+}
+
+// Managed (paged) memory of [p, p + bytes) is migrated to `device` ahead of the kernel; other memory is left alone.
+static cudaError_t prefetch_if_managed(const void* p, size_t bytes, int device, cudaStream_t s) {
+  if (!p || bytes == 0) return cudaSuccess;
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // an unregistered host pointer: nothing to prefetch
+    return cudaSuccess;
+  }
+  if (a.type != cudaMemoryTypeManaged) return cudaSuccess;
+  cudaMemLocation loc = {};
+  loc.type = cudaMemLocationTypeDevice;
+  loc.id = device;
+  return cudaMemPrefetchAsync(p, bytes, loc, 0, s);
+}
+
+int qlora_adamw_step(const qlora_adamw_tensor* tensors, int count, float lr, float beta1, float beta2, float eps,
+                     float weight_decay, int64_t step, int flags, void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if (count < 0 || (count > 0 && !tensors)) return fail(QLORA_ERR_INVALID_ARGUMENT, "tensors");
+  if (step < 1) return fail(QLORA_ERR_INVALID_ARGUMENT, "step = %lld (the first step is 1)", (long long)step);
+  if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f) || !(eps > 0.f))
+    return fail(QLORA_ERR_INVALID_ARGUMENT, "beta1 / beta2 must be in [0, 1), eps > 0");
+  if (flags & ~QLORA_ADAMW_PREFETCH) return fail(QLORA_ERR_INVALID_ARGUMENT, "flags 0x%x", flags);
+  if (count == 0) return QLORA_OK;
+  std::vector<qlora::AdamwTensor> ts(static_cast<size_t>(count));
+  for (int i = 0; i < count; ++i) {
+    const qlora_adamw_tensor& t = tensors[i];
+    if (t.numel < 0) return fail(QLORA_ERR_INVALID_ARGUMENT, "tensor %d: numel %lld", i, (long long)t.numel);
+    if (t.numel > 0 && (!t.master || !t.grad || !t.exp_avg || !t.exp_avg_sq))
+      return fail(QLORA_ERR_INVALID_ARGUMENT, "tensor %d: NULL pointer", i);
+    ts[static_cast<size_t>(i)] = qlora::AdamwTensor{t.master, reinterpret_cast<__nv_bfloat16*>(t.param), t.grad,
+                                                    t.exp_avg, t.exp_avg_sq, t.numel};
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (flags & QLORA_ADAMW_PREFETCH) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    for (const auto& t : ts) {
+      const size_t b4 = static_cast<size_t>(t.numel) * 4;
+      cudaError_t e = prefetch_if_managed(t.master, b4, dev, s);
+      if (e == cudaSuccess) e = prefetch_if_managed(t.exp_avg, b4, dev, s);
+      if (e == cudaSuccess) e = prefetch_if_managed(t.exp_avg_sq, b4, dev, s);
+      if (e == cudaSuccess) e = prefetch_if_managed(t.grad, b4, dev, s);
+      if (e != cudaSuccess) return cuda_ret(e, "prefetch of paged optimizer state");
+    }
+  }
+  const qlora::AdamwHyper h = qlora::adamw_hyper(lr, beta1, beta2, eps, weight_decay, step);
+  Span sp(P_ADAMW, s, (count + 239) / 240);
+  return cuda_ret(qlora::launch_adamw(ts.data(), count, h, di->num_sms, s), "adamw");
 }
 
 int qlora_linear_fwd_workspace_bytes(int64_t m, int64_t n, int64_t k, int r, size_t* bytes) {

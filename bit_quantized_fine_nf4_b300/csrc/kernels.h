@@ -89,6 +89,21 @@ cudaError_t launch_nf4_merge(const Nf4Dev& w, const __nv_bfloat16* lora_a, const
 cudaError_t launch_lowrank_update(const void* dense, int dense_bf16, const Nf4Dev* sub, const __nv_bfloat16* lora_a,
                                   const __nv_bfloat16* lora_b, int r, float coef, float* out, int64_t n, int64_t k,
                                   cudaStream_t s);
+// AdamW on a list of tensors in one launch (adamw.cu).
+struct AdamwTensor {
+  float* master;          // float32 weights (updated)
+  __nv_bfloat16* param;   // bf16 copy the kernels read (written; may be null)
+  const float* grad;
+  float* exp_avg;
+  float* exp_avg_sq;
+  int64_t numel;
+};
+struct AdamwHyper {
+  float decay, beta1, omb1, beta2, omb2, step_size, bc2_sqrt, eps;
+};
+// The float32 factors of step `step` (1-based), formed in double precision.
+AdamwHyper adamw_hyper(double lr, double beta1, double beta2, double eps, double weight_decay, int64_t step);
+cudaError_t launch_adamw(const AdamwTensor* tensors, int count, const AdamwHyper& h, int num_sms, cudaStream_t s);
 // 2-D bf16 tensor map, 128-byte swizzle, zero fill outside [outer x inner] (qgemm.cu).
 bool make_tensor_map_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
                              uint32_t box_inner, uint32_t box_outer);

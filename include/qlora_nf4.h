@@ -255,6 +255,43 @@ int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problem
 int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/* ----------------------------------------------------------------- optimizer */
+
+#define QLORA_ADAMW_PREFETCH 1 /* qlora_adamw_step: migrate managed state to the device before the update */
+
+/* One trained tensor (a LoRA A or B) for qlora_adamw_step; device-accessible pointers. */
+typedef struct qlora_adamw_tensor {
+  float* master;        /* f32 [numel] weights, updated in place */
+  uint16_t* param;      /* bf16 [numel] copy the linear reads (A or B), written; may be NULL */
+  const float* grad;    /* f32 [numel] gradient (dA or dB of qlora_linear_bwd) */
+  float* exp_avg;       /* f32 [numel] first moment, updated */
+  float* exp_avg_sq;    /* f32 [numel] second moment, updated */
+  int64_t numel;
+} qlora_adamw_tensor;
+
+/*
+ * One AdamW step (decoupled weight decay; Loshchilov and Hutter 2019) on a list
+ * of tensors, in one kernel launch per 240 tensors.  The pages train only the
+ * LoRA matrices with a paged AdamW (P1 tutorial section 3.3, optim =
+ * "paged_adamw_8bit"; tbr8.org section 5, "paged_adamw_32bit"; glossary
+ * "QLoRA", "How QLoRA works": optimizer state in NVIDIA unified memory, paged
+ * to CPU RAM during memory spikes).  This is the 32-bit variant: master
+ * weights, exp_avg and exp_avg_sq in float32; they may live in memory from
+ * cudaMallocManaged, which the driver pages between GPU and host on demand
+ * (QLORA_ADAMW_PREFETCH migrates each managed range to the device on `stream`
+ * before the update instead of faulting it in page by page).  The library
+ * allocates nothing.  Per element, every float32 operation rounded once, in
+ * this order (bit-exact against the definition):
+ *   p = master * (1 - lr wd);  m = b1 m + (1 - b1) g;  v = b2 v + (1 - b2)(g g);
+ *   p = p - (lr / (1 - b1^t)) * (m / (sqrt(v) / sqrt(1 - b2^t) + eps));
+ *   master = p;  param = bf16_rn(p)
+ * with 1 - lr wd, 1 - b1, 1 - b2, lr / (1 - b1^t) and sqrt(1 - b2^t) formed
+ * in double precision and rounded to float32.  step t >= 1 (1 for the first
+ * update); 0 <= b1, b2 < 1; eps > 0.  Tensors must not overlap.
+ */
+int qlora_adamw_step(const qlora_adamw_tensor* tensors, int count, float lr, float beta1, float beta2, float eps,
+                     float weight_decay, int64_t step, int flags, void* stream);
+
 /* ----------------------------------------------------------------- MLP glue */
 
 /*

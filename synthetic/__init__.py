@@ -99,6 +99,20 @@ def linear_case(n: int, k: int, m: int, r: int, alpha: float, device="cpu", base
     return LinearCase(w, x, a, b, dy, float(alpha), r)
 
 
+def structured_weight(n: int, k: int, rank: int = 8, device="cpu", seed: int = 0, dtype=torch.float32):
+    """N(0, 0.02^2) plus a rank-``rank`` part of about the same Frobenius norm, with
+    geometrically decaying strengths (a weight whose spectrum has a few large
+    directions on top of a noise floor, as pretrained projections do): the
+    workload of the LoftQ initialisation."""
+    g = _gen(device, seed)
+    noise = torch.randn((n, k), generator=g, device=device, dtype=torch.float32) * W_STD
+    u = torch.randn((n, rank), generator=g, device=device, dtype=torch.float32) / math.sqrt(n)
+    v = torch.randn((rank, k), generator=g, device=device, dtype=torch.float32) / math.sqrt(k)
+    strength = W_STD * math.sqrt(n * k) * torch.tensor([0.7 ** i for i in range(rank)], device=device)
+    strength = strength / float(torch.sqrt((strength ** 2).sum() / (W_STD ** 2 * n * k)))
+    return (noise + (u * strength[None, :]) @ v).to(dtype)
+
+
 def weight(n: int, k: int, device="cpu", seed: int = 0, dtype=torch.bfloat16) -> torch.Tensor:
     """A single N(0, 0.02^2) weight [n, k]."""
     return _normal((n, k), W_STD, _gen(device, seed), device, dtype)
