@@ -44,6 +44,9 @@ EXPORTS = (
     "qlora_linear_fwd",
     "qlora_linear_bwd_workspace_bytes",
     "qlora_linear_bwd",
+    "qlora_dropout_mask",
+    "qlora_linear_fwd_dropout",
+    "qlora_linear_bwd_dropout",
     "qlora_linear_fwd_grouped_workspace_bytes",
     "qlora_linear_fwd_grouped",
     "qlora_adamw_step",
@@ -139,6 +142,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "qlora_linear_bwd_workspace_bytes": (c_int, [_I64, _I64, _I64, c_int, _PSZ]),
         "qlora_linear_bwd": (c_int, [_P, _P, _I64, _PW, _P, _P, c_int, c_float, _P, _P, _P, _P, c_int, _P, _SZ,
                                      _P]),
+        "qlora_dropout_mask": (c_int, [ctypes.c_uint64, ctypes.c_uint64, _I64, _I64, c_float, _P, _P]),
+        "qlora_linear_fwd_dropout": (c_int, [_P, _I64, _PW, _P, _P, c_int, c_float, _P, c_float, _P, _P, _P, _P, _SZ,
+                                             _P]),
+        "qlora_linear_bwd_dropout": (c_int, [_P, _P, _I64, _PW, _P, _P, c_int, c_float, _P, c_float, _P, _P, _P, _P,
+                                             c_int, _P, _SZ, _P]),
         "qlora_linear_fwd_grouped_workspace_bytes": (c_int, [_PP, c_int, _PSZ]),
         "qlora_linear_fwd_grouped": (c_int, [_PP, c_int, _P, _SZ, _P]),
         "qlora_adamw_step": (c_int, [ctypes.POINTER(_AdamwTensor), c_int, c_float, c_float, c_float, c_float,
@@ -351,6 +359,59 @@ def linear_bwd(dy: torch.Tensor, x: torch.Tensor, rec: NF4Weight, lora_a: torch.
     _check(lib.qlora_linear_bwd(_ptr(dy), _ptr(x), m, ctypes.byref(c), _ptr(lora_a), _ptr(lora_b), r, float(alpha),
                                 _ptr(t_save), _ptr(dx), _ptr(da), _ptr(db), int(flags), _ptr(ws), wsb,
                                 _stream(stream)))
+    return dx, da, db
+
+
+def dropout_mask(seed: int, offset: int, m: int, k: int, p: float, out: torch.Tensor | None = None,
+                 device="cuda", stream=None) -> torch.Tensor:
+    """uint8 [m, k/8] keep bits of LoRA dropout (qlora_dropout_mask)."""
+    if out is None:
+        out = torch.empty((m, k // 8), dtype=torch.uint8, device=device)
+    _check(load().qlora_dropout_mask(int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1), m, k, float(p),
+                                     _ptr(out) if m else None, _stream(stream)))
+    return out
+
+
+def linear_fwd_dropout(x: torch.Tensor, rec: NF4Weight, lora_a: torch.Tensor, lora_b: torch.Tensor, alpha: float,
+                       mask: torch.Tensor, p: float, y=None, t_save=None, x_drop=None, workspace=None, stream=None):
+    """Forward with dropout on the LoRA input.  Returns (y, t_save, x_drop)."""
+    lib = load()
+    m = x.shape[0]
+    r = lora_a.shape[0]
+    dev = x.device
+    if y is None:
+        y = torch.empty((m, rec.n), dtype=torch.bfloat16, device=dev)
+    if t_save is None:
+        t_save = torch.empty((m, r), dtype=torch.float32, device=dev)
+    if x_drop is None:
+        x_drop = torch.empty_like(x)
+    ws, wsb = _ws(fwd_workspace_bytes(m, rec.n, rec.k, r), dev, workspace)
+    c = rec.c_struct()
+    _check(lib.qlora_linear_fwd_dropout(_ptr(x), m, ctypes.byref(c), _ptr(lora_a), _ptr(lora_b), r, float(alpha),
+                                        _ptr(mask), float(p), _ptr(x_drop), _ptr(y), _ptr(t_save), _ptr(ws), wsb,
+                                        _stream(stream)))
+    return y, t_save, x_drop
+
+
+def linear_bwd_dropout(dy: torch.Tensor, x_drop: torch.Tensor, rec: NF4Weight, lora_a: torch.Tensor,
+                       lora_b: torch.Tensor, alpha: float, mask: torch.Tensor, p: float, t_save: torch.Tensor,
+                       dx=None, da=None, db=None, flags: int = 0, workspace=None, stream=None):
+    """Backward of linear_fwd_dropout.  Returns (dx, da, db)."""
+    lib = load()
+    m = x_drop.shape[0]
+    r = lora_a.shape[0]
+    dev = x_drop.device
+    if dx is None:
+        dx = torch.empty((m, rec.k), dtype=torch.bfloat16, device=dev)
+    if da is None:
+        da = torch.empty((r, rec.k), dtype=torch.float32, device=dev)
+    if db is None:
+        db = torch.empty((rec.n, r), dtype=torch.float32, device=dev)
+    ws, wsb = _ws(bwd_workspace_bytes(m, rec.n, rec.k, r), dev, workspace)
+    c = rec.c_struct()
+    _check(lib.qlora_linear_bwd_dropout(_ptr(dy), _ptr(x_drop), m, ctypes.byref(c), _ptr(lora_a), _ptr(lora_b), r,
+                                        float(alpha), _ptr(mask), float(p), _ptr(t_save), _ptr(dx), _ptr(da), _ptr(db),
+                                        int(flags), _ptr(ws), wsb, _stream(stream)))
     return dx, da, db
 
 

@@ -149,12 +149,12 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 // and, while profiling is on, bracketed by two CUDA events on its stream.
 enum ProfName : int {
   P_QUANTIZE = 0, P_DEQUANTIZE, P_LORA_DOWN, P_FWD_GEMM, P_BWD_GEMM, P_LORA_GRADS, P_SILU_FWD, P_SILU_BWD,
-  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_MERGE, P_LOWRANK, P_ADAMW, P_COUNT
+  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_MERGE, P_LOWRANK, P_ADAMW, P_DROPOUT, P_COUNT
 };
 const char* const kProfNames[P_COUNT] = {"nf4_quantize(3 kernels)", "nf4_dequantize", "lora_down", "fwd_gemm",
                                          "bwd_dx_gemm", "lora_grads", "silu_mul_fwd", "silu_mul_bwd",
                                          "wait_selftest", "fwd_grouped(2 kernels)", "lora_side_fwd", "nf4_merge",
-                                         "lowrank_update", "adamw"};
+                                         "lowrank_update", "adamw", "dropout"};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<bool> g_prof_on{false};
 struct ProfRec {
@@ -386,9 +386,12 @@ int qlora_linear_fwd_workspace_bytes(int64_t m, int64_t n, int64_t k, int r, siz
   return QLORA_OK;
 }
 
-int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, const uint16_t* lora_a,
-                     const uint16_t* lora_b, int r, float alpha, uint16_t* y, float* t_save, void* workspace,
-                     size_t workspace_bytes, void* stream) {
+// The forward of qlora_linear_fwd and qlora_linear_fwd_dropout.  With a mask, the LoRA branch
+// reads x_drop = x * mask (written here first) and T carries the factor 1 / (1 - p).
+static int linear_fwd_impl(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, const uint16_t* lora_a,
+                           const uint16_t* lora_b, int r, float alpha, const uint8_t* mask, float p_drop,
+                           uint16_t* x_drop, uint16_t* y, float* t_save, void* workspace, size_t workspace_bytes,
+                           void* stream) {
   DevInfo* di = nullptr;
   int rc = device(&di);
   if (rc) return rc;
@@ -399,6 +402,7 @@ int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, co
   if ((rc = check_ptr(x, "x")) || (rc = check_ptr(lora_a, "lora_a")) || (rc = check_ptr(lora_b, "lora_b")) ||
       (rc = check_ptr(y, "y")) || (rc = check_ptr(t_save, "t_save")))
     return rc;
+  if (mask && ((rc = check_ptr(x_drop, "x_drop")) || (rc = check_ptr(mask, "mask")))) return rc;
   const FwdWs ws = fwd_ws(m, w->n, w->k, r, di->num_sms);
   if ((rc = check_ptr(workspace, "workspace"))) return rc;
   if (workspace_bytes < ws.total) return fail(QLORA_ERR_INVALID_ARGUMENT, "workspace %zu < %zu bytes", workspace_bytes, ws.total);
@@ -408,20 +412,30 @@ int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, co
   const float scale = alpha / static_cast<float>(r);
   const int M = static_cast<int>(m), N = static_cast<int>(w->n), K = static_cast<int>(w->k);
   cudaError_t e;
+  // the LoRA branch input: x, or x * mask under dropout (T then scaled by 1 / (1 - p))
+  const uint16_t* xl = x;
+  float t_scale = 1.0f;
+  if (mask) {
+    Span sp(P_DROPOUT, s, 1);
+    e = qlora::launch_dropout_apply(x, mask, x_drop, m * w->k, di->num_sms, s);
+    if (e != cudaSuccess) return cuda_ret(e, "dropout apply");
+    xl = x_drop;
+    t_scale = static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop)));
+  }
   {
     // T = X A^T on the SMs the GEMM's last wave leaves idle; the GEMM starts
     // beside it and waits for T only before its LoRA k block
     const int cap = qlora::idle_sms_beside(qlora::fwd_gemm_ctas(M, N, K, di->num_sms), di->num_sms);
     if (use_side(M, r)) {
       Span sp(P_LORA_SIDE_FWD, s, 1);
-      e = qlora::launch_lora_side_fwd(reinterpret_cast<const __nv_bfloat16*>(x),
+      e = qlora::launch_lora_side_fwd(reinterpret_cast<const __nv_bfloat16*>(xl),
                                       reinterpret_cast<const __nv_bfloat16*>(lora_a), M, K, r, scale, t_save, st, cap,
-                                      di->status, g_wait_ns.load(), s);
+                                      di->status, g_wait_ns.load(), s, t_scale);
     } else {
       Span sp(P_LORA_DOWN, s, 1);
-      e = qlora::launch_lora_down(reinterpret_cast<const __nv_bfloat16*>(x),
+      e = qlora::launch_lora_down(reinterpret_cast<const __nv_bfloat16*>(xl),
                                   reinterpret_cast<const __nv_bfloat16*>(lora_a), 1, M, K, r, scale, t_save, st,
-                                  base + ws.st, cap, s);
+                                  base + ws.st, cap, s, nullptr, nullptr, 0, 1.0f, t_scale);
     }
   }
   if (e != cudaSuccess) return cuda_ret(e, "lora_down");
@@ -434,6 +448,42 @@ int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, co
   return cuda_ret(e, "fwd_gemm");
 }
 
+int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, const uint16_t* lora_a,
+                     const uint16_t* lora_b, int r, float alpha, uint16_t* y, float* t_save, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+  return linear_fwd_impl(x, m, w, lora_a, lora_b, r, alpha, nullptr, 0.f, nullptr, y, t_save, workspace,
+                         workspace_bytes, stream);
+}
+
+static int check_dropout(const uint8_t* mask, float p) {
+  if (!mask) return fail(QLORA_ERR_INVALID_ARGUMENT, "mask is NULL");
+  if (!(p >= 0.f && p < 1.f)) return fail(QLORA_ERR_INVALID_ARGUMENT, "dropout probability %g not in [0, 1)", (double)p);
+  return QLORA_OK;
+}
+
+int qlora_linear_fwd_dropout(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, const uint16_t* lora_a,
+                             const uint16_t* lora_b, int r, float alpha, const uint8_t* mask, float p,
+                             uint16_t* x_drop, uint16_t* y, float* t_save, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  const int rc = check_dropout(mask, p);
+  if (rc) return rc;
+  return linear_fwd_impl(x, m, w, lora_a, lora_b, r, alpha, mask, p, x_drop, y, t_save, workspace, workspace_bytes,
+                         stream);
+}
+
+int qlora_dropout_mask(uint64_t seed, uint64_t offset, int64_t m, int64_t k, float p, uint8_t* mask, void* stream) {
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  if (m < 0 || k <= 0 || k % 64) return fail(QLORA_ERR_INVALID_ARGUMENT, "shape [%lld, %lld] (k %% 64 == 0)", (long long)m, (long long)k);
+  if (!(p >= 0.f && p < 1.f)) return fail(QLORA_ERR_INVALID_ARGUMENT, "dropout probability %g not in [0, 1)", (double)p);
+  if (m == 0) return QLORA_OK;
+  if ((rc = check_ptr(mask, "mask"))) return rc;
+  Span sp(P_DROPOUT, static_cast<cudaStream_t>(stream), 1);
+  return cuda_ret(qlora::launch_dropout_mask(seed, offset, m * k, p, mask, di->num_sms, static_cast<cudaStream_t>(stream)),
+                  "dropout mask");
+}
+
 int qlora_linear_bwd_workspace_bytes(int64_t m, int64_t n, int64_t k, int r, size_t* bytes) {
   if (!bytes) return fail(QLORA_ERR_INVALID_ARGUMENT, "bytes is NULL");
   if (m < 0 || n <= 0 || k <= 0 || m >= (1ll << 31)) return fail(QLORA_ERR_INVALID_ARGUMENT, "shape");
@@ -444,10 +494,13 @@ int qlora_linear_bwd_workspace_bytes(int64_t m, int64_t n, int64_t k, int r, siz
   return QLORA_OK;
 }
 
-int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlora_nf4_weight* w,
-                     const uint16_t* lora_a, const uint16_t* lora_b, int r, float alpha, const float* t_save,
-                     uint16_t* dx, float* da, float* db, int flags, void* workspace, size_t workspace_bytes,
-                     void* stream) {
+// The backward of qlora_linear_bwd and qlora_linear_bwd_dropout.  With a mask, x is the
+// dropped branch input x_drop of the forward, dA carries 1 / (1 - p), and the LoRA term of dX is
+// added after the GEMM, masked.
+static int linear_bwd_impl(const uint16_t* dy, const uint16_t* x, int64_t m, const qlora_nf4_weight* w,
+                           const uint16_t* lora_a, const uint16_t* lora_b, int r, float alpha, const uint8_t* mask,
+                           float p_drop, const float* t_save, uint16_t* dx, float* da, float* db, int flags,
+                           void* workspace, size_t workspace_bytes, void* stream) {
   DevInfo* di = nullptr;
   int rc = device(&di);
   if (rc) return rc;
@@ -476,6 +529,7 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
   void* ldws = base + ws.su + ws.st;
   void* lgws = base + ws.su + ws.st + ws.ld;
   const float scale = alpha / static_cast<float>(r);
+  const float inv_keep = mask ? static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop))) : 1.0f;
   const int M = static_cast<int>(m), N = static_cast<int>(w->n), K = static_cast<int>(w->k);
   const uint64_t wait = g_wait_ns.load();
   const __nv_bfloat16* dyb = reinterpret_cast<const __nv_bfloat16*>(dy);
@@ -501,19 +555,43 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
     Span sp(P_LORA_GRADS, di->side, 1);
     const int cap = qlora::idle_sms_beside(qlora::bwd_gemm_ctas(M, N, K), di->num_sms);
     e = qlora::launch_lora_grads(xb, dyb, su, st, M, N, K, r, da, db, (flags & QLORA_ACCUM_DA) ? 1 : 0,
-                                 (flags & QLORA_ACCUM_DB) ? 1 : 0, lgws, di->status, wait, cap, di->side);
+                                 (flags & QLORA_ACCUM_DB) ? 1 : 0, lgws, di->status, wait, cap, di->side, inv_keep);
   }
   cudaError_t ej = cudaEventRecord(di->join, di->side);
   if (e == cudaSuccess) {
     Span sp(P_BWD_GEMM, s, 1);
     e = qlora::launch_bwd_dx_gemm(dyb, M, to_dev(w), su, reinterpret_cast<const __nv_bfloat16*>(lora_a), r,
                                   reinterpret_cast<__nv_bfloat16*>(dx), (flags & QLORA_ACCUM_DX) ? 1 : 0, di->status,
-                                  wait, s);
+                                  wait, s, mask ? 0 : 1);
+  }
+  if (e == cudaSuccess && mask) {
+    Span sp(P_DROPOUT, s, 1);
+    e = qlora::launch_dropout_lora_dx(reinterpret_cast<__nv_bfloat16*>(dx), su,
+                                      reinterpret_cast<const __nv_bfloat16*>(lora_a), mask, M, K, r, inv_keep, s);
   }
   // always join, so a stream capture never ends with the side stream forked
   const cudaError_t ew = ej == cudaSuccess ? cudaStreamWaitEvent(s, di->join, 0) : ej;
   if (e == cudaSuccess) e = ew;
   return cuda_ret(e, "bwd dx gemm");
+}
+
+int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlora_nf4_weight* w,
+                     const uint16_t* lora_a, const uint16_t* lora_b, int r, float alpha, const float* t_save,
+                     uint16_t* dx, float* da, float* db, int flags, void* workspace, size_t workspace_bytes,
+                     void* stream) {
+  return linear_bwd_impl(dy, x, m, w, lora_a, lora_b, r, alpha, nullptr, 0.f, t_save, dx, da, db, flags, workspace,
+                         workspace_bytes, stream);
+}
+
+int qlora_linear_bwd_dropout(const uint16_t* dy, const uint16_t* x_drop, int64_t m, const qlora_nf4_weight* w,
+                             const uint16_t* lora_a, const uint16_t* lora_b, int r, float alpha, const uint8_t* mask,
+                             float p, const float* t_save, uint16_t* dx, float* da, float* db, int flags,
+                             void* workspace, size_t workspace_bytes, void* stream) {
+  const int rc = check_dropout(mask, p);
+  if (rc) return rc;
+  if (m > 0 && !aligned16(mask)) return fail(QLORA_ERR_INVALID_ARGUMENT, "mask is not 16-byte aligned");
+  return linear_bwd_impl(dy, x_drop, m, w, lora_a, lora_b, r, alpha, mask, p, t_save, dx, da, db, flags, workspace,
+                         workspace_bytes, stream);
 }
 
 // The grouped problems as the launcher sees them (shapes only are needed for the workspace plan).

@@ -39,7 +39,7 @@ __host__ __device__ inline int lora_ld(int r) { return (r + 7) & ~7; }
 cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int mt_kmajor, int M, int K, int r,
                              float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int max_ctas,
                              cudaStream_t s, const float* cvt_src = nullptr, __nv_bfloat16* cvt_dst = nullptr,
-                             int64_t cvt_rows = 0, float cvt_scale = 1.0f);
+                             int64_t cvt_rows = 0, float cvt_scale = 1.0f, float t_scale = 1.0f);
 cudaError_t launch_silu_mul_fwd(const uint16_t* g, const uint16_t* u, uint16_t* h, int64_t n, int num_sms,
                                 cudaStream_t s);
 cudaError_t launch_silu_mul_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u, uint16_t* dg, uint16_t* du,
@@ -61,16 +61,18 @@ cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, cons
                             uint64_t wait_ns, int num_sms, cudaStream_t s);
 
 // Backward dX[M, K] (+)= dY[M, N] deq(W) + sU[M, r] A[r, K]   (sU = bf16(s * dY B))
+// with_lora = 0: the LoRA k steps are left out (dX = dY deq(W) only; the dropout path adds its
+// masked LoRA term separately).
 cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
                                const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
-                               unsigned* status, uint64_t wait_ns, cudaStream_t s);
+                               unsigned* status, uint64_t wait_ns, cudaStream_t s, int with_lora = 1);
 
 // LoRA gradients: dA[r, K] (+)= sU^T X   and   dB[N, r] (+)= dY^T sT
 size_t lora_grads_workspace_bytes(int M, int N, int K, int r, int num_sms);
 cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __nv_bfloat16* su,
                               const __nv_bfloat16* st, int M, int N, int K, int r, float* da, float* db,
                               int accum_da, int accum_db, void* ws, unsigned* status, uint64_t wait_ns, int max_ctas,
-                              cudaStream_t s);
+                              cudaStream_t s, float da_scale = 1.0f);
 // CTA-pair versions of both GEMMs (qgemm_pair.cu), used for M > 256 tokens.
 bool use_pair_gemm(int M);
 int fwd_pair_ctas(int M, int N);
@@ -80,7 +82,7 @@ cudaError_t launch_fwd_gemm_pair(const __nv_bfloat16* x, int M, const Nf4Dev& w,
                                  uint64_t wait_ns, cudaStream_t s);
 cudaError_t launch_bwd_gemm_pair(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
                                  const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
-                                 unsigned* status, uint64_t wait_ns, cudaStream_t s);
+                                 unsigned* status, uint64_t wait_ns, cudaStream_t s, int with_lora = 1);
 // Low-rank combinations (nf4_merge.cu).
 // out[n, k] = bf16(deq(W) + scale * B A), the B A sum a float32 FMA chain in j order.
 cudaError_t launch_nf4_merge(const Nf4Dev& w, const __nv_bfloat16* lora_a, const __nv_bfloat16* lora_b, int r,
@@ -104,6 +106,16 @@ struct AdamwHyper {
 // The float32 factors of step `step` (1-based), formed in double precision.
 AdamwHyper adamw_hyper(double lr, double beta1, double beta2, double eps, double weight_decay, int64_t step);
 cudaError_t launch_adamw(const AdamwTensor* tensors, int count, const AdamwHyper& h, int num_sms, cudaStream_t s);
+// LoRA dropout (dropout.cu): Philox4x32-10 keep mask, one bit per element of an [m, k] input
+// (n_elems % 64 == 0), and x_drop = x * mask (bf16).
+cudaError_t launch_dropout_mask(uint64_t seed, uint64_t offset, int64_t n_elems, float p, uint8_t* mask, int num_sms,
+                                cudaStream_t s);
+cudaError_t launch_dropout_apply(const uint16_t* x, const uint8_t* mask, uint16_t* x_drop, int64_t n_elems, int num_sms,
+                                 cudaStream_t s);
+// dx[m, k] = bf16(dx + (keep(m, k) ? coef * sum_j su[m, j] a[j, k] : 0)), su with row stride lora_ld(r)
+// (nf4_merge.cu): the LoRA term of dX under dropout.
+cudaError_t launch_dropout_lora_dx(__nv_bfloat16* dx, const __nv_bfloat16* su, const __nv_bfloat16* lora_a,
+                                   const uint8_t* mask, int M, int K, int r, float coef, cudaStream_t s);
 // 2-D bf16 tensor map, 128-byte swizzle, zero fill outside [outer x inner] (qgemm.cu).
 bool make_tensor_map_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch,
                              uint32_t box_inner, uint32_t box_outer);
@@ -112,7 +124,7 @@ bool make_tensor_map_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, u
 bool lora_side_supported(int r);
 cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lora_a, int M, int K, int r, float scale,
                                  float* t_save, __nv_bfloat16* st, int max_ctas, unsigned* status, uint64_t wait_ns,
-                                 cudaStream_t s);
+                                 cudaStream_t s, float t_scale = 1.0f);
 // Grid sizes of the GEMMs and the SMs they leave idle (budget for side kernels).
 int fwd_gemm_ctas(int M, int N, int K, int num_sms);
 int bwd_gemm_ctas(int M, int N, int K);

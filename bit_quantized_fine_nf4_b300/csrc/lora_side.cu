@@ -20,6 +20,7 @@ struct SideParams {
   int M, K, r, rp;
   int stages, stage_bytes;
   float scale;
+  float t_scale;         // t_save = t_scale * (X A^T); 1 without dropout (1 / (1 - p) with it)
   unsigned long long wait_ns;
 };
 
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(kSideThreads, 1)
         if (tok < p.M) {
 #pragma unroll
           for (int q = 0; q < 16; q += 4) {
-            const float f[4] = {__uint_as_float(v[q]), __uint_as_float(v[q + 1]), __uint_as_float(v[q + 2]),
-                                __uint_as_float(v[q + 3])};
+            const float f[4] = {__fmul_rn(__uint_as_float(v[q]), p.t_scale), __fmul_rn(__uint_as_float(v[q + 1]), p.t_scale),
+                                __fmul_rn(__uint_as_float(v[q + 2]), p.t_scale), __fmul_rn(__uint_as_float(v[q + 3]), p.t_scale)};
             if (c + q < rk)  // rk % 8 == 0: four consecutive columns are all inside rk or all past it
               *reinterpret_cast<uint2*>(p.s_out + static_cast<int64_t>(tok) * rk + c + q) =
                   make_uint2(pack_bf16x2_rn(__fmul_rn(f[0], p.scale), __fmul_rn(f[1], p.scale)),
@@ -166,7 +167,7 @@ bool lora_side_supported(int r) { return r >= 1 && r <= 64; }
 
 cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lora_a, int M, int K, int r, float scale,
                                  float* t_save, __nv_bfloat16* st, int max_ctas, unsigned* status, uint64_t wait_ns,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, float t_scale) {
   const int rp = (r + 15) / 16 * 16;
   CUtensorMap ta, tb;
   if (!make_tensor_map_bf16_2d(&ta, x, K, M, static_cast<uint64_t>(K) * 2, 64, 128)) return cudaErrorInvalidValue;
@@ -183,6 +184,7 @@ cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lo
   prm.stages = (200 * 1024) / prm.stage_bytes;
   if (prm.stages > kSideMaxStages) prm.stages = kSideMaxStages;
   prm.scale = scale;
+  prm.t_scale = t_scale;
   prm.wait_ns = wait_ns;
   const size_t smem = 1024 + static_cast<size_t>(prm.stages) * prm.stage_bytes + (2 * kSideMaxStages + 4) * 8 + 16;
   const int tiles = (M + 127) / 128;

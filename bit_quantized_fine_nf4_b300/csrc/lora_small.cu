@@ -42,7 +42,8 @@ __device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, ui
 // 16-byte fragment loads of 8 rows x 4 threads hit distinct bank groups; every
 // tile then reads its fragments from there.  Unstaged, fragments come from
 // global memory (and gather 8 strided values when mt is [K, r]).
-// Outputs: out_f32 [M, r] (row stride r) and out_bf16 = bf16(scale * out)
+// Outputs (out = t_scale * in . mt^T, t_scale = 1 except under dropout):
+// out_f32 [M, r] (row stride r) and out_bf16 = bf16(scale * out)
 // [M, rk] with rk = r rounded up to a multiple of 8 (the row stride of the
 // internal bf16 LoRA operands, which the tensor-core kernels load by TMA); its
 // columns r .. rk-1 are zero.
@@ -67,7 +68,7 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
                                                       __nv_bfloat16* __restrict__ out_bf16,
                                                       const float* __restrict__ cvt_src,
                                                       __nv_bfloat16* __restrict__ cvt_dst, int64_t cvt_rows,
-                                                      float cvt_scale) {
+                                                      float cvt_scale, float t_scale) {
   constexpr int RP = NT * 8;
   extern __shared__ float s_red[];  // [W warps][16 rows][RP], then (STAGED) mt as [RP][K + 8] bf16
   unsigned short* s_mt = reinterpret_cast<unsigned short*>(s_red + W * 16 * RP);
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
       float v = 0.f;
 #pragma unroll
       for (int w = 0; w < W; ++w) v += s_red[w * 16 * RP + idx];
+      v = __fmul_rn(v, t_scale);  // 1 except under dropout (1 / (1 - p))
       const int row = m0 + idx / RP, j = idx % RP;
       if (row >= M) continue;
       // columns j >= r of the product are exactly zero (mt rows past r load as zero)
@@ -229,7 +231,7 @@ size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms) {
 cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int mt_kmajor, int M, int K, int r,
                              float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int max_ctas,
                              cudaStream_t s, const float* cvt_src, __nv_bfloat16* cvt_dst, int64_t cvt_rows,
-                             float cvt_scale) {
+                             float cvt_scale, float t_scale) {
   (void)ws;
   const int tiles = (M + 15) / 16;
   const int rp = r <= 16 ? 16 : (r <= 32 ? 32 : (r <= 64 ? 64 : 128));
@@ -259,7 +261,7 @@ cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, i
     cfg.blockDim = dim3(W * 32);                                                                                 \
     cfg.dynamicSmemBytes = smem;                                                                                 \
     e = cudaLaunchKernelEx(&cfg, k_lora_down<NT, KM, W, ST>, in, mt, M, K, r, scale, out_f32, out_bf16, cvt_src, \
-                           cvt_dst, cvt_rows, cvt_scale);                                                        \
+                           cvt_dst, cvt_rows, cvt_scale, t_scale);                                               \
   } while (0)
 #define QLORA_LD(NT, KM, W)           \
   do {                                \

@@ -2,6 +2,7 @@
 //
 //   merge / export   out_bf16[n, k] = bf16( deq(W)[n, k] + s * sum_j B[n, j] A[j, k] )
 //   dense update     out_f32[n, k]  = W[n, k] (- deq(Q)[n, k]) + c * sum_j B[n, j] A[j, k]
+//   dropout dX       dx[m, k] = bf16(dx[m, k] + (keep(m, k) ? c * sum_j sU[m, j] A[j, k] : 0))
 //
 // Day 25 notes "Fine-tuning and LoRA/QLoRA", section 2.6: after training the
 // product B A is added to W0 and the layer is a plain linear again.  P1 tutorial
@@ -45,9 +46,10 @@ struct MgParams {
   const float* mean;
   const void* dense;            // dense W [n, k] (float32 or bfloat16), dense update only
   const __nv_bfloat16* lora_a;  // [r, k]
-  const __nv_bfloat16* lora_b;  // [n, r]
-  void* out;                    // bf16 (merge) or float32 (update) [n, k]
-  int n, k, r;
+  const __nv_bfloat16* lora_b;  // [n, r] with row stride ldb
+  const uint8_t* mask;          // keep bits of [n, k] (masked variant), bit (n k + c) % 8 of byte (n k + c) / 8
+  void* out;                    // bf16 (merge, dropout dX) or float32 (update) [n, k]
+  int n, k, r, ldb;
   float coef;
 };
 
@@ -68,7 +70,7 @@ __device__ __forceinline__ void deq8(const MgParams& p, const float* s_lv, float
   }
 }
 
-template <int BASE, bool SUB_NF4, bool OUT_BF16>
+template <int BASE, bool SUB_NF4, bool OUT_BF16, bool MASKED>
 __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p) {
   extern __shared__ float s_mg[];
   float* s_a = s_mg;                        // [r][256]
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
   for (int i = threadIdx.x; i < p.r * kMgRows; i += kMgThreads) {
     const int row = i % kMgRows, j = i / kMgRows;  // consecutive threads write consecutive banks
     const int n = n0 + row;
-    s_bt[j * kMgRows + row] = n < p.n ? bf16_bits_to_f32(b16[static_cast<int64_t>(n) * p.r + j]) : 0.f;
+    s_bt[j * kMgRows + row] = n < p.n ? bf16_bits_to_f32(b16[static_cast<int64_t>(n) * p.ldb + j]) : 0.f;
   }
   if (threadIdx.x < 16) {
     constexpr uint32_t hex[16] = QLORA_NF4_LEVELS_HEX;
@@ -148,7 +150,7 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
         base[0] = v0.x; base[1] = v0.y; base[2] = v0.z; base[3] = v0.w;
         base[4] = v1.x; base[5] = v1.y; base[6] = v1.z; base[7] = v1.w;
       } else {
-        const uint4 v = ldg_nc_v4(static_cast<const __nv_bfloat16*>(p.dense) + o);
+        const uint4 v = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dense) + o);
         const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
@@ -163,10 +165,12 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
         for (int e = 0; e < 8; ++e) base[e] = __fsub_rn(base[e], q[e]);
       }
     }
+    const int64_t o = static_cast<int64_t>(n) * p.k + kc;
+    const uint32_t keep = MASKED ? p.mask[o >> 3] : 0xffu;
     float o8[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o8[e] = p.r > 0 ? __fadd_rn(base[e], __fmul_rn(p.coef, acc[i][e])) : base[e];
-    const int64_t o = static_cast<int64_t>(n) * p.k + kc;
+    for (int e = 0; e < 8; ++e)
+      o8[e] = (p.r > 0 && ((keep >> e) & 1u)) ? __fadd_rn(base[e], __fmul_rn(p.coef, acc[i][e])) : base[e];
     if (OUT_BF16) {
       *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o) =
           make_uint4(pack_bf16x2_rn(o8[0], o8[1]), pack_bf16x2_rn(o8[2], o8[3]), pack_bf16x2_rn(o8[4], o8[5]),
@@ -179,13 +183,14 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
   }
 }
 
-template <int BASE, bool SUB_NF4, bool OUT_BF16>
+template <int BASE, bool SUB_NF4, bool OUT_BF16, bool MASKED = false>
 static cudaError_t run_combine(const MgParams& p, cudaStream_t s) {
   const size_t smem = (static_cast<size_t>(p.r) * (kMgCols + kMgRows) + 16) * sizeof(float);
-  cudaError_t e = set_smem_limit_once(k_lowrank_combine<BASE, SUB_NF4, OUT_BF16>, (128 * (kMgCols + kMgRows) + 16) * 4);
+  cudaError_t e = set_smem_limit_once(k_lowrank_combine<BASE, SUB_NF4, OUT_BF16, MASKED>,
+                                      (128 * (kMgCols + kMgRows) + 16) * 4);
   if (e != cudaSuccess) return e;
   const dim3 grid((p.k + kMgCols - 1) / kMgCols, (p.n + kMgRows - 1) / kMgRows);
-  k_lowrank_combine<BASE, SUB_NF4, OUT_BF16><<<grid, kMgThreads, smem, s>>>(p);
+  k_lowrank_combine<BASE, SUB_NF4, OUT_BF16, MASKED><<<grid, kMgThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
@@ -202,6 +207,7 @@ cudaError_t launch_nf4_merge(const Nf4Dev& w, const __nv_bfloat16* lora_a, const
   p.n = static_cast<int>(w.n);
   p.k = static_cast<int>(w.k);
   p.r = r;
+  p.ldb = r;
   p.coef = scale;
   return run_combine<MG_NF4, false, true>(p, s);
 }
@@ -223,9 +229,26 @@ cudaError_t launch_lowrank_update(const void* dense, int dense_bf16, const Nf4De
   p.n = static_cast<int>(n);
   p.k = static_cast<int>(k);
   p.r = r;
+  p.ldb = r;
   p.coef = coef;
   if (dense_bf16) return sub ? run_combine<MG_BF16, true, false>(p, s) : run_combine<MG_BF16, false, false>(p, s);
   return sub ? run_combine<MG_F32, true, false>(p, s) : run_combine<MG_F32, false, false>(p, s);
+}
+
+cudaError_t launch_dropout_lora_dx(__nv_bfloat16* dx, const __nv_bfloat16* su, const __nv_bfloat16* lora_a,
+                                   const uint8_t* mask, int M, int K, int r, float coef, cudaStream_t s) {
+  MgParams p = {};
+  p.dense = dx;
+  p.lora_a = lora_a;
+  p.lora_b = su;
+  p.mask = mask;
+  p.out = dx;
+  p.n = M;
+  p.k = K;
+  p.r = r;
+  p.ldb = lora_ld(r);
+  p.coef = coef;
+  return run_combine<MG_BF16, false, true, true>(p, s);
 }
 
 }  // namespace qlora

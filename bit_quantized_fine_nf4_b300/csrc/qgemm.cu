@@ -351,6 +351,9 @@ __global__ void __launch_bounds__(kWbThreads, 1)
           for (int sl = 0; sl < 4; ++sl) tma_load_2d(sa + kWbABytes + sl * 8192, &tm_la, &full[s], k0 + sl * 64, e * 64);
         }
       }
+      // no LoRA k steps: still wait once for the preceding kernel, so this grid never completes
+      // before it does (later kernels of the stream rely on that order)
+      if (p.lora_blocks == 0) griddep_wait();
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -484,6 +487,7 @@ struct LgParams {
   int M, N, K, r;
   int tiles_a, tiles;  // 128-column tiles of dA^T (first tiles_a) and of dB
   int accum_da, accum_db;
+  float da_scale;      // dA = da_scale * (sU^T X); 1 except under dropout
   unsigned long long wait_ns;
 };
 
@@ -619,7 +623,7 @@ __global__ void __launch_bounds__(kLgThreads, 1)
             for (int jj = 0; jj < 16; ++jj) {
               if (j0 + jj >= p.r) break;
               float* d = p.da + static_cast<int64_t>(j0 + jj) * p.K + c;
-              const float val = __uint_as_float(v[jj]);
+              const float val = __fmul_rn(__uint_as_float(v[jj]), p.da_scale);
               *d = p.accum_da ? (*d + val) : val;
             }
           } else {
@@ -822,8 +826,9 @@ cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, cons
 
 cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
                                const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
-                               unsigned* status, uint64_t wait_ns, cudaStream_t s) {
-  if (use_pair_gemm(M)) return launch_bwd_gemm_pair(dy, M, w, su, lora_a, r, dx, accumulate, status, wait_ns, s);
+                               unsigned* status, uint64_t wait_ns, cudaStream_t s, int with_lora) {
+  if (use_pair_gemm(M))
+    return launch_bwd_gemm_pair(dy, M, w, su, lora_a, r, dx, accumulate, status, wait_ns, s, with_lora);
   const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
   CUtensorMap tdy, tsu, tla;
   if (!make_tensor_map_bf16_2d(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 256)) return cudaErrorInvalidValue;
@@ -841,7 +846,7 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
   prm.N = N;
   prm.K = K;
   prm.r = r;
-  prm.lora_blocks = (r + 63) / 64;
+  prm.lora_blocks = with_lora ? (r + 63) / 64 : 0;
   prm.accumulate = accumulate;
   prm.wait_ns = wait_ns;
   constexpr int kStages = 3;
@@ -862,7 +867,7 @@ size_t lora_grads_workspace_bytes(int M, int N, int K, int r, int num_sms) {
 cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, const __nv_bfloat16* su,
                               const __nv_bfloat16* st, int M, int N, int K, int r, float* da, float* db,
                               int accum_da, int accum_db, void* ws, unsigned* status, uint64_t wait_ns, int max_ctas,
-                              cudaStream_t s) {
+                              cudaStream_t s, float da_scale) {
   (void)ws;
   CUtensorMap tx, tdy, tsu, tst;
   if (!make_tensor_map_bf16_2d(&tx, x, K, M, static_cast<uint64_t>(K) * 2, 64, 64)) return cudaErrorInvalidValue;
@@ -882,6 +887,7 @@ cudaError_t launch_lora_grads(const __nv_bfloat16* x, const __nv_bfloat16* dy, c
   prm.tiles = prm.tiles_a + (N + 127) / 128;
   prm.accum_da = accum_da;
   prm.accum_db = accum_db;
+  prm.da_scale = da_scale;
   prm.wait_ns = wait_ns;
   int grid = prm.tiles < max_ctas ? prm.tiles : max_ctas;
   if (grid >= 2) grid &= ~1;  // clusters of two: the CTAs sit on whole TPCs, which the pair GEMMs need

@@ -207,6 +207,9 @@ __global__ void __launch_bounds__(kPrThreads, 1)
           tma_load_2d_to_pair_bar(st + kPrBox, tm, bar, kc, tb);
         }
       }
+      // no LoRA k steps: still wait once for the preceding kernel, so this grid never completes
+      // before it does (later kernels of the stream rely on that order)
+      if (p.lora_blocks == 0) griddep_wait();
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -423,13 +426,14 @@ cudaError_t launch_fwd_gemm_pair(const __nv_bfloat16* x, int M, const Nf4Dev& w,
 
 cudaError_t launch_bwd_gemm_pair(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
                                  const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
-                                 unsigned* status, uint64_t wait_ns, cudaStream_t s) {
+                                 unsigned* status, uint64_t wait_ns, cudaStream_t s, int with_lora) {
   const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
   CUtensorMap tdy, tsu;
   const int rk = lora_ld(r);
   if (!make_tensor_map_bf16_2d(&tdy, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 128)) return cudaErrorInvalidValue;
   if (!make_tensor_map_bf16_2d(&tsu, su, rk, M, static_cast<uint64_t>(rk) * 2, 64, 128)) return cudaErrorInvalidValue;
   PairParams prm = pair_params(w, nullptr, lora_a, dx, status, M, r, accumulate, wait_ns);
+  if (!with_lora) prm.lora_blocks = 0;
   prm.out_cols = K;
   CUtensorMap tdx = tsu;
   prm.staged_store = !accumulate && make_tensor_map_bf16_2d(&tdx, dx, K, M, static_cast<uint64_t>(K) * 2, 64, 128);

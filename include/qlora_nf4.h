@@ -217,6 +217,49 @@ int qlora_linear_bwd(const uint16_t* dy, const uint16_t* x, int64_t m, const qlo
                      uint16_t* dx, float* da, float* db, int flags, void* workspace, size_t workspace_bytes,
                      void* stream);
 
+/* ----------------------------------------------------------------- LoRA dropout */
+
+/*
+ * Keep mask of LoRA dropout for an [m, k] branch input (k % 64 == 0): one bit
+ * per element, bit e % 8 of byte e / 8 for element e = row * k + col (1 = kept),
+ * m * k / 8 bytes.  Every page's LoRA configuration sets lora_dropout = 0.05
+ * (P1 tutorial section 3.3; tbr8.org section 4; fedte.cc section 2).  Drawn by
+ * Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2, 3",
+ * 2011): element e takes 32-bit word e % 4 of Philox(counter = (e / 4 low
+ * word, e / 4 high word, offset low word, offset high word), key = (seed low
+ * word, seed high word)) and is kept when that word >= floor(p * 2^32),
+ * 0 <= p < 1.  A fresh (seed, offset) per step gives a fresh mask; the same
+ * pair gives the same bits on every device.
+ */
+int qlora_dropout_mask(uint64_t seed, uint64_t offset, int64_t m, int64_t k, float p, uint8_t* mask, void* stream);
+
+/*
+ * qlora_linear_fwd with dropout on the LoRA branch input (inverted dropout: the
+ * kept elements are scaled by 1 / (1 - p); the frozen path sees x itself):
+ *   x_drop bf16 [m, k] = x * mask        (written; keep it for the backward)
+ *   t_save f32  [m, r] = (x_drop A^T) / (1 - p)
+ *   y      bf16 [m, n] = x deq(W)^T + s t_save B^T
+ * mask as qlora_dropout_mask writes it; same workspace as qlora_linear_fwd.
+ */
+int qlora_linear_fwd_dropout(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, const uint16_t* lora_a,
+                             const uint16_t* lora_b, int r, float alpha, const uint8_t* mask, float p,
+                             uint16_t* x_drop, uint16_t* y, float* t_save, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/*
+ * Backward of qlora_linear_fwd_dropout (the same mask, p, and the forward's
+ * x_drop and t_save): U = dY B;
+ *   dx = dY deq(W) + (s U A) * mask / (1 - p)
+ *   da = s U^T x_drop / (1 - p),   db = s dY^T t_save
+ * Flags and workspace as qlora_linear_bwd.  The LoRA term of dx goes through
+ * the mask, so it is added to the frozen-path product after the GEMM (one more
+ * rounding to bf16 than without dropout).
+ */
+int qlora_linear_bwd_dropout(const uint16_t* dy, const uint16_t* x_drop, int64_t m, const qlora_nf4_weight* w,
+                             const uint16_t* lora_a, const uint16_t* lora_b, int r, float alpha, const uint8_t* mask,
+                             float p, const float* t_save, uint16_t* dx, float* da, float* db, int flags,
+                             void* workspace, size_t workspace_bytes, void* stream);
+
 /*
  * One small-token forward problem of a grouped call (host struct; the
  * pointers in it are device pointers, `w` points to a host record struct).
