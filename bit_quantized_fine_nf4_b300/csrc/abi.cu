@@ -153,7 +153,7 @@ enum ProfName : int {
 };
 const char* const kProfNames[P_COUNT] = {"nf4_quantize(3 kernels)", "nf4_dequantize", "lora_down", "fwd_gemm",
                                          "bwd_dx_gemm", "lora_grads", "silu_mul_fwd", "silu_mul_bwd",
-                                         "wait_selftest", "fwd_grouped(2 kernels)", "lora_side_fwd", "nf4_merge",
+                                         "wait_selftest", "fwd_grouped", "lora_side_fwd", "nf4_merge",
                                          "lowrank_update", "adamw", "dropout"};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<bool> g_prof_on{false};
@@ -603,7 +603,7 @@ static int grouped_problems(const qlora_linear_problem* problems, int count, std
     const qlora_linear_problem& q = problems[i];
     if ((rc = check_weight(q.w))) return fail(rc, "problem %d: %s", i, t_last_error);
     if (q.m < 1 || q.m > 16) return fail(QLORA_ERR_UNSUPPORTED, "problem %d: m = %lld (the grouped path takes 1..16 tokens)", i, (long long)q.m);
-    if (q.r < 8 || q.r > 64 || (q.r % 8)) return fail(QLORA_ERR_UNSUPPORTED, "problem %d: r = %d (grouped path: 8 <= r <= 64, r %% 8 == 0)", i, q.r);
+    if (q.r < 1 || q.r > 128) return fail(QLORA_ERR_UNSUPPORTED, "problem %d: r = %d (need 1 <= r <= 128)", i, q.r);
     if (check_pointers) {
       if ((rc = check_ptr(q.x, "x")) || (rc = check_ptr(q.lora_a, "lora_a")) || (rc = check_ptr(q.lora_b, "lora_b")) ||
           (rc = check_ptr(q.y, "y")))
@@ -625,14 +625,17 @@ static int grouped_problems(const qlora_linear_problem* problems, int count, std
 }
 
 // Workspace of the launches: problems go out in chunks of at most
-// fwd_grouped_max_problems(), each chunk with its own plan.
+// decode_max_problems(), each chunk with its own plan.
 static size_t grouped_workspace(const std::vector<qlora::GroupedProblem>& gp, int num_sms) {
-  const int count = static_cast<int>(gp.size()), chunk = qlora::fwd_grouped_max_problems();
+  const int count = static_cast<int>(gp.size()), chunk = qlora::decode_max_problems();
   size_t tot = 0;
   for (int i0 = 0; i0 < count; i0 += chunk)
-    tot += qlora::fwd_grouped_workspace_bytes(gp.data() + i0, count - i0 < chunk ? count - i0 : chunk, num_sms);
+    tot += qlora::decode_workspace_bytes(gp.data() + i0, count - i0 < chunk ? count - i0 : chunk, num_sms);
   return tot;
 }
+
+// Call epochs of the grouped forward (tags of its workspace counters).
+static std::atomic<uint32_t> g_decode_epoch{0x51a7u};
 
 int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problems, int count, size_t* bytes) {
   if (!bytes) return fail(QLORA_ERR_INVALID_ARGUMENT, "bytes is NULL");
@@ -661,14 +664,15 @@ int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, vo
   if ((rc = check_ptr(workspace, "workspace"))) return rc;
   if (workspace_bytes < need) return fail(QLORA_ERR_INVALID_ARGUMENT, "workspace %zu < %zu bytes", workspace_bytes, need);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int chunk = qlora::fwd_grouped_max_problems();
+  const int chunk = qlora::decode_max_problems();
   char* ws = static_cast<char*>(workspace);
   for (int i0 = 0; i0 < count; i0 += chunk) {
     const int n = count - i0 < chunk ? count - i0 : chunk;
-    Span sp(P_FWD_GROUPED, s, 2);
-    cudaError_t e = qlora::launch_fwd_grouped(gp.data() + i0, n, ws, di->status, g_wait_ns.load(), di->num_sms, s);
+    Span sp(P_FWD_GROUPED, s, 1);
+    cudaError_t e = qlora::launch_decode(gp.data() + i0, n, ws, g_decode_epoch.fetch_add(1u), di->status,
+                                         g_wait_ns.load(), di->num_sms, s);
     if (e != cudaSuccess) return cuda_ret(e, "fwd grouped");
-    ws += qlora::fwd_grouped_workspace_bytes(gp.data() + i0, n, di->num_sms);
+    ws += qlora::decode_workspace_bytes(gp.data() + i0, n, di->num_sms);
   }
   return QLORA_OK;
 }

@@ -130,21 +130,24 @@ int fwd_gemm_ctas(int M, int N, int K, int num_sms);
 int bwd_gemm_ctas(int M, int N, int K);
 int idle_sms_beside(int gemm_ctas, int num_sms);
 
-// Grouped small-token forward (qgemv_grouped.cu): one problem of the list.
+// Grouped small-token forward (decode.cu): one problem of the list.
 struct GroupedProblem {
-  const __nv_bfloat16* x;       // [m, k], m <= 16
+  const __nv_bfloat16* x;       // [m, k], 1 <= m <= 16
   Nf4Dev w;                     // [n, k]
   const __nv_bfloat16* lora_a;  // [r, k]
   const __nv_bfloat16* lora_b;  // [n, r]
-  int m, r;                     // r <= 64
+  int m, r;                     // 1 <= r <= 128
   float alpha;
   __nv_bfloat16* y;             // [m, n]
   float* t_save;                // [m, r] or null
 };
-int fwd_grouped_max_problems();
-size_t fwd_grouped_workspace_bytes(const GroupedProblem* probs, int count, int num_sms);
-cudaError_t launch_fwd_grouped(const GroupedProblem* probs, int count, void* ws, unsigned* status, uint64_t wait_ns,
-                               int num_sms, cudaStream_t s);
+// Problems per launch; a longer list goes out in several launches.
+int decode_max_problems();
+size_t decode_workspace_bytes(const GroupedProblem* probs, int count, int num_sms);
+// One launch for the whole list (count <= decode_max_problems()); `epoch` tags this call's
+// counters in the workspace (any value that differs between calls sharing a workspace).
+cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, uint32_t epoch, unsigned* status,
+                          uint64_t wait_ns, int num_sms, cudaStream_t s);
 
 // Bounded-wait self test: one CTA waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t wait_ns, cudaStream_t s);

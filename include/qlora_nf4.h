@@ -270,7 +270,7 @@ typedef struct qlora_linear_problem {
   const qlora_nf4_weight* w;   /* [n, k] */
   const uint16_t* lora_a;      /* bf16 [r, k] */
   const uint16_t* lora_b;      /* bf16 [n, r] */
-  int r;                       /* 8 <= r <= 64, r % 8 == 0 */
+  int r;                       /* 1 <= r <= 128 */
   float alpha;
   uint16_t* y;                 /* bf16 [m, n] (overwritten) */
   float* t_save;               /* f32 [m, r] = X A^T, or NULL */
@@ -285,15 +285,20 @@ int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problem
 
 /*
  * qlora_linear_fwd for a list of independent small-token problems (decode:
- * each matrix of a layer stack applied to 1..16 tokens), in two kernel
- * launches per 300 problems: all X A^T products, then one pass that streams
- * every weight of the list.  Same arithmetic as qlora_linear_fwd (bf16
- * operands, fp32 accumulation, s X A^T rounded to bf16), except that with at
- * most 2 tokens the levels multiply in float32 (L times the float32 block
- * scale, where the tensor-core path rounds bf16(L a')).  Short lists split the
- * k range of each 256-row tile over several SMs; the splits' float32 partial
- * sums are added in a fixed order, so every y is deterministic.  `problems` is
- * a host array of `count` entries.
+ * each matrix of a layer stack, or one decoder stage's q,k,v, applied to
+ * 1..16 tokens), in ONE kernel launch per 128 problems.  The launch starts
+ * while the preceding kernel of the stream still runs, pre-loads its weight
+ * codes into L2 and waits for that kernel only before it reads anything the
+ * stream wrote (x, the workspace), so consecutive calls keep HBM streaming.
+ * Arithmetic: bf16 operands, float32 accumulation, s X A^T rounded to bf16 as
+ * in qlora_linear_fwd; the weights enter as bf16(L[code]) with the block scale
+ * a' applied in float32 to each 64-wide block's partial sum (within 2^-8 per
+ * weight of the bf16_rn(L a') qlora_linear_fwd uses).  Split tiles add their
+ * float32 partial sums in a fixed order, so every y is deterministic.
+ * `problems` is a host array of `count` entries; 1 <= m <= 16, 1 <= r <= 128.
+ * The workspace holds per-call counters tagged with a call number and returned
+ * to zero by the call itself: it needs no initialisation and may be reused by
+ * later calls (and graph replays) ordered on the same stream.
  */
 int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, void* workspace, size_t workspace_bytes,
                              void* stream);

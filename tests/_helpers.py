@@ -21,20 +21,25 @@ def rel_fro(got, ref) -> float:
 
 
 def max_row_rel(got, ref) -> float:
-    """Largest per-row relative error ||got_i - ref_i|| / ||ref_i|| over the rows of a 2-D array.
+    """Largest per-row error ||got_i - ref_i|| / max(||ref_i||, rms row norm) over the rows of a 2-D array.
 
     A whole-tensor Frobenius norm can hide one wrong row or a wrong tail tile
     (one bad row of 2048 moves it by about 0.02); this bounds every row on its
-    own.  Rows whose reference is exactly zero are compared absolutely.
+    own.  A row whose reference nearly cancels (a one-element row of dB at
+    rank 1, say) is measured against the root-mean-square row norm instead of
+    its own tiny norm: a wrong row still shows an error of about one rms row.
     """
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     if got.ndim == 1:
         got, ref = got[None, :], ref[None, :]
+    if not ref.size:
+        return 0.0
     num = np.linalg.norm(got - ref, axis=1)
     den = np.linalg.norm(ref, axis=1)
-    den = np.where(den > 0, den, 1.0)
-    return float((num / den).max()) if num.size else 0.0
+    rms = np.linalg.norm(ref) / np.sqrt(ref.shape[0])
+    den = np.maximum(den, rms if rms > 0 else 1.0)
+    return float((num / den).max())
 
 
 def assert_close(got, ref, tol, what=""):

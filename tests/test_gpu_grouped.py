@@ -1,9 +1,13 @@
 """GPU parity: the grouped small-token forward (decode over a list of matrices).
 
 A list of independent problems with mixed shapes (Llama-7B projection shapes,
-ragged rows), token counts 1..16 and ranks 8..64 runs as one
+ragged rows), token counts 1..16 and ranks 1..128 runs as one
 qlora_linear_fwd_grouped call; every output is compared with the float64
-oracle (GEMM tolerance) and with the single-problem entry point.
+oracle (GEMM tolerance, whole tensor and every row) and with the
+single-problem entry point.  A chain of dependent calls (each input the
+previous call's output, as a decoder's layers are) checks that the weights
+the next call prefetches early never let it read its input early, and a CUDA
+graph replay of the chain checks the per-call counters start clean every time.
 """
 
 import numpy as np
@@ -12,13 +16,14 @@ import torch
 
 import synthetic
 from oracle import linear, nf4
-from tests._helpers import GEMM_TOL, t_save_tol, rel_fro, to_np32, to_np64
+from tests._helpers import GEMM_TOL, assert_close, t_save_tol, rel_fro, to_np32, to_np64
 
 pytestmark = pytest.mark.gpu
 
 SHAPES = [  # (n, k, m, r)
     (4096, 4096, 1, 16), (4096, 4096, 4, 16), (11008, 4096, 16, 16), (4096, 11008, 4, 16),
     (136, 640, 3, 8), (264, 320, 16, 64), (512, 512, 7, 24), (128, 64, 1, 8),
+    (200, 1088, 9, 1), (72, 256, 12, 5), (384, 512, 16, 128), (1032, 2112, 2, 100),
 ]
 
 
@@ -45,10 +50,12 @@ def test_grouped_matches_oracle_and_single_calls(lib):
         ref = nf4.quantize(to_np32(c.w.cpu()), n, k)
         wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
         yr, tr = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
-        assert rel_fro(to_np64(ys[i]), yr) < GEMM_TOL, SHAPES[i]
+        assert_close(to_np64(ys[i]), yr, GEMM_TOL, str(SHAPES[i]))
         assert rel_fro(to_np64(probs[i][6]), tr) < t_save_tol(c.k), SHAPES[i]
+        # the single-problem path keeps bf16_rn(L a') per weight, the grouped path bf16(L) a':
+        # within 2^-8 of each other per weight, far less over a sum
         y1, _ = lib.linear_fwd(c.x, rec, c.a, c.b, c.alpha)
-        assert rel_fro(to_np64(ys[i]), to_np64(y1)) < 1e-2, SHAPES[i]
+        assert rel_fro(to_np64(ys[i]), to_np64(y1)) < 5e-3, SHAPES[i]
 
 
 def test_grouped_rejects_large_token_counts(lib):
@@ -134,3 +141,55 @@ def test_grouped_long_list_one_and_two_tokens(lib):
         wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
         yr, _ = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
         assert rel_fro(to_np64(ys[i]), yr) < GEMM_TOL, shapes[i]
+
+
+def _chain(lib, recs, loras, x0, graph_replays=0):
+    """Dependent calls: call i reads call i-1's output (every matrix is square)."""
+    outs = [torch.empty_like(x0) for _ in recs]
+    steps = []
+    prev = x0
+    for i, rec in enumerate(recs):
+        steps.append(lib.GroupedForward([(prev, rec, loras[i][0], loras[i][1], 32.0, outs[i], None)]))
+        prev = outs[i]
+
+    def run():
+        for g in steps:
+            g.run()
+
+    run()
+    torch.cuda.synchronize()
+    first = [o.clone() for o in outs]
+    if graph_replays:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            run()
+        for _ in range(graph_replays):
+            for o in outs:
+                o.fill_(float("nan"))
+            graph.replay()
+            torch.cuda.synchronize()
+            for a, b in zip(first, outs):
+                assert torch.equal(a, b)
+    return first
+
+
+@pytest.mark.parametrize("m", [1, 4, 16])
+def test_grouped_chain_of_dependent_calls(lib, m):
+    n = 1024
+    layers = 6
+    recs, loras = [], []
+    for i in range(layers):
+        w = synthetic.weight(n, n, device="cuda", seed=3000 + i)
+        recs.append(lib.quantize(w))
+        loras.append(synthetic.lora_pair(n, n, 16, device="cuda", seed=3100 + 2 * i))
+    x0 = synthetic.activations(m, n, device="cuda", seed=3200)
+    outs = _chain(lib, recs, loras, x0, graph_replays=2)
+    lib.check_status()
+    # oracle chain, fed with the GPU's own bf16 inputs at every layer (isolates each call)
+    prev = to_np64(x0)
+    for i in range(layers):
+        ref = nf4.quantize(to_np32(synthetic.weight(n, n, device="cuda", seed=3000 + i).cpu()), n, n)
+        wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, n)
+        yr, _ = linear.lora_forward(prev, wd, to_np64(loras[i][0]), to_np64(loras[i][1]), 32.0, 16)
+        assert_close(to_np64(outs[i]), yr, GEMM_TOL, "layer %d" % i)
+        prev = to_np64(outs[i])
