@@ -18,7 +18,9 @@ launching stream, max over ranks.  Also on the line:
   tokens; ``decode_per_layer`` is the decoder's dependency order, four calls a
   layer), dequantise and quantise GB/s, the Llama-7B MLP block fwd+bwd
   (``mlp_block``) and the 65B-shaped quantise stream + up-projection step
-  (``llama65b``), each with its fraction of the measured roofline.
+  (``llama65b``), each with its fraction of the measured roofline; the
+  merge / export rate, the headline step with LoRA dropout p = 0.05, and one
+  AdamW step over the LoRA matrices of a 32-layer 7B stack.
 
 ``--gpus N`` without a torchrun environment re-launches this script under
 ``torch.distributed.run`` with N ranks on 127.0.0.1 (one replica per GPU); under
@@ -28,10 +30,10 @@ torchrun, ``WORLD_SIZE`` must equal N.
 bounded sample of the same workload and prints the same line with
 ``"impl": "reference"``.
 
-``--only quant [--shape NxK]`` / ``--only decode [--decode-layers L]`` run just
-that secondary measurement (quantise + dequantise of one bf16 weight; the 1-token
-decode sweep) and print its figures -- a small, repeatable workload for
-profilers, not a bench line.
+``--only quant [--shape NxK]`` / ``--only decode [--decode-layers L]
+[--decode-tokens 1,4,16]`` run just that secondary measurement (quantise +
+dequantise of one bf16 weight; the decode sweep) and print its figures -- a
+small, repeatable workload for profilers, not a bench line.
 """
 
 from __future__ import annotations
@@ -463,6 +465,84 @@ def llama65b(q, torch, steps, flush, layers=80, m=4096, r=64, alpha=16.0):
     return out
 
 
+def merge_rate(q, torch, flush, n=4096, k=4096, r=16, alpha=32.0):
+    """Merge / export of the 4096^2 attention projection: bf16(deq(W) + s B A), GB/s of the weight
+    record read and the bf16 weight written (HBM-bound; r float32 FMAs per weight on the CUDA cores)."""
+    import synthetic
+    case = synthetic.linear_case(n, k, 1, r, alpha, device="cuda", base_seed=4)
+    rec = q.quantize(case.w)
+    out = torch.empty((n, k), dtype=torch.bfloat16, device="cuda")
+    for _ in range(3):
+        q.merge(rec, case.a, case.b, alpha, out=out)
+    ms = statistics.median(time_events(torch, lambda: q.merge(rec, case.a, case.b, alpha, out=out), 10, flush))
+    q.check_status()
+    byts = rec.nbytes() + n * k * 2 + case.a.numel() * 2 + case.b.numel() * 2
+    return {"shape": [n, k], "r": r, "ms": ms, "gbs": byts / ms / 1e6, "bytes": byts}
+
+
+def dropout_step(q, torch, steps, flush, p=0.05):
+    """The headline fwd+bwd with LoRA dropout p = 0.05 on the branch input (mask drawn every step)."""
+    import synthetic
+    case = synthetic.linear_case(N_, K_, M_, R_, ALPHA_, device="cuda", base_seed=0)
+    rec = q.quantize(case.w)
+    x, a, b, dy = case.x, case.a, case.b, case.dy
+    mask = torch.empty((M_, K_ // 8), dtype=torch.uint8, device="cuda")
+    y = torch.empty((M_, N_), dtype=torch.bfloat16, device="cuda")
+    xd = torch.empty_like(x)
+    t = torch.empty((M_, R_), dtype=torch.float32, device="cuda")
+    dx = torch.empty((M_, K_), dtype=torch.bfloat16, device="cuda")
+    da = torch.empty((R_, K_), dtype=torch.float32, device="cuda")
+    db = torch.empty((N_, R_), dtype=torch.float32, device="cuda")
+    wsf = torch.empty(max(q.fwd_workspace_bytes(M_, N_, K_, R_), 256), dtype=torch.uint8, device="cuda")
+    wsb = torch.empty(max(q.bwd_workspace_bytes(M_, N_, K_, R_), 256), dtype=torch.uint8, device="cuda")
+
+    def fwd_bwd():
+        q.dropout_mask(7, 11, M_, K_, p, out=mask)
+        q.linear_fwd_dropout(x, rec, a, b, ALPHA_, mask, p, y=y, t_save=t, x_drop=xd, workspace=wsf)
+        q.linear_bwd_dropout(dy, xd, rec, a, b, ALPHA_, mask, p, t, dx=dx, da=da, db=db, workspace=wsb)
+
+    fwd_bwd()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        fwd_bwd()
+    for _ in range(3):
+        flush()
+        graph.replay()
+    ms = statistics.median(time_events(torch, graph.replay, steps, flush))
+    q.check_status()
+    flops = step_flops(M_, N_, K_, R_)
+    return {"p": p, "ms_per_step": ms, "tflops": flops / (ms / 1e3) / 1e12}
+
+
+def adamw_rate(q, torch, layers=32, r=16):
+    """One AdamW step over the LoRA A and B of every linear of a 32-layer Llama-7B stack
+    (448 tensors, 40 M parameters; one launch per 240 tensors)."""
+    import synthetic
+    ts = []
+    for _ in range(layers):
+        for (n, k) in synthetic.LLAMA7B_LAYER:
+            for shape in ((r, k), (n, r)):
+                nel = shape[0] * shape[1]
+                ts.append({"master": torch.randn(nel, device="cuda"), "param": torch.empty(nel, dtype=torch.bfloat16,
+                                                                                           device="cuda"),
+                           "grad": torch.randn(nel, device="cuda") * 1e-3, "exp_avg": torch.zeros(nel, device="cuda"),
+                           "exp_avg_sq": torch.zeros(nel, device="cuda")})
+    params = sum(t["grad"].numel() for t in ts)
+    step = [1]
+
+    def one():
+        q.adamw_step(ts, lr=1e-4, step=step[0])
+        step[0] += 1
+
+    for _ in range(3):
+        one()
+    ms = statistics.median(time_events(torch, one, 10))
+    q.check_status()
+    byts = params * (4 * 4 + 3 * 4 + 2)  # read master, grad, m, v; write master, m, v, bf16 param
+    return {"tensors": len(ts), "params": params, "ms": ms, "gbs": byts / ms / 1e6}
+
+
 def traffic_for(kernel: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it matches the current source."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -644,6 +724,10 @@ def run_ours(args, world, rank, local):
                         "frac_of_hbm": sweep["t%d" % t]["per_layer"]["frac_of_hbm"],
                         "ms_per_pass": sweep["t%d" % t]["per_layer"]["ms_per_pass"]}
             for t in (1, 4, 16) if "t%d" % t in sweep}
+        secondary["merge"] = merge_rate(q, torch, flush)
+        secondary["merge"]["frac_of_hbm"] = secondary["merge"]["gbs"] / peaks["hbm_gbs"]
+        secondary["dropout_step"] = dropout_step(q, torch, args.steps, flush)
+        secondary["adamw"] = adamw_rate(q, torch)
         cs = ClockSampler(local)
         cs.start()
         secondary["mlp_block"] = mlp_block(q, torch, args.steps, flush)
@@ -701,6 +785,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--decode-layers", type=int, default=32)
+    ap.add_argument("--decode-tokens", default="1", help="token counts of --only decode, e.g. 1,4,16")
     ap.add_argument("--only", choices=("quant", "decode"), default=None,
                     help="run one secondary measurement alone (a workload for profilers)")
     ap.add_argument("--shape", default="22016x8192", help="weight shape for --only quant")
@@ -713,7 +798,8 @@ def main(argv=None):
             n, k = (int(v) for v in args.shape.lower().split("x"))
             print(json.dumps(dequant_quant_rates(q, torch, None, n=n, k=k)), flush=True)
         else:
-            print(json.dumps(decode_sweep(q, torch, layers=args.decode_layers, tokens=(1,))), flush=True)
+            toks = tuple(int(t) for t in args.decode_tokens.split(","))
+            print(json.dumps(decode_sweep(q, torch, layers=args.decode_layers, tokens=toks)), flush=True)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -14,20 +14,23 @@
 // preceding kernel of the stream; right after that wait it lets the next
 // kernel launch, which prefetches its own weights while this one computes.
 //
-// Work: the list is cut into units of equal size -- T units (problem, a range
-// of k) that compute partial X A^T, placed first, then W units (problem, tile
-// of 128 rows, 256 k) -- and every CTA (one per SM) takes one contiguous run of
-// units.  A run accumulates the units of one row tile in registers; a tile
-// split between runs leaves float32 partials that the last arriving CTA adds in
-// run order (deterministic).  The tile's finaliser adds the LoRA term with
-// sT = bf16(s T), which the last T unit of the problem publishes; finalisers
-// that get there first wait for it (bounded wait; every CTA of the grid is
-// resident: the grid has at most one CTA per SM and the next kernel can only
-// launch after every CTA of this one has started).
+// Work: first, X A^T is cut into about one k-slice per CTA (slice i on CTA
+// i % grid, the 8 warps splitting its 16-k chunks); the last slice of a
+// problem adds the slices' partials in slice order and publishes
+// sT = bf16(s X A^T).  Then the weights are cut into W units of equal size
+// (problem, tile of 128 rows, 256 k) and every CTA (one per SM) takes one
+// contiguous run of them.  A run accumulates the units of one row tile in
+// registers; a tile split between runs leaves float32 partials that the last
+// arriving CTA adds in run order (deterministic).  The tile's finaliser adds
+// the LoRA term with sT; a finaliser that gets there first waits for it
+// (bounded wait; every CTA of the grid is resident: the grid has at most one
+// CTA per SM and the next kernel can only launch after every CTA of this one
+// has started).
 //
 // A W unit: warp w owns rows 16w .. 16w+15 of the tile; per 64-wide absmax
 // block, lanes stage the 16 rows x 32 code bytes into a shared-memory ring with
-// cp.async (kDcRing blocks ahead), decode them with the byte-permute table of
+// cp.async (kDcRing blocks ahead; the block scales are loaded two blocks
+// ahead, the X fragments before the decode), decode them with the byte-permute table of
 // the bf16 NF4 levels into mma.sync m16n8k16 A fragments (k permuted so lane
 // (g, q) holds k = 16c + 4q .. 4q+3 of chunk c), and multiply with the X
 // fragments (8 tokens per MMA, 1 or 2 groups) into a per-block accumulator,
@@ -56,7 +59,7 @@ constexpr int kDcRing = 6;                 // cp.async ring depth per warp, in b
 constexpr int kDcPitch = 48;               // shared-memory bytes per staged row piece (32 used, padded: no bank conflicts)
 constexpr int kDcStage = 16 * kDcPitch;    // one block of the warp's 16 rows
 constexpr int kDcMaxProbs = 128;
-constexpr int kDcTChunk = 256;             // k per T sub-chunk
+constexpr int kDcPrefetchUnits = 24;       // W units a CTA keeps prefetched into L2 ahead of its consumer
 
 struct DcProb {
   const uint8_t* codes;
@@ -68,15 +71,15 @@ struct DcProb {
   const __nv_bfloat16* b;   // [n, r]
   __nv_bfloat16* y;         // [m, n]
   float* t_save;            // [m, r] or null
-  float* tpart;             // [t_units][16][r] partial X A^T
+  float* tpart;             // [t_slices][16][r] partial X A^T
   __nv_bfloat16* st;        // [16][r] bf16(s T)
   float* ypart;             // [tiles][maxseg][16][128] partial Y
   unsigned long long* cnt;  // [2 + tiles]: T, tiles done, then one per tile
   int n, k, m, r;
   float scale;
-  int t_units, t_sub;       // T units and 256-k sub-chunks per T unit
-  int tiles, ku;            // row tiles, W units per tile (k / 256)
-  int u0_t, u0_w;           // first T unit, first W unit (global unit index)
+  int t_slices, t_w, s0;    // X A^T: slices of t_w 64-wide blocks, first global slice
+  int tiles, ku;            // row tiles, W units per tile (ceil(k / 256))
+  long long u0_w;           // first W unit (global unit index)
 };
 
 struct DcParams {
@@ -84,7 +87,8 @@ struct DcParams {
   int grid;
   int maxseg;
   uint32_t epoch;
-  long long units;            // all units of the call
+  long long units;            // W units of the call
+  int slices;                 // X A^T slices of the call (slice i goes to CTA i % grid)
   unsigned long long wait_ns;
   unsigned* status;
   DcProb prob[kDcMaxProbs];
@@ -142,12 +146,19 @@ __device__ __forceinline__ uint32_t dc_arrive(unsigned long long* c, uint32_t ep
   }
 }
 
-__device__ __forceinline__ int dc_find_prob(const DcParams& p, long long u, bool t_unit) {
+__device__ __forceinline__ int dc_find_prob(const DcParams& p, long long u) {  // problem of W unit u
   int lo = 0, hi = p.count - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    const long long s = t_unit ? p.prob[mid].u0_t : p.prob[mid].u0_w;
-    if (s <= u) lo = mid; else hi = mid - 1;
+    if (p.prob[mid].u0_w <= u) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+__device__ __forceinline__ int dc_find_slice(const DcParams& p, int sl) {  // problem of X A^T slice sl
+  int lo = 0, hi = p.count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.prob[mid].s0 <= sl) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -164,56 +175,54 @@ __device__ __forceinline__ uint2 dc_xfrag(const DcProb& pr, int tok, int kk) {
 template <int NG>
 __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant__ DcParams p) {
   __shared__ __align__(16) uint8_t s_ring[kDcWarps][kDcRing][kDcStage];
+  __shared__ float s_red[kDcWarps][16][16];
   __shared__ int s_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   const long long u_begin = dc_run_start(blockIdx.x, p.units, p.grid);
   const long long u_end = dc_run_start(blockIdx.x + 1, p.units, p.grid);
 
-  // ---------------------------------------------------------------- L2 prefetch of this run's bytes
-  for (long long u = u_begin; u < u_end; ++u) {
-    const bool tu = u < p.prob[0].u0_w;
-    const DcProb& pr = p.prob[dc_find_prob(p, u, tu)];
-    if (tu) {
-      const int k0 = static_cast<int>(u - pr.u0_t) * pr.t_sub * kDcTChunk;
-      const int kn = min(pr.t_sub * kDcTChunk, pr.k - k0);
-      for (int j = threadIdx.x; j < pr.r; j += kDcThreads)
-        prefetch_l2_bulk(pr.a + static_cast<int64_t>(j) * pr.k + k0, static_cast<uint32_t>(kn) * 2);
-    } else {
-      const long long w = u - pr.u0_w;
-      const int tile = static_cast<int>(w / pr.ku), kun = static_cast<int>(w % pr.ku);
-      for (int i = threadIdx.x; i < kDcRows; i += kDcThreads) {
-        const int row = tile * kDcRows + i;
-        if (row < pr.n) {
-          prefetch_l2_bulk(pr.codes + static_cast<int64_t>(row) * (pr.k / 2) + kun * 128, 128);
-          prefetch_l2_line(pr.absq + static_cast<int64_t>(row) * (pr.k / 64) + kun * kDcUnitBlocks);
-        }
+  // ---------------------------------------------------------------- L2 prefetch (before the wait)
+  // the first kDcPrefetchUnits W units of this run (every unit's codes when the call is a decoder
+  // stage; later units of long lists are prefetched as the run advances) and this CTA's T slices
+  for (long long u = u_begin; u < u_end && u < u_begin + kDcPrefetchUnits; ++u) {
+    const DcProb& pr = p.prob[dc_find_prob(p, u)];
+    const long long w = u - pr.u0_w;
+    const int tile = static_cast<int>(w / pr.ku), kun = static_cast<int>(w % pr.ku);
+    const int nb = min(kDcUnitBlocks, pr.k / 64 - kun * kDcUnitBlocks);  // the last unit of a row may be short
+    for (int i = threadIdx.x; i < kDcRows; i += kDcThreads) {
+      const int row = tile * kDcRows + i;
+      if (row < pr.n) {
+        prefetch_l2_bulk(pr.codes + static_cast<int64_t>(row) * (pr.k / 2) + kun * 128, static_cast<uint32_t>(nb) * 32);
+        prefetch_l2_line(pr.absq + static_cast<int64_t>(row) * (pr.k / 64) + kun * kDcUnitBlocks);
       }
     }
+  }
+  for (int sl = blockIdx.x; sl < p.slices; sl += p.grid) {
+    const DcProb& pr = p.prob[dc_find_slice(p, sl)];
+    const int kb0 = (sl - pr.s0) * pr.t_w, kb1 = min(pr.k / 64, kb0 + pr.t_w);
+    for (int j = threadIdx.x; j < pr.r; j += kDcThreads)
+      prefetch_l2_bulk(pr.a + static_cast<int64_t>(j) * pr.k + kb0 * 64, static_cast<uint32_t>(kb1 - kb0) * 128);
   }
   // X, sT, the counters and the workspace may come from earlier kernels of the stream
   griddep_wait();
   griddep_launch_dependents();
 
-  const Nf4Table lv = dc_level_table();
-  bool alive = true;
-
-  // ---------------------------------------------------------------- T units
-  long long u = u_begin;
-  for (; u < u_end && u < p.prob[0].u0_w && alive; ++u) {
-    const int pi = dc_find_prob(p, u, true);
-    const DcProb& pr = p.prob[pi];
-    const int tu = static_cast<int>(u - pr.u0_t);
-    const int k0 = tu * pr.t_sub * kDcTChunk;
-    const int kend = min(pr.k, k0 + pr.t_sub * kDcTChunk);
-    // warp w: LoRA rows j = 16 w .. 16 w + 15 (r <= 128)
-    float acc[NG][4];
+  // ---------------------------------------------------------------- T = X A^T, spread over every CTA
+  // slice sl (problem p, 64-wide blocks [kb0, kb1)) goes to CTA sl % grid; the 8 warps split its
+  // 16-k chunks, the CTA adds their partial sums in warp order into the slice's partial
+  for (int sl = blockIdx.x; sl < p.slices; sl += p.grid) {
+    const DcProb& pr = p.prob[dc_find_slice(p, sl)];
+    const int si = sl - pr.s0;
+    const int kb0 = si * pr.t_w, kb1 = min(pr.k / 64, kb0 + pr.t_w);
+    const int nch = (kb1 - kb0) * 4;
+    for (int jg = 0; jg * 16 < pr.r; ++jg) {
+      float acc[NG][4];
 #pragma unroll
-    for (int t = 0; t < NG; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-    const int j0 = warp * 16 + g, j1 = j0 + 8;
-    if (warp * 16 < pr.r) {
-      for (int kk = k0; kk < kend; kk += 16) {
-        const int kq = kk + 4 * q;
+      for (int t = 0; t < NG; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+      const int j0 = jg * 16 + g, j1 = j0 + 8;
+      for (int ch = warp; ch < nch; ch += kDcWarps) {
+        const int kq = kb0 * 64 + ch * 16 + 4 * q;
         const uint2 a0 = j0 < pr.r ? ldg_nc_v2(pr.a + static_cast<int64_t>(j0) * pr.k + kq) : make_uint2(0u, 0u);
         const uint2 a1 = j1 < pr.r ? ldg_nc_v2(pr.a + static_cast<int64_t>(j1) * pr.k + kq) : make_uint2(0u, 0u);
 #pragma unroll
@@ -222,69 +231,112 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
           dc_mma(acc[t], a0.x, a1.x, a0.y, a1.y, xb.x, xb.y);
         }
       }
-      // d[0] = (row j0, token 2q), d[1] = (j0, 2q+1), d[2] = (j1, 2q), d[3] = (j1, 2q+1)
-      float* part = pr.tpart + static_cast<int64_t>(tu) * 16 * pr.r;
+      // C fragment: d[0] = (row j0, tok 2q), d[1] = (j0, 2q+1), d[2] = (j1, 2q), d[3] = (j1, 2q+1)
 #pragma unroll
       for (int t = 0; t < NG; ++t) {
         const int tk = t * 8 + 2 * q;
-        if (j0 < pr.r) {
-          part[tk * pr.r + j0] = acc[t][0];
-          part[(tk + 1) * pr.r + j0] = acc[t][1];
-        }
-        if (j1 < pr.r) {
-          part[tk * pr.r + j1] = acc[t][2];
-          part[(tk + 1) * pr.r + j1] = acc[t][3];
+        s_red[warp][tk][g] = acc[t][0];
+        s_red[warp][tk + 1][g] = acc[t][1];
+        s_red[warp][tk][g + 8] = acc[t][2];
+        s_red[warp][tk + 1][g + 8] = acc[t][3];
+      }
+      __syncthreads();
+      {
+        const int tok = threadIdx.x >> 4, j = threadIdx.x & 15;  // 256 threads = 16 tokens x 16 j
+        if (tok < NG * 8 && jg * 16 + j < pr.r) {
+          float v = 0.f;
+#pragma unroll
+          for (int w = 0; w < kDcWarps; ++w) v += s_red[w][tok][j];
+          pr.tpart[(static_cast<int64_t>(si) * 16 + tok) * pr.r + jg * 16 + j] = v;
         }
       }
+      __syncthreads();
     }
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_flag = dc_arrive(pr.cnt, p.epoch) == static_cast<uint32_t>(pr.t_units);
+    if (threadIdx.x == 0) s_flag = dc_arrive(pr.cnt, p.epoch) == static_cast<uint32_t>(pr.t_slices);
     __syncthreads();
     if (s_flag) {
-      // last T unit of the problem: T = sum of the partials in unit order -> t_save, sT
+      // last slice of the problem: T = the slices' partials added in slice order -> t_save, sT
       __threadfence();
       for (int i = threadIdx.x; i < 16 * pr.r; i += kDcThreads) {
         const int tok = i / pr.r, j = i % pr.r;
         float v = 0.f;
-        for (int c = 0; c < pr.t_units; ++c) v += __ldcg(pr.tpart + (static_cast<int64_t>(c) * 16 + tok) * pr.r + j);
+        if (tok < pr.m)
+          for (int c = 0; c < pr.t_slices; ++c) v += __ldcg(pr.tpart + (static_cast<int64_t>(c) * 16 + tok) * pr.r + j);
         if (tok < pr.m && pr.t_save) pr.t_save[tok * pr.r + j] = v;
         pr.st[tok * pr.r + j] = __float2bfloat16_rn(tok < pr.m ? __fmul_rn(v, pr.scale) : 0.f);
       }
       __threadfence();
       __syncthreads();
-      if (threadIdx.x == 0) atomicAdd(pr.cnt, 1ull);  // count = t_units + 1: sT published
+      if (threadIdx.x == 0) atomicAdd(pr.cnt, 1ull);  // count = t_slices + 1: sT published
     }
     __syncthreads();
   }
 
   // ---------------------------------------------------------------- W units
-  if (u >= u_end || !alive) return;
-  // the run's (problem, tile, block) steps, walked twice: by the cp.async producer (ahead) and the consumer
+  if (u_begin >= u_end) return;
+  // the run's (problem, tile, block) steps, walked by three cursors: the cp.async stager (kDcRing - 1
+  // blocks ahead), the block-scale loader (2 ahead) and the consumer
   struct Cursor {
     long long u;
     int kb;  // block within the unit
+    int nb;  // blocks in the unit (the last unit of a row may hold fewer than kDcUnitBlocks)
+    int pi, tile, kun;
+  };
+  auto enter = [&](Cursor& c) {  // describe unit c.u
+    if (c.u >= u_end) return;
+    c.pi = dc_find_prob(p, c.u);
+    const DcProb& pr = p.prob[c.pi];
+    const long long w = c.u - pr.u0_w;
+    c.tile = static_cast<int>(w / pr.ku);
+    c.kun = static_cast<int>(w % pr.ku);
+    c.nb = min(kDcUnitBlocks, pr.k / 64 - c.kun * kDcUnitBlocks);
+  };
+  auto advance = [&](Cursor& c) {
+    if (++c.kb == c.nb) {
+      c.kb = 0;
+      ++c.u;
+      enter(c);
+    }
   };
   const uint32_t ring0 = smem_u32(&s_ring[warp][0][0]);
-  // stage block step `cur` of this warp's 16 rows into ring slot `slot`
-  auto stage = [&](const Cursor& cur, int slot) {
-    const int pi = dc_find_prob(p, cur.u, false);
-    const DcProb& pr = p.prob[pi];
-    const long long w = cur.u - pr.u0_w;
-    const int tile = static_cast<int>(w / pr.ku), kun = static_cast<int>(w % pr.ku);
-    const int row = tile * kDcRows + warp * 16 + (lane >> 1);
-    const int kb = kun * kDcUnitBlocks + cur.kb;
+  // stage block step `c` of this warp's 16 rows into ring slot `slot`
+  auto stage = [&](const Cursor& c, int slot) {
+    const DcProb& pr = p.prob[c.pi];
+    const int row = c.tile * kDcRows + warp * 16 + (lane >> 1);
+    const int kb = c.kun * kDcUnitBlocks + c.kb;
     const bool ok = row < pr.n;
     const uint8_t* src = pr.codes + (ok ? static_cast<int64_t>(row) * (pr.k / 2) + kb * 32 + (lane & 1) * 16 : 0);
     cp_async16(ring0 + slot * kDcStage + (lane >> 1) * kDcPitch + (lane & 1) * 16, src, ok);
   };
-  auto advance = [&](Cursor& cur) {
-    if (++cur.kb == kDcUnitBlocks) {
-      cur.kb = 0;
-      ++cur.u;
-    }
+  // raw block scales of rows g, g+8 for block step `c`
+  struct Scales {
+    int q0, q1;
+    float s0, s1, mu;
   };
-  Cursor pre{u, 0};
+  auto load_scales = [&](const Cursor& c) {
+    Scales sc{0, 0, 0.f, 0.f, 0.f};
+    if (c.u >= u_end) return sc;
+    const DcProb& pr = p.prob[c.pi];
+    const int kbr = pr.k / 64, kb = c.kun * kDcUnitBlocks + c.kb;
+    const int r0 = c.tile * kDcRows + warp * 16 + g, r1 = r0 + 8;
+    sc.mu = __ldg(pr.mean);
+    if (r0 < pr.n) {
+      const int64_t bi = static_cast<int64_t>(r0) * kbr + kb;
+      sc.q0 = __ldg(pr.absq + bi);
+      sc.s0 = __ldg(pr.step + (bi >> 8));
+    }
+    if (r1 < pr.n) {
+      const int64_t bi = static_cast<int64_t>(r1) * kbr + kb;
+      sc.q1 = __ldg(pr.absq + bi);
+      sc.s1 = __ldg(pr.step + (bi >> 8));
+    }
+    return sc;
+  };
+
+  Cursor pre{u_begin, 0, 0, 0, 0, 0};
+  enter(pre);
   int issued = 0;
   for (; issued < kDcRing - 1; ++issued) {
     if (pre.u < u_end) {
@@ -293,6 +345,13 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
     }
     cp_async_commit();
   }
+  Cursor cur{u_begin, 0, 0, 0, 0, 0};
+  enter(cur);
+  Cursor scl = cur;
+  Scales sq0 = load_scales(scl);
+  advance(scl);
+  Scales sq1 = load_scales(scl);
+  advance(scl);
 
   float run[NG][4];
   auto zero_run = [&]() {
@@ -301,10 +360,11 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
   };
   zero_run();
   int cur_pi = -1, cur_tile = -1;
-  long long seg_first = u;  // first unit of the current segment
+  bool alive = true;
 
-  // Finish the segment of tile (pi, tile) that ends at unit `seg_last`.
-  auto flush = [&](int pi, int tile, long long seg_last) {
+  // Finish this run's segment of tile (pi, tile): add the segments' partials when the tile is
+  // split between runs (the last arriving run does it), then the LoRA term, then write y.
+  auto flush = [&](int pi, int tile) {
     const DcProb& pr = p.prob[pi];
     const long long tu0 = pr.u0_w + static_cast<long long>(tile) * pr.ku;  // first unit of the tile
     const long long tu1 = tu0 + pr.ku - 1;
@@ -347,6 +407,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
             vals[t][3] += __ldcg(ps + (tk + 1) * kDcRows + rr + 8);
           }
         }
+        __syncthreads();
         if (threadIdx.x == 0) *reinterpret_cast<volatile unsigned long long*>(pr.cnt + 2 + tile) =
             static_cast<unsigned long long>(p.epoch) << 32;
       }
@@ -356,11 +417,10 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
 #pragma unroll
         for (int e = 0; e < 4; ++e) vals[t][e] = run[t][e];
     }
-    (void)seg_last;
     if (!finalise) return;
-    // wait until the problem's sT is published (count t_units + 1)
+    // wait until the problem's sT is published (count t_slices + 1)
     if (threadIdx.x == 0) {
-      const unsigned long long want = (static_cast<unsigned long long>(p.epoch) << 32) | (pr.t_units + 1u);
+      const unsigned long long want = (static_cast<unsigned long long>(p.epoch) << 32) | (pr.t_slices + 1u);
       bool ok = *reinterpret_cast<volatile unsigned long long*>(pr.cnt) == want;
       if (!ok) {
         const uint64_t t0 = globaltimer_ns();
@@ -389,12 +449,10 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
         for (int e = 0; e < 2; ++e) {
           const int tok = t * 8 + 2 * q + e;
           if (tok >= pr.m) continue;
-          float v = vals[t][2 * h + e];
           const __nv_bfloat16* srow = pr.st + tok * pr.r;
           float l = 0.f;
-          for (int j = 0; j < pr.r; ++j)
-            l = fmaf(__bfloat162float(__ldcg(srow + j)), __bfloat162float(brow[j]), l);
-          pr.y[static_cast<int64_t>(tok) * pr.n + row] = __float2bfloat16_rn(v + l);
+          for (int j = 0; j < pr.r; ++j) l = fmaf(__bfloat162float(__ldcg(srow + j)), __bfloat162float(brow[j]), l);
+          pr.y[static_cast<int64_t>(tok) * pr.n + row] = __float2bfloat16_rn(vals[t][2 * h + e] + l);
         }
       }
     }
@@ -406,24 +464,39 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
     }
   };
 
-  Cursor cur{u, 0};
+  const Nf4Table lv = dc_level_table();
   const uint32_t pick = (q & 1) ? 0x7632u : 0x5410u;  // the two code bytes of chunk c in the 32-bit word
   float blk[NG][4];
   while (cur.u < u_end && alive) {
-    const int pi = dc_find_prob(p, cur.u, false);
-    const DcProb& pr = p.prob[pi];
-    const long long w = cur.u - pr.u0_w;
-    const int tile = static_cast<int>(w / pr.ku), kun = static_cast<int>(w % pr.ku);
-    if (pi != cur_pi || tile != cur_tile) {
+    const DcProb& pr = p.prob[cur.pi];
+    if (cur.pi != cur_pi || cur.tile != cur_tile) {
       if (cur_pi >= 0) {
-        flush(cur_pi, cur_tile, cur.u - 1);
+        flush(cur_pi, cur_tile);
         if (!alive) break;
       }
-      cur_pi = pi;
-      cur_tile = tile;
-      seg_first = cur.u;
+      cur_pi = cur.pi;
+      cur_tile = cur.tile;
       zero_run();
     }
+    if (cur.kb == 0 && cur.u + kDcPrefetchUnits < u_end && lane < 16) {
+      // keep the L2 stream kDcPrefetchUnits units ahead of the consumer (long runs)
+      Cursor f{cur.u + kDcPrefetchUnits, 0, 0, 0, 0, 0};
+      enter(f);
+      const DcProb& pf = p.prob[f.pi];
+      const int row = f.tile * kDcRows + warp * 16 + lane;
+      if (row < pf.n)
+        prefetch_l2_bulk(pf.codes + static_cast<int64_t>(row) * (pf.k / 2) + f.kun * 128, static_cast<uint32_t>(f.nb) * 32);
+    }
+    // X fragments of the 4 chunks of this block (issued before the decode)
+    const int kbase = (cur.kun * kDcUnitBlocks + cur.kb) * 64;
+    uint2 xf[4][NG];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int t = 0; t < NG; ++t) xf[c][t] = dc_xfrag(pr, t * 8 + g, kbase + 16 * c + 4 * q);
+    // scales two blocks ahead
+    const Scales sq2 = load_scales(scl);
+    advance(scl);
     // keep the ring kDcRing - 1 blocks ahead
     if (pre.u < u_end) {
       stage(pre, issued % kDcRing);
@@ -434,20 +507,6 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
     cp_async_wait<kDcRing - 1>();
     __syncwarp();
     const int slot = (issued - kDcRing) % kDcRing;
-    const int kb = kun * kDcUnitBlocks + cur.kb;
-    const int row0 = tile * kDcRows + warp * 16 + g, row1 = row0 + 8;
-    const int kbr = pr.k / 64;
-    // restored block scales of rows g, g + 8
-    const float mu = *pr.mean;
-    float a2[2] = {0.f, 0.f};
-    if (row0 < pr.n) {
-      const int64_t bi = static_cast<int64_t>(row0) * kbr + kb;
-      a2[0] = restore_absmax(pr.absq[bi], pr.step[bi >> 8], mu);
-    }
-    if (row1 < pr.n) {
-      const int64_t bi = static_cast<int64_t>(row1) * kbr + kb;
-      a2[1] = restore_absmax(pr.absq[bi], pr.step[bi >> 8], mu);
-    }
     const uint8_t* st0 = &s_ring[warp][slot][0];
     const uint4 c0a = *reinterpret_cast<const uint4*>(st0 + g * kDcPitch);
     const uint4 c0b = *reinterpret_cast<const uint4*>(st0 + g * kDcPitch + 16);
@@ -459,7 +518,6 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
     const uint32_t r1w[8] = {c1a.x, c1a.y, c1a.z, c1a.w, c1b.x, c1b.y, c1b.z, c1b.w};
 #pragma unroll
     for (int t = 0; t < NG; ++t) blk[t][0] = blk[t][1] = blk[t][2] = blk[t][3] = 0.f;
-    const int kbase = kb * 64;
 #pragma unroll
     for (int cp = 0; cp < 2; ++cp) {  // chunk pairs (0,1), (2,3)
       const int wi = 4 * cp + (q >> 1);
@@ -471,27 +529,27 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int c = 2 * cp + h;
-        const int kq = kbase + 16 * c + 4 * q;
 #pragma unroll
-        for (int t = 0; t < NG; ++t) {
-          const uint2 xb = dc_xfrag(pr, t * 8 + g, kq);
-          dc_mma(blk[t], d0[2 * h], d1[2 * h], d0[2 * h + 1], d1[2 * h + 1], xb.x, xb.y);
-        }
+        for (int t = 0; t < NG; ++t)
+          dc_mma(blk[t], d0[2 * h], d1[2 * h], d0[2 * h + 1], d1[2 * h + 1], xf[c][t].x, xf[c][t].y);
       }
     }
+    const float a20 = restore_absmax(static_cast<int8_t>(sq0.q0), sq0.s0, sq0.mu);
+    const float a21 = restore_absmax(static_cast<int8_t>(sq0.q1), sq0.s1, sq0.mu);
 #pragma unroll
     for (int t = 0; t < NG; ++t) {
-      run[t][0] = fmaf(a2[0], blk[t][0], run[t][0]);
-      run[t][1] = fmaf(a2[0], blk[t][1], run[t][1]);
-      run[t][2] = fmaf(a2[1], blk[t][2], run[t][2]);
-      run[t][3] = fmaf(a2[1], blk[t][3], run[t][3]);
+      run[t][0] = fmaf(a20, blk[t][0], run[t][0]);
+      run[t][1] = fmaf(a20, blk[t][1], run[t][1]);
+      run[t][2] = fmaf(a21, blk[t][2], run[t][2]);
+      run[t][3] = fmaf(a21, blk[t][3], run[t][3]);
     }
+    sq0 = sq1;
+    sq1 = sq2;
     __syncwarp();  // the slot is refilled by a later stage()
     advance(cur);
   }
   cp_async_wait<0>();
-  if (cur_pi >= 0 && alive) flush(cur_pi, cur_tile, cur.u - 1);
-  (void)seg_first;
+  if (cur_pi >= 0 && alive) flush(cur_pi, cur_tile);
 }
 
 // ---------------------------------------------------------------------------- host
@@ -499,42 +557,50 @@ int decode_max_problems() { return kDcMaxProbs; }
 
 namespace {
 struct DcPlan {
-  int grid, maxseg;
+  int grid, maxseg, slices;
   long long units;
   size_t ws_bytes;
   std::vector<size_t> off_cnt, off_tpart, off_st, off_ypart;
-  std::vector<int> t_units, t_sub, tiles, ku, u0_t, u0_w;
+  std::vector<int> t_slices, t_w, s0, tiles, ku;
+  std::vector<long long> u0_w;
 };
 
 size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
 DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
   DcPlan pl;
-  pl.grid = num_sms > 0 ? num_sms : 1;
-  pl.t_units.resize(count);
-  pl.t_sub.resize(count);
+  const int sms = num_sms > 0 ? num_sms : 1;
+  pl.t_slices.resize(count);
+  pl.t_w.resize(count);
+  pl.s0.resize(count);
   pl.tiles.resize(count);
   pl.ku.resize(count);
-  pl.u0_t.resize(count);
   pl.u0_w.resize(count);
+  // W units
   long long u = 0;
-  for (int i = 0; i < count; ++i) {
-    const int kc = static_cast<int>(probs[i].w.k / kDcTChunk);  // k % 64 == 0, k >= 64
-    const int kchunks = kc > 0 ? kc : 1;
-    pl.t_sub[i] = (kchunks + 7) / 8;  // about 8 T units per problem
-    pl.t_units[i] = (kchunks + pl.t_sub[i] - 1) / pl.t_sub[i];
-    if (static_cast<long long>(pl.t_units[i]) * pl.t_sub[i] * kDcTChunk < probs[i].w.k) ++pl.t_units[i];
-    pl.u0_t[i] = static_cast<int>(u);
-    u += pl.t_units[i];
-  }
   for (int i = 0; i < count; ++i) {
     pl.tiles[i] = static_cast<int>((probs[i].w.n + kDcRows - 1) / kDcRows);
     pl.ku[i] = static_cast<int>((probs[i].w.k + 255) / 256);
-    pl.u0_w[i] = static_cast<int>(u);
+    pl.u0_w[i] = u;
     u += static_cast<long long>(pl.tiles[i]) * pl.ku[i];
   }
   pl.units = u;
-  if (pl.grid > u) pl.grid = static_cast<int>(u);
+  pl.grid = static_cast<int>(u < sms ? u : sms);
+  // X A^T slices: about one per CTA over the whole list, in proportion to each problem's r k
+  double work = 0.0;
+  for (int i = 0; i < count; ++i) work += static_cast<double>((probs[i].r + 15) / 16) * probs[i].w.k;
+  int sl = 0;
+  for (int i = 0; i < count; ++i) {
+    const int blocks = static_cast<int>(probs[i].w.k / 64);
+    const double share = static_cast<double>((probs[i].r + 15) / 16) * probs[i].w.k / work;
+    int want = static_cast<int>(share * pl.grid + 0.5);
+    want = want < 1 ? 1 : (want > blocks ? blocks : want);
+    pl.t_w[i] = (blocks + want - 1) / want;
+    pl.t_slices[i] = (blocks + pl.t_w[i] - 1) / pl.t_w[i];
+    pl.s0[i] = sl;
+    sl += pl.t_slices[i];
+  }
+  pl.slices = sl;
   // the most runs any tile is split over
   auto cta_of = [&](long long uu) { return static_cast<int>(((uu + 1) * pl.grid - 1) / pl.units); };
   pl.maxseg = 1;
@@ -553,7 +619,7 @@ DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
     pl.off_cnt[i] = off;
     off += al256(static_cast<size_t>(2 + pl.tiles[i]) * 8);
     pl.off_tpart[i] = off;
-    off += al256(static_cast<size_t>(pl.t_units[i]) * 16 * probs[i].r * 4);
+    off += al256(static_cast<size_t>(pl.t_slices[i]) * 16 * probs[i].r * 4);
     pl.off_st[i] = off;
     off += al256(static_cast<size_t>(16) * probs[i].r * 2);
     pl.off_ypart[i] = off;
@@ -580,6 +646,7 @@ cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, uint
   prm.maxseg = pl.maxseg;
   prm.epoch = epoch;
   prm.units = pl.units;
+  prm.slices = pl.slices;
   prm.wait_ns = wait_ns;
   prm.status = status;
   int mmax = 1;
@@ -605,11 +672,11 @@ cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, uint
     d.m = g.m;
     d.r = g.r;
     d.scale = g.alpha / static_cast<float>(g.r);
-    d.t_units = pl.t_units[i];
-    d.t_sub = pl.t_sub[i];
+    d.t_slices = pl.t_slices[i];
+    d.t_w = pl.t_w[i];
+    d.s0 = pl.s0[i];
     d.tiles = pl.tiles[i];
     d.ku = pl.ku[i];
-    d.u0_t = pl.u0_t[i];
     d.u0_w = pl.u0_w[i];
     if (g.m > mmax) mmax = g.m;
   }
