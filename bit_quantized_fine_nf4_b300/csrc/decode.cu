@@ -310,29 +310,35 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
     const uint8_t* src = pr.codes + (ok ? static_cast<int64_t>(row) * (pr.k / 2) + kb * 32 + (lane & 1) * 16 : 0);
     cp_async16(ring0 + slot * kDcStage + (lane >> 1) * kDcPitch + (lane & 1) * 16, src, ok);
   };
-  // raw block scales of rows g, g+8 for block step `c`
+  // raw block scales of rows g, g+8 for the (up to 4) blocks of unit `c`, loaded a whole unit
+  // before they are used (so the loads are long complete when the registers are reused)
   struct Scales {
-    int q0, q1;
-    float s0, s1, mu;
+    int q0[kDcUnitBlocks], q1[kDcUnitBlocks];
+    float s0[kDcUnitBlocks], s1[kDcUnitBlocks];
+    float mu;
   };
-  auto load_scales = [&](const Cursor& c) {
-    Scales sc{0, 0, 0.f, 0.f, 0.f};
-    if (c.u >= u_end) return sc;
+  auto load_scales = [&](const Cursor& c, Scales& sc) {
+    if (c.u >= u_end) return;
     const DcProb& pr = p.prob[c.pi];
-    const int kbr = pr.k / 64, kb = c.kun * kDcUnitBlocks + c.kb;
+    const int kbr = pr.k / 64;
     const int r0 = c.tile * kDcRows + warp * 16 + g, r1 = r0 + 8;
     sc.mu = __ldg(pr.mean);
-    if (r0 < pr.n) {
-      const int64_t bi = static_cast<int64_t>(r0) * kbr + kb;
-      sc.q0 = __ldg(pr.absq + bi);
-      sc.s0 = __ldg(pr.step + (bi >> 8));
+#pragma unroll
+    for (int b = 0; b < kDcUnitBlocks; ++b) {
+      const int kb = c.kun * kDcUnitBlocks + b;
+      sc.q0[b] = sc.q1[b] = 0;
+      sc.s0[b] = sc.s1[b] = 0.f;
+      if (b < c.nb && r0 < pr.n) {
+        const int64_t bi = static_cast<int64_t>(r0) * kbr + kb;
+        sc.q0[b] = __ldg(pr.absq + bi);
+        sc.s0[b] = __ldg(pr.step + (bi >> 8));
+      }
+      if (b < c.nb && r1 < pr.n) {
+        const int64_t bi = static_cast<int64_t>(r1) * kbr + kb;
+        sc.q1[b] = __ldg(pr.absq + bi);
+        sc.s1[b] = __ldg(pr.step + (bi >> 8));
+      }
     }
-    if (r1 < pr.n) {
-      const int64_t bi = static_cast<int64_t>(r1) * kbr + kb;
-      sc.q1 = __ldg(pr.absq + bi);
-      sc.s1 = __ldg(pr.step + (bi >> 8));
-    }
-    return sc;
   };
 
   Cursor pre{u_begin, 0, 0, 0, 0, 0};
@@ -347,11 +353,8 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
   }
   Cursor cur{u_begin, 0, 0, 0, 0, 0};
   enter(cur);
-  Cursor scl = cur;
-  Scales sq0 = load_scales(scl);
-  advance(scl);
-  Scales sq1 = load_scales(scl);
-  advance(scl);
+  Scales sc_cur, sc_nxt;
+  load_scales(cur, sc_cur);
 
   float run[NG][4];
   auto zero_run = [&]() {
@@ -478,8 +481,11 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
       cur_tile = cur.tile;
       zero_run();
     }
-    if (cur.kb == 0 && cur.u + kDcPrefetchUnits < u_end && lane < 16) {
-      // keep the L2 stream kDcPrefetchUnits units ahead of the consumer (long runs)
+    // the next unit's block scales, and its L2 prefetch kDcPrefetchUnits units ahead (long runs)
+    Cursor nx{cur.u + 1, 0, 0, 0, 0, 0};
+    enter(nx);
+    load_scales(nx, sc_nxt);
+    if (cur.u + kDcPrefetchUnits < u_end && lane < 16) {
       Cursor f{cur.u + kDcPrefetchUnits, 0, 0, 0, 0, 0};
       enter(f);
       const DcProb& pf = p.prob[f.pi];
@@ -487,66 +493,68 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
       if (row < pf.n)
         prefetch_l2_bulk(pf.codes + static_cast<int64_t>(row) * (pf.k / 2) + f.kun * 128, static_cast<uint32_t>(f.nb) * 32);
     }
-    // X fragments of the 4 chunks of this block (issued before the decode)
-    const int kbase = (cur.kun * kDcUnitBlocks + cur.kb) * 64;
-    uint2 xf[4][NG];
+    const int nb = cur.nb;
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int b = 0; b < kDcUnitBlocks; ++b) {
+      if (b >= nb) break;
+      // X fragments of the 4 chunks of this block (issued before the decode)
+      const int kbase = (cur.kun * kDcUnitBlocks + b) * 64;
+      uint2 xf[4][NG];
 #pragma unroll
-      for (int t = 0; t < NG; ++t) xf[c][t] = dc_xfrag(pr, t * 8 + g, kbase + 16 * c + 4 * q);
-    // scales two blocks ahead
-    const Scales sq2 = load_scales(scl);
-    advance(scl);
-    // keep the ring kDcRing - 1 blocks ahead
-    if (pre.u < u_end) {
-      stage(pre, issued % kDcRing);
-      advance(pre);
-    }
-    cp_async_commit();
-    ++issued;
-    cp_async_wait<kDcRing - 1>();
-    __syncwarp();
-    const int slot = (issued - kDcRing) % kDcRing;
-    const uint8_t* st0 = &s_ring[warp][slot][0];
-    const uint4 c0a = *reinterpret_cast<const uint4*>(st0 + g * kDcPitch);
-    const uint4 c0b = *reinterpret_cast<const uint4*>(st0 + g * kDcPitch + 16);
-    const uint4 c1a = *reinterpret_cast<const uint4*>(st0 + (g + 8) * kDcPitch);
-    const uint4 c1b = *reinterpret_cast<const uint4*>(st0 + (g + 8) * kDcPitch + 16);
-    // chunk c (16 k) uses code bytes 8c + 2q, 8c + 2q + 1 of the 32-byte block; a word of
-    // chunks (c, c+1) = bytes (8c + 2q, +1, 8c + 8 + 2q, +1)
-    const uint32_t r0w[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
-    const uint32_t r1w[8] = {c1a.x, c1a.y, c1a.z, c1a.w, c1b.x, c1b.y, c1b.z, c1b.w};
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-    for (int t = 0; t < NG; ++t) blk[t][0] = blk[t][1] = blk[t][2] = blk[t][3] = 0.f;
-#pragma unroll
-    for (int cp = 0; cp < 2; ++cp) {  // chunk pairs (0,1), (2,3)
-      const int wi = 4 * cp + (q >> 1);
-      const uint32_t w0 = prmt(r0w[wi], r0w[wi + 2], pick);
-      const uint32_t w1 = prmt(r1w[wi], r1w[wi + 2], pick);
-      uint32_t d0[4], d1[4];
-      nf4_decode_word(lv, w0, d0);
-      nf4_decode_word(lv, w1, d1);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int c = 2 * cp + h;
-#pragma unroll
-        for (int t = 0; t < NG; ++t)
-          dc_mma(blk[t], d0[2 * h], d1[2 * h], d0[2 * h + 1], d1[2 * h + 1], xf[c][t].x, xf[c][t].y);
+        for (int t = 0; t < NG; ++t) xf[c][t] = dc_xfrag(pr, t * 8 + g, kbase + 16 * c + 4 * q);
+      // keep the ring kDcRing - 1 blocks ahead
+      if (pre.u < u_end) {
+        stage(pre, issued % kDcRing);
+        advance(pre);
       }
-    }
-    const float a20 = restore_absmax(static_cast<int8_t>(sq0.q0), sq0.s0, sq0.mu);
-    const float a21 = restore_absmax(static_cast<int8_t>(sq0.q1), sq0.s1, sq0.mu);
+      cp_async_commit();
+      ++issued;
+      cp_async_wait<kDcRing - 1>();
+      __syncwarp();
+      const int slot = (issued - kDcRing) % kDcRing;
+      const uint8_t* st0 = &s_ring[warp][slot][0];
+      const uint4 c0a = *reinterpret_cast<const uint4*>(st0 + g * kDcPitch);
+      const uint4 c0b = *reinterpret_cast<const uint4*>(st0 + g * kDcPitch + 16);
+      const uint4 c1a = *reinterpret_cast<const uint4*>(st0 + (g + 8) * kDcPitch);
+      const uint4 c1b = *reinterpret_cast<const uint4*>(st0 + (g + 8) * kDcPitch + 16);
+      // chunk c (16 k) uses code bytes 8c + 2q, 8c + 2q + 1 of the 32-byte block; a word of
+      // chunks (c, c+1) = bytes (8c + 2q, +1, 8c + 8 + 2q, +1)
+      const uint32_t r0w[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
+      const uint32_t r1w[8] = {c1a.x, c1a.y, c1a.z, c1a.w, c1b.x, c1b.y, c1b.z, c1b.w};
 #pragma unroll
-    for (int t = 0; t < NG; ++t) {
-      run[t][0] = fmaf(a20, blk[t][0], run[t][0]);
-      run[t][1] = fmaf(a20, blk[t][1], run[t][1]);
-      run[t][2] = fmaf(a21, blk[t][2], run[t][2]);
-      run[t][3] = fmaf(a21, blk[t][3], run[t][3]);
+      for (int t = 0; t < NG; ++t) blk[t][0] = blk[t][1] = blk[t][2] = blk[t][3] = 0.f;
+#pragma unroll
+      for (int cp = 0; cp < 2; ++cp) {  // chunk pairs (0,1), (2,3)
+        // words 4cp + q/2 and 4cp + 2 + q/2, chosen with static indices (no local memory)
+        const bool hq = (q >> 1) != 0;
+        const uint32_t w0 = prmt(hq ? r0w[4 * cp + 1] : r0w[4 * cp], hq ? r0w[4 * cp + 3] : r0w[4 * cp + 2], pick);
+        const uint32_t w1 = prmt(hq ? r1w[4 * cp + 1] : r1w[4 * cp], hq ? r1w[4 * cp + 3] : r1w[4 * cp + 2], pick);
+        uint32_t d0[4], d1[4];
+        nf4_decode_word(lv, w0, d0);
+        nf4_decode_word(lv, w1, d1);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = 2 * cp + h;
+#pragma unroll
+          for (int t = 0; t < NG; ++t)
+            dc_mma(blk[t], d0[2 * h], d1[2 * h], d0[2 * h + 1], d1[2 * h + 1], xf[c][t].x, xf[c][t].y);
+        }
+      }
+      const float a20 = restore_absmax(static_cast<int8_t>(sc_cur.q0[b]), sc_cur.s0[b], sc_cur.mu);
+      const float a21 = restore_absmax(static_cast<int8_t>(sc_cur.q1[b]), sc_cur.s1[b], sc_cur.mu);
+#pragma unroll
+      for (int t = 0; t < NG; ++t) {
+        run[t][0] = fmaf(a20, blk[t][0], run[t][0]);
+        run[t][1] = fmaf(a20, blk[t][1], run[t][1]);
+        run[t][2] = fmaf(a21, blk[t][2], run[t][2]);
+        run[t][3] = fmaf(a21, blk[t][3], run[t][3]);
+      }
+      __syncwarp();  // the slot is refilled by a later stage()
     }
-    sq0 = sq1;
-    sq1 = sq2;
-    __syncwarp();  // the slot is refilled by a later stage()
-    advance(cur);
+    sc_cur = sc_nxt;
+    cur = nx;
   }
   cp_async_wait<0>();
   if (cur_pi >= 0 && alive) flush(cur_pi, cur_tile);
