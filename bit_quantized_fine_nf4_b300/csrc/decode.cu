@@ -166,6 +166,21 @@ __device__ __forceinline__ int dc_find_slice(const DcParams& p, int sl) {  // pr
 // The bf16 NF4 levels as byte planes for nf4_decode_word (scale 1).
 __device__ __forceinline__ Nf4Table dc_level_table() { return nf4_table(1.0f); }
 
+// Four bf16 values row[j .. j+3] of a row of length r (zero past r) as two bf16x2 words.
+// `readonly`: the row is not written during the kernel (non-coherent path); otherwise it is read
+// through L2 (sT, written by another CTA of this grid).
+__device__ __forceinline__ uint2 dc_ld_bf16x4(const __nv_bfloat16* row, int j, int r, bool readonly) {
+  if ((r & 3) == 0 && j + 4 <= r) {  // 8-byte aligned: rows of r % 4 == 0 values, j % 4 == 0
+    if (readonly) return ldg_nc_v2(row + j);
+    return __ldcg(reinterpret_cast<const uint2*>(row + j));
+  }
+  const unsigned short* u = reinterpret_cast<const unsigned short*>(row);
+  uint32_t v[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) v[e] = j + e < r ? (readonly ? __ldg(u + j + e) : __ldcg(u + j + e)) : 0u;
+  return make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
+}
+
 // X fragment of chunk c (16 k at k0 + 16 c) for token group tg: b0 = X[tok][k + 4q .. +1], b1 = X[tok][k + 4q + 2 .. +3].
 __device__ __forceinline__ uint2 dc_xfrag(const DcProb& pr, int tok, int kk) {
   if (tok >= pr.m) return make_uint2(0u, 0u);
@@ -262,8 +277,20 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
       for (int i = threadIdx.x; i < 16 * pr.r; i += kDcThreads) {
         const int tok = i / pr.r, j = i % pr.r;
         float v = 0.f;
-        if (tok < pr.m)
-          for (int c = 0; c < pr.t_slices; ++c) v += __ldcg(pr.tpart + (static_cast<int64_t>(c) * 16 + tok) * pr.r + j);
+        if (tok < pr.m) {
+          // slice order, eight loads in flight at a time
+          const float* src = pr.tpart + static_cast<int64_t>(tok) * pr.r + j;
+          const int64_t stride = static_cast<int64_t>(16) * pr.r;
+          int c = 0;
+          for (; c + 8 <= pr.t_slices; c += 8) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = __ldcg(src + (c + e) * stride);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v += x[e];
+          }
+          for (; c < pr.t_slices; ++c) v += __ldcg(src + c * stride);
+        }
         if (tok < pr.m && pr.t_save) pr.t_save[tok * pr.r + j] = v;
         pr.st[tok * pr.r + j] = __float2bfloat16_rn(tok < pr.m ? __fmul_rn(v, pr.scale) : 0.f);
       }
@@ -439,25 +466,34 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
     __syncthreads();
     if (!s_flag) { alive = false; return; }
     __threadfence();
-    // y = vals + sum_j sT[tok][j] B[row][j]
-    const int rows[2] = {rbase + g, rbase + g + 8};
+    // y = vals + sT B^T: the LoRA up-projection as extra 16-wide k chunks of the same MMA
+    // (A = rows of B, k = j; B operand = sT [tok][j]), accumulated in float32
+    const int row0 = rbase + g, row1 = row0 + 8;
+    for (int j0 = 0; j0 < pr.r; j0 += 16) {
+      const int jq = j0 + 4 * q;
+      const uint2 b0 = row0 < pr.n ? dc_ld_bf16x4(pr.b + static_cast<int64_t>(row0) * pr.r, jq, pr.r, true)
+                                   : make_uint2(0u, 0u);
+      const uint2 b1 = row1 < pr.n ? dc_ld_bf16x4(pr.b + static_cast<int64_t>(row1) * pr.r, jq, pr.r, true)
+                                   : make_uint2(0u, 0u);
+#pragma unroll
+      for (int t = 0; t < NG; ++t) {
+        const int tok = t * 8 + g;
+        const uint2 sb = tok < pr.m ? dc_ld_bf16x4(pr.st + tok * pr.r, jq, pr.r, false) : make_uint2(0u, 0u);
+        dc_mma(vals[t], b0.x, b1.x, b0.y, b1.y, sb.x, sb.y);
+      }
+    }
+    const int rows[2] = {row0, row1};
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int row = rows[h];
       if (row >= pr.n) continue;
-      const __nv_bfloat16* brow = pr.b + static_cast<int64_t>(row) * pr.r;
 #pragma unroll
-      for (int t = 0; t < NG; ++t) {
+      for (int t = 0; t < NG; ++t)
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int tok = t * 8 + 2 * q + e;
-          if (tok >= pr.m) continue;
-          const __nv_bfloat16* srow = pr.st + tok * pr.r;
-          float l = 0.f;
-          for (int j = 0; j < pr.r; ++j) l = fmaf(__bfloat162float(__ldcg(srow + j)), __bfloat162float(brow[j]), l);
-          pr.y[static_cast<int64_t>(tok) * pr.n + row] = __float2bfloat16_rn(vals[t][2 * h + e] + l);
+          if (tok < pr.m) pr.y[static_cast<int64_t>(tok) * pr.n + row] = __float2bfloat16_rn(vals[t][2 * h + e]);
         }
-      }
     }
     // the problem's last tile returns its T and tiles-done counters to (epoch, 0)
     __syncthreads();

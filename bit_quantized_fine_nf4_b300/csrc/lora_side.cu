@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kSideThreads, 1)
   griddep_launch_dependents();  // the GEMM that follows needs sT only for its last k block
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles = (p.M + 127) / 128;
-  const int n1 = p.K / 64;
+  const int n1 = (p.K + 63) / 64;  // K % 64 == 0 for X A^T; dY B reduces over N (N % 8 == 0; TMA zero-fills the tail)
   const uint32_t alloc = 2 * RP <= 32 ? 32 : 2 * RP <= 64 ? 64 : 128;
   const uint32_t idesc = idesc_bf16_f32(128, RP, 0, p.mn_b);
 
