@@ -149,12 +149,12 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 // and, while profiling is on, bracketed by two CUDA events on its stream.
 enum ProfName : int {
   P_QUANTIZE = 0, P_DEQUANTIZE, P_LORA_DOWN, P_FWD_GEMM, P_BWD_GEMM, P_LORA_GRADS, P_SILU_FWD, P_SILU_BWD,
-  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_MERGE, P_LOWRANK, P_ADAMW, P_DROPOUT, P_LORA_SIDE_BWD, P_COUNT
+  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_MERGE, P_LOWRANK, P_ADAMW, P_DROPOUT, P_COUNT
 };
 const char* const kProfNames[P_COUNT] = {"nf4_quantize(3 kernels)", "nf4_dequantize", "lora_down", "fwd_gemm",
                                          "bwd_dx_gemm", "lora_grads", "silu_mul_fwd", "silu_mul_bwd",
                                          "wait_selftest", "fwd_grouped", "lora_side_fwd", "nf4_merge",
-                                         "lowrank_update", "adamw", "dropout", "lora_side_bwd"};
+                                         "lowrank_update", "adamw", "dropout"};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<bool> g_prof_on{false};
 struct ProfRec {
@@ -540,14 +540,7 @@ static int linear_bwd_impl(const uint16_t* dy, const uint16_t* x, int64_t m, con
   // and, forked onto the side stream after U, the dA / dB kernel on the SMs the
   // GEMM leaves idle; the caller's stream waits for the side stream before the
   // call returns.
-  if (qlora::use_pair_gemm(M) && qlora::lora_u_supported(r)) {
-    // U = dY B by TMA + tcgen05 on the SMs the dX pair GEMM leaves idle: the GEMM starts beside
-    // it and waits for sU only before its LoRA k steps; sT = bf16(s * t_save) in the same launch
-    Span sp(P_LORA_SIDE_BWD, s, 1);
-    const int cap = qlora::idle_sms_beside(qlora::bwd_gemm_ctas(M, N, K), di->num_sms);
-    e = qlora::launch_lora_u(dyb, reinterpret_cast<const __nv_bfloat16*>(lora_b), M, N, r, scale, su, cap, di->status,
-                             wait, s, t_save, st);
-  } else {
+  {
     // U = dY B (B read as stored) on all SMs and, in the same launch, sT = bf16(s * t_save)
     Span sp(P_LORA_DOWN, s, 1);
     e = qlora::launch_lora_down(dyb, reinterpret_cast<const __nv_bfloat16*>(lora_b), 0, M, N, r, scale, nullptr, su,

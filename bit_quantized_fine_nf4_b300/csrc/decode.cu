@@ -9,7 +9,7 @@
 // gate,up | down), each only a few microseconds of HBM time.
 //
 // Across calls (programmatic dependent launch): each CTA first issues L2
-// prefetches for every code byte it will read -- the weights do not depend on
+// prefetches (one plain prefetch per 128-byte line) for the code bytes it will read first -- the weights do not depend on
 // the previous kernel -- and only then waits (griddepcontrol.wait) for the
 // preceding kernel of the stream; right after that wait it lets the next
 // kernel launch, which prefetches its own weights while this one computes.
@@ -118,11 +118,16 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void prefetch_l2_line(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
+// L2 prefetch of `bytes` bytes from p: one plain prefetch per 128-byte line touched (regular
+// memory instructions: a warp covers 32 lines per instruction, unlike one bulk copy per row).
+__device__ __forceinline__ void dc_prefetch_codes(const void* p, int bytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(127);
+  const uintptr_t a1 = reinterpret_cast<uintptr_t>(p) + bytes;
+  for (uintptr_t a = a0; a < a1; a += 128) prefetch_l2_line(reinterpret_cast<const void*>(a));
 }
 
 // First unit of CTA c when `units` units are dealt to `grid` CTAs in contiguous runs.
@@ -208,7 +213,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
     for (int i = threadIdx.x; i < kDcRows; i += kDcThreads) {
       const int row = tile * kDcRows + i;
       if (row < pr.n) {
-        prefetch_l2_bulk(pr.codes + static_cast<int64_t>(row) * (pr.k / 2) + kun * 128, static_cast<uint32_t>(nb) * 32);
+        dc_prefetch_codes(pr.codes + static_cast<int64_t>(row) * (pr.k / 2) + kun * 128, nb * 32);
         prefetch_l2_line(pr.absq + static_cast<int64_t>(row) * (pr.k / 64) + kun * kDcUnitBlocks);
       }
     }
@@ -217,7 +222,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
     const DcProb& pr = p.prob[dc_find_slice(p, sl)];
     const int kb0 = (sl - pr.s0) * pr.t_w, kb1 = min(pr.k / 64, kb0 + pr.t_w);
     for (int j = threadIdx.x; j < pr.r; j += kDcThreads)
-      prefetch_l2_bulk(pr.a + static_cast<int64_t>(j) * pr.k + kb0 * 64, static_cast<uint32_t>(kb1 - kb0) * 128);
+      dc_prefetch_codes(pr.a + static_cast<int64_t>(j) * pr.k + kb0 * 64, (kb1 - kb0) * 128);
   }
   // X, sT, the counters and the workspace may come from earlier kernels of the stream
   griddep_wait();
@@ -526,8 +531,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
       enter(f);
       const DcProb& pf = p.prob[f.pi];
       const int row = f.tile * kDcRows + warp * 16 + lane;
-      if (row < pf.n)
-        prefetch_l2_bulk(pf.codes + static_cast<int64_t>(row) * (pf.k / 2) + f.kun * 128, static_cast<uint32_t>(f.nb) * 32);
+      if (row < pf.n) dc_prefetch_codes(pf.codes + static_cast<int64_t>(row) * (pf.k / 2) + f.kun * 128, f.nb * 32);
     }
     const int nb = cur.nb;
 #pragma unroll

@@ -122,12 +122,7 @@ bool make_tensor_map_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, u
 // Forward LoRA down-projection beside the pair GEMM (lora_side.cu), 1 <= r <= 64:
 // T = X A^T -> t_save, sT = bf16(s T), by at most max_ctas CTAs.
 bool lora_side_supported(int r);
-// Backward U = dY B beside the dX pair GEMM (lora_side.cu), r % 8 == 0, r <= 64: sU = bf16(s U)
-// [M, lora_ld(r)], and st = bf16(s t_save) in the same launch, by at most max_ctas CTAs.
-bool lora_u_supported(int r);
-cudaError_t launch_lora_u(const __nv_bfloat16* dy, const __nv_bfloat16* lora_b, int M, int N, int r, float scale,
-                          __nv_bfloat16* su, int max_ctas, unsigned* status, uint64_t wait_ns, cudaStream_t s,
-                          const float* t_save, __nv_bfloat16* st);
+
 cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lora_a, int M, int K, int r, float scale,
                                  float* t_save, __nv_bfloat16* st, int max_ctas, unsigned* status, uint64_t wait_ns,
                                  cudaStream_t s, float t_scale = 1.0f);

@@ -1,10 +1,6 @@
-// LoRA down-projections beside the CTA-pair GEMMs, on the SMs their grids leave
-// idle (Day 25 notes "Fine-tuning and LoRA/QLoRA", section 2.1: the branch
-// B (A x); section 6.2: scaled by s = alpha / r):
-//   forward   T = X A^T:  t_save = T (fp32), sT = bf16(s T)
-//   backward  U = dY B:   sU = bf16(s U), and the side job sT = bf16(s t_save)
-// In the backward the dX GEMM starts beside this kernel and needs sU only for
-// its last (LoRA) k steps, so U is off the step's critical path.
+// LoRA down-projection T = X A^T of the forward, beside the CTA-pair GEMM, on
+// few SMs (Day 25 notes "Fine-tuning and LoRA/QLoRA", section 2.1: the branch
+// B (A x); section 6.2: scaled by s = alpha / r):  t_save = T (fp32), sT = bf16(s T).
 //
 // Each CTA walks 128-token tiles: TMA streams X [128 tok x 64 k] and A_lora
 // [RP x 64 k] (K-major, 128B swizzle; RP = r rounded up to 16, rows past r are
@@ -23,13 +19,6 @@ struct SideParams {
   unsigned* status;
   int M, K, r, rp;
   int stages, stage_bytes;
-  int mn_b;              // 1: the LoRA matrix is B [K, r] as stored (MN-major operand, U = dY B), 0: A [r, K]
-  // side job of the backward, done by the epilogue warps while the first tile streams:
-  // cvt_dst [cvt_rows, lora_ld(r)] = bf16(cvt_scale * cvt_src [cvt_rows, r])
-  const float* cvt_src;
-  __nv_bfloat16* cvt_dst;
-  long long cvt_rows;
-  float cvt_scale;
   float scale;
   float t_scale;         // t_save = t_scale * (X A^T); 1 without dropout (1 / (1 - p) with it)
   unsigned long long wait_ns;
@@ -57,9 +46,9 @@ __global__ void __launch_bounds__(kSideThreads, 1)
   griddep_launch_dependents();  // the GEMM that follows needs sT only for its last k block
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles = (p.M + 127) / 128;
-  const int n1 = (p.K + 63) / 64;  // K % 64 == 0 for X A^T; dY B reduces over N (N % 8 == 0; TMA zero-fills the tail)
+  const int n1 = p.K / 64;
   const uint32_t alloc = 2 * RP <= 32 ? 32 : 2 * RP <= 64 ? 64 : 128;
-  const uint32_t idesc = idesc_bf16_f32(128, RP, 0, p.mn_b);
+  const uint32_t idesc = idesc_bf16_f32(128, RP, 0, 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSideMaxStages; ++s) {
@@ -95,10 +84,7 @@ __global__ void __launch_bounds__(kSideThreads, 1)
           uint8_t* st = smem + s * SB;
           mbar_arrive_expect_tx(&full[s], kSideBox + RP * 128);
           tma_load_2d(st, &tm_a, &full[s], i * 64, tile * 128);
-          if (p.mn_b)
-            tma_load_2d(st + kSideBox, &tm_b, &full[s], 0, i * 64);  // B rows n = 64 i .., all 64 j columns
-          else
-            tma_load_2d(st + kSideBox, &tm_b, &full[s], i * 64, 0);  // A rows j, k = 64 i ..
+          tma_load_2d(st + kSideBox, &tm_b, &full[s], i * 64, 0);
         }
       }
     }
@@ -118,10 +104,8 @@ __global__ void __launch_bounds__(kSideThreads, 1)
           const uint32_t a = smem_u32(smem + s * SB);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16_ss(d, sdesc_sw128(a + kk * 32, 16, 1024),
-                        p.mn_b ? sdesc_sw128(a + kSideBox + kk * 2048, 8192, 1024)   // [64 n x 64 j], j contiguous
-                               : sdesc_sw128(a + kSideBox + kk * 32, 16, 1024),      // [RP j x 64 k], k contiguous
-                        idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16_ss(d, sdesc_sw128(a + kk * 32, 16, 1024), sdesc_sw128(a + kSideBox + kk * 32, 16, 1024), idesc,
+                        (i > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&empty[s]);
         }
         if (ok) mma_commit(&acc_full[buf]);
@@ -132,16 +116,6 @@ __global__ void __launch_bounds__(kSideThreads, 1)
     const int quarter = warp & 3;          // this warp's TMEM lane quarter
     const int lrow = quarter * 32 + lane;  // TMEM lane = token row of the tile
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-    if (p.cvt_rows > 0) {
-      const int rk = lora_ld(p.r);
-      const long long n_out = p.cvt_rows * rk, nthr = static_cast<long long>(gridDim.x) * 128;
-      for (long long i = static_cast<long long>(blockIdx.x) * 128 + (threadIdx.x - 64); i < n_out; i += nthr) {
-        const long long row = i / rk;
-        const int jj = static_cast<int>(i - row * rk);
-        p.cvt_dst[i] = jj < p.r ? __float2bfloat16_rn(__fmul_rn(p.cvt_src[row * p.r + jj], p.cvt_scale))
-                                : __float2bfloat16_rn(0.f);
-      }
-    }
     int j = 0;
     for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x, ++j) {
       const int buf = j & 1;
@@ -164,7 +138,6 @@ __global__ void __launch_bounds__(kSideThreads, 1)
               *reinterpret_cast<uint2*>(p.s_out + static_cast<int64_t>(tok) * rk + c + q) =
                   make_uint2(pack_bf16x2_rn(__fmul_rn(f[0], p.scale), __fmul_rn(f[1], p.scale)),
                              pack_bf16x2_rn(__fmul_rn(f[2], p.scale), __fmul_rn(f[3], p.scale)));
-            if (!p.t_out) continue;
             float* to = p.t_out + static_cast<int64_t>(tok) * p.r + c + q;
             if ((p.r & 3) == 0) {  // rows of t_save start on 16-byte boundaries
               if (c + q < p.r) *reinterpret_cast<float4*>(to) = make_float4(f[0], f[1], f[2], f[3]);
@@ -192,11 +165,27 @@ __global__ void __launch_bounds__(kSideThreads, 1)
 // ------------------------------------------------------------------ host
 bool lora_side_supported(int r) { return r >= 1 && r <= 64; }
 
-static cudaError_t run_side(const CUtensorMap& ta, const CUtensorMap& tb, SideParams& prm, int M, int max_ctas,
-                            cudaStream_t s) {
-  prm.stage_bytes = kSideBox + prm.rp * 128;
+cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lora_a, int M, int K, int r, float scale,
+                                 float* t_save, __nv_bfloat16* st, int max_ctas, unsigned* status, uint64_t wait_ns,
+                                 cudaStream_t s, float t_scale) {
+  const int rp = (r + 15) / 16 * 16;
+  CUtensorMap ta, tb;
+  if (!make_tensor_map_bf16_2d(&ta, x, K, M, static_cast<uint64_t>(K) * 2, 64, 128)) return cudaErrorInvalidValue;
+  if (!make_tensor_map_bf16_2d(&tb, lora_a, K, r, static_cast<uint64_t>(K) * 2, 64, rp)) return cudaErrorInvalidValue;
+  SideParams prm = {};
+  prm.t_out = t_save;
+  prm.s_out = st;
+  prm.status = status;
+  prm.M = M;
+  prm.K = K;
+  prm.r = r;
+  prm.rp = rp;
+  prm.stage_bytes = kSideBox + rp * 128;
   prm.stages = (200 * 1024) / prm.stage_bytes;
   if (prm.stages > kSideMaxStages) prm.stages = kSideMaxStages;
+  prm.scale = scale;
+  prm.t_scale = t_scale;
+  prm.wait_ns = wait_ns;
   const size_t smem = 1024 + static_cast<size_t>(prm.stages) * prm.stage_bytes + (2 * kSideMaxStages + 4) * 8 + 16;
   const int tiles = (M + 127) / 128;
   int grid = tiles < max_ctas ? tiles : max_ctas;
@@ -219,56 +208,6 @@ static cudaError_t run_side(const CUtensorMap& ta, const CUtensorMap& tb, SidePa
   e = cudaLaunchKernelEx(&cfg, k_lora_side, ta, tb, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
-}
-
-cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lora_a, int M, int K, int r, float scale,
-                                 float* t_save, __nv_bfloat16* st, int max_ctas, unsigned* status, uint64_t wait_ns,
-                                 cudaStream_t s, float t_scale) {
-  const int rp = (r + 15) / 16 * 16;
-  CUtensorMap ta, tb;
-  if (!make_tensor_map_bf16_2d(&ta, x, K, M, static_cast<uint64_t>(K) * 2, 64, 128)) return cudaErrorInvalidValue;
-  if (!make_tensor_map_bf16_2d(&tb, lora_a, K, r, static_cast<uint64_t>(K) * 2, 64, rp)) return cudaErrorInvalidValue;
-  SideParams prm = {};
-  prm.t_out = t_save;
-  prm.s_out = st;
-  prm.status = status;
-  prm.M = M;
-  prm.K = K;
-  prm.r = r;
-  prm.rp = rp;
-  prm.mn_b = 0;
-  prm.scale = scale;
-  prm.t_scale = t_scale;
-  prm.wait_ns = wait_ns;
-  return run_side(ta, tb, prm, M, max_ctas, s);
-}
-
-bool lora_u_supported(int r) { return r >= 8 && r <= 64 && r % 8 == 0; }
-
-cudaError_t launch_lora_u(const __nv_bfloat16* dy, const __nv_bfloat16* lora_b, int M, int N, int r, float scale,
-                          __nv_bfloat16* su, int max_ctas, unsigned* status, uint64_t wait_ns, cudaStream_t s,
-                          const float* t_save, __nv_bfloat16* st) {
-  CUtensorMap ta, tb;
-  if (!make_tensor_map_bf16_2d(&ta, dy, N, M, static_cast<uint64_t>(N) * 2, 64, 128)) return cudaErrorInvalidValue;
-  // B [N, r] as stored: boxes of 64 rows n x 64 columns j (columns past r read as zero)
-  if (!make_tensor_map_bf16_2d(&tb, lora_b, r, N, static_cast<uint64_t>(r) * 2, 64, 64)) return cudaErrorInvalidValue;
-  SideParams prm = {};
-  prm.t_out = nullptr;
-  prm.s_out = su;
-  prm.status = status;
-  prm.M = M;
-  prm.K = N;
-  prm.r = r;
-  prm.rp = 64;
-  prm.mn_b = 1;
-  prm.cvt_src = t_save;
-  prm.cvt_dst = st;
-  prm.cvt_rows = t_save ? M : 0;
-  prm.cvt_scale = scale;
-  prm.scale = scale;
-  prm.t_scale = 1.0f;
-  prm.wait_ns = wait_ns;
-  return run_side(ta, tb, prm, M, max_ctas, s);
 }
 
 }  // namespace qlora
