@@ -440,6 +440,8 @@ class GroupedForward:
         b_ = ctypes.c_size_t(0)
         _check(lib.qlora_linear_fwd_grouped_workspace_bytes(self.arr, n, ctypes.byref(b_)))
         dev = problems[0][0].device if n else "cuda"
+        if workspace is None:  # the grouped call's workspace starts zero-filled (its counters)
+            workspace = torch.zeros(max(b_.value, 256), dtype=torch.uint8, device=dev)
         self.ws, self.wsb = _ws(b_.value, dev, workspace)
 
     def run(self, stream=None):

@@ -634,8 +634,6 @@ static size_t grouped_workspace(const std::vector<qlora::GroupedProblem>& gp, in
   return tot;
 }
 
-// Call epochs of the grouped forward (tags of its workspace counters).
-static std::atomic<uint32_t> g_decode_epoch{0x51a7u};
 
 int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problems, int count, size_t* bytes) {
   if (!bytes) return fail(QLORA_ERR_INVALID_ARGUMENT, "bytes is NULL");
@@ -669,8 +667,7 @@ int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, vo
   for (int i0 = 0; i0 < count; i0 += chunk) {
     const int n = count - i0 < chunk ? count - i0 : chunk;
     Span sp(P_FWD_GROUPED, s, 1);
-    cudaError_t e = qlora::launch_decode(gp.data() + i0, n, ws, g_decode_epoch.fetch_add(1u), di->status,
-                                         g_wait_ns.load(), di->num_sms, s);
+    cudaError_t e = qlora::launch_decode(gp.data() + i0, n, ws, di->status, g_wait_ns.load(), di->num_sms, s);
     if (e != cudaSuccess) return cuda_ret(e, "fwd grouped");
     ws += qlora::decode_workspace_bytes(gp.data() + i0, n, di->num_sms);
   }

@@ -18,7 +18,7 @@
 // i % grid, the 8 warps splitting its 16-k chunks); the last slice of a
 // problem adds the slices' partials in slice order and publishes
 // sT = bf16(s X A^T).  Then the weights are cut into W units of equal size
-// (problem, tile of 128 rows, 256 k) and every CTA (one per SM) takes one
+// (problem, tile of 128 rows, 256 k) and every CTA (two per SM) takes one
 // contiguous run of them.  A run accumulates the units of one row tile in
 // registers; a tile split between runs leaves float32 partials that the last
 // arriving CTA adds in run order (deterministic).  The tile's finaliser adds
@@ -39,9 +39,10 @@
 // the block's partial sums (within 2^-8 relative of the bf16_rn(L a') the
 // fwd/bwd GEMMs use).
 //
-// Counters are 64-bit (call epoch, count): a word left by another call (or
-// never initialised) is reset by its first arriver, and every counter is
-// returned to (epoch, 0) by its last user, so graph replays of one call work.
+// Counters are plain words updated with one atomic add each (many CTAs arrive
+// on the same word, so no retry loops); every counter is returned to zero by
+// its last user, so a workspace that starts zeroed stays zeroed across calls
+// and graph replays.
 #include <algorithm>
 #include <cstdio>
 #include <vector>
@@ -52,6 +53,7 @@
 namespace qlora {
 
 constexpr int kDcWarps = 8;
+constexpr int kDcCtasPerSm = 2;            // two CTAs (16 warps) per SM hide the decode's latency
 constexpr int kDcThreads = kDcWarps * 32;
 constexpr int kDcRows = kDcWarps * 16;     // rows per tile
 constexpr int kDcUnitBlocks = 4;           // 64-wide blocks per W unit (256 k)
@@ -74,7 +76,7 @@ struct DcProb {
   float* tpart;             // [t_slices][16][r] partial X A^T
   __nv_bfloat16* st;        // [16][r] bf16(s T)
   float* ypart;             // [tiles][maxseg][16][128] partial Y
-  unsigned long long* cnt;  // [2 + tiles]: T, tiles done, then one per tile
+  unsigned* cnt;            // [2 + tiles]: T, tiles done, then one per tile (zero between calls)
   int n, k, m, r;
   float scale;
   int t_slices, t_w, s0;    // X A^T: slices of t_w 64-wide blocks, first global slice
@@ -86,7 +88,6 @@ struct DcParams {
   int count;
   int grid;
   int maxseg;
-  uint32_t epoch;
   long long units;            // W units of the call
   int slices;                 // X A^T slices of the call (slice i goes to CTA i % grid)
   unsigned long long wait_ns;
@@ -139,17 +140,9 @@ __device__ __forceinline__ int dc_cta_of(long long u, long long units, int grid)
   return static_cast<int>(((u + 1) * grid - 1) / units);
 }
 
-// Arrive on a (epoch, count) counter; returns the count after this arrival.
-__device__ __forceinline__ uint32_t dc_arrive(unsigned long long* c, uint32_t epoch) {
-  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(c);
-  for (;;) {
-    const uint32_t cnt = static_cast<uint32_t>(old >> 32) == epoch ? static_cast<uint32_t>(old) : 0u;
-    const unsigned long long want = (static_cast<unsigned long long>(epoch) << 32) | (cnt + 1u);
-    const unsigned long long prev = atomicCAS(c, old, want);
-    if (prev == old) return cnt + 1u;
-    old = prev;
-  }
-}
+// Arrive on a counter (one atomic, no retry loop: many CTAs arrive on the same word); returns
+// the count after this arrival.  Every counter is returned to zero by its last user.
+__device__ __forceinline__ uint32_t dc_arrive(unsigned* c) { return atomicAdd(c, 1u) + 1u; }
 
 __device__ __forceinline__ int dc_find_prob(const DcParams& p, long long u) {  // problem of W unit u
   int lo = 0, hi = p.count - 1;
@@ -193,7 +186,7 @@ __device__ __forceinline__ uint2 dc_xfrag(const DcProb& pr, int tok, int kk) {
 }
 
 template <int NG>
-__global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant__ DcParams p) {
+__global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __grid_constant__ DcParams p) {
   __shared__ __align__(16) uint8_t s_ring[kDcWarps][kDcRing][kDcStage];
   __shared__ float s_red[kDcWarps][16][16];
   __shared__ int s_flag;
@@ -274,7 +267,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
     }
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_flag = dc_arrive(pr.cnt, p.epoch) == static_cast<uint32_t>(pr.t_slices);
+    if (threadIdx.x == 0) s_flag = dc_arrive(pr.cnt) == static_cast<uint32_t>(pr.t_slices);
     __syncthreads();
     if (s_flag) {
       // last slice of the problem: T = the slices' partials added in slice order -> t_save, sT
@@ -301,7 +294,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
       }
       __threadfence();
       __syncthreads();
-      if (threadIdx.x == 0) atomicAdd(pr.cnt, 1ull);  // count = t_slices + 1: sT published
+      if (threadIdx.x == 0) atomicAdd(pr.cnt, 1u);  // count = t_slices + 1: sT published
     }
     __syncthreads();
   }
@@ -422,7 +415,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
       }
       __threadfence();
       __syncthreads();
-      if (threadIdx.x == 0) s_flag = dc_arrive(pr.cnt + 2 + tile, p.epoch) == static_cast<uint32_t>(nseg);
+      if (threadIdx.x == 0) s_flag = dc_arrive(pr.cnt + 2 + tile) == static_cast<uint32_t>(nseg);
       __syncthreads();
       finalise = s_flag != 0;
       if (finalise) {
@@ -443,8 +436,7 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
           }
         }
         __syncthreads();
-        if (threadIdx.x == 0) *reinterpret_cast<volatile unsigned long long*>(pr.cnt + 2 + tile) =
-            static_cast<unsigned long long>(p.epoch) << 32;
+        if (threadIdx.x == 0) *reinterpret_cast<volatile unsigned*>(pr.cnt + 2 + tile) = 0u;
       }
     } else {
 #pragma unroll
@@ -455,12 +447,12 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
     if (!finalise) return;
     // wait until the problem's sT is published (count t_slices + 1)
     if (threadIdx.x == 0) {
-      const unsigned long long want = (static_cast<unsigned long long>(p.epoch) << 32) | (pr.t_slices + 1u);
-      bool ok = *reinterpret_cast<volatile unsigned long long*>(pr.cnt) == want;
+      const unsigned want = static_cast<unsigned>(pr.t_slices) + 1u;
+      bool ok = *reinterpret_cast<volatile unsigned*>(pr.cnt) == want;
       if (!ok) {
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t it = 1;; ++it) {
-          if (*reinterpret_cast<volatile unsigned long long*>(pr.cnt) == want) { ok = true; break; }
+          if (*reinterpret_cast<volatile unsigned*>(pr.cnt) == want) { ok = true; break; }
           if ((it & 63u) == 0 && globaltimer_ns() - t0 > p.wait_ns) break;
           __nanosleep(64);
         }
@@ -500,11 +492,11 @@ __global__ void __launch_bounds__(kDcThreads, 1) k_decode(const __grid_constant_
           if (tok < pr.m) pr.y[static_cast<int64_t>(tok) * pr.n + row] = __float2bfloat16_rn(vals[t][2 * h + e]);
         }
     }
-    // the problem's last tile returns its T and tiles-done counters to (epoch, 0)
+    // the problem's last tile returns its T and tiles-done counters to zero
     __syncthreads();
-    if (threadIdx.x == 0 && dc_arrive(pr.cnt + 1, p.epoch) == static_cast<uint32_t>(pr.tiles)) {
-      *reinterpret_cast<volatile unsigned long long*>(pr.cnt) = static_cast<unsigned long long>(p.epoch) << 32;
-      *reinterpret_cast<volatile unsigned long long*>(pr.cnt + 1) = static_cast<unsigned long long>(p.epoch) << 32;
+    if (threadIdx.x == 0 && dc_arrive(pr.cnt + 1) == static_cast<uint32_t>(pr.tiles)) {
+      *reinterpret_cast<volatile unsigned*>(pr.cnt) = 0u;
+      *reinterpret_cast<volatile unsigned*>(pr.cnt + 1) = 0u;
     }
   };
 
@@ -633,7 +625,8 @@ DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
     u += static_cast<long long>(pl.tiles[i]) * pl.ku[i];
   }
   pl.units = u;
-  pl.grid = static_cast<int>(u < sms ? u : sms);
+  const long long slots = static_cast<long long>(sms) * kDcCtasPerSm;  // every CTA of the grid resident at once
+  pl.grid = static_cast<int>(u < slots ? u : slots);
   // X A^T slices: about one per CTA over the whole list, in proportion to each problem's r k
   double work = 0.0;
   for (int i = 0; i < count; ++i) work += static_cast<double>((probs[i].r + 15) / 16) * probs[i].w.k;
@@ -665,7 +658,7 @@ DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
   pl.off_ypart.resize(count);
   for (int i = 0; i < count; ++i) {
     pl.off_cnt[i] = off;
-    off += al256(static_cast<size_t>(2 + pl.tiles[i]) * 8);
+    off += al256(static_cast<size_t>(2 + pl.tiles[i]) * 4);
     pl.off_tpart[i] = off;
     off += al256(static_cast<size_t>(pl.t_slices[i]) * 16 * probs[i].r * 4);
     pl.off_st[i] = off;
@@ -682,8 +675,8 @@ size_t decode_workspace_bytes(const GroupedProblem* probs, int count, int num_sm
   return dc_plan(probs, count, num_sms).ws_bytes;
 }
 
-cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, uint32_t epoch, unsigned* status,
-                          uint64_t wait_ns, int num_sms, cudaStream_t s) {
+cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, unsigned* status, uint64_t wait_ns,
+                          int num_sms, cudaStream_t s) {
   if (count <= 0) return cudaSuccess;
   const DcPlan pl = dc_plan(probs, count, num_sms);
   static DcParams prm;  // 20+ KB: not on the host stack; launches copy it
@@ -692,7 +685,6 @@ cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, uint
   prm.count = count;
   prm.grid = pl.grid;
   prm.maxseg = pl.maxseg;
-  prm.epoch = epoch;
   prm.units = pl.units;
   prm.slices = pl.slices;
   prm.wait_ns = wait_ns;
@@ -714,7 +706,7 @@ cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, uint
     d.tpart = reinterpret_cast<float*>(base + pl.off_tpart[i]);
     d.st = reinterpret_cast<__nv_bfloat16*>(base + pl.off_st[i]);
     d.ypart = reinterpret_cast<float*>(base + pl.off_ypart[i]);
-    d.cnt = reinterpret_cast<unsigned long long*>(base + pl.off_cnt[i]);
+    d.cnt = reinterpret_cast<unsigned*>(base + pl.off_cnt[i]);
     d.n = static_cast<int>(g.w.n);
     d.k = static_cast<int>(g.w.k);
     d.m = g.m;

@@ -145,10 +145,10 @@ struct GroupedProblem {
 // Problems per launch; a longer list goes out in several launches.
 int decode_max_problems();
 size_t decode_workspace_bytes(const GroupedProblem* probs, int count, int num_sms);
-// One launch for the whole list (count <= decode_max_problems()); `epoch` tags this call's
-// counters in the workspace (any value that differs between calls sharing a workspace).
-cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, uint32_t epoch, unsigned* status,
-                          uint64_t wait_ns, int num_sms, cudaStream_t s);
+// One launch for the whole list (count <= decode_max_problems()).  The workspace's counters
+// must be zero before the first call; every call leaves them zero.
+cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, unsigned* status, uint64_t wait_ns,
+                          int num_sms, cudaStream_t s);
 
 // Bounded-wait self test: one CTA waits on an mbarrier nothing arrives on.
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t wait_ns, cudaStream_t s);

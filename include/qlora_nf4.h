@@ -296,9 +296,10 @@ int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problem
  * weight of the bf16_rn(L a') qlora_linear_fwd uses).  Split tiles add their
  * float32 partial sums in a fixed order, so every y is deterministic.
  * `problems` is a host array of `count` entries; 1 <= m <= 16, 1 <= r <= 128.
- * The workspace holds per-call counters tagged with a call number and returned
- * to zero by the call itself: it needs no initialisation and may be reused by
- * later calls (and graph replays) ordered on the same stream.
+ * The workspace holds counters of the split reductions: it must be zero-filled
+ * before its first use (cudaMemsetAsync once); every call returns them to zero,
+ * so it may then be reused by later calls (and graph replays) ordered on the
+ * same stream.  After a call that latched QLORA_ERR_TIMEOUT, zero it again.
  */
 int qlora_linear_fwd_grouped(const qlora_linear_problem* problems, int count, void* workspace, size_t workspace_bytes,
                              void* stream);
