@@ -31,9 +31,11 @@ bounded sample of the same workload and prints the same line with
 ``"impl": "reference"``.
 
 ``--only quant [--shape NxK]`` / ``--only decode [--decode-layers L]
-[--decode-tokens 1,4,16]`` run just that secondary measurement (quantise +
-dequantise of one bf16 weight; the decode sweep) and print its figures -- a
-small, repeatable workload for profilers, not a bench line.
+[--decode-tokens 1,4,16]`` / ``--only merge`` / ``--only smalltok [--tokens M]``
+run just that secondary measurement (quantise + dequantise of one bf16 weight;
+the decode sweep; the merge of the 4096^2 projection; fwd+bwd at M <= 256
+tokens) and print its figures -- small, repeatable workloads for profilers,
+not bench lines.
 """
 
 from __future__ import annotations
@@ -543,6 +545,25 @@ def adamw_rate(q, torch, layers=32, r=16):
     return {"tensors": len(ts), "params": params, "ms": ms, "gbs": byts / ms / 1e6}
 
 
+def small_token_step(q, torch, m=128, n=4096, k=4096, r=16, alpha=32.0, steps=10):
+    """fwd+bwd of the 4096^2 projection at m <= 256 tokens: the small-token GEMMs (k_qgemm_wa,
+    k_qgemm_wb).  Returns ms per step and TFLOP/s (a profiler workload)."""
+    import synthetic
+    case = synthetic.linear_case(n, k, m, r, alpha, device="cuda", base_seed=6)
+    rec = q.quantize(case.w)
+
+    def step():
+        y, t = q.linear_fwd(case.x, rec, case.a, case.b, alpha)
+        q.linear_bwd(case.dy, case.x, rec, case.a, case.b, alpha, t)
+
+    for _ in range(3):
+        step()
+    ms = statistics.median(time_events(torch, step, steps))
+    q.check_status()
+    return {"m": m, "n": n, "k": k, "r": r, "ms_per_step": ms,
+            "tflops": step_flops(m, n, k, r) / (ms / 1e3) / 1e12}
+
+
 def traffic_for(kernel: str):
     """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if it matches the current source."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
@@ -786,7 +807,8 @@ def main(argv=None):
     ap.add_argument("--ref-rows", type=int, default=128)
     ap.add_argument("--decode-layers", type=int, default=32)
     ap.add_argument("--decode-tokens", default="1", help="token counts of --only decode, e.g. 1,4,16")
-    ap.add_argument("--only", choices=("quant", "decode"), default=None,
+    ap.add_argument("--tokens", type=int, default=128, help="tokens of --only smalltok (<= 256: small-token GEMMs)")
+    ap.add_argument("--only", choices=("quant", "decode", "merge", "smalltok"), default=None,
                     help="run one secondary measurement alone (a workload for profilers)")
     ap.add_argument("--shape", default="22016x8192", help="weight shape for --only quant")
     args = ap.parse_args(argv)
@@ -797,6 +819,10 @@ def main(argv=None):
         if args.only == "quant":
             n, k = (int(v) for v in args.shape.lower().split("x"))
             print(json.dumps(dequant_quant_rates(q, torch, None, n=n, k=k)), flush=True)
+        elif args.only == "merge":
+            print(json.dumps(merge_rate(q, torch, None)), flush=True)
+        elif args.only == "smalltok":
+            print(json.dumps(small_token_step(q, torch, m=args.tokens)), flush=True)
         else:
             toks = tuple(int(t) for t in args.decode_tokens.split(","))
             print(json.dumps(decode_sweep(q, torch, layers=args.decode_layers, tokens=toks)), flush=True)

@@ -301,85 +301,78 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
 
   // ---------------------------------------------------------------- W units
   if (u_begin >= u_end) return;
-  // the run's (problem, tile, block) steps, walked by three cursors: the cp.async stager (kDcRing - 1
-  // blocks ahead), the block-scale loader (2 ahead) and the consumer
-  struct Cursor {
-    long long u;
-    int kb;  // block within the unit
-    int nb;  // blocks in the unit (the last unit of a row may hold fewer than kDcUnitBlocks)
-    int pi, tile, kun;
+  // A unit's description; looked up once per unit (binary search over the problem list).
+  struct Unit {
+    int pi, tile, kun, nb;  // nb: blocks in the unit (the last unit of a row may hold fewer than 4)
   };
-  auto enter = [&](Cursor& c) {  // describe unit c.u
-    if (c.u >= u_end) return;
-    c.pi = dc_find_prob(p, c.u);
-    const DcProb& pr = p.prob[c.pi];
-    const long long w = c.u - pr.u0_w;
-    c.tile = static_cast<int>(w / pr.ku);
-    c.kun = static_cast<int>(w % pr.ku);
-    c.nb = min(kDcUnitBlocks, pr.k / 64 - c.kun * kDcUnitBlocks);
+  auto describe = [&](long long uu) {
+    Unit d;
+    d.pi = dc_find_prob(p, uu);
+    const DcProb& pr = p.prob[d.pi];
+    const long long w = uu - pr.u0_w;
+    d.tile = static_cast<int>(w / pr.ku);
+    d.kun = static_cast<int>(w % pr.ku);
+    d.nb = min(kDcUnitBlocks, pr.k / 64 - d.kun * kDcUnitBlocks);
+    return d;
   };
-  auto advance = [&](Cursor& c) {
-    if (++c.kb == c.nb) {
-      c.kb = 0;
-      ++c.u;
-      enter(c);
+  // ---- the cp.async stager: runs kDcRing - 1 blocks ahead of the consumer through the run
+  const uint32_t stage_dst0 = smem_u32(&s_ring[warp][0][0]) + (lane >> 1) * kDcPitch + (lane & 1) * 16;
+  long long st_u = u_begin;
+  int st_kb = 0, st_nb = 0, st_slot = 0;
+  const uint8_t* st_src = nullptr;
+  bool st_ok = false;
+  auto st_enter = [&]() {
+    if (st_u >= u_end) return;
+    const Unit d = describe(st_u);
+    const DcProb& pr = p.prob[d.pi];
+    const int row = d.tile * kDcRows + warp * 16 + (lane >> 1);
+    st_ok = row < pr.n;
+    st_src = pr.codes + (st_ok ? static_cast<int64_t>(row) * (pr.k / 2) + d.kun * 128 + (lane & 1) * 16 : 0);
+    st_nb = d.nb;
+    st_kb = 0;
+  };
+  auto stage_next = [&]() {
+    if (st_u < u_end) {
+      cp_async16(stage_dst0 + st_slot * kDcStage, st_src, st_ok);
+      st_src += 32;
+      if (++st_kb == st_nb) {
+        ++st_u;
+        st_enter();
+      }
     }
+    cp_async_commit();
+    st_slot = st_slot + 1 == kDcRing ? 0 : st_slot + 1;
   };
-  const uint32_t ring0 = smem_u32(&s_ring[warp][0][0]);
-  // stage block step `c` of this warp's 16 rows into ring slot `slot`
-  auto stage = [&](const Cursor& c, int slot) {
-    const DcProb& pr = p.prob[c.pi];
-    const int row = c.tile * kDcRows + warp * 16 + (lane >> 1);
-    const int kb = c.kun * kDcUnitBlocks + c.kb;
-    const bool ok = row < pr.n;
-    const uint8_t* src = pr.codes + (ok ? static_cast<int64_t>(row) * (pr.k / 2) + kb * 32 + (lane & 1) * 16 : 0);
-    cp_async16(ring0 + slot * kDcStage + (lane >> 1) * kDcPitch + (lane & 1) * 16, src, ok);
-  };
-  // raw block scales of rows g, g+8 for the (up to 4) blocks of unit `c`, loaded a whole unit
-  // before they are used (so the loads are long complete when the registers are reused)
+  st_enter();
+  for (int i = 0; i < kDcRing - 1; ++i) stage_next();
+  int use_slot = 0;
+
+  // raw block scales of rows g, g+8 for the blocks of a unit, loaded one unit before use
   struct Scales {
     int q0[kDcUnitBlocks], q1[kDcUnitBlocks];
     float s0[kDcUnitBlocks], s1[kDcUnitBlocks];
     float mu;
   };
-  auto load_scales = [&](const Cursor& c, Scales& sc) {
-    if (c.u >= u_end) return;
-    const DcProb& pr = p.prob[c.pi];
+  auto load_scales = [&](const Unit& d, Scales& sc) {
+    const DcProb& pr = p.prob[d.pi];
     const int kbr = pr.k / 64;
-    const int r0 = c.tile * kDcRows + warp * 16 + g, r1 = r0 + 8;
+    const int r0 = d.tile * kDcRows + warp * 16 + g, r1 = r0 + 8;
+    const int64_t b0 = static_cast<int64_t>(r0) * kbr + d.kun * kDcUnitBlocks;
+    const int64_t b1 = b0 + static_cast<int64_t>(8) * kbr;
     sc.mu = __ldg(pr.mean);
 #pragma unroll
     for (int b = 0; b < kDcUnitBlocks; ++b) {
-      const int kb = c.kun * kDcUnitBlocks + b;
-      sc.q0[b] = sc.q1[b] = 0;
-      sc.s0[b] = sc.s1[b] = 0.f;
-      if (b < c.nb && r0 < pr.n) {
-        const int64_t bi = static_cast<int64_t>(r0) * kbr + kb;
-        sc.q0[b] = __ldg(pr.absq + bi);
-        sc.s0[b] = __ldg(pr.step + (bi >> 8));
-      }
-      if (b < c.nb && r1 < pr.n) {
-        const int64_t bi = static_cast<int64_t>(r1) * kbr + kb;
-        sc.q1[b] = __ldg(pr.absq + bi);
-        sc.s1[b] = __ldg(pr.step + (bi >> 8));
-      }
+      const bool in = b < d.nb;
+      sc.q0[b] = (in && r0 < pr.n) ? __ldg(pr.absq + b0 + b) : 0;
+      sc.s0[b] = (in && r0 < pr.n) ? __ldg(pr.step + ((b0 + b) >> 8)) : 0.f;
+      sc.q1[b] = (in && r1 < pr.n) ? __ldg(pr.absq + b1 + b) : 0;
+      sc.s1[b] = (in && r1 < pr.n) ? __ldg(pr.step + ((b1 + b) >> 8)) : 0.f;
     }
   };
-
-  Cursor pre{u_begin, 0, 0, 0, 0, 0};
-  enter(pre);
-  int issued = 0;
-  for (; issued < kDcRing - 1; ++issued) {
-    if (pre.u < u_end) {
-      stage(pre, issued % kDcRing);
-      advance(pre);
-    }
-    cp_async_commit();
-  }
-  Cursor cur{u_begin, 0, 0, 0, 0, 0};
-  enter(cur);
+  long long cu = u_begin;
+  Unit cd = describe(cu);
   Scales sc_cur, sc_nxt;
-  load_scales(cur, sc_cur);
+  load_scales(cd, sc_cur);
 
   float run[NG][4];
   auto zero_run = [&]() {
@@ -502,65 +495,66 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
 
   const Nf4Table lv = dc_level_table();
   const uint32_t pick = (q & 1) ? 0x7632u : 0x5410u;  // the two code bytes of chunk c in the 32-bit word
+  const bool hq = (q >> 1) != 0;
+  const uint32_t ring_row0 = smem_u32(&s_ring[warp][0][0]) + g * kDcPitch;
   float blk[NG][4];
-  while (cur.u < u_end && alive) {
-    const DcProb& pr = p.prob[cur.pi];
-    if (cur.pi != cur_pi || cur.tile != cur_tile) {
+  while (cu < u_end && alive) {
+    const DcProb& pr = p.prob[cd.pi];
+    if (cd.pi != cur_pi || cd.tile != cur_tile) {
       if (cur_pi >= 0) {
         flush(cur_pi, cur_tile);
         if (!alive) break;
       }
-      cur_pi = cur.pi;
-      cur_tile = cur.tile;
+      cur_pi = cd.pi;
+      cur_tile = cd.tile;
       zero_run();
     }
-    // the next unit's block scales, and its L2 prefetch kDcPrefetchUnits units ahead (long runs)
-    Cursor nx{cur.u + 1, 0, 0, 0, 0, 0};
-    enter(nx);
-    load_scales(nx, sc_nxt);
-    if (cur.u + kDcPrefetchUnits < u_end && lane < 16) {
-      Cursor f{cur.u + kDcPrefetchUnits, 0, 0, 0, 0, 0};
-      enter(f);
+    // the next unit: its description, its block scales, and its L2 prefetch kDcPrefetchUnits ahead
+    Unit nd = cd;
+    if (cu + 1 < u_end) {
+      nd = describe(cu + 1);
+      load_scales(nd, sc_nxt);
+    }
+    if (cu + kDcPrefetchUnits < u_end && lane < 16) {
+      const Unit f = describe(cu + kDcPrefetchUnits);
       const DcProb& pf = p.prob[f.pi];
       const int row = f.tile * kDcRows + warp * 16 + lane;
       if (row < pf.n) dc_prefetch_codes(pf.codes + static_cast<int64_t>(row) * (pf.k / 2) + f.kun * 128, f.nb * 32);
     }
-    const int nb = cur.nb;
+    // this lane's token rows of X for the unit (tokens g and g + 8), chunk c at +16 c, block b at +64 b
+    const int k0 = cd.kun * kDcUnitBlocks * 64 + 4 * q;
+    const __nv_bfloat16* xp[NG];
+#pragma unroll
+    for (int t = 0; t < NG; ++t) xp[t] = (t * 8 + g < pr.m) ? pr.x + static_cast<int64_t>(t * 8 + g) * pr.k + k0 : nullptr;
 #pragma unroll
     for (int b = 0; b < kDcUnitBlocks; ++b) {
-      if (b >= nb) break;
-      // X fragments of the 4 chunks of this block (issued before the decode)
-      const int kbase = (cur.kun * kDcUnitBlocks + b) * 64;
+      if (b >= cd.nb) break;
       uint2 xf[4][NG];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int t = 0; t < NG; ++t)
 #pragma unroll
-        for (int t = 0; t < NG; ++t) xf[c][t] = dc_xfrag(pr, t * 8 + g, kbase + 16 * c + 4 * q);
-      // keep the ring kDcRing - 1 blocks ahead
-      if (pre.u < u_end) {
-        stage(pre, issued % kDcRing);
-        advance(pre);
-      }
-      cp_async_commit();
-      ++issued;
+        for (int c = 0; c < 4; ++c) xf[c][t] = xp[t] ? ldg_nc_v2(xp[t] + b * 64 + 16 * c) : make_uint2(0u, 0u);
+      stage_next();
       cp_async_wait<kDcRing - 1>();
       __syncwarp();
-      const int slot = (issued - kDcRing) % kDcRing;
-      const uint8_t* st0 = &s_ring[warp][slot][0];
-      const uint4 c0a = *reinterpret_cast<const uint4*>(st0 + g * kDcPitch);
-      const uint4 c0b = *reinterpret_cast<const uint4*>(st0 + g * kDcPitch + 16);
-      const uint4 c1a = *reinterpret_cast<const uint4*>(st0 + (g + 8) * kDcPitch);
-      const uint4 c1b = *reinterpret_cast<const uint4*>(st0 + (g + 8) * kDcPitch + 16);
-      // chunk c (16 k) uses code bytes 8c + 2q, 8c + 2q + 1 of the 32-byte block; a word of
-      // chunks (c, c+1) = bytes (8c + 2q, +1, 8c + 8 + 2q, +1)
-      const uint32_t r0w[8] = {c0a.x, c0a.y, c0a.z, c0a.w, c0b.x, c0b.y, c0b.z, c0b.w};
-      const uint32_t r1w[8] = {c1a.x, c1a.y, c1a.z, c1a.w, c1b.x, c1b.y, c1b.z, c1b.w};
+      const uint32_t rr = ring_row0 + use_slot * kDcStage;
+      use_slot = use_slot + 1 == kDcRing ? 0 : use_slot + 1;
+      uint32_t r0w[8], r1w[8];
+      {
+        uint4 v;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(rr));
+        r0w[0] = v.x; r0w[1] = v.y; r0w[2] = v.z; r0w[3] = v.w;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(rr + 16));
+        r0w[4] = v.x; r0w[5] = v.y; r0w[6] = v.z; r0w[7] = v.w;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(rr + 8 * kDcPitch));
+        r1w[0] = v.x; r1w[1] = v.y; r1w[2] = v.z; r1w[3] = v.w;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(rr + 8 * kDcPitch + 16));
+        r1w[4] = v.x; r1w[5] = v.y; r1w[6] = v.z; r1w[7] = v.w;
+      }
 #pragma unroll
       for (int t = 0; t < NG; ++t) blk[t][0] = blk[t][1] = blk[t][2] = blk[t][3] = 0.f;
 #pragma unroll
-      for (int cp = 0; cp < 2; ++cp) {  // chunk pairs (0,1), (2,3)
-        // words 4cp + q/2 and 4cp + 2 + q/2, chosen with static indices (no local memory)
-        const bool hq = (q >> 1) != 0;
+      for (int cp = 0; cp < 2; ++cp) {  // chunk pairs (0,1), (2,3); words 4cp + q/2 and 4cp + 2 + q/2
         const uint32_t w0 = prmt(hq ? r0w[4 * cp + 1] : r0w[4 * cp], hq ? r0w[4 * cp + 3] : r0w[4 * cp + 2], pick);
         const uint32_t w1 = prmt(hq ? r1w[4 * cp + 1] : r1w[4 * cp], hq ? r1w[4 * cp + 3] : r1w[4 * cp + 2], pick);
         uint32_t d0[4], d1[4];
@@ -583,10 +577,11 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
         run[t][2] = fmaf(a21, blk[t][2], run[t][2]);
         run[t][3] = fmaf(a21, blk[t][3], run[t][3]);
       }
-      __syncwarp();  // the slot is refilled by a later stage()
+      __syncwarp();  // the slot is refilled by a later stage_next()
     }
     sc_cur = sc_nxt;
-    cur = nx;
+    cd = nd;
+    ++cu;
   }
   cp_async_wait<0>();
   if (cur_pi >= 0 && alive) flush(cur_pi, cur_tile);
