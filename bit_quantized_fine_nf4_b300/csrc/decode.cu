@@ -161,8 +161,20 @@ __device__ __forceinline__ int dc_find_slice(const DcParams& p, int sl) {  // pr
   return lo;
 }
 
-// The bf16 NF4 levels as byte planes for nf4_decode_word (scale 1).
-__device__ __forceinline__ Nf4Table dc_level_table() { return nf4_table(1.0f); }
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+// Decode one 32-bit word of packed codes (byte b: element 2b in the high nibble, 2b+1 in the low)
+// into 4 bf16x2 words (element 2i in the low half of out[i]) through this lane's column of the
+// level-pair table (row stride 128 bytes).
+__device__ __forceinline__ void dc_decode_word(uint32_t lut_lane, uint32_t w, uint32_t (&out)[4]) {
+  out[0] = lds32(lut_lane + ((w << 7) & 0x7f80u));
+  out[1] = lds32(lut_lane + ((w >> 1) & 0x7f80u));
+  out[2] = lds32(lut_lane + ((w >> 9) & 0x7f80u));
+  out[3] = lds32(lut_lane + ((w >> 17) & 0x7f80u));
+}
 
 // Four bf16 values row[j .. j+3] of a row of length r (zero past r) as two bf16x2 words.
 // `readonly`: the row is not written during the kernel (non-coherent path); otherwise it is read
@@ -190,6 +202,9 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
   __shared__ __align__(16) uint8_t s_ring[kDcWarps][kDcRing][kDcStage];
   __shared__ float s_red[kDcWarps][16][16];
   __shared__ int s_flag;
+  // level pairs of a code byte: s_lut[b * 32 + lane] = bf16 L[b >> 4] | (bf16 L[b & 15]) << 16, the
+  // byte's two weights in mma fragment order; one column per lane, so lookups never conflict
+  extern __shared__ __align__(16) uint32_t s_lut[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
   const long long u_begin = dc_run_start(blockIdx.x, p.units, p.grid);
@@ -216,6 +231,15 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     const int kb0 = (sl - pr.s0) * pr.t_w, kb1 = min(pr.k / 64, kb0 + pr.t_w);
     for (int j = threadIdx.x; j < pr.r; j += kDcThreads)
       dc_prefetch_codes(pr.a + static_cast<int64_t>(j) * pr.k + kb0 * 64, (kb1 - kb0) * 128);
+  }
+  {
+    constexpr uint32_t hex[16] = QLORA_NF4_LEVELS_HEX;
+    for (int i = threadIdx.x; i < 256 * 32; i += kDcThreads) {
+      const int b = i >> 5;
+      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(hex[b >> 4])));
+      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(hex[b & 15])));
+      s_lut[i] = lo | (hi << 16);
+    }
   }
   // X, sT, the counters and the workspace may come from earlier kernels of the stream
   griddep_wait();
@@ -493,9 +517,9 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     }
   };
 
-  const Nf4Table lv = dc_level_table();
+  __syncthreads();  // s_lut written
+  const uint32_t lut = smem_u32(s_lut + lane);
   const uint32_t pick = (q & 1) ? 0x7632u : 0x5410u;  // the two code bytes of chunk c in the 32-bit word
-  const bool hq = (q >> 1) != 0;
   const uint32_t ring_row0 = smem_u32(&s_ring[warp][0][0]) + g * kDcPitch;
   float blk[NG][4];
   while (cu < u_end && alive) {
@@ -539,27 +563,20 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
       __syncwarp();
       const uint32_t rr = ring_row0 + use_slot * kDcStage;
       use_slot = use_slot + 1 == kDcRing ? 0 : use_slot + 1;
-      uint32_t r0w[8], r1w[8];
-      {
-        uint4 v;
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(rr));
-        r0w[0] = v.x; r0w[1] = v.y; r0w[2] = v.z; r0w[3] = v.w;
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(rr + 16));
-        r0w[4] = v.x; r0w[5] = v.y; r0w[6] = v.z; r0w[7] = v.w;
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(rr + 8 * kDcPitch));
-        r1w[0] = v.x; r1w[1] = v.y; r1w[2] = v.z; r1w[3] = v.w;
-        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(rr + 8 * kDcPitch + 16));
-        r1w[4] = v.x; r1w[5] = v.y; r1w[6] = v.z; r1w[7] = v.w;
-      }
+      // the code words this lane decodes: words 4cp + q/2 and 4cp + 2 + q/2 of rows g and g + 8
+      const uint32_t wq = rr + 4 * (q >> 1);
+      const uint32_t a00 = lds32(wq), a01 = lds32(wq + 8), a02 = lds32(wq + 16), a03 = lds32(wq + 24);
+      const uint32_t a10 = lds32(wq + 8 * kDcPitch), a11 = lds32(wq + 8 * kDcPitch + 8);
+      const uint32_t a12 = lds32(wq + 8 * kDcPitch + 16), a13 = lds32(wq + 8 * kDcPitch + 24);
 #pragma unroll
       for (int t = 0; t < NG; ++t) blk[t][0] = blk[t][1] = blk[t][2] = blk[t][3] = 0.f;
 #pragma unroll
-      for (int cp = 0; cp < 2; ++cp) {  // chunk pairs (0,1), (2,3); words 4cp + q/2 and 4cp + 2 + q/2
-        const uint32_t w0 = prmt(hq ? r0w[4 * cp + 1] : r0w[4 * cp], hq ? r0w[4 * cp + 3] : r0w[4 * cp + 2], pick);
-        const uint32_t w1 = prmt(hq ? r1w[4 * cp + 1] : r1w[4 * cp], hq ? r1w[4 * cp + 3] : r1w[4 * cp + 2], pick);
+      for (int cp = 0; cp < 2; ++cp) {  // chunk pairs (0,1), (2,3)
+        const uint32_t w0 = prmt(cp ? a02 : a00, cp ? a03 : a01, pick);
+        const uint32_t w1 = prmt(cp ? a12 : a10, cp ? a13 : a11, pick);
         uint32_t d0[4], d1[4];
-        nf4_decode_word(lv, w0, d0);
-        nf4_decode_word(lv, w1, d1);
+        dc_decode_word(lut, w0, d0);
+        dc_decode_word(lut, w1, d1);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int c = 2 * cp + h;
@@ -715,10 +732,13 @@ cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, unsi
     d.u0_w = pl.u0_w[i];
     if (g.m > mmax) mmax = g.m;
   }
+  constexpr size_t kLut = 256 * 32 * 4;
+  cudaError_t e0 = mmax <= 8 ? set_smem_limit_once(k_decode<1>, kLut) : set_smem_limit_once(k_decode<2>, kLut);
+  if (e0 != cudaSuccess) return e0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid);
   cfg.blockDim = dim3(kDcThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kLut;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
