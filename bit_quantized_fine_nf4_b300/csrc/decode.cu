@@ -61,7 +61,8 @@ constexpr int kDcRing = 6;                 // cp.async ring depth per warp, in b
 constexpr int kDcPitch = 48;               // shared-memory bytes per staged row piece (32 used, padded: no bank conflicts)
 constexpr int kDcStage = 16 * kDcPitch;    // one block of the warp's 16 rows
 constexpr int kDcMaxProbs = 128;
-constexpr int kDcPrefetchUnits = 24;       // W units a CTA keeps prefetched into L2 ahead of its consumer
+constexpr int kDcPrefetchUnits = 24;
+constexpr int kDcMaxSlices = 16;           // X A^T slices per problem (each finaliser adds them all)       // W units a CTA keeps prefetched into L2 ahead of its consumer
 
 struct DcProb {
   const uint8_t* codes;
@@ -74,7 +75,6 @@ struct DcProb {
   __nv_bfloat16* y;         // [m, n]
   float* t_save;            // [m, r] or null
   float* tpart;             // [t_slices][16][r] partial X A^T
-  __nv_bfloat16* st;        // [16][r] bf16(s T)
   float* ypart;             // [tiles][maxseg][16][128] partial Y
   unsigned* cnt;            // [2 + tiles]: T, tiles done, then one per tile (zero between calls)
   int n, k, m, r;
@@ -291,76 +291,59 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     }
     __threadfence();
     __syncthreads();
-    if (threadIdx.x == 0) s_flag = dc_arrive(pr.cnt) == static_cast<uint32_t>(pr.t_slices);
-    __syncthreads();
-    if (s_flag) {
-      // last slice of the problem: T = the slices' partials added in slice order -> t_save, sT
-      __threadfence();
-      for (int i = threadIdx.x; i < 16 * pr.r; i += kDcThreads) {
-        const int tok = i / pr.r, j = i % pr.r;
-        float v = 0.f;
-        if (tok < pr.m) {
-          // slice order, eight loads in flight at a time
-          const float* src = pr.tpart + static_cast<int64_t>(tok) * pr.r + j;
-          const int64_t stride = static_cast<int64_t>(16) * pr.r;
-          int c = 0;
-          for (; c + 8 <= pr.t_slices; c += 8) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = __ldcg(src + (c + e) * stride);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v += x[e];
-          }
-          for (; c < pr.t_slices; ++c) v += __ldcg(src + c * stride);
-        }
-        if (tok < pr.m && pr.t_save) pr.t_save[tok * pr.r + j] = v;
-        pr.st[tok * pr.r + j] = __float2bfloat16_rn(tok < pr.m ? __fmul_rn(v, pr.scale) : 0.f);
-      }
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) atomicAdd(pr.cnt, 1u);  // count = t_slices + 1: sT published
-    }
-    __syncthreads();
+    if (threadIdx.x == 0) dc_arrive(pr.cnt);  // count == t_slices: every slice partial of the problem is written
   }
 
   // ---------------------------------------------------------------- W units
   if (u_begin >= u_end) return;
-  // A unit's description; looked up once per unit (binary search over the problem list).
+  // A unit's place: problem, row tile, 256-k unit within the tile, blocks in the unit.  Found by a
+  // binary search and one division at the start of the run; after that the cursors step (the
+  // units of a run are consecutive: k units of a tile, then the next tile, then the next problem).
   struct Unit {
     int pi, tile, kun, nb;  // nb: blocks in the unit (the last unit of a row may hold fewer than 4)
   };
+  auto unit_nb = [&](const Unit& d) { return min(kDcUnitBlocks, p.prob[d.pi].k / 64 - d.kun * kDcUnitBlocks); };
   auto describe = [&](long long uu) {
     Unit d;
     d.pi = dc_find_prob(p, uu);
     const DcProb& pr = p.prob[d.pi];
-    const long long w = uu - pr.u0_w;
-    d.tile = static_cast<int>(w / pr.ku);
-    d.kun = static_cast<int>(w % pr.ku);
-    d.nb = min(kDcUnitBlocks, pr.k / 64 - d.kun * kDcUnitBlocks);
+    const int w = static_cast<int>(uu - pr.u0_w);
+    d.tile = w / pr.ku;
+    d.kun = w - d.tile * pr.ku;
+    d.nb = unit_nb(d);
     return d;
+  };
+  auto step_unit = [&](Unit& d) {
+    if (++d.kun == p.prob[d.pi].ku) {
+      d.kun = 0;
+      if (++d.tile == p.prob[d.pi].tiles) {
+        d.tile = 0;
+        if (d.pi + 1 < p.count) ++d.pi;
+      }
+    }
+    d.nb = unit_nb(d);
   };
   // ---- the cp.async stager: runs kDcRing - 1 blocks ahead of the consumer through the run
   const uint32_t stage_dst0 = smem_u32(&s_ring[warp][0][0]) + (lane >> 1) * kDcPitch + (lane & 1) * 16;
   long long st_u = u_begin;
-  int st_kb = 0, st_nb = 0, st_slot = 0;
+  int st_kb = 0, st_slot = 0;
+  Unit st_d = describe(u_begin);
   const uint8_t* st_src = nullptr;
   bool st_ok = false;
   auto st_enter = [&]() {
-    if (st_u >= u_end) return;
-    const Unit d = describe(st_u);
-    const DcProb& pr = p.prob[d.pi];
-    const int row = d.tile * kDcRows + warp * 16 + (lane >> 1);
+    const DcProb& pr = p.prob[st_d.pi];
+    const int row = st_d.tile * kDcRows + warp * 16 + (lane >> 1);
     st_ok = row < pr.n;
-    st_src = pr.codes + (st_ok ? static_cast<int64_t>(row) * (pr.k / 2) + d.kun * 128 + (lane & 1) * 16 : 0);
-    st_nb = d.nb;
+    st_src = pr.codes + (st_ok ? static_cast<int64_t>(row) * (pr.k / 2) + st_d.kun * 128 + (lane & 1) * 16 : 0);
     st_kb = 0;
   };
   auto stage_next = [&]() {
     if (st_u < u_end) {
       cp_async16(stage_dst0 + st_slot * kDcStage, st_src, st_ok);
       st_src += 32;
-      if (++st_kb == st_nb) {
+      if (++st_kb == st_d.nb) {
         ++st_u;
+        step_unit(st_d);
         st_enter();
       }
     }
@@ -397,6 +380,8 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
   Unit cd = describe(cu);
   Scales sc_cur, sc_nxt;
   load_scales(cd, sc_cur);
+  // the rolling L2 prefetch cursor, kDcPrefetchUnits units ahead of the consumer
+  Unit pf_d = describe(u_begin + kDcPrefetchUnits < u_end ? u_begin + kDcPrefetchUnits : u_begin);
 
   float run[NG][4];
   auto zero_run = [&]() {
@@ -462,14 +447,14 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
         for (int e = 0; e < 4; ++e) vals[t][e] = run[t][e];
     }
     if (!finalise) return;
-    // wait until the problem's sT is published (count t_slices + 1)
+    // wait until every X A^T slice of the problem is written (count == t_slices)
     if (threadIdx.x == 0) {
-      const unsigned want = static_cast<unsigned>(pr.t_slices) + 1u;
-      bool ok = *reinterpret_cast<volatile unsigned*>(pr.cnt) == want;
+      const unsigned want = static_cast<unsigned>(pr.t_slices);
+      bool ok = *reinterpret_cast<volatile unsigned*>(pr.cnt) >= want;
       if (!ok) {
         const uint64_t t0 = globaltimer_ns();
         for (uint32_t it = 1;; ++it) {
-          if (*reinterpret_cast<volatile unsigned*>(pr.cnt) == want) { ok = true; break; }
+          if (*reinterpret_cast<volatile unsigned*>(pr.cnt) >= want) { ok = true; break; }
           if ((it & 63u) == 0 && globaltimer_ns() - t0 > p.wait_ns) break;
           __nanosleep(64);
         }
@@ -480,6 +465,38 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     __syncthreads();
     if (!s_flag) { alive = false; return; }
     __threadfence();
+    // sT = bf16(s X A^T) for this problem, the slices' partials added in slice order (every
+    // finaliser of the problem adds the same values in the same order); the finaliser of tile 0
+    // also writes t_save.  Kept in shared memory as bf16 pairs [16 tokens][64 pairs].
+    uint32_t* s_st = reinterpret_cast<uint32_t*>(&s_red[0][0][0]);
+    {
+      const int rpad = (pr.r + 15) & ~15, hp = rpad / 2;
+      const int64_t cstride = static_cast<int64_t>(16) * pr.r;
+      for (int i = threadIdx.x; i < 16 * hp; i += kDcThreads) {
+        const int tok = i / hp, jp = i % hp, j = 2 * jp;
+        float v0 = 0.f, v1 = 0.f;
+        if (tok < pr.m) {
+          const float* src = pr.tpart + static_cast<int64_t>(tok) * pr.r + j;
+          float x0[kDcMaxSlices], x1[kDcMaxSlices];
+#pragma unroll
+          for (int c = 0; c < kDcMaxSlices; ++c) {
+            x0[c] = (c < pr.t_slices && j < pr.r) ? __ldcg(src + c * cstride) : 0.f;
+            x1[c] = (c < pr.t_slices && j + 1 < pr.r) ? __ldcg(src + c * cstride + 1) : 0.f;
+          }
+#pragma unroll
+          for (int c = 0; c < kDcMaxSlices; ++c) {
+            v0 += x0[c];
+            v1 += x1[c];
+          }
+          if (tile == 0 && pr.t_save) {
+            if (j < pr.r) pr.t_save[tok * pr.r + j] = v0;
+            if (j + 1 < pr.r) pr.t_save[tok * pr.r + j + 1] = v1;
+          }
+        }
+        s_st[tok * 64 + jp] = tok < pr.m ? pack_bf16x2_rn(__fmul_rn(v0, pr.scale), __fmul_rn(v1, pr.scale)) : 0u;
+      }
+    }
+    __syncthreads();
     // y = vals + sT B^T: the LoRA up-projection as extra 16-wide k chunks of the same MMA
     // (A = rows of B, k = j; B operand = sT [tok][j]), accumulated in float32
     const int row0 = rbase + g, row1 = row0 + 8;
@@ -491,9 +508,8 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
                                    : make_uint2(0u, 0u);
 #pragma unroll
       for (int t = 0; t < NG; ++t) {
-        const int tok = t * 8 + g;
-        const uint2 sb = tok < pr.m ? dc_ld_bf16x4(pr.st + tok * pr.r, jq, pr.r, false) : make_uint2(0u, 0u);
-        dc_mma(vals[t], b0.x, b1.x, b0.y, b1.y, sb.x, sb.y);
+        const uint32_t* sp = s_st + (t * 8 + g) * 64 + jq / 2;
+        dc_mma(vals[t], b0.x, b1.x, b0.y, b1.y, sp[0], sp[1]);
       }
     }
     const int rows[2] = {row0, row1};
@@ -533,17 +549,18 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
       cur_tile = cd.tile;
       zero_run();
     }
-    // the next unit: its description, its block scales, and its L2 prefetch kDcPrefetchUnits ahead
+    // the next unit: its place, its block scales, and the L2 prefetch kDcPrefetchUnits ahead
     Unit nd = cd;
-    if (cu + 1 < u_end) {
-      nd = describe(cu + 1);
-      load_scales(nd, sc_nxt);
-    }
-    if (cu + kDcPrefetchUnits < u_end && lane < 16) {
-      const Unit f = describe(cu + kDcPrefetchUnits);
-      const DcProb& pf = p.prob[f.pi];
-      const int row = f.tile * kDcRows + warp * 16 + lane;
-      if (row < pf.n) dc_prefetch_codes(pf.codes + static_cast<int64_t>(row) * (pf.k / 2) + f.kun * 128, f.nb * 32);
+    step_unit(nd);
+    if (cu + 1 < u_end) load_scales(nd, sc_nxt);
+    if (cu + kDcPrefetchUnits < u_end) {
+      if (lane < 16) {
+        const DcProb& pf = p.prob[pf_d.pi];
+        const int row = pf_d.tile * kDcRows + warp * 16 + lane;
+        if (row < pf.n)
+          dc_prefetch_codes(pf.codes + static_cast<int64_t>(row) * (pf.k / 2) + pf_d.kun * 128, pf_d.nb * 32);
+      }
+      step_unit(pf_d);
     }
     // this lane's token rows of X for the unit (tokens g and g + 8), chunk c at +16 c, block b at +64 b
     const int k0 = cd.kun * kDcUnitBlocks * 64 + 4 * q;
@@ -612,7 +629,7 @@ struct DcPlan {
   int grid, maxseg, slices;
   long long units;
   size_t ws_bytes;
-  std::vector<size_t> off_cnt, off_tpart, off_st, off_ypart;
+  std::vector<size_t> off_cnt, off_tpart, off_ypart;
   std::vector<int> t_slices, t_w, s0, tiles, ku;
   std::vector<long long> u0_w;
 };
@@ -648,6 +665,7 @@ DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
     const double share = static_cast<double>((probs[i].r + 15) / 16) * probs[i].w.k / work;
     int want = static_cast<int>(share * pl.grid + 0.5);
     want = want < 1 ? 1 : (want > blocks ? blocks : want);
+    if (want > kDcMaxSlices) want = kDcMaxSlices;
     pl.t_w[i] = (blocks + want - 1) / want;
     pl.t_slices[i] = (blocks + pl.t_w[i] - 1) / pl.t_w[i];
     pl.s0[i] = sl;
@@ -666,15 +684,12 @@ DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
   size_t off = 0;
   pl.off_cnt.resize(count);
   pl.off_tpart.resize(count);
-  pl.off_st.resize(count);
   pl.off_ypart.resize(count);
   for (int i = 0; i < count; ++i) {
     pl.off_cnt[i] = off;
     off += al256(static_cast<size_t>(2 + pl.tiles[i]) * 4);
     pl.off_tpart[i] = off;
     off += al256(static_cast<size_t>(pl.t_slices[i]) * 16 * probs[i].r * 4);
-    pl.off_st[i] = off;
-    off += al256(static_cast<size_t>(16) * probs[i].r * 2);
     pl.off_ypart[i] = off;
     off += al256(static_cast<size_t>(pl.tiles[i]) * pl.maxseg * 16 * kDcRows * 4);
   }
@@ -716,7 +731,6 @@ cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, unsi
     d.y = g.y;
     d.t_save = g.t_save;
     d.tpart = reinterpret_cast<float*>(base + pl.off_tpart[i]);
-    d.st = reinterpret_cast<__nv_bfloat16*>(base + pl.off_st[i]);
     d.ypart = reinterpret_cast<float*>(base + pl.off_ypart[i]);
     d.cnt = reinterpret_cast<unsigned*>(base + pl.off_cnt[i]);
     d.n = static_cast<int>(g.w.n);
