@@ -109,6 +109,15 @@ __device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
   asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
+// The same load predicated in the instruction itself (zero when `on` is false; no branch).
+__device__ __forceinline__ uint2 ldg_nc_v2_if(const void* p, bool on) {
+  uint2 v = make_uint2(0u, 0u);
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q ld.global.nc.v2.u32 {%0,%1}, [%3];\n\t}"
+      : "+r"(v.x), "+r"(v.y)
+      : "r"(static_cast<int>(on)), "l"(p));
+  return v;
+}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
@@ -233,13 +242,22 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
       dc_prefetch_codes(pr.a + static_cast<int64_t>(j) * pr.k + kb0 * 64, (kb1 - kb0) * 128);
   }
   {
-    constexpr uint32_t hex[16] = QLORA_NF4_LEVELS_HEX;
+    // the 16 bf16 levels go through shared memory (a dynamically indexed local array would put
+    // the whole kernel on a stack frame)
+    __shared__ uint32_t s_lv[16];
+    if (threadIdx.x < 16) {
+      constexpr uint32_t hex[16] = QLORA_NF4_LEVELS_HEX;
+      uint32_t v = 0;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v = threadIdx.x == c ? hex[c] : v;
+      s_lv[threadIdx.x] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v)));
+    }
+    __syncthreads();
     for (int i = threadIdx.x; i < 256 * 32; i += kDcThreads) {
       const int b = i >> 5;
-      const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(hex[b >> 4])));
-      const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(hex[b & 15])));
-      s_lut[i] = lo | (hi << 16);
+      s_lut[i] = s_lv[b >> 4] | (s_lv[b & 15] << 16);
     }
+    __syncthreads();  // a CTA with no T slice reads the table next
   }
   // X, sT, the counters and the workspace may come from earlier kernels of the stream
   griddep_wait();
@@ -327,6 +345,7 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
   const uint32_t stage_dst0 = smem_u32(&s_ring[warp][0][0]) + (lane >> 1) * kDcPitch + (lane & 1) * 16;
   long long st_u = u_begin;
   int st_kb = 0, st_slot = 0;
+  int st_left = static_cast<int>(u_end - u_begin);  // units the stager has not finished
   Unit st_d = describe(u_begin);
   const uint8_t* st_src = nullptr;
   bool st_ok = false;
@@ -338,11 +357,12 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     st_kb = 0;
   };
   auto stage_next = [&]() {
-    if (st_u < u_end) {
+    if (st_left > 0) {
       cp_async16(stage_dst0 + st_slot * kDcStage, st_src, st_ok);
       st_src += 32;
       if (++st_kb == st_d.nb) {
         ++st_u;
+        --st_left;
         step_unit(st_d);
         st_enter();
       }
@@ -565,8 +585,12 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     // this lane's token rows of X for the unit (tokens g and g + 8), chunk c at +16 c, block b at +64 b
     const int k0 = cd.kun * kDcUnitBlocks * 64 + 4 * q;
     const __nv_bfloat16* xp[NG];
+    bool xon[NG];
 #pragma unroll
-    for (int t = 0; t < NG; ++t) xp[t] = (t * 8 + g < pr.m) ? pr.x + static_cast<int64_t>(t * 8 + g) * pr.k + k0 : nullptr;
+    for (int t = 0; t < NG; ++t) {
+      xon[t] = t * 8 + g < pr.m;  // rows of absent tokens read as zero (the pointer stays inside X)
+      xp[t] = pr.x + static_cast<int64_t>(xon[t] ? t * 8 + g : 0) * pr.k + k0;
+    }
 #pragma unroll
     for (int b = 0; b < kDcUnitBlocks; ++b) {
       if (b >= cd.nb) break;
@@ -574,7 +598,7 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
 #pragma unroll
       for (int t = 0; t < NG; ++t)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) xf[c][t] = xp[t] ? ldg_nc_v2(xp[t] + b * 64 + 16 * c) : make_uint2(0u, 0u);
+        for (int c = 0; c < 4; ++c) xf[c][t] = ldg_nc_v2_if(xp[t] + b * 64 + 16 * c, xon[t]);
       stage_next();
       cp_async_wait<kDcRing - 1>();
       __syncwarp();
