@@ -5,46 +5,52 @@
 // and adds the LoRA output; Day 25 notes, section 4.4: inference runs the
 // 4-bit base with the adapter attached.  With a handful of tokens the step is a
 // stream over the weight codes, so the kernel is built around keeping HBM busy
-// across calls: a decoder layer makes four dependent calls (q,k,v | o |
-// gate,up | down), each only a few microseconds of HBM time.
+// and the chain of dependent steps inside one call short: a decoder layer
+// makes four dependent calls (q,k,v | o | gate,up | down), each only a few
+// microseconds of HBM time.
 //
-// Across calls (programmatic dependent launch): each CTA first issues L2
-// prefetches (one plain prefetch per 128-byte line) for the code bytes it will read first -- the weights do not depend on
-// the previous kernel -- and only then waits (griddepcontrol.wait) for the
-// preceding kernel of the stream; right after that wait it lets the next
-// kernel launch, which prefetches its own weights while this one computes.
+// Across calls (programmatic dependent launch): before it waits for the
+// preceding kernel of the stream (griddepcontrol.wait), each CTA issues L2
+// prefetches for the first tiles of its run and starts its cp.async ring on
+// their code bytes -- weights, scales and B do not depend on the previous
+// kernel.  So the codes are read before the wait: a kernel that writes a
+// weight record must not let its dependents launch early (the quantiser's
+// last kernel does not).  Right after the wait it lets the next kernel launch.
 //
-// Work: first, X A^T is cut into about one k-slice per CTA (slice i on CTA
-// i % grid, the 8 warps splitting its 16-k chunks); the last slice of a
-// problem adds the slices' partials in slice order and publishes
-// sT = bf16(s X A^T).  Then the weights are cut into W units of equal size
-// (problem, tile of 128 rows, 256 k) and every CTA (two per SM) takes one
-// contiguous run of them.  A run accumulates the units of one row tile in
-// registers; a tile split between runs leaves float32 partials that the last
-// arriving CTA adds in run order (deterministic).  The tile's finaliser adds
-// the LoRA term with sT; a finaliser that gets there first waits for it
-// (bounded wait; every CTA of the grid is resident: the grid has at most one
-// CTA per SM and the next kernel can only launch after every CTA of this one
-// has started).
+// Work: a TILE is 16 rows of one problem over the whole of k.  Tiles are
+// dealt to the CTAs (two per SM) in contiguous runs of balanced cost; within a
+// tile the 8 warps split the 64-wide absmax blocks of k into 8 contiguous
+// ranges, and at the end of the tile their float32 partial sums are added in
+// warp order in shared memory.  No tile is split between CTAs, so there is no
+// cross-CTA reduction of Y and the result does not depend on the grid.
 //
-// A W unit: warp w owns rows 16w .. 16w+15 of the tile; per 64-wide absmax
-// block, lanes stage the 16 rows x 32 code bytes into a shared-memory ring with
-// cp.async (kDcRing blocks ahead; the block scales are loaded two blocks
-// ahead, the X fragments before the decode), decode them with the byte-permute table of
-// the bf16 NF4 levels into mma.sync m16n8k16 A fragments (k permuted so lane
-// (g, q) holds k = 16c + 4q .. 4q+3 of chunk c), and multiply with the X
-// fragments (8 tokens per MMA, 1 or 2 groups) into a per-block accumulator,
-// which is scaled by the block's restored scale a' and added to the run's sum.
-// So the effective weight is bf16(L[code]) * a' with a' applied in float32 to
-// the block's partial sums (within 2^-8 relative of the bf16_rn(L a') the
-// fwd/bwd GEMMs use).
+// X A^T is cut into at most 16 k-slices per problem (slice i on CTA i % grid,
+// computed before the CTA's tiles); each slice's partial is published with a
+// counter, and the first tile of a problem in a CTA's run waits (bounded) for
+// them and adds them in slice order into sT = bf16(s X A^T), kept in shared
+// memory for the following tiles of the problem.  The tile's epilogue then adds
+// sT B^T (a float32 FMA chain in j order) and writes y.  Every CTA of the grid
+// is resident at once (grid <= 2 x SMs), so the waits always end.
 //
-// Counters are plain words updated with one atomic add each (many CTAs arrive
-// on the same word, so no retry loops); every counter is returned to zero by
-// its last user, so a workspace that starts zeroed stays zeroed across calls
-// and graph replays.
+// A block of a warp: lanes stage the 16 rows x 32 code bytes into a per-warp
+// shared-memory ring with cp.async (kDcRing blocks ahead, across tiles);
+// lane (g, q) then reads bytes 8q .. 8q+7 of rows g and g + 8 (elements 16q ..
+// 16q+15 of the block) and turns each byte into its bf16 level pair with one
+// lookup in a byte-indexed table, giving mma.sync m16n8k16 A fragments for the
+// k permutation "MMA c, slots (2q, 2q+1) <- elements 16q+4c, +1; slots (2q+8,
+// 2q+9) <- elements 16q+4c+2, +3"; the X fragment of the same permutation is
+// X[tok][16q .. 16q+15], two 16-byte loads.  The block's product (8 tokens per
+// MMA, 1 or 2 groups) is scaled by the block's restored scale a' in float32
+// and added to the warp's sum.  So the effective weight is bf16(L[code]) * a'
+// (within 2^-8 relative of the bf16_rn(L a') the fwd/bwd GEMMs use).
+//
+// Counters (per problem: X A^T slices published, tiles finished) are plain
+// words updated with one atomic add each; the last finisher of a problem
+// returns both to zero, so a workspace that starts zeroed stays zeroed across
+// calls and graph replays.
 #include <algorithm>
 #include <cstdio>
+#include <mutex>
 #include <vector>
 
 #include "common.cuh"
@@ -55,14 +61,19 @@ namespace qlora {
 constexpr int kDcWarps = 8;
 constexpr int kDcCtasPerSm = 2;            // two CTAs (16 warps) per SM hide the decode's latency
 constexpr int kDcThreads = kDcWarps * 32;
-constexpr int kDcRows = kDcWarps * 16;     // rows per tile
-constexpr int kDcUnitBlocks = 4;           // 64-wide blocks per W unit (256 k)
-constexpr int kDcRing = 6;                 // cp.async ring depth per warp, in blocks
-constexpr int kDcPitch = 48;               // shared-memory bytes per staged row piece (32 used, padded: no bank conflicts)
-constexpr int kDcStage = 16 * kDcPitch;    // one block of the warp's 16 rows
+constexpr int kDcTileRows = 16;            // rows per tile (the MMA's m)
+constexpr int kDcRing = 8;                 // cp.async ring depth per warp, in blocks
+constexpr int kDcSlot = kDcTileRows * 32;  // one staged block: 16 rows x 32 code bytes, rows packed
 constexpr int kDcMaxProbs = 128;
-constexpr int kDcPrefetchUnits = 24;
-constexpr int kDcMaxSlices = 16;           // X A^T slices per problem (each finaliser adds them all)       // W units a CTA keeps prefetched into L2 ahead of its consumer
+constexpr int kDcMaxSlices = 16;           // X A^T slices per problem (each first tile adds them all)
+constexpr int kDcPrefetchTiles = 4;        // tiles of its run a CTA keeps prefetched into L2 ahead
+constexpr int kDcMaxCtas = 320;            // run table size (>= kDcCtasPerSm x SMs)
+constexpr int kDcMaxR = 128;
+// dynamic shared memory: ring | Y partials [2][warps][16 tok][16 rows] | sT [16 tok][128] (float)
+constexpr size_t kDcRingBytes = static_cast<size_t>(kDcWarps) * kDcRing * kDcSlot;
+constexpr size_t kDcRedBytes = 2ull * kDcWarps * 16 * 16 * 4;
+constexpr size_t kDcTBytes = 16ull * kDcMaxR * 4;
+constexpr size_t kDcDynSmem = kDcRingBytes + kDcRedBytes + kDcTBytes;
 
 struct DcProb {
   const uint8_t* codes;
@@ -75,23 +86,20 @@ struct DcProb {
   __nv_bfloat16* y;         // [m, n]
   float* t_save;            // [m, r] or null
   float* tpart;             // [t_slices][16][r] partial X A^T
-  float* ypart;             // [tiles][maxseg][16][128] partial Y
-  unsigned* cnt;            // [2 + tiles]: T, tiles done, then one per tile (zero between calls)
+  unsigned* cnt;            // [2]: X A^T slices published, tiles finished (zero between calls)
   int n, k, m, r;
   float scale;
   int t_slices, t_w, s0;    // X A^T: slices of t_w 64-wide blocks, first global slice
-  int tiles, ku;            // row tiles, W units per tile (ceil(k / 256))
-  long long u0_w;           // first W unit (global unit index)
+  int tiles, u0;            // 16-row tiles, first global tile
 };
 
 struct DcParams {
   int count;
   int grid;
-  int maxseg;
-  long long units;            // W units of the call
   int slices;                 // X A^T slices of the call (slice i goes to CTA i % grid)
   unsigned long long wait_ns;
   unsigned* status;
+  int run0[kDcMaxCtas + 1];   // CTA c takes the global tiles [run0[c], run0[c + 1])
   DcProb prob[kDcMaxProbs];
 };
 
@@ -109,12 +117,12 @@ __device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
   asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
-// The same load predicated in the instruction itself (zero when `on` is false; no branch).
-__device__ __forceinline__ uint2 ldg_nc_v2_if(const void* p, bool on) {
-  uint2 v = make_uint2(0u, 0u);
+// A 16-byte load predicated in the instruction itself (zero when `on` is false; no branch).
+__device__ __forceinline__ uint4 ldg_nc_v4_if(const void* p, bool on) {
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
   asm volatile(
-      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q ld.global.nc.v2.u32 {%0,%1}, [%3];\n\t}"
-      : "+r"(v.x), "+r"(v.y)
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %4, 0;\n\t@q ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%5];\n\t}"
+      : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
       : "r"(static_cast<int>(on)), "l"(p));
   return v;
 }
@@ -132,32 +140,25 @@ __device__ __forceinline__ void prefetch_l2_line(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
-// L2 prefetch of `bytes` bytes from p: one plain prefetch per 128-byte line touched (regular
-// memory instructions: a warp covers 32 lines per instruction, unlike one bulk copy per row).
-__device__ __forceinline__ void dc_prefetch_codes(const void* p, int bytes) {
+// L2 prefetch of [p, p + bytes) by `nthr` threads (this one is `tid`): one plain prefetch per
+// 128-byte line.
+__device__ __forceinline__ void dc_prefetch_range(const void* p, int64_t bytes, int tid, int nthr) {
+  if (bytes <= 0) return;
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(p) & ~uintptr_t(127);
-  const uintptr_t a1 = reinterpret_cast<uintptr_t>(p) + bytes;
-  for (uintptr_t a = a0; a < a1; a += 128) prefetch_l2_line(reinterpret_cast<const void*>(a));
-}
-
-// First unit of CTA c when `units` units are dealt to `grid` CTAs in contiguous runs.
-__device__ __forceinline__ long long dc_run_start(int c, long long units, int grid) {
-  return static_cast<long long>(c) * units / grid;
-}
-// CTA whose run holds unit u.
-__device__ __forceinline__ int dc_cta_of(long long u, long long units, int grid) {
-  return static_cast<int>(((u + 1) * grid - 1) / units);
+  const uintptr_t a1 = reinterpret_cast<uintptr_t>(p) + static_cast<uintptr_t>(bytes);
+  for (uintptr_t a = a0 + static_cast<uintptr_t>(tid) * 128; a < a1; a += static_cast<uintptr_t>(nthr) * 128)
+    prefetch_l2_line(reinterpret_cast<const void*>(a));
 }
 
 // Arrive on a counter (one atomic, no retry loop: many CTAs arrive on the same word); returns
-// the count after this arrival.  Every counter is returned to zero by its last user.
-__device__ __forceinline__ uint32_t dc_arrive(unsigned* c) { return atomicAdd(c, 1u) + 1u; }
+// the count after this arrival.
+__device__ __forceinline__ uint32_t dc_arrive(unsigned* c, unsigned v = 1u) { return atomicAdd(c, v) + v; }
 
-__device__ __forceinline__ int dc_find_prob(const DcParams& p, long long u) {  // problem of W unit u
+__device__ __forceinline__ int dc_find_tile(const DcParams& p, int t) {  // problem of global tile t
   int lo = 0, hi = p.count - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (p.prob[mid].u0_w <= u) lo = mid; else hi = mid - 1;
+    if (p.prob[mid].u0 <= t) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -170,81 +171,63 @@ __device__ __forceinline__ int dc_find_slice(const DcParams& p, int sl) {  // pr
   return lo;
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+__device__ __forceinline__ uint2 lds64(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
   return v;
 }
-// Decode one 32-bit word of packed codes (byte b: element 2b in the high nibble, 2b+1 in the low)
-// into 4 bf16x2 words (element 2i in the low half of out[i]) through this lane's column of the
-// level-pair table (row stride 128 bytes).
-__device__ __forceinline__ void dc_decode_word(uint32_t lut_lane, uint32_t w, uint32_t (&out)[4]) {
-  out[0] = lds32(lut_lane + ((w << 7) & 0x7f80u));
-  out[1] = lds32(lut_lane + ((w >> 1) & 0x7f80u));
-  out[2] = lds32(lut_lane + ((w >> 9) & 0x7f80u));
-  out[3] = lds32(lut_lane + ((w >> 17) & 0x7f80u));
-}
 
-// Four bf16 values row[j .. j+3] of a row of length r (zero past r) as two bf16x2 words.
-// `readonly`: the row is not written during the kernel (non-coherent path); otherwise it is read
-// through L2 (sT, written by another CTA of this grid).
-__device__ __forceinline__ uint2 dc_ld_bf16x4(const __nv_bfloat16* row, int j, int r, bool readonly) {
-  if ((r & 3) == 0 && j + 4 <= r) {  // 8-byte aligned: rows of r % 4 == 0 values, j % 4 == 0
-    if (readonly) return ldg_nc_v2(row + j);
-    return __ldcg(reinterpret_cast<const uint2*>(row + j));
+// First 64-wide block of warp w's share of a row of nbk blocks (the 8 warps take contiguous ranges).
+__device__ __forceinline__ int dc_warp_block(int w, int nbk) { return (w * nbk) >> 3; }
+
+// L2 prefetch of tile t_local of problem pr (codes, raw scales, rows of B) by the CTA's threads.
+__device__ __forceinline__ void dc_prefetch_tile(const DcProb& pr, int t_local) {
+  const int r0 = t_local * kDcTileRows, rows = min(kDcTileRows, pr.n - r0), nbk = pr.k >> 6;
+  dc_prefetch_range(pr.codes + static_cast<int64_t>(r0) * (pr.k >> 1), static_cast<int64_t>(rows) * (pr.k >> 1),
+                    threadIdx.x, kDcThreads);
+  dc_prefetch_range(pr.absq + static_cast<int64_t>(r0) * nbk, static_cast<int64_t>(rows) * nbk, threadIdx.x,
+                    kDcThreads);
+  dc_prefetch_range(pr.b + static_cast<int64_t>(r0) * pr.r, static_cast<int64_t>(rows) * pr.r * 2, threadIdx.x,
+                    kDcThreads);
+  if (threadIdx.x == 0) {
+    const int64_t s0 = (static_cast<int64_t>(r0) * nbk) >> 8, s1 = (static_cast<int64_t>(r0 + rows) * nbk - 1) >> 8;
+    dc_prefetch_range(pr.step + s0, (s1 - s0 + 1) * 4, 0, 1);
   }
-  const unsigned short* u = reinterpret_cast<const unsigned short*>(row);
-  uint32_t v[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) v[e] = j + e < r ? (readonly ? __ldg(u + j + e) : __ldcg(u + j + e)) : 0u;
-  return make_uint2(v[0] | (v[1] << 16), v[2] | (v[3] << 16));
-}
-
-// X fragment of chunk c (16 k at k0 + 16 c) for token group tg: b0 = X[tok][k + 4q .. +1], b1 = X[tok][k + 4q + 2 .. +3].
-__device__ __forceinline__ uint2 dc_xfrag(const DcProb& pr, int tok, int kk) {
-  if (tok >= pr.m) return make_uint2(0u, 0u);
-  return ldg_nc_v2(pr.x + static_cast<int64_t>(tok) * pr.k + kk);
 }
 
 template <int NG>
 __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __grid_constant__ DcParams p) {
-  __shared__ __align__(16) uint8_t s_ring[kDcWarps][kDcRing][kDcStage];
-  __shared__ float s_red[kDcWarps][16][16];
-  __shared__ int s_flag;
   // level pairs of a code byte: s_lut[b * 32 + lane] = bf16 L[b >> 4] | (bf16 L[b & 15]) << 16, the
-  // byte's two weights in mma fragment order; one column per lane, so lookups never conflict
-  extern __shared__ __align__(16) uint32_t s_lut[];
+  // byte's two weights in mma fragment order; one column per lane, so lookups never conflict.  A
+  // static array: a lookup is one shared load at [index + the table's fixed address].
+  __shared__ __align__(16) uint32_t s_lut[256 * 32];
+  __shared__ uint32_t s_lv[16];
+  __shared__ int s_flag;
+  extern __shared__ __align__(16) uint8_t s_dyn[];
+  float* s_red = reinterpret_cast<float*>(s_dyn + kDcRingBytes);                 // [2][warps][16][16]
+  float* s_t = reinterpret_cast<float*>(s_dyn + kDcRingBytes + kDcRedBytes);     // [16][kDcMaxR]
+
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, q = lane & 3;
-  const long long u_begin = dc_run_start(blockIdx.x, p.units, p.grid);
-  const long long u_end = dc_run_start(blockIdx.x + 1, p.units, p.grid);
+  const int t_begin = p.run0[blockIdx.x], t_end = p.run0[blockIdx.x + 1];
 
-  // ---------------------------------------------------------------- L2 prefetch (before the wait)
-  // the first kDcPrefetchUnits W units of this run (every unit's codes when the call is a decoder
-  // stage; later units of long lists are prefetched as the run advances) and this CTA's T slices
-  for (long long u = u_begin; u < u_end && u < u_begin + kDcPrefetchUnits; ++u) {
-    const DcProb& pr = p.prob[dc_find_prob(p, u)];
-    const long long w = u - pr.u0_w;
-    const int tile = static_cast<int>(w / pr.ku), kun = static_cast<int>(w % pr.ku);
-    const int nb = min(kDcUnitBlocks, pr.k / 64 - kun * kDcUnitBlocks);  // the last unit of a row may be short
-    for (int i = threadIdx.x; i < kDcRows; i += kDcThreads) {
-      const int row = tile * kDcRows + i;
-      if (row < pr.n) {
-        dc_prefetch_codes(pr.codes + static_cast<int64_t>(row) * (pr.k / 2) + kun * 128, nb * 32);
-        prefetch_l2_line(pr.absq + static_cast<int64_t>(row) * (pr.k / 64) + kun * kDcUnitBlocks);
-      }
+  // ---------------------------------------------------------------- prologue (before the wait)
+  if (t_begin < t_end) {
+    int pi = dc_find_tile(p, t_begin);
+    for (int t = t_begin; t < t_end && t < t_begin + kDcPrefetchTiles; ++t) {
+      if (t - p.prob[pi].u0 == p.prob[pi].tiles) ++pi;
+      dc_prefetch_tile(p.prob[pi], t - p.prob[pi].u0);
     }
   }
   for (int sl = blockIdx.x; sl < p.slices; sl += p.grid) {
     const DcProb& pr = p.prob[dc_find_slice(p, sl)];
     const int kb0 = (sl - pr.s0) * pr.t_w, kb1 = min(pr.k / 64, kb0 + pr.t_w);
-    for (int j = threadIdx.x; j < pr.r; j += kDcThreads)
-      dc_prefetch_codes(pr.a + static_cast<int64_t>(j) * pr.k + kb0 * 64, (kb1 - kb0) * 128);
+    for (int j = warp; j < pr.r; j += kDcWarps)
+      dc_prefetch_range(pr.a + static_cast<int64_t>(j) * pr.k + kb0 * 64, (kb1 - kb0) * 128, lane, 32);
   }
   {
     // the 16 bf16 levels go through shared memory (a dynamically indexed local array would put
     // the whole kernel on a stack frame)
-    __shared__ uint32_t s_lv[16];
     if (threadIdx.x < 16) {
       constexpr uint32_t hex[16] = QLORA_NF4_LEVELS_HEX;
       uint32_t v = 0;
@@ -257,13 +240,51 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
       const int b = i >> 5;
       s_lut[i] = s_lv[b >> 4] | (s_lv[b & 15] << 16);
     }
-    __syncthreads();  // a CTA with no T slice reads the table next
   }
-  // X, sT, the counters and the workspace may come from earlier kernels of the stream
+
+  // ---- the cp.async stager: runs kDcRing - 1 blocks ahead of the consumer through the whole run
+  // (tiles, then problems); lane l copies bytes 16 (l & 1) .. +15 of row l >> 1 of each block.
+  const uint32_t ring0 = smem_u32(s_dyn) + warp * (kDcRing * kDcSlot);
+  const uint32_t stage_lane = ring0 + (lane >> 1) * 32 + (lane & 1) * 16;
+  int st_t = t_begin, st_pi = t_begin < t_end ? dc_find_tile(p, t_begin) : 0;
+  int st_kb = 0, st_kb1 = 0, st_slot = 0;
+  const uint8_t* st_src = nullptr;
+  bool st_ok = false;
+  // place the stager on the first tile at or after st_t where this warp has blocks
+  auto st_enter = [&]() {
+    for (; st_t < t_end; ++st_t) {
+      if (st_t - p.prob[st_pi].u0 == p.prob[st_pi].tiles) ++st_pi;
+      const DcProb& pr = p.prob[st_pi];
+      const int nbk = pr.k >> 6;
+      st_kb = dc_warp_block(warp, nbk);
+      st_kb1 = dc_warp_block(warp + 1, nbk);
+      if (st_kb == st_kb1) continue;
+      const int row = (st_t - pr.u0) * kDcTileRows + (lane >> 1);
+      st_ok = row < pr.n;
+      st_src = pr.codes + (st_ok ? static_cast<int64_t>(row) * (pr.k >> 1) + st_kb * 32 + (lane & 1) * 16 : 0);
+      return;
+    }
+  };
+  auto stage_next = [&]() {
+    if (st_t < t_end) {
+      cp_async16(stage_lane + st_slot * kDcSlot, st_src, st_ok);
+      st_src += 32;
+      if (++st_kb == st_kb1) {
+        ++st_t;
+        st_enter();
+      }
+    }
+    cp_async_commit();
+    st_slot = st_slot + 1 == kDcRing ? 0 : st_slot + 1;
+  };
+  st_enter();
+  for (int i = 0; i < kDcRing - 1; ++i) stage_next();
+
+  // X, the counters and the workspace may come from earlier kernels of the stream
   griddep_wait();
   griddep_launch_dependents();
 
-  // ---------------------------------------------------------------- T = X A^T, spread over every CTA
+  // ---------------------------------------------------------------- X A^T slices
   // slice sl (problem p, 64-wide blocks [kb0, kb1)) goes to CTA sl % grid; the 8 warps split its
   // 16-k chunks, the CTA adds their partial sums in warp order into the slice's partial
   for (int sl = blockIdx.x; sl < p.slices; sl += p.grid) {
@@ -271,6 +292,7 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     const int si = sl - pr.s0;
     const int kb0 = si * pr.t_w, kb1 = min(pr.k / 64, kb0 + pr.t_w);
     const int nch = (kb1 - kb0) * 4;
+    float* red = s_red;  // [warps][16 tok][16 j]
     for (int jg = 0; jg * 16 < pr.r; ++jg) {
       float acc[NG][4];
 #pragma unroll
@@ -282,7 +304,8 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
         const uint2 a1 = j1 < pr.r ? ldg_nc_v2(pr.a + static_cast<int64_t>(j1) * pr.k + kq) : make_uint2(0u, 0u);
 #pragma unroll
         for (int t = 0; t < NG; ++t) {
-          const uint2 xb = dc_xfrag(pr, t * 8 + g, kq);
+          const int tok = t * 8 + g;
+          const uint2 xb = tok < pr.m ? ldg_nc_v2(pr.x + static_cast<int64_t>(tok) * pr.k + kq) : make_uint2(0u, 0u);
           dc_mma(acc[t], a0.x, a1.x, a0.y, a1.y, xb.x, xb.y);
         }
       }
@@ -290,10 +313,10 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
 #pragma unroll
       for (int t = 0; t < NG; ++t) {
         const int tk = t * 8 + 2 * q;
-        s_red[warp][tk][g] = acc[t][0];
-        s_red[warp][tk + 1][g] = acc[t][1];
-        s_red[warp][tk][g + 8] = acc[t][2];
-        s_red[warp][tk + 1][g + 8] = acc[t][3];
+        red[(warp * 16 + tk) * 16 + g] = acc[t][0];
+        red[(warp * 16 + tk + 1) * 16 + g] = acc[t][1];
+        red[(warp * 16 + tk) * 16 + g + 8] = acc[t][2];
+        red[(warp * 16 + tk + 1) * 16 + g + 8] = acc[t][3];
       }
       __syncthreads();
       {
@@ -301,7 +324,7 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
         if (tok < NG * 8 && jg * 16 + j < pr.r) {
           float v = 0.f;
 #pragma unroll
-          for (int w = 0; w < kDcWarps; ++w) v += s_red[w][tok][j];
+          for (int w = 0; w < kDcWarps; ++w) v += red[(w * 16 + tok) * 16 + j];
           pr.tpart[(static_cast<int64_t>(si) * 16 + tok) * pr.r + jg * 16 + j] = v;
         }
       }
@@ -311,338 +334,197 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     __syncthreads();
     if (threadIdx.x == 0) dc_arrive(pr.cnt);  // count == t_slices: every slice partial of the problem is written
   }
+  __syncthreads();  // s_lut written (a CTA without a slice gets here straight from the table fill)
+  if (t_begin >= t_end) {
+    cp_async_wait<0>();
+    return;
+  }
 
-  // ---------------------------------------------------------------- W units
-  if (u_begin >= u_end) return;
-  // A unit's place: problem, row tile, 256-k unit within the tile, blocks in the unit.  Found by a
-  // binary search and one division at the start of the run; after that the cursors step (the
-  // units of a run are consecutive: k units of a tile, then the next tile, then the next problem).
-  struct Unit {
-    int pi, tile, kun, nb;  // nb: blocks in the unit (the last unit of a row may hold fewer than 4)
+  // ---------------------------------------------------------------- tiles
+  const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
+  const unsigned char* lut_base = reinterpret_cast<const unsigned char*>(s_lut);
+  // one table lookup: the level pair of the code byte held in bits 7 .. 14 of `idx`
+  auto lut = [&](uint32_t idx) -> uint32_t {
+    return *reinterpret_cast<const uint32_t*>(lut_base + ((idx & 0x7f80u) | lane4));
   };
-  auto unit_nb = [&](const Unit& d) { return min(kDcUnitBlocks, p.prob[d.pi].k / 64 - d.kun * kDcUnitBlocks); };
-  auto describe = [&](long long uu) {
-    Unit d;
-    d.pi = dc_find_prob(p, uu);
-    const DcProb& pr = p.prob[d.pi];
-    const int w = static_cast<int>(uu - pr.u0_w);
-    d.tile = w / pr.ku;
-    d.kun = w - d.tile * pr.ku;
-    d.nb = unit_nb(d);
-    return d;
-  };
-  auto step_unit = [&](Unit& d) {
-    if (++d.kun == p.prob[d.pi].ku) {
-      d.kun = 0;
-      if (++d.tile == p.prob[d.pi].tiles) {
-        d.tile = 0;
-        if (d.pi + 1 < p.count) ++d.pi;
-      }
-    }
-    d.nb = unit_nb(d);
-  };
-  // ---- the cp.async stager: runs kDcRing - 1 blocks ahead of the consumer through the run
-  const uint32_t stage_dst0 = smem_u32(&s_ring[warp][0][0]) + (lane >> 1) * kDcPitch + (lane & 1) * 16;
-  long long st_u = u_begin;
-  int st_kb = 0, st_slot = 0;
-  int st_left = static_cast<int>(u_end - u_begin);  // units the stager has not finished
-  Unit st_d = describe(u_begin);
-  const uint8_t* st_src = nullptr;
-  bool st_ok = false;
-  auto st_enter = [&]() {
-    const DcProb& pr = p.prob[st_d.pi];
-    const int row = st_d.tile * kDcRows + warp * 16 + (lane >> 1);
-    st_ok = row < pr.n;
-    st_src = pr.codes + (st_ok ? static_cast<int64_t>(row) * (pr.k / 2) + st_d.kun * 128 + (lane & 1) * 16 : 0);
-    st_kb = 0;
-  };
-  auto stage_next = [&]() {
-    if (st_left > 0) {
-      cp_async16(stage_dst0 + st_slot * kDcStage, st_src, st_ok);
-      st_src += 32;
-      if (++st_kb == st_d.nb) {
-        ++st_u;
-        --st_left;
-        step_unit(st_d);
-        st_enter();
-      }
-    }
-    cp_async_commit();
-    st_slot = st_slot + 1 == kDcRing ? 0 : st_slot + 1;
-  };
-  st_enter();
-  for (int i = 0; i < kDcRing - 1; ++i) stage_next();
+  const uint32_t read_lane = smem_u32(s_dyn) + warp * (kDcRing * kDcSlot) + g * 32 + q * 8;
   int use_slot = 0;
-
-  // raw block scales of rows g, g+8 for the blocks of a unit, loaded one unit before use
-  struct Scales {
-    int q0[kDcUnitBlocks], q1[kDcUnitBlocks];
-    float s0[kDcUnitBlocks], s1[kDcUnitBlocks];
-    float mu;
-  };
-  auto load_scales = [&](const Unit& d, Scales& sc) {
-    const DcProb& pr = p.prob[d.pi];
-    const int kbr = pr.k / 64;
-    const int r0 = d.tile * kDcRows + warp * 16 + g, r1 = r0 + 8;
-    const int64_t b0 = static_cast<int64_t>(r0) * kbr + d.kun * kDcUnitBlocks;
-    const int64_t b1 = b0 + static_cast<int64_t>(8) * kbr;
-    sc.mu = __ldg(pr.mean);
-#pragma unroll
-    for (int b = 0; b < kDcUnitBlocks; ++b) {
-      const bool in = b < d.nb;
-      sc.q0[b] = (in && r0 < pr.n) ? __ldg(pr.absq + b0 + b) : 0;
-      sc.s0[b] = (in && r0 < pr.n) ? __ldg(pr.step + ((b0 + b) >> 8)) : 0.f;
-      sc.q1[b] = (in && r1 < pr.n) ? __ldg(pr.absq + b1 + b) : 0;
-      sc.s1[b] = (in && r1 < pr.n) ? __ldg(pr.step + ((b1 + b) >> 8)) : 0.f;
-    }
-  };
-  long long cu = u_begin;
-  Unit cd = describe(cu);
-  Scales sc_cur, sc_nxt;
-  load_scales(cd, sc_cur);
-  // the rolling L2 prefetch cursor, kDcPrefetchUnits units ahead of the consumer
-  Unit pf_d = describe(u_begin + kDcPrefetchUnits < u_end ? u_begin + kDcPrefetchUnits : u_begin);
-
-  float run[NG][4];
-  auto zero_run = [&]() {
-#pragma unroll
-    for (int t = 0; t < NG; ++t) run[t][0] = run[t][1] = run[t][2] = run[t][3] = 0.f;
-  };
-  zero_run();
-  int cur_pi = -1, cur_tile = -1;
+  int cpi = dc_find_tile(p, t_begin);      // problem of the current tile
+  int t_pi = -1;                           // problem whose sT is in s_t
+  int pf_t = t_begin + kDcPrefetchTiles;   // next tile to prefetch into L2
+  int pf_pi = cpi;
+  int done_here = 0;                       // tiles of problem cpi finished by this CTA
+  int buf = 0;
   bool alive = true;
 
-  // Finish this run's segment of tile (pi, tile): add the segments' partials when the tile is
-  // split between runs (the last arriving run does it), then the LoRA term, then write y.
-  auto flush = [&](int pi, int tile) {
-    const DcProb& pr = p.prob[pi];
-    const long long tu0 = pr.u0_w + static_cast<long long>(tile) * pr.ku;  // first unit of the tile
-    const long long tu1 = tu0 + pr.ku - 1;
-    const int c0 = dc_cta_of(tu0, p.units, p.grid), c1 = dc_cta_of(tu1, p.units, p.grid);
-    const int nseg = c1 - c0 + 1, seg = static_cast<int>(blockIdx.x) - c0;
-    const int rbase = tile * kDcRows + warp * 16;
-    float* slot = pr.ypart + (static_cast<int64_t>(tile) * p.maxseg) * 16 * kDcRows;
-    float vals[NG][4];
-    bool finalise = true;
-    if (nseg > 1) {
-      // C fragment: d[0] = (row g, tok 2q), d[1] = (g, 2q+1), d[2] = (g+8, 2q), d[3] = (g+8, 2q+1)
-      float* mine = slot + static_cast<int64_t>(seg) * 16 * kDcRows;
-#pragma unroll
-      for (int t = 0; t < NG; ++t) {
-        const int tk = t * 8 + 2 * q, rr = warp * 16 + g;
-        mine[tk * kDcRows + rr] = run[t][0];
-        mine[(tk + 1) * kDcRows + rr] = run[t][1];
-        mine[tk * kDcRows + rr + 8] = run[t][2];
-        mine[(tk + 1) * kDcRows + rr + 8] = run[t][3];
+  // the tiles-finished count of problem pi: the last finisher returns both counters to zero
+  auto finish_problem = [&](int pi, int n_done) {
+    if (threadIdx.x == 0 && n_done > 0) {
+      const DcProb& pr = p.prob[pi];
+      if (dc_arrive(pr.cnt + 1, static_cast<unsigned>(n_done)) == static_cast<uint32_t>(pr.tiles)) {
+        *reinterpret_cast<volatile unsigned*>(pr.cnt) = 0u;
+        *reinterpret_cast<volatile unsigned*>(pr.cnt + 1) = 0u;
       }
-      __threadfence();
-      __syncthreads();
-      if (threadIdx.x == 0) s_flag = dc_arrive(pr.cnt + 2 + tile) == static_cast<uint32_t>(nseg);
-      __syncthreads();
-      finalise = s_flag != 0;
-      if (finalise) {
-        __threadfence();
-#pragma unroll
-        for (int t = 0; t < NG; ++t)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) vals[t][e] = 0.f;
-        for (int sgi = 0; sgi < nseg; ++sgi) {
-          const float* ps = slot + static_cast<int64_t>(sgi) * 16 * kDcRows;
-#pragma unroll
-          for (int t = 0; t < NG; ++t) {
-            const int tk = t * 8 + 2 * q, rr = warp * 16 + g;
-            vals[t][0] += __ldcg(ps + tk * kDcRows + rr);
-            vals[t][1] += __ldcg(ps + (tk + 1) * kDcRows + rr);
-            vals[t][2] += __ldcg(ps + tk * kDcRows + rr + 8);
-            vals[t][3] += __ldcg(ps + (tk + 1) * kDcRows + rr + 8);
-          }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) *reinterpret_cast<volatile unsigned*>(pr.cnt + 2 + tile) = 0u;
-      }
-    } else {
-#pragma unroll
-      for (int t = 0; t < NG; ++t)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) vals[t][e] = run[t][e];
-    }
-    if (!finalise) return;
-    // wait until every X A^T slice of the problem is written (count == t_slices)
-    if (threadIdx.x == 0) {
-      const unsigned want = static_cast<unsigned>(pr.t_slices);
-      bool ok = *reinterpret_cast<volatile unsigned*>(pr.cnt) >= want;
-      if (!ok) {
-        const uint64_t t0 = globaltimer_ns();
-        for (uint32_t it = 1;; ++it) {
-          if (*reinterpret_cast<volatile unsigned*>(pr.cnt) >= want) { ok = true; break; }
-          if ((it & 63u) == 0 && globaltimer_ns() - t0 > p.wait_ns) break;
-          __nanosleep(64);
-        }
-      }
-      s_flag = ok;
-      if (!ok) latch_status(p.status, ST_TIMEOUT);
-    }
-    __syncthreads();
-    if (!s_flag) { alive = false; return; }
-    __threadfence();
-    // sT = bf16(s X A^T) for this problem, the slices' partials added in slice order (every
-    // finaliser of the problem adds the same values in the same order); the finaliser of tile 0
-    // also writes t_save.  Kept in shared memory as bf16 pairs [16 tokens][64 pairs].
-    uint32_t* s_st = reinterpret_cast<uint32_t*>(&s_red[0][0][0]);
-    {
-      const int rpad = (pr.r + 15) & ~15, hp = rpad / 2;
-      const int64_t cstride = static_cast<int64_t>(16) * pr.r;
-      for (int i = threadIdx.x; i < 16 * hp; i += kDcThreads) {
-        const int tok = i / hp, jp = i % hp, j = 2 * jp;
-        float v0 = 0.f, v1 = 0.f;
-        if (tok < pr.m) {
-          const float* src = pr.tpart + static_cast<int64_t>(tok) * pr.r + j;
-          float x0[kDcMaxSlices], x1[kDcMaxSlices];
-#pragma unroll
-          for (int c = 0; c < kDcMaxSlices; ++c) {
-            x0[c] = (c < pr.t_slices && j < pr.r) ? __ldcg(src + c * cstride) : 0.f;
-            x1[c] = (c < pr.t_slices && j + 1 < pr.r) ? __ldcg(src + c * cstride + 1) : 0.f;
-          }
-#pragma unroll
-          for (int c = 0; c < kDcMaxSlices; ++c) {
-            v0 += x0[c];
-            v1 += x1[c];
-          }
-          if (tile == 0 && pr.t_save) {
-            if (j < pr.r) pr.t_save[tok * pr.r + j] = v0;
-            if (j + 1 < pr.r) pr.t_save[tok * pr.r + j + 1] = v1;
-          }
-        }
-        s_st[tok * 64 + jp] = tok < pr.m ? pack_bf16x2_rn(__fmul_rn(v0, pr.scale), __fmul_rn(v1, pr.scale)) : 0u;
-      }
-    }
-    __syncthreads();
-    // y = vals + sT B^T: the LoRA up-projection as extra 16-wide k chunks of the same MMA
-    // (A = rows of B, k = j; B operand = sT [tok][j]), accumulated in float32
-    const int row0 = rbase + g, row1 = row0 + 8;
-    for (int j0 = 0; j0 < pr.r; j0 += 16) {
-      const int jq = j0 + 4 * q;
-      const uint2 b0 = row0 < pr.n ? dc_ld_bf16x4(pr.b + static_cast<int64_t>(row0) * pr.r, jq, pr.r, true)
-                                   : make_uint2(0u, 0u);
-      const uint2 b1 = row1 < pr.n ? dc_ld_bf16x4(pr.b + static_cast<int64_t>(row1) * pr.r, jq, pr.r, true)
-                                   : make_uint2(0u, 0u);
-#pragma unroll
-      for (int t = 0; t < NG; ++t) {
-        const uint32_t* sp = s_st + (t * 8 + g) * 64 + jq / 2;
-        dc_mma(vals[t], b0.x, b1.x, b0.y, b1.y, sp[0], sp[1]);
-      }
-    }
-    const int rows[2] = {row0, row1};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int row = rows[h];
-      if (row >= pr.n) continue;
-#pragma unroll
-      for (int t = 0; t < NG; ++t)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int tok = t * 8 + 2 * q + e;
-          if (tok < pr.m) pr.y[static_cast<int64_t>(tok) * pr.n + row] = __float2bfloat16_rn(vals[t][2 * h + e]);
-        }
-    }
-    // the problem's last tile returns its T and tiles-done counters to zero
-    __syncthreads();
-    if (threadIdx.x == 0 && dc_arrive(pr.cnt + 1) == static_cast<uint32_t>(pr.tiles)) {
-      *reinterpret_cast<volatile unsigned*>(pr.cnt) = 0u;
-      *reinterpret_cast<volatile unsigned*>(pr.cnt + 1) = 0u;
     }
   };
 
-  __syncthreads();  // s_lut written
-  const uint32_t lut = smem_u32(s_lut + lane);
-  const uint32_t pick = (q & 1) ? 0x7632u : 0x5410u;  // the two code bytes of chunk c in the 32-bit word
-  const uint32_t ring_row0 = smem_u32(&s_ring[warp][0][0]) + g * kDcPitch;
-  float blk[NG][4];
-  while (cu < u_end && alive) {
-    const DcProb& pr = p.prob[cd.pi];
-    if (cd.pi != cur_pi || cd.tile != cur_tile) {
-      if (cur_pi >= 0) {
-        flush(cur_pi, cur_tile);
-        if (!alive) break;
-      }
-      cur_pi = cd.pi;
-      cur_tile = cd.tile;
-      zero_run();
+  for (int t = t_begin; t < t_end; ++t) {
+    if (t - p.prob[cpi].u0 == p.prob[cpi].tiles) {
+      finish_problem(cpi, done_here);
+      done_here = 0;
+      ++cpi;
     }
-    // the next unit: its place, its block scales, and the L2 prefetch kDcPrefetchUnits ahead
-    Unit nd = cd;
-    step_unit(nd);
-    if (cu + 1 < u_end) load_scales(nd, sc_nxt);
-    if (cu + kDcPrefetchUnits < u_end) {
-      if (lane < 16) {
-        const DcProb& pf = p.prob[pf_d.pi];
-        const int row = pf_d.tile * kDcRows + warp * 16 + lane;
-        if (row < pf.n)
-          dc_prefetch_codes(pf.codes + static_cast<int64_t>(row) * (pf.k / 2) + pf_d.kun * 128, pf_d.nb * 32);
-      }
-      step_unit(pf_d);
-    }
-    // this lane's token rows of X for the unit (tokens g and g + 8), chunk c at +16 c, block b at +64 b
-    const int k0 = cd.kun * kDcUnitBlocks * 64 + 4 * q;
+    const DcProb& pr = p.prob[cpi];
+    const int row0 = (t - pr.u0) * kDcTileRows;
+    const int nbk = pr.k >> 6;
+    const int kb0 = dc_warp_block(warp, nbk), kb1 = dc_warp_block(warp + 1, nbk);
+    // raw scales of rows g and g + 8 (zero past n: those rows' codes are staged as zero too)
+    const int ra = row0 + g, rb = ra + 8;
+    const bool oka = ra < pr.n, okb = rb < pr.n;
+    const int64_t ia = static_cast<int64_t>(oka ? ra : 0) * nbk, ib = static_cast<int64_t>(okb ? rb : 0) * nbk;
+    const float mu = __ldg(pr.mean);
+    // this lane's X rows: tokens t * 8 + g, elements 16 q .. 16 q + 15 of each block
     const __nv_bfloat16* xp[NG];
     bool xon[NG];
 #pragma unroll
-    for (int t = 0; t < NG; ++t) {
-      xon[t] = t * 8 + g < pr.m;  // rows of absent tokens read as zero (the pointer stays inside X)
-      xp[t] = pr.x + static_cast<int64_t>(xon[t] ? t * 8 + g : 0) * pr.k + k0;
+    for (int tg = 0; tg < NG; ++tg) {
+      xon[tg] = tg * 8 + g < pr.m;
+      xp[tg] = pr.x + static_cast<int64_t>(xon[tg] ? tg * 8 + g : 0) * pr.k + 16 * q;
     }
+    float acc[NG][4];
 #pragma unroll
-    for (int b = 0; b < kDcUnitBlocks; ++b) {
-      if (b >= cd.nb) break;
-      uint2 xf[4][NG];
+    for (int tg = 0; tg < NG; ++tg) acc[tg][0] = acc[tg][1] = acc[tg][2] = acc[tg][3] = 0.f;
+    // the block's scales, one block ahead
+    int qa = 0, qb = 0;
+    float sa = 0.f, sb = 0.f;
+    if (kb0 < kb1) {
+      qa = oka ? __ldg(pr.absq + ia + kb0) : 0;
+      qb = okb ? __ldg(pr.absq + ib + kb0) : 0;
+      sa = __ldg(pr.step + ((ia + kb0) >> 8));
+      sb = __ldg(pr.step + ((ib + kb0) >> 8));
+    }
+    for (int kb = kb0; kb < kb1; ++kb) {
+      uint4 xv[NG][2];
 #pragma unroll
-      for (int t = 0; t < NG; ++t)
-#pragma unroll
-        for (int c = 0; c < 4; ++c) xf[c][t] = ldg_nc_v2_if(xp[t] + b * 64 + 16 * c, xon[t]);
+      for (int tg = 0; tg < NG; ++tg) {
+        xv[tg][0] = ldg_nc_v4_if(xp[tg] + kb * 64, xon[tg]);
+        xv[tg][1] = ldg_nc_v4_if(xp[tg] + kb * 64 + 8, xon[tg]);
+      }
+      const int kn = kb + 1 < kb1 ? kb + 1 : kb;
+      const int qa_n = oka ? __ldg(pr.absq + ia + kn) : 0;
+      const int qb_n = okb ? __ldg(pr.absq + ib + kn) : 0;
+      const float sa_n = __ldg(pr.step + ((ia + kn) >> 8));
+      const float sb_n = __ldg(pr.step + ((ib + kn) >> 8));
       stage_next();
       cp_async_wait<kDcRing - 1>();
       __syncwarp();
-      const uint32_t rr = ring_row0 + use_slot * kDcStage;
+      const uint32_t rs = read_lane + use_slot * kDcSlot;
       use_slot = use_slot + 1 == kDcRing ? 0 : use_slot + 1;
-      // the code words this lane decodes: words 4cp + q/2 and 4cp + 2 + q/2 of rows g and g + 8
-      const uint32_t wq = rr + 4 * (q >> 1);
-      const uint32_t a00 = lds32(wq), a01 = lds32(wq + 8), a02 = lds32(wq + 16), a03 = lds32(wq + 24);
-      const uint32_t a10 = lds32(wq + 8 * kDcPitch), a11 = lds32(wq + 8 * kDcPitch + 8);
-      const uint32_t a12 = lds32(wq + 8 * kDcPitch + 16), a13 = lds32(wq + 8 * kDcPitch + 24);
+      const uint2 ca = lds64(rs), cb = lds64(rs + 8 * 32);  // rows g and g + 8, bytes 8q .. 8q+7
+      float blk[NG][4];
 #pragma unroll
-      for (int t = 0; t < NG; ++t) blk[t][0] = blk[t][1] = blk[t][2] = blk[t][3] = 0.f;
+      for (int tg = 0; tg < NG; ++tg) blk[tg][0] = blk[tg][1] = blk[tg][2] = blk[tg][3] = 0.f;
 #pragma unroll
-      for (int cp = 0; cp < 2; ++cp) {  // chunk pairs (0,1), (2,3)
-        const uint32_t w0 = prmt(cp ? a02 : a00, cp ? a03 : a01, pick);
-        const uint32_t w1 = prmt(cp ? a12 : a10, cp ? a13 : a11, pick);
-        uint32_t d0[4], d1[4];
-        dc_decode_word(lut, w0, d0);
-        dc_decode_word(lut, w1, d1);
+      for (int h = 0; h < 2; ++h) {  // h = 0: bytes 0..3 (MMAs 0, 1); h = 1: bytes 4..7 (MMAs 2, 3)
+        const uint32_t wa = h ? ca.y : ca.x, wb = h ? cb.y : cb.x;
+        const uint32_t a00 = lut(wa << 7), a01 = lut(wa >> 1), a02 = lut(wa >> 9), a03 = lut(wa >> 17);
+        const uint32_t b00 = lut(wb << 7), b01 = lut(wb >> 1), b02 = lut(wb >> 9), b03 = lut(wb >> 17);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = 2 * cp + h;
-#pragma unroll
-          for (int t = 0; t < NG; ++t)
-            dc_mma(blk[t], d0[2 * h], d1[2 * h], d0[2 * h + 1], d1[2 * h + 1], xf[c][t].x, xf[c][t].y);
+        for (int tg = 0; tg < NG; ++tg) {
+          const uint4 x = xv[tg][h];
+          dc_mma(blk[tg], a00, b00, a01, b01, x.x, x.y);
+          dc_mma(blk[tg], a02, b02, a03, b03, x.z, x.w);
         }
       }
-      const float a20 = restore_absmax(static_cast<int8_t>(sc_cur.q0[b]), sc_cur.s0[b], sc_cur.mu);
-      const float a21 = restore_absmax(static_cast<int8_t>(sc_cur.q1[b]), sc_cur.s1[b], sc_cur.mu);
+      const float aa = restore_absmax(static_cast<int8_t>(qa), sa, mu);
+      const float ab = restore_absmax(static_cast<int8_t>(qb), sb, mu);
 #pragma unroll
-      for (int t = 0; t < NG; ++t) {
-        run[t][0] = fmaf(a20, blk[t][0], run[t][0]);
-        run[t][1] = fmaf(a20, blk[t][1], run[t][1]);
-        run[t][2] = fmaf(a21, blk[t][2], run[t][2]);
-        run[t][3] = fmaf(a21, blk[t][3], run[t][3]);
+      for (int tg = 0; tg < NG; ++tg) {
+        acc[tg][0] = fmaf(aa, blk[tg][0], acc[tg][0]);
+        acc[tg][1] = fmaf(aa, blk[tg][1], acc[tg][1]);
+        acc[tg][2] = fmaf(ab, blk[tg][2], acc[tg][2]);
+        acc[tg][3] = fmaf(ab, blk[tg][3], acc[tg][3]);
       }
+      qa = qa_n;
+      qb = qb_n;
+      sa = sa_n;
+      sb = sb_n;
       __syncwarp();  // the slot is refilled by a later stage_next()
     }
-    sc_cur = sc_nxt;
-    cd = nd;
-    ++cu;
+
+    // ---- epilogue: the warps' partials in warp order, + sT B^T, -> y
+    // C fragment: acc[tg][0] = (row g, tok 2q), [1] = (g, 2q+1), [2] = (g+8, 2q), [3] = (g+8, 2q+1)
+    float* red = s_red + buf * (kDcWarps * 256);  // [warp][tok][row]
+#pragma unroll
+    for (int tg = 0; tg < NG; ++tg) {
+      const int tk = tg * 8 + 2 * q;
+      red[(warp * 16 + tk) * 16 + g] = acc[tg][0];
+      red[(warp * 16 + tk + 1) * 16 + g] = acc[tg][1];
+      red[(warp * 16 + tk) * 16 + g + 8] = acc[tg][2];
+      red[(warp * 16 + tk + 1) * 16 + g + 8] = acc[tg][3];
+    }
+    if (cpi != t_pi) {
+      // first tile of this problem in the run: wait for its X A^T slices, then sT into s_t
+      if (threadIdx.x == 0) {
+        const unsigned want = static_cast<unsigned>(pr.t_slices);
+        bool ok = *reinterpret_cast<volatile unsigned*>(pr.cnt) >= want;
+        if (!ok) {
+          const uint64_t t0 = globaltimer_ns();
+          for (uint32_t it = 1;; ++it) {
+            if (*reinterpret_cast<volatile unsigned*>(pr.cnt) >= want) { ok = true; break; }
+            if ((it & 63u) == 0 && globaltimer_ns() - t0 > p.wait_ns) break;
+            __nanosleep(64);
+          }
+        }
+        s_flag = ok;
+        if (!ok) latch_status(p.status, ST_TIMEOUT);
+      }
+      __syncthreads();
+      if (!s_flag) {
+        alive = false;
+        break;
+      }
+      __threadfence();
+      const int64_t cstride = static_cast<int64_t>(16) * pr.r;
+      for (int i = threadIdx.x; i < pr.m * pr.r; i += kDcThreads) {
+        const int tok = i / pr.r, j = i - tok * pr.r;
+        const float* src = pr.tpart + static_cast<int64_t>(tok) * pr.r + j;
+        float xs[kDcMaxSlices];
+#pragma unroll
+        for (int c = 0; c < kDcMaxSlices; ++c) xs[c] = c < pr.t_slices ? __ldcg(src + c * cstride) : 0.f;
+        float v = 0.f;
+#pragma unroll
+        for (int c = 0; c < kDcMaxSlices; ++c) v += xs[c];
+        if (t == pr.u0 && pr.t_save) pr.t_save[i] = v;
+        s_t[tok * kDcMaxR + j] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(v, pr.scale)));
+      }
+      t_pi = cpi;
+    }
+    __syncthreads();
+    {
+      const int tok = threadIdx.x >> 4, rl = threadIdx.x & 15, row = row0 + rl;
+      if (tok < pr.m && row < pr.n) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDcWarps; ++w) v += red[(w * 16 + tok) * 16 + rl];
+        const __nv_bfloat16* brow = pr.b + static_cast<int64_t>(row) * pr.r;
+        const float* trow = s_t + tok * kDcMaxR;
+        float l = 0.f;
+        for (int j = 0; j < pr.r; ++j) l = fmaf(trow[j], __bfloat162float(brow[j]), l);
+        pr.y[static_cast<int64_t>(tok) * pr.n + row] = __float2bfloat16_rn(v + l);
+      }
+    }
+    buf ^= 1;
+    ++done_here;
+    // keep kDcPrefetchTiles tiles of the run prefetched into L2
+    if (pf_t < t_end) {
+      if (pf_t - p.prob[pf_pi].u0 >= p.prob[pf_pi].tiles) pf_pi = dc_find_tile(p, pf_t);
+      dc_prefetch_tile(p.prob[pf_pi], pf_t - p.prob[pf_pi].u0);
+      ++pf_t;
+    }
   }
   cp_async_wait<0>();
-  if (cur_pi >= 0 && alive) flush(cur_pi, cur_tile);
+  if (alive) finish_problem(cpi, done_here);
 }
 
 // ---------------------------------------------------------------------------- host
@@ -650,12 +532,11 @@ int decode_max_problems() { return kDcMaxProbs; }
 
 namespace {
 struct DcPlan {
-  int grid, maxseg, slices;
-  long long units;
+  int grid, slices, tiles;
   size_t ws_bytes;
-  std::vector<size_t> off_cnt, off_tpart, off_ypart;
-  std::vector<int> t_slices, t_w, s0, tiles, ku;
-  std::vector<long long> u0_w;
+  std::vector<int> run0;
+  std::vector<size_t> off_cnt, off_tpart;
+  std::vector<int> t_slices, t_w, s0, ptiles, u0;
 };
 
 size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
@@ -666,20 +547,35 @@ DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
   pl.t_slices.resize(count);
   pl.t_w.resize(count);
   pl.s0.resize(count);
-  pl.tiles.resize(count);
-  pl.ku.resize(count);
-  pl.u0_w.resize(count);
-  // W units
-  long long u = 0;
+  pl.ptiles.resize(count);
+  pl.u0.resize(count);
+  // 16-row tiles; a tile's cost is its 64-wide blocks plus a fixed share for its epilogue
+  int t = 0;
+  double cost = 0.0;
+  std::vector<double> tile_cost(static_cast<size_t>(count));
   for (int i = 0; i < count; ++i) {
-    pl.tiles[i] = static_cast<int>((probs[i].w.n + kDcRows - 1) / kDcRows);
-    pl.ku[i] = static_cast<int>((probs[i].w.k + 255) / 256);
-    pl.u0_w[i] = u;
-    u += static_cast<long long>(pl.tiles[i]) * pl.ku[i];
+    pl.ptiles[i] = static_cast<int>((probs[i].w.n + kDcTileRows - 1) / kDcTileRows);
+    pl.u0[i] = t;
+    t += pl.ptiles[i];
+    tile_cost[static_cast<size_t>(i)] = static_cast<double>(probs[i].w.k / 64) + 2.0;
+    cost += tile_cost[static_cast<size_t>(i)] * pl.ptiles[i];
   }
-  pl.units = u;
-  const long long slots = static_cast<long long>(sms) * kDcCtasPerSm;  // every CTA of the grid resident at once
-  pl.grid = static_cast<int>(u < slots ? u : slots);
+  pl.tiles = t;
+  int slots = sms * kDcCtasPerSm;  // every CTA of the grid resident at once
+  if (slots > kDcMaxCtas) slots = kDcMaxCtas;
+  pl.grid = t < slots ? t : slots;
+  // contiguous runs of balanced cost: CTA c starts at the first tile whose cost prefix reaches
+  // c / grid of the total
+  pl.run0.assign(static_cast<size_t>(pl.grid) + 1, t);
+  {
+    int c = 0;
+    double pre = 0.0;
+    for (int i = 0; i < count && c < pl.grid; ++i)
+      for (int lt = 0; lt < pl.ptiles[i] && c < pl.grid; ++lt) {
+        while (c < pl.grid && pre >= cost * c / pl.grid) pl.run0[static_cast<size_t>(c++)] = pl.u0[i] + lt;
+        pre += tile_cost[static_cast<size_t>(i)];
+      }
+  }
   // X A^T slices: about one per CTA over the whole list, in proportion to each problem's r k
   double work = 0.0;
   for (int i = 0; i < count; ++i) work += static_cast<double>((probs[i].r + 15) / 16) * probs[i].w.k;
@@ -696,26 +592,14 @@ DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
     sl += pl.t_slices[i];
   }
   pl.slices = sl;
-  // the most runs any tile is split over
-  auto cta_of = [&](long long uu) { return static_cast<int>(((uu + 1) * pl.grid - 1) / pl.units); };
-  pl.maxseg = 1;
-  for (int i = 0; i < count; ++i)
-    for (int t = 0; t < pl.tiles[i]; ++t) {
-      const long long a = pl.u0_w[i] + static_cast<long long>(t) * pl.ku[i];
-      const int s = cta_of(a + pl.ku[i] - 1) - cta_of(a) + 1;
-      if (s > pl.maxseg) pl.maxseg = s;
-    }
   size_t off = 0;
   pl.off_cnt.resize(count);
   pl.off_tpart.resize(count);
-  pl.off_ypart.resize(count);
   for (int i = 0; i < count; ++i) {
     pl.off_cnt[i] = off;
-    off += al256(static_cast<size_t>(2 + pl.tiles[i]) * 4);
+    off += al256(2 * 4);
     pl.off_tpart[i] = off;
     off += al256(static_cast<size_t>(pl.t_slices[i]) * 16 * probs[i].r * 4);
-    pl.off_ypart[i] = off;
-    off += al256(static_cast<size_t>(pl.tiles[i]) * pl.maxseg * 16 * kDcRows * 4);
   }
   pl.ws_bytes = off;
   return pl;
@@ -735,11 +619,10 @@ cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, unsi
   std::lock_guard<std::mutex> lk(mu);
   prm.count = count;
   prm.grid = pl.grid;
-  prm.maxseg = pl.maxseg;
-  prm.units = pl.units;
   prm.slices = pl.slices;
   prm.wait_ns = wait_ns;
   prm.status = status;
+  for (int c = 0; c <= pl.grid; ++c) prm.run0[c] = pl.run0[static_cast<size_t>(c)];
   int mmax = 1;
   char* base = static_cast<char*>(ws);
   for (int i = 0; i < count; ++i) {
@@ -755,7 +638,6 @@ cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, unsi
     d.y = g.y;
     d.t_save = g.t_save;
     d.tpart = reinterpret_cast<float*>(base + pl.off_tpart[i]);
-    d.ypart = reinterpret_cast<float*>(base + pl.off_ypart[i]);
     d.cnt = reinterpret_cast<unsigned*>(base + pl.off_cnt[i]);
     d.n = static_cast<int>(g.w.n);
     d.k = static_cast<int>(g.w.k);
@@ -765,18 +647,17 @@ cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, unsi
     d.t_slices = pl.t_slices[i];
     d.t_w = pl.t_w[i];
     d.s0 = pl.s0[i];
-    d.tiles = pl.tiles[i];
-    d.ku = pl.ku[i];
-    d.u0_w = pl.u0_w[i];
+    d.tiles = pl.ptiles[i];
+    d.u0 = pl.u0[i];
     if (g.m > mmax) mmax = g.m;
   }
-  constexpr size_t kLut = 256 * 32 * 4;
-  cudaError_t e0 = mmax <= 8 ? set_smem_limit_once(k_decode<1>, kLut) : set_smem_limit_once(k_decode<2>, kLut);
+  cudaError_t e0 =
+      mmax <= 8 ? set_smem_limit_once(k_decode<1>, kDcDynSmem) : set_smem_limit_once(k_decode<2>, kDcDynSmem);
   if (e0 != cudaSuccess) return e0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.grid);
   cfg.blockDim = dim3(kDcThreads);
-  cfg.dynamicSmemBytes = kLut;
+  cfg.dynamicSmemBytes = kDcDynSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
