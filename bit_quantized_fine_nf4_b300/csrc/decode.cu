@@ -127,6 +127,15 @@ __device__ __forceinline__ uint4 ldg_nc_v4_if(const void* p, bool on) {
   return v;
 }
 
+// A signed byte load predicated in the instruction itself (0 when `on` is false).
+__device__ __forceinline__ int ldg_s8_if(const int8_t* p, bool on) {
+  int v = 0;
+  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t@q ld.global.nc.s8 %0, [%2];\n\t}"
+               : "+r"(v)
+               : "r"(static_cast<int>(on)), "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
 }
@@ -244,38 +253,41 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
 
   // ---- the cp.async stager: runs kDcRing - 1 blocks ahead of the consumer through the whole run
   // (tiles, then problems); lane l copies bytes 16 (l & 1) .. +15 of row l >> 1 of each block.
+  static_assert((kDcRing & (kDcRing - 1)) == 0, "the ring's slot offset wraps with a mask");
   const uint32_t ring0 = smem_u32(s_dyn) + warp * (kDcRing * kDcSlot);
   const uint32_t stage_lane = ring0 + (lane >> 1) * 32 + (lane & 1) * 16;
   int st_t = t_begin, st_pi = t_begin < t_end ? dc_find_tile(p, t_begin) : 0;
-  int st_kb = 0, st_kb1 = 0, st_slot = 0;
+  int st_cnt = 0;        // blocks left in the stager's current tile (0: the run is staged)
+  uint32_t st_off = 0;   // ring slot offset
   const uint8_t* st_src = nullptr;
   bool st_ok = false;
   // place the stager on the first tile at or after st_t where this warp has blocks
   auto st_enter = [&]() {
+    st_cnt = 0;
     for (; st_t < t_end; ++st_t) {
       if (st_t - p.prob[st_pi].u0 == p.prob[st_pi].tiles) ++st_pi;
       const DcProb& pr = p.prob[st_pi];
       const int nbk = pr.k >> 6;
-      st_kb = dc_warp_block(warp, nbk);
-      st_kb1 = dc_warp_block(warp + 1, nbk);
-      if (st_kb == st_kb1) continue;
+      const int kb = dc_warp_block(warp, nbk);
+      st_cnt = dc_warp_block(warp + 1, nbk) - kb;
+      if (st_cnt == 0) continue;
       const int row = (st_t - pr.u0) * kDcTileRows + (lane >> 1);
       st_ok = row < pr.n;
-      st_src = pr.codes + (st_ok ? static_cast<int64_t>(row) * (pr.k >> 1) + st_kb * 32 + (lane & 1) * 16 : 0);
+      st_src = pr.codes + (st_ok ? static_cast<int64_t>(row) * (pr.k >> 1) + kb * 32 + (lane & 1) * 16 : 0);
       return;
     }
   };
   auto stage_next = [&]() {
-    if (st_t < t_end) {
-      cp_async16(stage_lane + st_slot * kDcSlot, st_src, st_ok);
+    if (st_cnt > 0) {
+      cp_async16(stage_lane + st_off, st_src, st_ok);
       st_src += 32;
-      if (++st_kb == st_kb1) {
+      if (--st_cnt == 0) {
         ++st_t;
         st_enter();
       }
     }
     cp_async_commit();
-    st_slot = st_slot + 1 == kDcRing ? 0 : st_slot + 1;
+    st_off = (st_off + kDcSlot) & (kDcRing * kDcSlot - 1);
   };
   st_enter();
   for (int i = 0; i < kDcRing - 1; ++i) stage_next();
@@ -348,7 +360,7 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     return *reinterpret_cast<const uint32_t*>(lut_base + ((idx & 0x7f80u) | lane4));
   };
   const uint32_t read_lane = smem_u32(s_dyn) + warp * (kDcRing * kDcSlot) + g * 32 + q * 8;
-  int use_slot = 0;
+  uint32_t use_off = 0;  // ring slot offset of the consumer
   int cpi = dc_find_tile(p, t_begin);      // problem of the current tile
   int t_pi = -1;                           // problem whose sT is in s_t
   int pf_t = t_begin + kDcPrefetchTiles;   // next tile to prefetch into L2
@@ -377,49 +389,47 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     const DcProb& pr = p.prob[cpi];
     const int row0 = (t - pr.u0) * kDcTileRows;
     const int nbk = pr.k >> 6;
-    const int kb0 = dc_warp_block(warp, nbk), kb1 = dc_warp_block(warp + 1, nbk);
-    // raw scales of rows g and g + 8 (zero past n: those rows' codes are staged as zero too)
+    const int kb0 = dc_warp_block(warp, nbk), nb = dc_warp_block(warp + 1, nbk) - kb0;
+    // rows g and g + 8 of the tile (past n: scale 0; their codes are staged as zero too)
     const int ra = row0 + g, rb = ra + 8;
     const bool oka = ra < pr.n, okb = rb < pr.n;
-    const int64_t ia = static_cast<int64_t>(oka ? ra : 0) * nbk, ib = static_cast<int64_t>(okb ? rb : 0) * nbk;
     const float mu = __ldg(pr.mean);
-    // this lane's X rows: tokens t * 8 + g, elements 16 q .. 16 q + 15 of each block
-    const __nv_bfloat16* xp[NG];
+    const float* step = pr.step;
+    // raw scales: flattened block index f = row * nbk + kb; a row's bytes are contiguous
+    const int64_t fa = static_cast<int64_t>(oka ? ra : 0) * nbk + kb0, fb = static_cast<int64_t>(okb ? rb : 0) * nbk + kb0;
+    const int8_t* qpa = pr.absq + fa;
+    const int8_t* qpb = pr.absq + fb;
+    // the block's float32 step changes every 256 flattened blocks: value and the j where it next changes
+    float sa = __ldg(step + (fa >> 8)), sb = __ldg(step + (fb >> 8));
+    int swa = static_cast<int>(256 - (fa & 255)), swb = static_cast<int>(256 - (fb & 255));
+    // this lane's X rows: tokens tg * 8 + g, elements 16 q .. 16 q + 15 of each block
+    const char* xq[NG];
     bool xon[NG];
 #pragma unroll
     for (int tg = 0; tg < NG; ++tg) {
       xon[tg] = tg * 8 + g < pr.m;
-      xp[tg] = pr.x + static_cast<int64_t>(xon[tg] ? tg * 8 + g : 0) * pr.k + 16 * q;
+      xq[tg] = reinterpret_cast<const char*>(pr.x + static_cast<int64_t>(xon[tg] ? tg * 8 + g : 0) * pr.k + 16 * q +
+                                             kb0 * 64);
     }
     float acc[NG][4];
 #pragma unroll
     for (int tg = 0; tg < NG; ++tg) acc[tg][0] = acc[tg][1] = acc[tg][2] = acc[tg][3] = 0.f;
-    // the block's scales, one block ahead
-    int qa = 0, qb = 0;
-    float sa = 0.f, sb = 0.f;
-    if (kb0 < kb1) {
-      qa = oka ? __ldg(pr.absq + ia + kb0) : 0;
-      qb = okb ? __ldg(pr.absq + ib + kb0) : 0;
-      sa = __ldg(pr.step + ((ia + kb0) >> 8));
-      sb = __ldg(pr.step + ((ib + kb0) >> 8));
-    }
-    for (int kb = kb0; kb < kb1; ++kb) {
+    // raw scale bytes of the current pair of blocks, loaded one pair ahead
+    int qa0 = ldg_s8_if(qpa, oka && nb > 0), qb0 = ldg_s8_if(qpb, okb && nb > 0);
+    int qa1 = ldg_s8_if(qpa + 1, oka && nb > 1), qb1 = ldg_s8_if(qpb + 1, okb && nb > 1);
+    // one block: j = its index within the warp's range, u = 0 / 1 its place in the pair
+    auto one_block = [&](int j, int u, int qa, int qb) {
       uint4 xv[NG][2];
 #pragma unroll
       for (int tg = 0; tg < NG; ++tg) {
-        xv[tg][0] = ldg_nc_v4_if(xp[tg] + kb * 64, xon[tg]);
-        xv[tg][1] = ldg_nc_v4_if(xp[tg] + kb * 64 + 8, xon[tg]);
+        xv[tg][0] = ldg_nc_v4_if(xq[tg] + u * 128, xon[tg]);
+        xv[tg][1] = ldg_nc_v4_if(xq[tg] + u * 128 + 16, xon[tg]);
       }
-      const int kn = kb + 1 < kb1 ? kb + 1 : kb;
-      const int qa_n = oka ? __ldg(pr.absq + ia + kn) : 0;
-      const int qb_n = okb ? __ldg(pr.absq + ib + kn) : 0;
-      const float sa_n = __ldg(pr.step + ((ia + kn) >> 8));
-      const float sb_n = __ldg(pr.step + ((ib + kn) >> 8));
       stage_next();
       cp_async_wait<kDcRing - 1>();
       __syncwarp();
-      const uint32_t rs = read_lane + use_slot * kDcSlot;
-      use_slot = use_slot + 1 == kDcRing ? 0 : use_slot + 1;
+      const uint32_t rs = read_lane + use_off;
+      use_off = (use_off + kDcSlot) & (kDcRing * kDcSlot - 1);
       const uint2 ca = lds64(rs), cb = lds64(rs + 8 * 32);  // rows g and g + 8, bytes 8q .. 8q+7
       float blk[NG][4];
 #pragma unroll
@@ -436,6 +446,14 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
           dc_mma(blk[tg], a02, b02, a03, b03, x.z, x.w);
         }
       }
+      if (j == swa) {  // rare: this row's block crosses into the next step group
+        sa = __ldg(step + ((fa + j) >> 8));
+        swa += 256;
+      }
+      if (j == swb) {
+        sb = __ldg(step + ((fb + j) >> 8));
+        swb += 256;
+      }
       const float aa = restore_absmax(static_cast<int8_t>(qa), sa, mu);
       const float ab = restore_absmax(static_cast<int8_t>(qb), sb, mu);
 #pragma unroll
@@ -445,12 +463,24 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
         acc[tg][2] = fmaf(ab, blk[tg][2], acc[tg][2]);
         acc[tg][3] = fmaf(ab, blk[tg][3], acc[tg][3]);
       }
-      qa = qa_n;
-      qb = qb_n;
-      sa = sa_n;
-      sb = sb_n;
       __syncwarp();  // the slot is refilled by a later stage_next()
+    };
+    int j = 0;
+    for (; j + 2 <= nb; j += 2) {
+      const int na0 = ldg_s8_if(qpa + 2, oka && j + 2 < nb), nb0 = ldg_s8_if(qpb + 2, okb && j + 2 < nb);
+      const int na1 = ldg_s8_if(qpa + 3, oka && j + 3 < nb), nb1 = ldg_s8_if(qpb + 3, okb && j + 3 < nb);
+      one_block(j, 0, qa0, qb0);
+      one_block(j + 1, 1, qa1, qb1);
+      qa0 = na0;
+      qb0 = nb0;
+      qa1 = na1;
+      qb1 = nb1;
+      qpa += 2;
+      qpb += 2;
+#pragma unroll
+      for (int tg = 0; tg < NG; ++tg) xq[tg] += 256;
     }
+    if (j < nb) one_block(j, 0, qa0, qb0);
 
     // ---- epilogue: the warps' partials in warp order, + sT B^T, -> y
     // C fragment: acc[tg][0] = (row g, tok 2q), [1] = (g, 2q+1), [2] = (g+8, 2q), [3] = (g+8, 2q+1)
