@@ -604,6 +604,9 @@ static int grouped_problems(const qlora_linear_problem* problems, int count, std
     if ((rc = check_weight(q.w))) return fail(rc, "problem %d: %s", i, t_last_error);
     if (q.m < 1 || q.m > 16) return fail(QLORA_ERR_UNSUPPORTED, "problem %d: m = %lld (the grouped path takes 1..16 tokens)", i, (long long)q.m);
     if (q.r < 1 || q.r > 128) return fail(QLORA_ERR_UNSUPPORTED, "problem %d: r = %d (need 1 <= r <= 128)", i, q.r);
+    if (q.w->k > 131072)
+      return fail(QLORA_ERR_UNSUPPORTED, "problem %d: k = %lld (the grouped path takes k <= 131072)", i,
+                  (long long)q.w->k);
     if (check_pointers) {
       if ((rc = check_ptr(q.x, "x")) || (rc = check_ptr(q.lora_a, "lora_a")) || (rc = check_ptr(q.lora_b, "lora_b")) ||
           (rc = check_ptr(q.y, "y")))

@@ -30,10 +30,11 @@
 // them and adds them in slice order into sT = bf16(s X A^T), kept in shared
 // memory for the following tiles of the problem.  The tile's epilogue then adds
 // sT B^T (a float32 FMA chain in j order) and writes y.  Every CTA of the grid
-// is resident at once (grid <= 2 x SMs), so the waits always end.
+// is resident at once (grid <= resident CTAs per SM x SMs), so the waits always end.
 //
 // A block of a warp: lanes stage the 16 rows x 32 code bytes into a per-warp
-// shared-memory ring with cp.async (kDcRing blocks ahead, across tiles);
+// shared-memory ring with cp.async (kDcRing - 2 blocks ahead, across tiles;
+// the block's raw scale bytes ride the same ring);
 // lane (g, q) then reads bytes 8q .. 8q+7 of rows g and g + 8 (elements 16q ..
 // 16q+15 of the block) and turns each byte into its bf16 level pair with one
 // lookup in a byte-indexed table, giving mma.sync m16n8k16 A fragments for the
@@ -62,15 +63,17 @@ constexpr int kDcWarps = 8;
 constexpr int kDcCtasPerSm = 2;            // two CTAs (16 warps) per SM hide the decode's latency
 constexpr int kDcThreads = kDcWarps * 32;
 constexpr int kDcTileRows = 16;            // rows per tile (the MMA's m)
-constexpr int kDcRing = 8;                 // cp.async ring depth per warp, in blocks
+constexpr int kDcRing = 12;                // cp.async ring depth per warp, in blocks (staged kDcRing - 2 ahead)
 constexpr int kDcSlot = kDcTileRows * 32;  // one staged block: 16 rows x 32 code bytes, rows packed
+constexpr int kDcScaleSlot = kDcTileRows * 4;  // and the aligned 4-byte word holding each row's raw scale
 constexpr int kDcMaxProbs = 128;
 constexpr int kDcMaxSlices = 16;           // X A^T slices per problem (each first tile adds them all)
 constexpr int kDcPrefetchTiles = 4;        // tiles of its run a CTA keeps prefetched into L2 ahead
 constexpr int kDcMaxCtas = 320;            // run table size (>= kDcCtasPerSm x SMs)
 constexpr int kDcMaxR = 128;
-// dynamic shared memory: ring | Y partials [2][warps][16 tok][16 rows] | sT [16 tok][128] (float)
-constexpr size_t kDcRingBytes = static_cast<size_t>(kDcWarps) * kDcRing * kDcSlot;
+// dynamic shared memory: code ring | scale ring | Y partials [2][warps][16 tok][16 rows] | sT [16 tok][128] (float)
+constexpr size_t kDcCodeRingBytes = static_cast<size_t>(kDcWarps) * kDcRing * kDcSlot;
+constexpr size_t kDcRingBytes = kDcCodeRingBytes + static_cast<size_t>(kDcWarps) * kDcRing * kDcScaleSlot;
 constexpr size_t kDcRedBytes = 2ull * kDcWarps * 16 * 16 * 4;
 constexpr size_t kDcTBytes = 16ull * kDcMaxR * 4;
 constexpr size_t kDcDynSmem = kDcRingBytes + kDcRedBytes + kDcTBytes;
@@ -103,9 +106,10 @@ struct DcParams {
   DcProb prob[kDcMaxProbs];
 };
 
+// (not volatile: a pure function of its operands, so the compiler may interleave independent MMAs)
 __device__ __forceinline__ void dc_mma(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                        uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -127,17 +131,15 @@ __device__ __forceinline__ uint4 ldg_nc_v4_if(const void* p, bool on) {
   return v;
 }
 
-// A signed byte load predicated in the instruction itself (0 when `on` is false).
-__device__ __forceinline__ int ldg_s8_if(const int8_t* p, bool on) {
-  int v = 0;
-  asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t@q ld.global.nc.s8 %0, [%2];\n\t}"
-               : "+r"(v)
-               : "r"(static_cast<int>(on)), "l"(p));
-  return v;
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
+}
+// 4-byte cp.async issued only when `on` (predicated in the instruction; src-size 0 zero-fills)
+__device__ __forceinline__ void cp_async4_if(uint32_t dst, const void* src, bool valid, bool on) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %3, 0;\n\t@q cp.async.ca.shared.global [%0], [%1], 4, %2;\n\t}" ::"r"(dst),
+      "l"(src), "r"(valid ? 4 : 0), "r"(static_cast<int>(on))
+      : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -245,22 +247,30 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
       s_lv[threadIdx.x] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v)));
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < 256 * 32; i += kDcThreads) {
-      const int b = i >> 5;
-      s_lut[i] = s_lv[b >> 4] | (s_lv[b & 15] << 16);
+    // row b of the table is 32 copies of one word: 16-byte stores, 8 per thread
+    for (int i = threadIdx.x; i < 256 * 8; i += kDcThreads) {
+      const int b = i >> 3;
+      const uint32_t v = s_lv[b >> 4] | (s_lv[b & 15] << 16);
+      reinterpret_cast<uint4*>(s_lut)[i] = make_uint4(v, v, v, v);
     }
   }
 
-  // ---- the cp.async stager: runs kDcRing - 1 blocks ahead of the consumer through the whole run
-  // (tiles, then problems); lane l copies bytes 16 (l & 1) .. +15 of row l >> 1 of each block.
-  static_assert((kDcRing & (kDcRing - 1)) == 0, "the ring's slot offset wraps with a mask");
+  // ---- the cp.async stager: runs kDcRing - 2 blocks ahead of the consumer through the whole run
+  // (tiles, then problems).  Per block, lane l copies bytes 16 (l & 1) .. +15 of row l >> 1, and
+  // lane l < 16 the aligned 4-byte word of the raw scales that holds row l's scale of the block
+  // (n % 8 == 0 makes the scale array a multiple of 8 bytes, so the word is inside it).
   const uint32_t ring0 = smem_u32(s_dyn) + warp * (kDcRing * kDcSlot);
+  const uint32_t sring0 = smem_u32(s_dyn) + static_cast<uint32_t>(kDcCodeRingBytes) + warp * (kDcRing * kDcScaleSlot);
   const uint32_t stage_lane = ring0 + (lane >> 1) * 32 + (lane & 1) * 16;
+  const uint32_t sstage_lane = sring0 + (lane & 15) * 4;
   int st_t = t_begin, st_pi = t_begin < t_end ? dc_find_tile(p, t_begin) : 0;
-  int st_cnt = 0;        // blocks left in the stager's current tile (0: the run is staged)
-  uint32_t st_off = 0;   // ring slot offset
+  int st_cnt = 0;        // ring slots left in the stager's current tile (its blocks rounded up to a pair)
+  int st_real = 0;       // of which real blocks
+  uint32_t st_off = 0;   // code ring slot offset (the scale slot is at st_off / 8)
   const uint8_t* st_src = nullptr;
-  bool st_ok = false;
+  const int8_t* st_absq = nullptr;
+  int64_t st_qf = 0;     // flattened scale index of row (lane & 15), current block
+  bool st_ok = false, st_qok = false;
   // place the stager on the first tile at or after st_t where this warp has blocks
   auto st_enter = [&]() {
     st_cnt = 0;
@@ -269,28 +279,41 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
       const DcProb& pr = p.prob[st_pi];
       const int nbk = pr.k >> 6;
       const int kb = dc_warp_block(warp, nbk);
-      st_cnt = dc_warp_block(warp + 1, nbk) - kb;
-      if (st_cnt == 0) continue;
-      const int row = (st_t - pr.u0) * kDcTileRows + (lane >> 1);
+      st_real = dc_warp_block(warp + 1, nbk) - kb;
+      if (st_real == 0) continue;
+      st_cnt = (st_real + 1) & ~1;
+      const int row0 = (st_t - pr.u0) * kDcTileRows;
+      const int row = row0 + (lane >> 1);
       st_ok = row < pr.n;
       st_src = pr.codes + (st_ok ? static_cast<int64_t>(row) * (pr.k >> 1) + kb * 32 + (lane & 1) * 16 : 0);
+      const int qrow = row0 + (lane & 15);
+      st_qok = qrow < pr.n;
+      st_absq = pr.absq;
+      st_qf = st_qok ? static_cast<int64_t>(qrow) * nbk + kb : 0;
       return;
     }
   };
+  // one ring slot: the next block's codes and scales (nothing in the pad slot of an odd range)
   auto stage_next = [&]() {
     if (st_cnt > 0) {
-      cp_async16(stage_lane + st_off, st_src, st_ok);
-      st_src += 32;
+      if (st_real > 0) {
+        cp_async16(stage_lane + st_off, st_src, st_ok);
+        cp_async4_if(sstage_lane + (st_off >> 3), st_absq + (st_qf & ~int64_t(3)), st_qok, lane < 16);
+        st_src += 32;
+        ++st_qf;
+        --st_real;
+      }
       if (--st_cnt == 0) {
         ++st_t;
         st_enter();
       }
     }
     cp_async_commit();
-    st_off = (st_off + kDcSlot) & (kDcRing * kDcSlot - 1);
+    st_off = st_off + kDcSlot == kDcRing * kDcSlot ? 0u : st_off + kDcSlot;
   };
   st_enter();
-  for (int i = 0; i < kDcRing - 1; ++i) stage_next();
+  // kDcRing - 2 slots ahead: a pair is staged while the pair before it is still being read
+  for (int i = 0; i < kDcRing - 2; ++i) stage_next();
 
   // X, the counters and the workspace may come from earlier kernels of the stream
   griddep_wait();
@@ -353,13 +376,17 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
   }
 
   // ---------------------------------------------------------------- tiles
-  const uint32_t lane4 = static_cast<uint32_t>(lane) * 4u;
-  const unsigned char* lut_base = reinterpret_cast<const unsigned char*>(s_lut);
-  // one table lookup: the level pair of the code byte held in bits 7 .. 14 of `idx`
-  auto lut = [&](uint32_t idx) -> uint32_t {
-    return *reinterpret_cast<const uint32_t*>(lut_base + ((idx & 0x7f80u) | lane4));
+  // one table lookup: the level pair of byte `i` of code word w (byte extracted with a permute,
+  // then one multiply-add gives this lane's table address)
+  const uint32_t lut_lane = smem_u32(s_lut) + static_cast<uint32_t>(lane) * 4u;
+  auto lut = [&](uint32_t w, int i) -> uint32_t {
+    const uint32_t b = __byte_perm(w, 0u, 0x4440u + i);
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(b * 128u + lut_lane));
+    return v;
   };
-  const uint32_t read_lane = smem_u32(s_dyn) + warp * (kDcRing * kDcSlot) + g * 32 + q * 8;
+  const unsigned char* ring_read = s_dyn + warp * (kDcRing * kDcSlot) + g * 32 + q * 8;
+  const unsigned char* sring_read = s_dyn + kDcCodeRingBytes + warp * (kDcRing * kDcScaleSlot) + g * 4;
   uint32_t use_off = 0;  // ring slot offset of the consumer
   int cpi = dc_find_tile(p, t_begin);      // problem of the current tile
   int t_pi = -1;                           // problem whose sT is in s_t
@@ -390,55 +417,52 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     const int row0 = (t - pr.u0) * kDcTileRows;
     const int nbk = pr.k >> 6;
     const int kb0 = dc_warp_block(warp, nbk), nb = dc_warp_block(warp + 1, nbk) - kb0;
-    // rows g and g + 8 of the tile (past n: scale 0; their codes are staged as zero too)
-    const int ra = row0 + g, rb = ra + 8;
-    const bool oka = ra < pr.n, okb = rb < pr.n;
+    // rows g and g + 8 of the tile (past n: the stager zero-filled their codes and scales, and
+    // their sums are never stored)
+    const int ra = row0 + g < pr.n ? row0 + g : 0, rb = row0 + g + 8 < pr.n ? row0 + g + 8 : 0;
     const float mu = __ldg(pr.mean);
-    const float* step = pr.step;
-    // raw scales: flattened block index f = row * nbk + kb; a row's bytes are contiguous
-    const int64_t fa = static_cast<int64_t>(oka ? ra : 0) * nbk + kb0, fb = static_cast<int64_t>(okb ? rb : 0) * nbk + kb0;
-    const int8_t* qpa = pr.absq + fa;
-    const int8_t* qpb = pr.absq + fb;
-    // the block's float32 step changes every 256 flattened blocks: value and the j where it next changes
-    float sa = __ldg(step + (fa >> 8)), sb = __ldg(step + (fb >> 8));
-    int swa = static_cast<int>(256 - (fa & 255)), swb = static_cast<int>(256 - (fb & 255));
-    // this lane's X rows: tokens tg * 8 + g, elements 16 q .. 16 q + 15 of each block
-    const char* xq[NG];
-    bool xon[NG];
+    // flattened block index f = row * nbk + kb: the raw scale is byte f & 3 of the staged word
+    const int64_t fa = static_cast<int64_t>(ra) * nbk + kb0, fb = static_cast<int64_t>(rb) * nbk + kb0;
+    const int fa3 = static_cast<int>(fa & 3), fb3 = static_cast<int>(fb & 3);
+    // the float32 step of a block changes every 256 flattened blocks; a warp's range (< 256 blocks
+    // for k <= 131072) meets at most one change: the two values and the j where it happens
+    const int64_t nstep = (static_cast<int64_t>(pr.n) * nbk + 255) >> 8;
+    const float sa0 = __ldg(pr.step + (fa >> 8)), sb0 = __ldg(pr.step + (fb >> 8));
+    const float sa1 = (fa >> 8) + 1 < nstep ? __ldg(pr.step + (fa >> 8) + 1) : sa0;
+    const float sb1 = (fb >> 8) + 1 < nstep ? __ldg(pr.step + (fb >> 8) + 1) : sb0;
+    const int swa = static_cast<int>(256 - (fa & 255)), swb = static_cast<int>(256 - (fb & 255));
+    // this lane's X rows: tokens tg * 8 + g (an absent token reads token 0: its column of the
+    // product is never stored), elements 16 q .. 16 q + 15 of each block
+    const uint4* xq[NG];
 #pragma unroll
-    for (int tg = 0; tg < NG; ++tg) {
-      xon[tg] = tg * 8 + g < pr.m;
-      xq[tg] = reinterpret_cast<const char*>(pr.x + static_cast<int64_t>(xon[tg] ? tg * 8 + g : 0) * pr.k + 16 * q +
-                                             kb0 * 64);
-    }
+    for (int tg = 0; tg < NG; ++tg)
+      xq[tg] = reinterpret_cast<const uint4*>(pr.x + static_cast<int64_t>(tg * 8 + g < pr.m ? tg * 8 + g : 0) * pr.k +
+                                              16 * q + kb0 * 64);
     float acc[NG][4];
 #pragma unroll
     for (int tg = 0; tg < NG; ++tg) acc[tg][0] = acc[tg][1] = acc[tg][2] = acc[tg][3] = 0.f;
-    // raw scale bytes of the current pair of blocks, loaded one pair ahead
-    int qa0 = ldg_s8_if(qpa, oka && nb > 0), qb0 = ldg_s8_if(qpb, okb && nb > 0);
-    int qa1 = ldg_s8_if(qpa + 1, oka && nb > 1), qb1 = ldg_s8_if(qpb + 1, okb && nb > 1);
-    // one block: j = its index within the warp's range, u = 0 / 1 its place in the pair
-    auto one_block = [&](int j, int u, int qa, int qb) {
+    // one block: j = its index in the warp's range, slot its code ring offset, u = 0 / 1 its place in the pair
+    auto one_block = [&](int j, uint32_t slot, int u) {
       uint4 xv[NG][2];
 #pragma unroll
       for (int tg = 0; tg < NG; ++tg) {
-        xv[tg][0] = ldg_nc_v4_if(xq[tg] + u * 128, xon[tg]);
-        xv[tg][1] = ldg_nc_v4_if(xq[tg] + u * 128 + 16, xon[tg]);
+        xv[tg][0] = __ldg(xq[tg] + 8 * u);
+        xv[tg][1] = __ldg(xq[tg] + 8 * u + 1);
       }
-      stage_next();
-      cp_async_wait<kDcRing - 1>();
-      __syncwarp();
-      const uint32_t rs = read_lane + use_off;
-      use_off = (use_off + kDcSlot) & (kDcRing * kDcSlot - 1);
-      const uint2 ca = lds64(rs), cb = lds64(rs + 8 * 32);  // rows g and g + 8, bytes 8q .. 8q+7
+      // rows g and g + 8, bytes 8q .. 8q+7, and their scale words (plain shared loads: ordered
+      // after the ring wait)
+      const uint2 ca = *reinterpret_cast<const uint2*>(ring_read + slot);
+      const uint2 cb = *reinterpret_cast<const uint2*>(ring_read + slot + 8 * 32);
+      const uint32_t qwa = *reinterpret_cast<const uint32_t*>(sring_read + (slot >> 3));
+      const uint32_t qwb = *reinterpret_cast<const uint32_t*>(sring_read + (slot >> 3) + 8 * 4);
       float blk[NG][4];
 #pragma unroll
       for (int tg = 0; tg < NG; ++tg) blk[tg][0] = blk[tg][1] = blk[tg][2] = blk[tg][3] = 0.f;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {  // h = 0: bytes 0..3 (MMAs 0, 1); h = 1: bytes 4..7 (MMAs 2, 3)
         const uint32_t wa = h ? ca.y : ca.x, wb = h ? cb.y : cb.x;
-        const uint32_t a00 = lut(wa << 7), a01 = lut(wa >> 1), a02 = lut(wa >> 9), a03 = lut(wa >> 17);
-        const uint32_t b00 = lut(wb << 7), b01 = lut(wb >> 1), b02 = lut(wb >> 9), b03 = lut(wb >> 17);
+        const uint32_t a00 = lut(wa, 0), a01 = lut(wa, 1), a02 = lut(wa, 2), a03 = lut(wa, 3);
+        const uint32_t b00 = lut(wb, 0), b01 = lut(wb, 1), b02 = lut(wb, 2), b03 = lut(wb, 3);
 #pragma unroll
         for (int tg = 0; tg < NG; ++tg) {
           const uint4 x = xv[tg][h];
@@ -446,16 +470,10 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
           dc_mma(blk[tg], a02, b02, a03, b03, x.z, x.w);
         }
       }
-      if (j == swa) {  // rare: this row's block crosses into the next step group
-        sa = __ldg(step + ((fa + j) >> 8));
-        swa += 256;
-      }
-      if (j == swb) {
-        sb = __ldg(step + ((fb + j) >> 8));
-        swb += 256;
-      }
-      const float aa = restore_absmax(static_cast<int8_t>(qa), sa, mu);
-      const float ab = restore_absmax(static_cast<int8_t>(qb), sb, mu);
+      const int sha = ((fa3 + j) & 3) * 8, shb = ((fb3 + j) & 3) * 8;
+      const int qa = static_cast<int>(qwa << (24 - sha)) >> 24, qb = static_cast<int>(qwb << (24 - shb)) >> 24;
+      const float aa = restore_absmax(static_cast<int8_t>(qa), j < swa ? sa0 : sa1, mu);
+      const float ab = restore_absmax(static_cast<int8_t>(qb), j < swb ? sb0 : sb1, mu);
 #pragma unroll
       for (int tg = 0; tg < NG; ++tg) {
         acc[tg][0] = fmaf(aa, blk[tg][0], acc[tg][0]);
@@ -463,24 +481,20 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
         acc[tg][2] = fmaf(ab, blk[tg][2], acc[tg][2]);
         acc[tg][3] = fmaf(ab, blk[tg][3], acc[tg][3]);
       }
-      __syncwarp();  // the slot is refilled by a later stage_next()
     };
-    int j = 0;
-    for (; j + 2 <= nb; j += 2) {
-      const int na0 = ldg_s8_if(qpa + 2, oka && j + 2 < nb), nb0 = ldg_s8_if(qpb + 2, okb && j + 2 < nb);
-      const int na1 = ldg_s8_if(qpa + 3, oka && j + 3 < nb), nb1 = ldg_s8_if(qpb + 3, okb && j + 3 < nb);
-      one_block(j, 0, qa0, qb0);
-      one_block(j + 1, 1, qa1, qb1);
-      qa0 = na0;
-      qb0 = nb0;
-      qa1 = na1;
-      qb1 = nb1;
-      qpa += 2;
-      qpb += 2;
+    for (int j = 0; j < nb; j += 2) {
+      stage_next();
+      stage_next();
+      cp_async_wait<kDcRing - 2>();  // this pair's two slots have landed
+      __syncwarp();
+      const uint32_t s0 = use_off, s1 = use_off + kDcSlot == kDcRing * kDcSlot ? 0u : use_off + kDcSlot;
+      use_off = s1 + kDcSlot == kDcRing * kDcSlot ? 0u : s1 + kDcSlot;
+      one_block(j, s0, 0);
+      if (j + 1 < nb) one_block(j + 1, s1, 1);
+      __syncwarp();  // the pair's slots are refilled by a later stage_next()
 #pragma unroll
-      for (int tg = 0; tg < NG; ++tg) xq[tg] += 256;
+      for (int tg = 0; tg < NG; ++tg) xq[tg] += 16;
     }
-    if (j < nb) one_block(j, 0, qa0, qb0);
 
     // ---- epilogue: the warps' partials in warp order, + sT B^T, -> y
     // C fragment: acc[tg][0] = (row g, tok 2q), [1] = (g, 2q+1), [2] = (g+8, 2q), [3] = (g+8, 2q+1)
@@ -540,7 +554,20 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
         const __nv_bfloat16* brow = pr.b + static_cast<int64_t>(row) * pr.r;
         const float* trow = s_t + tok * kDcMaxR;
         float l = 0.f;
-        for (int j = 0; j < pr.r; ++j) l = fmaf(trow[j], __bfloat162float(brow[j]), l);
+        if ((pr.r & 7) == 0) {  // 16-byte rows: 8 values a load, the loads independent of the chain
+#pragma unroll 4
+          for (int j = 0; j < pr.r; j += 8) {
+            const uint4 bv = __ldg(reinterpret_cast<const uint4*>(brow + j));
+            const uint32_t w[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              l = fmaf(trow[j + 2 * e], __uint_as_float(w[e] << 16), l);
+              l = fmaf(trow[j + 2 * e + 1], __uint_as_float(w[e] & 0xffff0000u), l);
+            }
+          }
+        } else {
+          for (int j = 0; j < pr.r; ++j) l = fmaf(trow[j], __bfloat162float(brow[j]), l);
+        }
         pr.y[static_cast<int64_t>(tok) * pr.n + row] = __float2bfloat16_rn(v + l);
       }
     }
@@ -571,6 +598,26 @@ struct DcPlan {
 
 size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// CTAs of the kernel resident per SM (the waits inside need the whole grid resident at once).
+int dc_ctas_per_sm() {
+  static int cached = -1;
+  if (cached < 0) {
+    int a = 0, b = 0;
+    if (cudaFuncSetAttribute(k_decode<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kDcDynSmem)) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_decode<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kDcDynSmem)) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&a, k_decode<1>, kDcThreads, kDcDynSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, k_decode<2>, kDcThreads, kDcDynSmem) != cudaSuccess) {
+      cudaGetLastError();
+      return 1;
+    }
+    const int c = a < b ? a : b;
+    cached = c < 1 ? 1 : (c > kDcCtasPerSm ? kDcCtasPerSm : c);
+  }
+  return cached;
+}
+
 DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
   DcPlan pl;
   const int sms = num_sms > 0 ? num_sms : 1;
@@ -591,7 +638,7 @@ DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
     cost += tile_cost[static_cast<size_t>(i)] * pl.ptiles[i];
   }
   pl.tiles = t;
-  int slots = sms * kDcCtasPerSm;  // every CTA of the grid resident at once
+  int slots = sms * dc_ctas_per_sm();  // every CTA of the grid resident at once
   if (slots > kDcMaxCtas) slots = kDcMaxCtas;
   pl.grid = t < slots ? t : slots;
   // contiguous runs of balanced cost: CTA c starts at the first tile whose cost prefix reaches

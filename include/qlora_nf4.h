@@ -293,10 +293,15 @@ int qlora_linear_fwd_grouped_workspace_bytes(const qlora_linear_problem* problem
  * Arithmetic: bf16 operands, float32 accumulation, s X A^T rounded to bf16 as
  * in qlora_linear_fwd; the weights enter as bf16(L[code]) with the block scale
  * a' applied in float32 to each 64-wide block's partial sum (within 2^-8 per
- * weight of the bf16_rn(L a') qlora_linear_fwd uses).  Split tiles add their
- * float32 partial sums in a fixed order, so every y is deterministic.
- * `problems` is a host array of `count` entries; 1 <= m <= 16, 1 <= r <= 128.
- * The workspace holds counters of the split reductions: it must be zero-filled
+ * weight of the bf16_rn(L a') qlora_linear_fwd uses).  Each 16-row tile of y
+ * is summed by one CTA in a fixed order, so every y is deterministic.
+ * `problems` is a host array of `count` entries; 1 <= m <= 16, 1 <= r <= 128,
+ * k <= 131072 (QLORA_ERR_UNSUPPORTED otherwise).  The weight codes are read
+ * before the wait for the preceding kernel: a kernel that writes the weight
+ * records must complete before the call (every kernel of this library that
+ * writes a record does).
+ * The workspace holds counters (X A^T slices published, tiles finished) and
+ * the X A^T slice partials: it must be zero-filled
  * before its first use (cudaMemsetAsync once); every call returns them to zero,
  * so it may then be reused by later calls (and graph replays) ordered on the
  * same stream.  After a call that latched QLORA_ERR_TIMEOUT, zero it again.
