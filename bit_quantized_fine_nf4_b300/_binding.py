@@ -465,21 +465,35 @@ def _addr(x) -> int | None:
     return _ptr(x)
 
 
+class AdamwStep:
+    """A prepared tensor list for qlora_adamw_step: the ctypes array is built once (the list of
+    dicts with keys ``master``, ``param`` (bf16 copy or None), ``grad``, ``exp_avg``,
+    ``exp_avg_sq`` and, when the entries are raw addresses or ManagedBuffer objects, ``numel``),
+    so that ``run()`` per optimizer step is a single call."""
+
+    def __init__(self, tensors):
+        self.count = len(tensors)
+        self.arr = (_AdamwTensor * max(self.count, 1))()
+        self._keep = list(tensors)
+        for i, t in enumerate(tensors):
+            numel = t.get("numel")
+            if numel is None:
+                numel = t["grad"].numel()
+            self.arr[i] = _AdamwTensor(_addr(t["master"]), _addr(t.get("param")), _addr(t["grad"]),
+                                       _addr(t["exp_avg"]), _addr(t["exp_avg_sq"]), int(numel))
+
+    def run(self, lr: float, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8, weight_decay: float = 0.0,
+            step: int = 1, prefetch: bool = False, stream=None) -> None:
+        _check(load().qlora_adamw_step(self.arr, self.count, float(lr), float(beta1), float(beta2), float(eps),
+                                       float(weight_decay), int(step), ADAMW_PREFETCH if prefetch else 0,
+                                       _stream(stream)))
+
+
 def adamw_step(tensors, lr: float, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
                weight_decay: float = 0.0, step: int = 1, prefetch: bool = False, stream=None) -> None:
-    """One AdamW step (qlora_adamw_step) on a list of dicts with keys ``master``, ``param``
-    (bf16 copy or None), ``grad``, ``exp_avg``, ``exp_avg_sq`` and, when the entries are raw
-    addresses or ManagedBuffer objects, ``numel``.  All tensors of the list go in one launch."""
-    arr = (_AdamwTensor * max(len(tensors), 1))()
-    for i, t in enumerate(tensors):
-        numel = t.get("numel")
-        if numel is None:
-            numel = t["grad"].numel()
-        arr[i] = _AdamwTensor(_addr(t["master"]), _addr(t.get("param")), _addr(t["grad"]), _addr(t["exp_avg"]),
-                              _addr(t["exp_avg_sq"]), int(numel))
-    _check(load().qlora_adamw_step(arr, len(tensors), float(lr), float(beta1), float(beta2), float(eps),
-                                   float(weight_decay), int(step), ADAMW_PREFETCH if prefetch else 0,
-                                   _stream(stream)))
+    """One AdamW step (qlora_adamw_step) on a list of dicts (see AdamwStep).  All tensors of the
+    list go in one launch per 240 tensors."""
+    AdamwStep(tensors).run(lr, beta1, beta2, eps, weight_decay, step, prefetch, stream)
 
 
 class ManagedBuffer:

@@ -58,13 +58,65 @@ __global__ void __launch_bounds__(kAwThreads) k_adamw(const __grid_constant__ Aw
     const AdamwTensor& t = p.t[lo];
     const int64_t e0 = (item - p.item0[lo]) * kAwChunk;
     const int64_t e1 = min(t.numel, e0 + kAwChunk);
-    for (int64_t i = e0 + threadIdx.x; i < e1; i += kAwThreads) {
-      float master = t.master[i], m = t.exp_avg[i], v = t.exp_avg_sq[i];
-      adamw_one(p, master, t.grad[i], m, v);
-      t.master[i] = master;
-      t.exp_avg[i] = m;
-      t.exp_avg_sq[i] = v;
-      if (t.param) t.param[i] = __float2bfloat16_rn(master);
+    float* __restrict__ mp = t.master;
+    const float* __restrict__ gp = t.grad;
+    float* __restrict__ ap = t.exp_avg;
+    float* __restrict__ vp = t.exp_avg_sq;
+    __nv_bfloat16* __restrict__ pp = t.param;
+    const bool vec = ((reinterpret_cast<uintptr_t>(mp) | reinterpret_cast<uintptr_t>(gp) |
+                       reinterpret_cast<uintptr_t>(ap) | reinterpret_cast<uintptr_t>(vp)) & 15u) == 0 &&
+                     (reinterpret_cast<uintptr_t>(pp) & 7u) == 0;
+    int64_t i = e0 + threadIdx.x;
+    if (vec) {
+      // 16-byte accesses, two float4 groups per thread in flight: every load of the pair is
+      // issued before the first store (e0 is a multiple of 8192, so the groups stay aligned)
+      constexpr int64_t kStride = 4 * kAwThreads;
+      int64_t j = e0 + 4 * threadIdx.x;
+      for (; j + kStride + 4 <= e1; j += 2 * kStride) {
+        float4 w[2], g[2], m[2], v[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int64_t o = j + u * kStride;
+          w[u] = *reinterpret_cast<const float4*>(mp + o);
+          g[u] = *reinterpret_cast<const float4*>(gp + o);
+          m[u] = *reinterpret_cast<const float4*>(ap + o);
+          v[u] = *reinterpret_cast<const float4*>(vp + o);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int64_t o = j + u * kStride;
+          adamw_one(p, w[u].x, g[u].x, m[u].x, v[u].x);
+          adamw_one(p, w[u].y, g[u].y, m[u].y, v[u].y);
+          adamw_one(p, w[u].z, g[u].z, m[u].z, v[u].z);
+          adamw_one(p, w[u].w, g[u].w, m[u].w, v[u].w);
+          *reinterpret_cast<float4*>(mp + o) = w[u];
+          *reinterpret_cast<float4*>(ap + o) = m[u];
+          *reinterpret_cast<float4*>(vp + o) = v[u];
+          if (pp)
+            *reinterpret_cast<uint2*>(pp + o) = make_uint2(pack_bf16x2_rn(w[u].x, w[u].y), pack_bf16x2_rn(w[u].z, w[u].w));
+        }
+      }
+      for (; j + 4 <= e1; j += kStride) {
+        float4 w = *reinterpret_cast<const float4*>(mp + j), g = *reinterpret_cast<const float4*>(gp + j);
+        float4 m = *reinterpret_cast<const float4*>(ap + j), v = *reinterpret_cast<const float4*>(vp + j);
+        adamw_one(p, w.x, g.x, m.x, v.x);
+        adamw_one(p, w.y, g.y, m.y, v.y);
+        adamw_one(p, w.z, g.z, m.z, v.z);
+        adamw_one(p, w.w, g.w, m.w, v.w);
+        *reinterpret_cast<float4*>(mp + j) = w;
+        *reinterpret_cast<float4*>(ap + j) = m;
+        *reinterpret_cast<float4*>(vp + j) = v;
+        if (pp) *reinterpret_cast<uint2*>(pp + j) = make_uint2(pack_bf16x2_rn(w.x, w.y), pack_bf16x2_rn(w.z, w.w));
+      }
+      i = e0 + ((e1 - e0) & ~int64_t(3)) + threadIdx.x;  // the last numel % 4 elements
+    }
+    for (; i < e1; i += kAwThreads) {
+      float master = mp[i], m = ap[i], v = vp[i];
+      adamw_one(p, master, gp[i], m, v);
+      mp[i] = master;
+      ap[i] = m;
+      vp[i] = v;
+      if (pp) pp[i] = __float2bfloat16_rn(master);
     }
   }
 }

@@ -55,17 +55,25 @@ struct MgParams {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b) { return __uint_as_float(b << 16); }
 
-// The 8 dequantised weights of row n, columns k .. k+7 (k % 8 == 0), as float32
-// holding bf16 values.
-__device__ __forceinline__ void deq8(const MgParams& p, const float* s_lv, float mu, int n, int k, float (&w)[8]) {
+// Raw operands of the 8 dequantised weights of one row, columns k .. k+7 (k % 8 == 0): the code
+// word, the block's raw scale and its step.
+struct Nf4Raw8 {
+  uint32_t word;
+  int q;
+  float step;
+};
+__device__ __forceinline__ Nf4Raw8 load_raw8(const MgParams& p, int n, int k) {
   const int64_t e0 = static_cast<int64_t>(n) * p.k + k;
-  const uint32_t word = *reinterpret_cast<const uint32_t*>(p.codes + e0 / 2);
   const int64_t b = e0 / 64;
-  const float a2 = restore_absmax(p.absq[b], p.step[b >> 8], mu);
+  return {*reinterpret_cast<const uint32_t*>(p.codes + e0 / 2), static_cast<int>(p.absq[b]), p.step[b >> 8]};
+}
+// The 8 dequantised weights as float32 holding bf16 values: bf16_rn(L[code] * a').
+__device__ __forceinline__ void deq8(const Nf4Raw8& raw, const float* s_lv, float mu, float (&w)[8]) {
+  const float a2 = restore_absmax(static_cast<int8_t>(raw.q), raw.step, mu);
 #pragma unroll
   for (int e = 0; e < 8; ++e) {
     // element 2i sits in the high nibble of byte i
-    const uint32_t c = (word >> (8 * (e >> 1) + ((e & 1) ? 0 : 4))) & 15u;
+    const uint32_t c = (raw.word >> (8 * (e >> 1) + ((e & 1) ? 0 : 4))) & 15u;
     w[e] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(s_lv[c], a2)));
   }
 }
@@ -79,6 +87,27 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
   const int n0 = blockIdx.y * kMgRows, k0 = blockIdx.x * kMgCols;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kcols = min(kMgCols, p.k - k0);  // a multiple of 64
+  // Every HBM read of this thread's 4 rows x 8 columns is issued first, so its latency overlaps
+  // the staging of A and B and the FMA chain (rows past n and lanes past the tile read row n0,
+  // column k0 and store nothing).
+  const bool lane_on = lane * 8 < kcols;
+  const int kc = k0 + (lane_on ? lane * 8 : 0);
+  Nf4Raw8 raw[4];
+  uint4 dv[4][BASE == MG_F32 ? 2 : 1];
+  uint32_t keep8[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = n0 + warp * 4 + i < p.n ? n0 + warp * 4 + i : n0;
+    const int64_t o = static_cast<int64_t>(n) * p.k + kc;
+    if (BASE == MG_NF4 || SUB_NF4) raw[i] = load_raw8(p, n, kc);
+    if (BASE == MG_F32) {  // plain loads: the dense input may be the output (in place)
+      dv[i][0] = *reinterpret_cast<const uint4*>(static_cast<const float*>(p.dense) + o);
+      dv[i][BASE == MG_F32 ? 1 : 0] = *reinterpret_cast<const uint4*>(static_cast<const float*>(p.dense) + o + 4);
+    } else if (BASE == MG_BF16) {
+      dv[i][0] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dense) + o);
+    }
+    keep8[i] = MASKED ? p.mask[o >> 3] : 0xffu;
+  }
   // stage A[:, k0 .. k0 + kcols) and B[n0 .. n0 + 32, :]^T as float32
   for (int i = threadIdx.x; i < p.r * (kMgCols / 8); i += kMgThreads) {
     const int j = i / (kMgCols / 8), c8 = (i % (kMgCols / 8)) * 8;
@@ -105,8 +134,7 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
   }
   __syncthreads();
 
-  const int kc = k0 + lane * 8;
-  if (lane * 8 >= kcols) return;
+  if (!lane_on) return;
   float acc[4][8];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
@@ -141,17 +169,16 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
     if (n >= p.n) break;
     float base[8];
     if (BASE == MG_NF4) {
-      deq8(p, s_lv, mu, n, kc, base);
+      deq8(raw[i], s_lv, mu, base);
     } else {
-      const int64_t o = static_cast<int64_t>(n) * p.k + kc;
       if (BASE == MG_F32) {
-        const float4 v0 = *reinterpret_cast<const float4*>(static_cast<const float*>(p.dense) + o);
-        const float4 v1 = *reinterpret_cast<const float4*>(static_cast<const float*>(p.dense) + o + 4);
-        base[0] = v0.x; base[1] = v0.y; base[2] = v0.z; base[3] = v0.w;
-        base[4] = v1.x; base[5] = v1.y; base[6] = v1.z; base[7] = v1.w;
+        const uint32_t wv[8] = {dv[i][0].x, dv[i][0].y, dv[i][0].z, dv[i][0].w,
+                                dv[i][BASE == MG_F32 ? 1 : 0].x, dv[i][BASE == MG_F32 ? 1 : 0].y,
+                                dv[i][BASE == MG_F32 ? 1 : 0].z, dv[i][BASE == MG_F32 ? 1 : 0].w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) base[e] = __uint_as_float(wv[e]);
       } else {
-        const uint4 v = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.dense) + o);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t wv[4] = {dv[i][0].x, dv[i][0].y, dv[i][0].z, dv[i][0].w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
           base[2 * h] = bf16_bits_to_f32(wv[h] & 0xffffu);
@@ -159,14 +186,14 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
         }
       }
       if (SUB_NF4) {
-        float q[8];
-        deq8(p, s_lv, mu, n, kc, q);
+        float qd[8];
+        deq8(raw[i], s_lv, mu, qd);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) base[e] = __fsub_rn(base[e], q[e]);
+        for (int e = 0; e < 8; ++e) base[e] = __fsub_rn(base[e], qd[e]);
       }
     }
     const int64_t o = static_cast<int64_t>(n) * p.k + kc;
-    const uint32_t keep = MASKED ? p.mask[o >> 3] : 0xffu;
+    const uint32_t keep = keep8[i];
     float o8[8];
 #pragma unroll
     for (int e = 0; e < 8; ++e)

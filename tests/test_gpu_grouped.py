@@ -67,6 +67,28 @@ def test_grouped_rejects_large_token_counts(lib):
     lib.check_status()
 
 
+def test_grouped_long_rows_and_k_limit(lib):
+    """k = 32768: 64 absmax blocks per warp and row (the cp.async ring wraps many times, the
+    block steps change group inside a warp's range); k above 131072 is refused."""
+    c = synthetic.linear_case(24, 32768, 2, 8, 16.0, device="cuda", base_seed=77)
+    rec = lib.quantize(c.w)
+    t = torch.empty((c.m, c.r), dtype=torch.float32, device="cuda")
+    (y,) = lib.linear_fwd_grouped([(c.x, rec, c.a, c.b, c.alpha, None, t)])
+    lib.check_status()
+    n, k = c.w.shape
+    ref = nf4.quantize(to_np32(c.w.cpu()), n, k)
+    wd = nf4.dequantize(ref["codes"], ref["q"], ref["step"], ref["mu"], n, k)
+    yr, tr = linear.lora_forward(to_np64(c.x), wd, to_np64(c.a), to_np64(c.b), c.alpha, c.r)
+    assert_close(to_np64(y), yr, GEMM_TOL, "k=32768")
+    assert rel_fro(to_np64(t), tr) < t_save_tol(k)
+    big = synthetic.linear_case(8, 131136, 1, 1, 2.0, device="cuda", base_seed=78)
+    brec = lib.quantize(big.w)
+    with pytest.raises(lib.QloraError) as e:
+        lib.linear_fwd_grouped([(big.x, brec, big.a, big.b, big.alpha, None, None)])
+    assert e.value.code == lib.QLORA_ERR_UNSUPPORTED
+    lib.check_status()
+
+
 SMALL_SHAPES = [  # at most 1 / 2 tokens: the CUDA-core decode path; at most 4: the tensor path
     (4096, 4096, 1, 16), (4096, 11008, 4, 16), (11008, 4096, 2, 16), (136, 640, 3, 8),
     (264, 320, 4, 64), (128, 64, 1, 8), (512, 4160, 2, 24), (1032, 2112, 1, 32),
