@@ -509,7 +509,8 @@ def dropout_step(q, torch, steps, flush, p=0.05):
     with torch.cuda.graph(graph):
         fwd_bwd()
     for _ in range(3):
-        flush()
+        if flush is not None:
+            flush()
         graph.replay()
     ms = statistics.median(time_events(torch, graph.replay, steps, flush))
     q.check_status()
@@ -809,7 +810,7 @@ def main(argv=None):
     ap.add_argument("--decode-layers", type=int, default=32)
     ap.add_argument("--decode-tokens", default="1", help="token counts of --only decode, e.g. 1,4,16")
     ap.add_argument("--tokens", type=int, default=128, help="tokens of --only smalltok (<= 256: small-token GEMMs)")
-    ap.add_argument("--only", choices=("quant", "decode", "merge", "smalltok", "adamw"), default=None,
+    ap.add_argument("--only", choices=("quant", "decode", "merge", "smalltok", "adamw", "dropout"), default=None,
                     help="run one secondary measurement alone (a workload for profilers)")
     ap.add_argument("--shape", default="22016x8192", help="weight shape for --only quant")
     args = ap.parse_args(argv)
@@ -824,6 +825,8 @@ def main(argv=None):
             print(json.dumps(merge_rate(q, torch, None)), flush=True)
         elif args.only == "adamw":
             print(json.dumps(adamw_rate(q, torch)), flush=True)
+        elif args.only == "dropout":
+            print(json.dumps(dropout_step(q, torch, args.steps, None)), flush=True)
         elif args.only == "smalltok":
             print(json.dumps(small_token_step(q, torch, m=args.tokens)), flush=True)
         else:
