@@ -108,6 +108,18 @@ int check_ptr(const void* p, const char* name) {
   return QLORA_OK;
 }
 
+// A forward of 1..16 tokens without dropout runs as a one-problem grouped decode launch (the
+// weight stream kernel); larger ones go through the tensor-core GEMMs.
+bool use_decode(int64_t m, int64_t k) { return m >= 1 && m <= 16 && k <= 131072; }
+qlora::GroupedProblem decode_shape(int64_t m, int64_t n, int64_t k, int r) {
+  qlora::GroupedProblem g{};
+  g.w.n = n;
+  g.w.k = k;
+  g.m = static_cast<int>(m);
+  g.r = r;
+  return g;
+}
+
 struct FwdWs {
   size_t st, ld, gemm, total;
 };
@@ -121,6 +133,11 @@ FwdWs fwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
   w.ld = align256(qlora::lora_down_workspace_bytes(static_cast<int>(m), static_cast<int>(k), r, sms));
   w.gemm = align256(qlora::fwd_gemm_workspace_bytes(static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), sms));
   w.total = w.st + w.ld + w.gemm;
+  if (use_decode(m, k)) {  // the decode plan reuses the same workspace (the dropout forward does not take it)
+    const qlora::GroupedProblem g = decode_shape(m, n, k, r);
+    const size_t dec = align256(qlora::decode_workspace_bytes(&g, 1, sms));
+    if (dec > w.total) w.total = dec;
+  }
   return w;
 }
 
@@ -412,6 +429,21 @@ static int linear_fwd_impl(const uint16_t* x, int64_t m, const qlora_nf4_weight*
   const float scale = alpha / static_cast<float>(r);
   const int M = static_cast<int>(m), N = static_cast<int>(w->n), K = static_cast<int>(w->k);
   cudaError_t e;
+  if (!mask && use_decode(m, w->k)) {
+    qlora::GroupedProblem g = decode_shape(m, w->n, w->k, r);
+    g.x = reinterpret_cast<const __nv_bfloat16*>(x);
+    g.w = to_dev(w);
+    g.lora_a = reinterpret_cast<const __nv_bfloat16*>(lora_a);
+    g.lora_b = reinterpret_cast<const __nv_bfloat16*>(lora_b);
+    g.alpha = alpha;
+    g.y = reinterpret_cast<__nv_bfloat16*>(y);
+    g.t_save = t_save;
+    Span sp(P_FWD_GROUPED, s, 1);
+    // the decode's two per-problem counters sit at the start of its plan and must start at zero
+    e = cudaMemsetAsync(workspace, 0, 256, s);
+    if (e == cudaSuccess) e = qlora::launch_decode(&g, 1, workspace, di->status, g_wait_ns.load(), di->num_sms, s);
+    return cuda_ret(e, "fwd decode");
+  }
   // the LoRA branch input: x, or x * mask under dropout (T then scaled by 1 / (1 - p))
   const uint16_t* xl = x;
   float t_scale = 1.0f;

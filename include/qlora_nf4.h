@@ -192,7 +192,10 @@ int qlora_linear_fwd_workspace_bytes(int64_t m, int64_t n, int64_t k, int r, siz
  *   t_save f32  [m, r]      X A^T, written for the backward pass
  * The NF4 codes are decoded straight into tensor-core operands; no bf16 copy
  * of W is written to memory.  Accumulation is float32; s (X A^T) enters the
- * product rounded to bfloat16.
+ * product rounded to bfloat16.  With 1 <= m <= 16 (and k <= 131072) the call
+ * runs as a one-problem qlora_linear_fwd_grouped launch (the weight-streaming
+ * decode kernel and its reading bf16(L[code]) * a', see there); it then uses
+ * the first 256 bytes of the workspace as counters and zeroes them itself.
  */
 int qlora_linear_fwd(const uint16_t* x, int64_t m, const qlora_nf4_weight* w, const uint16_t* lora_a,
                      const uint16_t* lora_b, int r, float alpha, uint16_t* y, float* t_save, void* workspace,
