@@ -20,11 +20,12 @@
 //   merge:  bf16_rn(deq + s * acc)   (s * acc rounded, then the add rounded);
 //   update: (W - deq(Q)) + c * acc   (each operation rounded once in float32).
 //
-// Layout: a CTA of 8 warps takes a tile of 32 rows x 256 columns; warp w owns
-// rows 4w .. 4w+3, lane l the 8 columns 8l .. 8l+7 of each.  A[:, tile columns]
-// is staged once in shared memory as float32 [r][256], B[tile rows, :] as
-// float32 [r][32] (transposed), so each term costs two 16-byte loads of A, one
-// broadcast load of B and 16 packed float32x2 FMAs for 32 outputs.  The
+// Layout: a CTA of 8 warps takes a tile of 8 R rows x 256 columns (R = 8, or 4
+// for the float32 dense base); warp w owns rows R w .. R w + R - 1, lane l the 8
+// columns 8l .. 8l+7 of each.  A[:, tile columns] is staged once in shared
+// memory as float32 [r][256], B[tile rows, :] as float32 [r][8 R] (transposed),
+// so each term costs two 16-byte loads of A, R/4 broadcast loads of B and 4 R
+// packed float32x2 FMAs for 8 R outputs.  The
 // weight is HBM traffic (0.516 B per weight read, 2 or 4 B written); the FMA
 // chain is r multiply-adds per weight on the CUDA cores.
 #include "common.cuh"
@@ -32,7 +33,6 @@
 
 namespace qlora {
 
-constexpr int kMgRows = 32;
 constexpr int kMgCols = 256;
 constexpr int kMgThreads = 256;
 
@@ -67,37 +67,46 @@ __device__ __forceinline__ Nf4Raw8 load_raw8(const MgParams& p, int n, int k) {
   const int64_t b = e0 / 64;
   return {*reinterpret_cast<const uint32_t*>(p.codes + e0 / 2), static_cast<int>(p.absq[b]), p.step[b >> 8]};
 }
-// The 8 dequantised weights as float32 holding bf16 values: bf16_rn(L[code] * a').
+// The 8 dequantised weights as float32 holding bf16 values: bf16_rn(L[code] * a'), in pairs (one
+// packed multiply and one packed round per two weights; each lane rounds like __fmul_rn and
+// __float2bfloat16_rn).
 __device__ __forceinline__ void deq8(const Nf4Raw8& raw, const float* s_lv, float mu, float (&w)[8]) {
   const float a2 = restore_absmax(static_cast<int8_t>(raw.q), raw.step, mu);
+  const float2 aa = make_float2(a2, a2);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    // element 2i sits in the high nibble of byte i
-    const uint32_t c = (raw.word >> (8 * (e >> 1) + ((e & 1) ? 0 : 4))) & 15u;
-    w[e] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(s_lv[c], a2)));
+  for (int i = 0; i < 4; ++i) {
+    // byte i: element 2i in the high nibble, 2i + 1 in the low nibble
+    const uint32_t byte = (raw.word >> (8 * i)) & 0xffu;
+    const float2 l = make_float2(s_lv[byte >> 4], s_lv[byte & 15u]);
+    const float2 v = __fmul2_rn(l, aa);
+    const uint32_t pk = pack_bf16x2_rn(v.x, v.y);
+    w[2 * i] = __uint_as_float(pk << 16);
+    w[2 * i + 1] = __uint_as_float(pk & 0xffff0000u);
   }
 }
 
-template <int BASE, bool SUB_NF4, bool OUT_BF16, bool MASKED>
-__global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p) {
+// ROWS rows x 8 columns per lane; a CTA of 8 warps covers 8 * ROWS rows x 256 columns.
+template <int BASE, bool SUB_NF4, bool OUT_BF16, bool MASKED, int ROWS>
+__global__ void __launch_bounds__(kMgThreads, 2) k_lowrank_combine(const MgParams p) {
+  constexpr int kRows = 8 * ROWS;           // rows of the CTA tile
   extern __shared__ float s_mg[];
   float* s_a = s_mg;                        // [r][256]
-  float* s_bt = s_a + p.r * kMgCols;        // [r][32]
-  float* s_lv = s_bt + p.r * kMgRows;       // [16]
-  const int n0 = blockIdx.y * kMgRows, k0 = blockIdx.x * kMgCols;
+  float* s_bt = s_a + p.r * kMgCols;        // [r][kRows]
+  float* s_lv = s_bt + p.r * kRows;         // [16]
+  const int n0 = blockIdx.y * kRows, k0 = blockIdx.x * kMgCols;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kcols = min(kMgCols, p.k - k0);  // a multiple of 64
-  // Every HBM read of this thread's 4 rows x 8 columns is issued first, so its latency overlaps
-  // the staging of A and B and the FMA chain (rows past n and lanes past the tile read row n0,
-  // column k0 and store nothing).
+  // Every HBM read of this thread's ROWS rows x 8 columns is issued first, so its latency
+  // overlaps the staging of A and B and the FMA chain (rows past n and lanes past the tile read
+  // row n0, column k0 and store nothing).
   const bool lane_on = lane * 8 < kcols;
   const int kc = k0 + (lane_on ? lane * 8 : 0);
-  Nf4Raw8 raw[4];
-  uint4 dv[4][BASE == MG_F32 ? 2 : 1];
-  uint32_t keep8[4];
+  Nf4Raw8 raw[ROWS];
+  uint4 dv[ROWS][BASE == MG_F32 ? 2 : 1];
+  uint32_t keep8[ROWS];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int n = n0 + warp * 4 + i < p.n ? n0 + warp * 4 + i : n0;
+  for (int i = 0; i < ROWS; ++i) {
+    const int n = n0 + warp * ROWS + i < p.n ? n0 + warp * ROWS + i : n0;
     const int64_t o = static_cast<int64_t>(n) * p.k + kc;
     if (BASE == MG_NF4 || SUB_NF4) raw[i] = load_raw8(p, n, kc);
     if (BASE == MG_F32) {  // plain loads: the dense input may be the output (in place)
@@ -108,7 +117,7 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
     }
     keep8[i] = MASKED ? p.mask[o >> 3] : 0xffu;
   }
-  // stage A[:, k0 .. k0 + kcols) and B[n0 .. n0 + 32, :]^T as float32
+  // stage A[:, k0 .. k0 + kcols) and B[n0 .. n0 + kRows, :]^T as float32
   for (int i = threadIdx.x; i < p.r * (kMgCols / 8); i += kMgThreads) {
     const int j = i / (kMgCols / 8), c8 = (i % (kMgCols / 8)) * 8;
     float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
@@ -123,49 +132,54 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
     *reinterpret_cast<float4*>(s_a + j * kMgCols + c8 + 4) = hi;
   }
   const unsigned short* b16 = reinterpret_cast<const unsigned short*>(p.lora_b);
-  for (int i = threadIdx.x; i < p.r * kMgRows; i += kMgThreads) {
-    const int row = i % kMgRows, j = i / kMgRows;  // consecutive threads write consecutive banks
+  for (int i = threadIdx.x; i < p.r * kRows; i += kMgThreads) {
+    const int row = i % kRows, j = i / kRows;  // consecutive threads write consecutive banks
     const int n = n0 + row;
-    s_bt[j * kMgRows + row] = n < p.n ? bf16_bits_to_f32(b16[static_cast<int64_t>(n) * p.ldb + j]) : 0.f;
+    s_bt[j * kRows + row] = n < p.n ? bf16_bits_to_f32(b16[static_cast<int64_t>(n) * p.ldb + j]) : 0.f;
   }
   if (threadIdx.x < 16) {
     constexpr uint32_t hex[16] = QLORA_NF4_LEVELS_HEX;
-    s_lv[threadIdx.x] = __uint_as_float(hex[threadIdx.x]);
+    uint32_t v = 0;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) v = threadIdx.x == c ? hex[c] : v;
+    s_lv[threadIdx.x] = __uint_as_float(v);
   }
   __syncthreads();
 
   if (!lane_on) return;
-  float acc[4][8];
+  float2 acc[ROWS][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < ROWS; ++i)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+    for (int h = 0; h < 4; ++h) acc[i][h] = make_float2(0.f, 0.f);
   const float* a_col = s_a + lane * 8;
-  const float* b_row = s_bt + warp * 4;
+  const float* b_row = s_bt + warp * ROWS;
   for (int j = 0; j < p.r; ++j) {
     const float4 a0 = *reinterpret_cast<const float4*>(a_col + j * kMgCols);
     const float4 a1 = *reinterpret_cast<const float4*>(a_col + j * kMgCols + 4);
-    const float4 bb = *reinterpret_cast<const float4*>(b_row + j * kMgRows);
-    const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+    float bv[ROWS];
+#pragma unroll
+    for (int i4 = 0; i4 < ROWS; i4 += 4) {
+      const float4 bb = *reinterpret_cast<const float4*>(b_row + j * kRows + i4);
+      bv[i4] = bb.x;
+      bv[i4 + 1] = bb.y;
+      bv[i4 + 2] = bb.z;
+      bv[i4 + 3] = bb.w;
+    }
     const float2 ap[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w), make_float2(a1.x, a1.y),
                           make_float2(a1.z, a1.w)};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
+    for (int i = 0; i < ROWS; ++i) {
       const float2 b2 = make_float2(bv[i], bv[i]);
 #pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        float2 c = make_float2(acc[i][2 * h], acc[i][2 * h + 1]);
-        c = __ffma2_rn(b2, ap[h], c);
-        acc[i][2 * h] = c.x;
-        acc[i][2 * h + 1] = c.y;
-      }
+      for (int h = 0; h < 4; ++h) acc[i][h] = __ffma2_rn(b2, ap[h], acc[i][h]);
     }
   }
 
   const float mu = (BASE == MG_NF4 || SUB_NF4) ? *p.mean : 0.f;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int n = n0 + warp * 4 + i;
+  for (int i = 0; i < ROWS; ++i) {
+    const int n = n0 + warp * ROWS + i;
     if (n >= p.n) break;
     float base[8];
     if (BASE == MG_NF4) {
@@ -196,8 +210,15 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
     const uint32_t keep = keep8[i];
     float o8[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      o8[e] = (p.r > 0 && ((keep >> e) & 1u)) ? __fadd_rn(base[e], __fmul_rn(p.coef, acc[i][e])) : base[e];
+    for (int h = 0; h < 4; ++h) {
+      // base + coef * acc, each operation rounded once (scalar: a packed multiply followed by a
+      // packed add may be contracted into one fused operation)
+      const float s0 = __fadd_rn(base[2 * h], __fmul_rn(p.coef, acc[i][h].x));
+      const float s1 = __fadd_rn(base[2 * h + 1], __fmul_rn(p.coef, acc[i][h].y));
+      const bool k0b = p.r > 0 && ((keep >> (2 * h)) & 1u), k1b = p.r > 0 && ((keep >> (2 * h + 1)) & 1u);
+      o8[2 * h] = k0b ? s0 : base[2 * h];
+      o8[2 * h + 1] = k1b ? s1 : base[2 * h + 1];
+    }
     if (OUT_BF16) {
       *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + o) =
           make_uint4(pack_bf16x2_rn(o8[0], o8[1]), pack_bf16x2_rn(o8[2], o8[3]), pack_bf16x2_rn(o8[4], o8[5]),
@@ -212,12 +233,16 @@ __global__ void __launch_bounds__(kMgThreads) k_lowrank_combine(const MgParams p
 
 template <int BASE, bool SUB_NF4, bool OUT_BF16, bool MASKED = false>
 static cudaError_t run_combine(const MgParams& p, cudaStream_t s) {
-  const size_t smem = (static_cast<size_t>(p.r) * (kMgCols + kMgRows) + 16) * sizeof(float);
-  cudaError_t e = set_smem_limit_once(k_lowrank_combine<BASE, SUB_NF4, OUT_BF16, MASKED>,
-                                      (128 * (kMgCols + kMgRows) + 16) * 4);
+  // 8 rows per lane (halves the shared-memory loads of A per FMA); the dense updates (a float32
+  // base, or a subtracted record) keep 4: their preloaded operands would not fit the registers
+  constexpr int ROWS = (BASE == MG_F32 || SUB_NF4) ? 4 : 8;
+  constexpr int kRows = 8 * ROWS;
+  auto kern = k_lowrank_combine<BASE, SUB_NF4, OUT_BF16, MASKED, ROWS>;
+  const size_t smem = (static_cast<size_t>(p.r) * (kMgCols + kRows) + 16) * sizeof(float);
+  cudaError_t e = set_smem_limit_once(kern, (128 * (kMgCols + kRows) + 16) * 4);
   if (e != cudaSuccess) return e;
-  const dim3 grid((p.k + kMgCols - 1) / kMgCols, (p.n + kMgRows - 1) / kMgRows);
-  k_lowrank_combine<BASE, SUB_NF4, OUT_BF16, MASKED><<<grid, kMgThreads, smem, s>>>(p);
+  const dim3 grid((p.k + kMgCols - 1) / kMgCols, (p.n + kRows - 1) / kRows);
+  kern<<<grid, kMgThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
