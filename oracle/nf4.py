@@ -99,12 +99,12 @@ def nf4_levels_f64() -> np.ndarray:
     images); every level is divided by the largest quantile, which both sides
     share (the one at P_TOP).
     """
-    upper = _side_quantiles(8)
-    lower = _side_quantiles(7)
-    top = upper[0]
-    negative = [-q / top for q in lower]                # -1 first, rising toward 0
-    positive = [q / top for q in reversed(upper)]       # smallest first, +1 last
-    return np.array(negative + [0.0] + positive, dtype=np.float64)
+    q_hi = _side_quantiles(8)          # largest first; q_hi[0] is the quantile at P_TOP
+    q_lo = _side_quantiles(7)
+    scale = q_hi[0]
+    below = [-q / scale for q in q_lo]            # -1 first, rising toward 0
+    above = [q / scale for q in q_hi[::-1]]       # smallest first, +1 last
+    return np.array(below + [0.0] + above, dtype=np.float64)
 
 
 def nf4_levels_f32() -> np.ndarray:
