@@ -89,7 +89,7 @@ def test_grouped_long_rows_and_k_limit(lib):
     lib.check_status()
 
 
-SMALL_SHAPES = [  # at most 1 / 2 tokens: the CUDA-core decode path; at most 4: the tensor path
+SMALL_SHAPES = [  # lists capped at 1, 2 or 4 tokens (one token group of the MMA), k of 1 to 172 blocks
     (4096, 4096, 1, 16), (4096, 11008, 4, 16), (11008, 4096, 2, 16), (136, 640, 3, 8),
     (264, 320, 4, 64), (128, 64, 1, 8), (512, 4160, 2, 24), (1032, 2112, 1, 32),
 ]
@@ -112,17 +112,17 @@ def test_grouped_small_token_path(lib, mmax):
         assert rel_fro(to_np64(ys[i]), yr) < GEMM_TOL, shapes[i]
 
 
-SPLIT_LISTS = [  # short lists at 1-2 tokens: each 256-row tile's k range is split over several SMs
-    [(4096, 4096, 1, 16)],                        # 16 tiles -> 8 splits
-    [(4096, 11008, 1, 16)],                       # the down projection: 8 splits of 86 steps
-    [(296, 1088, 2, 8), (264, 2112, 1, 16)],      # ragged rows, 17 blocks a row (odd), 2 splits
-    [(1032, 4160, 2, 24)],                        # 33 steps over 8 splits: the last split is empty
+SHORT_LISTS = [  # short lists at 1-2 tokens: one 16-row tile per CTA, its k range split over 8 warps
+    [(4096, 4096, 1, 16)],                        # 256 tiles, 8 blocks per warp
+    [(4096, 11008, 1, 16)],                       # the down projection: 21-22 blocks per warp
+    [(296, 1088, 2, 8), (264, 2112, 1, 16)],      # ragged rows; 17 and 33 blocks a row (odd warp ranges)
+    [(1032, 4160, 2, 24)],                        # 65 blocks a row, 65 tiles of which the last is half full
 ]
 
 
-@pytest.mark.parametrize("which", range(len(SPLIT_LISTS)))
-def test_grouped_split_k_matches_oracle_and_is_deterministic(lib, which):
-    shapes = SPLIT_LISTS[which]
+@pytest.mark.parametrize("which", range(len(SHORT_LISTS)))
+def test_grouped_short_lists_match_oracle_and_are_deterministic(lib, which):
+    shapes = SHORT_LISTS[which]
     cases = [synthetic.linear_case(n, k, m, r, 2.0 * r, device="cuda", base_seed=900 + 10 * i + which)
              for i, (n, k, m, r) in enumerate(shapes)]
     recs = [lib.quantize(c.w) for c in cases]
