@@ -4,7 +4,7 @@ The CUDA path (through the C ABI) and the oracle see the same seeded bf16
 inputs; the oracle quantises W itself.  The bar is GEMM_TOL, the relative
 Frobenius error for bf16-in / fp32-accumulate outputs and gradients, applied
 to the whole tensor and to every row on its own.  Cases span several tiles
-with ragged tails, the small-token decode path (split-K), ranks 8 / 16 / 64 /
+with ragged tails, forwards of 1..16 tokens (the decode kernel), ranks 8 / 16 / 64 /
 128, the isolated LoRA path (W = 0) and B = 0, and the full-size workloads:
 the 4096^2 attention projection and the 4096 x 11008 MLP down projection at
 2048 tokens (every row), the 11008 x 4096 gate shape and the 65B up projection
