@@ -438,6 +438,16 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
     for (int tg = 0; tg < NG; ++tg)
       xq[tg] = reinterpret_cast<const uint4*>(pr.x + static_cast<int64_t>(tg * 8 + g < pr.m ? tg * 8 + g : 0) * pr.k +
                                               16 * q + kb0 * 64);
+    // this thread's row of B for the tile's epilogue (tokens tok < m, row row0 + rl), loaded now so
+    // the epilogue does not wait for it; r <= 16 with 16-byte rows (otherwise read there)
+    const int e_tok = threadIdx.x >> 4, e_row = row0 + (threadIdx.x & 15);
+    const bool b_pre = (pr.r & 7) == 0 && pr.r <= 16 && e_tok < pr.m && e_row < pr.n;
+    uint4 bpre[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+    if (b_pre) {
+      const uint4* bq = reinterpret_cast<const uint4*>(pr.b + static_cast<int64_t>(e_row) * pr.r);
+      bpre[0] = __ldg(bq);
+      if (pr.r > 8) bpre[1] = __ldg(bq + 1);
+    }
     float acc[NG][4];
 #pragma unroll
     for (int tg = 0; tg < NG; ++tg) acc[tg][0] = acc[tg][1] = acc[tg][2] = acc[tg][3] = 0.f;
@@ -554,7 +564,18 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
         const __nv_bfloat16* brow = pr.b + static_cast<int64_t>(row) * pr.r;
         const float* trow = s_t + tok * kDcMaxR;
         float l = 0.f;
-        if ((pr.r & 7) == 0) {  // 16-byte rows: 8 values a load, the loads independent of the chain
+        if (b_pre) {
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (h * 8 >= pr.r) break;
+            const uint32_t w[4] = {bpre[h].x, bpre[h].y, bpre[h].z, bpre[h].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              l = fmaf(trow[h * 8 + 2 * e], __uint_as_float(w[e] << 16), l);
+              l = fmaf(trow[h * 8 + 2 * e + 1], __uint_as_float(w[e] & 0xffff0000u), l);
+            }
+          }
+        } else if ((pr.r & 7) == 0) {  // 16-byte rows: 8 values a load, the loads independent of the chain
 #pragma unroll 4
           for (int j = 0; j < pr.r; j += 8) {
             const uint4 bv = __ldg(reinterpret_cast<const uint4*>(brow + j));
