@@ -99,10 +99,11 @@ struct DcProb {
 struct DcParams {
   int count;
   int grid;
-  int slices;                 // X A^T slices of the call (slice i goes to CTA i % grid)
+  int slices;                 // X A^T slices of the call
   unsigned long long wait_ns;
   unsigned* status;
   int run0[kDcMaxCtas + 1];   // CTA c takes the global tiles [run0[c], run0[c + 1])
+  short sl0[kDcMaxCtas + 1];  // and computes the X A^T slices [sl0[c], sl0[c + 1]) first
   DcProb prob[kDcMaxProbs];
 };
 
@@ -230,7 +231,7 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
       dc_prefetch_tile(p.prob[pi], t - p.prob[pi].u0);
     }
   }
-  for (int sl = blockIdx.x; sl < p.slices; sl += p.grid) {
+  for (int sl = p.sl0[blockIdx.x]; sl < p.sl0[blockIdx.x + 1]; ++sl) {
     const DcProb& pr = p.prob[dc_find_slice(p, sl)];
     const int kb0 = (sl - pr.s0) * pr.t_w, kb1 = min(pr.k / 64, kb0 + pr.t_w);
     for (int j = warp; j < pr.r; j += kDcWarps)
@@ -320,9 +321,9 @@ __global__ void __launch_bounds__(kDcThreads, kDcCtasPerSm) k_decode(const __gri
   griddep_launch_dependents();
 
   // ---------------------------------------------------------------- X A^T slices
-  // slice sl (problem p, 64-wide blocks [kb0, kb1)) goes to CTA sl % grid; the 8 warps split its
-  // 16-k chunks, the CTA adds their partial sums in warp order into the slice's partial
-  for (int sl = blockIdx.x; sl < p.slices; sl += p.grid) {
+  // slice sl (problem p, 64-wide blocks [kb0, kb1)): the 8 warps split its 16-k chunks, the CTA
+  // adds their partial sums in warp order into the slice's partial
+  for (int sl = p.sl0[blockIdx.x]; sl < p.sl0[blockIdx.x + 1]; ++sl) {
     const DcProb& pr = p.prob[dc_find_slice(p, sl)];
     const int si = sl - pr.s0;
     const int kb0 = si * pr.t_w, kb1 = min(pr.k / 64, kb0 + pr.t_w);
@@ -612,7 +613,7 @@ namespace {
 struct DcPlan {
   int grid, slices, tiles;
   size_t ws_bytes;
-  std::vector<int> run0;
+  std::vector<int> run0, sl0;
   std::vector<size_t> off_cnt, off_tpart;
   std::vector<int> t_slices, t_w, s0, ptiles, u0;
 };
@@ -661,27 +662,27 @@ DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
   pl.tiles = t;
   int slots = sms * dc_ctas_per_sm();  // every CTA of the grid resident at once
   if (slots > kDcMaxCtas) slots = kDcMaxCtas;
-  pl.grid = t < slots ? t : slots;
-  // contiguous runs of balanced cost: CTA c starts at the first tile whose cost prefix reaches
-  // c / grid of the total
-  pl.run0.assign(static_cast<size_t>(pl.grid) + 1, t);
+  const int tile_ctas = t < slots ? t : slots;
+  // contiguous runs of balanced cost over the tile CTAs: CTA c starts at the first tile whose cost
+  // prefix reaches c / tile_ctas of the total
+  std::vector<int> run0(static_cast<size_t>(tile_ctas) + 1, t);
   {
     int c = 0;
     double pre = 0.0;
-    for (int i = 0; i < count && c < pl.grid; ++i)
-      for (int lt = 0; lt < pl.ptiles[i] && c < pl.grid; ++lt) {
-        while (c < pl.grid && pre >= cost * c / pl.grid) pl.run0[static_cast<size_t>(c++)] = pl.u0[i] + lt;
+    for (int i = 0; i < count && c < tile_ctas; ++i)
+      for (int lt = 0; lt < pl.ptiles[i] && c < tile_ctas; ++lt) {
+        while (c < tile_ctas && pre >= cost * c / tile_ctas) run0[static_cast<size_t>(c++)] = pl.u0[i] + lt;
         pre += tile_cost[static_cast<size_t>(i)];
       }
   }
-  // X A^T slices: about one per CTA over the whole list, in proportion to each problem's r k
+  // X A^T slices: about one per tile CTA over the whole list, in proportion to each problem's r k
   double work = 0.0;
   for (int i = 0; i < count; ++i) work += static_cast<double>((probs[i].r + 15) / 16) * probs[i].w.k;
   int sl = 0;
   for (int i = 0; i < count; ++i) {
     const int blocks = static_cast<int>(probs[i].w.k / 64);
     const double share = static_cast<double>((probs[i].r + 15) / 16) * probs[i].w.k / work;
-    int want = static_cast<int>(share * pl.grid + 0.5);
+    int want = static_cast<int>(share * tile_ctas + 0.5);
     want = want < 1 ? 1 : (want > blocks ? blocks : want);
     if (want > kDcMaxSlices) want = kDcMaxSlices;
     pl.t_w[i] = (blocks + want - 1) / want;
@@ -690,6 +691,41 @@ DcPlan dc_plan(const GroupedProblem* probs, int count, int num_sms) {
     sl += pl.t_slices[i];
   }
   pl.slices = sl;
+  // Who computes the slices (they come first in a CTA, so they delay its tiles): CTAs of their own
+  // when the grid has room for them, else the tile CTAs whose runs cost least, a contiguous range
+  // of slices each.
+  const int extra = t < slots ? std::min(slots - t, sl) : 0;
+  pl.grid = tile_ctas + extra;
+  pl.run0 = run0;
+  pl.run0.resize(static_cast<size_t>(pl.grid) + 1, t);
+  for (int c = tile_ctas; c <= pl.grid; ++c) pl.run0[static_cast<size_t>(c)] = t;
+  std::vector<int> who;  // the slice CTAs
+  if (extra > 0) {
+    for (int c = tile_ctas; c < pl.grid; ++c) who.push_back(c);
+  } else {
+    // cost prefix over the tiles, then each run's cost in O(1)
+    std::vector<double> cpre(static_cast<size_t>(t) + 1, 0.0);
+    for (int i = 0, tt = 0; i < count; ++i)
+      for (int lt = 0; lt < pl.ptiles[i]; ++lt, ++tt)
+        cpre[static_cast<size_t>(tt) + 1] = cpre[static_cast<size_t>(tt)] + tile_cost[static_cast<size_t>(i)];
+    std::vector<std::pair<double, int>> by_cost;
+    by_cost.reserve(static_cast<size_t>(tile_ctas));
+    for (int c = 0; c < tile_ctas; ++c)
+      by_cost.push_back({cpre[static_cast<size_t>(run0[static_cast<size_t>(c) + 1])] -
+                             cpre[static_cast<size_t>(run0[static_cast<size_t>(c)])],
+                         c});
+    std::stable_sort(by_cost.begin(), by_cost.end(),
+                     [](const std::pair<double, int>& a, const std::pair<double, int>& b) { return a.first < b.first; });
+    const int e = std::min(sl, tile_ctas);
+    for (int k = 0; k < e; ++k) who.push_back(by_cost[static_cast<size_t>(k)].second);
+    std::sort(who.begin(), who.end());
+  }
+  std::vector<int> nsl(static_cast<size_t>(pl.grid), 0);
+  for (size_t k = 0; k < who.size(); ++k)
+    nsl[static_cast<size_t>(who[k])] = static_cast<int>((static_cast<long long>(k + 1) * sl) / static_cast<long long>(who.size()) -
+                                                        (static_cast<long long>(k) * sl) / static_cast<long long>(who.size()));
+  pl.sl0.assign(static_cast<size_t>(pl.grid) + 1, 0);
+  for (int c = 0; c < pl.grid; ++c) pl.sl0[static_cast<size_t>(c) + 1] = pl.sl0[static_cast<size_t>(c)] + nsl[static_cast<size_t>(c)];
   size_t off = 0;
   pl.off_cnt.resize(count);
   pl.off_tpart.resize(count);
@@ -720,7 +756,10 @@ cudaError_t launch_decode(const GroupedProblem* probs, int count, void* ws, unsi
   prm.slices = pl.slices;
   prm.wait_ns = wait_ns;
   prm.status = status;
-  for (int c = 0; c <= pl.grid; ++c) prm.run0[c] = pl.run0[static_cast<size_t>(c)];
+  for (int c = 0; c <= pl.grid; ++c) {
+    prm.run0[c] = pl.run0[static_cast<size_t>(c)];
+    prm.sl0[c] = static_cast<short>(pl.sl0[static_cast<size_t>(c)]);
+  }
   int mmax = 1;
   char* base = static_cast<char*>(ws);
   for (int i = 0; i < count; ++i) {
