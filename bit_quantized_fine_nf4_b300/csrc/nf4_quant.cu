@@ -436,13 +436,13 @@ __global__ void __launch_bounds__(kQbThreads, kQbCtasPerSm)
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint32_t wv[4] = {q[c].x, q[c].y, q[c].z, q[c].w};
-        uint32_t pk = 0;
+        uint32_t by[4];  // byte h = code(weight 2h) in the high nibble, code(weight 2h + 1) in the low
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-          pk |= qz_code(__uint_as_float(wv[h] << 16), a, r16, lane_tab) << (h * 8 + 4);
-          pk |= qz_code(__uint_as_float(wv[h] & 0xffff0000u), a, r16, lane_tab) << (h * 8);
-        }
-        packed[c] = pk;
+        for (int h = 0; h < 4; ++h)
+          by[h] = qz_code(__uint_as_float(wv[h] << 16), a, r16, lane_tab) * 16u +
+                  qz_code(__uint_as_float(wv[h] & 0xffff0000u), a, r16, lane_tab);
+        // the four bytes into one word with three byte permutes
+        packed[c] = prmt(prmt(by[0], by[1], 0x0040u), prmt(by[2], by[3], 0x0040u), 0x5410u);
       }
       lo = make_uint4(packed[0], packed[1], packed[2], packed[3]);
       hi = make_uint4(packed[4], packed[5], packed[6], packed[7]);
