@@ -145,19 +145,20 @@ FwdWs fwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 bool use_side(int64_t m, int r) { return qlora::use_pair_gemm(static_cast<int>(m)) && qlora::lora_side_supported(r); }
 
 struct BwdWs {
-  size_t su, st, ld, lg, total;
+  size_t su, st, ld, lg, gemm, total;
 };
 BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
   BwdWs w;
   if (m <= 0) {
-    w.su = w.st = w.ld = w.lg = w.total = 0;
+    w.su = w.st = w.ld = w.lg = w.gemm = w.total = 0;
     return w;
   }
   w.su = lora_operand_bytes(m, r);
   w.st = w.su;
   w.ld = align256(qlora::lora_down_workspace_bytes(static_cast<int>(m), static_cast<int>(n), r, sms));
   w.lg = align256(qlora::lora_grads_workspace_bytes(static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), r, sms));
-  w.total = w.su + w.st + w.ld + w.lg;
+  w.gemm = align256(qlora::bwd_gemm_workspace_bytes(static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), sms));
+  w.total = w.su + w.st + w.ld + w.lg + w.gemm;
   return w;
 }
 
@@ -560,6 +561,7 @@ static int linear_bwd_impl(const uint16_t* dy, const uint16_t* x, int64_t m, con
   __nv_bfloat16* st = reinterpret_cast<__nv_bfloat16*>(base + ws.su);
   void* ldws = base + ws.su + ws.st;
   void* lgws = base + ws.su + ws.st + ws.ld;
+  void* gemmws = base + ws.su + ws.st + ws.ld + ws.lg;
   const float scale = alpha / static_cast<float>(r);
   const float inv_keep = mask ? static_cast<float>(1.0 / (1.0 - static_cast<double>(p_drop))) : 1.0f;
   const int M = static_cast<int>(m), N = static_cast<int>(w->n), K = static_cast<int>(w->k);
@@ -585,7 +587,7 @@ static int linear_bwd_impl(const uint16_t* dy, const uint16_t* x, int64_t m, con
   if (e != cudaSuccess) return cuda_ret(e, "fork to the side stream");
   {
     Span sp(P_LORA_GRADS, di->side, 1);
-    const int cap = qlora::idle_sms_beside(qlora::bwd_gemm_ctas(M, N, K), di->num_sms);
+    const int cap = qlora::idle_sms_beside(qlora::bwd_gemm_ctas(M, N, K, di->num_sms), di->num_sms);
     e = qlora::launch_lora_grads(xb, dyb, su, st, M, N, K, r, da, db, (flags & QLORA_ACCUM_DA) ? 1 : 0,
                                  (flags & QLORA_ACCUM_DB) ? 1 : 0, lgws, di->status, wait, cap, di->side, inv_keep);
   }
@@ -593,8 +595,8 @@ static int linear_bwd_impl(const uint16_t* dy, const uint16_t* x, int64_t m, con
   if (e == cudaSuccess) {
     Span sp(P_BWD_GEMM, s, 1);
     e = qlora::launch_bwd_dx_gemm(dyb, M, to_dev(w), su, reinterpret_cast<const __nv_bfloat16*>(lora_a), r,
-                                  reinterpret_cast<__nv_bfloat16*>(dx), (flags & QLORA_ACCUM_DX) ? 1 : 0, di->status,
-                                  wait, s, mask ? 0 : 1);
+                                  reinterpret_cast<__nv_bfloat16*>(dx), (flags & QLORA_ACCUM_DX) ? 1 : 0, gemmws,
+                                  di->status, wait, di->num_sms, s, mask ? 0 : 1);
   }
   if (e == cudaSuccess && mask) {
     Span sp(P_DROPOUT, s, 1);

@@ -63,9 +63,11 @@ cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, cons
 // Backward dX[M, K] (+)= dY[M, N] deq(W) + sU[M, r] A[r, K]   (sU = bf16(s * dY B))
 // with_lora = 0: the LoRA k steps are left out (dX = dY deq(W) only; the dropout path adds its
 // masked LoRA term separately).
+// ws: bwd_gemm_workspace_bytes (fp32 partials of the split n blocks and per-tile counters).
+size_t bwd_gemm_workspace_bytes(int M, int N, int K, int num_sms);
 cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
-                               const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
-                               unsigned* status, uint64_t wait_ns, cudaStream_t s, int with_lora = 1);
+                               const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate, void* ws,
+                               unsigned* status, uint64_t wait_ns, int num_sms, cudaStream_t s, int with_lora = 1);
 
 // LoRA gradients: dA[r, K] (+)= sU^T X   and   dB[N, r] (+)= dY^T sT
 size_t lora_grads_workspace_bytes(int M, int N, int K, int r, int num_sms);
@@ -128,7 +130,7 @@ cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lo
                                  cudaStream_t s, float t_scale = 1.0f);
 // Grid sizes of the GEMMs and the SMs they leave idle (budget for side kernels).
 int fwd_gemm_ctas(int M, int N, int K, int num_sms);
-int bwd_gemm_ctas(int M, int N, int K);
+int bwd_gemm_ctas(int M, int N, int K, int num_sms);
 int idle_sms_beside(int gemm_ctas, int num_sms);
 
 // Grouped small-token forward (decode.cu): one problem of the list.

@@ -44,7 +44,7 @@ struct WaParams {
   const float* mean;
   const __nv_bfloat16* lora_b;  // [N, r]
   __nv_bfloat16* y;             // [M, N]
-  float* partial;               // [splits][tiles][128][NTOK] (split-K only)
+  float* partial;               // [splits][tiles][NTOK / 4 column groups][128 rows] float4 (split-K only)
   unsigned* counters;           // [tiles]
   unsigned* status;
   int M, N, K, r;
@@ -206,9 +206,11 @@ __global__ void __launch_bounds__(kWaThreads, 1)
     const int col_lo = (kShare == NTOK) ? 0 : team * kShare;
     const int ncols = (kShare == NTOK) ? (team == 0 ? NTOK : 0) : kShare;
     const uint32_t dcol = tbase + lane_field + Cfg::kDCol;
+    const int ncv = min(NTOK, p.M - tok0);  // columns that hold tokens
+    const int ntiles = gridDim.x * gridDim.y;
     if (ok) {
       if (p.splits == 1) {
-        for (int c = col_lo; c < col_lo + ncols; c += 16) {
+        for (int c = col_lo; c < col_lo + ncols && c < ncv; c += 16) {
           uint32_t v[16];
           __syncwarp();
           tmem_ld_32x32b_x16(dcol + c, v);
@@ -222,16 +224,18 @@ __global__ void __launch_bounds__(kWaThreads, 1)
           }
         }
       } else {
-        float* part = p.partial + (static_cast<int64_t>(split) * gridDim.x * gridDim.y + tile) * 128 * NTOK +
-                      (quarter * 32 + lane) * NTOK;
-        for (int c = col_lo; c < col_lo + ncols; c += 16) {
+        // partial of this split: [column / 4][128 rows] float4, so a warp's store is 512 contiguous bytes
+        float4* part = reinterpret_cast<float4*>(p.partial) +
+                       (static_cast<int64_t>(split) * ntiles + tile) * (NTOK / 4) * 128 + quarter * 32 + lane;
+        for (int c = col_lo; c < col_lo + ncols && c < ncv; c += 16) {
           uint32_t v[16];
           __syncwarp();
           tmem_ld_32x32b_x16(dcol + c, v);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; j += 4)
-            *reinterpret_cast<uint4*>(part + c + j) = make_uint4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            part[((c + j) >> 2) * 128] = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                                     __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
         }
       }
     }
@@ -242,15 +246,40 @@ __global__ void __launch_bounds__(kWaThreads, 1)
       named_bar_sync(1, kWaTeams * 128);
       if (*reinterpret_cast<volatile int*>(last_flag)) {
         __threadfence();
-        if (row_ok) {
-          for (int c = col_lo; c < col_lo + ncols; ++c) {
-            const int tok = tok0 + c;
-            if (tok >= p.M) break;
-            float acc = 0.f;
-            for (int sp = 0; sp < p.splits; ++sp)
-              acc += __ldcg(p.partial + (static_cast<int64_t>(sp) * gridDim.x * gridDim.y + tile) * 128 * NTOK +
-                            (quarter * 32 + lane) * NTOK + c);
-            p.y[static_cast<int64_t>(tok) * p.N + row] = __float2bfloat16_rn(acc);
+        // the last split adds the partials in split order; all producer threads share the
+        // (4-column group, row) items, four items per thread in flight
+        const int items = ((ncv + 3) >> 2) * 128;
+        const int64_t sstride = static_cast<int64_t>(ntiles) * (NTOK / 4) * 128;
+        const float4* src = reinterpret_cast<const float4*>(p.partial) + static_cast<int64_t>(tile) * (NTOK / 4) * 128;
+        constexpr int kRt = kWaTeams * 128;
+        for (int it0 = threadIdx.x - 64; it0 < items; it0 += 4 * kRt) {
+          float4 acc[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            acc[u] = it0 + u * kRt < items ? __ldcg(src + it0 + u * kRt) : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int sp = 1; sp < p.splits; ++sp) {
+            float4 v[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              v[u] = it0 + u * kRt < items ? __ldcg(src + sp * sstride + it0 + u * kRt) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              acc[u].x += v[u].x;
+              acc[u].y += v[u].y;
+              acc[u].z += v[u].z;
+              acc[u].w += v[u].w;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int it = it0 + u * kRt;
+            const int orow = n0 + (it & 127), otok = tok0 + (it >> 7) * 4;
+            if (it < items && orow < p.N) {
+              const float f[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (otok + e < p.M) p.y[static_cast<int64_t>(otok + e) * p.N + orow] = __float2bfloat16_rn(f[e]);
+            }
           }
         }
         if (threadIdx.x == 64) p.counters[tile] = 0;
@@ -273,9 +302,12 @@ struct WbParams {
   const float* step;
   const float* mean;
   __nv_bfloat16* dx;  // [M, K]
+  float* partial;     // [splits][tiles][64 column groups of 4][256 tokens] float4 (split n only)
+  unsigned* counters; // [tiles]
   unsigned* status;
   int M, N, K, r;
   int lora_blocks, accumulate;
+  int splits, nb_per_split;  // the n blocks are split over `splits` CTAs per tile (the last adds the LoRA steps)
   unsigned long long wait_ns;
 };
 
@@ -304,12 +336,16 @@ __global__ void __launch_bounds__(kWbThreads, 1)
   uint64_t* acc_full = empty + STAGES;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  int* last_flag = abort_flag + 1;
   volatile int* vabort = abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int k0 = blockIdx.x * 256, tok0 = blockIdx.y * 256;
-  const int n_main = (p.N + 63) / 64;
-  const int n_iter = n_main + p.lora_blocks;
+  const int k0 = blockIdx.x * 256, tok0 = blockIdx.y * 256, split = blockIdx.z;
+  const int tile = blockIdx.x + gridDim.x * blockIdx.y, ntiles = gridDim.x * gridDim.y;
+  // this CTA's n blocks [nb0, nb0 + n_main); the last split also runs the LoRA k steps
+  const int nb0 = split * p.nb_per_split;
+  const int n_main = min((p.N + 63) / 64 - nb0, p.nb_per_split);
+  const int n_iter = n_main + (split == p.splits - 1 ? p.lora_blocks : 0);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -318,6 +354,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
+    *last_flag = 0;
     fence_mbarrier_init();
   }
   if (warp == 0) {
@@ -341,7 +378,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
         uint8_t* sa = smem + s * kWbStage;
         if (i < n_main) {
           mbar_arrive_expect_tx(&full[s], kWbABytes);
-          tma_load_2d(sa, &tm_dy, &full[s], i * 64, tok0);
+          tma_load_2d(sa, &tm_dy, &full[s], (nb0 + i) * 64, tok0);
         } else {
           const int e = i - n_main;
           if (e == 0) griddep_wait();  // sU is written by the preceding LoRA down kernel
@@ -353,7 +390,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
       }
       // no LoRA k steps: still wait once for the preceding kernel, so this grid never completes
       // before it does (later kernels of the stream rely on that order)
-      if (p.lora_blocks == 0) griddep_wait();
+      if (n_iter == n_main) griddep_wait();
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -389,7 +426,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
     int8_t nq = 0;
     float nstep = 0.f;
     auto fetch = [&](int i) {
-      const int n = i * 64 + rrow;
+      const int n = (nb0 + i) * 64 + rrow;
       if (i < n_main && n < p.N && kblk < kb_row) {
         const uint8_t* cp = p.codes + static_cast<int64_t>(n) * (p.K / 2) + kblk * 32;
         nc0 = ldg_nc_v4(cp);
@@ -405,7 +442,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
       const int s = i % STAGES;
       const uint32_t ph = (i / STAGES) & 1;
       const bool is_main = i < n_main;
-      const int n = i * 64 + rrow;
+      const int n = (nb0 + i) * 64 + rrow;
       const bool uok = is_main && (n < p.N) && (kblk < kb_row);
       const uint4 c0 = nc0, c1 = nc1;
       const float a2 = restore_absmax(nq, nstep, mu);
@@ -438,7 +475,26 @@ __global__ void __launch_bounds__(kWbThreads, 1)
     const int quarter = warp & 3;
     const int wq = (warp - 2) >> 2;  // 0..3 among the warps of this quarter
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-    if (ok) {
+    const int ntok = min(256, p.M - tok0);  // tokens of this tile
+    if (ok && p.splits > 1) {
+      // partial of this split: [column / 4][256 tokens] float4, a warp's store is 512 contiguous bytes
+      float4* part = reinterpret_cast<float4*>(p.partial) + (static_cast<int64_t>(split) * ntiles + tile) * 64 * 256;
+      for (int chunk = wq; chunk < 16; chunk += 4) {
+        const int acc = chunk >> 3, col = (chunk & 7) * 32;
+        if (acc * 128 >= ntok) continue;  // warp-uniform: no token of this accumulator
+        const int tl = acc * 128 + quarter * 32 + lane;
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(tbase + lane_field + acc * 256 + col, v);
+        tmem_ld_wait();
+        if (tl < ntok && k0 + col < p.K) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            part[((col >> 2) + q) * 256 + tl] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+        }
+      }
+    } else if (ok) {
       for (int chunk = wq; chunk < 16; chunk += 4) {
         const int acc = chunk >> 3, col = (chunk & 7) * 32;
         const int tok = tok0 + acc * 128 + quarter * 32 + lane;
@@ -467,6 +523,64 @@ __global__ void __launch_bounds__(kWbThreads, 1)
                                 pack_bf16x2_rn(f[6], f[7]));
           }
         }
+      }
+    }
+    if (p.splits > 1) {
+      __threadfence();
+      named_bar_sync(1, 2 * kWbTeamThreads);
+      if (threadIdx.x == 64) *last_flag = (atomicAdd(p.counters + tile, 1u) == static_cast<unsigned>(p.splits - 1));
+      named_bar_sync(1, 2 * kWbTeamThreads);
+      if (*reinterpret_cast<volatile int*>(last_flag)) {
+        __threadfence();
+        // the last split adds the partials in split order; all producer threads share the
+        // (4-column group, token) items, two per thread in flight
+        const int ngrp = min(64, (p.K - k0) >> 2);
+        const int items = ngrp * ntok;
+        const int64_t sstride = static_cast<int64_t>(ntiles) * 64 * 256;
+        const float4* src = reinterpret_cast<const float4*>(p.partial) + static_cast<int64_t>(tile) * 64 * 256;
+        constexpr int kRt = 2 * kWbTeamThreads;
+        for (int it0 = threadIdx.x - 64; it0 < items; it0 += 2 * kRt) {
+          int off[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int it = it0 + u * kRt;
+            off[u] = (it / ntok) * 256 + it % ntok;
+          }
+          float4 acc[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            acc[u] = it0 + u * kRt < items ? __ldcg(src + off[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int sp = 1; sp < p.splits; ++sp) {
+            float4 v[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+              v[u] = it0 + u * kRt < items ? __ldcg(src + sp * sstride + off[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              acc[u].x += v[u].x;
+              acc[u].y += v[u].y;
+              acc[u].z += v[u].z;
+              acc[u].w += v[u].w;
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (it0 + u * kRt < items) {
+              float f[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+              uint2* dst = reinterpret_cast<uint2*>(p.dx + static_cast<int64_t>(tok0 + (off[u] & 255)) * p.K + k0 +
+                                                    (off[u] >> 8) * 4);
+              if (p.accumulate) {
+                const uint2 old = *dst;
+                f[0] += __uint_as_float(old.x << 16);
+                f[1] += __uint_as_float(old.x & 0xffff0000u);
+                f[2] += __uint_as_float(old.y << 16);
+                f[3] += __uint_as_float(old.y & 0xffff0000u);
+              }
+              *dst = make_uint2(pack_bf16x2_rn(f[0], f[1]), pack_bf16x2_rn(f[2], f[3]));
+            }
+          }
+        }
+        if (threadIdx.x == 64) p.counters[tile] = 0;
       }
     }
   }
@@ -723,21 +837,50 @@ static FwdPlan plan_fwd(int M, int N, int K, int num_sms) {
   FwdPlan pl;
   if (M < 1) M = 1;
   if (num_sms < 1) num_sms = 1;
-  pl.ntok = M <= 16 ? 16 : (M <= 64 ? 64 : 256);
+  pl.ntok = M <= 16 ? 16 : (M <= 64 ? 64 : (M <= 128 ? 128 : 256));
   pl.row_tiles = (N + 127) / 128;
   pl.tok_tiles = (M + pl.ntok - 1) / pl.ntok;
   const int tiles = pl.row_tiles * pl.tok_tiles;
   const int kb_total = K / 64;
-  int splits = 1;
-  if (tiles < num_sms) {
-    const int want = pl.ntok == 256 ? num_sms : 2 * num_sms;  // small tiles: two CTAs per SM fit
-    splits = (want + tiles - 1) / tiles;
-    if (splits > kb_total) splits = kb_total;
-    if (pl.ntok == 256 && splits > 4) splits = 4;
-  }
+  // split k while the grid still fits one wave (one 576-thread CTA per SM); the last CTA of a
+  // tile adds the partials, so more than 4 splits costs more in that sum than it saves
+  int splits = num_sms / tiles;
+  if (splits > 4) splits = 4;
+  if (splits > kb_total) splits = kb_total;
+  if (splits < 1) splits = 1;
   pl.kb_per_split = (kb_total + splits - 1) / splits;
   pl.splits = (kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
   return pl;
+}
+
+struct BwdPlan {
+  int ktiles, tok_tiles, splits, nb_per_split;
+};
+
+// Backward dX: 256-column x 256-token tiles; with few tiles (small token counts) the n blocks of
+// a tile are split over up to 4 CTAs while the grid fits one wave, the last CTA adding the partials.
+static BwdPlan plan_bwd(int M, int N, int K, int num_sms) {
+  BwdPlan pl;
+  if (M < 1) M = 1;
+  if (num_sms < 1) num_sms = 1;
+  pl.ktiles = (K + 255) / 256;
+  pl.tok_tiles = (M + 255) / 256;
+  const int tiles = pl.ktiles * pl.tok_tiles, nb = (N + 63) / 64 > 0 ? (N + 63) / 64 : 1;
+  int splits = num_sms / tiles;
+  if (splits > 4) splits = 4;
+  if (splits > nb) splits = nb;
+  if (splits < 1) splits = 1;
+  pl.nb_per_split = (nb + splits - 1) / splits;
+  pl.splits = (nb + pl.nb_per_split - 1) / pl.nb_per_split;
+  return pl;
+}
+
+size_t bwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
+  if (use_pair_gemm(M)) return 0;
+  const BwdPlan pl = plan_bwd(M, N, K, num_sms);
+  if (pl.splits == 1) return 0;
+  const size_t tiles = static_cast<size_t>(pl.ktiles) * pl.tok_tiles;
+  return pl.splits * tiles * 256 * 256 * sizeof(float) + tiles * 4 + 256;
 }
 
 size_t fwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
@@ -821,12 +964,13 @@ cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, cons
   const dim3 grid(pl.row_tiles, pl.tok_tiles, pl.splits);
   if (pl.ntok == 16) return run_wa<16, 4>(tx, tst, prm, grid, s);
   if (pl.ntok == 64) return run_wa<64, 4>(tx, tst, prm, grid, s);
+  if (pl.ntok == 128) return run_wa<128, 4>(tx, tst, prm, grid, s);
   return run_wa<256, 4>(tx, tst, prm, grid, s);
 }
 
 cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, const __nv_bfloat16* su,
-                               const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate,
-                               unsigned* status, uint64_t wait_ns, cudaStream_t s, int with_lora) {
+                               const __nv_bfloat16* lora_a, int r, __nv_bfloat16* dx, int accumulate, void* ws,
+                               unsigned* status, uint64_t wait_ns, int num_sms, cudaStream_t s, int with_lora) {
   if (use_pair_gemm(M))
     return launch_bwd_gemm_pair(dy, M, w, su, lora_a, r, dx, accumulate, status, wait_ns, s, with_lora);
   const int N = static_cast<int>(w.n), K = static_cast<int>(w.k);
@@ -849,11 +993,23 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
   prm.lora_blocks = with_lora ? (r + 63) / 64 : 0;
   prm.accumulate = accumulate;
   prm.wait_ns = wait_ns;
+  const BwdPlan pl = plan_bwd(M, N, K, num_sms);
+  prm.splits = pl.splits;
+  prm.nb_per_split = pl.nb_per_split;
+  prm.partial = nullptr;
+  prm.counters = nullptr;
+  if (pl.splits > 1) {
+    const size_t tiles = static_cast<size_t>(pl.ktiles) * pl.tok_tiles;
+    prm.partial = static_cast<float*>(ws);
+    prm.counters = reinterpret_cast<unsigned*>(prm.partial + pl.splits * tiles * 256 * 256);
+    const cudaError_t e = cudaMemsetAsync(prm.counters, 0, tiles * 4, s);
+    if (e != cudaSuccess) return e;
+  }
   constexpr int kStages = 3;
   const size_t smem = WbCfg<kStages>::kSmem;
   cudaError_t e = set_smem_limit_once(k_qgemm_wb<kStages>, smem);
   if (e != cudaSuccess) return e;
-  const dim3 grid((K + 255) / 256, (M + 255) / 256);
+  const dim3 grid(pl.ktiles, pl.tok_tiles, pl.splits);
   e = launch_pdl(k_qgemm_wb<kStages>, grid, dim3(kWbThreads), smem, s, 1, tdy, tsu, tla, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -919,10 +1075,10 @@ int fwd_gemm_ctas(int M, int N, int K, int num_sms) {
   return pl.row_tiles * pl.tok_tiles * pl.splits;
 }
 
-int bwd_gemm_ctas(int M, int N, int K) {
-  (void)N;
+int bwd_gemm_ctas(int M, int N, int K, int num_sms) {
   if (use_pair_gemm(M)) return bwd_pair_ctas(M, K);
-  return ((K + 255) / 256) * ((M + 255) / 256);
+  const BwdPlan pl = plan_bwd(M, N, K, num_sms);
+  return pl.ktiles * pl.tok_tiles * pl.splits;
 }
 
 cudaError_t launch_wait_selftest(unsigned* status, uint64_t wait_ns, cudaStream_t s) {

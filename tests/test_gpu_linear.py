@@ -72,6 +72,14 @@ def test_ragged_tiles(lib, m, n, k, r):
     _check_all(lib, case)
 
 
+# 17..256 tokens run the small-token GEMMs with k split over up to four CTAs per 128-row tile and
+# the partials added by the tile's last CTA: 65..128 tokens (the 128-token variant), a ragged
+# row tail (1000 = 7 x 128 + 104), and the 4096^2 weight at 128 tokens.
+@pytest.mark.parametrize("m,n,k,r", [(100, 1000, 2048, 16), (128, 4096, 4096, 16), (65, 384, 768, 8)])
+def test_small_token_split_k(lib, m, n, k, r):
+    _check_all(lib, synthetic.linear_case(n, k, m, r, 2.0 * r, base_seed=m * 7 + n + k))
+
+
 @pytest.mark.parametrize("m", [1, 4, 16])
 def test_decode_tokens(lib, m):
     case = synthetic.linear_case(4096, 4096, m, 16, 32.0, base_seed=100 + m)
