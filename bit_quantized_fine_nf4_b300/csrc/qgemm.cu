@@ -53,6 +53,7 @@ struct WaParams {
 };
 
 constexpr int kWaTeams = 4;      // producer teams (4 warps each) taking k blocks round-robin
+constexpr int kMaxSplitK = 4;    // split-K / split-n ways of the small-token GEMMs (partials summed by the last CTA)
 constexpr int kWaThreads = 64 + kWaTeams * 128;  // warp 0: TMA + TMEM alloc, warp 1: MMA, then the producer teams
 
 template <int NTOK, int STAGES>
@@ -247,35 +248,36 @@ __global__ void __launch_bounds__(kWaThreads, 1)
       if (*reinterpret_cast<volatile int*>(last_flag)) {
         __threadfence();
         // the last split adds the partials in split order; all producer threads share the
-        // (4-column group, row) items, four items per thread in flight
+        // (4-column group, row) items
         const int items = ((ncv + 3) >> 2) * 128;
         const int64_t sstride = static_cast<int64_t>(ntiles) * (NTOK / 4) * 128;
         const float4* src = reinterpret_cast<const float4*>(p.partial) + static_cast<int64_t>(tile) * (NTOK / 4) * 128;
         constexpr int kRt = kWaTeams * 128;
-        for (int it0 = threadIdx.x - 64; it0 < items; it0 += 4 * kRt) {
-          float4 acc[4];
+        for (int it0 = threadIdx.x - 64; it0 < items; it0 += 2 * kRt) {
+          // every split's loads of two items are issued before the first add
+          float4 v[kMaxSplitK][2];
 #pragma unroll
-          for (int u = 0; u < 4; ++u)
-            acc[u] = it0 + u * kRt < items ? __ldcg(src + it0 + u * kRt) : make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int sp = 1; sp < p.splits; ++sp) {
-            float4 v[4];
+          for (int sp = 0; sp < kMaxSplitK; ++sp)
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              v[u] = it0 + u * kRt < items ? __ldcg(src + sp * sstride + it0 + u * kRt) : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int u = 0; u < 2; ++u)
+              v[sp][u] = sp < p.splits && it0 + u * kRt < items ? __ldcg(src + sp * sstride + it0 + u * kRt)
+                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              acc[u].x += v[u].x;
-              acc[u].y += v[u].y;
-              acc[u].z += v[u].z;
-              acc[u].w += v[u].w;
+          for (int u = 0; u < 2; ++u) {
+            float4 acc = v[0][u];
+#pragma unroll
+            for (int sp = 1; sp < kMaxSplitK; ++sp) {
+              if (sp < p.splits) {
+                acc.x += v[sp][u].x;
+                acc.y += v[sp][u].y;
+                acc.z += v[sp][u].z;
+                acc.w += v[sp][u].w;
+              }
             }
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
             const int it = it0 + u * kRt;
             const int orow = n0 + (it & 127), otok = tok0 + (it >> 7) * 4;
             if (it < items && orow < p.N) {
-              const float f[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
+              const float f[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e)
                 if (otok + e < p.M) p.y[static_cast<int64_t>(otok + e) * p.N + orow] = __float2bfloat16_rn(f[e]);
@@ -533,7 +535,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
       if (*reinterpret_cast<volatile int*>(last_flag)) {
         __threadfence();
         // the last split adds the partials in split order; all producer threads share the
-        // (4-column group, token) items, two per thread in flight
+        // (4-column group, token) items
         const int ngrp = min(64, (p.K - k0) >> 2);
         const int items = ngrp * ntok;
         const int64_t sstride = static_cast<int64_t>(ntiles) * 64 * 256;
@@ -546,27 +548,27 @@ __global__ void __launch_bounds__(kWbThreads, 1)
             const int it = it0 + u * kRt;
             off[u] = (it / ntok) * 256 + it % ntok;
           }
-          float4 acc[2];
+          // every split's loads of two items are issued before the first add
+          float4 v[kMaxSplitK][2];
 #pragma unroll
-          for (int u = 0; u < 2; ++u)
-            acc[u] = it0 + u * kRt < items ? __ldcg(src + off[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int sp = 1; sp < p.splits; ++sp) {
-            float4 v[2];
+          for (int sp = 0; sp < kMaxSplitK; ++sp)
 #pragma unroll
             for (int u = 0; u < 2; ++u)
-              v[u] = it0 + u * kRt < items ? __ldcg(src + sp * sstride + off[u]) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              acc[u].x += v[u].x;
-              acc[u].y += v[u].y;
-              acc[u].z += v[u].z;
-              acc[u].w += v[u].w;
-            }
-          }
+              v[sp][u] = sp < p.splits && it0 + u * kRt < items ? __ldcg(src + sp * sstride + off[u])
+                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
+            float f[4] = {v[0][u].x, v[0][u].y, v[0][u].z, v[0][u].w};
+#pragma unroll
+            for (int sp = 1; sp < kMaxSplitK; ++sp) {
+              if (sp < p.splits) {
+                f[0] += v[sp][u].x;
+                f[1] += v[sp][u].y;
+                f[2] += v[sp][u].z;
+                f[3] += v[sp][u].w;
+              }
+            }
             if (it0 + u * kRt < items) {
-              float f[4] = {acc[u].x, acc[u].y, acc[u].z, acc[u].w};
               uint2* dst = reinterpret_cast<uint2*>(p.dx + static_cast<int64_t>(tok0 + (off[u] & 255)) * p.K + k0 +
                                                     (off[u] >> 8) * 4);
               if (p.accumulate) {
@@ -845,7 +847,7 @@ static FwdPlan plan_fwd(int M, int N, int K, int num_sms) {
   // split k while the grid still fits one wave (one 576-thread CTA per SM); the last CTA of a
   // tile adds the partials, so more than 4 splits costs more in that sum than it saves
   int splits = num_sms / tiles;
-  if (splits > 4) splits = 4;
+  if (splits > kMaxSplitK) splits = kMaxSplitK;
   if (splits > kb_total) splits = kb_total;
   if (splits < 1) splits = 1;
   pl.kb_per_split = (kb_total + splits - 1) / splits;
@@ -867,7 +869,7 @@ static BwdPlan plan_bwd(int M, int N, int K, int num_sms) {
   pl.tok_tiles = (M + 255) / 256;
   const int tiles = pl.ktiles * pl.tok_tiles, nb = (N + 63) / 64 > 0 ? (N + 63) / 64 : 1;
   int splits = num_sms / tiles;
-  if (splits > 4) splits = 4;
+  if (splits > kMaxSplitK) splits = kMaxSplitK;
   if (splits > nb) splits = nb;
   if (splits < 1) splits = 1;
   pl.nb_per_split = (nb + splits - 1) / splits;
