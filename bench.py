@@ -32,10 +32,11 @@ bounded sample of the same workload and prints the same line with
 
 ``--only quant [--shape NxK]`` / ``--only decode [--decode-layers L]
 [--decode-tokens 1,4,16]`` / ``--only merge`` / ``--only smalltok [--tokens M]``
-run just that secondary measurement (quantise + dequantise of one bf16 weight;
-the decode sweep; the merge of the 4096^2 projection; fwd+bwd at M <= 256
-tokens) and print its figures -- small, repeatable workloads for profilers,
-not bench lines.
+/ ``--only mlp`` / ``--only upproj65b`` run just that secondary measurement
+(quantise + dequantise of one bf16 weight; the decode sweep; the merge of the
+4096^2 projection; fwd+bwd at M <= 256 tokens; the Llama-7B MLP block; the
+65B up-projection fwd+bwd without the 80-layer quantise) and print its figures
+-- small, repeatable workloads for profilers, not bench lines.
 """
 
 from __future__ import annotations
@@ -391,7 +392,8 @@ def mlp_block(q, torch, steps, flush, hidden=4096, inter=11008, m=2048, r=16, al
     with torch.cuda.graph(graph):
         fwd_bwd()
     for _ in range(3):
-        flush()
+        if flush is not None:
+            flush()
         graph.replay()
     ms = statistics.median(time_events(torch, graph.replay, steps, flush))
     q.check_status()
@@ -431,7 +433,20 @@ def llama65b(q, torch, steps, flush, layers=80, m=4096, r=64, alpha=16.0):
     q.check_status()
     resident = sum(rc.nbytes() for rc in recs)
     qbytes = 2 * params + resident
-    up = recs[4]  # layer 0 up-projection, 22016 x 8192
+    out = {"layers": layers, "matrices": len(recs), "params": params, "resident_gb": resident / 1e9,
+           "quantize_ms": qms, "quantize_gbs": qbytes / qms / 1e6, "weight_generation_ms_not_counted": gen_ms,
+           "upproj_fwd_bwd": upproj_step(q, torch, steps, flush, recs[4], m=m, r=r, alpha=alpha)}
+    del recs
+    torch.cuda.empty_cache()
+    return out
+
+
+def upproj_step(q, torch, steps, flush, up=None, m=4096, r=64, alpha=16.0):
+    """fwd+bwd of a Llama-65B up-projection (22016x8192 NF4 record `up`, quantised here when None)
+    at m tokens, rank r, captured once in a CUDA graph and replayed."""
+    import synthetic
+    if up is None:
+        up = q.quantize(synthetic.weight(22016, 8192, device="cuda", seed=synthetic.stack_seed(0, 4)))
     a, b = synthetic.lora_pair(up.n, up.k, r, device="cuda", seed=77)
     x = synthetic.activations(m, up.k, device="cuda", seed=78)
     dy = synthetic.activations(m, up.n, device="cuda", seed=79)
@@ -453,18 +468,14 @@ def llama65b(q, torch, steps, flush, layers=80, m=4096, r=64, alpha=16.0):
     with torch.cuda.graph(graph):
         fwd_bwd()
     for _ in range(3):
-        flush()
+        if flush is not None:
+            flush()
         graph.replay()
     ms = statistics.median(time_events(torch, graph.replay, steps, flush))
     q.check_status()
     flops = step_flops(m, up.n, up.k, r)
-    out = {"layers": layers, "matrices": len(recs), "params": params, "resident_gb": resident / 1e9,
-           "quantize_ms": qms, "quantize_gbs": qbytes / qms / 1e6, "weight_generation_ms_not_counted": gen_ms,
-           "upproj_fwd_bwd": {"n": up.n, "k": up.k, "m": m, "r": r, "alpha": alpha, "ms_per_step": ms,
-                              "tflops": flops / (ms / 1e3) / 1e12, "flops_per_step": flops}}
-    del recs, up, x, dy, y, dx
-    torch.cuda.empty_cache()
-    return out
+    return {"n": up.n, "k": up.k, "m": m, "r": r, "alpha": alpha, "ms_per_step": ms,
+            "tflops": flops / (ms / 1e3) / 1e12, "flops_per_step": flops}
 
 
 def merge_rate(q, torch, flush, n=4096, k=4096, r=16, alpha=32.0):
@@ -810,7 +821,8 @@ def main(argv=None):
     ap.add_argument("--decode-layers", type=int, default=32)
     ap.add_argument("--decode-tokens", default="1", help="token counts of --only decode, e.g. 1,4,16")
     ap.add_argument("--tokens", type=int, default=128, help="tokens of --only smalltok (<= 256: small-token GEMMs)")
-    ap.add_argument("--only", choices=("quant", "decode", "merge", "smalltok", "adamw", "dropout"), default=None,
+    ap.add_argument("--only", choices=("quant", "decode", "merge", "smalltok", "adamw", "dropout", "mlp", "upproj65b"),
+                    default=None,
                     help="run one secondary measurement alone (a workload for profilers)")
     ap.add_argument("--shape", default="22016x8192", help="weight shape for --only quant")
     args = ap.parse_args(argv)
@@ -829,6 +841,10 @@ def main(argv=None):
             print(json.dumps(dropout_step(q, torch, args.steps, None)), flush=True)
         elif args.only == "smalltok":
             print(json.dumps(small_token_step(q, torch, m=args.tokens)), flush=True)
+        elif args.only == "mlp":
+            print(json.dumps(mlp_block(q, torch, args.steps, None)), flush=True)
+        elif args.only == "upproj65b":
+            print(json.dumps(upproj_step(q, torch, args.steps, None)), flush=True)
         else:
             toks = tuple(int(t) for t in args.decode_tokens.split(","))
             print(json.dumps(decode_sweep(q, torch, layers=args.decode_layers, tokens=toks)), flush=True)

@@ -143,6 +143,12 @@ FwdWs fwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 
 // The forward's LoRA down-projection runs as the tiled TMA kernel beside the CTA-pair GEMM.
 bool use_side(int64_t m, int r) { return qlora::use_pair_gemm(static_cast<int>(m)) && qlora::lora_side_supported(r); }
+// The backward's U = dY B runs there too, on a k-major copy of B (the TMA kernel walks k in 64-wide
+// boxes), where the fragment-gathering kernel is slow: wide r, long n, or few tokens (measured: the
+// 4096^2 projection at 2048 tokens and r = 16 is faster on k_lora_down, 12 against 16 us).
+bool use_side_bwd(int64_t m, int64_t n, int r) {
+  return qlora::lora_side_supported(r) && n % 64 == 0 && (r > 16 || n > 4096 || m <= 256);
+}
 
 struct BwdWs {
   size_t su, st, ld, lg, gemm, total;
@@ -156,6 +162,12 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
   w.su = lora_operand_bytes(m, r);
   w.st = w.su;
   w.ld = align256(qlora::lora_down_workspace_bytes(static_cast<int>(m), static_cast<int>(n), r, sms));
+  if (use_side_bwd(m, n, r)) {
+    // B^T [r, n], then the split-k partials and counters of U = dY B
+    const size_t bt = align256(static_cast<size_t>(r) * n * 2) +
+                      align256(qlora::lora_side_bwd_workspace_bytes(static_cast<int>(m), static_cast<int>(n), r, sms));
+    if (bt > w.ld) w.ld = bt;
+  }
   w.lg = align256(qlora::lora_grads_workspace_bytes(static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), r, sms));
   w.gemm = align256(qlora::bwd_gemm_workspace_bytes(static_cast<int>(m), static_cast<int>(n), static_cast<int>(k), sms));
   w.total = w.su + w.st + w.ld + w.lg + w.gemm;
@@ -167,12 +179,13 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 // and, while profiling is on, bracketed by two CUDA events on its stream.
 enum ProfName : int {
   P_QUANTIZE = 0, P_DEQUANTIZE, P_LORA_DOWN, P_FWD_GEMM, P_BWD_GEMM, P_LORA_GRADS, P_SILU_FWD, P_SILU_BWD,
-  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_MERGE, P_LOWRANK, P_ADAMW, P_DROPOUT, P_COUNT
+  P_SELFTEST, P_FWD_GROUPED, P_LORA_SIDE_FWD, P_MERGE, P_LOWRANK, P_ADAMW, P_DROPOUT, P_LORA_SIDE_BWD, P_TRANSPOSE,
+  P_COUNT
 };
 const char* const kProfNames[P_COUNT] = {"nf4_quantize(3 kernels)", "nf4_dequantize", "lora_down", "fwd_gemm",
                                          "bwd_dx_gemm", "lora_grads", "silu_mul_fwd", "silu_mul_bwd",
                                          "wait_selftest", "fwd_grouped", "lora_side_fwd", "nf4_merge",
-                                         "lowrank_update", "adamw", "dropout"};
+                                         "lowrank_update", "adamw", "dropout", "lora_side_bwd", "lora_b_transpose"};
 std::atomic<unsigned long long> g_launches{0};
 std::atomic<bool> g_prof_on{false};
 struct ProfRec {
@@ -574,7 +587,23 @@ static int linear_bwd_impl(const uint16_t* dy, const uint16_t* x, int64_t m, con
   // and, forked onto the side stream after U, the dA / dB kernel on the SMs the
   // GEMM leaves idle; the caller's stream waits for the side stream before the
   // call returns.
-  {
+  if (use_side_bwd(M, N, r)) {
+    // B^T (a k-major copy of B) and, in the same launch, sT = bf16(s * t_save) and U's split
+    // counters cleared; then U = dY B by the TMA kernel with k split over the SMs (the dX GEMM
+    // launches as U's CTAs finish and waits for sU only before its LoRA k block)
+    __nv_bfloat16* bt = static_cast<__nv_bfloat16*>(ldws);
+    void* uws = static_cast<char*>(ldws) + align256(static_cast<size_t>(r) * N * 2);
+    unsigned* cnt = qlora::lora_side_bwd_counters(uws, M, N, r, di->num_sms);
+    {
+      Span sp(P_TRANSPOSE, s, 1);
+      e = qlora::launch_transpose_kr(reinterpret_cast<const __nv_bfloat16*>(lora_b), bt, N, r, di->num_sms, s, t_save,
+                                     st, static_cast<int64_t>(M), scale, cnt, cnt ? (M + 127) / 128 : 0);
+    }
+    if (e == cudaSuccess) {
+      Span sp(P_LORA_SIDE_BWD, s, 1);
+      e = qlora::launch_lora_side_bwd(dyb, bt, M, N, r, scale, su, uws, di->num_sms, di->status, wait, s);
+    }
+  } else {
     // U = dY B (B read as stored) on all SMs and, in the same launch, sT = bf16(s * t_save)
     Span sp(P_LORA_DOWN, s, 1);
     e = qlora::launch_lora_down(dyb, reinterpret_cast<const __nv_bfloat16*>(lora_b), 0, M, N, r, scale, nullptr, su,

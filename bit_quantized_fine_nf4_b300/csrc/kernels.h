@@ -28,6 +28,11 @@ cudaError_t launch_nf4_dequantize(const uint8_t* codes, const int8_t* absq, cons
 
 // lora_small.cu
 size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms);
+// mtk [r, K] = mt^T for mt [K, r] (K % 8 == 0), plus two side jobs in the same launch:
+// cvt_dst = bf16(cvt_scale * cvt_src) as in launch_lora_down, and zero_words words set to zero.
+cudaError_t launch_transpose_kr(const __nv_bfloat16* mt, __nv_bfloat16* mtk, int K, int r, int num_sms, cudaStream_t s,
+                                const float* cvt_src, __nv_bfloat16* cvt_dst, int64_t cvt_rows, float cvt_scale,
+                                unsigned* zero, int zero_words);
 // Row stride of the internal bf16 LoRA operands sT / sU ([rows, r] padded with
 // zero columns): r rounded up to a multiple of 8, so every row starts on a
 // 16-byte boundary as TMA requires.
@@ -124,6 +129,14 @@ bool make_tensor_map_bf16_2d(CUtensorMap* m, const void* base, uint64_t inner, u
 // Forward LoRA down-projection beside the pair GEMM (lora_side.cu), 1 <= r <= 64:
 // T = X A^T -> t_save, sT = bf16(s T), by at most max_ctas CTAs.
 bool lora_side_supported(int r);
+// Backward U = dY B beside the dX GEMM: dY [M, N], bt = B^T [r, N] (N % 64 == 0), su = bf16(scale U)
+// [M, lora_ld(r)]; k is split over CTAs (ws: lora_side_bwd_workspace_bytes; its counter words,
+// lora_side_bwd_counters, must be zero at launch and are zero again afterwards).
+size_t lora_side_bwd_workspace_bytes(int M, int K, int r, int num_sms);
+unsigned* lora_side_bwd_counters(void* ws, int M, int K, int r, int num_sms);
+cudaError_t launch_lora_side_bwd(const __nv_bfloat16* dy, const __nv_bfloat16* bt, int M, int N, int r, float scale,
+                                 __nv_bfloat16* su, void* ws, int num_sms, unsigned* status, uint64_t wait_ns,
+                                 cudaStream_t s);
 
 cudaError_t launch_lora_side_fwd(const __nv_bfloat16* x, const __nv_bfloat16* lora_a, int M, int K, int r, float scale,
                                  float* t_save, __nv_bfloat16* st, int max_ctas, unsigned* status, uint64_t wait_ns,

@@ -228,6 +228,48 @@ size_t lora_down_workspace_bytes(int M, int K, int r, int num_sms) {
   return 0;  // no cross-CTA reduction
 }
 
+// mtk[j, k] = mt[k, j]: one thread per (8 consecutive k, j), j fastest so a warp reads whole rows
+// of mt.  Side jobs in the same launch: cvt_dst = bf16(cvt_scale * cvt_src) as in k_lora_down, and
+// zero_words words of `zero` cleared.
+__global__ void __launch_bounds__(256) k_transpose_kr(const unsigned short* __restrict__ mt,
+                                                      unsigned short* __restrict__ mtk, int K, int r,
+                                                      const float* __restrict__ cvt_src,
+                                                      __nv_bfloat16* __restrict__ cvt_dst, int64_t cvt_rows,
+                                                      float cvt_scale, unsigned* __restrict__ zero, int zero_words) {
+  const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_words; i += nthreads) zero[i] = 0u;
+  const int64_t total = static_cast<int64_t>(K / 8) * r;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += nthreads) {
+    const int j = static_cast<int>(i % r);
+    const int64_t k0 = (i / r) * 8;
+    uint32_t v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __ldg(mt + (k0 + e) * r + j);
+    *reinterpret_cast<uint4*>(mtk + static_cast<int64_t>(j) * K + k0) =
+        make_uint4(v[0] | (v[1] << 16), v[2] | (v[3] << 16), v[4] | (v[5] << 16), v[6] | (v[7] << 16));
+  }
+  const int rk = (r + 7) & ~7;
+  const int64_t n_out = cvt_rows * rk;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_out; i += nthreads) {
+    const int64_t row = i / rk;
+    const int j = static_cast<int>(i - row * rk);
+    cvt_dst[i] = j < r ? __float2bfloat16_rn(__fmul_rn(cvt_src[row * r + j], cvt_scale)) : __float2bfloat16_rn(0.f);
+  }
+}
+
+cudaError_t launch_transpose_kr(const __nv_bfloat16* mt, __nv_bfloat16* mtk, int K, int r, int num_sms, cudaStream_t s,
+                                const float* cvt_src, __nv_bfloat16* cvt_dst, int64_t cvt_rows, float cvt_scale,
+                                unsigned* zero, int zero_words) {
+  const int64_t work = static_cast<int64_t>(K / 8) * r + cvt_rows * ((r + 7) & ~7);
+  int64_t blocks = (work + 255) / 256;
+  if (blocks > 8 * static_cast<int64_t>(num_sms)) blocks = 8 * static_cast<int64_t>(num_sms);
+  if (blocks < 1) blocks = 1;
+  k_transpose_kr<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<const unsigned short*>(mt),
+                                                              reinterpret_cast<unsigned short*>(mtk), K, r, cvt_src,
+                                                              cvt_dst, cvt_rows, cvt_scale, zero, zero_words);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, int mt_kmajor, int M, int K, int r,
                              float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int max_ctas,
                              cudaStream_t s, const float* cvt_src, __nv_bfloat16* cvt_dst, int64_t cvt_rows,

@@ -324,11 +324,27 @@ __global__ void __launch_bounds__(kPrThreads, 1)
                    pack_bf16x2_rn(f[2], f[3]), pack_bf16x2_rn(f[4], f[5]), pack_bf16x2_rn(f[6], f[7]));
           } else if (tok < p.M) {
             __nv_bfloat16* d = p.out + static_cast<int64_t>(tok) * p.out_cols + col;
+            if ((p.out_cols & 7) == 0 && col + 8 <= p.out_cols) {
+              // 16-byte read-modify-write (accumulate: float32 sum of the old bf16 and the result)
+              uint4* d4 = reinterpret_cast<uint4*>(d);
+              if (p.accumulate) {
+                const uint4 o = *d4;
+                const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (col + j < p.out_cols) {
-                const float o = p.accumulate ? __bfloat162float(d[j]) : 0.f;
-                d[j] = __float2bfloat16_rn(f[j] + o);
+                for (int j = 0; j < 4; ++j) {
+                  f[2 * j] += __uint_as_float(ow[j] << 16);
+                  f[2 * j + 1] += __uint_as_float(ow[j] & 0xffff0000u);
+                }
+              }
+              *d4 = make_uint4(pack_bf16x2_rn(f[0], f[1]), pack_bf16x2_rn(f[2], f[3]), pack_bf16x2_rn(f[4], f[5]),
+                               pack_bf16x2_rn(f[6], f[7]));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                if (col + j < p.out_cols) {
+                  const float o = p.accumulate ? __bfloat162float(d[j]) : 0.f;
+                  d[j] = __float2bfloat16_rn(f[j] + o);
+                }
               }
             }
           }

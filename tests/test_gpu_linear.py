@@ -218,6 +218,19 @@ def test_pair_accumulate_flags(lib):
     _accumulate_against_oracle(lib, synthetic.linear_case(384, 320, 520, 16, 32.0, base_seed=21))
 
 
+# More tiles than CTA pairs fit at once (74 on a B300): 1030 tokens make 3 token tiles (the last
+# ragged), 32 x 3 = 96 pair tiles in two waves -- in the forward (n = 8192) and in the backward
+# (k = 8192); U = dY B of the backward runs on the k-major copy of B beside the dX GEMM.
+@pytest.mark.parametrize("m,n,k,r", [(1030, 8192, 2048, 16), (1030, 2048, 8192, 16)])
+def test_pair_multi_wave(lib, m, n, k, r):
+    _check_all(lib, synthetic.linear_case(n, k, m, r, 2.0 * r, base_seed=m + n // 64 + k // 64))
+
+
+def test_pair_multi_wave_accumulate(lib):
+    """Gradient accumulation into dX (16-byte read-modify-write in the GEMM epilogue), two waves."""
+    _accumulate_against_oracle(lib, synthetic.linear_case(2048, 8192, 1030, 16, 32.0, base_seed=77))
+
+
 def test_pair_lora_path_alone_with_zero_weight(lib):
     case = synthetic.linear_case(512, 256, 600, 16, 32.0, base_seed=22)
     case.w.zero_()
