@@ -83,6 +83,9 @@ __global__ void __launch_bounds__(kSideThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
+  // launched early (programmatic dependent launch): the set-up above overlaps the preceding kernel;
+  // its input rows and the outputs may belong to the preceding kernels of the stream
+  griddep_wait();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -290,13 +293,15 @@ static cudaError_t launch_side(const __nv_bfloat16* in, const __nv_bfloat16* mt,
   cfg.blockDim = dim3(kSideThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = grid >= 2 ? 1 : 0;
+  cfg.numAttrs = grid >= 2 ? 2 : 1;
   e = cudaLaunchKernelEx(&cfg, k_lora_side, ta, tb, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

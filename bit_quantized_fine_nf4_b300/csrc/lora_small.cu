@@ -107,6 +107,9 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
     }
     __syncthreads();
   }
+  // launched early (programmatic dependent launch): `in`, t_save and the outputs may belong to the
+  // preceding kernels of the stream (the LoRA matrix staged above does not)
+  griddep_wait();
   const int rk = (r + 7) & ~7;
   if (cvt_rows > 0) {
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -236,6 +239,8 @@ __global__ void __launch_bounds__(256) k_transpose_kr(const unsigned short* __re
                                                       const float* __restrict__ cvt_src,
                                                       __nv_bfloat16* __restrict__ cvt_dst, int64_t cvt_rows,
                                                       float cvt_scale, unsigned* __restrict__ zero, int zero_words) {
+  griddep_launch_dependents();
+  griddep_wait();  // launched early: the workspace it writes may be in use by the preceding kernels
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_words; i += nthreads) zero[i] = 0u;
   const int64_t total = static_cast<int64_t>(K / 8) * r;
@@ -264,9 +269,19 @@ cudaError_t launch_transpose_kr(const __nv_bfloat16* mt, __nv_bfloat16* mtk, int
   int64_t blocks = (work + 255) / 256;
   if (blocks > 8 * static_cast<int64_t>(num_sms)) blocks = 8 * static_cast<int64_t>(num_sms);
   if (blocks < 1) blocks = 1;
-  k_transpose_kr<<<static_cast<unsigned>(blocks), 256, 0, s>>>(reinterpret_cast<const unsigned short*>(mt),
-                                                              reinterpret_cast<unsigned short*>(mtk), K, r, cvt_src,
-                                                              cvt_dst, cvt_rows, cvt_scale, zero, zero_words);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_transpose_kr, reinterpret_cast<const unsigned short*>(mt),
+                                           reinterpret_cast<unsigned short*>(mtk), K, r, cvt_src, cvt_dst, cvt_rows,
+                                           cvt_scale, zero, zero_words);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -283,13 +298,15 @@ cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, i
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 2;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = grid >= 2 ? 1 : 0;
+  cfg.numAttrs = grid >= 2 ? 2 : 1;
   cudaError_t e = cudaSuccess;
   // mt staged in shared memory when it fits beside the reduction buffer
   const size_t stage_bytes = static_cast<size_t>(rp) * (static_cast<size_t>(K) + 8) * 2;
