@@ -193,6 +193,8 @@ __device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + expf
 
 __global__ void __launch_bounds__(256) k_silu_mul_fwd(const uint32_t* __restrict__ g, const uint32_t* __restrict__ u,
                                                       uint32_t* __restrict__ h, int64_t n2) {
+  griddep_launch_dependents();
+  griddep_wait();  // launched early: g and u come from the preceding kernels
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n2;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint32_t gw = g[i], uw = u[i];
@@ -209,6 +211,8 @@ __global__ void __launch_bounds__(256) k_silu_mul_fwd(const uint32_t* __restrict
 __global__ void __launch_bounds__(256) k_silu_mul_bwd(const uint32_t* __restrict__ dh, const uint32_t* __restrict__ g,
                                                       const uint32_t* __restrict__ u, uint32_t* __restrict__ dg,
                                                       uint32_t* __restrict__ du, int64_t n2) {
+  griddep_launch_dependents();
+  griddep_wait();  // launched early: dh comes from the preceding kernels
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n2;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint32_t dw = dh[i], gw = g[i], uw = u[i];
@@ -347,15 +351,31 @@ cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, i
   return cudaGetLastError();
 }
 
+// A 256-thread 1-D launch with programmatic stream serialization (the kernel waits with
+// griddep_wait before it touches memory the preceding kernels may still use).
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl_1d(void (*kernel)(KArgs...), int64_t grid, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(256);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_silu_mul_fwd(const uint16_t* g, const uint16_t* u, uint16_t* h, int64_t n, int num_sms,
                                 cudaStream_t s) {
   const int64_t n2 = n / 2;
   int64_t grid = (n2 + 255) / 256;
   if (grid > num_sms * 16) grid = num_sms * 16;
   if (grid < 1) grid = 1;
-  k_silu_mul_fwd<<<static_cast<unsigned>(grid), 256, 0, s>>>(reinterpret_cast<const uint32_t*>(g),
-                                                             reinterpret_cast<const uint32_t*>(u),
-                                                             reinterpret_cast<uint32_t*>(h), n2);
+  const cudaError_t e = launch_pdl_1d(k_silu_mul_fwd, grid, s, reinterpret_cast<const uint32_t*>(g),
+                                      reinterpret_cast<const uint32_t*>(u), reinterpret_cast<uint32_t*>(h), n2);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -365,9 +385,10 @@ cudaError_t launch_silu_mul_bwd(const uint16_t* dh, const uint16_t* g, const uin
   int64_t grid = (n2 + 255) / 256;
   if (grid > num_sms * 16) grid = num_sms * 16;
   if (grid < 1) grid = 1;
-  k_silu_mul_bwd<<<static_cast<unsigned>(grid), 256, 0, s>>>(
-      reinterpret_cast<const uint32_t*>(dh), reinterpret_cast<const uint32_t*>(g),
-      reinterpret_cast<const uint32_t*>(u), reinterpret_cast<uint32_t*>(dg), reinterpret_cast<uint32_t*>(du), n2);
+  const cudaError_t e = launch_pdl_1d(k_silu_mul_bwd, grid, s, reinterpret_cast<const uint32_t*>(dh),
+                                      reinterpret_cast<const uint32_t*>(g), reinterpret_cast<const uint32_t*>(u),
+                                      reinterpret_cast<uint32_t*>(dg), reinterpret_cast<uint32_t*>(du), n2);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

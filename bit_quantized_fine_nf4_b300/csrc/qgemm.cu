@@ -53,7 +53,15 @@ struct WaParams {
 };
 
 constexpr int kWaTeams = 4;      // producer teams (4 warps each) taking k blocks round-robin
-constexpr int kMaxSplitK = 4;    // split-K / split-n ways of the small-token GEMMs (partials summed by the last CTA)
+constexpr int kMaxSplitK = 4;    // split-K / split-n ways of the small-token GEMMs
+
+// 16-byte store into the shared memory of CTA `rank` of the cluster, at the offset `local` has here.
+__device__ __forceinline__ void st_cluster_v4(uint32_t local, uint32_t rank, float4 v) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local), "r"(rank));
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
 constexpr int kWaThreads = 64 + kWaTeams * 128;  // warp 0: TMA + TMEM alloc, warp 1: MMA, then the producer teams
 
 template <int NTOK, int STAGES>
@@ -304,12 +312,12 @@ struct WbParams {
   const float* step;
   const float* mean;
   __nv_bfloat16* dx;  // [M, K]
-  float* partial;     // [splits][tiles][64 column groups of 4][256 tokens] float4 (split n only)
-  unsigned* counters; // [tiles]
   unsigned* status;
   int M, N, K, r;
   int lora_blocks, accumulate;
-  int splits, nb_per_split;  // the n blocks are split over `splits` CTAs per tile (the last adds the LoRA steps)
+  // the n blocks of a tile are split over `splits` CTAs, one cluster (the last also runs the LoRA
+  // steps); their float32 results are added through distributed shared memory
+  int splits, nb_per_split;
   unsigned long long wait_ns;
 };
 
@@ -338,12 +346,11 @@ __global__ void __launch_bounds__(kWbThreads, 1)
   uint64_t* acc_full = empty + STAGES;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-  int* last_flag = abort_flag + 1;
   volatile int* vabort = abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // split = this CTA's rank in its cluster (clusters of `splits` CTAs along z)
   const int k0 = blockIdx.x * 256, tok0 = blockIdx.y * 256, split = blockIdx.z;
-  const int tile = blockIdx.x + gridDim.x * blockIdx.y, ntiles = gridDim.x * gridDim.y;
   // this CTA's n blocks [nb0, nb0 + n_main); the last split also runs the LoRA k steps
   const int nb0 = split * p.nb_per_split;
   const int n_main = min((p.N + 63) / 64 - nb0, p.nb_per_split);
@@ -356,7 +363,6 @@ __global__ void __launch_bounds__(kWbThreads, 1)
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
-    *last_flag = 0;
     fence_mbarrier_init();
   }
   if (warp == 0) {
@@ -367,6 +373,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
+  bool prod_ok = false;  // producers: the accumulators hold this CTA's result
 
   if (warp == 0) {
     if (lane == 0) {
@@ -474,29 +481,11 @@ __global__ void __launch_bounds__(kWbThreads, 1)
     ok = ok && !*vabort;
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
+    prod_ok = ok;
     const int quarter = warp & 3;
     const int wq = (warp - 2) >> 2;  // 0..3 among the warps of this quarter
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
-    const int ntok = min(256, p.M - tok0);  // tokens of this tile
-    if (ok && p.splits > 1) {
-      // partial of this split: [column / 4][256 tokens] float4, a warp's store is 512 contiguous bytes
-      float4* part = reinterpret_cast<float4*>(p.partial) + (static_cast<int64_t>(split) * ntiles + tile) * 64 * 256;
-      for (int chunk = wq; chunk < 16; chunk += 4) {
-        const int acc = chunk >> 3, col = (chunk & 7) * 32;
-        if (acc * 128 >= ntok) continue;  // warp-uniform: no token of this accumulator
-        const int tl = acc * 128 + quarter * 32 + lane;
-        uint32_t v[32];
-        __syncwarp();
-        tmem_ld_32x32b_x32(tbase + lane_field + acc * 256 + col, v);
-        tmem_ld_wait();
-        if (tl < ntok && k0 + col < p.K) {
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            part[((col >> 2) + q) * 256 + tl] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
-                                                            __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
-        }
-      }
-    } else if (ok) {
+    if (ok && p.splits == 1) {
       for (int chunk = wq; chunk < 16; chunk += 4) {
         const int acc = chunk >> 3, col = (chunk & 7) * 32;
         const int tok = tok0 + acc * 128 + quarter * 32 + lane;
@@ -527,67 +516,104 @@ __global__ void __launch_bounds__(kWbThreads, 1)
         }
       }
     }
-    if (p.splits > 1) {
-      __threadfence();
-      named_bar_sync(1, 2 * kWbTeamThreads);
-      if (threadIdx.x == 64) *last_flag = (atomicAdd(p.counters + tile, 1u) == static_cast<unsigned>(p.splits - 1));
-      named_bar_sync(1, 2 * kWbTeamThreads);
-      if (*reinterpret_cast<volatile int*>(last_flag)) {
-        __threadfence();
-        // the last split adds the partials in split order; all producer threads share the
-        // (4-column group, token) items
-        const int ngrp = min(64, (p.K - k0) >> 2);
-        const int items = ngrp * ntok;
-        const int64_t sstride = static_cast<int64_t>(ntiles) * 64 * 256;
-        const float4* src = reinterpret_cast<const float4*>(p.partial) + static_cast<int64_t>(tile) * 64 * 256;
-        constexpr int kRt = 2 * kWbTeamThreads;
-        for (int it0 = threadIdx.x - 64; it0 < items; it0 += 2 * kRt) {
-          int off[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int it = it0 + u * kRt;
-            off[u] = (it / ntok) * 256 + it % ntok;
-          }
-          // every split's loads of two items are issued before the first add
-          float4 v[kMaxSplitK][2];
-#pragma unroll
-          for (int sp = 0; sp < kMaxSplitK; ++sp)
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-              v[sp][u] = sp < p.splits && it0 + u * kRt < items ? __ldcg(src + sp * sstride + off[u])
-                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float f[4] = {v[0][u].x, v[0][u].y, v[0][u].z, v[0][u].w};
-#pragma unroll
-            for (int sp = 1; sp < kMaxSplitK; ++sp) {
-              if (sp < p.splits) {
-                f[0] += v[sp][u].x;
-                f[1] += v[sp][u].y;
-                f[2] += v[sp][u].z;
-                f[3] += v[sp][u].w;
-              }
-            }
-            if (it0 + u * kRt < items) {
-              uint2* dst = reinterpret_cast<uint2*>(p.dx + static_cast<int64_t>(tok0 + (off[u] & 255)) * p.K + k0 +
-                                                    (off[u] >> 8) * 4);
-              if (p.accumulate) {
-                const uint2 old = *dst;
-                f[0] += __uint_as_float(old.x << 16);
-                f[1] += __uint_as_float(old.x & 0xffff0000u);
-                f[2] += __uint_as_float(old.y << 16);
-                f[3] += __uint_as_float(old.y & 0xffff0000u);
-              }
-              *dst = make_uint2(pack_bf16x2_rn(f[0], f[1]), pack_bf16x2_rn(f[2], f[3]));
-            }
-          }
-        }
-        if (threadIdx.x == 64) p.counters[tile] = 0;
-      }
-    }
   }
   tc_fence_before();
   __syncthreads();
+  if (p.splits > 1) {
+    // Split n: the tile's 8 chunks of 32 output columns are owned round-robin (chunk c by the CTA
+    // of cluster rank c % splits).  Each CTA sends every chunk it does not own, as float32 values of
+    // both accumulators, to the owner's now idle stage buffers -- slot s (s - 1 past the owner) for
+    // sender s, laid out [owned chunk c / splits][accumulator][8 groups of 4 columns][128 rows]
+    // float4 -- and each owner adds the splits' values in split order and writes dX.
+    tc_fence_after();
+    cluster_sync();  // every CTA of the cluster is past its k loop: the stage buffers are free
+    const int ntok = min(256, p.M - tok0);
+    const int quarter = warp & 3, wq = (warp - 2) >> 2;
+    const int row = quarter * 32 + lane;
+    const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t base = smem_u32(smem);
+    const uint32_t slot_bytes = static_cast<uint32_t>((8 + p.splits - 1) / p.splits) * (2 * 8 * 128 * 16);
+    // unit u = (accumulator u >> 3, chunk u & 7); a warp takes the units u = wq (mod 4)
+    auto unit_kept = [&](int acc, int cc) { return acc * 128 < ntok && k0 + 32 * cc < p.K; };
+    if (warp >= 2 && prod_ok) {
+      for (int u = wq; u < 16; u += 4) {
+        const int acc = u >> 3, cc = u & 7, o = cc % p.splits;
+        if (o == split || !unit_kept(acc, cc)) continue;  // warp-uniform
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(tbase + lane_field + acc * 256 + 32 * cc, v);
+        tmem_ld_wait();
+        const uint32_t slot = static_cast<uint32_t>(split < o ? split : split - 1);
+        const uint32_t at = base + slot * slot_bytes + static_cast<uint32_t>(((cc / p.splits) * 2 + acc) * 8) * 2048u +
+                            static_cast<uint32_t>(row) * 16u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          st_cluster_v4(at + q * 2048u, static_cast<uint32_t>(o),
+                        make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                    __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3])));
+      }
+    }
+    cluster_sync();  // the slots have landed
+    if (warp >= 2 && prod_ok) {
+      for (int u = wq; u < 16; u += 4) {
+        const int acc = u >> 3, cc = u & 7;
+        if (cc % p.splits != split || !unit_kept(acc, cc)) continue;  // warp-uniform
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(tbase + lane_field + acc * 256 + 32 * cc, v);
+        tmem_ld_wait();
+        const int tl = acc * 128 + row;
+        if (tl >= ntok) continue;
+        const uint32_t in_slot = static_cast<uint32_t>(((cc / p.splits) * 2 + acc) * 8) * 2048u +
+                                 static_cast<uint32_t>(row) * 16u;
+#pragma unroll
+        for (int q8 = 0; q8 < 4; ++q8) {  // 8 columns per 16-byte store
+          float f[8];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int q = 2 * q8 + h;
+            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp = 0; sp < p.splits; ++sp) {
+              float4 x;
+              if (sp == split) {
+                x = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                                __uint_as_float(v[4 * q + 3]));
+              } else {
+                const uint32_t slot = static_cast<uint32_t>(sp < split ? sp : sp - 1);
+                x = *reinterpret_cast<const float4*>(smem + slot * slot_bytes + in_slot + q * 2048u);
+              }
+              if (sp == 0) {
+                sum = x;
+              } else {
+                sum.x += x.x;
+                sum.y += x.y;
+                sum.z += x.z;
+                sum.w += x.w;
+              }
+            }
+            f[4 * h] = sum.x;
+            f[4 * h + 1] = sum.y;
+            f[4 * h + 2] = sum.z;
+            f[4 * h + 3] = sum.w;
+          }
+          uint4* dst = reinterpret_cast<uint4*>(p.dx + static_cast<int64_t>(tok0 + tl) * p.K + k0 + 32 * cc + 8 * q8);
+          if (p.accumulate) {
+            const uint4 old = *dst;
+            const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              f[2 * j] += __uint_as_float(ow[j] << 16);
+              f[2 * j + 1] += __uint_as_float(ow[j] & 0xffff0000u);
+            }
+          }
+          *dst = make_uint4(pack_bf16x2_rn(f[0], f[1]), pack_bf16x2_rn(f[2], f[3]), pack_bf16x2_rn(f[4], f[5]),
+                            pack_bf16x2_rn(f[6], f[7]));
+        }
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+  }
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
@@ -878,11 +904,8 @@ static BwdPlan plan_bwd(int M, int N, int K, int num_sms) {
 }
 
 size_t bwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
-  if (use_pair_gemm(M)) return 0;
-  const BwdPlan pl = plan_bwd(M, N, K, num_sms);
-  if (pl.splits == 1) return 0;
-  const size_t tiles = static_cast<size_t>(pl.ktiles) * pl.tok_tiles;
-  return pl.splits * tiles * 256 * 256 * sizeof(float) + tiles * 4 + 256;
+  (void)M, (void)N, (void)K, (void)num_sms;
+  return 0;  // split n adds its partials inside a cluster
 }
 
 size_t fwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
@@ -898,8 +921,17 @@ size_t fwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
 // waits for it (griddep_wait) only before loading that kernel's output.
 // `cluster` > 1: clusters of that many CTAs along x.
 template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl_z(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                int cluster, int cluster_z, Args&&... args);
+template <typename... KArgs, typename... Args>
 static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                               int cluster, Args&&... args) {
+  return launch_pdl_z(kernel, grid, block, smem, s, cluster, 1, std::forward<Args>(args)...);
+}
+// `cluster` > 1: clusters of that many CTAs along x; `cluster_z` > 1: along z.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_pdl_z(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                int cluster, int cluster_z, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -911,9 +943,9 @@ static cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.x = cluster;
   attr[1].val.clusterDim.y = 1;
-  attr[1].val.clusterDim.z = 1;
+  attr[1].val.clusterDim.z = cluster_z;
   cfg.attrs = attr;
-  cfg.numAttrs = cluster > 1 ? 2 : 1;
+  cfg.numAttrs = (cluster > 1 || cluster_z > 1) ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -998,21 +1030,13 @@ cudaError_t launch_bwd_dx_gemm(const __nv_bfloat16* dy, int M, const Nf4Dev& w, 
   const BwdPlan pl = plan_bwd(M, N, K, num_sms);
   prm.splits = pl.splits;
   prm.nb_per_split = pl.nb_per_split;
-  prm.partial = nullptr;
-  prm.counters = nullptr;
-  if (pl.splits > 1) {
-    const size_t tiles = static_cast<size_t>(pl.ktiles) * pl.tok_tiles;
-    prm.partial = static_cast<float*>(ws);
-    prm.counters = reinterpret_cast<unsigned*>(prm.partial + pl.splits * tiles * 256 * 256);
-    const cudaError_t e = cudaMemsetAsync(prm.counters, 0, tiles * 4, s);
-    if (e != cudaSuccess) return e;
-  }
+  (void)ws;
   constexpr int kStages = 3;
   const size_t smem = WbCfg<kStages>::kSmem;
   cudaError_t e = set_smem_limit_once(k_qgemm_wb<kStages>, smem);
   if (e != cudaSuccess) return e;
   const dim3 grid(pl.ktiles, pl.tok_tiles, pl.splits);
-  e = launch_pdl(k_qgemm_wb<kStages>, grid, dim3(kWbThreads), smem, s, 1, tdy, tsu, tla, prm);
+  e = launch_pdl_z(k_qgemm_wb<kStages>, grid, dim3(kWbThreads), smem, s, 1, pl.splits, tdy, tsu, tla, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
