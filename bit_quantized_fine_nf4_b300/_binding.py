@@ -58,6 +58,7 @@ EXPORTS = (
     "qlora_set_wait_limit_ns",
     "qlora_selftest_wait_timeout",
     "qlora_device_sm_count",
+    "qlora_copy_many",
     "qlora_launch_count",
     "qlora_profile_enable",
     "qlora_profile_collect",
@@ -97,6 +98,10 @@ class _Problem(ctypes.Structure):
         ("y", ctypes.c_void_p),
         ("t_save", ctypes.c_void_p),
     ]
+
+
+class _Copy(ctypes.Structure):
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
 
 
 class _AdamwTensor(ctypes.Structure):
@@ -159,6 +164,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "qlora_set_wait_limit_ns": (c_int, [ctypes.c_uint64]),
         "qlora_selftest_wait_timeout": (c_int, [ctypes.c_uint64, _P]),
         "qlora_device_sm_count": (c_int, []),
+        "qlora_copy_many": (c_int, [ctypes.POINTER(_Copy), c_int, _P]),
         "qlora_launch_count": (ctypes.c_ulonglong, []),
         "qlora_profile_enable": (c_int, [c_int]),
         "qlora_profile_collect": (c_int, []),
@@ -580,6 +586,20 @@ def selftest_wait_timeout(wait_ns: int, stream=None) -> None:
 
 def device_sm_count() -> int:
     return load().qlora_device_sm_count()
+
+
+def copy_many(pairs, stream=None) -> None:
+    """Copy each (dst, src) pair of equally sized contiguous tensors (device, or pinned host)
+    in stream order, the pieces spread over the library's copy streams (qlora_copy_many)."""
+    arr = (_Copy * max(1, len(pairs)))()
+    for i, (dst, src) in enumerate(pairs):
+        if not (dst.is_contiguous() and src.is_contiguous()):
+            raise ValueError("copy_many: tensors must be contiguous")
+        nb = dst.numel() * dst.element_size()
+        if nb != src.numel() * src.element_size():
+            raise ValueError("copy_many: pair %d has %d and %d bytes" % (i, nb, src.numel() * src.element_size()))
+        arr[i] = _Copy(dst.data_ptr(), src.data_ptr(), nb)
+    _check(load().qlora_copy_many(arr, len(pairs), _stream(stream)))
 
 
 def launch_count() -> int:

@@ -28,6 +28,11 @@ struct DevInfo {
   cudaStream_t side = nullptr;
   cudaEvent_t fork = nullptr, join = nullptr;
   std::mutex side_mu;
+  // qlora_copy_many's copy streams (forked from the caller's stream, joined back)
+  static constexpr int kCopyStreams = 4;
+  cudaStream_t copy[kCopyStreams] = {};
+  cudaEvent_t copy_fork = nullptr, copy_join[kCopyStreams] = {};
+  std::mutex copy_mu;
 };
 std::mutex g_mu;
 DevInfo g_dev[128];
@@ -62,6 +67,11 @@ int device(DevInfo** out) {
       e = cudaStreamCreateWithFlags(&di.side, cudaStreamNonBlocking);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&di.fork, cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&di.join, cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&di.copy_fork, cudaEventDisableTiming);
+      for (int i = 0; i < DevInfo::kCopyStreams && e == cudaSuccess; ++i) {
+        e = cudaStreamCreateWithFlags(&di.copy[i], cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&di.copy_join[i], cudaEventDisableTiming);
+      }
       if (e != cudaSuccess) return fail(QLORA_ERR_CUDA, "side stream: %s", cudaGetErrorString(e));
     }
     di.ready = true;
@@ -851,6 +861,49 @@ int qlora_profile_reset(void) {
     g_prof_calls[i] = 0;
   }
   return QLORA_OK;
+}
+
+int qlora_copy_many(const qlora_copy* copies, int count, void* stream) {
+  if (count < 0 || (count > 0 && copies == nullptr)) return fail(QLORA_ERR_INVALID_ARGUMENT, "copy list");
+  for (int i = 0; i < count; ++i)
+    if (copies[i].bytes > 0 && (copies[i].dst == nullptr || copies[i].src == nullptr))
+      return fail(QLORA_ERR_INVALID_ARGUMENT, "copy %d: NULL pointer", i);
+  if (count == 0) return QLORA_OK;
+  DevInfo* di = nullptr;
+  int rc = device(&di);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  constexpr size_t kMinPiece = size_t(2) << 20;
+  constexpr int kN = DevInfo::kCopyStreams;
+  std::lock_guard<std::mutex> lk(di->copy_mu);
+  cudaError_t e = cudaEventRecord(di->copy_fork, s);
+  for (int i = 0; i < kN && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(di->copy[i], di->copy_fork, 0);
+  if (e != cudaSuccess) return cuda_ret(e, "fork to the copy streams");
+  int next = 0;
+  cudaError_t ec = cudaSuccess;
+  for (int i = 0; i < count && ec == cudaSuccess; ++i) {
+    const size_t bytes = copies[i].bytes;
+    if (bytes == 0) continue;
+    size_t pieces = bytes / kMinPiece;
+    if (pieces < 1) pieces = 1;
+    if (pieces > static_cast<size_t>(kN)) pieces = kN;
+    const size_t per = ((bytes + pieces - 1) / pieces + 15) & ~size_t(15);
+    for (size_t off = 0; off < bytes && ec == cudaSuccess; off += per) {
+      const size_t len = bytes - off < per ? bytes - off : per;
+      ec = cudaMemcpyAsync(static_cast<char*>(copies[i].dst) + off, static_cast<const char*>(copies[i].src) + off, len,
+                           cudaMemcpyDefault, di->copy[next]);
+      next = (next + 1) % kN;
+    }
+  }
+  // always join, so a stream capture never ends with the copy streams forked
+  cudaError_t ej = cudaSuccess;
+  for (int i = 0; i < kN; ++i) {
+    cudaError_t e1 = cudaEventRecord(di->copy_join[i], di->copy[i]);
+    if (e1 == cudaSuccess) e1 = cudaStreamWaitEvent(s, di->copy_join[i], 0);
+    if (ej == cudaSuccess) ej = e1;
+  }
+  if (ec != cudaSuccess) return cuda_ret(ec, "copy");
+  return cuda_ret(ej, "join the copy streams");
 }
 
 int qlora_device_sm_count(void) {

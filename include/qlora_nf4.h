@@ -394,6 +394,31 @@ int qlora_selftest_wait_timeout(uint64_t wait_ns, void* stream);
 /* Number of multiprocessors the kernels size their grids for (0 if no device). */
 int qlora_device_sm_count(void);
 
+/* ----------------------------------------------------------------- host <-> device copies */
+
+/*
+ * Moving a step's inputs and results between pinned host memory and the GPU.
+ * Not on the pages: plumbing for feeding the linears from the host.
+ *
+ * qlora_copy_many copies `count` byte ranges, in stream order on `stream`:
+ * each copy is cut into pieces of at least 2 MB, dealt round-robin over four
+ * internal copy streams forked from `stream` (one cudaMemcpyAsync per piece)
+ * and joined back before the call returns, so several copy engines share the
+ * host link (one stream moves about 30 GB/s host-to-device on a B300's PCIe 6
+ * x16 link, four about 50).  dst and src are any pointers the CUDA runtime
+ * can address (device memory, pinned or registered host memory; pageable host
+ * memory works but is not asynchronous); ranges must not overlap.  The caller
+ * owns every buffer.  count == 0 is a no-op.  Errors: INVALID_ARGUMENT (NULL
+ * list, or a NULL pointer with a non-zero size), CUDA (a copy could not be
+ * issued).  Works inside a stream capture (the fork and join become graph edges).
+ */
+typedef struct {
+  void* dst;
+  const void* src;
+  size_t bytes;
+} qlora_copy;
+int qlora_copy_many(const qlora_copy* copies, int count, void* stream);
+
 /* ----------------------------------------------------------------- tracing */
 
 /* Total number of kernels the entry points above have launched in this process. */
