@@ -44,11 +44,9 @@ struct WaParams {
   const float* mean;
   const __nv_bfloat16* lora_b;  // [N, r]
   __nv_bfloat16* y;             // [M, N]
-  float* partial;               // [splits][tiles][NTOK / 4 column groups][128 rows] float4 (split-K only)
-  unsigned* counters;           // [tiles]
   unsigned* status;
   int M, N, K, r;
-  int kb_per_split, splits, lora_blocks;
+  int kb_per_split, splits, lora_blocks;  // k split over `splits` CTAs of one cluster (the last adds LoRA)
   unsigned long long wait_ns;
 };
 
@@ -75,6 +73,17 @@ struct WaCfg {
   static_assert(NTOK % 16 == 0 && NTOK >= 16 && NTOK <= 256, "MMA N for M = 128");
 };
 
+// The token columns a producer team reads back from the accumulator: NTOK / 4 each, or all of
+// them for team 0 when that share would be under 16 (one 16-column TMEM load).
+template <int NTOK>
+__device__ __forceinline__ int wa_col_lo(int team) {
+  return (NTOK / kWaTeams) >= 16 ? team * (NTOK / kWaTeams) : 0;
+}
+template <int NTOK>
+__device__ __forceinline__ int wa_ncols(int team) {
+  return (NTOK / kWaTeams) >= 16 ? NTOK / kWaTeams : (team == 0 ? NTOK : 0);
+}
+
 template <int NTOK, int STAGES>
 __global__ void __launch_bounds__(kWaThreads, 1)
     k_qgemm_wa(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_st, const WaParams p) {
@@ -87,12 +96,11 @@ __global__ void __launch_bounds__(kWaThreads, 1)
   uint64_t* acc_full = empty + STAGES;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_full + 1);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
-  int* last_flag = abort_flag + 1;
   volatile int* vabort = abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // split = this CTA's rank in its cluster (clusters of `splits` CTAs along z)
   const int n0 = blockIdx.x * 128, tok0 = blockIdx.y * NTOK, split = blockIdx.z;
-  const int tile = blockIdx.x + gridDim.x * blockIdx.y;
   const int kb_total = p.K / 64;
   const int kb_begin = split * p.kb_per_split;
   const int kb_end = min(kb_total, kb_begin + p.kb_per_split);
@@ -106,7 +114,6 @@ __global__ void __launch_bounds__(kWaThreads, 1)
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
-    *last_flag = 0;
     fence_mbarrier_init();
   }
   if (warp == 0) {
@@ -117,6 +124,7 @@ __global__ void __launch_bounds__(kWaThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_holder;
+  bool prod_ok = false;  // producers: the accumulator holds this CTA's result
 
   if (warp == 0) {
     if (lane == 0) {
@@ -210,89 +218,95 @@ __global__ void __launch_bounds__(kWaThreads, 1)
     ok = ok && !*vabort;
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    // column share of this team: NTOK / kWaTeams columns (all of them for team 0 when NTOK is small)
-    constexpr int kShare = (NTOK / kWaTeams) >= 16 ? NTOK / kWaTeams : NTOK;
-    const int col_lo = (kShare == NTOK) ? 0 : team * kShare;
-    const int ncols = (kShare == NTOK) ? (team == 0 ? NTOK : 0) : kShare;
-    const uint32_t dcol = tbase + lane_field + Cfg::kDCol;
-    const int ncv = min(NTOK, p.M - tok0);  // columns that hold tokens
-    const int ntiles = gridDim.x * gridDim.y;
-    if (ok) {
-      if (p.splits == 1) {
-        for (int c = col_lo; c < col_lo + ncols && c < ncv; c += 16) {
-          uint32_t v[16];
-          __syncwarp();
-          tmem_ld_32x32b_x16(dcol + c, v);
-          tmem_ld_wait();
-          if (row_ok) {
+    prod_ok = ok;
+    if (ok && p.splits == 1) {
+      const uint32_t dcol = tbase + lane_field + Cfg::kDCol;
+      const int ncv = min(NTOK, p.M - tok0);  // columns that hold tokens
+      for (int c = wa_col_lo<NTOK>(team); c < wa_col_lo<NTOK>(team) + wa_ncols<NTOK>(team) && c < ncv; c += 16) {
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld_32x32b_x16(dcol + c, v);
+        tmem_ld_wait();
+        if (row_ok) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int tok = tok0 + c + j;
-              if (tok < p.M) p.y[static_cast<int64_t>(tok) * p.N + row] = __float2bfloat16_rn(__uint_as_float(v[j]));
-            }
+          for (int j = 0; j < 16; ++j) {
+            const int tok = tok0 + c + j;
+            if (tok < p.M) p.y[static_cast<int64_t>(tok) * p.N + row] = __float2bfloat16_rn(__uint_as_float(v[j]));
           }
-        }
-      } else {
-        // partial of this split: [column / 4][128 rows] float4, so a warp's store is 512 contiguous bytes
-        float4* part = reinterpret_cast<float4*>(p.partial) +
-                       (static_cast<int64_t>(split) * ntiles + tile) * (NTOK / 4) * 128 + quarter * 32 + lane;
-        for (int c = col_lo; c < col_lo + ncols && c < ncv; c += 16) {
-          uint32_t v[16];
-          __syncwarp();
-          tmem_ld_32x32b_x16(dcol + c, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 16; j += 4)
-            part[((c + j) >> 2) * 128] = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                                     __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
         }
       }
     }
-    if (p.splits > 1) {
-      __threadfence();
-      named_bar_sync(1, kWaTeams * 128);
-      if (threadIdx.x == 64) *last_flag = (atomicAdd(p.counters + tile, 1u) == static_cast<unsigned>(p.splits - 1));
-      named_bar_sync(1, kWaTeams * 128);
-      if (*reinterpret_cast<volatile int*>(last_flag)) {
-        __threadfence();
-        // the last split adds the partials in split order; all producer threads share the
-        // (4-column group, row) items
-        const int items = ((ncv + 3) >> 2) * 128;
-        const int64_t sstride = static_cast<int64_t>(ntiles) * (NTOK / 4) * 128;
-        const float4* src = reinterpret_cast<const float4*>(p.partial) + static_cast<int64_t>(tile) * (NTOK / 4) * 128;
-        constexpr int kRt = kWaTeams * 128;
-        for (int it0 = threadIdx.x - 64; it0 < items; it0 += 2 * kRt) {
-          // every split's loads of two items are issued before the first add
-          float4 v[kMaxSplitK][2];
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (p.splits > 1) {
+    // Split k: the accumulator's four TMEM lane quarters (32 weight rows each) are owned
+    // round-robin (quarter q by the CTA of cluster rank q % splits).  Each CTA sends the quarters
+    // it does not own, as float32 [token / 4][32 rows] float4 slices, into the owner's now idle
+    // stage buffers -- slot s (s - 1 past the owner) for sender s, laid out [owned quarter
+    // q / splits][token / 4][32 rows] -- and each owner adds the splits in split order and writes Y.
+    tc_fence_after();
+    cluster_sync();  // every CTA of the cluster is past its k loop: the stage buffers are free
+    const int ncv = min(NTOK, p.M - tok0);
+    const int team = (warp - 2) >> 2, quarter = warp & 3;
+    const int o = quarter % p.splits;
+    const uint32_t dcol = tbase + (static_cast<uint32_t>(quarter * 32) << 16) + Cfg::kDCol;
+    const uint32_t base = smem_u32(smem);
+    const uint32_t slot_bytes = static_cast<uint32_t>((4 + p.splits - 1) / p.splits) * (NTOK / 4) * 32 * 16;
+    const uint32_t lq_off = static_cast<uint32_t>(quarter / p.splits) * (NTOK / 4) * 32 * 16 + lane * 16;
+    const int c_lo = wa_col_lo<NTOK>(team), c_hi = c_lo + wa_ncols<NTOK>(team);
+    if (warp >= 2 && prod_ok && o != split) {
+      const uint32_t slot = static_cast<uint32_t>(split < o ? split : split - 1);
+      for (int c = c_lo; c < c_hi && c < ncv; c += 16) {
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld_32x32b_x16(dcol + c, v);
+        tmem_ld_wait();
 #pragma unroll
-          for (int sp = 0; sp < kMaxSplitK; ++sp)
+        for (int j = 0; j < 16; j += 4)
+          st_cluster_v4(base + slot * slot_bytes + lq_off + ((c + j) >> 2) * 512u, static_cast<uint32_t>(o),
+                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                    __uint_as_float(v[j + 3])));
+      }
+    }
+    cluster_sync();  // the slices have landed
+    if (warp >= 2 && prod_ok && o == split) {
+      const int row = n0 + quarter * 32 + lane;
+      for (int c = c_lo; c < c_hi && c < ncv; c += 16) {
+        uint32_t v[16];
+        __syncwarp();
+        tmem_ld_32x32b_x16(dcol + c, v);
+        tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 2; ++u)
-              v[sp][u] = sp < p.splits && it0 + u * kRt < items ? __ldcg(src + sp * sstride + it0 + u * kRt)
-                                                              : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            float4 acc = v[0][u];
-#pragma unroll
-            for (int sp = 1; sp < kMaxSplitK; ++sp) {
-              if (sp < p.splits) {
-                acc.x += v[sp][u].x;
-                acc.y += v[sp][u].y;
-                acc.z += v[sp][u].z;
-                acc.w += v[sp][u].w;
-              }
+        for (int j = 0; j < 16; j += 4) {
+          float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int sp = 0; sp < p.splits; ++sp) {
+            float4 x;
+            if (sp == split) {
+              x = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                              __uint_as_float(v[j + 3]));
+            } else {
+              const uint32_t slot = static_cast<uint32_t>(sp < split ? sp : sp - 1);
+              x = *reinterpret_cast<const float4*>(smem + slot * slot_bytes + lq_off + ((c + j) >> 2) * 512u);
             }
-            const int it = it0 + u * kRt;
-            const int orow = n0 + (it & 127), otok = tok0 + (it >> 7) * 4;
-            if (it < items && orow < p.N) {
-              const float f[4] = {acc.x, acc.y, acc.z, acc.w};
+            if (sp == 0) {
+              sum = x;
+            } else {
+              sum.x += x.x;
+              sum.y += x.y;
+              sum.z += x.z;
+              sum.w += x.w;
+            }
+          }
+          if (row < p.N) {
+            const float f[4] = {sum.x, sum.y, sum.z, sum.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (otok + e < p.M) p.y[static_cast<int64_t>(otok + e) * p.N + orow] = __float2bfloat16_rn(f[e]);
+            for (int e = 0; e < 4; ++e) {
+              const int tok = tok0 + c + j + e;
+              if (tok < p.M) p.y[static_cast<int64_t>(tok) * p.N + row] = __float2bfloat16_rn(f[e]);
             }
           }
         }
-        if (threadIdx.x == 64) p.counters[tile] = 0;
       }
     }
   }
@@ -870,8 +884,8 @@ static FwdPlan plan_fwd(int M, int N, int K, int num_sms) {
   pl.tok_tiles = (M + pl.ntok - 1) / pl.ntok;
   const int tiles = pl.row_tiles * pl.tok_tiles;
   const int kb_total = K / 64;
-  // split k while the grid still fits one wave (one 576-thread CTA per SM); the last CTA of a
-  // tile adds the partials, so more than 4 splits costs more in that sum than it saves
+  // split k while the grid still fits one wave (one 576-thread CTA per SM); the splits of a tile
+  // form one cluster and add their partials through distributed shared memory
   int splits = num_sms / tiles;
   if (splits > kMaxSplitK) splits = kMaxSplitK;
   if (splits > kb_total) splits = kb_total;
@@ -909,11 +923,8 @@ size_t bwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
 }
 
 size_t fwd_gemm_workspace_bytes(int M, int N, int K, int num_sms) {
-  if (use_pair_gemm(M)) return 0;
-  const FwdPlan pl = plan_fwd(M, N, K, num_sms);
-  if (pl.splits == 1) return 0;
-  const size_t tiles = static_cast<size_t>(pl.row_tiles) * pl.tok_tiles;
-  return pl.splits * tiles * 128 * pl.ntok * sizeof(float) + tiles * 4 + 256;
+  (void)M, (void)N, (void)K, (void)num_sms;
+  return 0;  // split k adds its partials inside a cluster
 }
 
 // Launch with programmatic stream serialization: the kernel may start while the
@@ -955,7 +966,8 @@ static cudaError_t run_wa(const CUtensorMap& tx, const CUtensorMap& tst, const W
   using Cfg = WaCfg<NTOK, STAGES>;
   cudaError_t e = set_smem_limit_once(k_qgemm_wa<NTOK, STAGES>, Cfg::kSmem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(k_qgemm_wa<NTOK, STAGES>, grid, dim3(kWaThreads), Cfg::kSmem, s, 1, tx, tst, prm);
+  e = launch_pdl_z(k_qgemm_wa<NTOK, STAGES>, grid, dim3(kWaThreads), Cfg::kSmem, s, 1, static_cast<int>(grid.z), tx,
+                   tst, prm);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -977,8 +989,6 @@ cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, cons
   prm.mean = w.mean;
   prm.lora_b = lora_b;
   prm.y = y;
-  prm.partial = nullptr;
-  prm.counters = nullptr;
   prm.status = status;
   prm.M = M;
   prm.N = N;
@@ -988,14 +998,8 @@ cudaError_t launch_fwd_gemm(const __nv_bfloat16* x, int M, const Nf4Dev& w, cons
   prm.splits = pl.splits;
   prm.lora_blocks = (r + 63) / 64;
   prm.wait_ns = wait_ns;
-  if (pl.splits > 1) {
-    const size_t tiles = static_cast<size_t>(pl.row_tiles) * pl.tok_tiles;
-    prm.partial = static_cast<float*>(ws);
-    prm.counters = reinterpret_cast<unsigned*>(prm.partial + pl.splits * tiles * 128 * pl.ntok);
-    const cudaError_t e = cudaMemsetAsync(prm.counters, 0, tiles * 4, s);
-    if (e != cudaSuccess) return e;
-  }
-  const dim3 grid(pl.row_tiles, pl.tok_tiles, pl.splits);
+  (void)ws;
+  const dim3 grid(pl.row_tiles, pl.tok_tiles, pl.splits);  // the splits of a tile form one cluster
   if (pl.ntok == 16) return run_wa<16, 4>(tx, tst, prm, grid, s);
   if (pl.ntok == 64) return run_wa<64, 4>(tx, tst, prm, grid, s);
   if (pl.ntok == 128) return run_wa<128, 4>(tx, tst, prm, grid, s);
