@@ -357,7 +357,8 @@ def dequant_quant_rates(q, torch, flush, n=22016, k=8192):
 
 
 def mlp_block(q, torch, steps, flush, hidden=4096, inter=11008, m=2048, r=16, alpha=32.0):
-    """Llama-7B MLP block fwd+bwd: gate/up [inter, hidden], down [hidden, inter], SiLU*up between."""
+    """Llama-7B MLP block fwd+bwd: gate/up [inter, hidden], down [hidden, inter], SiLU*up between
+    (the gate and up forwards on two streams)."""
     import synthetic
     dev = "cuda"
     recs = [q.quantize(synthetic.weight(n, k, device=dev, seed=s)) for (n, k, s) in
@@ -374,10 +375,18 @@ def mlp_block(q, torch, steps, flush, hidden=4096, inter=11008, m=2048, r=16, al
     dbs = [torch.empty((rec.n, r), dtype=torch.float32, device=dev) for rec in recs]
     wsf = torch.empty(max(q.fwd_workspace_bytes(m, rec.n, rec.k, r) for rec in recs) + 256, dtype=torch.uint8, device=dev)
     wsb = torch.empty(max(q.bwd_workspace_bytes(m, rec.n, rec.k, r) for rec in recs) + 256, dtype=torch.uint8, device=dev)
+    # gate and up read the same X and are independent: the up forward runs on a second stream
+    # (its own workspace), so its CTAs take the SMs the gate GEMM's last partial wave leaves idle
+    s_up = torch.cuda.Stream()
+    wsf_up = torch.empty_like(wsf)
 
     def fwd_bwd():
+        main = torch.cuda.current_stream()
+        s_up.wait_stream(main)
         q.linear_fwd(x, recs[0], *loras[0], alpha, y=g, t_save=ts[0], workspace=wsf)
-        q.linear_fwd(x, recs[1], *loras[1], alpha, y=u, t_save=ts[1], workspace=wsf)
+        with torch.cuda.stream(s_up):
+            q.linear_fwd(x, recs[1], *loras[1], alpha, y=u, t_save=ts[1], workspace=wsf_up)
+        main.wait_stream(s_up)
         q.silu_mul_fwd(g, u, h)
         q.linear_fwd(h, recs[2], *loras[2], alpha, y=yv, t_save=ts[2], workspace=wsf)
         q.linear_bwd(dy, h, recs[2], *loras[2], alpha, ts[2], dx=dh, da=das[2], db=dbs[2], workspace=wsb)
