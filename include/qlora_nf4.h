@@ -24,7 +24,11 @@
  *   - bfloat16 tensors are passed as uint16_t* (raw bf16 bits).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *     Calls are asynchronous on that stream and never synchronise the host,
- *     except qlora_get_status.
+ *     except qlora_get_status.  Calls on different streams may run at the same
+ *     time when they use distinct workspaces and outputs (e.g. the gate and up
+ *     forwards of an MLP block); the backward calls of a device share one
+ *     internal stream for their dA / dB kernel, so those kernels of concurrent
+ *     backward calls run one after the other.
  *   - Argument errors are returned synchronously, before anything is launched.
  *     Errors found on the device (a bounded wait that expired, a non-finite
  *     weight) are latched in a per-device status word and returned by
