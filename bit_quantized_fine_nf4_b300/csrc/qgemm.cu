@@ -15,13 +15,15 @@
 //               one 64-wide k block = one absmax block = 32 TMEM columns);
 //   B operand = NTOK token rows of X (then of sT = bf16(s X A^T)), TMA, 128B swizzle.
 //   The LoRA up-projection is one (or two, r > 64) extra k blocks of the same
-//   accumulator.  Optional split-K with a fixed-order reduction (decode shapes).
+//   accumulator.  Few tiles: k split over the CTAs of a cluster, whose results
+//   are added in split order through distributed shared memory.
 // k_qgemm_wb  (backward dX)
 //   D[m, k] = sum_n dY[m, n] deq(W)[n, k]  +  sum_j sU[m, j] A[j, k]
 //   A operand = 2 x 128 token rows of dY (then sU = bf16(s dY B)), TMA, two
 //               accumulators sharing each dequantised B block;
 //   B operand = deq(W)[n-block of 64, 256 output columns], MN-major 128B swizzle,
 //               written by the producers with st.shared (then LoRA A rows, TMA).
+//   Few tiles: n split over the CTAs of a cluster, added as in k_qgemm_wa.
 // k_lora_grad (LoRA gradients, both MN-major operands, HBM-bound)
 //   dA^T[k, j] = sum_m X[m, k] sU[m, j],   dB[n, j] = sum_m dY[m, n] sT[m, j].
 #include <cudaTypedefs.h>
