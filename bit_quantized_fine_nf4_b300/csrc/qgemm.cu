@@ -53,7 +53,9 @@ struct WaParams {
 };
 
 constexpr int kWaTeams = 4;      // producer teams (4 warps each) taking k blocks round-robin
-constexpr int kMaxSplitK = 4;    // split-K / split-n ways of the small-token GEMMs
+// split ways of the small-token GEMMs: clusters of up to 4 CTAs (one per SM); clusters of 8
+// measured slower -- they need 8 free SMs of one GPC at once beside the other kernels
+constexpr int kMaxSplitK = 4;
 
 // 16-byte store into the shared memory of CTA `rank` of the cluster, at the offset `local` has here.
 __device__ __forceinline__ void st_cluster_v4(uint32_t local, uint32_t rank, float4 v) {
@@ -540,7 +542,8 @@ __global__ void __launch_bounds__(kWbThreads, 1)
     // of cluster rank c % splits).  Each CTA sends every chunk it does not own, as float32 values of
     // both accumulators, to the owner's now idle stage buffers -- slot s (s - 1 past the owner) for
     // sender s, laid out [owned chunk c / splits][accumulator][8 groups of 4 columns][128 rows]
-    // float4 -- and each owner adds the splits' values in split order and writes dX.
+    // float4, over the accumulators that hold tokens -- and each owner adds the splits' values in
+    // split order and writes dX.
     tc_fence_after();
     cluster_sync();  // every CTA of the cluster is past its k loop: the stage buffers are free
     const int ntok = min(256, p.M - tok0);
@@ -548,7 +551,8 @@ __global__ void __launch_bounds__(kWbThreads, 1)
     const int row = quarter * 32 + lane;
     const uint32_t lane_field = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t base = smem_u32(smem);
-    const uint32_t slot_bytes = static_cast<uint32_t>((8 + p.splits - 1) / p.splits) * (2 * 8 * 128 * 16);
+    const int nacc = ntok > 128 ? 2 : 1;  // accumulators holding tokens
+    const uint32_t slot_bytes = static_cast<uint32_t>((8 + p.splits - 1) / p.splits * nacc) * (8 * 128 * 16);
     // unit u = (accumulator u >> 3, chunk u & 7); a warp takes the units u = wq (mod 4)
     auto unit_kept = [&](int acc, int cc) { return acc * 128 < ntok && k0 + 32 * cc < p.K; };
     if (warp >= 2 && prod_ok) {
@@ -560,7 +564,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
         tmem_ld_32x32b_x32(tbase + lane_field + acc * 256 + 32 * cc, v);
         tmem_ld_wait();
         const uint32_t slot = static_cast<uint32_t>(split < o ? split : split - 1);
-        const uint32_t at = base + slot * slot_bytes + static_cast<uint32_t>(((cc / p.splits) * 2 + acc) * 8) * 2048u +
+        const uint32_t at = base + slot * slot_bytes + static_cast<uint32_t>(((cc / p.splits) * nacc + acc) * 8) * 2048u +
                             static_cast<uint32_t>(row) * 16u;
 #pragma unroll
         for (int q = 0; q < 8; ++q)
@@ -580,7 +584,7 @@ __global__ void __launch_bounds__(kWbThreads, 1)
         tmem_ld_wait();
         const int tl = acc * 128 + row;
         if (tl >= ntok) continue;
-        const uint32_t in_slot = static_cast<uint32_t>(((cc / p.splits) * 2 + acc) * 8) * 2048u +
+        const uint32_t in_slot = static_cast<uint32_t>(((cc / p.splits) * nacc + acc) * 8) * 2048u +
                                  static_cast<uint32_t>(row) * 16u;
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {  // 8 columns per 16-byte store
@@ -902,7 +906,7 @@ struct BwdPlan {
 };
 
 // Backward dX: 256-column x 256-token tiles; with few tiles (small token counts) the n blocks of
-// a tile are split over up to 4 CTAs while the grid fits one wave, the last CTA adding the partials.
+// a tile are split over up to 4 CTAs of a cluster while the grid fits one wave.
 static BwdPlan plan_bwd(int M, int N, int K, int num_sms) {
   BwdPlan pl;
   if (M < 1) M = 1;
