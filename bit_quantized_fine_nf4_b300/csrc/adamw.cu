@@ -48,6 +48,8 @@ __device__ __forceinline__ void adamw_one(const AwParams& p, float& master, floa
 }
 
 __global__ void __launch_bounds__(kAwThreads) k_adamw(const __grid_constant__ AwParams p) {
+  griddep_launch_dependents();
+  griddep_wait();  // launched early: the gradients come from the preceding kernels
   const int64_t total = p.item0[p.count];
   for (int64_t item = blockIdx.x; item < total; item += gridDim.x) {
     int lo = 0, hi = p.count - 1;  // tensor of this item
@@ -142,8 +144,8 @@ cudaError_t launch_adamw(const AdamwTensor* tensors, int count, const AdamwHyper
     p.eps = h.eps;
     if (items == 0) continue;
     const int64_t grid = items < 4LL * num_sms ? items : 4LL * num_sms;
-    k_adamw<<<static_cast<unsigned>(grid), kAwThreads, 0, s>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl_plain(k_adamw, dim3(static_cast<unsigned>(grid)), dim3(kAwThreads), 0, s, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
