@@ -48,8 +48,8 @@ __device__ __forceinline__ void adamw_one(const AwParams& p, float& master, floa
 }
 
 __global__ void __launch_bounds__(kAwThreads) k_adamw(const __grid_constant__ AwParams p) {
-  griddep_launch_dependents();
   griddep_wait();  // launched early: the gradients come from the preceding kernels
+  griddep_launch_dependents();
   const int64_t total = p.item0[p.count];
   for (int64_t item = blockIdx.x; item < total; item += gridDim.x) {
     int lo = 0, hi = p.count - 1;  // tensor of this item

@@ -104,6 +104,11 @@ __device__ __forceinline__ void abort_cta(unsigned* status, int* abort_flag) {
 }
 
 // ------------------------------------------------------------------ programmatic dependent launch
+// Every kernel here keeps two rules, which together order a chain of such launches:
+//  * it calls griddep_launch_dependents only after its own griddep_wait has returned, so when the
+//    next kernel starts, every kernel before this one has completed;
+//  * before its griddep_wait it reads nothing the immediately preceding kernel writes (only data
+//    of earlier kernels, the frozen NF4 record, or its own parameters) and writes nothing.
 // Let the next kernel in the stream start launching now (it still has to wait
 // with griddep_wait before it reads anything this grid writes).
 __device__ __forceinline__ void griddep_launch_dependents() {

@@ -35,8 +35,8 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 
 __global__ void __launch_bounds__(256) k_dropout_mask(uint32_t* __restrict__ mask, int64_t n_words, uint64_t seed,
                                                       uint64_t offset, uint32_t threshold) {
-  griddep_launch_dependents();
   griddep_wait();  // launched early: the previous mask may still be read by the preceding kernels
+  griddep_launch_dependents();
   const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
   const uint32_t o0 = static_cast<uint32_t>(offset), o1 = static_cast<uint32_t>(offset >> 32);
   for (int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; w < n_words;
@@ -59,8 +59,8 @@ __global__ void __launch_bounds__(256) k_dropout_mask(uint32_t* __restrict__ mas
 // x_drop[e] = keep(e) ? x[e] : 0 (bf16, exact); 8 elements (one mask byte) per thread step.
 __global__ void __launch_bounds__(256) k_dropout_apply(const uint4* __restrict__ x, const uint8_t* __restrict__ mask,
                                                        uint4* __restrict__ x_drop, int64_t n8) {
-  griddep_launch_dependents();
   griddep_wait();  // launched early: x and the mask come from the preceding kernels
+  griddep_launch_dependents();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint4 v = x[i];

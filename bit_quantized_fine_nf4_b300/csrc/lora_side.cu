@@ -53,7 +53,6 @@ __global__ void __launch_bounds__(kSideThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
   volatile int* vabort = abort_flag;
 
-  griddep_launch_dependents();  // the GEMM that follows needs sT only for its last k block
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tiles = (p.M + 127) / 128;
   const int n1 = p.K / 64;
@@ -86,6 +85,9 @@ __global__ void __launch_bounds__(kSideThreads, 1)
   // launched early (programmatic dependent launch): the set-up above overlaps the preceding kernel;
   // its input rows and the outputs may belong to the preceding kernels of the stream
   griddep_wait();
+  // the GEMM that follows needs sT / sU only for its last k block; it may start now, since every
+  // kernel before this one has completed
+  griddep_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {

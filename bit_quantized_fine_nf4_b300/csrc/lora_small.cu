@@ -73,7 +73,11 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
   extern __shared__ float s_red[];  // [W warps][16 rows][RP], then (STAGED) mt as [RP][K + 8] bf16
   unsigned short* s_mt = reinterpret_cast<unsigned short*>(s_red + W * 16 * RP);
   const int mt_pitch = K + 8;
-  // the GEMM that consumes this kernel's output only needs it for its last k block
+  // launched early (programmatic dependent launch): `in`, the LoRA matrix (an optimiser step may
+  // have just written it), t_save and the outputs may belong to the preceding kernels of the stream
+  griddep_wait();
+  // the GEMM that consumes this kernel's output only needs it for its last k block; it may start
+  // now, since every kernel before this one has completed
   griddep_launch_dependents();
   if (STAGED) {
     if (MT_KMAJOR) {
@@ -107,9 +111,6 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
     }
     __syncthreads();
   }
-  // launched early (programmatic dependent launch): `in`, t_save and the outputs may belong to the
-  // preceding kernels of the stream (the LoRA matrix staged above does not)
-  griddep_wait();
   const int rk = (r + 7) & ~7;
   if (cvt_rows > 0) {
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -193,8 +194,8 @@ __device__ __forceinline__ float sigmoidf_(float g) { return 1.0f / (1.0f + expf
 
 __global__ void __launch_bounds__(256) k_silu_mul_fwd(const uint32_t* __restrict__ g, const uint32_t* __restrict__ u,
                                                       uint32_t* __restrict__ h, int64_t n2) {
-  griddep_launch_dependents();
   griddep_wait();  // launched early: g and u come from the preceding kernels
+  griddep_launch_dependents();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n2;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint32_t gw = g[i], uw = u[i];
@@ -211,8 +212,8 @@ __global__ void __launch_bounds__(256) k_silu_mul_fwd(const uint32_t* __restrict
 __global__ void __launch_bounds__(256) k_silu_mul_bwd(const uint32_t* __restrict__ dh, const uint32_t* __restrict__ g,
                                                       const uint32_t* __restrict__ u, uint32_t* __restrict__ dg,
                                                       uint32_t* __restrict__ du, int64_t n2) {
-  griddep_launch_dependents();
   griddep_wait();  // launched early: dh comes from the preceding kernels
+  griddep_launch_dependents();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n2;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const uint32_t dw = dh[i], gw = g[i], uw = u[i];
@@ -243,8 +244,8 @@ __global__ void __launch_bounds__(256) k_transpose_kr(const unsigned short* __re
                                                       const float* __restrict__ cvt_src,
                                                       __nv_bfloat16* __restrict__ cvt_dst, int64_t cvt_rows,
                                                       float cvt_scale, unsigned* __restrict__ zero, int zero_words) {
-  griddep_launch_dependents();
   griddep_wait();  // launched early: the workspace it writes may be in use by the preceding kernels
+  griddep_launch_dependents();
   const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < zero_words; i += nthreads) zero[i] = 0u;
   const int64_t total = static_cast<int64_t>(K / 8) * r;

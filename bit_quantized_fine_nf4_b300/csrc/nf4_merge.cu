@@ -88,8 +88,8 @@ __device__ __forceinline__ void deq8(const Nf4Raw8& raw, const float* s_lv, floa
 // ROWS rows x 8 columns per lane; a CTA of 8 warps covers 8 * ROWS rows x 256 columns.
 template <int BASE, bool SUB_NF4, bool OUT_BF16, bool MASKED, int ROWS>
 __global__ void __launch_bounds__(kMgThreads, 2) k_lowrank_combine(const MgParams p) {
-  griddep_launch_dependents();
   griddep_wait();  // launched early: dX (in place) and the LoRA matrices may come from the preceding kernels
+  griddep_launch_dependents();
   constexpr int kRows = 8 * ROWS;           // rows of the CTA tile
   extern __shared__ float s_mg[];
   float* s_a = s_mg;                        // [r][256]

@@ -620,6 +620,11 @@ __global__ void __launch_bounds__(256) k_absmax_dq(const float* __restrict__ abs
         if (i0 + i < n_a) q[i0 + i] = static_cast<int8_t>((packed[i >> 2] >> ((i & 3) * 8)) & 0xffu);
     }
   }
+  // The record is complete once this grid has exited.  A kernel launched after it with programmatic
+  // dependent launch may start when the last CTA exits and read the record before its own
+  // griddepcontrol.wait (the decode kernel stages weights that early), so every thread makes its
+  // stores performed device-wide before it exits.
+  __threadfence();
 }
 
 // ------------------------------------------------------------------ dequantise

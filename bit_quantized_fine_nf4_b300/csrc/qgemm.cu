@@ -684,7 +684,6 @@ __global__ void __launch_bounds__(kLgThreads, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
   volatile int* vabort = abort_flag;
 
-  griddep_launch_dependents();  // the dX GEMM that follows needs nothing from this kernel until its end
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_iter = (p.M + 63) / 64;
 
@@ -712,6 +711,8 @@ __global__ void __launch_bounds__(kLgThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       griddep_wait();  // sU and sT come from the preceding kernel
+      // the kernels that follow may start launching now (every kernel before this one has completed)
+      griddep_launch_dependents();
       tma_prefetch_desc(&tm_x);
       tma_prefetch_desc(&tm_dy);
       int g = 0;

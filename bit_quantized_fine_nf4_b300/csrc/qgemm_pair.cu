@@ -197,6 +197,9 @@ __global__ void __launch_bounds__(kPrThreads, 1)
           tm = &tm_low;
           kc = (i - n_main) * 64;
         }
+        // no LoRA k steps: still wait for the preceding kernel, before the last stage so that the
+        // epilogue (which lets the next kernel launch) runs only after the wait has returned
+        if (p.lora_blocks == 0 && i == n_iter - 1) griddep_wait();
         if (rank == 0) {
           mbar_arrive_expect_tx(&full[s], 2 * kPrActBytes);  // both CTAs' boxes
           tma_load_2d(st, tm, &full[s], kc, ta);
@@ -207,9 +210,7 @@ __global__ void __launch_bounds__(kPrThreads, 1)
           tma_load_2d_to_pair_bar(st + kPrBox, tm, bar, kc, tb);
         }
       }
-      // no LoRA k steps: still wait once for the preceding kernel, so this grid never completes
-      // before it does (later kernels of the stream rely on that order)
-      if (p.lora_blocks == 0) griddep_wait();
+      griddep_wait();  // returns at once after the waits above; covers a loop ended by an abort
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
