@@ -153,11 +153,17 @@ FwdWs fwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
 
 // The forward's LoRA down-projection runs as the tiled TMA kernel beside the CTA-pair GEMM.
 bool use_side(int64_t m, int r) { return qlora::use_pair_gemm(static_cast<int>(m)) && qlora::lora_side_supported(r); }
-// The backward's U = dY B runs there too, on a k-major copy of B (the TMA kernel walks k in 64-wide
-// boxes), where the fragment-gathering kernel is slow: wide r, long n, or few tokens (measured: the
-// 4096^2 projection at 2048 tokens and r = 16 is faster on k_lora_down, 12 against 16 us).
-bool use_side_bwd(int64_t m, int64_t n, int r) {
-  return qlora::lora_side_supported(r) && n % 64 == 0 && (r > 16 || n > 4096 || m <= 256);
+// The backward's U = dY B, by shape:
+//  * r <= 16 and more than 256 tokens in at most a wave of 64-row blocks: k_lora_down_ks, k split
+//    over a cluster (each CTA stages only its slice of B, 128 KB of dY in flight per CTA);
+//  * wide r, long n or few tokens: the TMA kernel beside the GEMMs, on a k-major copy of B;
+//  * otherwise k_lora_down (persistent over 16-row tiles, B staged once per CTA).
+enum UPath { U_KS, U_SIDE, U_DOWN };
+UPath u_path(int64_t m, int64_t n, int r, int sms) {
+  int splits = 0, cps = 0;
+  if (m > 256 && qlora::lora_down_ks_plan(static_cast<int>(m), static_cast<int>(n), r, sms, &splits, &cps)) return U_KS;
+  if (qlora::lora_side_supported(r) && n % 64 == 0 && (r > 16 || n > 4096 || m <= 256)) return U_SIDE;
+  return U_DOWN;
 }
 
 struct BwdWs {
@@ -172,7 +178,7 @@ BwdWs bwd_ws(int64_t m, int64_t n, int64_t k, int r, int sms) {
   w.su = lora_operand_bytes(m, r);
   w.st = w.su;
   w.ld = align256(qlora::lora_down_workspace_bytes(static_cast<int>(m), static_cast<int>(n), r, sms));
-  if (use_side_bwd(m, n, r)) {
+  if (u_path(m, n, r, sms) == U_SIDE) {
     // B^T [r, n], then the split-k partials and counters of U = dY B
     const size_t bt = align256(static_cast<size_t>(r) * n * 2) +
                       align256(qlora::lora_side_bwd_workspace_bytes(static_cast<int>(m), static_cast<int>(n), r, sms));
@@ -597,7 +603,8 @@ static int linear_bwd_impl(const uint16_t* dy, const uint16_t* x, int64_t m, con
   // and, forked onto the side stream after U, the dA / dB kernel on the SMs the
   // GEMM leaves idle; the caller's stream waits for the side stream before the
   // call returns.
-  if (use_side_bwd(M, N, r)) {
+  const UPath up = u_path(M, N, r, di->num_sms);
+  if (up == U_SIDE) {
     // B^T (a k-major copy of B) and, in the same launch, sT = bf16(s * t_save) and U's split
     // counters cleared; then U = dY B by the TMA kernel with k split over the SMs (the dX GEMM
     // launches as U's CTAs finish and waits for sU only before its LoRA k block)
@@ -613,6 +620,11 @@ static int linear_bwd_impl(const uint16_t* dy, const uint16_t* x, int64_t m, con
       Span sp(P_LORA_SIDE_BWD, s, 1);
       e = qlora::launch_lora_side_bwd(dyb, bt, M, N, r, scale, su, uws, di->num_sms, di->status, wait, s);
     }
+  } else if (up == U_KS) {
+    // U = dY B (B read as stored), k split over clusters, and in the same launch sT = bf16(s * t_save)
+    Span sp(P_LORA_DOWN, s, 1);
+    e = qlora::launch_lora_down_ks(dyb, reinterpret_cast<const __nv_bfloat16*>(lora_b), 0, M, N, r, scale, nullptr,
+                                   su, di->num_sms, s, t_save, st, static_cast<int64_t>(M), scale);
   } else {
     // U = dY B (B read as stored) on all SMs and, in the same launch, sT = bf16(s * t_save)
     Span sp(P_LORA_DOWN, s, 1);

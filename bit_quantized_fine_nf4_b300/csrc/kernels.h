@@ -45,6 +45,13 @@ cudaError_t launch_lora_down(const __nv_bfloat16* in, const __nv_bfloat16* mt, i
                              float scale, float* out_f32, __nv_bfloat16* out_bf16, void* ws, int max_ctas,
                              cudaStream_t s, const float* cvt_src = nullptr, __nv_bfloat16* cvt_dst = nullptr,
                              int64_t cvt_rows = 0, float cvt_scale = 1.0f, float t_scale = 1.0f);
+// The same product for r <= 16 with k split over a cluster of up to 4 CTAs per 64-row block (one
+// wave of row blocks at most); lora_down_ks_plan says whether a shape takes it and its split.
+bool lora_down_ks_plan(int M, int K, int r, int num_sms, int* splits, int* chunks_per_split);
+cudaError_t launch_lora_down_ks(const __nv_bfloat16* in, const __nv_bfloat16* mt, int mt_kmajor, int M, int K, int r,
+                                float scale, float* out_f32, __nv_bfloat16* out_bf16, int num_sms, cudaStream_t s,
+                                const float* cvt_src = nullptr, __nv_bfloat16* cvt_dst = nullptr,
+                                int64_t cvt_rows = 0, float cvt_scale = 1.0f, float t_scale = 1.0f);
 cudaError_t launch_silu_mul_fwd(const uint16_t* g, const uint16_t* u, uint16_t* h, int64_t n, int num_sms,
                                 cudaStream_t s);
 cudaError_t launch_silu_mul_bwd(const uint16_t* dh, const uint16_t* g, const uint16_t* u, uint16_t* dg, uint16_t* du,

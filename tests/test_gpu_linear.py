@@ -214,6 +214,16 @@ def test_pair_tiles_ragged(lib, m, n, k, r):
     _check_all(lib, case)
 
 
+# U = dY B of the backward with k split over a cluster of up to four CTAs per 64-row block: four
+# shares with a ragged k (n = 1000 ends inside a 32-wide chunk), two shares (65 row blocks), one
+# share (141 row blocks, the whole of B staged per CTA) and, past a wave of row blocks, the
+# persistent kernel over 16-row tiles.
+@pytest.mark.parametrize("m,n,k,r", [(700, 1000, 256, 16), (4100, 512, 256, 8), (9000, 264, 128, 16),
+                                     (9500, 256, 128, 12)])
+def test_u_split_over_cluster(lib, m, n, k, r):
+    _check_all(lib, synthetic.linear_case(n, k, m, r, 2.0 * r, base_seed=m + n + k + r))
+
+
 def test_pair_accumulate_flags(lib):
     _accumulate_against_oracle(lib, synthetic.linear_case(384, 320, 520, 16, 32.0, base_seed=21))
 
