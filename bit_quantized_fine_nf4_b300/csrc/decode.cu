@@ -132,20 +132,12 @@ __device__ __forceinline__ uint4 ldg_nc_v4_if(const void* p, bool on) {
   return v;
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
 // 4-byte cp.async issued only when `on` (predicated in the instruction; src-size 0 zero-fills)
 __device__ __forceinline__ void cp_async4_if(uint32_t dst, const void* src, bool valid, bool on) {
   asm volatile(
       "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %3, 0;\n\t@q cp.async.ca.shared.global [%0], [%1], 4, %2;\n\t}" ::"r"(dst),
       "l"(src), "r"(valid ? 4 : 0), "r"(static_cast<int>(on))
       : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_l2_line(const void* p) {

@@ -91,19 +91,36 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
     } else {
       // mt[k][j] -> s_mt[j][k]; one thread per (k, 8 j)
       const int jg = RP / 8;
-      for (int i = threadIdx.x; i < K * jg; i += W * 32) {
-        const int k = i / jg, j0 = (i - k * jg) * 8;
-        const unsigned short* src = reinterpret_cast<const unsigned short*>(mt) + static_cast<int64_t>(k) * r;
-        if ((r & 7) == 0) {  // rows of mt start on 16-byte boundaries
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (j0 < r) v = *reinterpret_cast<const uint4*>(src + j0);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const int total = K * jg;
+      if ((r & 7) == 0) {
+        // rows of mt start on 16-byte boundaries: 16-byte loads, eight in flight per thread
+        for (int i0 = threadIdx.x; i0 < total; i0 += 8 * W * 32) {
+          uint4 v[8];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            s_mt[(j0 + 2 * e) * mt_pitch + k] = static_cast<unsigned short>(w[e] & 0xffffu);
-            s_mt[(j0 + 2 * e + 1) * mt_pitch + k] = static_cast<unsigned short>(w[e] >> 16);
+          for (int b = 0; b < 8; ++b) {
+            const int i = i0 + b * W * 32;
+            const int k = i / jg, j0 = (i - k * jg) * 8;
+            v[b] = (i < total && j0 < r)
+                       ? ldg_nc_v4(reinterpret_cast<const unsigned short*>(mt) + static_cast<int64_t>(k) * r + j0)
+                       : make_uint4(0, 0, 0, 0);
           }
-        } else {
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const int i = i0 + b * W * 32;
+            if (i >= total) break;
+            const int k = i / jg, j0 = (i - k * jg) * 8;
+            const uint32_t w[4] = {v[b].x, v[b].y, v[b].z, v[b].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              s_mt[(j0 + 2 * e) * mt_pitch + k] = static_cast<unsigned short>(w[e] & 0xffffu);
+              s_mt[(j0 + 2 * e + 1) * mt_pitch + k] = static_cast<unsigned short>(w[e] >> 16);
+            }
+          }
+        }
+      } else {
+        for (int i = threadIdx.x; i < total; i += W * 32) {
+          const int k = i / jg, j0 = (i - k * jg) * 8;
+          const unsigned short* src = reinterpret_cast<const unsigned short*>(mt) + static_cast<int64_t>(k) * r;
 #pragma unroll
           for (int e = 0; e < 8; ++e) s_mt[(j0 + e) * mt_pitch + k] = j0 + e < r ? src[j0 + e] : 0;
         }
@@ -126,7 +143,10 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
   const int n_chunks = (K + 31) / 32;  // K % 8 == 0: a thread's 8-wide slice is fully inside K or past it
   const int tiles = (M + 15) / 16;
   const uint4 zero = make_uint4(0, 0, 0, 0);
-  constexpr int UNROLL = (NT <= 2 && (MT_KMAJOR || STAGED)) ? 4 : 2;
+  // staged: the LoRA fragments come from shared memory as the MMAs need them, so eight chunks of
+  // `in` (128 KB per CTA) can be in flight; unstaged: fragments are loaded with the chunk
+  constexpr int UNROLL = (NT <= 2 && STAGED) ? 8 : (NT <= 2 && MT_KMAJOR) ? 4 : 2;
+  constexpr int BV = STAGED ? 1 : UNROLL;
   for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
     const int m0 = tile * 16;
     const int rowa = m0 + g, rowb = m0 + g + 8;
@@ -136,28 +156,34 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
 #pragma unroll
     for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
     for (int c = warp; c < n_chunks; c += UNROLL * W) {
-      uint4 xa[UNROLL], xb[UNROLL], bv[UNROLL][NT];
+      uint4 xa[UNROLL], xb[UNROLL], bv[BV][NT];
 #pragma unroll
       for (int u = 0; u < UNROLL; ++u) {
         const int kb = (c + u * W) * 32 + q * 8;
         const bool kin = kb < K;
         xa[u] = (kin && rowa < M) ? ldg_nc_v4(ina + kb) : zero;
         xb[u] = (kin && rowb < M) ? ldg_nc_v4(inb + kb) : zero;
+        if (!STAGED) {
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          const int j = t * 8 + g;
-          if (STAGED)
-            bv[u][t] = kin ? *reinterpret_cast<const uint4*>(s_mt + j * mt_pitch + kb) : zero;
-          else
-            bv[u][t] = (kin && j < r) ? load_mt_frag<NT, MT_KMAJOR>(mt, j, kb, K, r) : zero;
+          for (int t = 0; t < NT; ++t) {
+            const int j = t * 8 + g;
+            bv[u % BV][t] = (kin && j < r) ? load_mt_frag<NT, MT_KMAJOR>(mt, j, kb, K, r) : zero;
+          }
         }
       }
 #pragma unroll
       for (int u = 0; u < UNROLL; ++u) {
+        if (STAGED) {
+          const int kb = (c + u * W) * 32 + q * 8;
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            bv[0][t] = kb < K ? *reinterpret_cast<const uint4*>(s_mt + (t * 8 + g) * mt_pitch + kb) : zero;
+        }
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          mma_m16n8k16_bf16(acc[t], xa[u].x, xb[u].x, xa[u].y, xb[u].y, bv[u][t].x, bv[u][t].y);
-          mma_m16n8k16_bf16(acc[t], xa[u].z, xb[u].z, xa[u].w, xb[u].w, bv[u][t].z, bv[u][t].w);
+          const uint4 bw = bv[u % BV][t];
+          mma_m16n8k16_bf16(acc[t], xa[u].x, xb[u].x, xa[u].y, xb[u].y, bw.x, bw.y);
+          mma_m16n8k16_bf16(acc[t], xa[u].z, xb[u].z, xa[u].w, xb[u].w, bw.z, bw.w);
         }
       }
     }

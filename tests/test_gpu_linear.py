@@ -218,8 +218,10 @@ def test_pair_tiles_ragged(lib, m, n, k, r):
 # shares with a ragged k (n = 1000 ends inside a 32-wide chunk), two shares (65 row blocks), one
 # share (141 row blocks, the whole of B staged per CTA) and, past a wave of row blocks, the
 # persistent kernel over 16-row tiles.
+# The CTA-pair dX GEMM shapes around it: a ragged n = 1000 with r = 12 (scalar staging of B) and
+# 15 column tiles of dX at 1900 tokens.
 @pytest.mark.parametrize("m,n,k,r", [(700, 1000, 256, 16), (4100, 512, 256, 8), (9000, 264, 128, 16),
-                                     (9500, 256, 128, 12)])
+                                     (9500, 256, 128, 12), (2000, 1000, 4096, 12), (1900, 4096, 3840, 16)])
 def test_u_split_over_cluster(lib, m, n, k, r):
     _check_all(lib, synthetic.linear_case(n, k, m, r, 2.0 * r, base_seed=m + n + k + r))
 
