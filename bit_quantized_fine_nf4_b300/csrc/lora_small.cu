@@ -220,7 +220,8 @@ __global__ void __launch_bounds__(W * 32) k_lora_down(const __nv_bfloat16* __res
 // a multiple of 128, so the 16-byte fragment loads of a quarter warp hit distinct bank groups),
 // and its 16 warps (row group = warp % 4, k part = warp / 4, 32-wide chunks taken in turn) issue
 // all 16-byte loads of up to 8 chunks before the first MMA: 8 KB per warp, 128 KB per CTA in
-// flight.  Sums, all in a fixed order: the four k parts of a row group in shared memory, then the
+// flight (the first such trip before the slice of mt is staged, so the two overlap).  Sums, all in
+// a fixed order: the four k parts of a row group in shared memory, then the
 // S ranks' partials sent with st.shared::cluster to the rank owning the row group (group % S) and
 // added there in rank order.  Outputs and the side job as in k_lora_down.
 constexpr int kLdkThreads = 512;
