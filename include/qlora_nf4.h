@@ -29,6 +29,14 @@
  *     forwards of an MLP block); the backward calls of a device share one
  *     internal stream for their dA / dB kernel, so those kernels of concurrent
  *     backward calls run one after the other.
+ *   - The kernels are launched with programmatic dependent launch: a kernel may
+ *     start before the one ahead of it on the stream has finished, and waits for
+ *     it (griddepcontrol.wait) before touching its outputs.  Every kernel of the
+ *     library lets the next one start only after that wait, and the first kernel
+ *     of a forward call reads only the NF4 record before it.  So a caller's own
+ *     kernel that writes the record (or anything a call reads) must not let the
+ *     next kernel of the stream launch early (griddepcontrol.launch_dependents)
+ *     before those writes are done; ordinary launches never do.
  *   - Argument errors are returned synchronously, before anything is launched.
  *     Errors found on the device (a bounded wait that expired, a non-finite
  *     weight) are latched in a per-device status word and returned by
